@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) implementation of the Mamba-2 SSD selective scan, its
+decode step and the Mamba-1 diagonal scan.
+
+The compute path is the C-ABI library ``libssdscan.so`` (hand-written CUDA,
+declared in ``include/ssd_scan.h``); :mod:`.binding` is the thin Python layer
+over it (argument marshalling only). :mod:`.inputs` draws seeded synthetic
+workloads. Importing the package does not load the CUDA library; the first
+call into :mod:`.binding` does, and fails loudly if it has not been built.
+"""
+__all__ = ["inputs", "binding"]
+
+
+def __getattr__(name):
+    if name == "binding":
+        from . import binding
+        return binding
+    if name == "inputs":
+        from . import inputs
+        return inputs
+    raise AttributeError(name)

@@ -1,0 +1,191 @@
+/*
+ * Float64 CPU oracle for the selective state-space scans.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or
+ * include this file: only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark run it. It shares no code with the CUDA
+ * library.
+ *
+ * What it computes is the plain token-by-token definition of each scan, in
+ * float64, with no chunking, blocking or reordering:
+ *
+ *   Mamba-2 SSD, per batch b and head h (group g = h / (H/G)):
+ *     alpha_t   = exp(dt_t * A_h)
+ *     h_t[p,n]  = alpha_t * h_{t-1}[p,n] + dt_t * x_t[p] * B_t[n]
+ *     y_t[p]    = sum_n C_t[n] * h_t[p,n] + D_h * x_t[p]
+ *   This is the generic selective update h_t = A_t h_{t-1} + B_t x_t,
+ *   y_t = C_t h_t + D_t x_t of "COREY: Entropy-Guided Runtime Chunk Scheduling
+ *   for Selective Scan Kernels" (section 3.1, Preliminaries), with the scalar
+ *   per-head decay exp(dt*A) and the Euler input term dt*B of the Mamba-2 SSD
+ *   layer ("Compiler-First State Space Duality ...", abstract: diagonal
+ *   per-head dynamics). y uses the updated state h_t.
+ *
+ *   Decode step: the same update for one token, applied in place to a carried
+ *   state (the O(1) cached decode of the same page, Figure 1).
+ *
+ *   Mamba-1 diagonal scan, per batch b and channel d:
+ *     h_t[n] = exp(dt_t * A[d,n]) * h_{t-1}[n] + dt_t * x_t * B_t[n]
+ *     y_t    = sum_n C_t[n] * h_t[n] + D_d * x_t
+ *   (the selective_scan_fn workload of the COREY page, section 5.1).
+ *
+ * Layouts (row-major, innermost last):
+ *   SSD:    x[B,L,H,P]  dt[B,L,H]  A[H]  Bm,Cm[B,L,G,N]  D[H]  state[B,H,P,N]
+ *           y[B,L,H,P]
+ *   decode: x[B,H,P]    dt[B,H]    A[H]  Bm,Cm[B,G,N]    D[H]  state[B,H,P,N]
+ *           y[B,H,P]
+ *   diag:   x,dt[B,L,Dm]  A[Dm,N]  Bm,Cm[B,L,N]  D[Dm]  state[B,Dm,N]  y[B,L,Dm]
+ * D and the initial state may be NULL (read as zero); a NULL final state is
+ * not written. Independent (b,h) or (b,d) units run on nthreads POSIX threads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int64_t B, L, H, P, N, G;
+    const double *x, *dt, *A, *Bm, *Cm, *D, *init;
+    double *y, *final_state;
+    int64_t next_unit, n_units;
+    pthread_mutex_t lock;
+} ssd_job;
+
+static int64_t take_unit(int64_t *next, int64_t n, pthread_mutex_t *lock) {
+    pthread_mutex_lock(lock);
+    int64_t u = *next < n ? (*next)++ : -1;
+    pthread_mutex_unlock(lock);
+    return u;
+}
+
+/* One (b,h) unit of the SSD recurrence, token by token. */
+static void ssd_unit(const ssd_job *j, int64_t b, int64_t h, double *st) {
+    const int64_t L = j->L, H = j->H, P = j->P, N = j->N, G = j->G;
+    const int64_t g = h / (H / G);
+    const double Ah = j->A[h];
+    const double Dh = j->D ? j->D[h] : 0.0;
+    if (j->init)
+        memcpy(st, j->init + (b * H + h) * P * N, sizeof(double) * P * N);
+    else
+        memset(st, 0, sizeof(double) * P * N);
+    for (int64_t t = 0; t < L; ++t) {
+        const double dt = j->dt[(b * L + t) * H + h];
+        const double alpha = exp(dt * Ah);
+        const double *xt = j->x + ((b * L + t) * H + h) * P;
+        const double *Bt = j->Bm + ((b * L + t) * G + g) * N;
+        const double *Ct = j->Cm + ((b * L + t) * G + g) * N;
+        double *yt = j->y + ((b * L + t) * H + h) * P;
+        for (int64_t p = 0; p < P; ++p) {
+            double *row = st + p * N;
+            const double u = dt * xt[p];
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                row[n] = alpha * row[n] + u * Bt[n];
+                acc += Ct[n] * row[n];
+            }
+            yt[p] = acc + Dh * xt[p];
+        }
+    }
+    if (j->final_state)
+        memcpy(j->final_state + (b * H + h) * P * N, st, sizeof(double) * P * N);
+}
+
+static void *ssd_worker(void *arg) {
+    ssd_job *j = (ssd_job *)arg;
+    double *st = (double *)malloc(sizeof(double) * (size_t)(j->P * j->N > 0 ? j->P * j->N : 1));
+    for (;;) {
+        int64_t u = take_unit(&j->next_unit, j->n_units, &j->lock);
+        if (u < 0) break;
+        ssd_unit(j, u / j->H, u % j->H, st);
+    }
+    free(st);
+    return NULL;
+}
+
+static void run_threads(void *(*fn)(void *), void *job, int nthreads, int64_t n_units) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n_units) nthreads = (int)(n_units > 0 ? n_units : 1);
+    if (nthreads > 256) nthreads = 256;
+    pthread_t tid[256];
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i)
+        if (pthread_create(&tid[started], NULL, fn, job) == 0) ++started;
+    fn(job);
+    for (int i = 0; i < started; ++i) pthread_join(tid[i], NULL);
+}
+
+/* Returns 0 on success, -1 on invalid sizes. */
+int oracle_ssd_seq(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
+                   const double *x, const double *dt, const double *A, const double *Bm,
+                   const double *Cm, const double *D, const double *init_state, double *y,
+                   double *final_state, int nthreads) {
+    if (B < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G != 0) return -1;
+    ssd_job j = {B, L, H, P, N, G, x, dt, A, Bm, Cm, D, init_state, y, final_state, 0, B * H};
+    pthread_mutex_init(&j.lock, NULL);
+    run_threads(ssd_worker, &j, nthreads, B * H);
+    pthread_mutex_destroy(&j.lock);
+    return 0;
+}
+
+/* One decode token, state updated in place: the L=1 case of the same unit. */
+int oracle_ssd_decode(int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, double *state,
+                      const double *x, const double *dt, const double *A, const double *Bm,
+                      const double *Cm, const double *D, double *y, int nthreads) {
+    return oracle_ssd_seq(B, 1, H, P, N, G, x, dt, A, Bm, Cm, D, state, y, state, nthreads);
+}
+
+typedef struct {
+    int64_t B, L, Dm, N;
+    const double *x, *dt, *A, *Bm, *Cm, *D, *init;
+    double *y, *final_state;
+    int64_t next_unit, n_units;
+    pthread_mutex_t lock;
+} diag_job;
+
+/* One (b,d) unit of the Mamba-1 diagonal recurrence. */
+static void diag_unit(const diag_job *j, int64_t b, int64_t d, double *st) {
+    const int64_t L = j->L, Dm = j->Dm, N = j->N;
+    const double *Ad = j->A + d * N;
+    const double Dd = j->D ? j->D[d] : 0.0;
+    if (j->init)
+        memcpy(st, j->init + (b * Dm + d) * N, sizeof(double) * N);
+    else
+        memset(st, 0, sizeof(double) * N);
+    for (int64_t t = 0; t < L; ++t) {
+        const double dt = j->dt[(b * L + t) * Dm + d];
+        const double xt = j->x[(b * L + t) * Dm + d];
+        const double *Bt = j->Bm + (b * L + t) * N;
+        const double *Ct = j->Cm + (b * L + t) * N;
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            st[n] = exp(dt * Ad[n]) * st[n] + dt * xt * Bt[n];
+            acc += Ct[n] * st[n];
+        }
+        j->y[(b * L + t) * Dm + d] = acc + Dd * xt;
+    }
+    if (j->final_state) memcpy(j->final_state + (b * Dm + d) * N, st, sizeof(double) * N);
+}
+
+static void *diag_worker(void *arg) {
+    diag_job *j = (diag_job *)arg;
+    double *st = (double *)malloc(sizeof(double) * (size_t)(j->N > 0 ? j->N : 1));
+    for (;;) {
+        int64_t u = take_unit(&j->next_unit, j->n_units, &j->lock);
+        if (u < 0) break;
+        diag_unit(j, u / j->Dm, u % j->Dm, st);
+    }
+    free(st);
+    return NULL;
+}
+
+int oracle_diag_seq(int64_t B, int64_t L, int64_t Dm, int64_t N, const double *x,
+                    const double *dt, const double *A, const double *Bm, const double *Cm,
+                    const double *D, const double *init_state, double *y, double *final_state,
+                    int nthreads) {
+    if (B < 0 || L < 0 || Dm < 1 || N < 1) return -1;
+    diag_job j = {B, L, Dm, N, x, dt, A, Bm, Cm, D, init_state, y, final_state, 0, B * Dm};
+    pthread_mutex_init(&j.lock, NULL);
+    run_threads(diag_worker, &j, nthreads, B * Dm);
+    pthread_mutex_destroy(&j.lock);
+    return 0;
+}

@@ -1,0 +1,59 @@
+"""The oracle's pins must be able to fail.
+
+Each case plants one plausible mistake in a temporary copy of the C oracle
+source (on the CPU, never in the product), loads the mutant in place of the
+real oracle, and checks that at least one pin of tests/test_oracle_pins.py
+rejects it.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ssd_oracle.c")
+
+MUTANTS = {
+    "y_from_previous_state": ("row[n] = alpha * row[n] + u * Bt[n];\n                acc += Ct[n] * row[n];",
+                              "acc += Ct[n] * row[n];\n                row[n] = alpha * row[n] + u * Bt[n];"),
+    "dropped_D": ("yt[p] = acc + Dh * xt[p];", "yt[p] = acc;"),
+    "wrong_sign_of_A": ("const double alpha = exp(dt * Ah);", "const double alpha = exp(-dt * Ah);"),
+    "dt_missing_on_input": ("const double u = dt * xt[p];", "const double u = xt[p];"),
+    "wrong_group_index": ("const int64_t g = h / (H / G);", "const int64_t g = h % G;"),
+    "diag_decay_index": ("st[n] = exp(dt * Ad[n]) * st[n]", "st[n] = exp(dt * Ad[0]) * st[n]"),
+}
+
+PINS = [
+    pins.test_A_zero_closed_form, pins.test_single_token_closed_form, pins.test_memoryless_under_strong_decay,
+    pins.test_dt_zero_keeps_state, pins.test_lfilter_constant_dt, pins.test_brute_force_tiny,
+    pins.test_hand_worked_example, pins.test_quadratic_form_matches_recurrence,
+    pins.test_mamba2_equals_mamba1_with_tied_decay, pins.test_diag_lfilter_constant_dt,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, f"mutation anchor for {name} not found in the oracle source"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new, 1))
+    so = tmp_path / "mutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", str(mut), "-o", str(so), "-lm"],
+                   check=True)
+    oracle._load()  # make sure the real library's argtypes are set up first
+    lib = ctypes.CDLL(str(so))
+    for fname in ("oracle_ssd_seq", "oracle_ssd_decode", "oracle_diag_seq"):
+        getattr(lib, fname).argtypes = getattr(oracle._lib, fname).argtypes
+        getattr(lib, fname).restype = ctypes.c_int
+    monkeypatch.setattr(oracle, "_lib", lib)
+    failed = []
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin rejects the mutant {name}"
