@@ -1,0 +1,599 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the SSD selective scan on one GB300 (or N replicas).
+
+One step = one chunked SSD prefill (chunk state -> state passing -> chunk scan,
+with the in-chunk cumulative sums fused into both chunk kernels) of the
+Mamba-2-130M-shaped layer workload: batch 1, L 4096, 24 heads, headdim 64,
+d_state 128, 1 group, bf16 x/dt/B/C/y with float32 state and accumulation,
+seeded synthetic inputs. The timed region replays a CUDA graph of exactly K
+steps; the steps rotate over copies of the inputs whose total size exceeds
+the L2 cache, so every step reads its inputs from HBM.
+
+The same JSON line also carries, each in its own timed region: the decode
+workload (batch 64, 80 heads, 64 x 128 fp32 state, 1000 in-place steps, one
+CUDA graph), the Mamba-1 diagonal scan (batch 8, L 2048, 5120 channels,
+d_state 16, chunk sweep), the per-stage kernel times, the end-to-end number
+through the C ABI with host buffers, and the float64 CPU oracle timed on the
+host cores.
+
+`--impl reference` times the float64 CPU oracle on the same workload (a
+bounded sample of tokens per step) and prints the same kind of line.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU (weak
+scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "ssd_m2_130m_L4096"
+DECODE = "decode_B64_H80"
+MAMBA1 = "mamba1_B8_L2048_D5120"
+METRIC = "SSD prefill tokens/s + % roofline; decode steps/s + state HBM GB/s"
+STAGES = ("chunk_state", "state_pass", "chunk_scan")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- helpers
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device="cpu") -> float:
+    """Max of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def file_hash(*paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ssd_compulsory_bytes(w: dict, io_bytes: int = 2) -> dict:
+    """Algorithmic bytes of one prefill: every input read once, y and the final
+    state written once (no initial state in these workloads)."""
+    Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    tok = Bz * L
+    x = tok * H * P * io_bytes
+    dt = tok * H * io_bytes
+    bc = tok * G * N * io_bytes
+    return {"x": x, "dt": dt, "B": bc, "C": bc, "y": x, "final_state": Bz * H * P * N * 4,
+            "total": 2 * x + dt + 2 * bc + Bz * H * P * N * 4}
+
+
+def stage_algorithmic_bytes(w: dict, stage: str) -> int:
+    """Compulsory bytes each stage kernel must move (intermediate workspace
+    traffic is overhead, not credited)."""
+    b = ssd_compulsory_bytes(w)
+    if stage == "chunk_state":
+        return b["x"] + b["dt"] + b["B"]
+    if stage == "state_pass":
+        return b["final_state"]
+    return b["x"] + b["dt"] + b["B"] + b["C"] + b["y"]
+
+
+def ssd_flops(w: dict, Q: int) -> float:
+    """Useful flops (causal MACs x2 of intra-chunk, chunk-state and output
+    contractions, C.B^T once per group)."""
+    Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    return float(Bz * L * (H * (Q * P + 4 * N * P) + G * Q * N))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our arm
+
+def _traffic_for(kernel: str):
+    """ncu DRAM bytes per launch recorded in profiles/traffic.json, only if the
+    kernel's source is unchanged since the capture; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "mamba_ssd_selective_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or file_hash(src) != rec.get("source_hash"):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    from mamba_ssd_selective_gb300 import binding, inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    binding.load()
+    peaks = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0)) or 129 * 2 ** 20
+    bf = torch.bfloat16
+    K, W = args.steps, args.warmup
+    out = {}
+
+    sampler = ClockSampler(local).start() if rank == 0 else None
+
+    # ---------------- prefill (headline)
+    w = dict(inputs.WORKLOADS[HEADLINE])
+    d = inputs.ssd_inputs(w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                          io_dtype="bf16", seed=0)
+
+    def t_(a, dtype=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+    base = {"x": t_(d["x"], bf), "dt": t_(d["dt"], bf), "B": t_(d["B"], bf), "C": t_(d["C"], bf)}
+    A, Dv = t_(d["A"]), t_(d["D"])
+    Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    ws_max = max(binding.ssd_workspace_size(Bz, L, H, P, N, G, bf, q) for q in (64, 128, 256))
+    per_set = sum(v.numel() * v.element_size() for v in base.values()) * 2 + ws_max + Bz * H * P * N * 4
+    n_sets = max(2, math.ceil(3 * l2 / per_set))
+    sets = []
+    for _ in range(n_sets):
+        s = {k: v.clone() for k, v in base.items()}
+        s["y"] = torch.empty_like(base["x"])
+        s["final"] = torch.empty((Bz, H, P, N), dtype=torch.float32, device=dev)
+        s["ws"] = torch.empty(ws_max, dtype=torch.uint8, device=dev)
+        sets.append(s)
+
+    def step(s, q):
+        binding.ssd_scan_chunked(s["x"], s["dt"], A, s["B"], s["C"], Dv, None, chunk_size=q, y=s["y"],
+                                 final_state=s["final"], workspace=s["ws"])
+
+    def capture(nsteps, q, stage_events=None):
+        g = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream(device=dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(stream):
+            for i in range(min(nsteps, n_sets)):  # eager warm-up on the capture stream
+                step(sets[i % n_sets], q)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for i in range(nsteps):
+                if stage_events is not None:
+                    binding.ssd_record_stage_events(stage_events[i])
+                step(sets[i % n_sets], q)
+        return g
+
+    def time_graph(g, reps=1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    # chunk sweep: the best static chunk per workload is the one reported
+    sweep = {}
+    S = 8 * n_sets
+    for q in (64, 128, 256):
+        g = capture(S, q)
+        for _ in range(max(W, 3)):
+            g.replay()
+        ms = time_graph(g, reps=5) / (5 * S)
+        sweep[q] = ms
+        del g
+    best_q = args.chunk or min(sweep, key=sweep.get)
+
+    # the timed region: exactly K steps in one graph
+    g = capture(K, best_q)
+    gw = capture(max(W, 3), best_q)
+    for _ in range(2):
+        gw.replay()
+    # keep the GPU busy ~1 s before the timed region so that the clock samples
+    # describe the clocks under this load
+    if rank == 0:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            gw.replay()
+            torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed_region")
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_total = reduce_max(e0.elapsed_time(e1), world, device=dev)
+    ms_step = ms_total / K
+    tokens = Bz * L
+    value = world * tokens * K / (ms_total / 1e3)
+    del g, gw
+
+    # per-stage kernel times, CUDA events between the stages of every step of a
+    # second K'-step graph of the same workload
+    Ks = min(K, 256)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Ks)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize(dev)
+    gs = capture(Ks, best_q, stage_events=evs)
+    gs.replay()
+    torch.cuda.synchronize(dev)
+    stage_ms = {nm: statistics.mean(r[i].elapsed_time(r[i + 1]) for r in evs) for i, nm in enumerate(STAGES)}
+    del gs
+    dom = max(stage_ms, key=stage_ms.get)
+    dom_bytes = stage_algorithmic_bytes(w, dom)
+    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+    comp = ssd_compulsory_bytes(w)
+    src_of = {"chunk_state": "chunked_tc.cu", "state_pass": "chunked_simt.cu", "chunk_scan": "chunked_tc.cu"}
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "traffic": _traffic_for(dom), "algorithmic_bytes": dom_bytes,
+                "launch_ms": round(stage_ms[dom], 5), "peak_source": peaks["source"]}
+    step_gbs = comp["total"] / (ms_step / 1e3) / 1e9
+    out["prefill"] = {
+        "step_roofline": {"bound": "hbm", "compulsory_bytes": comp["total"], "achieved": round(step_gbs, 1),
+                          "peak": hbm_peak, "unit": "GB/s", "frac": round(step_gbs / hbm_peak, 4)},
+        "tflops": round(ssd_flops(w, best_q) / (ms_step / 1e3) / 1e12, 2),
+        "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+        "chunk_sweep_ms_per_step": {str(k): round(v, 5) for k, v in sweep.items()},
+    }
+
+    # ---------------- end to end through the C ABI with host buffers
+    hx = {k: v.cpu().pin_memory() for k, v in base.items()}
+    hA, hD = A.cpu().pin_memory(), Dv.cpu().pin_memory()
+    hy = torch.empty(base["x"].shape, dtype=bf).pin_memory()
+    hf = torch.empty((Bz, H, P, N), dtype=torch.float32).pin_memory()
+    s0 = sets[0]
+    dA, dD = torch.empty_like(A), torch.empty_like(Dv)
+
+    def e2e_step():
+        for k in hx:
+            s0[k].copy_(hx[k], non_blocking=True)
+        dA.copy_(hA, non_blocking=True)
+        dD.copy_(hD, non_blocking=True)
+        binding.ssd_scan_chunked(s0["x"], s0["dt"], dA, s0["B"], s0["C"], dD, None, chunk_size=best_q, y=s0["y"],
+                                 final_state=s0["final"], workspace=s0["ws"])
+        hy.copy_(s0["y"], non_blocking=True)
+        hf.copy_(s0["final"], non_blocking=True)
+
+    Ke = max(1, min(K, 50))
+    for _ in range(max(W, 3)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms_e2e = reduce_max(e0.elapsed_time(e1), world, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in hx.values()) + hA.numel() * 4 + hD.numel() * 4
+    d2h = hy.numel() * hy.element_size() + hf.numel() * 4
+    e2e = {"value": world * tokens * Ke / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": Ke}
+    del sets, hx
+
+    # ---------------- decode workload
+    if not args.skip_extra:
+        out["decode"] = bench_decode(torch, binding, inputs, dev, hbm_peak, peaks["source"], W)
+        out["mamba1"] = bench_mamba1(torch, binding, inputs, dev, hbm_peak, peaks["source"], K, W)
+
+    clocks = sampler.stop() if sampler else None
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded: x,B,C~N(0,1); dt=softplus(N(0,.5)+b), A=-exp(U(0,ln16)))",
+        "config": {"workload": HEADLINE, "batch": Bz, "seqlen": L, "nheads": H, "headdim": P, "dstate": N,
+                   "ngroups": G, "chunk": best_q, "io": "bf16 x/dt/B/C/y, fp32 state and accumulation",
+                   "l2": f"inputs rotate over {n_sets} copies ({n_sets * per_set / 2**20:.0f} MiB > L2 "
+                         f"{l2 / 2**20:.0f} MiB)", "graph": "K steps in one CUDA graph",
+                   "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
+        "roofline": roofline,
+        "gpu_launches": 3 * K,
+        "e2e": e2e,
+    }
+    line.update(out)
+    if not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if clocks is not None:
+        line["clocks"] = clocks
+    print(json.dumps(line), flush=True)
+
+
+def bench_decode(torch, binding, inputs, dev, hbm_peak, peak_src, W):
+    w = inputs.WORKLOADS[DECODE]
+    Bz, H, P, N, G, steps = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["steps"]
+    bf = torch.bfloat16
+
+    def t_(a, dtype=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+    state = t_(inputs.decode_state(Bz, H, P, N, seed=0))
+    prm = inputs.decode_params(H, seed=0)
+    A, Dv = t_(prm["A"]), t_(prm["D"])
+    xs = torch.empty((steps, Bz, H, P), dtype=bf, device=dev)
+    dts = torch.empty((steps, Bz, H), dtype=bf, device=dev)
+    Bs = torch.empty((steps, Bz, G, N), dtype=bf, device=dev)
+    Cs = torch.empty((steps, Bz, G, N), dtype=bf, device=dev)
+    for s in range(steps):
+        di = inputs.decode_step_inputs(s, Bz, H, P, N, G, io_dtype="bf16", seed=0)
+        xs[s], dts[s], Bs[s], Cs[s] = t_(di["x"], bf), t_(di["dt"], bf), t_(di["B"], bf), t_(di["C"], bf)
+    ys = torch.empty_like(xs)
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        binding.ssd_decode_step(state, xs[0], dts[0], A, Bs[0], Cs[0], Dv, y=ys[0])
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        for s in range(steps):
+            binding.ssd_decode_step(state, xs[s], dts[s], A, Bs[s], Cs[s], Dv, y=ys[s])
+    for _ in range(max(W, 3) // 3 + 1):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    state_bytes = 2 * Bz * H * P * N * 4
+    step_bytes = state_bytes + Bz * H * P * 2 * 2 + Bz * H * 2 + 2 * Bz * G * N * 2
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    return {"workload": DECODE, "steps": steps, "ms_per_step": round(ms, 6), "steps_per_s": round(1e3 / ms, 1),
+            "state_gbs": round(state_bytes / (ms / 1e3) / 1e9, 1), "gpu_launches": steps,
+            "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes": step_bytes,
+                         "traffic": _traffic_for("decode_step"), "frac_of_8tbs": round(gbs / 8000.0, 4),
+                         "peak_source": peak_src}}
+
+
+def bench_mamba1(torch, binding, inputs, dev, hbm_peak, peak_src, K, W):
+    w = inputs.WORKLOADS[MAMBA1]
+    Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
+    bf = torch.bfloat16
+    d = inputs.diag_inputs(Bz, L, Dm, N, io_dtype="bf16", seed=0)
+
+    def t_(a, dtype=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+    x, dt, Bm, Cm = t_(d["x"], bf), t_(d["dt"], bf), t_(d["B"], bf), t_(d["C"], bf)
+    A, Dv = t_(d["A"]), t_(d["D"])
+    y = torch.empty_like(x)
+    hT = torch.empty((Bz, Dm, N), dtype=torch.float32, device=dev)
+    reps = max(5, min(K, 50))
+    sweep = {}
+    for chunk in (256, 512, 1024, 2048):
+        for _ in range(max(W, 3)):
+            binding.selective_scan_diag(x, dt, A, Bm, Cm, Dv, None, chunk_size=chunk, y=y, final_state=hT)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            binding.selective_scan_diag(x, dt, A, Bm, Cm, Dv, None, chunk_size=chunk, y=y, final_state=hT)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        sweep[chunk] = e0.elapsed_time(e1) / reps
+    best = min(sweep, key=sweep.get)
+    ms = sweep[best]
+    nbytes = 3 * Bz * L * Dm * 2 + 2 * Bz * L * N * 2 + Dm * N * 4 + Dm * 4 + Bz * Dm * N * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    n_exp = Bz * L * Dm * N
+    return {"workload": MAMBA1, "chunk": best, "ms": round(ms, 5), "tokens_per_s": round(Bz * L / (ms / 1e3), 1),
+            "chunk_sweep_ms": {str(k): round(v, 5) for k, v in sweep.items()},
+            "exp_per_s": round(n_exp / (ms / 1e3), 1), "gpu_launches": reps,
+            "roofline": {"bound": "hbm", "kernel": "diag_scan", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes": nbytes,
+                         "traffic": _traffic_for("diag_scan"), "peak_source": peak_src}}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample_tokens(w: dict, seconds: float, threads: int) -> int:
+    """Tokens of the workload (from the start of the sequence, all heads) the
+    oracle processes in about `seconds`, measured on a short probe run."""
+    import oracle
+    from mamba_ssd_selective_gb300 import inputs
+    probe = min(256, w["seqlen"])
+    d = inputs.ssd_inputs(w["batch"], probe, w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                          io_dtype="bf16", seed=0)
+    t0 = time.perf_counter()
+    oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=threads)
+    dt_probe = max(time.perf_counter() - t0, 1e-4)
+    return int(max(16, min(w["seqlen"], probe * seconds / dt_probe)))
+
+
+def cpu_baseline(w: dict, seconds: float = 10.0) -> dict:
+    """The float64 oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    from mamba_ssd_selective_gb300 import inputs
+    threads = oracle.default_threads()
+    Ls = oracle_sample_tokens(w, seconds, threads)
+    d = inputs.ssd_inputs(w["batch"], Ls, w["nheads"], w["headdim"], w["dstate"], w["ngroups"], io_dtype="bf16",
+                          seed=0)
+    t0 = time.perf_counter()
+    oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=threads)
+    el = time.perf_counter() - t0
+    return {"value": round(w["batch"] * Ls / el, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {Ls} of {w['seqlen']} tokens, all {w['nheads']} heads, float64 token-by-token "
+                      f"recurrence, {el:.2f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: same workload, metric and unit."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return  # rank 0 alone runs and prints
+    import oracle
+    from mamba_ssd_selective_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload or HEADLINE]
+    K, W = args.steps, args.warmup
+    threads = oracle.default_threads()
+    budget = float(args.ref_budget_s)
+    Ls = oracle_sample_tokens(w, budget / max(1, K + W), threads)
+    d = inputs.ssd_inputs(w["batch"], Ls, w["nheads"], w["headdim"], w["dstate"], w["ngroups"], io_dtype="bf16",
+                          seed=0)
+    for _ in range(W):
+        oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=threads)
+    el = time.perf_counter() - t0
+    tokens = w["batch"] * Ls
+    value = tokens * K / el
+    sample = f"first {Ls} of {w['seqlen']} tokens per step, all {w['nheads']} heads, float64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload or HEADLINE, "batch": w["batch"], "seqlen": w["seqlen"],
+                   "nheads": w["nheads"], "headdim": w["headdim"], "dstate": w["dstate"], "ngroups": w["ngroups"],
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--chunk", type=int, default=0, help="force a chunk size (default: best of 64/128/256)")
+    ap.add_argument("--workload", default=None, help="reference arm: workload name (default: the headline)")
+    ap.add_argument("--ref-budget-s", type=float, default=60.0, help="reference arm: total oracle seconds")
+    ap.add_argument("--skip-extra", action="store_true", help="skip the decode and Mamba-1 lines")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # at least three warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    world, _, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * ssd_scan.h -- C ABI of libssdscan.so: the Mamba-2 state-space-duality (SSD)
+ * selective scan, its one-token decode step, and the Mamba-1 diagonal
+ * selective scan, as hand-written CUDA kernels for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (per batch b and head h, group g = h / (nheads/ngroups)):
+ *
+ *     h_t[p,n] = exp(dt_t * A_h) * h_{t-1}[p,n] + dt_t * x_t[p] * B_t[n]
+ *     y_t[p]   = sum_n C_t[n] * h_t[p,n] + D_h * x_t[p]
+ *
+ * the generic selective update h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t +
+ * D_t x_t of "COREY: Entropy-Guided Runtime Chunk Scheduling for Selective
+ * Scan Kernels" (section 3.1) with the scalar per-head decay of the SSD layer
+ * ("Compiler-First State Space Duality and Portable O(1) Autoregressive
+ * Caching for Inference", abstract: diagonal per-head dynamics, fixed-size
+ * chunking). y uses the updated state h_t. dt is used as given: no softplus
+ * and no bias are applied inside.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *    dense, row-major with the innermost dimension last, and 16-byte aligned.
+ *    The caller owns every buffer (inputs, outputs, workspace); the library
+ *    allocates nothing and never frees.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream): they
+ *    validate their arguments on the host, enqueue kernels and return. There
+ *    is no host synchronisation and no exception crosses the ABI.
+ *  - Validation happens before any CUDA call: an invalid argument returns
+ *    SSD_ERR_INVALID_ARG (or SSD_ERR_UNSUPPORTED for a valid but unbuilt
+ *    shape) and enqueues nothing. SSD_ERR_CUDA reports a failed launch.
+ *    ssd_last_error() then describes the failure (thread-local text).
+ *  - Results are deterministic: no atomics in any reduction, so runs are
+ *    bitwise reproducible and a batch of sequences gives bitwise the same
+ *    rows as each sequence alone.
+ *  - io_dtype selects the element type of x, dt, B, C and y (float32 or
+ *    bfloat16). A, D and every state are float32 in all cases; decays,
+ *    cumulative sums and exponentials are always evaluated in float32
+ *    ("Compiler-First State Space Duality ...", Table 8: decay kept in
+ *    float32).
+ */
+#ifndef SSD_SCAN_H
+#define SSD_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment, short workspace */
+    SSD_ERR_UNSUPPORTED = 2, /* valid arguments, shape outside what the kernels handle */
+    SSD_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+    SSD_ERR_TIMEOUT = 4      /* a bounded in-kernel wait gave up (see ssd_workspace_status) */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Option bits for ssd_dims.flags. */
+#define SSD_FLAG_SIMT 1 /* bf16 prefill: use the CUDA-core kernels instead of the tensor-core ones */
+
+typedef struct {
+    int64_t batch;    /* B >= 0                                   */
+    int64_t seqlen;   /* L >= 0 (prefill); ignored by the decode step */
+    int64_t nheads;   /* H >= 1                                   */
+    int64_t headdim;  /* P >= 1                                   */
+    int64_t dstate;   /* N >= 1                                   */
+    int64_t ngroups;  /* G >= 1, H % G == 0; head h reads B/C group h/(H/G) */
+    int32_t io_dtype; /* ssd_dtype of x, dt, B, C, y              */
+    int32_t flags;    /* SSD_FLAG_* bits, 0 by default            */
+} ssd_dims;
+
+/*
+ * Bytes of device workspace ssd_scan_chunked needs for these sizes and chunk
+ * size; 0 if the arguments are invalid. The workspace holds the per-chunk
+ * states [B, ceil(L/Q), H, P, N] (float32, plus a bfloat16 copy on the
+ * tensor-core path), the per-chunk decay totals and a status word.
+ */
+size_t ssd_workspace_size(const ssd_dims *dims, int chunk_size);
+
+/*
+ * Chunked SSD prefill over a whole sequence (the SSD scan run "chunk by chunk,
+ * each chunk continuing from the previous chunk's state", "Recurrence Scan",
+ * first section; fixed-size chunking, "Compiler-First State Space Duality
+ * ...", abstract).
+ *
+ *   x          [B, L, H, P]  io_dtype
+ *   dt         [B, L, H]     io_dtype, used as given (already positive)
+ *   A          [H]           float32, the per-head decay rate (normally < 0)
+ *   B, C       [B, L, G, N]  io_dtype
+ *   D          [H]           float32, may be NULL (no skip term)
+ *   init_state [B, H, P, N]  float32, may be NULL (zero initial state)
+ *   chunk_size Q in {64, 128, 256}; L need not be a multiple of Q. The result
+ *              does not depend on Q beyond float32 rounding.
+ *   y          [B, L, H, P]  io_dtype, written
+ *   final_state[B, H, P, N]  float32, the state after token L-1 (init_state,
+ *              or zero, when L = 0); may be NULL (not written). It may be the
+ *              same buffer as init_state (the state is then updated in place).
+ *   workspace  device buffer of at least ssd_workspace_size(dims, Q) bytes,
+ *              256-byte aligned; contents on entry are ignored. Two calls in
+ *              flight at once need two workspaces.
+ *
+ * bf16 inputs with P = 64 and N = 128 run on the tensor cores (tcgen05 MMAs
+ * with float32 accumulation in tensor memory, operands staged by TMA) unless
+ * dims->flags has SSD_FLAG_SIMT; every other case, and all float32 inputs,
+ * run on the CUDA cores in float32 (limit: nheads * ceil(P/64) * ceil(N/64)
+ * <= 65535).
+ */
+ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt, const float *A,
+                            const void *B, const void *C, const float *D, const float *init_state,
+                            int chunk_size, void *y, float *final_state, void *workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * One decode token for a batch of sequences, state updated in place (the
+ * O(1) cached decode of "Compiler-First State Space Duality ...", Figure 1;
+ * the state is laid out [B, H, P, N] with N contiguous, so a warp streams one
+ * (b, h, p) row with coalesced 128-bit accesses -- the opposite of the
+ * one-thread-per-channel mapping whose uncoalesced state reads the
+ * "Mamba-2 SSD fused layer via VGpuWarp" log diagnoses).
+ *
+ *   state [B, H, P, N] float32, read and overwritten with the new state
+ *   x     [B, H, P]    io_dtype      dt [B, H] io_dtype
+ *   A     [H]          float32       B, C [B, G, N] io_dtype
+ *   D     [H]          float32, may be NULL
+ *   y     [B, H, P]    io_dtype, written
+ * dims->seqlen is ignored. Equivalent to ssd_scan_chunked with L = 1 and
+ * init_state = final_state = state.
+ */
+ssd_status ssd_decode_step(const ssd_dims *dims, float *state, const void *x, const void *dt,
+                           const float *A, const void *B, const void *C, const float *D, void *y,
+                           cudaStream_t stream);
+
+/*
+ * Mamba-1 selective scan with a per-channel diagonal A (the selective_scan_fn
+ * workload of "COREY ...", section 5.1 and appendix A.9; d_state 16):
+ *
+ *     h_t[n] = exp(dt_t[d] * A[d,n]) * h_{t-1}[n] + dt_t[d] * x_t[d] * B_t[n]
+ *     y_t[d] = sum_n C_t[n] * h_t[n] + D[d] * x_t[d]
+ *
+ *   x, dt      [batch, seqlen, dim]  io_dtype (dt used as given)
+ *   A          [dim, dstate]         float32
+ *   B, C       [batch, seqlen, dstate] io_dtype
+ *   D          [dim]                 float32, may be NULL
+ *   init_state [batch, dim, dstate]  float32, may be NULL
+ *   chunk_size tokens per pass, a multiple of 32, >= 32: the kernel walks the
+ *              sequence chunk by chunk carrying the state exactly in
+ *              registers, so the output is bitwise independent of it
+ *              (runtime chunk routing preserves outputs bitwise, "COREY ...",
+ *              section 5.4).
+ *   y          [batch, seqlen, dim]  io_dtype, written
+ *   final_state[batch, dim, dstate]  float32, may be NULL
+ * Limits: 1 <= dstate <= 64.
+ */
+ssd_status selective_scan_diag(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                               int32_t io_dtype, const void *x, const void *dt, const float *A,
+                               const void *B, const void *C, const float *D,
+                               const float *init_state, int chunk_size, void *y,
+                               float *final_state, cudaStream_t stream);
+
+/*
+ * Status word of a workspace: waits for `stream`, then reports SSD_OK or the
+ * first error a kernel recorded there during the last ssd_scan_chunked call
+ * that used it (SSD_ERR_TIMEOUT when a bounded wait gave up). Every bounded
+ * wait in the kernels records its failure here and returns instead of
+ * spinning forever.
+ */
+ssd_status ssd_workspace_status(const void *workspace, cudaStream_t stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one kernel that waits on a
+ * shared-memory barrier nothing will ever complete, with a budget of
+ * `spin_limit` polls, records SSD_ERR_TIMEOUT in the workspace status word
+ * and exits. The caller then reads ssd_workspace_status(workspace, stream),
+ * which must report SSD_ERR_TIMEOUT while the context stays usable.
+ * workspace: at least 256 bytes. spin_limit: 1 .. 1<<20.
+ */
+ssd_status ssd_selftest_bounded_wait(void *workspace, int spin_limit, cudaStream_t stream);
+
+/*
+ * Per-stage timing of the next ssd_scan_chunked call made on this thread.
+ * `events` points to 4 CUDA events created by the caller (timing enabled, on
+ * the device of the call); that call records them on its stream before its
+ * first kernel and after each stage -- chunk state, state passing, chunk scan
+ * -- so that cudaEventElapsedTime(e[i], e[i+1]) is the device time of stage i.
+ * Inside stream capture they are recorded as external event nodes. The request
+ * is consumed by that one call; the stages are then launched without
+ * programmatic overlap. count must be 4; events = NULL cancels a request.
+ */
+ssd_status ssd_record_stage_events(cudaEvent_t *events, int count);
+
+/* Thread-local description of the last error returned on this thread. */
+const char *ssd_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_SCAN_H */

@@ -7,14 +7,12 @@ over it (argument marshalling only). :mod:`.inputs` draws seeded synthetic
 workloads. Importing the package does not load the CUDA library; the first
 call into :mod:`.binding` does, and fails loudly if it has not been built.
 """
-__all__ = ["inputs", "binding"]
+import importlib
+
+__all__ = ["inputs", "binding", "build"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    if name == "inputs":
-        from . import inputs
-        return inputs
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

@@ -1,0 +1,226 @@
+"""Thin Python binding of libssdscan.so (C ABI in include/ssd_scan.h).
+
+Argument marshalling only: checks that torch tensors have the documented
+shapes, dtypes, device and layout (the C ABI receives raw pointers and cannot),
+allocates outputs and the workspace with torch when the caller passes none,
+and forwards pointers plus the current CUDA stream. Every step of the scan
+runs in the library's CUDA kernels; there is no fallback. If the library has
+not been built, or does not load, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = 0, 1, 2, 3, 4
+SSD_F32, SSD_BF16 = 0, 1
+SSD_FLAG_SIMT = 1
+
+_STATUS_NAMES = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
+                 4: "SSD_ERR_TIMEOUT"}
+
+
+class SsdError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class ssd_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("io_dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Loads libssdscan.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m mamba_ssd_selective_gb300.build` (or __graft_entry__.build())")
+            lib = ctypes.CDLL(path)
+            vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+            dp = ctypes.POINTER(ssd_dims)
+            lib.ssd_workspace_size.argtypes = [dp, ctypes.c_int]
+            lib.ssd_workspace_size.restype = sz
+            lib.ssd_scan_chunked.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp, sz, vp]
+            lib.ssd_decode_step.argtypes = [dp] + [vp] * 9
+            lib.selective_scan_diag.argtypes = [i64, i64, i64, i64, i32] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
+            lib.ssd_workspace_status.argtypes = [vp, vp]
+            lib.ssd_selftest_bounded_wait.argtypes = [vp, ctypes.c_int, vp]
+            lib.ssd_record_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+            lib.ssd_record_stage_events.restype = ctypes.c_int
+            lib.ssd_last_error.argtypes = []
+            lib.ssd_last_error.restype = ctypes.c_char_p
+            for f in (lib.ssd_scan_chunked, lib.ssd_decode_step, lib.selective_scan_diag, lib.ssd_workspace_status,
+                      lib.ssd_selftest_bounded_wait):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != SSD_OK:
+        raise SsdError(status, load().ssd_last_error().decode())
+
+
+def _io_code(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return SSD_F32
+    if dtype == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"io dtype must be float32 or bfloat16, got {dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(Bsz, L, H, P, N, G, io, flags=0) -> ssd_dims:
+    return ssd_dims(Bsz, L, H, P, N, G, io, flags)
+
+
+def ssd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, io_dtype, chunk_size) -> int:
+    d = _dims(batch, seqlen, nheads, headdim, dstate, ngroups, _io_code(io_dtype))
+    return int(load().ssd_workspace_size(ctypes.byref(d), int(chunk_size)))
+
+
+def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=256, y=None, final_state=None,
+                     workspace=None, stream=None, simt=False, want_final_state=True):
+    """Chunked SSD prefill. x[B,L,H,P], dt[B,L,H], B/C[B,L,G,N] (float32 or
+    bfloat16), A[H], D[H], init_state[B,H,P,N] (float32). Returns (y, final_state)."""
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev, io = x.device, x.dtype
+    _need(x, "x", (Bsz, L, H, P), io, dev)
+    _need(dt, "dt", (Bsz, L, H), io, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(B, "B", (Bsz, L, G, N), io, dev)
+    _need(C, "C", (Bsz, L, G, N), io, dev)
+    _need(D, "D", (H,), torch.float32, dev)
+    _need(init_state, "init_state", (Bsz, H, P, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", (Bsz, L, H, P), io, dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((Bsz, H, P, N), dtype=torch.float32, device=dev)
+    _need(final_state, "final_state", (Bsz, H, P, N), torch.float32, dev)
+    d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else 0)
+    lib = load()
+    ws_bytes = int(lib.ssd_workspace_size(ctypes.byref(d), int(chunk_size)))
+    if ws_bytes == 0:
+        _check(lib.ssd_scan_chunked(ctypes.byref(d), None, None, None, None, None, None, None, int(chunk_size),
+                                    None, None, None, 0, None))
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    elif workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError(f"workspace too small: {workspace.numel() * workspace.element_size()} < {ws_bytes}")
+    _check(lib.ssd_scan_chunked(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream, dev)))
+    return y, final_state
+
+
+def ssd_decode_step(state, x, dt, A, B, C, D=None, y=None, stream=None):
+    """One decode token; `state` [B,H,P,N] float32 is updated in place. Returns y[B,H,P]."""
+    Bsz, H, P, N = state.shape
+    G = B.shape[1]
+    dev, io = x.device, x.dtype
+    _need(state, "state", (Bsz, H, P, N), torch.float32, dev)
+    _need(x, "x", (Bsz, H, P), io, dev)
+    _need(dt, "dt", (Bsz, H), io, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(B, "B", (Bsz, G, N), io, dev)
+    _need(C, "C", (Bsz, G, N), io, dev)
+    _need(D, "D", (H,), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", (Bsz, H, P), io, dev)
+    d = _dims(Bsz, 1, H, P, N, G, _io_code(io))
+    _check(load().ssd_decode_step(ctypes.byref(d), _ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                  _ptr(D), _ptr(y), _stream(stream, dev)))
+    return y
+
+
+def selective_scan_diag(x, dt, A, B, C, D=None, init_state=None, chunk_size=2048, y=None, final_state=None,
+                        stream=None, want_final_state=True):
+    """Mamba-1 diagonal scan. x/dt[B,L,D], A[D,N], B/C[B,L,N], D[D],
+    init_state[B,D,N]. Returns (y, final_state)."""
+    Bsz, L, Dm = x.shape
+    N = A.shape[1]
+    dev, io = x.device, x.dtype
+    _need(x, "x", (Bsz, L, Dm), io, dev)
+    _need(dt, "dt", (Bsz, L, Dm), io, dev)
+    _need(A, "A", (Dm, N), torch.float32, dev)
+    _need(B, "B", (Bsz, L, N), io, dev)
+    _need(C, "C", (Bsz, L, N), io, dev)
+    _need(D, "D", (Dm,), torch.float32, dev)
+    _need(init_state, "init_state", (Bsz, Dm, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", (Bsz, L, Dm), io, dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((Bsz, Dm, N), dtype=torch.float32, device=dev)
+    _need(final_state, "final_state", (Bsz, Dm, N), torch.float32, dev)
+    _check(load().selective_scan_diag(Bsz, L, Dm, N, _io_code(io), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                      _ptr(D), _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state),
+                                      _stream(stream, dev)))
+    return y, final_state
+
+
+def ssd_workspace_status(workspace, stream=None) -> int:
+    """Waits for the stream and returns the status word of a workspace (0 = OK)."""
+    return int(load().ssd_workspace_status(_ptr(workspace), _stream(stream, workspace.device)))
+
+
+def ssd_record_stage_events(events) -> None:
+    """Arms per-stage timing of the next ssd_scan_chunked call on this thread.
+    `events`: 4 torch.cuda.Event(enable_timing=True) that have been recorded
+    once (so that the CUDA events exist), or None to cancel."""
+    if events is None:
+        _check(load().ssd_record_stage_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(int(e.cuda_event)) for e in events])
+    _check(load().ssd_record_stage_events(arr, len(events)))
+
+
+def ssd_selftest_bounded_wait(workspace, spin_limit, stream=None) -> None:
+    _check(load().ssd_selftest_bounded_wait(_ptr(workspace), int(spin_limit), _stream(stream, workspace.device)))

@@ -1,0 +1,342 @@
+// Chunked SSD prefill on the CUDA cores, float32 arithmetic.
+//
+// The sequence is cut into chunks of Q tokens, each chunk continuing from the
+// previous chunk's state ("Recurrence Scan", first section). With
+// a_t = dt_t * A_h and cs the inclusive cumulative sum of a inside a chunk,
+// the recurrence re-associates exactly into three steps:
+//
+//   chunk state  S_c[p,n]   = sum_j exp(cs_end - cs_j) dt_j x_j[p] B_j[n]
+//   state pass   h_in(c+1)  = exp(cs_end(c)) h_in(c) + S_c,  h_in(0) = h0
+//   chunk scan   y_i[p]     = sum_{j<=i} (C_i . B_j) exp(cs_i - cs_j) dt_j x_j[p]
+//                           + exp(cs_i) sum_n C_i[n] h_in(c)[p,n] + D x_i[p]
+//
+// (j, i run over the tokens of one chunk). The causal mask is a static
+// predicate on (i, j) ("Compiler-First State Space Duality ...", Table 7:
+// static mask). This path serves float32 inputs and every shape the
+// tensor-core path does not take; its register tiles are 4x4 per thread over
+// 64x64 output tiles.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kT = 256;
+constexpr int kTile = 64;
+
+// Loads dt of one chunk (zero past the end of the sequence) into s_dt and the
+// inclusive cumulative sum of dt*A into s_cs.
+template <typename T>
+__device__ __forceinline__ void chunk_cumsum(const T *__restrict__ dt, int64_t b, int64_t L, int64_t H, int h,
+                                             int64_t t0, int Q, float Ah, float *s_dt, float *s_cs,
+                                             float *scratch) {
+    const int tid = threadIdx.x;
+    float d = 0.f;
+    if (tid < Q && t0 + tid < L) d = to_f32(dt[(b * L + t0 + tid) * H + h]);
+    if (tid < Q) s_dt[tid] = d;
+    block_inclusive_scan_256(d * Ah, Q, s_cs, scratch);
+}
+
+// S_c for one (b, c, h) and one 64x64 tile of (p, n).
+template <typename T>
+__global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP, int tilesN) {
+    const int c = blockIdx.x;
+    const int tiles = tilesP * tilesN;
+    const int h = blockIdx.y / tiles, pt = (blockIdx.y % tiles) / tilesN, nt = blockIdx.y % tilesN;
+    const int64_t b = blockIdx.z;
+    const int64_t L = a.L, H = a.H, P = a.P, N = a.N, G = a.G;
+    const int Q = a.Q;
+    const int g = (int)(h / (H / G));
+    const int64_t t0 = (int64_t)c * Q;
+    const int Qv = (int)imin<int64_t>(Q, L - t0);
+    const T *x = (const T *)a.x, *Bm = (const T *)a.Bm;
+
+    __shared__ float s_dt[256], s_cs[256], s_w[256], scratch[8];
+    __shared__ float Xs[32][kTile + 4], Bs[32][kTile + 4];
+
+    chunk_cumsum<T>((const T *)a.dt, b, L, H, h, t0, Q, a.A[h], s_dt, s_cs, scratch);
+    const float cs_end = s_cs[Q - 1];  // padded tokens carry a = 0
+    const int tid = threadIdx.x;
+    if (tid < Q) s_w[tid] = expf(cs_end - s_cs[tid]) * s_dt[tid];
+    if (pt == 0 && nt == 0 && tid == 0) a.chunk_sum[(b * H + h) * a.nc + c] = cs_end;
+    __syncthreads();
+
+    const int ty = tid / 16, tx = tid % 16;
+    float acc[4][4] = {};
+    for (int j0 = 0; j0 < Qv; j0 += 32) {
+        for (int e = tid; e < 32 * kTile; e += kT) {
+            const int jj = e / kTile, q = e % kTile, j = j0 + jj;
+            const int64_t p = (int64_t)pt * kTile + q, n = (int64_t)nt * kTile + q;
+            const int64_t tok = b * L + t0 + j;
+            Xs[jj][q] = (j < Qv && p < P) ? s_w[j] * to_f32(x[(tok * H + h) * P + p]) : 0.f;
+            Bs[jj][q] = (j < Qv && n < N) ? to_f32(Bm[(tok * G + g) * N + n]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+            float xa[4], bb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xa[i] = Xs[jj][ty * 4 + i];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) bb[k] = Bs[jj][tx * 4 + k];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(xa[i], bb[k], acc[i][k]);
+        }
+        __syncthreads();
+    }
+    float *S = a.states + (((b * a.nc + c) * H + h) * P) * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t p = (int64_t)pt * kTile + ty * 4 + i;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t n = (int64_t)nt * kTile + tx * 4 + k;
+            if (p < P && n < N) S[p * N + n] = acc[i][k];
+        }
+    }
+}
+
+// Serial pass over the chunks of one (b, h), one state element per thread:
+// replaces S_c with the entering state h_in(c) (float32 in place and/or a
+// bfloat16 copy) and writes the final state.
+template <bool F32_INPLACE, bool BF16>
+__global__ void __launch_bounds__(kT) state_pass_kernel(ChunkedArgs a) {
+    // Wait for the producer of the chunk states when launched as a programmatic
+    // dependent of it; a no-op for an ordinary launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t PN = a.P * a.N;
+    const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+    const int h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    if (e >= PN) return;
+    const int64_t H = a.H, nc = a.nc;
+    float hv = a.init_state ? a.init_state[(b * H + h) * PN + e] : 0.f;
+    const float *cs = a.chunk_sum + (b * H + h) * nc;
+    const int64_t stride = H * PN;  // next chunk, same (b, h, element)
+    int64_t idx = ((b * nc) * H + h) * PN + e;
+    float s = nc > 0 ? a.states[idx] : 0.f;
+    for (int64_t c = 0; c < nc; ++c, idx += stride) {
+        const float s_next = (c + 1 < nc) ? a.states[idx + stride] : 0.f;
+        if (F32_INPLACE) a.states[idx] = hv;
+        if (BF16) {
+            __nv_bfloat16 v = __float2bfloat16_rn(hv);
+            a.states_bf16[idx] = *reinterpret_cast<uint16_t *>(&v);
+        }
+        hv = fmaf(expf(cs[c]), hv, s);
+        s = s_next;
+    }
+    if (a.final_state) a.final_state[(b * H + h) * PN + e] = hv;
+}
+
+// y for 64 rows of one chunk and one 64-wide tile of p, for one (b, h).
+template <typename T>
+__global__ void __launch_bounds__(kT) chunk_scan_simt(ChunkedArgs a, int tilesP) {
+    const int RBs = a.Q / kTile;
+    const int c = blockIdx.x / RBs, rb = blockIdx.x % RBs;
+    const int h = blockIdx.y / tilesP, pt = blockIdx.y % tilesP;
+    const int64_t b = blockIdx.z;
+    const int64_t L = a.L, H = a.H, P = a.P, N = a.N, G = a.G;
+    const int Q = a.Q;
+    const int g = (int)(h / (H / G));
+    const int64_t t0 = (int64_t)c * Q;
+    const int Qv = (int)imin<int64_t>(Q, L - t0);
+    if (rb * kTile >= Qv) return;
+    const T *x = (const T *)a.x, *Bm = (const T *)a.Bm, *Cm = (const T *)a.Cm;
+    T *y = (T *)a.y;
+    const int K = (rb + 1) * kTile;  // columns j of this row block: 0 .. K-1
+    const int GS = K + 1;            // padded row stride of G_s
+
+    extern __shared__ float smem[];
+    float *s_dt = smem, *s_cs = smem + 256, *scratch = smem + 512;
+    float *G_s = smem + 520;                 // [64][GS]
+    float *Cs = G_s + kTile * GS;            // [64][33]
+    float *Ws = Cs + kTile * 33;             // [64][33] or [32][65]
+
+    chunk_cumsum<T>((const T *)a.dt, b, L, H, h, t0, Q, a.A[h], s_dt, s_cs, scratch);
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int i_base = rb * kTile;  // chunk-local first row
+
+    // Phase 1: G[i, j] = (C_i . B_j) exp(cs_i - cs_j) dt_j for j <= i, else 0.
+    for (int jb = 0; jb <= rb; ++jb) {
+        float acc[4][4] = {};
+        for (int n0 = 0; n0 < N; n0 += 32) {
+            for (int e = tid; e < kTile * 32; e += kT) {
+                const int r = e / 32, nn = e % 32;
+                const int64_t n = n0 + nn;
+                const int ic = i_base + r, jc = jb * kTile + r;
+                Cs[r * 33 + nn] = (ic < Qv && n < N) ? to_f32(Cm[((b * L + t0 + ic) * G + g) * N + n]) : 0.f;
+                Ws[r * 33 + nn] = (jc < Qv && n < N) ? to_f32(Bm[((b * L + t0 + jc) * G + g) * N + n]) : 0.f;
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int nn = 0; nn < 32; ++nn) {
+                float ca[4], bb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ca[i] = Cs[(ty * 4 + i) * 33 + nn];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) bb[k] = Ws[(tx * 4 + k) * 33 + nn];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(ca[i], bb[k], acc[i][k]);
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int il = i_base + ty * 4 + i;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int jl = jb * kTile + tx * 4 + k;
+                float v = 0.f;
+                if (jl <= il && jl < Qv) v = acc[i][k] * expf(s_cs[il] - s_cs[jl]) * s_dt[jl];
+                G_s[(ty * 4 + i) * GS + jb * kTile + tx * 4 + k] = v;
+            }
+        }
+    }
+    __syncthreads();
+
+    // Phase 2: intra-chunk part G . X plus the entering-state part.
+    const int64_t p_base = (int64_t)pt * kTile;
+    float acc[4][4] = {};
+    for (int j0 = 0; j0 < K; j0 += 32) {
+        for (int e = tid; e < 32 * kTile; e += kT) {
+            const int jj = e / kTile, q = e % kTile, j = j0 + jj;
+            const int64_t p = p_base + q;
+            Ws[jj * 65 + q] = (j < Qv && p < P) ? to_f32(x[((b * L + t0 + j) * H + h) * P + p]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+            float ga[4], xb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ga[i] = G_s[(ty * 4 + i) * GS + j0 + jj];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) xb[k] = Ws[jj * 65 + tx * 4 + k];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(ga[i], xb[k], acc[i][k]);
+        }
+        __syncthreads();
+    }
+    float off[4][4] = {};
+    const float *hin = a.states + (((b * a.nc + c) * H + h) * P) * N;
+    for (int n0 = 0; n0 < N; n0 += 32) {
+        for (int e = tid; e < kTile * 32; e += kT) {
+            const int r = e / 32, nn = e % 32;
+            const int64_t n = n0 + nn;
+            const int ic = i_base + r;
+            const int64_t p = p_base + r;
+            Cs[r * 33 + nn] = (ic < Qv && n < N) ? to_f32(Cm[((b * L + t0 + ic) * G + g) * N + n]) : 0.f;
+            Ws[r * 33 + nn] = (p < P && n < N) ? hin[p * N + n] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int nn = 0; nn < 32; ++nn) {
+            float ca[4], hb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ca[i] = Cs[(ty * 4 + i) * 33 + nn];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) hb[k] = Ws[(tx * 4 + k) * 33 + nn];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) off[i][k] = fmaf(ca[i], hb[k], off[i][k]);
+        }
+        __syncthreads();
+    }
+    const float Dh = a.D ? a.D[h] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int il = i_base + ty * 4 + i;
+        if (il >= Qv) continue;
+        const float decay_in = expf(s_cs[il]);
+        const int64_t tok = b * L + t0 + il;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t p = p_base + tx * 4 + k;
+            if (p >= P) continue;
+            const int64_t o = (tok * H + h) * P + p;
+            const float xv = to_f32(x[o]);
+            y[o] = from_f32<T>(acc[i][k] + decay_in * off[i][k] + Dh * xv);
+        }
+    }
+}
+
+size_t scan_smem_bytes(int Q) {
+    const int K = Q;  // largest row block
+    return sizeof(float) * (520 + (size_t)kTile * (K + 1) + kTile * 33 + std::max(kTile * 33, 32 * 65));
+}
+
+template <typename T>
+cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
+    const int tilesP = (int)((a.P + kTile - 1) / kTile), tilesN = (int)((a.N + kTile - 1) / kTile);
+    cudaError_t e0 = mark_stage(a, 0, stream);
+    if (e0 != cudaSuccess) return e0;
+    if (a.nc > 0 && a.B > 0) {
+        chunk_state_simt<T><<<dim3((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B), kT, 0,
+                              stream>>>(a, tilesP, tilesN);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = mark_stage(a, 1, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_state_pass(a, true, false, stream, false);
+    if (e != cudaSuccess) return e;
+    e = mark_stage(a, 2, stream);
+    if (e != cudaSuccess) return e;
+    if (a.nc > 0 && a.B > 0) {
+        const size_t smem = scan_smem_bytes(a.Q);
+        static int configured = 0;  // the attribute only grows; set it once per process
+        if ((int)smem > configured) {
+            e = cudaFuncSetAttribute(chunk_scan_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)scan_smem_bytes(256));
+            if (e != cudaSuccess) return e;
+            configured = (int)scan_smem_bytes(256);
+        }
+        chunk_scan_simt<T><<<dim3((unsigned)(a.nc * (a.Q / kTile)), (unsigned)(a.H * tilesP), (unsigned)a.B), kT,
+                             smem, stream>>>(a, tilesP);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return mark_stage(a, 3, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool write_bf16, cudaStream_t stream,
+                              bool programmatic) {
+    if (a.B == 0) return cudaSuccess;
+    const int64_t PN = a.P * a.N;
+    dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B);
+    ChunkedArgs args = a;
+    void (*kern)(ChunkedArgs);
+    if (write_f32_inplace && write_bf16) kern = state_pass_kernel<true, true>;
+    else if (write_f32_inplace) kern = state_pass_kernel<true, false>;
+    else if (write_bf16) kern = state_pass_kernel<false, true>;
+    else kern = state_pass_kernel<false, false>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kT);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (programmatic) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+cudaError_t launch_chunked_simt(const ChunkedArgs &a, cudaStream_t stream) {
+    if (a.io == IO_BF16) return launch_simt_t<__nv_bfloat16>(a, stream);
+    return launch_simt_t<float>(a, stream);
+}
+
+}  // namespace ssd

@@ -1,0 +1,61 @@
+// Shared device helpers of the SSD kernels: element conversion, warp
+// reductions and the chunk-local inclusive cumulative sum of dt*A.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+template <typename I> __host__ __device__ __forceinline__ I imin(I a, I b) { return a < b ? a : b; }
+template <typename I> __host__ __device__ __forceinline__ I imax(I a, I b) { return a > b ? a : b; }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Inclusive prefix sum over a[0..n) held one value per thread (threads >= n
+// hold 0), for blockDim.x == 256 and n <= 256. Result written to out[0..n).
+// Fixed association (warp shuffle scan, then a scan of the 8 warp totals), so
+// it is bitwise reproducible. `scratch` holds at least 8 floats. Ends with a
+// __syncthreads().
+__device__ __forceinline__ void block_inclusive_scan_256(float a, int n, float *out, float *scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float v = a;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < 8 ? scratch[lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            float u = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += u;
+        }
+        if (lane < 8) scratch[lane] = t;  // inclusive totals
+    }
+    __syncthreads();
+    if (warp > 0) v += scratch[warp - 1];
+    if ((int)threadIdx.x < n) out[threadIdx.x] = v;
+    __syncthreads();
+}
+
+}  // namespace ssd

@@ -1,0 +1,65 @@
+// Internal host-side launchers shared between the C-ABI layer (ssd_api.cu)
+// and the kernel translation units. Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+enum IoType { IO_F32 = 0, IO_BF16 = 1 };
+
+// Sizes and pointers of one chunked SSD prefill call (layouts as in ssd_scan.h).
+struct ChunkedArgs {
+    int64_t B, L, H, P, N, G;
+    int Q;       // chunk size
+    int64_t nc;  // number of chunks, ceil(L / Q)
+    int io;      // IoType
+    const void *x, *dt, *Bm, *Cm;
+    const float *A, *D, *init_state;
+    void *y;
+    float *final_state;
+    // workspace carve
+    int *status;             // device status word
+    float *states;           // [B, nc, H, P, N] float32: chunk states, then entering states
+    uint16_t *states_bf16;   // [B, nc, H, P, N] bfloat16 entering states (tensor-core path)
+    float *chunk_sum;        // [B, H, nc] float32: sum of dt*A over each chunk
+    // optional stage timing: events[0..3] recorded before stage 1 and after
+    // stages 1, 2, 3 (all NULL when not requested)
+    cudaEvent_t stage_ev[4];
+};
+
+// Records stage event i of `a` on `stream` if requested (external node when
+// the stream is being captured).
+cudaError_t mark_stage(const ChunkedArgs &a, int i, cudaStream_t stream);
+
+// Workspace layout (byte offsets from the workspace base).
+struct WorkspaceLayout {
+    size_t status, states, states_bf16, chunk_sum, total;
+};
+WorkspaceLayout workspace_layout(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
+
+cudaError_t launch_decode(int io, int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, float *state,
+                          const void *x, const void *dt, const float *A, const void *Bm, const void *Cm,
+                          const float *D, void *y, cudaStream_t stream);
+
+// CUDA-core (float32 arithmetic) chunked path: chunk-state, state passing, chunk scan.
+cudaError_t launch_chunked_simt(const ChunkedArgs &a, cudaStream_t stream);
+
+// Tensor-core path (bf16 operands, tcgen05 MMAs). Returns cudaErrorNotSupported
+// when the shape is outside what it handles.
+bool chunked_tc_supported(const ChunkedArgs &a);
+cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream);
+
+// State passing across chunks (shared by both paths).
+cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool write_bf16,
+                              cudaStream_t stream, bool programmatic);
+
+cudaError_t launch_diag(int io, int64_t B, int64_t L, int64_t Dm, int64_t N, const void *x, const void *dt,
+                        const float *A, const void *Bm, const void *Cm, const float *D,
+                        const float *init_state, int chunk, void *y, float *final_state,
+                        cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
+
+}  // namespace ssd

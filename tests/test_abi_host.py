@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build, load, and export every function include/ssd_scan.h
+declares; argument validation must reject bad calls before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mamba_ssd_selective_gb300 import build as nvbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mamba_ssd_selective_gb300 import binding
+    nvbuild.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?(?:size_t|ssd_status|char|void|int)\s*\*?\s*(\w+)\s*\(", text, re.M):
+            names.append(m.group(1))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ("ssd_scan_chunked", "ssd_decode_step", "selective_scan_diag", "ssd_workspace_size",
+                 "ssd_last_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libssdscan.so does not export {name}"
+
+
+def test_library_links_no_libcuda_and_no_oracle():
+    # the CUDA runtime is static and the driver API is fetched at run time, so the
+    # library loads on a machine without a GPU driver; it never links the oracle
+    nvbuild.build()
+    import subprocess
+    out = subprocess.run(["readelf", "-d", nvbuild.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+    assert "oracle" not in out
+
+
+def _dims(binding, **kw):
+    base = dict(batch=1, seqlen=256, nheads=4, headdim=64, dstate=16, ngroups=1, io_dtype=0, flags=0)
+    base.update(kw)
+    return binding.ssd_dims(**base)
+
+
+def test_workspace_size(lib):
+    from mamba_ssd_selective_gb300 import binding
+    d = _dims(binding, batch=2, seqlen=1000, nheads=3, headdim=64, dstate=128, io_dtype=1)
+    ws = lib.ssd_workspace_size(ctypes.byref(d), 128)
+    nc = (1000 + 127) // 128
+    n_state = 2 * nc * 3 * 64 * 128
+    assert ws >= 256 + n_state * 4 + n_state * 2 + 2 * 3 * nc * 4
+    assert ws % 256 == 0
+    assert lib.ssd_workspace_size(ctypes.byref(d), 100) == 0          # bad chunk size
+    assert lib.ssd_workspace_size(None, 128) == 0                      # no dims
+    bad = _dims(binding, nheads=3, ngroups=2)
+    assert lib.ssd_workspace_size(ctypes.byref(bad), 64) == 0          # H % G != 0
+
+
+def _scan(lib, d, chunk=64, x=0x1000, ws=0x100000, ws_bytes=1 << 30):
+    vp = ctypes.c_void_p
+    return lib.ssd_scan_chunked(ctypes.byref(d) if d is not None else None, vp(x), vp(0x1000), vp(0x1000),
+                                vp(0x1000), vp(0x1000), None, None, chunk, vp(0x1000), None,
+                                vp(ws) if ws else None, ws_bytes, None)
+
+
+def test_validation_rejects_before_any_cuda_call(lib):
+    from mamba_ssd_selective_gb300 import binding
+    E = binding.SSD_ERR_INVALID_ARG
+    d = _dims(binding)
+    assert _scan(lib, None) == E
+    assert b"dims" in lib.ssd_last_error()
+    assert _scan(lib, d, chunk=100) == E
+    assert b"chunk_size" in lib.ssd_last_error()
+    assert _scan(lib, d, x=0) == E                                     # NULL x
+    assert _scan(lib, d, x=0x1008) == E                                # misaligned x
+    assert b"aligned" in lib.ssd_last_error()
+    assert _scan(lib, d, ws=0) == E                                    # NULL workspace
+    assert _scan(lib, d, ws=0x100010) == E                             # workspace not 256-aligned
+    assert _scan(lib, d, ws_bytes=16) == E                             # workspace too small
+    assert b"too small" in lib.ssd_last_error()
+    assert _scan(lib, _dims(binding, nheads=6, ngroups=4)) == E
+    assert _scan(lib, _dims(binding, io_dtype=7)) == E
+    assert _scan(lib, _dims(binding, flags=8)) == E
+    assert _scan(lib, _dims(binding, headdim=0)) == E
+    assert _scan(lib, _dims(binding, seqlen=-1)) == E
+    assert _scan(lib, _dims(binding, nheads=70000)) == binding.SSD_ERR_UNSUPPORTED
+    # an empty batch is a valid no-op and touches nothing
+    assert _scan(lib, _dims(binding, batch=0), x=0, ws=0) == binding.SSD_OK
+
+
+def test_decode_and_diag_validation(lib):
+    from mamba_ssd_selective_gb300 import binding
+    vp = ctypes.c_void_p
+    d = _dims(binding)
+    E = binding.SSD_ERR_INVALID_ARG
+    assert lib.ssd_decode_step(ctypes.byref(d), None, *[vp(0x1000)] * 5, None, vp(0x1000), None) == E
+    assert lib.ssd_decode_step(ctypes.byref(d), vp(0x1004), *[vp(0x1000)] * 5, None, vp(0x1000), None) == E
+    assert lib.ssd_decode_step(ctypes.byref(_dims(binding, batch=0)), *[None] * 9) == binding.SSD_OK
+    args = [vp(0x1000)] * 5 + [None, None]
+    assert lib.selective_scan_diag(1, 64, 128, 16, 1, *args, 48, vp(0x1000), None, None) == E   # chunk % 32
+    assert lib.selective_scan_diag(1, 64, 128, 65, 1, *args, 64, vp(0x1000), None, None) == \
+        binding.SSD_ERR_UNSUPPORTED
+    assert lib.selective_scan_diag(1, 64, 0, 16, 1, *args, 64, vp(0x1000), None, None) == E
+    assert lib.selective_scan_diag(1, 64, 128, 16, 3, *args, 64, vp(0x1000), None, None) == E
+    assert lib.selective_scan_diag(0, 64, 128, 16, 1, *[None] * 7, 64, None, None, None) == binding.SSD_OK
+    assert lib.ssd_selftest_bounded_wait(None, 10, None) == E
+    assert lib.ssd_selftest_bounded_wait(vp(0x1000), 0, None) == E
+
+
+def test_binding_checks_shapes_on_cpu_tensors():
+    import torch
+    from mamba_ssd_selective_gb300 import binding
+    x = torch.zeros(1, 8, 2, 4)
+    with pytest.raises((ValueError, TypeError)):
+        binding.ssd_scan_chunked(x, torch.zeros(1, 8, 3), torch.zeros(2), torch.zeros(1, 8, 1, 4),
+                                 torch.zeros(1, 8, 1, 4), chunk_size=64)

@@ -1,0 +1,315 @@
+"""Parity of the CUDA kernels with the float64 oracle, through the C ABI.
+
+Small cases compare every element; the full-size workloads compare every
+element where the oracle finishes in seconds and sampled heads / channels
+otherwise. Tolerances are in tests/helpers.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mamba_ssd_selective_gb300 import inputs
+from tests.helpers import IO_TORCH, check, check_bf16, dev, head_slice, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    from mamba_ssd_selective_gb300 import binding
+    binding.load()
+    return binding
+
+
+def run_scan(ssd, d, io, chunk, simt=False, init=True, D=True, want_final=True):
+    t = IO_TORCH[io]
+    y, hT = ssd.ssd_scan_chunked(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                 dev(d["D"]) if D else None, dev(d["init_state"]) if init else None,
+                                 chunk_size=chunk, simt=simt, want_final_state=want_final)
+    torch.cuda.synchronize()
+    return y, hT
+
+
+def ref_scan(d, init=True, D=True):
+    return oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"] if D else None,
+                          d["init_state"] if init else None)
+
+
+# ----------------------------------------------------------------- prefill
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_prefill_tiny_f32_workload(ssd, chunk):
+    """B1 L256 H4 P64 N16 G1, float32, zero initial state (chunk 64 is the workload's own)."""
+    w = inputs.WORKLOADS["ssd_tiny_f32"]
+    d = inputs.ssd_inputs(w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                          io_dtype="f32", seed=0)
+    yr, hr = ref_scan(d, init=False)
+    y, h = run_scan(ssd, d, "f32", chunk, init=False)
+    check("f32", y, yr, "y")
+    check("f32", h, hr, "final_state")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+@pytest.mark.parametrize("shape", [(2, 333, 4, 48, 20, 2), (1, 300, 2, 64, 128, 1), (3, 129, 6, 80, 70, 3)])
+def test_prefill_ragged_groups_init(ssd, io, chunk, shape):
+    """Ragged L (not a multiple of the chunk), P/N not multiples of 64, groups, init state and D."""
+    Bz, L, H, P, N, G = shape
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype=io, seed=7, init_state=True)
+    yr, hr = ref_scan(d)
+    y, h = run_scan(ssd, d, io, chunk)
+    check(io, y, yr, "y")
+    check(io, h, hr, "final_state")
+
+
+@pytest.mark.parametrize("simt", [False, True])
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_prefill_m2_130m_workload_full(ssd, chunk, simt):
+    """B1 L4096 H24 P64 N128 G1, bf16 inputs / fp32 state: every element of y and the state."""
+    w = inputs.WORKLOADS["ssd_m2_130m_L4096"]
+    d = inputs.ssd_inputs(w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                          io_dtype="bf16", seed=0)
+    yr, hr = _cached_ref("m2_130m", d)
+    y, h = run_scan(ssd, d, "bf16", chunk, simt=simt, init=False)
+    check("bf16", y, yr, "y")
+    check("bf16", h, hr, "final_state")
+
+
+_REF_CACHE = {}
+
+
+def _cached_ref(key, d, init=False):
+    if key not in _REF_CACHE:
+        _REF_CACHE[key] = ref_scan(d, init=init)
+    return _REF_CACHE[key]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["ssd_m2_2p7b_L1024", "ssd_m2_2p7b_L4096", "ssd_m2_2p7b_L8192",
+                                  "ssd_m2_2p7b_B8_L2048"])
+def test_prefill_m2_2p7b_workloads_sampled_heads(ssd, name):
+    """H80 P64 N128 workloads at full size on the GPU; the oracle checks sampled heads
+    (all batches, all tokens, y and final state), for each chunk size."""
+    w = inputs.WORKLOADS[name]
+    d = inputs.ssd_inputs(w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                          io_dtype="bf16", seed=0)
+    heads = [0, 37, 79]
+    refs = {h: ref_scan(head_slice(d, h), init=False) for h in heads}
+    for chunk in (64, 128, 256):
+        y, hT = run_scan(ssd, d, "bf16", chunk, init=False)
+        for h in heads:
+            yr, hr = refs[h]
+            check_bf16(y[:, :, h:h + 1], yr, f"{name} chunk {chunk} head {h} y")
+            check_bf16(hT[:, h:h + 1], hr, f"{name} chunk {chunk} head {h} state")
+        del y, hT
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_prefill_edge_lengths(ssd, io):
+    """L = 0 (state passes through), 1, shorter than a chunk, one past a chunk."""
+    for L in (0, 1, 5, 65, 257):
+        d = inputs.ssd_inputs(2, L, 2, 64, 128, 1, io_dtype=io, seed=L, init_state=True)
+        yr, hr = ref_scan(d)
+        for chunk in (64, 256):
+            y, h = run_scan(ssd, d, io, chunk)
+            if L:
+                check(io, y, yr, f"L={L} y")
+            check(io, h, hr, f"L={L} state")
+    # L = 0 without an initial state gives a zero final state
+    d = inputs.ssd_inputs(1, 0, 2, 64, 16, 1, io_dtype=io, seed=1)
+    _, h = run_scan(ssd, d, io, 64, init=False)
+    assert float(h.abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_prefill_optional_outputs_and_aliasing(ssd, io):
+    """D = NULL, final_state = NULL, and final_state aliasing init_state."""
+    t = IO_TORCH[io]
+    d = inputs.ssd_inputs(1, 200, 4, 64, 128, 1, io_dtype=io, seed=3, init_state=True)
+    yr, hr = ref_scan(d, D=False)
+    y, h = run_scan(ssd, d, io, 128, D=False, want_final=False)
+    assert h is None
+    check(io, y, yr, "y without D")
+    st = dev(d["init_state"])
+    y2, h2 = ssd.ssd_scan_chunked(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                  None, st, chunk_size=128, final_state=st)
+    torch.cuda.synchronize()
+    assert h2.data_ptr() == st.data_ptr()
+    check(io, st, hr, "state updated in place")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_prefill_deterministic_and_batched_equals_solo(ssd, io):
+    d = inputs.ssd_inputs(3, 300, 4, 64, 128, 1, io_dtype=io, seed=5, init_state=True)
+    y1, h1 = run_scan(ssd, d, io, 128)
+    y2, h2 = run_scan(ssd, d, io, 128)
+    assert torch.equal(y1, y2) and torch.equal(h1, h2)
+    for b in range(3):
+        db = {k: (v[b:b + 1] if (v is not None and k not in ("A", "D")) else v) for k, v in d.items()}
+        yb, hb = run_scan(ssd, db, io, 128)
+        assert torch.equal(yb[0], y1[b]) and torch.equal(hb[0], h1[b])
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_prefill_split_resume_and_decode_continuation(ssd, io):
+    """scan(L1) then scan(L2 | state) == scan(L1 + L2); prefill(L) then one decode
+    step == prefill(L + 1)."""
+    t = IO_TORCH[io]
+    d = inputs.ssd_inputs(2, 301, 4, 64, 128, 1, io_dtype=io, seed=9, init_state=True)
+    yf, hf = run_scan(ssd, d, io, 128)
+    cut = 170
+    a = {k: (v[:, :cut] if k in ("x", "dt", "B", "C") else v) for k, v in d.items()}
+    b = {k: (v[:, cut:] if k in ("x", "dt", "B", "C") else v) for k, v in d.items()}
+    y1, h1 = run_scan(ssd, a, io, 128)
+    b["init_state"] = host(h1)
+    y2, h2 = run_scan(ssd, b, io, 128)
+    check(io, host(torch.cat([y1, y2], 1)), host(yf), "split y")
+    check(io, host(h2), host(hf), "split state")
+    # prefill(L-1) + decode == prefill(L)
+    p = {k: (v[:, :300] if k in ("x", "dt", "B", "C") else v) for k, v in d.items()}
+    _, hp = run_scan(ssd, p, io, 128)
+    yd = ssd.ssd_decode_step(hp, dev(d["x"][:, 300], t), dev(d["dt"][:, 300], t), dev(d["A"]),
+                             dev(d["B"][:, 300], t), dev(d["C"][:, 300], t), dev(d["D"]))
+    torch.cuda.synchronize()
+    check(io, host(yd), host(yf[:, 300]), "decode after prefill y")
+    check(io, host(hp), host(hf), "decode after prefill state")
+
+
+def test_prefill_chunk_size_independent_within_tolerance(ssd):
+    d = inputs.ssd_inputs(1, 1000, 4, 64, 128, 1, io_dtype="bf16", seed=2, init_state=True)
+    y64, h64 = run_scan(ssd, d, "bf16", 64)
+    for q in (128, 256):
+        yq, hq = run_scan(ssd, d, "bf16", q)
+        check_bf16(yq, host(y64), f"chunk {q} vs 64 y")
+        check_bf16(hq, host(h64), f"chunk {q} vs 64 state")
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode_inputs(step, Bz, H, P, N, G, io):
+    return inputs.decode_step_inputs(step, Bz, H, P, N, G, io_dtype=io, seed=0)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(4, 80, 64, 128, 1), (3, 6, 10, 30, 2), (2, 4, 64, 256, 4)])
+def test_decode_steps_every_element(ssd, io, shape):
+    Bz, H, P, N, G = shape
+    t = IO_TORCH[io]
+    st_ref = inputs.decode_state(Bz, H, P, N, seed=0)
+    prm = inputs.decode_params(H, seed=0)
+    st = dev(st_ref)
+    A, D = dev(prm["A"]), dev(prm["D"])
+    for s in range(10):
+        di = _decode_inputs(s, Bz, H, P, N, G, io)
+        y = ssd.ssd_decode_step(st, dev(di["x"], t), dev(di["dt"], t), A, dev(di["B"], t), dev(di["C"], t), D)
+        yr, st_ref = oracle.ssd_decode(st_ref, di["x"], di["dt"], prm["A"], di["B"], di["C"], prm["D"])
+        torch.cuda.synchronize()
+        check(io, y, yr, f"step {s} y")
+    check(io, st, st_ref, "state after 10 steps")
+
+
+@pytest.mark.slow
+def test_decode_workload_1000_steps_sampled(ssd):
+    """B64 H80 P64 N128, fp32 state ~N(0,0.1), bf16 per-step inputs, 1000 in-place
+    steps. The oracle replays sampled (b, h) rows as one 1000-token sequence
+    (decode == prefill of the same tokens, pinned on the oracle) and checks y
+    at steps 1, 10, 100, 1000 and the state after step 1000."""
+    w = inputs.WORKLOADS["decode_B64_H80"]
+    Bz, H, P, N, G, steps = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["steps"]
+    t = torch.bfloat16
+    st0 = inputs.decode_state(Bz, H, P, N, seed=0)
+    prm = inputs.decode_params(H, seed=0)
+    st = dev(st0)
+    A, D = dev(prm["A"]), dev(prm["D"])
+    samples = [(0, 0), (17, 41), (63, 79), (32, 5)]
+    seq = {k: [] for k in ("x", "dt", "B", "C")}
+    ys = {}
+    for s in range(steps):
+        di = _decode_inputs(s, Bz, H, P, N, G, "bf16")
+        y = ssd.ssd_decode_step(st, dev(di["x"], t), dev(di["dt"], t), A, dev(di["B"], t), dev(di["C"], t), D)
+        if s + 1 in (1, 10, 100, 1000):
+            ys[s + 1] = host(y)
+        for k in seq:
+            seq[k].append(di[k])
+    torch.cuda.synchronize()
+    stg = host(st)
+    for (b, h) in samples:
+        g = h // (H // G)
+        x = np.stack([a[b, h] for a in seq["x"]])[None, :, None, :]
+        dt = np.array([a[b, h] for a in seq["dt"]])[None, :, None]
+        Bm = np.stack([a[b, g] for a in seq["B"]])[None, :, None, :]
+        Cm = np.stack([a[b, g] for a in seq["C"]])[None, :, None, :]
+        yr, hr = oracle.ssd_seq(x, dt, prm["A"][h:h + 1], Bm, Cm, prm["D"][h:h + 1], st0[b:b + 1, h:h + 1])
+        for s, yg in ys.items():
+            check_bf16(yg[b, h], yr[0, s - 1, 0], f"(b,h)=({b},{h}) y at step {s}")
+        check_bf16(stg[b, h], hr[0, 0], f"(b,h)=({b},{h}) state after {steps} steps")
+
+
+# ------------------------------------------------------------------ Mamba-1
+
+def run_diag(ssd, d, io, chunk, init=True):
+    t = IO_TORCH[io]
+    y, h = ssd.selective_scan_diag(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                   dev(d["D"]), dev(d["init_state"]) if init else None, chunk_size=chunk)
+    torch.cuda.synchronize()
+    return y, h
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 300, 256, 16), (1, 77, 130, 5), (2, 64, 100, 40)])
+def test_diag_every_element(ssd, io, shape):
+    Bz, L, Dm, N = shape
+    d = inputs.diag_inputs(Bz, L, Dm, N, io_dtype=io, seed=4, init_state=True)
+    yr, hr = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"])
+    y, h = run_diag(ssd, d, io, 64)
+    check(io, y, yr, "y")
+    check(io, h, hr, "final_state")
+
+
+def test_diag_chunk_size_bitwise_independent(ssd):
+    d = inputs.diag_inputs(2, 1000, 300, 16, io_dtype="bf16", seed=6, init_state=True)
+    y0, h0 = run_diag(ssd, d, "bf16", 32)
+    for c in (96, 256, 512, 1024, 2048):
+        y, h = run_diag(ssd, d, "bf16", c)
+        assert torch.equal(y, y0) and torch.equal(h, h0), f"chunk {c}"
+
+
+@pytest.mark.slow
+def test_diag_mamba1_workload_sampled(ssd):
+    """B8 L2048 D5120 N16, A = -(1..16): full size on the GPU; the oracle checks
+    sampled channels of every batch (all tokens, y and final state)."""
+    w = inputs.WORKLOADS["mamba1_B8_L2048_D5120"]
+    d = inputs.diag_inputs(w["batch"], w["seqlen"], w["dim"], w["dstate"], io_dtype="bf16", seed=0)
+    chans = np.array([0, 1, 127, 128, 2049, 4000, 5119])
+    ds = dict(x=d["x"][:, :, chans], dt=d["dt"][:, :, chans], A=d["A"][chans], B=d["B"], C=d["C"], D=d["D"][chans])
+    yr, hr = oracle.diag_seq(ds["x"], ds["dt"], ds["A"], ds["B"], ds["C"], ds["D"])
+    for chunk in (256, 2048):
+        y, h = run_diag(ssd, d, "bf16", chunk, init=False)
+        yh, hh = host(y)[:, :, chans], host(h)[:, chans]
+        for i, c in enumerate(chans):
+            check_bf16(yh[:, :, i], yr[:, :, i], f"channel {c} y")
+            check_bf16(hh[:, i], hr[:, i], f"channel {c} state")
+
+
+# ------------------------------------------------------- failure detection
+
+def test_bounded_wait_times_out_and_context_survives(ssd):
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
+    ssd.ssd_selftest_bounded_wait(ws, 1000)
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_ERR_TIMEOUT
+    # the context is still usable
+    d = inputs.ssd_inputs(1, 64, 2, 64, 16, 1, io_dtype="f32", seed=1)
+    yr, hr = ref_scan(d, init=False)
+    y, h = run_scan(ssd, d, "f32", 64, init=False)
+    check("f32", y, yr, "y after timeout self-test")
+
+
+def test_workspace_status_ok_after_tensor_core_scan(ssd):
+    d = inputs.ssd_inputs(1, 512, 4, 64, 128, 1, io_dtype="bf16", seed=1)
+    t = torch.bfloat16
+    ws = torch.empty(ssd.ssd_workspace_size(1, 512, 4, 64, 128, 1, t, 128), dtype=torch.uint8, device="cuda")
+    ssd.ssd_scan_chunked(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                         dev(d["D"]), None, chunk_size=128, workspace=ws)
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
