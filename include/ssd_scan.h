@@ -114,6 +114,30 @@ ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt,
                             size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * ssd_scan_chunked without a caller-provided workspace, for callers that
+ * cannot allocate device memory where they run the scan: code running while
+ * the stream is being captured into a CUDA graph (cudaMalloc is refused during
+ * capture), plug-ins whose host framework owns all device memory, and
+ * latency-critical loops that cannot take the device-wide synchronisation of an
+ * allocation. The pages have no counterpart of this call; it exists for such
+ * callers only.
+ *
+ * Same arguments and results as ssd_scan_chunked, minus the workspace: the
+ * per-chunk states live in a 64 MiB scratch array compiled into the library
+ * (a file-scope __device__ array that every GPU loading it holds until the
+ * process exits). Sizes whose ssd_workspace_size() exceeds 64 MiB return
+ * SSD_ERR_UNSUPPORTED and launch nothing. The first call on each device looks
+ * up the scratch address with that device current; make it before any stream
+ * capture begins. Nothing here allocates. All calls on a device share the
+ * scratch: calls whose kernels may overlap on the GPU (e.g. on two unordered
+ * streams) race on it and must be serialised by the caller.
+ */
+ssd_status ssd_scan_chunked_noalloc(const ssd_dims *dims, const void *x, const void *dt, const float *A,
+                                    const void *B, const void *C, const float *D,
+                                    const float *init_state, int chunk_size, void *y,
+                                    float *final_state, cudaStream_t stream);
+
+/*
  * One decode token for a batch of sequences, state updated in place (the
  * O(1) cached decode of "Compiler-First State Space Duality ...", Figure 1;
  * the state is laid out [B, H, P, N] with N contiguous, so a warp streams one

@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
             lib.ssd_workspace_size.argtypes = [dp, ctypes.c_int]
             lib.ssd_workspace_size.restype = sz
             lib.ssd_scan_chunked.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp, sz, vp]
+            lib.ssd_scan_chunked_noalloc.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
+            lib.ssd_scan_chunked_noalloc.restype = ctypes.c_int
             lib.ssd_decode_step.argtypes = [dp] + [vp] * 9
             lib.selective_scan_diag.argtypes = [i64, i64, i64, i64, i32] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
             lib.ssd_workspace_status.argtypes = [vp, vp]
@@ -156,6 +158,37 @@ def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=256, y=
     _check(lib.ssd_scan_chunked(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                                 _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream, dev)))
+    return y, final_state
+
+
+def ssd_scan_chunked_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size=256, y=None, final_state=None,
+                             stream=None, simt=False):
+    """ssd_scan_chunked without a workspace argument: the per-chunk states go to
+    the library's built-in 64 MiB device scratch, so the C call allocates
+    nothing (for callers that cannot allocate where they run the scan, e.g.
+    inside someone else's graph capture). `y` and `final_state` must be given
+    by such callers; they are allocated here only for convenience when None.
+    Returns (y, final_state)."""
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev, io = x.device, x.dtype
+    _need(dt, "dt", (Bsz, L, H), io, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(B, "B", (Bsz, L, G, N), io, dev)
+    _need(C, "C", (Bsz, L, G, N), io, dev)
+    _need(D, "D", (H,), torch.float32, dev)
+    _need(init_state, "init_state", (Bsz, H, P, N), torch.float32, dev)
+    _need(x, "x", (Bsz, L, H, P), io, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", (Bsz, L, H, P), io, dev)
+    _need(final_state, "final_state", (Bsz, H, P, N), torch.float32, dev)
+    d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else 0)
+    _check(load().ssd_scan_chunked_noalloc(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                           _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state),
+                                           _stream(stream, dev)))
     return y, final_state
 
 

@@ -62,4 +62,7 @@ cudaError_t launch_diag(int io, int64_t B, int64_t L, int64_t Dm, int64_t N, con
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 
+// Sets the thread-local text returned by ssd_last_error() and returns `status`.
+int set_error(int status, const char *fmt, ...);
+
 }  // namespace ssd

@@ -58,6 +58,14 @@ bool valid_chunk(int q) { return q == 64 || q == 128 || q == 256; }
 }  // namespace
 
 namespace ssd {
+int set_error(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
 cudaError_t mark_stage(const ChunkedArgs &a, int i, cudaStream_t stream) {
     if (!a.stage_ev[i]) return cudaSuccess;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
