@@ -100,36 +100,78 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
     }
 }
 
-// Serial pass over the chunks of one (b, h), one state element per thread:
-// replaces S_c with the entering state h_in(c) (float32 in place and/or a
-// bfloat16 copy) and writes the final state.
-template <bool F32_INPLACE, bool BF16>
+// Serial pass over the chunks of one (b, h): replaces S_c with the entering
+// state h_in(c) (float32 in place and/or a bfloat16 copy) and writes the
+// final state. VW consecutive state elements per thread; the chunk states of
+// kPF chunks are loaded before the serial update consumes them, so each
+// thread keeps kPF independent loads in flight.
+constexpr int kPF = 8;
+
+template <bool F32_INPLACE, bool BF16, int VW>
 __global__ void __launch_bounds__(kT) state_pass_kernel(ChunkedArgs a) {
     // Wait for the producer of the chunk states when launched as a programmatic
     // dependent of it; a no-op for an ordinary launch.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the chunk scan may start its independent prologue now; it waits for
+    // this grid's completion before it reads the entering states
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t PN = a.P * a.N;
-    const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+    const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * VW;
     const int h = blockIdx.y;
     const int64_t b = blockIdx.z;
     if (e >= PN) return;
     const int64_t H = a.H, nc = a.nc;
-    float hv = a.init_state ? a.init_state[(b * H + h) * PN + e] : 0.f;
+    float hv[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k) hv[k] = a.init_state ? a.init_state[(b * H + h) * PN + e + k] : 0.f;
     const float *cs = a.chunk_sum + (b * H + h) * nc;
     const int64_t stride = H * PN;  // next chunk, same (b, h, element)
-    int64_t idx = ((b * nc) * H + h) * PN + e;
-    float s = nc > 0 ? a.states[idx] : 0.f;
-    for (int64_t c = 0; c < nc; ++c, idx += stride) {
-        const float s_next = (c + 1 < nc) ? a.states[idx + stride] : 0.f;
-        if (F32_INPLACE) a.states[idx] = hv;
-        if (BF16) {
-            __nv_bfloat16 v = __float2bfloat16_rn(hv);
-            a.states_bf16[idx] = *reinterpret_cast<uint16_t *>(&v);
+    const int64_t base = ((b * nc) * H + h) * PN + e;
+    for (int64_t c0 = 0; c0 < nc; c0 += kPF) {
+        float s[kPF][VW], dA[kPF];
+#pragma unroll
+        for (int u = 0; u < kPF; ++u) {
+            if (c0 + u < nc) {
+                const float *src = a.states + base + (c0 + u) * stride;
+                if constexpr (VW == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    s[u][0] = v.x; s[u][1] = v.y; s[u][2] = v.z; s[u][3] = v.w;
+                } else {
+                    s[u][0] = *src;
+                }
+                dA[u] = expf(cs[c0 + u]);
+            }
         }
-        hv = fmaf(expf(cs[c]), hv, s);
-        s = s_next;
+#pragma unroll
+        for (int u = 0; u < kPF; ++u) {
+            if (c0 + u < nc) {
+                const int64_t idx = base + (c0 + u) * stride;
+                if (F32_INPLACE) {
+                    if constexpr (VW == 4)
+                        *reinterpret_cast<float4 *>(a.states + idx) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                    else
+                        a.states[idx] = hv[0];
+                }
+                if (BF16) {
+                    if constexpr (VW == 4) {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(hv[0], hv[1]);
+                        __nv_bfloat162 hi = __floats2bfloat162_rn(hv[2], hv[3]);
+                        uint2 pk = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                        *reinterpret_cast<uint2 *>(a.states_bf16 + idx) = pk;
+                    } else {
+                        __nv_bfloat16 v = __float2bfloat16_rn(hv[0]);
+                        a.states_bf16[idx] = *reinterpret_cast<uint16_t *>(&v);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < VW; ++k) hv[k] = fmaf(dA[u], hv[k], s[u][k]);
+            }
+        }
     }
-    if (a.final_state) a.final_state[(b * H + h) * PN + e] = hv;
+    if (a.final_state) {
+#pragma unroll
+        for (int k = 0; k < VW; ++k) a.final_state[(b * H + h) * PN + e + k] = hv[k];
+    }
 }
 
 // y for 64 rows of one chunk and one 64-wide tile of p, for one (b, h).
@@ -309,17 +351,25 @@ cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
+template <int VW>
+void (*pick_state_pass(bool f32, bool bf16))(ChunkedArgs) {
+    if (f32 && bf16) return state_pass_kernel<true, true, VW>;
+    if (f32) return state_pass_kernel<true, false, VW>;
+    if (bf16) return state_pass_kernel<false, true, VW>;
+    return state_pass_kernel<false, false, VW>;
+}
+
 cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool write_bf16, cudaStream_t stream,
                               bool programmatic) {
     if (a.B == 0) return cudaSuccess;
     const int64_t PN = a.P * a.N;
-    dim3 grid((unsigned)((PN + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B);
-    ChunkedArgs args = a;
-    void (*kern)(ChunkedArgs);
-    if (write_f32_inplace && write_bf16) kern = state_pass_kernel<true, true>;
-    else if (write_f32_inplace) kern = state_pass_kernel<true, false>;
-    else if (write_bf16) kern = state_pass_kernel<false, true>;
-    else kern = state_pass_kernel<false, false>;
+    // float4 path: every (b, c, h) block of PN floats starts 16-byte aligned
+    const bool vec = (PN % 4 == 0) && (reinterpret_cast<uintptr_t>(a.init_state) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(a.final_state) % 16 == 0);
+    const int VW = vec ? 4 : 1;
+    dim3 grid((unsigned)((PN / VW + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B);
+    void (*kern)(ChunkedArgs) = vec ? pick_state_pass<4>(write_f32_inplace, write_bf16)
+                                    : pick_state_pass<1>(write_f32_inplace, write_bf16);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kT);
@@ -331,7 +381,7 @@ cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, args);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_chunked_simt(const ChunkedArgs &a, cudaStream_t stream) {

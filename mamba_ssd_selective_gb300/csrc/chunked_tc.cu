@@ -1,5 +1,34 @@
-// Tensor-core (tcgen05) chunked SSD prefill for bf16 inputs, and the
-// bounded-wait self-test kernel.
+// Tensor-core chunked SSD prefill for bf16 inputs with headdim P = 64 and
+// d_state N = 128 (the Mamba-2 layer shapes), and the bounded-wait self-test.
+//
+// Same three steps as the CUDA-core path (see chunked_simt.cu for the algebra:
+// chunk state, state passing, chunk scan), with both chunk kernels built on
+// tcgen05 MMAs: bf16 operands staged in shared memory by TMA with the 128-byte
+// swizzle, float32 accumulators in tensor memory (TMEM), one elected thread
+// issuing the MMAs, 4 warps moving accumulators TMEM -> registers for the
+// epilogues. Decays, cumulative sums and exponentials stay float32.
+//
+//   chunk_state_tc  one CTA per (b, chunk c, head h):
+//       S_c^T[n, p] = sum_j B_j[n] * (w_j x_j[p]),  w_j = exp(cs_end - cs_j) dt_j
+//       one MMA chain M = 128 (n), N = 64 (p), K = Q (j); both operands
+//       MN-major (tokens are the outer dimension in HBM).
+//   state_pass      (shared with the CUDA-core path) writes the entering
+//       states as a bf16 copy, the B operand of the output MMA.
+//   chunk_scan_tc   one CTA per (b, 128-token tile, head h):
+//       S  = C_tile B_k^T            (M = 128 rows i, N = 128 cols j, K = N)
+//       S' = S o exp(cs_i - cs_j) dt_j, static causal & same-chunk mask
+//       Y += S' X_k                  (M = 128, N = P, K = 128)  per K-block k
+//       Yo = C_tile h_in^T           (M = 128, N = P, K = N)    per chunk
+//       y  = Y + exp(cs_i - cs_chunk_start) Yo + D x  -> bf16 -> TMA store
+//   The K-blocks of a tile are the 128-token blocks from the start of the
+//   tile's chunk up to the tile (1 block for Q <= 128, 2 for the second half
+//   of a 256-token chunk); a 128-token tile holds two 64-token chunks.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "ssd_scan.h"
@@ -7,6 +36,813 @@
 
 namespace ssd {
 namespace {
+
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: a wait this long means something is broken
+constexpr int kRows = 128;                   // token rows per tile (MMA M)
+constexpr int kP = 64;                       // headdim handled here
+constexpr int kN = 128;                      // d_state handled here
+
+struct TcParams {
+    ChunkedArgs a;
+    CUtensorMap mx;    // x  as (H*P, L, B), box (64, R, 1)
+    CUtensorMap mb;    // B  as (G*N, L, B), box (64, R, 1)
+    CUtensorMap mc;    // C  as (G*N, L, B), box (64, 128, 1)   (chunk scan)
+    CUtensorMap my;    // y  as (H*P, L, B), box (64, 128, 1)   (chunk scan)
+    CUtensorMap mh;    // bf16 entering states as (N, B*nc*H*P), box (64, 64)   (chunk scan)
+    CUtensorMap my32;  // y  as (H*P, L, B), box (32, 32, 1), 64-byte swizzle (persistent chunk scan)
+    int hb;            // heads per work item of the persistent chunk scan (divides H / G)
+    int nhg;           // head groups, H / hb
+    int64_t n_items;   // work items of the persistent chunk scan, B * tiles * nhg
+};
+
+// ---------------------------------------------------------------- helpers
+
+// In-place inclusive prefix sum of buf[0..n) (n <= 256) by a 128-thread CTA;
+// thread t owns elements 2t and 2t+1. Fixed association. `tot` holds 4 floats.
+__device__ __forceinline__ void cta128_inclusive_scan(float *buf, int n, float *tot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e0 = 2 * tid, e1 = e0 + 1;
+    const float v0 = e0 < n ? buf[e0] : 0.f, v1 = e1 < n ? buf[e1] : 0.f;
+    const float s = v0 + v1;
+    float incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) tot[warp] = incl;
+    __syncthreads();
+    float base = 0.f;
+    for (int w = 0; w < warp; ++w) base += tot[w];
+    const float excl = base + incl - s;
+    if (e0 < n) buf[e0] = excl + v0;
+    if (e1 < n) buf[e1] = excl + v0 + v1;
+    __syncthreads();
+}
+
+__device__ __forceinline__ void record_failure(int *status) { atomicCAS(status, SSD_OK, SSD_ERR_TIMEOUT); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// --------------------------------------------------------- chunk state
+
+__global__ void __launch_bounds__(128) chunk_state_tc(const __grid_constant__ TcParams prm) {
+    const ChunkedArgs &a = prm.a;
+    const int c = blockIdx.x, h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int Q = a.Q, R = Q < kRows ? Q : kRows;
+    const int g = (int)(h / (a.H / a.G));
+    const int64_t t0 = (int64_t)c * Q;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sB = smem;                    // B^T operand: 2 panels (n 0-63, 64-127) x Q rows x 128 B
+    uint8_t *sX = smem + Q * 256;          // x operand: Q rows x 128 B, scaled by w_j in place
+    float *s_dt = reinterpret_cast<float *>(sX + Q * 128);
+    float *s_cs = s_dt + 256;
+    float *s_w = s_cs + 256;
+    float *s_tot = s_w + 256;
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_tot + 8);
+    uint64_t *bar_mma = bar_ld + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
+    int *s_fail = reinterpret_cast<int *>(tmem_slot + 1);
+
+    if (tid == 0) {
+        tc::mbar_init(bar_ld, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::fence_mbar_init();
+        *s_fail = 0;
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, 64);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar_ld, (uint32_t)Q * 384u);
+        for (int half = 0; half < 2; ++half)
+            for (int r0 = 0; r0 < Q; r0 += R)
+                tc::tma_load_3d(sB + half * Q * 128 + r0 * 128, &prm.mb, bar_ld, g * kN + half * 64,
+                                (int)(t0 + r0), (int)b);
+        for (int r0 = 0; r0 < Q; r0 += R)
+            tc::tma_load_3d(sX + r0 * 128, &prm.mx, bar_ld, h * kP, (int)(t0 + r0), (int)b);
+    }
+
+    // in-chunk cumulative sum of dt*A while the tiles land
+    const __nv_bfloat16 *dt = static_cast<const __nv_bfloat16 *>(a.dt);
+    const float Ah = a.A[h];
+    for (int j = tid; j < Q; j += 128) {
+        const float d = (t0 + j < a.L) ? __bfloat162float(dt[(b * a.L + t0 + j) * a.H + h]) : 0.f;
+        s_dt[j] = d;
+        s_cs[j] = d * Ah;
+    }
+    __syncthreads();
+    cta128_inclusive_scan(s_cs, Q, s_tot);
+    const float cs_end = s_cs[Q - 1];
+    for (int j = tid; j < Q; j += 128) s_w[j] = __expf(cs_end - s_cs[j]) * s_dt[j];
+    if (tid == 0) a.chunk_sum[(b * a.H + h) * a.nc + c] = cs_end;
+
+    if (!tc::mbar_wait(bar_ld, 0, kWaitNs)) *s_fail = 1;
+    __syncthreads();
+    if (*s_fail) {
+        if (tid == 0) record_failure(a.status);
+    } else {
+        // x_j <- w_j x_j in place: a 128-byte row holds all 64 p of token j
+        for (int e = tid; e < Q * 8; e += 128) {
+            const int row = e >> 3;
+            uint4 *ptr = reinterpret_cast<uint4 *>(sX + row * 128 + (e & 7) * 16);
+            uint4 v = *ptr;
+            const float w = s_w[row];
+            uint32_t *u = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 p2 = *reinterpret_cast<__nv_bfloat162 *>(&u[k]);
+                const float2 f = __bfloat1622float2(p2);
+                u[k] = pack_bf16x2(f.x * w, f.y * w);
+            }
+            *ptr = v;
+        }
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc::tc_fence_after();
+            const uint32_t idesc = tc::idesc_bf16(128, kP, true, true);
+            const uint32_t b0 = tc::smem_u32(sB), x0 = tc::smem_u32(sX);
+            for (int k = 0; k < Q; k += 16) {
+                const uint64_t da = tc::sdesc_sw128(b0 + k * 128, Q * 128, 1024);
+                const uint64_t db = tc::sdesc_sw128(x0 + k * 128, Q * 128, 1024);
+                tc::mma_bf16(tmem, da, db, idesc, k > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(bar_mma, 0, kWaitNs)) *s_fail = 1;
+        __syncthreads();
+        if (*s_fail) {
+            if (tid == 0) record_failure(a.status);
+        } else {
+            tc::tc_fence_after();
+            // lane 32*warp + l of TMEM holds n = 32*warp + l; columns are p
+            float v[32];
+            const int n = warp * 32 + lane;
+            float *S = a.states + (((b * a.nc + c) * a.H + h) * kP) * kN;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + half * 32, v);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) S[(half * 32 + q) * kN + n] = v[q];
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 64);
+    // let the state pass start its launch while this grid drains
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------- chunk scan
+
+__global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcParams prm) {
+    const ChunkedArgs &a = prm.a;
+    const int tile = blockIdx.x, h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int Q = a.Q;
+    const int g = (int)(h / (a.H / a.G));
+    const int64_t t0 = (int64_t)tile * kRows;
+    // K-range: from the start of the tile's chunk (Q >= 128) or the tile itself
+    const int64_t ks = Q > kRows ? (t0 / Q) * Q : t0;
+    const int nk = (int)((t0 - ks) / kRows) + 1;  // K-blocks of 128 tokens
+    const int kl = nk * kRows;
+    const int roff = (int)(t0 - ks);              // K-range index of tile row 0
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i = tid;                            // tile row = TMEM lane
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sC = smem;                   // C tile, K-major: 2 panels x 128 rows x 128 B (later: y staging)
+    uint8_t *sB = smem + 32768;           // B block, K-major: 2 panels x 128 rows (later: S', then h_in)
+    uint8_t *sX = smem + 65536;           // x block, MN-major: 128 rows x 128 B
+    float *s_dt = reinterpret_cast<float *>(smem + 81920);
+    float *s_cs = s_dt + 256;
+    float *s_colf = s_cs + 256;  // exp(cs_r - cs_j) dt_j, r = last column of j's 32-block
+    float *s_tot = s_colf + 256;
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_tot + 8);
+    uint64_t *bar_mma = bar_ld + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
+    int *s_fail = reinterpret_cast<int *>(tmem_slot + 1);
+
+    if (tid == 0) {
+        tc::mbar_init(bar_ld, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::fence_mbar_init();
+        *s_fail = 0;
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, 256);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
+    uint32_t ph_ld = 0, ph_mma = 0;
+
+    auto load_block = [&](int kb) {  // B and x rows of K-block kb
+        const int64_t r = ks + (int64_t)kb * kRows;
+        tc::mbar_arrive_expect_tx(bar_ld, kb == 0 ? 32768u + 32768u + 16384u : 32768u + 16384u);
+        if (kb == 0) {
+            tc::tma_load_3d(sC, &prm.mc, bar_ld, g * kN, (int)t0, (int)b);
+            tc::tma_load_3d(sC + 16384, &prm.mc, bar_ld, g * kN + 64, (int)t0, (int)b);
+        }
+        tc::tma_load_3d(sB, &prm.mb, bar_ld, g * kN, (int)r, (int)b);
+        tc::tma_load_3d(sB + 16384, &prm.mb, bar_ld, g * kN + 64, (int)r, (int)b);
+        tc::tma_load_3d(sX, &prm.mx, bar_ld, h * kP, (int)r, (int)b);
+    };
+    if (tid == 0) load_block(0);
+
+    // cumulative sum of dt*A over the K-range
+    const __nv_bfloat16 *dt = static_cast<const __nv_bfloat16 *>(a.dt);
+    const float Ah = a.A[h];
+    for (int j = tid; j < kl; j += 128) {
+        const float d = (ks + j < a.L) ? __bfloat162float(dt[(b * a.L + ks + j) * a.H + h]) : 0.f;
+        s_dt[j] = d;
+        s_cs[j] = d * Ah;
+    }
+    __syncthreads();
+    cta128_inclusive_scan(s_cs, kl, s_tot);
+    for (int j = tid; j < kl; j += 128) s_colf[j] = __expf(s_cs[j | 31] - s_cs[j]) * s_dt[j];
+    __syncthreads();
+
+    const int ir = roff + i;  // K-range index of this thread's row
+    const float cs_i = s_cs[ir];
+    const uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
+    const uint32_t idesc_y = tc::idesc_bf16(128, kP, false, true);
+    const uint32_t idesc_o = tc::idesc_bf16(128, kP, false, false);
+    const uint32_t c0 = tc::smem_u32(sC), b0 = tc::smem_u32(sB), x0 = tc::smem_u32(sX);
+    bool ok = true;
+
+    for (int kb = 0; kb < nk && ok; ++kb) {
+        if (!tc::mbar_wait(bar_ld, ph_ld, kWaitNs)) *s_fail = 1;
+        ph_ld ^= 1;
+        __syncthreads();
+        if (*s_fail) { ok = false; break; }
+        // S = C B_kb^T into TMEM columns [0, 128)
+        if (tid == 0) {
+            tc::tc_fence_after();
+            for (int k = 0; k < kN; k += 16) {
+                const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                const uint64_t db = tc::sdesc_sw128(b0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                tc::mma_bf16(tmem, da, db, idesc_s, k > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(bar_mma, ph_mma, kWaitNs)) *s_fail = 1;
+        ph_mma ^= 1;
+        __syncthreads();
+        if (*s_fail) { ok = false; break; }
+        tc::tc_fence_after();
+        // S' = S o decay o dt_j under the causal same-chunk mask, bf16, K-major,
+        // into the B block's space (B is no longer needed). Columns come in
+        // 32-wide blocks J of the K-range; this warp's rows all lie in block
+        // Jd. Blocks after Jd are zero; blocks before it use the factorised
+        // decay exp(cs_i - cs_r) exp(cs_r - cs_j) with r the last column of
+        // the block (both factors <= 1 for a decaying head); block Jd takes
+        // exp(cs_i - cs_j) directly.
+        const int Jd = (roff >> 5) + warp;
+        for (int cc = 0; cc < 4; ++cc) {
+            const int J = kb * 4 + cc;
+            float v[32];
+            if (J <= Jd) {
+                tc::tmem_ld32(tl + cc * 32, v);
+                tc::tmem_ld_wait();
+                if (J < Jd) {
+                    const bool same = Q >= kRows || (J >> 1) == (Jd >> 1);
+                    const float rf = same ? __expf(cs_i - s_cs[J * 32 + 31]) : 0.f;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * s_colf[J * 32 + q];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int jr = J * 32 + q;
+                        v[q] = jr <= ir ? v[q] * __expf(cs_i - s_cs[jr]) * s_dt[jr] : 0.f;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+                const uint4 pk = make_uint4(pack_bf16x2(v[q], v[q + 1]), pack_bf16x2(v[q + 2], v[q + 3]),
+                                            pack_bf16x2(v[q + 4], v[q + 5]), pack_bf16x2(v[q + 6], v[q + 7]));
+                *reinterpret_cast<uint4 *>(sB + tc::sw128_offset(i, cc * 32 + q, kRows)) = pk;
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+        // Y (+)= S' X_kb into TMEM columns [128, 192)
+        if (tid == 0) {
+            tc::tc_fence_after();
+            for (int k = 0; k < kRows; k += 16) {
+                const uint64_t da = tc::sdesc_sw128(b0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                const uint64_t db = tc::sdesc_sw128(x0 + k * 128, 16384, 1024);
+                tc::mma_bf16(tmem + 128, da, db, idesc_y, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(bar_mma, ph_mma, kWaitNs)) *s_fail = 1;
+        ph_mma ^= 1;
+        __syncthreads();
+        if (*s_fail) { ok = false; break; }
+        if (kb + 1 < nk && tid == 0) load_block(kb + 1);
+    }
+
+    // entering states of the tile's chunk(s): written by the state pass
+    const int nsub = Q < kRows ? kRows / Q : 1;  // chunks in this tile (2 for Q = 64)
+    if (ok) {
+        if (tid == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            tc::mbar_arrive_expect_tx(bar_ld, (uint32_t)nsub * 16384u);
+            for (int s = 0; s < nsub; ++s) {
+                const int64_t cidx = (t0 + (int64_t)s * Q) / Q;
+                const int row0 = (int)(((b * a.nc + cidx) * a.H + h) * kP);
+                tc::tma_load_2d(sB + s * 16384, &prm.mh, bar_ld, 0, row0);
+                tc::tma_load_2d(sB + s * 16384 + 8192, &prm.mh, bar_ld, 64, row0);
+            }
+        }
+        if (!tc::mbar_wait(bar_ld, ph_ld, kWaitNs)) *s_fail = 1;
+        ph_ld ^= 1;
+        __syncthreads();
+        ok = !*s_fail;
+    }
+    if (ok) {
+        // Yo_s = C h_in(s)^T into TMEM columns [64 s, 64 s + 64)
+        if (tid == 0) {
+            tc::tc_fence_after();
+            for (int s = 0; s < nsub; ++s) {
+                const uint32_t h0 = b0 + s * 16384;
+                for (int k = 0; k < kN; k += 16) {
+                    const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                    const uint64_t db = tc::sdesc_sw128(h0 + (k >> 6) * 8192 + (k & 63) * 2, 16, 1024);
+                    tc::mma_bf16(tmem + s * 64, da, db, idesc_o, k > 0 ? 1u : 0u);
+                }
+            }
+            tc::mma_commit(bar_mma);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(bar_mma, ph_mma, kWaitNs)) *s_fail = 1;
+        ph_mma ^= 1;
+        __syncthreads();
+        ok = !*s_fail;
+    }
+    if (ok) {
+        tc::tc_fence_after();
+        // epilogue: y = Y + exp(cs_i - cs at the chunk start) Yo + D x
+        const int sub = Q < kRows ? (i / Q) : 0;  // warp-uniform (Q = 64: warps 0-1 / 2-3)
+        const float base = sub > 0 ? s_cs[roff + sub * Q - 1] : 0.f;
+        const float sc = __expf(cs_i - base);
+        const float Dh = a.D ? a.D[h] : 0.f;
+        for (int half = 0; half < 2; ++half) {
+            float yv[32], ov[32];
+            tc::tmem_ld32(tl + 128 + half * 32, yv);
+            tc::tmem_ld32(tl + sub * 64 + half * 32, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+                const int p0 = half * 32 + q;
+                const uint4 xr = *reinterpret_cast<const uint4 *>(sX + tc::sw128_offset(i, p0, kRows));
+                const uint32_t *xu = reinterpret_cast<const uint32_t *>(&xr);
+                uint32_t pk[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[m]));
+                    const float y0 = yv[q + 2 * m] + sc * ov[q + 2 * m] + Dh * xf.x;
+                    const float y1 = yv[q + 2 * m + 1] + sc * ov[q + 2 * m + 1] + Dh * xf.y;
+                    pk[m] = pack_bf16x2(y0, y1);
+                }
+                *reinterpret_cast<uint4 *>(sC + tc::sw128_offset(i, p0, kRows)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc::tma_store_3d(&prm.my, sC, h * kP, (int)t0, (int)b);
+            tc::bulk_commit();
+            tc::bulk_wait_all();
+        }
+    } else if (tid == 0) {
+        record_failure(a.status);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+    (void)lane;
+}
+
+// ------------------------------------------- persistent chunk scan (Q <= 128)
+//
+// One CTA per SM walks work items (b, 128-token tile, group of hb heads).
+// The heads of a group share the C and B tiles and S = C B^T; per head it
+// needs x, the entering state(s) and its own decay mask. Warp roles:
+//   warp 0       TMA producer of C, B (per item) and x (per head)
+//   warp 10      TMA producer of the entering states (waits for the state pass)
+//   warp 1       MMA issuer (one lane): S = C B^T; Yo = C h_in^T; Y = S' X
+//   warps 2..9   epilogue, two groups of four warps (one warp per TMEM lane
+//                quarter in each group). Per item: the cumulative sums of all
+//                its heads (the only cross-warp barriers). Per head: S' = S o
+//                decay (+ D on the diagonal, so that Y carries D x) into one
+//                of two S' buffers, group 0 the column blocks {0, 3}, group 1
+//                {1, 2} (balanced over the causal triangle); y = Y + scale Yo,
+//                group g the columns p in [32 g, 32 g + 32), each warp storing
+//                its 32 x 32 block with its own TMA store.
+// dt, A and D of the next item are loaded one item ahead. Rings between the
+// roles are guarded by mbarriers; S' and the accumulators are double-buffered
+// so the MMAs of head k+1 overlap the epilogue of head k. All waits are
+// bounded: a timeout raises a CTA-wide flag, every role then runs to the end
+// of its loop without waiting and the status word records SSD_ERR_TIMEOUT.
+
+constexpr int kHBMax = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kScanPThreads = 352;  // 11 warps
+constexpr int kEpiThreads = 256;
+
+__device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *fail) {
+    const uint32_t addr = tc::smem_u32(bar);
+    if (tc::mbar_try_wait(addr, parity)) return true;
+    if (*fail) return false;
+    const uint64_t t0 = tc::global_ns();
+    for (;;) {
+        if (tc::mbar_try_wait(addr, parity)) return true;
+        if (*fail) return false;
+        if (tc::global_ns() - t0 > kWaitNs) {
+            *fail = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+template <int I> __device__ __forceinline__ float pick4(const float (&v)[kHBMax], int k) {
+    return k == 0 ? v[0] : k == 1 ? v[1] : k == 2 ? v[2] : v[3];
+}
+
+__global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(const __grid_constant__ TcParams prm) {
+    const ChunkedArgs &a = prm.a;
+    const int Q = a.Q;               // 64 or 128
+    const int nsub = kRows / Q;      // chunks per tile
+    const int HB = prm.hb, nhg = prm.nhg;
+    const int64_t ntiles = (a.L + kRows - 1) / kRows;
+    const int64_t n_items = prm.n_items;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t HS = (uint32_t)nsub * 16384u;  // bytes of one entering-state stage
+    const uint32_t NHS = nsub == 1 ? 2u : 1u;      // entering-state stages (32 KB either way)
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sC = smem;                  // C tile, K-major, 2 panels
+    uint8_t *sB = smem + 32768;          // B tile, K-major, 2 panels
+    uint8_t *sX = smem + 65536;          // x ring: 2 x 16 KB, MN-major
+    uint8_t *sH = smem + 98304;          // entering-state ring: NHS x HS = 32 KB, K-major
+    uint8_t *sP = sH + 32768;            // S' (bf16, K-major): 2 x 32 KB
+    uint8_t *sY = sP + 65536;            // y staging: 8 warps x 2 KB (32 x 32 bf16, 64-byte swizzle)
+    float *s_cs = reinterpret_cast<float *>(sY + 16384);  // [kHBMax][128]
+    float *s_dt = s_cs + kHBMax * 128;                    // [kHBMax][128]
+    float *s_colf = s_dt + kHBMax * 128;                  // [kHBMax][128]
+    float *s_tot = s_colf + kHBMax * 128;                 // [kHBMax][4]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_tot + kHBMax * 4);
+    uint64_t *tile_full = bars + 0, *tile_empty = bars + 1;
+    uint64_t *x_full = bars + 2, *x_empty = bars + 4;      // [2] each
+    uint64_t *h_full = bars + 6, *h_empty = bars + 8;      // [2] each
+    uint64_t *s_full = bars + 10, *s_empty = bars + 11;
+    uint64_t *p_full = bars + 12, *p_empty = bars + 14;    // [2] each
+    uint64_t *acc_full = bars + 16, *acc_empty = bars + 18;  // [2] each
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+    volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    if (tid == 0) {
+        for (int k = 0; k < 20; ++k) tc::mbar_init(bars + k, 1);
+        tc::mbar_init(s_empty, kEpiThreads);
+        tc::mbar_init(p_full + 0, kEpiThreads);
+        tc::mbar_init(p_full + 1, kEpiThreads);
+        tc::mbar_init(acc_empty + 0, kEpiThreads);
+        tc::mbar_init(acc_empty + 1, kEpiThreads);
+        tc::fence_mbar_init();
+        *s_fail = 0;
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int hpg = (int)(a.H / a.G);  // heads per B/C group
+
+    auto decode = [&](int64_t u, int64_t &b, int64_t &tile, int &hg) {
+        hg = (int)(u % nhg);
+        const int64_t t = u / nhg;
+        tile = t % ntiles;
+        b = t / ntiles;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t tcnt = 0, xi = 0, xph = 0;
+            for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
+                int64_t b, tile;
+                int hg;
+                decode(u, b, tile, hg);
+                const int t0 = (int)(tile * kRows);
+                const int g = hg * HB / hpg;
+                if (!pwait(tile_empty, (tcnt & 1) ^ 1, s_fail)) break;
+                ++tcnt;
+                tc::mbar_arrive_expect_tx(tile_full, 65536u);
+                tc::tma_load_3d(sC, &prm.mc, tile_full, g * kN, t0, (int)b);
+                tc::tma_load_3d(sC + 16384, &prm.mc, tile_full, g * kN + 64, t0, (int)b);
+                tc::tma_load_3d(sB, &prm.mb, tile_full, g * kN, t0, (int)b);
+                tc::tma_load_3d(sB + 16384, &prm.mb, tile_full, g * kN + 64, t0, (int)b);
+                for (int k = 0; k < HB; ++k) {
+                    if (!pwait(&x_empty[xi], xph ^ 1, s_fail)) break;
+                    tc::mbar_arrive_expect_tx(&x_full[xi], 16384u);
+                    tc::tma_load_3d(sX + xi * 16384, &prm.mx, &x_full[xi], (hg * HB + k) * kP, t0, (int)b);
+                    if (++xi == 2) { xi = 0; xph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 10) {
+        // ------------------------------ TMA producer of entering states
+        if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            uint32_t hi = 0, hph = 0;
+            for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
+                int64_t b, tile;
+                int hg;
+                decode(u, b, tile, hg);
+                const int64_t t0 = tile * kRows;
+                for (int k = 0; k < HB; ++k) {
+                    if (!pwait(&h_empty[hi], hph ^ 1, s_fail)) break;
+                    tc::mbar_arrive_expect_tx(&h_full[hi], HS);
+                    for (int sb = 0; sb < nsub; ++sb) {
+                        const int64_t cidx = (t0 + (int64_t)sb * Q) / Q;
+                        const int row0 = (int)(((b * a.nc + cidx) * a.H + hg * HB + k) * kP);
+                        tc::tma_load_2d(sH + hi * HS + sb * 16384, &prm.mh, &h_full[hi], 0, row0);
+                        tc::tma_load_2d(sH + hi * HS + sb * 16384 + 8192, &prm.mh, &h_full[hi], 64, row0);
+                    }
+                    if (++hi == NHS) { hi = 0; hph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
+            const uint32_t idY = tc::idesc_bf16(128, kP, false, true);
+            const uint32_t idO = tc::idesc_bf16(128, kP, false, false);
+            const uint32_t c0 = tc::smem_u32(sC), b0 = tc::smem_u32(sB);
+            uint32_t tph = 0, sph = 0, xi = 0, xph = 0, hi = 0, hph = 0, ai = 0, aph = 0, nh = 0;
+            for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
+                if (!pwait(tile_full, tph, s_fail)) break;
+                tph ^= 1;
+                if (!pwait(s_empty, sph ^ 1, s_fail)) break;
+                sph ^= 1;
+                tc::tc_fence_after();
+                for (int k = 0; k < kN; k += 16) {
+                    const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                    const uint64_t db = tc::sdesc_sw128(b0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                    tc::mma_bf16(tmem, da, db, idS, k > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(s_full);
+                for (int kh = 0; kh < HB; ++kh, ++nh) {
+                    const uint32_t acc = tmem + 128 + ai * 192;
+                    const uint32_t pb = nh & 1, pph = (nh >> 1) & 1;
+                    if (!pwait(&acc_empty[ai], aph ^ 1, s_fail)) break;
+                    // Yo = C h_in^T first: its operands are ready long before S'
+                    if (!pwait(&h_full[hi], hph, s_fail)) break;
+                    tc::tc_fence_after();
+                    const uint32_t h0 = tc::smem_u32(sH + hi * HS);
+                    for (int sb = 0; sb < nsub; ++sb)
+                        for (int k = 0; k < kN; k += 16) {
+                            const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                            const uint64_t db =
+                                tc::sdesc_sw128(h0 + sb * 16384 + (k >> 6) * 8192 + (k & 63) * 2, 16, 1024);
+                            tc::mma_bf16(acc + 64 + 64 * sb, da, db, idO, k > 0 ? 1u : 0u);
+                        }
+                    tc::mma_commit(&h_empty[hi]);
+                    if (++hi == NHS) { hi = 0; hph ^= 1; }
+                    if (!pwait(&x_full[xi], xph, s_fail)) break;
+                    if (!pwait(&p_full[pb], pph, s_fail)) break;
+                    tc::tc_fence_after();
+                    const uint32_t x0 = tc::smem_u32(sX + xi * 16384);
+                    const uint32_t p0 = tc::smem_u32(sP + pb * 32768);
+                    for (int k = 0; k < kRows; k += 16) {
+                        const uint64_t da = tc::sdesc_sw128(p0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                        const uint64_t db = tc::sdesc_sw128(x0 + k * 128, 16384, 1024);
+                        tc::mma_bf16(acc, da, db, idY, k > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&p_empty[pb]);
+                    tc::mma_commit(&x_empty[xi]);
+                    if (++xi == 2) { xi = 0; xph ^= 1; }
+                    tc::mma_commit(&acc_full[ai]);
+                    if (++ai == 2) { ai = 0; aph ^= 1; }
+                }
+                tc::mma_commit(tile_empty);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int ew = warp - 2;            // 0 .. 7
+        const int grp = ew >> 2;            // column group
+        const int qd = warp & 3;            // TMEM lane quarter of this warp
+        const int i = qd * 32 + lane;       // tile row
+        const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16);
+        const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
+        const int Ja = grp == 0 ? 0 : 1, Jb = grp == 0 ? 3 : 2;  // this group's column blocks of S'
+        const int sub = (Q < kRows && i >= Q) ? 1 : 0;           // chunk of this row inside the tile
+        uint8_t *stg = sY + ew * 2048;                           // this warp's y staging
+        uint32_t sph = 0, ai = 0, aph = 0, nh = 0;
+
+        // per-item scalars of this thread's row, loaded one item ahead
+        float dtv[kHBMax], Av[kHBMax], Dv[kHBMax];
+        auto fetch = [&](int64_t u) {
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k) { dtv[k] = 0.f; Av[k] = 0.f; Dv[k] = 0.f; }
+            if (u >= n_items) return;
+            int64_t b, tile;
+            int hg;
+            decode(u, b, tile, hg);
+            const int64_t t0 = tile * kRows;
+            const bool row_in = t0 + i < a.L;
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k) {
+                if (k < HB) {
+                    const int h = hg * HB + k;
+                    dtv[k] = row_in ? __bfloat162float(dtp[(b * a.L + t0 + i) * a.H + h]) : 0.f;
+                    Av[k] = a.A[h];
+                    Dv[k] = a.D ? a.D[h] : 0.f;
+                }
+            }
+        };
+        fetch(blockIdx.x);
+        for (int64_t u = blockIdx.x; u < n_items; u += gridDim.x) {
+            int64_t b, tile;
+            int hg;
+            decode(u, b, tile, hg);
+            const int64_t t0 = tile * kRows;
+            float dcur[kHBMax], Acur[kHBMax], Dcur[kHBMax];
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k) { dcur[k] = dtv[k]; Acur[k] = Av[k]; Dcur[k] = Dv[k]; }
+            fetch(u + gridDim.x);  // next item's scalars, consumed one item later
+
+            // cumulative sums of every head of the item (the item's only barriers)
+            float csv[kHBMax], scv[kHBMax], incl[kHBMax], wtot[kHBMax];
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k) {
+                float v = dcur[k] * (Acur[k] * kLog2e);  // cumulative sums in base-2 units
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float w = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += w;
+                }
+                incl[k] = v;
+                wtot[k] = __shfl_sync(0xffffffffu, v, 31);
+                if (grp == 0 && lane == 31) s_tot[k * 4 + qd] = v;
+            }
+            epi_sync();
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k) {
+                float base = 0.f;
+                for (int w = 0; w < qd; ++w) base += s_tot[k * 4 + w];
+                csv[k] = base + incl[k];
+                const float bse = sub ? s_tot[k * 4 + 0] + s_tot[k * 4 + 1] : 0.f;  // end of the first 64-token chunk
+                scv[k] = tc::ex2(csv[k] - bse);
+                if (grp == 0 && k < HB) {
+                    s_cs[k * 128 + i] = csv[k];
+                    s_dt[k * 128 + i] = dcur[k];
+                    s_colf[k * 128 + i] = tc::ex2(base + wtot[k] - csv[k]) * dcur[k];  // decay from i to i|31, times dt_i
+                }
+            }
+            epi_sync();
+            pwait(s_full, sph, s_fail);
+            sph ^= 1;
+            tc::tc_fence_after();
+
+            // S' of head k (this group's column blocks) into S' buffer n & 1.
+            // Branch-free per element: the exponent is clamped to <= 0 so every
+            // lane computes it, and the causal mask is a select.
+            auto sprime = [&](int k, uint32_t n) {
+                const float cs_i = pick4<0>(csv, k), Dh = pick4<0>(Dcur, k);
+                const float *cs_ = s_cs + k * 128, *dt_ = s_dt + k * 128, *cf_ = s_colf + k * 128;
+                uint8_t *sp = sP + (n & 1) * 32768;
+                pwait(&p_empty[n & 1], ((n >> 1) & 1) ^ 1, s_fail);
+                const int Jd = qd;
+#pragma unroll 1
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int J = jj == 0 ? Ja : Jb;
+                    float v[32];
+                    if (J < Jd) {
+                        // block before this warp's rows: factorised decay
+                        tc::tmem_ld32(tq + J * 32, v);
+                        tc::tmem_ld_wait();
+                        const bool same = Q >= kRows || (J >> 1) == (Jd >> 1);
+                        const float rf = same ? tc::ex2(cs_i - cs_[J * 32 + 31]) : 0.f;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * cf_[J * 32 + q];
+                    } else if (J == Jd) {
+                        // block holding this warp's rows: exact decay, causal mask, D on the diagonal
+                        tc::tmem_ld32(tq + J * 32, v);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const int jr = J * 32 + q;
+                            const float e = tc::ex2(fminf(cs_i - cs_[jr], 0.f)) * dt_[jr];
+                            float f = jr <= i ? v[q] * e : 0.f;
+                            f += jr == i ? Dh : 0.f;
+                            v[q] = f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[q] = 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) {
+                        const uint4 pk = make_uint4(pack_bf16x2(v[q], v[q + 1]), pack_bf16x2(v[q + 2], v[q + 3]),
+                                                    pack_bf16x2(v[q + 4], v[q + 5]), pack_bf16x2(v[q + 6], v[q + 7]));
+                        *reinterpret_cast<uint4 *>(sp + tc::sw128_offset(i, J * 32 + q, kRows)) = pk;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                if (k == HB - 1) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(s_empty);  // S fully read for this item
+                }
+                tc::mbar_arrive(&p_full[n & 1]);
+            };
+            // y of head k: this warp's 32 rows x the 32 columns p in [32 grp, 32 grp + 32)
+            auto yout = [&](int k) {
+                pwait(&acc_full[ai], aph, s_fail);
+                tc::tc_fence_after();
+                const uint32_t acc = tq + 128 + ai * 192;
+                const float sc = pick4<0>(scv, k);
+                float yv[32], ov[32];
+                tc::tmem_ld32(acc + 32 * grp, yv);
+                tc::tmem_ld32(acc + 64 + 64 * sub + 32 * grp, ov);
+                tc::tmem_ld_wait();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&acc_empty[ai]);
+                if (++ai == 2) { ai = 0; aph ^= 1; }
+                if (lane == 0) tc::bulk_wait_read_all();  // this warp's previous store has read the staging
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int q = c * 8;
+                    uint4 pk;
+                    pk.x = pack_bf16x2(fmaf(sc, ov[q], yv[q]), fmaf(sc, ov[q + 1], yv[q + 1]));
+                    pk.y = pack_bf16x2(fmaf(sc, ov[q + 2], yv[q + 2]), fmaf(sc, ov[q + 3], yv[q + 3]));
+                    pk.z = pack_bf16x2(fmaf(sc, ov[q + 4], yv[q + 4]), fmaf(sc, ov[q + 5], yv[q + 5]));
+                    pk.w = pack_bf16x2(fmaf(sc, ov[q + 6], yv[q + 6]), fmaf(sc, ov[q + 7], yv[q + 7]));
+                    // 64-byte rows, 16-byte chunk index XOR (row / 2) % 4 (64-byte swizzle)
+                    *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_3d(&prm.my32, stg, (hg * HB + k) * kP + 32 * grp, (int)t0 + 32 * qd, (int)b);
+                    tc::bulk_commit();
+                }
+            };
+            // S'(k) runs one head ahead of y(k - 1); one call site each
+#pragma unroll 1
+            for (int k = 0; k <= HB; ++k) {
+                if (k < HB) sprime(k, nh + k);
+                if (k >= 1) yout(k - 1);
+            }
+            nh += HB;
+        }
+        if (lane == 0) tc::bulk_wait_all();
+        tc::tc_fence_before();
+    }
+    __syncthreads();
+    if (tid == 0 && *s_fail) record_failure(a.status);
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
 
 // A shared-memory barrier that nothing ever completes, waited on with a poll
 // budget: the wait must give up, record SSD_ERR_TIMEOUT and let the kernel exit.
@@ -20,9 +856,143 @@ __global__ void selftest_wait_kernel(int *status, int spin_limit) {
     if (threadIdx.x == 0) {
         const uint32_t addr = tc::smem_u32(&bar);
         bool done = false;
-        for (int i = 0; i < spin_limit && !done; ++i) done = tc::mbar_try_wait(addr, 0);
+        for (int k = 0; k < spin_limit && !done; ++k) done = tc::mbar_try_wait(addr, 0);
         if (!done) atomicCAS(status, SSD_OK, SSD_ERR_TIMEOUT);
     }
+}
+
+// ------------------------------------------------------- host helpers
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor map with the 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1.
+struct MapKey {
+    const void *base;
+    int rank;
+    int swz64;  // 64-byte swizzle instead of 128-byte
+    uint64_t dims[3], strides[2];
+    uint32_t box[3];
+    bool operator==(const MapKey &o) const {
+        if (base != o.base || rank != o.rank || swz64 != o.swz64) return false;
+        for (int k = 0; k < rank; ++k)
+            if (dims[k] != o.dims[k] || box[k] != o.box[k]) return false;
+        for (int k = 0; k + 1 < rank; ++k)
+            if (strides[k] != o.strides[k]) return false;
+        return true;
+    }
+};
+
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapKey g_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_next = 0, g_map_count = 0;
+
+bool make_map(CUtensorMap *out, const MapKey &k) {
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (int e = 0; e < g_map_count; ++e)
+            if (g_keys[e] == k) {
+                *out = g_maps[e];
+                return true;
+            }
+    }
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    for (int e = 0; e < k.rank; ++e) {
+        dims[e] = k.dims[e];
+        box[e] = k.box[e];
+    }
+    for (int e = 0; e + 1 < k.rank; ++e) strides[e] = k.strides[e];
+    CUtensorMap m;
+    CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)k.rank, const_cast<void *>(k.base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     k.swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    g_keys[g_map_next] = k;
+    g_maps[g_map_next] = m;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    if (g_map_count < kMapCache) ++g_map_count;
+    *out = m;
+    return true;
+}
+
+// (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (box_cols, box_rows, 1);
+// 128-byte swizzle for 64-column boxes, 64-byte swizzle for 32-column boxes
+bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
+                int box_cols = 64) {
+    MapKey k{};
+    k.swz64 = box_cols == 32;
+    k.base = base;
+    k.rank = 3;
+    k.dims[0] = (uint64_t)inner;
+    k.dims[1] = (uint64_t)L;
+    k.dims[2] = (uint64_t)B;
+    k.strides[0] = (uint64_t)inner * 2;
+    k.strides[1] = (uint64_t)inner * L * 2;
+    k.box[0] = (uint32_t)box_cols;
+    k.box[1] = (uint32_t)box_rows;
+    k.box[2] = 1;
+    return make_map(out, k);
+}
+
+int device_cc_major() {
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
+    return major;
+}
+
+size_t state_smem(int Q) { return (size_t)Q * 384 + 4096 + 1024; }
+constexpr size_t kScanSmem = 81920 + 5120 + 1024;
+
+size_t scanp_smem(int) { return 98304 + 32768 + 65536 + 16384 + 7168 + 1024; }
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            n = 1;
+    }
+    return n;
+}
+
+cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream_t stream, bool pdl,
+                      const TcParams &p, int threads = 128) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
@@ -34,8 +1004,84 @@ cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t strea
     return cudaGetLastError();
 }
 
-bool chunked_tc_supported(const ChunkedArgs &) { return false; }
+bool chunked_tc_supported(const ChunkedArgs &a) {
+    if (a.io != IO_BF16 || a.P != kP || a.N != kN) return false;
+    if (!(a.Q == 64 || a.Q == 128 || a.Q == 256)) return false;
+    if (a.L <= 0 || a.L > 0x7fffffffLL || a.B > 0x7fffffffLL) return false;
+    if (a.B * a.nc * a.H * a.P > 0x7fffffffLL) return false;
+    if (((a.H * a.P * 2) % 16) != 0 || ((a.G * a.N * 2) % 16) != 0) return false;
+    static int major = device_cc_major();
+    return major == 10;
+}
 
-cudaError_t launch_chunked_tc(const ChunkedArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    p.a = a;
+    const int R = a.Q < kRows ? a.Q : kRows;
+    const int64_t ntiles = (a.L + kRows - 1) / kRows;
+    bool ok = true;
+    ok &= map_tokens(&p.mx, a.x, a.H * a.P, a.L, a.B, kRows);
+    ok &= map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kRows);
+    ok &= map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kRows);
+    ok &= map_tokens(&p.my, a.y, a.H * a.P, a.L, a.B, kRows);
+    ok &= map_tokens(&p.my32, a.y, a.H * a.P, a.L, a.B, 32, 32);
+    {
+        MapKey k{};
+        k.base = a.states_bf16;
+        k.rank = 2;
+        k.dims[0] = kN;
+        k.dims[1] = (uint64_t)(a.B * a.nc * a.H * kP);
+        k.strides[0] = kN * 2;
+        k.box[0] = 64;
+        k.box[1] = 64;
+        ok &= make_map(&p.mh, k);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    TcParams ps = p;  // the chunk-state kernel reads Q-row boxes for Q = 64
+    if (R != kRows) {
+        ok &= map_tokens(&ps.mx, a.x, a.H * a.P, a.L, a.B, R);
+        ok &= map_tokens(&ps.mb, a.Bm, a.G * a.N, a.L, a.B, R);
+        if (!ok) return cudaErrorInvalidValue;
+    }
+
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)state_smem(256));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunk_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunk_scan_tc_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)scanp_smem(64));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    // persistent chunk scan for Q <= 128: head groups of hb heads sharing a B/C group
+    const int hpg = (int)(a.H / a.G);
+    p.hb = hpg % 4 == 0 ? 4 : hpg % 2 == 0 ? 2 : 1;
+    p.nhg = (int)(a.H / p.hb);
+    p.n_items = a.B * ntiles * p.nhg;
+    const bool staged = a.stage_ev[0] != nullptr;  // per-stage timing: no programmatic overlap
+    cudaError_t e = mark_stage(a, 0, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_ex(chunk_state_tc, dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), state_smem(a.Q), stream,
+                  false, ps);
+    if (e != cudaSuccess) return e;
+    if ((e = mark_stage(a, 1, stream)) != cudaSuccess) return e;
+    e = launch_state_pass(a, false, true, stream, !staged);
+    if (e != cudaSuccess) return e;
+    if ((e = mark_stage(a, 2, stream)) != cudaSuccess) return e;
+    if (a.Q <= kRows) {
+        const int64_t grid = p.n_items < num_sms() ? p.n_items : num_sms();
+        e = launch_ex(chunk_scan_tc_persistent, dim3((unsigned)grid), scanp_smem(a.Q), stream, !staged, p,
+                      kScanPThreads);
+    } else {
+        e = launch_ex(chunk_scan_tc, dim3((unsigned)ntiles, (unsigned)a.H, (unsigned)a.B), kScanSmem, stream,
+                      !staged, p);
+    }
+    if (e != cudaSuccess) return e;
+    return mark_stage(a, 3, stream);
+}
 
 }  // namespace ssd
