@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 //                of two S' buffers, group 0 the column blocks {0, 3}, group 1
 //                {1, 2} (balanced over the causal triangle); y = Y + scale Yo,
 //                group g the columns p in [32 g, 32 g + 32), each warp storing
-//                its 32 x 32 block with its own TMA store.
+//                its 32 x 32 block with 16-byte stores from registers.
 // dt, A and D of the next item are loaded one item ahead. Rings between the
 // roles are guarded by mbarriers; S' and the accumulators are double-buffered
 // so the MMAs of head k+1 overlap the epilogue of head k. All waits are
@@ -673,7 +673,6 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
         const int Ja = grp == 0 ? 0 : 1, Jb = grp == 0 ? 3 : 2;  // this group's column blocks of S'
         const int sub = (Q < kRows && i >= Q) ? 1 : 0;           // chunk of this row inside the tile
-        uint8_t *stg = sY + ew * 2048;                           // this warp's y staging
         uint32_t sph = 0, ai = 0, aph = 0, nh = 0;
 
         // per-item scalars of this thread's row, loaded one item ahead
@@ -805,24 +804,20 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                 tc::tc_fence_before();
                 tc::mbar_arrive(&acc_empty[ai]);
                 if (++ai == 2) { ai = 0; aph ^= 1; }
-                if (lane == 0) tc::bulk_wait_read_all();  // this warp's previous store has read the staging
-                __syncwarp();
+                // 16-byte stores straight from registers: this row's 32 columns
+                if (t0 + i < a.L) {
+                    __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(a.y) +
+                                          ((b * a.L + t0 + i) * a.H + hg * HB + k) * kP + 32 * grp;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int q = c * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16x2(fmaf(sc, ov[q], yv[q]), fmaf(sc, ov[q + 1], yv[q + 1]));
-                    pk.y = pack_bf16x2(fmaf(sc, ov[q + 2], yv[q + 2]), fmaf(sc, ov[q + 3], yv[q + 3]));
-                    pk.z = pack_bf16x2(fmaf(sc, ov[q + 4], yv[q + 4]), fmaf(sc, ov[q + 5], yv[q + 5]));
-                    pk.w = pack_bf16x2(fmaf(sc, ov[q + 6], yv[q + 6]), fmaf(sc, ov[q + 7], yv[q + 7]));
-                    // 64-byte rows, 16-byte chunk index XOR (row / 2) % 4 (64-byte swizzle)
-                    *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
-                }
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tc::tma_store_3d(&prm.my32, stg, (hg * HB + k) * kP + 32 * grp, (int)t0 + 32 * qd, (int)b);
-                    tc::bulk_commit();
+                    for (int c = 0; c < 4; ++c) {
+                        const int q = c * 8;
+                        uint4 pk;
+                        pk.x = pack_bf16x2(fmaf(sc, ov[q], yv[q]), fmaf(sc, ov[q + 1], yv[q + 1]));
+                        pk.y = pack_bf16x2(fmaf(sc, ov[q + 2], yv[q + 2]), fmaf(sc, ov[q + 3], yv[q + 3]));
+                        pk.z = pack_bf16x2(fmaf(sc, ov[q + 4], yv[q + 4]), fmaf(sc, ov[q + 5], yv[q + 5]));
+                        pk.w = pack_bf16x2(fmaf(sc, ov[q + 6], yv[q + 6]), fmaf(sc, ov[q + 7], yv[q + 7]));
+                        *reinterpret_cast<uint4 *>(yrow + q) = pk;
+                    }
                 }
             };
             // S'(k) runs one head ahead of y(k - 1); one call site each
@@ -833,7 +828,6 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             }
             nh += HB;
         }
-        if (lane == 0) tc::bulk_wait_all();
         tc::tc_fence_before();
     }
     __syncthreads();
