@@ -34,6 +34,27 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+// Packed float32 pairs (sm_100 family f32x2 arithmetic): two lanes of work per
+// FP32-pipe instruction.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool pred) {
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
     const int n = pred ? 16 : 0;  // zero-fill when out of range
@@ -68,14 +89,21 @@ diag_scan_bf16_kernel(int64_t L, int64_t Dm, int N, const __nv_bfloat16 *__restr
     __shared__ __align__(16) __nv_bfloat16 sx[2][kTT][kCh], sdt[2][kTT][kCh];
     __shared__ __align__(16) __nv_bfloat16 sB[2][kTT][NMAX], sC[2][kTT][NMAX];
     __shared__ __align__(16) __nv_bfloat16 sy[kTT][kCh];
+    __shared__ __align__(16) float sBf[kTT][NMAX], sCf[kTT][NMAX];
 
-    float h[NH], A2[NH];
+    uint64_t h2[NH / 2], a2[NH / 2];  // state pairs and decay-rate pairs (base 2)
 #pragma unroll
-    for (int j = 0; j < NH; ++j) {
-        const int n = nb + j;
-        const bool on = valid && n < N;
-        h[j] = (on && init) ? init[(b * Dm + d) * N + n] : 0.f;
-        A2[j] = on ? A[d * N + n] * kLog2e : 0.f;
+    for (int jp = 0; jp < NH / 2; ++jp) {
+        float hv[2], av[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int n = nb + 2 * jp + u;
+            const bool on = valid && n < N;
+            hv[u] = (on && init) ? init[(b * Dm + d) * N + n] : 0.f;
+            av[u] = on ? A[d * N + n] * kLog2e : 0.f;
+        }
+        h2[jp] = pk2(hv[0], hv[1]);
+        a2[jp] = pk2(av[0], av[1]);
     }
     const float Dd = (valid && D) ? D[d] : 0.f;
 
@@ -115,29 +143,31 @@ diag_scan_bf16_kernel(int64_t L, int64_t Dm, int N, const __nv_bfloat16 *__restr
                 cp_async_wait<0>();
             }
             __syncthreads();
+            // B and C of the tile as float32, shared by every channel of the CTA
+            for (int e = tid; e < tn * NMAX; e += kThr) {
+                const int tt = e / NMAX, n = e % NMAX;
+                sBf[tt][n] = __bfloat162float(sB[buf][tt][n]);
+                sCf[tt][n] = __bfloat162float(sC[buf][tt][n]);
+            }
+            __syncthreads();
             for (int tt = 0; tt < tn; ++tt) {
                 const float dtv = __bfloat162float(sdt[buf][tt][ch]);
                 const float xv = __bfloat162float(sx[buf][tt][ch]);
-                const float u = dtv * xv;
-                float acc0 = 0.f, acc1 = 0.f;
+                const uint64_t d2 = pk2(dtv, dtv), u2 = pk2(dtv * xv, dtv * xv);
+                uint64_t acc2 = pk2(0.f, 0.f);
 #pragma unroll
-                for (int j0 = 0; j0 < NH; j0 += 8) {
-                    const uint4 bq = *reinterpret_cast<const uint4 *>(&sB[buf][tt][nb + j0]);
-                    const uint4 cq = *reinterpret_cast<const uint4 *>(&sC[buf][tt][nb + j0]);
-                    const __nv_bfloat162 *bp = reinterpret_cast<const __nv_bfloat162 *>(&bq);
-                    const __nv_bfloat162 *cp = reinterpret_cast<const __nv_bfloat162 *>(&cq);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 bf = __bfloat1622float2(bp[k]);
-                        const float2 cf = __bfloat1622float2(cp[k]);
-                        const int j = j0 + 2 * k;
-                        h[j] = fmaf(ex2f(dtv * A2[j]), h[j], u * bf.x);
-                        h[j + 1] = fmaf(ex2f(dtv * A2[j + 1]), h[j + 1], u * bf.y);
-                        acc0 = fmaf(cf.x, h[j], acc0);
-                        acc1 = fmaf(cf.y, h[j + 1], acc1);
-                    }
+                for (int jp = 0; jp < NH / 2; ++jp) {
+                    float e0, e1;
+                    up2(mul2(d2, a2[jp]), e0, e1);
+                    const uint64_t al = pk2(ex2f(e0), ex2f(e1));
+                    const float2 bf = *reinterpret_cast<const float2 *>(&sBf[tt][nb + 2 * jp]);
+                    const float2 cf = *reinterpret_cast<const float2 *>(&sCf[tt][nb + 2 * jp]);
+                    h2[jp] = fma2(al, h2[jp], mul2(u2, pk2(bf.x, bf.y)));
+                    acc2 = fma2(pk2(cf.x, cf.y), h2[jp], acc2);
                 }
-                float acc = acc0 + acc1;
+                float a0, a1;
+                up2(acc2, a0, a1);
+                float acc = a0 + a1;
                 acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 if (half == 0) sy[tt][ch] = __float2bfloat16_rn(acc + Dd * xv);
             }
@@ -155,8 +185,12 @@ diag_scan_bf16_kernel(int64_t L, int64_t Dm, int N, const __nv_bfloat16 *__restr
     }
     if (final_state && valid) {
 #pragma unroll
-        for (int j = 0; j < NH; ++j)
-            if (nb + j < N) final_state[(b * Dm + d) * N + nb + j] = h[j];
+        for (int jp = 0; jp < NH / 2; ++jp) {
+            float h0, h1;
+            up2(h2[jp], h0, h1);
+            if (nb + 2 * jp < N) final_state[(b * Dm + d) * N + nb + 2 * jp] = h0;
+            if (nb + 2 * jp + 1 < N) final_state[(b * Dm + d) * N + nb + 2 * jp + 1] = h1;
+        }
     }
 }
 
