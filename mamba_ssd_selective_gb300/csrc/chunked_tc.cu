@@ -454,30 +454,36 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 
 // ------------------------------------------- persistent chunk scan (Q <= 128)
 //
-// One CTA per SM walks work items (b, 128-token tile, group of hb heads).
-// The heads of a group share the C and B tiles and S = C B^T; per head it
-// needs x, the entering state(s) and its own decay mask. Warp roles:
-//   warp 0       TMA producer of C, B (per item) and x (per head)
+// One CTA per SM walks work items (b, 128-token tile, group of hb heads that
+// share a B/C group). Per item, in tensor memory (TMEM, 512 columns):
+//   S       = C B^T                      columns [0, 128)          (MMA1)
+//   Yo(s,k) = C h_in(s, k)^T             128 + 64 (s hb + k)       (MMA3, one
+//             chain per chunk s of the tile with N = 64 hb: the C operand is
+//             read once for all heads of the item)
+//   S'(k)   = S o decay_k (+ D_k on the diagonal), bf16     384 / 448 (two buffers)
+//   Y(k)    = Yo'(k) + S'(k) X_k, accumulated by MMA2 onto Yo'(k) = the
+//             row-scaled entering-state term, which the epilogue writes back
+//             into the columns of Yo(0, k) before MMA2 (A operand of MMA2
+//             read from TMEM: S' never touches shared memory)
+// so y(k) = Y(k) leaves TMEM in one read. Warp roles:
+//   warp 0       TMA producer: C, B (per item), x (per head, 4-deep ring)
 //   warp 10      TMA producer of the entering states (waits for the state pass)
-//   warp 1       MMA issuer (one lane): S = C B^T; Yo = C h_in^T; Y = S' X
+//   warp 1       MMA issuer (one lane)
 //   warps 2..9   epilogue, two groups of four warps (one warp per TMEM lane
-//                quarter in each group). Per item: the cumulative sums of all
-//                its heads (the only cross-warp barriers). Per head: S' = S o
-//                decay (+ D on the diagonal, so that Y carries D x) into one
-//                of two S' buffers, group 0 the column blocks {0, 3}, group 1
-//                {1, 2} (balanced over the causal triangle); y = Y + scale Yo,
-//                group g the columns p in [32 g, 32 g + 32), each warp storing
-//                its 32 x 32 block with 16-byte stores from registers.
-// dt, A and D of the next item are loaded one item ahead. Rings between the
-// roles are guarded by mbarriers; S' and the accumulators are double-buffered
-// so the MMAs of head k+1 overlap the epilogue of head k. All waits are
-// bounded: a timeout raises a CTA-wide flag, every role then runs to the end
-// of its loop without waiting and the status word records SSD_ERR_TIMEOUT.
+//                quarter per group): cumulative sums of all heads of the item
+//                (the item's only cross-warp barriers); per head S' -- group 0
+//                the 32-column blocks {0, 3} of S, group 1 {1, 2}, balanced
+//                over the causal triangle --, the entering-state rescale and
+//                the y store of its 32 columns of p.
+// All waits are bounded: a timeout raises a CTA-wide flag, every role then
+// runs to the end of its loop without waiting and the status word records
+// SSD_ERR_TIMEOUT.
 
 constexpr int kHBMax = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kScanPThreads = 352;  // 11 warps
 constexpr int kEpiThreads = 256;
+constexpr int kXStages = 4;
 
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *fail) {
     const uint32_t addr = tc::smem_u32(bar);
@@ -496,7 +502,7 @@ __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile i
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <int I> __device__ __forceinline__ float pick4(const float (&v)[kHBMax], int k) {
+__device__ __forceinline__ float pick4(const float (&v)[kHBMax], int k) {
     return k == 0 ? v[0] : k == 1 ? v[1] : k == 2 ? v[2] : v[3];
 }
 
@@ -508,38 +514,36 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     const int64_t ntiles = (a.L + kRows - 1) / kRows;
     const int64_t n_items = prm.n_items;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t HS = (uint32_t)nsub * 16384u;  // bytes of one entering-state stage
-    const uint32_t NHS = nsub == 1 ? 2u : 1u;      // entering-state stages (32 KB either way)
+    const uint32_t HT = (uint32_t)HB * 16384u;  // entering-state tiles of one chunk (HB heads)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sC = smem;                  // C tile, K-major, 2 panels
     uint8_t *sB = smem + 32768;          // B tile, K-major, 2 panels
-    uint8_t *sX = smem + 65536;          // x ring: 2 x 16 KB, MN-major
-    uint8_t *sH = smem + 98304;          // entering-state ring: NHS x HS = 32 KB, K-major
-    uint8_t *sP = sH + 32768;            // S' (bf16, K-major): 2 x 32 KB
-    uint8_t *sY = sP + 65536;            // y staging: 8 warps x 2 KB (32 x 32 bf16, 64-byte swizzle)
-    float *s_cs = reinterpret_cast<float *>(sY + 16384);  // [kHBMax][128]
+    uint8_t *sX = smem + 65536;          // x ring: kXStages x 16 KB, MN-major
+    uint8_t *sH = sX + kXStages * 16384; // entering states: per chunk s, 2 panels of 64 hb rows (K-major, N = (k, p))
+    float *s_cs = reinterpret_cast<float *>(sH + 65536);  // [kHBMax][128]
     float *s_dt = s_cs + kHBMax * 128;                    // [kHBMax][128]
     float *s_colf = s_dt + kHBMax * 128;                  // [kHBMax][128]
     float *s_tot = s_colf + kHBMax * 128;                 // [kHBMax][4]
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_tot + kHBMax * 4);
     uint64_t *tile_full = bars + 0, *tile_empty = bars + 1;
-    uint64_t *x_full = bars + 2, *x_empty = bars + 4;      // [2] each
-    uint64_t *h_full = bars + 6, *h_empty = bars + 8;      // [2] each
-    uint64_t *s_full = bars + 10, *s_empty = bars + 11;
-    uint64_t *p_full = bars + 12, *p_empty = bars + 14;    // [2] each
-    uint64_t *acc_full = bars + 16, *acc_empty = bars + 18;  // [2] each
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+    uint64_t *h_full = bars + 2, *h_empty = bars + 3;
+    uint64_t *s_full = bars + 4, *s_empty = bars + 5;
+    uint64_t *yo_full = bars + 6, *acc_empty = bars + 7;
+    uint64_t *y_full = bars + 8;
+    uint64_t *p_full = bars + 9, *p_empty = bars + 11;                  // [2] each
+    uint64_t *x_full = bars + 13, *x_empty = bars + 13 + kXStages;      // [kXStages] each
+    constexpr int kBars = 13 + 2 * kXStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     if (tid == 0) {
-        for (int k = 0; k < 20; ++k) tc::mbar_init(bars + k, 1);
+        for (int k = 0; k < kBars; ++k) tc::mbar_init(bars + k, 1);
         tc::mbar_init(s_empty, kEpiThreads);
+        tc::mbar_init(acc_empty, kEpiThreads);
         tc::mbar_init(p_full + 0, kEpiThreads);
         tc::mbar_init(p_full + 1, kEpiThreads);
-        tc::mbar_init(acc_empty + 0, kEpiThreads);
-        tc::mbar_init(acc_empty + 1, kEpiThreads);
         tc::fence_mbar_init();
         *s_fail = 0;
     }
@@ -550,6 +554,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tAcc = tmem + 128, tP = tmem + 384;
     const int hpg = (int)(a.H / a.G);  // heads per B/C group
 
     auto decode = [&](int64_t u, int64_t &b, int64_t &tile, int &hg) {
@@ -580,7 +585,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                     if (!pwait(&x_empty[xi], xph ^ 1, s_fail)) break;
                     tc::mbar_arrive_expect_tx(&x_full[xi], 16384u);
                     tc::tma_load_3d(sX + xi * 16384, &prm.mx, &x_full[xi], (hg * HB + k) * kP, t0, (int)b);
-                    if (++xi == 2) { xi = 0; xph ^= 1; }
+                    if (++xi == kXStages) { xi = 0; xph ^= 1; }
                 }
             }
         }
@@ -588,22 +593,23 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         // ------------------------------ TMA producer of entering states
         if (lane == 0) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            uint32_t hi = 0, hph = 0;
+            uint32_t hcnt = 0;
             for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
                 int64_t b, tile;
                 int hg;
                 decode(u, b, tile, hg);
                 const int64_t t0 = tile * kRows;
-                for (int k = 0; k < HB; ++k) {
-                    if (!pwait(&h_empty[hi], hph ^ 1, s_fail)) break;
-                    tc::mbar_arrive_expect_tx(&h_full[hi], HS);
-                    for (int sb = 0; sb < nsub; ++sb) {
-                        const int64_t cidx = (t0 + (int64_t)sb * Q) / Q;
+                if (!pwait(h_empty, (hcnt & 1) ^ 1, s_fail)) break;
+                ++hcnt;
+                tc::mbar_arrive_expect_tx(h_full, (uint32_t)nsub * HT);
+                for (int sb = 0; sb < nsub; ++sb) {
+                    const int64_t cidx = (t0 + (int64_t)sb * Q) / Q;
+                    for (int k = 0; k < HB; ++k) {
                         const int row0 = (int)(((b * a.nc + cidx) * a.H + hg * HB + k) * kP);
-                        tc::tma_load_2d(sH + hi * HS + sb * 16384, &prm.mh, &h_full[hi], 0, row0);
-                        tc::tma_load_2d(sH + hi * HS + sb * 16384 + 8192, &prm.mh, &h_full[hi], 64, row0);
+                        uint8_t *dst = sH + sb * HT + k * 8192;
+                        tc::tma_load_2d(dst, &prm.mh, h_full, 0, row0);
+                        tc::tma_load_2d(dst + HB * 8192, &prm.mh, h_full, 64, row0);
                     }
-                    if (++hi == NHS) { hi = 0; hph ^= 1; }
                 }
             }
         }
@@ -612,55 +618,55 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         if (lane == 0) {
             const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
             const uint32_t idY = tc::idesc_bf16(128, kP, false, true);
-            const uint32_t idO = tc::idesc_bf16(128, kP, false, false);
-            const uint32_t c0 = tc::smem_u32(sC), b0 = tc::smem_u32(sB);
-            uint32_t tph = 0, sph = 0, xi = 0, xph = 0, hi = 0, hph = 0, ai = 0, aph = 0, nh = 0;
+            const uint32_t idO = tc::idesc_bf16(128, kP * HB, false, false);
+            const uint32_t c0 = tc::smem_u32(sC), b0 = tc::smem_u32(sB), h0 = tc::smem_u32(sH);
+            uint32_t tph = 0, sph = 0, hph = 0, aph = 0, xi = 0, xph = 0, nh = 0;
             for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
                 if (!pwait(tile_full, tph, s_fail)) break;
                 tph ^= 1;
+                // S = C B^T (the previous item's S has been read)
                 if (!pwait(s_empty, sph ^ 1, s_fail)) break;
                 sph ^= 1;
                 tc::tc_fence_after();
                 for (int k = 0; k < kN; k += 16) {
                     const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
                     const uint64_t db = tc::sdesc_sw128(b0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
-                    tc::mma_bf16(tmem, da, db, idS, k > 0 ? 1u : 0u);
+                    tc::mma_bf16(tS, da, db, idS, k > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(s_full);
+                // Yo(s, .) = C h_in(s, .)^T for all heads at once (the previous
+                // item's accumulators have been read)
+                if (!pwait(h_full, hph, s_fail)) break;
+                hph ^= 1;
+                if (!pwait(acc_empty, aph ^ 1, s_fail)) break;
+                aph ^= 1;
+                tc::tc_fence_after();
+                for (int sb = 0; sb < nsub; ++sb)
+                    for (int k = 0; k < kN; k += 16) {
+                        const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                        const uint64_t db =
+                            tc::sdesc_sw128(h0 + sb * HT + (k >> 6) * (HT / 2) + (k & 63) * 2, 16, 1024);
+                        tc::mma_bf16(tAcc + sb * HB * 64, da, db, idO, k > 0 ? 1u : 0u);
+                    }
+                tc::mma_commit(yo_full);
+                tc::mma_commit(h_empty);
+                tc::mma_commit(tile_empty);  // C and B are not read after this point
+                // Y(k) = Yo'(k) + S'(k) X_k
                 for (int kh = 0; kh < HB; ++kh, ++nh) {
-                    const uint32_t acc = tmem + 128 + ai * 192;
                     const uint32_t pb = nh & 1, pph = (nh >> 1) & 1;
-                    if (!pwait(&acc_empty[ai], aph ^ 1, s_fail)) break;
-                    // Yo = C h_in^T first: its operands are ready long before S'
-                    if (!pwait(&h_full[hi], hph, s_fail)) break;
-                    tc::tc_fence_after();
-                    const uint32_t h0 = tc::smem_u32(sH + hi * HS);
-                    for (int sb = 0; sb < nsub; ++sb)
-                        for (int k = 0; k < kN; k += 16) {
-                            const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
-                            const uint64_t db =
-                                tc::sdesc_sw128(h0 + sb * 16384 + (k >> 6) * 8192 + (k & 63) * 2, 16, 1024);
-                            tc::mma_bf16(acc + 64 + 64 * sb, da, db, idO, k > 0 ? 1u : 0u);
-                        }
-                    tc::mma_commit(&h_empty[hi]);
-                    if (++hi == NHS) { hi = 0; hph ^= 1; }
                     if (!pwait(&x_full[xi], xph, s_fail)) break;
                     if (!pwait(&p_full[pb], pph, s_fail)) break;
                     tc::tc_fence_after();
                     const uint32_t x0 = tc::smem_u32(sX + xi * 16384);
-                    const uint32_t p0 = tc::smem_u32(sP + pb * 32768);
                     for (int k = 0; k < kRows; k += 16) {
-                        const uint64_t da = tc::sdesc_sw128(p0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
                         const uint64_t db = tc::sdesc_sw128(x0 + k * 128, 16384, 1024);
-                        tc::mma_bf16(acc, da, db, idY, k > 0 ? 1u : 0u);
+                        tc::mma_bf16_ts(tAcc + kh * 64, tP + pb * 64 + k / 2, db, idY, 1u);
                     }
                     tc::mma_commit(&p_empty[pb]);
                     tc::mma_commit(&x_empty[xi]);
-                    if (++xi == 2) { xi = 0; xph ^= 1; }
-                    tc::mma_commit(&acc_full[ai]);
-                    if (++ai == 2) { ai = 0; aph ^= 1; }
+                    tc::mma_commit(y_full);
+                    if (++xi == kXStages) { xi = 0; xph ^= 1; }
                 }
-                tc::mma_commit(tile_empty);
             }
         }
     } else {
@@ -669,11 +675,11 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         const int grp = ew >> 2;            // column group
         const int qd = warp & 3;            // TMEM lane quarter of this warp
         const int i = qd * 32 + lane;       // tile row
-        const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16);
+        const uint32_t lq = (uint32_t)(qd * 32) << 16;
         const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
         const int Ja = grp == 0 ? 0 : 1, Jb = grp == 0 ? 3 : 2;  // this group's column blocks of S'
         const int sub = (Q < kRows && i >= Q) ? 1 : 0;           // chunk of this row inside the tile
-        uint32_t sph = 0, ai = 0, aph = 0, nh = 0;
+        uint32_t sph = 0, yoph = 0, ycnt = 0, nh = 0;
 
         // per-item scalars of this thread's row, loaded one item ahead
         float dtv[kHBMax], Av[kHBMax], Dv[kHBMax];
@@ -707,11 +713,11 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             for (int k = 0; k < kHBMax; ++k) { dcur[k] = dtv[k]; Acur[k] = Av[k]; Dcur[k] = Dv[k]; }
             fetch(u + gridDim.x);  // next item's scalars, consumed one item later
 
-            // cumulative sums of every head of the item (the item's only barriers)
+            // cumulative sums (base-2 units) of every head of the item
             float csv[kHBMax], scv[kHBMax], incl[kHBMax], wtot[kHBMax];
 #pragma unroll
             for (int k = 0; k < kHBMax; ++k) {
-                float v = dcur[k] * (Acur[k] * kLog2e);  // cumulative sums in base-2 units
+                float v = dcur[k] * (Acur[k] * kLog2e);
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float w = __shfl_up_sync(0xffffffffu, v, o);
@@ -738,16 +744,18 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             epi_sync();
             pwait(s_full, sph, s_fail);
             sph ^= 1;
+            pwait(yo_full, yoph, s_fail);
+            yoph ^= 1;
             tc::tc_fence_after();
 
-            // S' of head k (this group's column blocks) into S' buffer n & 1.
-            // Branch-free per element: the exponent is clamped to <= 0 so every
-            // lane computes it, and the causal mask is a select.
-            auto sprime = [&](int k, uint32_t n) {
-                const float cs_i = pick4<0>(csv, k), Dh = pick4<0>(Dcur, k);
+            // S'(k) into TMEM buffer n & 1, and the rescaled entering-state term
+            // Yo'(k) = exp(cs_i - cs_chunk_start) Yo(sub(i), k) into the columns
+            // of Yo(0, k), where MMA2 accumulates S'(k) X_k onto it
+            auto prepare = [&](int k, uint32_t n) {
+                const float cs_i = pick4(csv, k), Dh = pick4(Dcur, k), sc = pick4(scv, k);
                 const float *cs_ = s_cs + k * 128, *dt_ = s_dt + k * 128, *cf_ = s_colf + k * 128;
-                uint8_t *sp = sP + (n & 1) * 32768;
                 pwait(&p_empty[n & 1], ((n >> 1) & 1) ^ 1, s_fail);
+                tc::tc_fence_after();
                 const int Jd = qd;
 #pragma unroll 1
                 for (int jj = 0; jj < 2; ++jj) {
@@ -755,7 +763,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                     float v[32];
                     if (J < Jd) {
                         // block before this warp's rows: factorised decay
-                        tc::tmem_ld32(tq + J * 32, v);
+                        tc::tmem_ld32(tS + lq + J * 32, v);
                         tc::tmem_ld_wait();
                         const bool same = Q >= kRows || (J >> 1) == (Jd >> 1);
                         const float rf = same ? tc::ex2(cs_i - cs_[J * 32 + 31]) : 0.f;
@@ -763,7 +771,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                         for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * cf_[J * 32 + q];
                     } else if (J == Jd) {
                         // block holding this warp's rows: exact decay, causal mask, D on the diagonal
-                        tc::tmem_ld32(tq + J * 32, v);
+                        tc::tmem_ld32(tS + lq + J * 32, v);
                         tc::tmem_ld_wait();
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
@@ -777,55 +785,54 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
 #pragma unroll
                         for (int q = 0; q < 32; ++q) v[q] = 0.f;
                     }
+                    uint32_t pkd[16];
 #pragma unroll
-                    for (int q = 0; q < 32; q += 8) {
-                        const uint4 pk = make_uint4(pack_bf16x2(v[q], v[q + 1]), pack_bf16x2(v[q + 2], v[q + 3]),
-                                                    pack_bf16x2(v[q + 4], v[q + 5]), pack_bf16x2(v[q + 6], v[q + 7]));
-                        *reinterpret_cast<uint4 *>(sp + tc::sw128_offset(i, J * 32 + q, kRows)) = pk;
-                    }
+                    for (int q = 0; q < 16; ++q) pkd[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+                    tc::tmem_st16(tP + lq + (n & 1) * 64 + J * 16, pkd);
                 }
-                tc::fence_proxy_async_smem();
-                if (k == HB - 1) {
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(s_empty);  // S fully read for this item
+                {
+                    float ov[32];
+                    tc::tmem_ld32(tAcc + lq + (sub * HB + k) * 64 + 32 * grp, ov);
+                    tc::tmem_ld_wait();
+                    uint32_t r[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(sc * ov[q]);
+                    tc::tmem_st32(tAcc + lq + k * 64 + 32 * grp, r);
                 }
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                if (k == HB - 1) tc::mbar_arrive(s_empty);  // S fully read for this item
                 tc::mbar_arrive(&p_full[n & 1]);
             };
-            // y of head k: this warp's 32 rows x the 32 columns p in [32 grp, 32 grp + 32)
+            // y(k) = Y(k): this warp's 32 rows x the 32 columns p in [32 grp, 32 grp + 32)
             auto yout = [&](int k) {
-                pwait(&acc_full[ai], aph, s_fail);
+                pwait(y_full, ycnt & 1, s_fail);
+                ++ycnt;
                 tc::tc_fence_after();
-                const uint32_t acc = tq + 128 + ai * 192;
-                const float sc = pick4<0>(scv, k);
-                float yv[32], ov[32];
-                tc::tmem_ld32(acc + 32 * grp, yv);
-                tc::tmem_ld32(acc + 64 + 64 * sub + 32 * grp, ov);
+                float yv[32];
+                tc::tmem_ld32(tAcc + lq + k * 64 + 32 * grp, yv);
                 tc::tmem_ld_wait();
-                tc::tc_fence_before();
-                tc::mbar_arrive(&acc_empty[ai]);
-                if (++ai == 2) { ai = 0; aph ^= 1; }
-                // 16-byte stores straight from registers: this row's 32 columns
                 if (t0 + i < a.L) {
                     __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(a.y) +
                                           ((b * a.L + t0 + i) * a.H + hg * HB + k) * kP + 32 * grp;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int q = c * 8;
-                        uint4 pk;
-                        pk.x = pack_bf16x2(fmaf(sc, ov[q], yv[q]), fmaf(sc, ov[q + 1], yv[q + 1]));
-                        pk.y = pack_bf16x2(fmaf(sc, ov[q + 2], yv[q + 2]), fmaf(sc, ov[q + 3], yv[q + 3]));
-                        pk.z = pack_bf16x2(fmaf(sc, ov[q + 4], yv[q + 4]), fmaf(sc, ov[q + 5], yv[q + 5]));
-                        pk.w = pack_bf16x2(fmaf(sc, ov[q + 6], yv[q + 6]), fmaf(sc, ov[q + 7], yv[q + 7]));
+                        const uint4 pk = make_uint4(pack_bf16x2(yv[q], yv[q + 1]), pack_bf16x2(yv[q + 2], yv[q + 3]),
+                                                    pack_bf16x2(yv[q + 4], yv[q + 5]),
+                                                    pack_bf16x2(yv[q + 6], yv[q + 7]));
                         *reinterpret_cast<uint4 *>(yrow + q) = pk;
                     }
                 }
             };
-            // S'(k) runs one head ahead of y(k - 1); one call site each
+            // prepare(k) runs one head ahead of yout(k - 1); one call site each
 #pragma unroll 1
             for (int k = 0; k <= HB; ++k) {
-                if (k < HB) sprime(k, nh + k);
+                if (k < HB) prepare(k, nh + k);
                 if (k >= 1) yout(k - 1);
             }
+            tc::tc_fence_before();
+            tc::mbar_arrive(acc_empty);  // every accumulator of this item has been read
             nh += HB;
         }
         tc::tc_fence_before();
@@ -957,7 +964,7 @@ int device_cc_major() {
 size_t state_smem(int Q) { return (size_t)Q * 384 + 4096 + 1024; }
 constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
-size_t scanp_smem(int) { return 98304 + 32768 + 65536 + 16384 + 7168 + 1024; }
+size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 8192 + 1024; }
 
 int num_sms() {
     static int n = 0;
@@ -1051,9 +1058,11 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    // persistent chunk scan for Q <= 128: head groups of hb heads sharing a B/C group
+    // persistent chunk scan for Q <= 128: head groups of hb heads sharing a B/C
+    // group, at most 4 / (chunks per tile) so that their accumulators fit TMEM
     const int hpg = (int)(a.H / a.G);
-    p.hb = hpg % 4 == 0 ? 4 : hpg % 2 == 0 ? 2 : 1;
+    const int hbmax = a.Q >= kRows ? 4 : 2;
+    p.hb = (hbmax >= 4 && hpg % 4 == 0) ? 4 : hpg % 2 == 0 ? 2 : 1;
     p.nhg = (int)(a.H / p.hb);
     p.n_items = a.B * ntiles * p.nhg;
     const bool staged = a.stage_ev[0] != nullptr;  // per-stage timing: no programmatic overlap

@@ -8,6 +8,8 @@
 //   variant 2: A MN-major [K][M], B MN-major [K][N] written by threads D = A^T B
 //   variant 3: as variant 0 but both operands loaded by TMA (SWIZZLE_128B)
 //   variant 4: as variant 2 but both operands loaded by TMA
+//   variant 5: A [M][K] in tensor memory (written with tcgen05.st, two bf16
+//              per 32-bit column, lane = row), B K-major [N][K] in smem
 //
 // Sizes: M = 128; N in {64, 128}; K in {64, 128, 256}. All shared-memory
 // addresses a descriptor can reach stay inside the dynamic allocation.
@@ -44,7 +46,8 @@ probe_kernel(int variant, const __nv_bfloat16 *__restrict__ A, const __nv_bfloat
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool a_mn = (variant == 2 || variant == 4);
     const bool b_mn = (variant == 1 || variant == 2 || variant == 4);
-    const bool use_tma = variant >= 3;
+    const bool use_tma = variant == 3 || variant == 4;
+    const bool a_tmem = variant == 5;
 
     if (tid == 0) {
         mbar_init(bar_mma, 1);
@@ -52,10 +55,10 @@ probe_kernel(int variant, const __nv_bfloat16 *__restrict__ A, const __nv_bfloat
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
-    if (!use_tma) {
+    if (!use_tma && !a_tmem) {
         // A: K-major rows = m (K contiguous), or MN-major rows = k (M contiguous)
         for (int e = tid; e < kM * K; e += blockDim.x) {
             const int m = e / K, k = e % K;
@@ -65,6 +68,8 @@ probe_kernel(int variant, const __nv_bfloat16 *__restrict__ A, const __nv_bfloat
             else { const int kk = e / kM, mm = e % kM; off = sw128_offset(kk, mm, K); }
             *reinterpret_cast<__nv_bfloat16 *>(sA + off) = v;
         }
+    }
+    if (!use_tma) {
         for (int e = tid; e < N * K; e += blockDim.x) {
             const __nv_bfloat16 v = B[e];  // [N][K] for K-major, [K][N] for MN-major
             uint32_t off;
@@ -77,6 +82,28 @@ probe_kernel(int variant, const __nv_bfloat16 *__restrict__ A, const __nv_bfloat
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t tA = tmem + 128;  // A operand columns (variant 5): K/2 <= 128
+    if (a_tmem) {
+        // row m = TMEM lane; column c holds A[m][2c] (low half) and A[m][2c+1]
+        const int m = warp * 32 + (tid & 31);
+        for (int c0 = 0; c0 < K / 2; c0 += 32) {
+            uint32_t r[32];
+            for (int j = 0; j < 32; ++j) {
+                const int c = c0 + j;
+                uint32_t lo = 0, hi = 0;
+                if (c < K / 2) {
+                    lo = __bfloat16_as_ushort(A[m * K + 2 * c]);
+                    hi = __bfloat16_as_ushort(A[m * K + 2 * c + 1]);
+                }
+                r[j] = lo | (hi << 16);
+            }
+            tmem_st32(tA + ((uint32_t)(warp * 32) << 16) + c0, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
 
     bool ok = true;
     if (tid == 0) {
@@ -104,7 +131,8 @@ probe_kernel(int variant, const __nv_bfloat16 *__restrict__ A, const __nv_bfloat
                 else da = sdesc_sw128(a0 + k * 128, K * 128, 1024);
                 if (!b_mn) db = sdesc_sw128(b0 + (k >> 6) * N * 128 + (k & 63) * 2, 16, 1024);
                 else db = sdesc_sw128(b0 + k * 128, K * 128, 1024);
-                mma_bf16(tmem, da, db, idesc, k > 0 ? 1u : 0u);
+                if (a_tmem) mma_bf16_ts(tmem, tA + k / 2, db, idesc, k > 0 ? 1u : 0u);
+                else mma_bf16(tmem, da, db, idesc, k > 0 ? 1u : 0u);
             }
             mma_commit(bar_mma);
         } else {
@@ -128,7 +156,7 @@ probe_kernel(int variant, const __nv_bfloat16 *__restrict__ A, const __nv_bfloat
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -162,12 +190,12 @@ int make_map(CUtensorMap *m, const void *base, int rows, int cols, int box_rows)
 
 extern "C" int tc_probe(int variant, const void *A, const void *B, float *D, int N, int K, int *status,
                         cudaStream_t stream) {
-    if (variant < 0 || variant > 4) return -10;
+    if (variant < 0 || variant > 5) return -10;
     if (!(N == 64 || N == 128) || !(K == 64 || K == 128 || K == 256)) return -11;
     Maps maps;
     memset(&maps, 0, sizeof(maps));
     const bool a_mn = (variant == 2 || variant == 4), b_mn = (variant == 1 || variant == 2 || variant == 4);
-    if (variant >= 3) {
+    if (variant == 3 || variant == 4) {
         int r = a_mn ? make_map(&maps.a, A, K, kM, K) : make_map(&maps.a, A, kM, K, kM);
         if (r) return r;
         r = b_mn ? make_map(&maps.b, B, K, N, K) : make_map(&maps.b, B, N, K, N);

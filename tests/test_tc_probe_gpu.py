@@ -2,7 +2,7 @@
 
 Compiles tests/csrc/tc_probe.cu (one tcgen05 MMA tile per operand layout the
 tensor-core SSD kernels use: K-major and MN-major SW128 operands, written by
-threads or loaded by TMA) and compares each result with torch's float32
+threads or loaded by TMA, and an A operand held in tensor memory) and compares each result with torch's float32
 matmul of the same bf16 values.
 """
 import ctypes
@@ -32,7 +32,7 @@ def probe(tmp_path_factory, cuda_device):
     return lib
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
 @pytest.mark.parametrize("N,K", [(64, 64), (64, 128), (128, 128), (64, 256), (128, 256)])
 def test_tcgen05_tile(probe, variant, N, K):
     g = torch.Generator().manual_seed(variant * 1000 + N + K)
