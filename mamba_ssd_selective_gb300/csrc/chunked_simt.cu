@@ -16,6 +16,7 @@
 // tensor-core path does not take; its register tiles are 4x4 per thread over
 // 64x64 output tiles.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
     const float cs_end = s_cs[Q - 1];  // padded tokens carry a = 0
     const int tid = threadIdx.x;
     if (tid < Q) s_w[tid] = expf(cs_end - s_cs[tid]) * s_dt[tid];
-    if (pt == 0 && nt == 0 && tid == 0) a.chunk_sum[(b * H + h) * a.nc + c] = cs_end;
+    if (pt == 0 && nt == 0 && tid == 0) a.chunk_sum[(b * H + h) * a.nc + c] = expf(cs_end);  // decay over the chunk
     __syncthreads();
 
     const int ty = tid / 16, tx = tid % 16;
@@ -102,13 +103,15 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
 
 // Serial pass over the chunks of one (b, h): replaces S_c with the entering
 // state h_in(c) (float32 in place and/or a bfloat16 copy) and writes the
-// final state. VW consecutive state elements per thread; the chunk states of
-// kPF chunks are loaded before the serial update consumes them, so each
-// thread keeps kPF independent loads in flight.
+// final state. The chunk states are float32 (CUDA-core path) or bfloat16
+// (tensor-core path, read from and replaced in states_bf16). VW consecutive
+// state elements per thread; the chunk states of kPF chunks are loaded
+// before the serial update consumes them, so each thread keeps kPF
+// independent loads in flight.
 constexpr int kPF = 8;
 
-template <bool F32_INPLACE, bool BF16, int VW>
-__global__ void __launch_bounds__(kT) state_pass_kernel(ChunkedArgs a) {
+template <typename TIn, bool F32_INPLACE, bool BF16, int VW>
+__global__ void __launch_bounds__(kT, 2) state_pass_kernel(ChunkedArgs a) {
     // Wait for the producer of the chunk states when launched as a programmatic
     // dependent of it; a no-op for an ordinary launch.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -121,6 +124,8 @@ __global__ void __launch_bounds__(kT) state_pass_kernel(ChunkedArgs a) {
     const int64_t b = blockIdx.z;
     if (e >= PN) return;
     const int64_t H = a.H, nc = a.nc;
+    const TIn *src = std::is_same<TIn, float>::value ? reinterpret_cast<const TIn *>(a.states)
+                                                      : reinterpret_cast<const TIn *>(a.states_bf16);
     float hv[VW];
 #pragma unroll
     for (int k = 0; k < VW; ++k) hv[k] = a.init_state ? a.init_state[(b * H + h) * PN + e + k] : 0.f;
@@ -132,14 +137,19 @@ __global__ void __launch_bounds__(kT) state_pass_kernel(ChunkedArgs a) {
 #pragma unroll
         for (int u = 0; u < kPF; ++u) {
             if (c0 + u < nc) {
-                const float *src = a.states + base + (c0 + u) * stride;
-                if constexpr (VW == 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                const TIn *p = src + base + (c0 + u) * stride;
+                if constexpr (VW == 4 && std::is_same<TIn, float>::value) {
+                    const float4 v = *reinterpret_cast<const float4 *>(p);
                     s[u][0] = v.x; s[u][1] = v.y; s[u][2] = v.z; s[u][3] = v.w;
+                } else if constexpr (VW == 4) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+                    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+                    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+                    s[u][0] = lo.x; s[u][1] = lo.y; s[u][2] = hi.x; s[u][3] = hi.y;
                 } else {
-                    s[u][0] = *src;
+                    s[u][0] = to_f32(*p);
                 }
-                dA[u] = expf(cs[c0 + u]);
+                dA[u] = cs[c0 + u];
             }
         }
 #pragma unroll
@@ -351,25 +361,82 @@ cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-template <int VW>
+// Tensor-core path: bfloat16 chunk states in states_bf16, replaced in place by
+// the bfloat16 entering states; 4 elements per thread. Up to kPFB chunks are
+// held packed (two registers per chunk) so that one round trip to L2 brings in
+// the whole chain of most workloads.
+constexpr int kPFB = 16;
+
+__global__ void __launch_bounds__(kT, 2) state_pass_bf16_kernel(ChunkedArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t PN = a.P * a.N;
+    const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * 4;
+    const int h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    if (e >= PN) return;
+    const int64_t H = a.H, nc = a.nc;
+    float hv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) hv[k] = a.init_state ? a.init_state[(b * H + h) * PN + e + k] : 0.f;
+    const float *cs = a.chunk_sum + (b * H + h) * nc;
+    const int64_t stride = H * PN;
+    const int64_t base = ((b * nc) * H + h) * PN + e;
+    for (int64_t c0 = 0; c0 < nc; c0 += kPFB) {
+        uint2 raw[kPFB];
+#pragma unroll
+        for (int u = 0; u < kPFB; ++u)
+            if (c0 + u < nc) raw[u] = *reinterpret_cast<const uint2 *>(a.states_bf16 + base + (c0 + u) * stride);
+#pragma unroll
+        for (int u = 0; u < kPFB; ++u) {
+            if (c0 + u < nc) {
+                const int64_t idx = base + (c0 + u) * stride;
+                __nv_bfloat162 lo = __floats2bfloat162_rn(hv[0], hv[1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(hv[2], hv[3]);
+                *reinterpret_cast<uint2 *>(a.states_bf16 + idx) =
+                    make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                const float dA = cs[c0 + u];
+                const float2 s01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u].x));
+                const float2 s23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u].y));
+                hv[0] = fmaf(dA, hv[0], s01.x);
+                hv[1] = fmaf(dA, hv[1], s01.y);
+                hv[2] = fmaf(dA, hv[2], s23.x);
+                hv[3] = fmaf(dA, hv[3], s23.y);
+            }
+        }
+    }
+    if (a.final_state) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a.final_state[(b * H + h) * PN + e + k] = hv[k];
+    }
+}
+
+template <typename TIn, int VW>
 void (*pick_state_pass(bool f32, bool bf16))(ChunkedArgs) {
-    if (f32 && bf16) return state_pass_kernel<true, true, VW>;
-    if (f32) return state_pass_kernel<true, false, VW>;
-    if (bf16) return state_pass_kernel<false, true, VW>;
-    return state_pass_kernel<false, false, VW>;
+    if (f32 && bf16) return state_pass_kernel<TIn, true, true, VW>;
+    if (f32) return state_pass_kernel<TIn, true, false, VW>;
+    if (bf16) return state_pass_kernel<TIn, false, true, VW>;
+    return state_pass_kernel<TIn, false, false, VW>;
 }
 
 cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool write_bf16, cudaStream_t stream,
-                              bool programmatic) {
+                              bool programmatic, bool bf16_in) {
     if (a.B == 0) return cudaSuccess;
     const int64_t PN = a.P * a.N;
-    // float4 path: every (b, c, h) block of PN floats starts 16-byte aligned
+    // 4-wide path: every (b, c, h) block of PN states starts aligned
     const bool vec = (PN % 4 == 0) && (reinterpret_cast<uintptr_t>(a.init_state) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.final_state) % 16 == 0);
     const int VW = vec ? 4 : 1;
     dim3 grid((unsigned)((PN / VW + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B);
-    void (*kern)(ChunkedArgs) = vec ? pick_state_pass<4>(write_f32_inplace, write_bf16)
-                                    : pick_state_pass<1>(write_f32_inplace, write_bf16);
+    void (*kern)(ChunkedArgs);
+    if (bf16_in && vec && write_bf16 && !write_f32_inplace)
+        kern = state_pass_bf16_kernel;
+    else if (bf16_in)
+        kern = vec ? pick_state_pass<__nv_bfloat16, 4>(write_f32_inplace, write_bf16)
+                   : pick_state_pass<__nv_bfloat16, 1>(write_f32_inplace, write_bf16);
+    else
+        kern = vec ? pick_state_pass<float, 4>(write_f32_inplace, write_bf16)
+                   : pick_state_pass<float, 1>(write_f32_inplace, write_bf16);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kT);

@@ -41,6 +41,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: a wait this long means some
 constexpr int kRows = 128;                   // token rows per tile (MMA M)
 constexpr int kP = 64;                       // headdim handled here
 constexpr int kN = 128;                      // d_state handled here
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct TcParams {
     ChunkedArgs a;
@@ -88,28 +89,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // --------------------------------------------------------- chunk state
+//
+// One CTA per (b, chunk c, group of hb heads sharing a B/C group). All heads
+// of the group share the A operand B^T, so their chunk states come out of one
+// MMA chain with N = 64 hb (the tensor core's cost per instruction is nearly
+// flat in N up to 256): S^T[n, (k, p)] = sum_j B_j[n] (w_k,j x_k,j[p]) with
+// w_k,j = exp(cs_end - cs_j) dt_j of head k. The states go out as bfloat16.
 
-__global__ void __launch_bounds__(128) chunk_state_tc(const __grid_constant__ TcParams prm) {
+__global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ TcParams prm) {
     const ChunkedArgs &a = prm.a;
-    const int c = blockIdx.x, h = blockIdx.y;
+    const int c = blockIdx.x, hg = blockIdx.y;
     const int64_t b = blockIdx.z;
+    const int HB = prm.hb;
+    const int h0 = hg * HB;
     const int Q = a.Q, R = Q < kRows ? Q : kRows;
-    const int g = (int)(h / (a.H / a.G));
+    const int g = (int)(h0 / (a.H / a.G));
     const int64_t t0 = (int64_t)c * Q;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sB = smem;                    // B^T operand: 2 panels (n 0-63, 64-127) x Q rows x 128 B
-    uint8_t *sX = smem + Q * 256;          // x operand: Q rows x 128 B, scaled by w_j in place
-    float *s_dt = reinterpret_cast<float *>(sX + Q * 128);
-    float *s_cs = s_dt + 256;
-    float *s_w = s_cs + 256;
-    float *s_tot = s_w + 256;
+    uint8_t *sX = smem + Q * 256;          // x operands of the hb heads: hb panels of Q rows x 128 B
+    float *s_w = reinterpret_cast<float *>(sX + HB * Q * 128);  // [hb][Q]
+    float *s_cs = s_w + 4 * 256;                                // [Q] scratch of the cumulative sum
+    float *s_dt = s_cs + 256;                                   // [Q]
+    float *s_tot = s_dt + 256;
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_tot + 8);
     uint64_t *bar_mma = bar_ld + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
     int *s_fail = reinterpret_cast<int *>(tmem_slot + 1);
+    const uint32_t ncols = HB == 4 ? 256u : HB == 2 ? 128u : 64u;
 
     if (tid == 0) {
         tc::mbar_init(bar_ld, 1);
@@ -118,7 +128,7 @@ __global__ void __launch_bounds__(128) chunk_state_tc(const __grid_constant__ Tc
         *s_fail = 0;
     }
     if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, 64);
+        tc::tmem_alloc(tmem_slot, ncols);
         tc::tmem_relinquish();
     }
     __syncthreads();
@@ -126,54 +136,72 @@ __global__ void __launch_bounds__(128) chunk_state_tc(const __grid_constant__ Tc
     const uint32_t tmem = *tmem_slot;
 
     if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_ld, (uint32_t)Q * 384u);
+        tc::mbar_arrive_expect_tx(bar_ld, (uint32_t)Q * 256u + (uint32_t)HB * Q * 128u);
         for (int half = 0; half < 2; ++half)
             for (int r0 = 0; r0 < Q; r0 += R)
                 tc::tma_load_3d(sB + half * Q * 128 + r0 * 128, &prm.mb, bar_ld, g * kN + half * 64,
                                 (int)(t0 + r0), (int)b);
-        for (int r0 = 0; r0 < Q; r0 += R)
-            tc::tma_load_3d(sX + r0 * 128, &prm.mx, bar_ld, h * kP, (int)(t0 + r0), (int)b);
+        for (int k = 0; k < HB; ++k)
+            for (int r0 = 0; r0 < Q; r0 += R)
+                tc::tma_load_3d(sX + k * Q * 128 + r0 * 128, &prm.mx, bar_ld, (h0 + k) * kP, (int)(t0 + r0),
+                                (int)b);
     }
 
-    // in-chunk cumulative sum of dt*A while the tiles land
-    const __nv_bfloat16 *dt = static_cast<const __nv_bfloat16 *>(a.dt);
-    const float Ah = a.A[h];
-    for (int j = tid; j < Q; j += 128) {
-        const float d = (t0 + j < a.L) ? __bfloat162float(dt[(b * a.L + t0 + j) * a.H + h]) : 0.f;
-        s_dt[j] = d;
-        s_cs[j] = d * Ah;
+    // warp k: in-chunk cumulative sum of dt*A (base 2) of head k and its
+    // weights w_j; lane l owns Q/32 consecutive tokens
+    if (warp < HB) {
+        const __nv_bfloat16 *dt = static_cast<const __nv_bfloat16 *>(a.dt);
+        const int h = h0 + warp;
+        const float A2 = a.A[h] * kLog2e;
+        const int per = Q / 32;  // 2, 4 or 8
+        float dv[8], cs[8];
+        float run = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int j = lane * per + q;
+            dv[q] = (q < per && t0 + j < a.L) ? __bfloat162float(dt[(b * a.L + t0 + j) * a.H + h]) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            run += dv[q] * A2;
+            cs[q] = run;
+        }
+        float incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const float excl = incl - run;
+        const float cs_end = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < per) s_w[warp * 256 + lane * per + q] = tc::ex2(cs_end - (excl + cs[q])) * dv[q];
+        if (lane == 0) a.chunk_sum[(b * a.H + h) * a.nc + c] = tc::ex2(cs_end);  // decay over the chunk
     }
-    __syncthreads();
-    cta128_inclusive_scan(s_cs, Q, s_tot);
-    const float cs_end = s_cs[Q - 1];
-    for (int j = tid; j < Q; j += 128) s_w[j] = __expf(cs_end - s_cs[j]) * s_dt[j];
-    if (tid == 0) a.chunk_sum[(b * a.H + h) * a.nc + c] = cs_end;
 
     if (!tc::mbar_wait(bar_ld, 0, kWaitNs)) *s_fail = 1;
     __syncthreads();
     if (*s_fail) {
         if (tid == 0) record_failure(a.status);
     } else {
-        // x_j <- w_j x_j in place: a 128-byte row holds all 64 p of token j
-        for (int e = tid; e < Q * 8; e += 128) {
-            const int row = e >> 3;
+        // x_k,j <- w_k,j x_k,j in place (packed bf16 multiplies): a 128-byte row
+        // holds all 64 p of token j
+        for (int e = tid; e < HB * Q * 8; e += 256) {
+            const int row = e >> 3, k = row / Q, j = row - k * Q;
             uint4 *ptr = reinterpret_cast<uint4 *>(sX + row * 128 + (e & 7) * 16);
             uint4 v = *ptr;
-            const float w = s_w[row];
-            uint32_t *u = reinterpret_cast<uint32_t *>(&v);
+            const __nv_bfloat162 w2 = __float2bfloat162_rn(s_w[k * 256 + j]);
+            __nv_bfloat162 *u = reinterpret_cast<__nv_bfloat162 *>(&v);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                __nv_bfloat162 p2 = *reinterpret_cast<__nv_bfloat162 *>(&u[k]);
-                const float2 f = __bfloat1622float2(p2);
-                u[k] = pack_bf16x2(f.x * w, f.y * w);
-            }
+            for (int q = 0; q < 4; ++q) u[q] = __hmul2(u[q], w2);
             *ptr = v;
         }
         tc::fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc::tc_fence_after();
-            const uint32_t idesc = tc::idesc_bf16(128, kP, true, true);
+            const uint32_t idesc = tc::idesc_bf16(128, kP * HB, true, true);
             const uint32_t b0 = tc::smem_u32(sB), x0 = tc::smem_u32(sX);
             for (int k = 0; k < Q; k += 16) {
                 const uint64_t da = tc::sdesc_sw128(b0 + k * 128, Q * 128, 1024);
@@ -189,22 +217,26 @@ __global__ void __launch_bounds__(128) chunk_state_tc(const __grid_constant__ Tc
             if (tid == 0) record_failure(a.status);
         } else {
             tc::tc_fence_after();
-            // lane 32*warp + l of TMEM holds n = 32*warp + l; columns are p
-            float v[32];
-            const int n = warp * 32 + lane;
-            float *S = a.states + (((b * a.nc + c) * a.H + h) * kP) * kN;
+            // lane 32*(warp%4) + l of TMEM holds n; column 64 k + p. Warps w and
+            // w + 4 share a lane quarter and split the heads.
+            const int n = (warp & 3) * 32 + lane;
+            __nv_bfloat16 *S = reinterpret_cast<__nv_bfloat16 *>(a.states_bf16);
+            for (int k = warp >> 2; k < HB; k += 2) {
+                __nv_bfloat16 *Sk = S + (((b * a.nc + c) * a.H + h0 + k) * kP) * kN + n;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float v[32];
+                    tc::tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + k * 64 + half * 32, v);
+                    tc::tmem_ld_wait();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + half * 32, v);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 32; ++q) S[(half * 32 + q) * kN + n] = v[q];
+                    for (int q = 0; q < 32; ++q) Sk[(half * 32 + q) * kN] = __float2bfloat16_rn(v[q]);
+                }
             }
         }
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 64);
+    if (warp == 0) tc::tmem_dealloc(tmem, ncols);
     // let the state pass start its launch while this grid drains
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -480,7 +512,6 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 // SSD_ERR_TIMEOUT.
 
 constexpr int kHBMax = 4;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kScanPThreads = 352;  // 11 warps
 constexpr int kEpiThreads = 256;
 constexpr int kXStages = 4;
@@ -961,7 +992,7 @@ int device_cc_major() {
     return major;
 }
 
-size_t state_smem(int Q) { return (size_t)Q * 384 + 4096 + 1024; }
+size_t state_smem(int Q, int hb) { return (size_t)Q * 256 + (size_t)hb * Q * 128 + 8192 + 1024; }
 constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
 size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 8192 + 1024; }
@@ -1049,7 +1080,7 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)state_smem(256));
+                                             (int)state_smem(256, 2));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         if (e != cudaSuccess) return e;
@@ -1068,11 +1099,13 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
     const bool staged = a.stage_ev[0] != nullptr;  // per-stage timing: no programmatic overlap
     cudaError_t e = mark_stage(a, 0, stream);
     if (e != cudaSuccess) return e;
-    e = launch_ex(chunk_state_tc, dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), state_smem(a.Q), stream,
-                  false, ps);
+    // chunk state: groups of hb1 heads (hb1 * Q <= 512 keeps it within shared memory)
+    ps.hb = (a.Q <= 128 && hpg % 4 == 0) ? 4 : hpg % 2 == 0 ? 2 : 1;
+    e = launch_ex(chunk_state_tc, dim3((unsigned)a.nc, (unsigned)(a.H / ps.hb), (unsigned)a.B),
+                  state_smem(a.Q, ps.hb), stream, false, ps, 256);
     if (e != cudaSuccess) return e;
     if ((e = mark_stage(a, 1, stream)) != cudaSuccess) return e;
-    e = launch_state_pass(a, false, true, stream, !staged);
+    e = launch_state_pass(a, false, true, stream, !staged, /*bf16_in=*/true);
     if (e != cudaSuccess) return e;
     if ((e = mark_stage(a, 2, stream)) != cudaSuccess) return e;
     if (a.Q <= kRows) {

@@ -23,7 +23,7 @@ struct ChunkedArgs {
     int *status;             // device status word
     float *states;           // [B, nc, H, P, N] float32: chunk states, then entering states
     uint16_t *states_bf16;   // [B, nc, H, P, N] bfloat16 entering states (tensor-core path)
-    float *chunk_sum;        // [B, H, nc] float32: sum of dt*A over each chunk
+    float *chunk_sum;        // [B, H, nc] float32: decay over each chunk, exp(sum of dt*A)
     // optional stage timing: events[0..3] recorded before stage 1 and after
     // stages 1, 2, 3 (all NULL when not requested)
     cudaEvent_t stage_ev[4];
@@ -52,8 +52,11 @@ bool chunked_tc_supported(const ChunkedArgs &a);
 cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream);
 
 // State passing across chunks (shared by both paths).
+// bf16_in: the chunk states are bfloat16 in states_bf16 (tensor-core path) and
+// the entering states replace them in place; otherwise they are float32 in
+// states.
 cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool write_bf16,
-                              cudaStream_t stream, bool programmatic);
+                              cudaStream_t stream, bool programmatic, bool bf16_in = false);
 
 cudaError_t launch_diag(int io, int64_t B, int64_t L, int64_t Dm, int64_t N, const void *x, const void *dt,
                         const float *A, const void *Bm, const void *Cm, const float *D,
