@@ -362,53 +362,55 @@ cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
 }  // namespace
 
 // Tensor-core path: bfloat16 chunk states in states_bf16, replaced in place by
-// the bfloat16 entering states; 4 elements per thread. Up to kPFB chunks are
-// held packed (two registers per chunk) so that one round trip to L2 brings in
-// the whole chain of most workloads.
-constexpr int kPFB = 16;
+// the bfloat16 entering states; 2 elements per thread. Up to kPFB chunks are
+// loaded before the chain runs (one register per chunk), so that one round
+// trip to L2 brings in the whole chain of sequences up to kPFB chunks long.
+constexpr int kPFB = 32;
 
-__global__ void __launch_bounds__(kT, 2) state_pass_bf16_kernel(ChunkedArgs a) {
+__global__ void __launch_bounds__(kT, 3) state_pass_bf16_kernel(ChunkedArgs a) {
+    __shared__ float s_dA[kPFB];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t PN = a.P * a.N;
-    const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * 4;
+    const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * 2;
     const int h = blockIdx.y;
     const int64_t b = blockIdx.z;
-    if (e >= PN) return;
     const int64_t H = a.H, nc = a.nc;
-    float hv[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) hv[k] = a.init_state ? a.init_state[(b * H + h) * PN + e + k] : 0.f;
+    float h0 = 0.f, h1 = 0.f;
+    if (a.init_state && e < PN) {
+        const float2 v = *reinterpret_cast<const float2 *>(a.init_state + (b * H + h) * PN + e);
+        h0 = v.x;
+        h1 = v.y;
+    }
     const float *cs = a.chunk_sum + (b * H + h) * nc;
     const int64_t stride = H * PN;
-    const int64_t base = ((b * nc) * H + h) * PN + e;
+    __nv_bfloat16 *base = reinterpret_cast<__nv_bfloat16 *>(a.states_bf16) + ((b * nc) * H + h) * PN + e;
+    const bool act = e < PN;
     for (int64_t c0 = 0; c0 < nc; c0 += kPFB) {
-        uint2 raw[kPFB];
+        // the chunk decays of this (b, h), shared by the CTA
+        __syncthreads();
+        if (threadIdx.x < kPFB && c0 + threadIdx.x < nc) s_dA[threadIdx.x] = cs[c0 + threadIdx.x];
+        __syncthreads();
+        if (!act) continue;
+        uint32_t raw[kPFB];
 #pragma unroll
         for (int u = 0; u < kPFB; ++u)
-            if (c0 + u < nc) raw[u] = *reinterpret_cast<const uint2 *>(a.states_bf16 + base + (c0 + u) * stride);
+            if (c0 + u < nc) raw[u] = *reinterpret_cast<const uint32_t *>(base + (c0 + u) * stride);
 #pragma unroll
         for (int u = 0; u < kPFB; ++u) {
             if (c0 + u < nc) {
-                const int64_t idx = base + (c0 + u) * stride;
-                __nv_bfloat162 lo = __floats2bfloat162_rn(hv[0], hv[1]);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(hv[2], hv[3]);
-                *reinterpret_cast<uint2 *>(a.states_bf16 + idx) =
-                    make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-                const float dA = cs[c0 + u];
-                const float2 s01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u].x));
-                const float2 s23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u].y));
-                hv[0] = fmaf(dA, hv[0], s01.x);
-                hv[1] = fmaf(dA, hv[1], s01.y);
-                hv[2] = fmaf(dA, hv[2], s23.x);
-                hv[3] = fmaf(dA, hv[3], s23.y);
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+                *reinterpret_cast<__nv_bfloat162 *>(base + (c0 + u) * stride) = hv;
+                const float2 sv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u]));
+                const float dA = s_dA[u];
+                h0 = fmaf(dA, h0, sv.x);
+                h1 = fmaf(dA, h1, sv.y);
             }
         }
     }
-    if (a.final_state) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) a.final_state[(b * H + h) * PN + e + k] = hv[k];
-    }
+    if (!act) return;
+    if (a.final_state)
+        *reinterpret_cast<float2 *>(a.final_state + (b * H + h) * PN + e) = make_float2(h0, h1);
 }
 
 template <typename TIn, int VW>
@@ -429,8 +431,10 @@ cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool
     const int VW = vec ? 4 : 1;
     dim3 grid((unsigned)((PN / VW + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B);
     void (*kern)(ChunkedArgs);
-    if (bf16_in && vec && write_bf16 && !write_f32_inplace)
+    if (bf16_in && vec && write_bf16 && !write_f32_inplace) {
         kern = state_pass_bf16_kernel;
+        grid.x = (unsigned)((PN / 2 + kT - 1) / kT);
+    }
     else if (bf16_in)
         kern = vec ? pick_state_pass<__nv_bfloat16, 4>(write_f32_inplace, write_bf16)
                    : pick_state_pass<__nv_bfloat16, 1>(write_f32_inplace, write_bf16);

@@ -8,24 +8,27 @@
 // issuing the MMAs, 4 warps moving accumulators TMEM -> registers for the
 // epilogues. Decays, cumulative sums and exponentials stay float32.
 //
-//   chunk_state_tc  one CTA per (b, chunk c, head h):
-//       S_c^T[n, p] = sum_j B_j[n] * (w_j x_j[p]),  w_j = exp(cs_end - cs_j) dt_j
-//       one MMA chain M = 128 (n), N = 64 (p), K = Q (j); both operands
-//       MN-major (tokens are the outer dimension in HBM).
-//   state_pass      (shared with the CUDA-core path) writes the entering
-//       states as a bf16 copy, the B operand of the output MMA.
-//   chunk_scan_tc   one CTA per (b, 128-token tile, head h):
+//   chunk_state_tc  one CTA per (b, chunk c, group of hb heads sharing B):
+//       S_c^T[n, (k, p)] = sum_j B_j[n] * (w_k,j x_k,j[p]),
+//       w_k,j = exp(cs_end - cs_j) dt_j of head k; one MMA chain M = 128 (n),
+//       N = 64 hb, K = Q (j); both operands MN-major (tokens are the outer
+//       dimension in HBM). States leave as bfloat16, plus exp(cs_end).
+//   state_pass      (chunked_simt.cu) updates the bf16 states in place into the
+//       entering states h_in, the B operand of the output MMA.
+//   chunk_scan_tc_persistent  (Q <= 128) one CTA per SM over work items
+//       (b, 128-token tile, head group); warp-specialised, see its comment.
+//   chunk_scan_tc   (Q = 256) one CTA per (b, 128-token tile, head h):
 //       S  = C_tile B_k^T            (M = 128 rows i, N = 128 cols j, K = N)
 //       S' = S o exp(cs_i - cs_j) dt_j, static causal & same-chunk mask
 //       Y += S' X_k                  (M = 128, N = P, K = 128)  per K-block k
 //       Yo = C_tile h_in^T           (M = 128, N = P, K = N)    per chunk
 //       y  = Y + exp(cs_i - cs_chunk_start) Yo + D x  -> bf16 -> TMA store
 //   The K-blocks of a tile are the 128-token blocks from the start of the
-//   tile's chunk up to the tile (1 block for Q <= 128, 2 for the second half
-//   of a 256-token chunk); a 128-token tile holds two 64-token chunks.
+//   tile's chunk up to the tile (2 for the second half of a 256-token chunk).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 
@@ -89,6 +92,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // --------------------------------------------------------- chunk state
+
+// bytes of the operand space of chunk_state_tc: B^T and x
+__host__ __device__ constexpr int state_region(int Q, int hb) { return Q * 256 + hb * Q * 128; }
 //
 // One CTA per (b, chunk c, group of hb heads sharing a B/C group). All heads
 // of the group share the A operand B^T, so their chunk states come out of one
@@ -111,31 +117,25 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sB = smem;                    // B^T operand: 2 panels (n 0-63, 64-127) x Q rows x 128 B
     uint8_t *sX = smem + Q * 256;          // x operands of the hb heads: hb panels of Q rows x 128 B
-    float *s_w = reinterpret_cast<float *>(sX + HB * Q * 128);  // [hb][Q]
-    float *s_cs = s_w + 4 * 256;                                // [Q] scratch of the cumulative sum
-    float *s_dt = s_cs + 256;                                   // [Q]
-    float *s_tot = s_dt + 256;
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_tot + 8);
+    float *s_w = reinterpret_cast<float *>(smem + state_region(Q, HB));  // [hb][256]
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_w + 4 * 256);
     uint64_t *bar_mma = bar_ld + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
     int *s_fail = reinterpret_cast<int *>(tmem_slot + 1);
     const uint32_t ncols = HB == 4 ? 256u : HB == 2 ? 128u : 64u;
 
+    // TMEM first: until a CTA has given up its allocation permit, no other
+    // CTA is placed on its SM
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, ncols);
+        tc::tmem_relinquish();
+    }
+    // B^T and x by TMA; the cumulative sums and the CTA barrier overlap the loads
     if (tid == 0) {
         tc::mbar_init(bar_ld, 1);
         tc::mbar_init(bar_mma, 1);
         tc::fence_mbar_init();
         *s_fail = 0;
-    }
-    if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, ncols);
-        tc::tmem_relinquish();
-    }
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (tid == 0) {
         tc::mbar_arrive_expect_tx(bar_ld, (uint32_t)Q * 256u + (uint32_t)HB * Q * 128u);
         for (int half = 0; half < 2; ++half)
             for (int r0 = 0; r0 < Q; r0 += R)
@@ -146,21 +146,26 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
                 tc::tma_load_3d(sX + k * Q * 128 + r0 * 128, &prm.mx, bar_ld, (h0 + k) * kP, (int)(t0 + r0),
                                 (int)b);
     }
+    // warps < hb: dt of head h0 + warp, lane l owning Q/32 consecutive tokens
+    float dv[8];
+    if (warp < HB) {
+        const __nv_bfloat16 *dt = static_cast<const __nv_bfloat16 *>(a.dt);
+        const int per = Q / 32;  // 2, 4 or 8
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int j = lane * per + q;
+            dv[q] = (q < per && t0 + j < a.L) ? __bfloat162float(dt[(b * a.L + t0 + j) * a.H + h0 + warp]) : 0.f;
+        }
+    }
 
     // warp k: in-chunk cumulative sum of dt*A (base 2) of head k and its
     // weights w_j; lane l owns Q/32 consecutive tokens
     if (warp < HB) {
-        const __nv_bfloat16 *dt = static_cast<const __nv_bfloat16 *>(a.dt);
         const int h = h0 + warp;
         const float A2 = a.A[h] * kLog2e;
-        const int per = Q / 32;  // 2, 4 or 8
-        float dv[8], cs[8];
+        const int per = Q / 32;
+        float cs[8];
         float run = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int j = lane * per + q;
-            dv[q] = (q < per && t0 + j < a.L) ? __bfloat162float(dt[(b * a.L + t0 + j) * a.H + h]) : 0.f;
-        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             run += dv[q] * A2;
@@ -180,25 +185,34 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
         if (lane == 0) a.chunk_sum[(b * a.H + h) * a.nc + c] = tc::ex2(cs_end);  // decay over the chunk
     }
 
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
     if (!tc::mbar_wait(bar_ld, 0, kWaitNs)) *s_fail = 1;
     __syncthreads();
-    if (*s_fail) {
-        if (tid == 0) record_failure(a.status);
-    } else {
-        // x_k,j <- w_k,j x_k,j in place (packed bf16 multiplies): a 128-byte row
-        // holds all 64 p of token j
-        for (int e = tid; e < HB * Q * 8; e += 256) {
-            const int row = e >> 3, k = row / Q, j = row - k * Q;
-            uint4 *ptr = reinterpret_cast<uint4 *>(sX + row * 128 + (e & 7) * 16);
+    if (!*s_fail) {
+        // x_k,j <- w_k,j x_k,j in place (packed bf16 multiplies). Thread t
+        // takes 16-byte piece t & 7 of rows r = t / 8 + 32 i (row r = k Q + j
+        // holds all 64 p of token j of head k); the swizzle only permutes the
+        // pieces within a row.
+        const int lq = Q == 64 ? 6 : Q == 128 ? 7 : 8;
+        const int rows = HB * Q;
+        for (int r = tid >> 3; r < rows; r += 32) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(sX + r * 128 + (tid & 7) * 16);
             uint4 v = *ptr;
-            const __nv_bfloat162 w2 = __float2bfloat162_rn(s_w[k * 256 + j]);
+            const __nv_bfloat162 w2 = __float2bfloat162_rn(s_w[(r >> lq) * 256 + (r & (Q - 1))]);
             __nv_bfloat162 *u = reinterpret_cast<__nv_bfloat162 *>(&v);
 #pragma unroll
             for (int q = 0; q < 4; ++q) u[q] = __hmul2(u[q], w2);
             *ptr = v;
         }
         tc::fence_proxy_async_smem();
-        __syncthreads();
+    }
+    __syncthreads();
+    if (*s_fail) {
+        if (tid == 0) record_failure(a.status);
+    } else {
         if (tid == 0) {
             tc::tc_fence_after();
             const uint32_t idesc = tc::idesc_bf16(128, kP * HB, true, true);
@@ -236,7 +250,7 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, ncols);
+    if (warp == 1) tc::tmem_dealloc(tmem, ncols);
     // let the state pass start its launch while this grid drains
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -512,7 +526,7 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 // SSD_ERR_TIMEOUT.
 
 constexpr int kHBMax = 4;
-constexpr int kScanPThreads = 352;  // 11 warps
+constexpr int kScanPThreads = 384;  // 12 warps
 constexpr int kEpiThreads = 256;
 constexpr int kXStages = 4;
 
@@ -531,11 +545,6 @@ __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile i
     }
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-__device__ __forceinline__ float pick4(const float (&v)[kHBMax], int k) {
-    return k == 0 ? v[0] : k == 1 ? v[1] : k == 2 ? v[2] : v[3];
-}
 
 __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(const __grid_constant__ TcParams prm) {
     const ChunkedArgs &a = prm.a;
@@ -553,21 +562,50 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     uint8_t *sB = smem + 32768;          // B tile, K-major, 2 panels
     uint8_t *sX = smem + 65536;          // x ring: kXStages x 16 KB, MN-major
     uint8_t *sH = sX + kXStages * 16384; // entering states: per chunk s, 2 panels of 64 hb rows (K-major, N = (k, p))
-    float *s_cs = reinterpret_cast<float *>(sH + 65536);  // [kHBMax][128]
-    float *s_dt = s_cs + kHBMax * 128;                    // [kHBMax][128]
-    float *s_colf = s_dt + kHBMax * 128;                  // [kHBMax][128]
-    float *s_tot = s_colf + kHBMax * 128;                 // [kHBMax][4]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s_tot + kHBMax * 4);
+    // per-item scalars of every row and head, double-buffered by item:
+    // [2][kScal] floats = cs | dt | colf | sc, each [kHBMax][128], then D [kHBMax]
+    constexpr int kScal = 4 * kHBMax * 128 + kHBMax;
+    float *s_scal = reinterpret_cast<float *>(sH + 65536);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_scal + 2 * kScal + 4);
     uint64_t *tile_full = bars + 0, *tile_empty = bars + 1;
     uint64_t *h_full = bars + 2, *h_empty = bars + 3;
     uint64_t *s_full = bars + 4, *s_empty = bars + 5;
     uint64_t *yo_full = bars + 6, *acc_empty = bars + 7;
-    uint64_t *y_full = bars + 8;
-    uint64_t *p_full = bars + 9, *p_empty = bars + 11;                  // [2] each
-    uint64_t *x_full = bars + 13, *x_empty = bars + 13 + kXStages;      // [kXStages] each
-    constexpr int kBars = 13 + 2 * kXStages;
+    uint64_t *y_full = bars + 8;                                        // [2]
+    uint64_t *p_full = bars + 10, *p_empty = bars + 12;                 // [2] each
+    uint64_t *x_full = bars + 14, *x_empty = bars + 14 + kXStages;      // [kXStages] each
+    uint64_t *c_full = bars + 14 + 2 * kXStages, *c_empty = c_full + 2;  // [2] each
+    constexpr int kBars = 18 + 2 * kXStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int hpg = (int)(a.H / a.G);  // heads per B/C group
+    auto decode = [&](int64_t u, int64_t &b, int64_t &tile, int &hg) {
+        hg = (int)(u % nhg);
+        const int64_t t = u / nhg;
+        tile = t % ntiles;
+        b = t / ntiles;
+    };
+    // C and B of item u; returns the x column of its first head, the tile's
+    // first token and the sequence, for load_x
+    auto issue_tile = [&](int64_t u, int &xcol, int &t0, int &bb) {
+        int64_t b, tile;
+        int hg;
+        decode(u, b, tile, hg);
+        t0 = (int)(tile * kRows);
+        bb = (int)b;
+        xcol = hg * HB * kP;
+        const int g = hg * HB / hpg;
+        tc::mbar_arrive_expect_tx(tile_full, 65536u);
+        tc::tma_load_3d(sC, &prm.mc, tile_full, g * kN, t0, bb);
+        tc::tma_load_3d(sC + 16384, &prm.mc, tile_full, g * kN + 64, t0, bb);
+        tc::tma_load_3d(sB, &prm.mb, tile_full, g * kN, t0, bb);
+        tc::tma_load_3d(sB + 16384, &prm.mb, tile_full, g * kN + 64, t0, bb);
+    };
+    auto load_x = [&](int xcol, int t0, int bb, uint32_t x) {
+        tc::mbar_arrive_expect_tx(&x_full[x], 16384u);
+        tc::tma_load_3d(sX + x * 16384, &prm.mx, &x_full[x], xcol, t0, bb);
+    };
 
     if (tid == 0) {
         for (int k = 0; k < kBars; ++k) tc::mbar_init(bars + k, 1);
@@ -575,8 +613,17 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         tc::mbar_init(acc_empty, kEpiThreads);
         tc::mbar_init(p_full + 0, kEpiThreads);
         tc::mbar_init(p_full + 1, kEpiThreads);
+        tc::mbar_init(c_empty + 0, kEpiThreads);
+        tc::mbar_init(c_empty + 1, kEpiThreads);
         tc::fence_mbar_init();
         *s_fail = 0;
+        // the first item's operands (the x ring starts empty and holds every
+        // head of an item) go out before the TMEM allocation and the CTA barrier
+        if (blockIdx.x < n_items) {
+            int xcol, t0, bb;
+            issue_tile(blockIdx.x, xcol, t0, bb);
+            for (int k = 0; k < HB; ++k) load_x(xcol + k * kP, t0, bb, (uint32_t)k);
+        }
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, 512);
@@ -586,36 +633,20 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem, tAcc = tmem + 128, tP = tmem + 384;
-    const int hpg = (int)(a.H / a.G);  // heads per B/C group
-
-    auto decode = [&](int64_t u, int64_t &b, int64_t &tile, int &hg) {
-        hg = (int)(u % nhg);
-        const int64_t t = u / nhg;
-        tile = t % ntiles;
-        b = t / ntiles;
-    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t tcnt = 0, xi = 0, xph = 0;
-            for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
-                int64_t b, tile;
-                int hg;
-                decode(u, b, tile, hg);
-                const int t0 = (int)(tile * kRows);
-                const int g = hg * HB / hpg;
+            // the first item went out before the CTA barrier
+            uint32_t tcnt = 1, xi = (uint32_t)HB % kXStages, xph = HB == kXStages ? 1u : 0u;
+            for (int64_t u = blockIdx.x + gridDim.x; u < n_items && !*s_fail; u += gridDim.x) {
                 if (!pwait(tile_empty, (tcnt & 1) ^ 1, s_fail)) break;
                 ++tcnt;
-                tc::mbar_arrive_expect_tx(tile_full, 65536u);
-                tc::tma_load_3d(sC, &prm.mc, tile_full, g * kN, t0, (int)b);
-                tc::tma_load_3d(sC + 16384, &prm.mc, tile_full, g * kN + 64, t0, (int)b);
-                tc::tma_load_3d(sB, &prm.mb, tile_full, g * kN, t0, (int)b);
-                tc::tma_load_3d(sB + 16384, &prm.mb, tile_full, g * kN + 64, t0, (int)b);
+                int xcol, t0, bb;
+                issue_tile(u, xcol, t0, bb);
                 for (int k = 0; k < HB; ++k) {
                     if (!pwait(&x_empty[xi], xph ^ 1, s_fail)) break;
-                    tc::mbar_arrive_expect_tx(&x_full[xi], 16384u);
-                    tc::tma_load_3d(sX + xi * 16384, &prm.mx, &x_full[xi], (hg * HB + k) * kP, t0, (int)b);
+                    load_x(xcol + k * kP, t0, bb, xi);
                     if (++xi == kXStages) { xi = 0; xph ^= 1; }
                 }
             }
@@ -643,6 +674,71 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                     }
                 }
             }
+        }
+    } else if (warp == 11) {
+        // ------------------ per-item scalars, one item ahead of the epilogue
+        // For every head k of the item and tile row i (base-2 units):
+        //   cs   inclusive cumulative sum of dt*A over the tile's rows
+        //   colf exp(cs at the end of row i's 32-row block - cs_i) * dt_i
+        //   sc   exp(cs_i - cs at the start of row i's chunk)
+        // Lane l owns rows 4l .. 4l + 3.
+        const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
+        uint32_t ci = 0;
+        for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x, ++ci) {
+            int64_t b, tile;
+            int hg;
+            decode(u, b, tile, hg);
+            const int64_t t0 = tile * kRows;
+            float dv[kHBMax][4];
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t t = t0 + 4 * lane + q;
+                    dv[k][q] = (k < HB && t < a.L) ? __bfloat162float(dtp[(b * a.L + t) * a.H + hg * HB + k]) : 0.f;
+                }
+            const uint32_t buf = ci & 1;
+            if (!pwait(&c_empty[buf], ((ci >> 1) & 1) ^ 1, s_fail)) break;
+            float *cs_ = s_scal + buf * kScal, *dt_ = cs_ + kHBMax * 128, *cf_ = dt_ + kHBMax * 128;
+            float *sc_ = cf_ + kHBMax * 128, *D_ = sc_ + kHBMax * 128;
+#pragma unroll
+            for (int k = 0; k < kHBMax; ++k) {
+                if (k < HB) {
+                    const int h = hg * HB + k;
+                    const float A2 = a.A[h] * kLog2e;
+                    float c[4], run = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        run += dv[k][q] * A2;
+                        c[q] = run;
+                    }
+                    float incl = run;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float w = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += w;
+                    }
+                    const float excl = incl - run;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) c[q] += excl;
+                    const float blk_end = __shfl_sync(0xffffffffu, c[3], lane | 7);
+                    const float mid = __shfl_sync(0xffffffffu, c[3], 15);  // end of the first 64 rows
+                    const float c0 = (Q < kRows && lane >= 16) ? mid : 0.f;
+                    float4 vcs, vdt, vcf, vsc;
+                    vcs = make_float4(c[0], c[1], c[2], c[3]);
+                    vdt = make_float4(dv[k][0], dv[k][1], dv[k][2], dv[k][3]);
+                    vcf = make_float4(tc::ex2(blk_end - c[0]) * dv[k][0], tc::ex2(blk_end - c[1]) * dv[k][1],
+                                      tc::ex2(blk_end - c[2]) * dv[k][2], tc::ex2(blk_end - c[3]) * dv[k][3]);
+                    vsc = make_float4(tc::ex2(c[0] - c0), tc::ex2(c[1] - c0), tc::ex2(c[2] - c0), tc::ex2(c[3] - c0));
+                    reinterpret_cast<float4 *>(cs_ + k * 128)[lane] = vcs;
+                    reinterpret_cast<float4 *>(dt_ + k * 128)[lane] = vdt;
+                    reinterpret_cast<float4 *>(cf_ + k * 128)[lane] = vcf;
+                    reinterpret_cast<float4 *>(sc_ + k * 128)[lane] = vsc;
+                    if (lane == 0) D_[k] = a.D ? a.D[h] : 0.f;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&c_full[buf]);
         }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer
@@ -695,7 +791,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                     }
                     tc::mma_commit(&p_empty[pb]);
                     tc::mma_commit(&x_empty[xi]);
-                    tc::mma_commit(y_full);
+                    tc::mma_commit(&y_full[pb]);
                     if (++xi == kXStages) { xi = 0; xph ^= 1; }
                 }
             }
@@ -707,72 +803,20 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         const int qd = warp & 3;            // TMEM lane quarter of this warp
         const int i = qd * 32 + lane;       // tile row
         const uint32_t lq = (uint32_t)(qd * 32) << 16;
-        const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
         const int Ja = grp == 0 ? 0 : 1, Jb = grp == 0 ? 3 : 2;  // this group's column blocks of S'
         const int sub = (Q < kRows && i >= Q) ? 1 : 0;           // chunk of this row inside the tile
-        uint32_t sph = 0, yoph = 0, ycnt = 0, nh = 0;
+        uint32_t sph = 0, yoph = 0, nh = 0, ci = 0;
 
-        // per-item scalars of this thread's row, loaded one item ahead
-        float dtv[kHBMax], Av[kHBMax], Dv[kHBMax];
-        auto fetch = [&](int64_t u) {
-#pragma unroll
-            for (int k = 0; k < kHBMax; ++k) { dtv[k] = 0.f; Av[k] = 0.f; Dv[k] = 0.f; }
-            if (u >= n_items) return;
+        for (int64_t u = blockIdx.x; u < n_items; u += gridDim.x, ++ci) {
             int64_t b, tile;
             int hg;
             decode(u, b, tile, hg);
             const int64_t t0 = tile * kRows;
-            const bool row_in = t0 + i < a.L;
-#pragma unroll
-            for (int k = 0; k < kHBMax; ++k) {
-                if (k < HB) {
-                    const int h = hg * HB + k;
-                    dtv[k] = row_in ? __bfloat162float(dtp[(b * a.L + t0 + i) * a.H + h]) : 0.f;
-                    Av[k] = a.A[h];
-                    Dv[k] = a.D ? a.D[h] : 0.f;
-                }
-            }
-        };
-        fetch(blockIdx.x);
-        for (int64_t u = blockIdx.x; u < n_items; u += gridDim.x) {
-            int64_t b, tile;
-            int hg;
-            decode(u, b, tile, hg);
-            const int64_t t0 = tile * kRows;
-            float dcur[kHBMax], Acur[kHBMax], Dcur[kHBMax];
-#pragma unroll
-            for (int k = 0; k < kHBMax; ++k) { dcur[k] = dtv[k]; Acur[k] = Av[k]; Dcur[k] = Dv[k]; }
-            fetch(u + gridDim.x);  // next item's scalars, consumed one item later
-
-            // cumulative sums (base-2 units) of every head of the item
-            float csv[kHBMax], scv[kHBMax], incl[kHBMax], wtot[kHBMax];
-#pragma unroll
-            for (int k = 0; k < kHBMax; ++k) {
-                float v = dcur[k] * (Acur[k] * kLog2e);
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float w = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += w;
-                }
-                incl[k] = v;
-                wtot[k] = __shfl_sync(0xffffffffu, v, 31);
-                if (grp == 0 && lane == 31) s_tot[k * 4 + qd] = v;
-            }
-            epi_sync();
-#pragma unroll
-            for (int k = 0; k < kHBMax; ++k) {
-                float base = 0.f;
-                for (int w = 0; w < qd; ++w) base += s_tot[k * 4 + w];
-                csv[k] = base + incl[k];
-                const float bse = sub ? s_tot[k * 4 + 0] + s_tot[k * 4 + 1] : 0.f;  // end of the first 64-token chunk
-                scv[k] = tc::ex2(csv[k] - bse);
-                if (grp == 0 && k < HB) {
-                    s_cs[k * 128 + i] = csv[k];
-                    s_dt[k * 128 + i] = dcur[k];
-                    s_colf[k * 128 + i] = tc::ex2(base + wtot[k] - csv[k]) * dcur[k];  // decay from i to i|31, times dt_i
-                }
-            }
-            epi_sync();
+            // the item's cumulative sums and decays, from the scalar warp
+            const uint32_t buf = ci & 1;
+            pwait(&c_full[buf], (ci >> 1) & 1, s_fail);
+            const float *s_cs = s_scal + buf * kScal, *s_dt = s_cs + kHBMax * 128, *s_colf = s_dt + kHBMax * 128;
+            const float *s_sc = s_colf + kHBMax * 128, *s_D = s_sc + kHBMax * 128;
             pwait(s_full, sph, s_fail);
             sph ^= 1;
             pwait(yo_full, yoph, s_fail);
@@ -783,8 +827,8 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             // Yo'(k) = exp(cs_i - cs_chunk_start) Yo(sub(i), k) into the columns
             // of Yo(0, k), where MMA2 accumulates S'(k) X_k onto it
             auto prepare = [&](int k, uint32_t n) {
-                const float cs_i = pick4(csv, k), Dh = pick4(Dcur, k), sc = pick4(scv, k);
                 const float *cs_ = s_cs + k * 128, *dt_ = s_dt + k * 128, *cf_ = s_colf + k * 128;
+                const float cs_i = cs_[i], Dh = s_D[k], sc = s_sc[k * 128 + i];
                 pwait(&p_empty[n & 1], ((n >> 1) & 1) ^ 1, s_fail);
                 tc::tc_fence_after();
                 const int Jd = qd;
@@ -835,10 +879,12 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                 if (k == HB - 1) tc::mbar_arrive(s_empty);  // S fully read for this item
                 tc::mbar_arrive(&p_full[n & 1]);
             };
-            // y(k) = Y(k): this warp's 32 rows x the 32 columns p in [32 grp, 32 grp + 32)
-            auto yout = [&](int k) {
-                pwait(y_full, ycnt & 1, s_fail);
-                ++ycnt;
+            // y(k) = Y(k): this warp's 32 rows x the 32 columns p in [32 grp, 32 grp + 32).
+            // Head n completes y_full[n & 1]; the MMA of head n + 2 needs
+            // prepare(n + 2), which every thread runs after yout(n), so a
+            // barrier is never two phases ahead of its waiter.
+            auto yout = [&](int k, uint32_t n) {
+                pwait(&y_full[n & 1], (n >> 1) & 1, s_fail);
                 tc::tc_fence_after();
                 float yv[32];
                 tc::tmem_ld32(tAcc + lq + k * 64 + 32 * grp, yv);
@@ -860,10 +906,11 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
 #pragma unroll 1
             for (int k = 0; k <= HB; ++k) {
                 if (k < HB) prepare(k, nh + k);
-                if (k >= 1) yout(k - 1);
+                if (k >= 1) yout(k - 1, nh + k - 1);
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(acc_empty);  // every accumulator of this item has been read
+            tc::mbar_arrive(acc_empty);     // every accumulator of this item has been read
+            tc::mbar_arrive(&c_empty[buf]);  // and every scalar
             nh += HB;
         }
         tc::tc_fence_before();
@@ -992,10 +1039,10 @@ int device_cc_major() {
     return major;
 }
 
-size_t state_smem(int Q, int hb) { return (size_t)Q * 256 + (size_t)hb * Q * 128 + 8192 + 1024; }
+size_t state_smem(int Q, int hb) { return (size_t)state_region(Q, hb) + 4096 + 64 + 1024; }
 constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
-size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 8192 + 1024; }
+size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 2 * (4 * kHBMax * 128 + kHBMax) * 4 + 16 + 512 + 1024; }
 
 int num_sms() {
     static int n = 0;
@@ -1087,13 +1134,32 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
         e = cudaFuncSetAttribute(chunk_scan_tc_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)scanp_smem(64));
         if (e != cudaSuccess) return e;
+        // all of the unified L1 / shared memory as shared memory, so that two
+        // chunk-state CTAs fit on an SM from the start
+        for (const void *f : {(const void *)chunk_state_tc, (const void *)chunk_scan_tc,
+                              (const void *)chunk_scan_tc_persistent}) {
+            e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+        }
         configured = true;
     }
     // persistent chunk scan for Q <= 128: head groups of hb heads sharing a B/C
-    // group, at most 4 / (chunks per tile) so that their accumulators fit TMEM
+    // group, at most 4 / (chunks per tile) so that their accumulators fit TMEM.
+    // An item costs about one head's epilogue of fixed work plus one per head,
+    // and the busiest SM runs ceil(items / SMs) of them: take the hb that
+    // minimises that product (ties to the larger hb).
     const int hpg = (int)(a.H / a.G);
     const int hbmax = a.Q >= kRows ? 4 : 2;
-    p.hb = (hbmax >= 4 && hpg % 4 == 0) ? 4 : hpg % 2 == 0 ? 2 : 1;
+    {
+        int64_t best = INT64_MAX;
+        for (int hb = hbmax; hb >= 1; --hb) {
+            if (hpg % hb) continue;
+            const int64_t items = a.B * ntiles * (a.H / hb);
+            const int64_t cost = (items + num_sms() - 1) / num_sms() * (1 + hb);
+            if (cost < best) { best = cost; p.hb = hb; }
+        }
+    }
     p.nhg = (int)(a.H / p.hb);
     p.n_items = a.B * ntiles * p.nhg;
     const bool staged = a.stage_ev[0] != nullptr;  // per-stage timing: no programmatic overlap

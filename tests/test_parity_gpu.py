@@ -313,3 +313,23 @@ def test_workspace_status_ok_after_tensor_core_scan(ssd):
     ssd.ssd_scan_chunked(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
                          dev(d["D"]), None, chunk_size=128, workspace=ws)
     assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_tensor_core_scan_repeated_no_timeouts(ssd, chunk):
+    """Hundreds of back-to-back tensor-core scans of the 130M-shaped layer: no
+    bounded wait may expire (a lost barrier phase would), and every repetition
+    gives the same bits."""
+    w = inputs.WORKLOADS["ssd_m2_130m_L4096"]
+    Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=3)
+    t = torch.bfloat16
+    args = [dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t), dev(d["D"]), None]
+    ws = torch.empty(ssd.ssd_workspace_size(Bz, L, H, P, N, G, t, chunk), dtype=torch.uint8, device="cuda")
+    y0, h0 = ssd.ssd_scan_chunked(*args, chunk_size=chunk, workspace=ws)
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
+    y, h = torch.empty_like(y0), torch.empty_like(h0)
+    for rep in range(150):
+        ssd.ssd_scan_chunked(*args, chunk_size=chunk, y=y, final_state=h, workspace=ws)
+        assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK, f"bounded wait expired in repetition {rep}"
+    assert torch.equal(y, y0) and torch.equal(h, h0)
