@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "ssd_scan.h"
 
 namespace ssd {
 namespace {
@@ -43,6 +44,8 @@ __device__ __forceinline__ void chunk_cumsum(const T *__restrict__ dt, int64_t b
 // S_c for one (b, c, h) and one 64x64 tile of (p, n).
 template <typename T>
 __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP, int tilesN) {
+    // this call's status word starts clear (the first kernel of the call)
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) *a.status = SSD_OK;
     const int c = blockIdx.x;
     const int tiles = tilesP * tilesN;
     const int h = blockIdx.y / tiles, pt = (blockIdx.y % tiles) / tilesN, nt = blockIdx.y % tilesN;
@@ -112,6 +115,8 @@ constexpr int kPF = 8;
 
 template <typename TIn, bool F32_INPLACE, bool BF16, int VW>
 __global__ void __launch_bounds__(kT, 2) state_pass_kernel(ChunkedArgs a) {
+    // with no tokens this is the call's first kernel: clear its status word
+    if (a.nc == 0 && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) *a.status = SSD_OK;
     // Wait for the producer of the chunk states when launched as a programmatic
     // dependent of it; a no-op for an ordinary launch.
     asm volatile("griddepcontrol.wait;" ::: "memory");

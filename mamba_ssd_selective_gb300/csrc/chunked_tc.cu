@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
         tc::tmem_alloc(tmem_slot, ncols);
         tc::tmem_relinquish();
     }
+    // this call's status word starts clear (the first kernel of the call)
+    if (tid == 32 && c == 0 && hg == 0 && b == 0) *a.status = SSD_OK;
     // B^T and x by TMA; the cumulative sums and the CTA barrier overlap the loads
     if (tid == 0) {
         tc::mbar_init(bar_ld, 1);
@@ -526,8 +528,9 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 // SSD_ERR_TIMEOUT.
 
 constexpr int kHBMax = 4;
-constexpr int kScanPThreads = 384;  // 12 warps
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarp0 = 4;                        // first epilogue warp
+constexpr int kEpiThreads = 512;                    // 16 epilogue warps
+constexpr int kScanPThreads = 32 * kEpiWarp0 + kEpiThreads;  // 20 warps
 constexpr int kXStages = 4;
 
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *fail) {
@@ -651,7 +654,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                 }
             }
         }
-    } else if (warp == 10) {
+    } else if (warp == 2) {
         // ------------------------------ TMA producer of entering states
         if (lane == 0) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                 }
             }
         }
-    } else if (warp == 11) {
+    } else if (warp == 3) {
         // ------------------ per-item scalars, one item ahead of the epilogue
         // For every head k of the item and tile row i (base-2 units):
         //   cs   inclusive cumulative sum of dt*A over the tile's rows
@@ -798,13 +801,28 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int ew = warp - 2;            // 0 .. 7
-        const int grp = ew >> 2;            // column group
-        const int qd = warp & 3;            // TMEM lane quarter of this warp
+        // 16 warps: TMEM lane quarter qd = warp % 4 (rows 32 qd .. 32 qd + 31)
+        // and column group grp. Per head, warp (qd, grp) owns block J = grp
+        // (32 columns j) of S' for its rows and the 16 columns p in
+        // [16 grp, 16 grp + 16) of the entering-state term and of y.
+        const int grp = (warp - kEpiWarp0) >> 2;
+        const int qd = warp & 3;
         const int i = qd * 32 + lane;       // tile row
         const uint32_t lq = (uint32_t)(qd * 32) << 16;
-        const int Ja = grp == 0 ? 0 : 1, Jb = grp == 0 ? 3 : 2;  // this group's column blocks of S'
-        const int sub = (Q < kRows && i >= Q) ? 1 : 0;           // chunk of this row inside the tile
+        const int J = grp;
+        const int sub = (Q < kRows && i >= Q) ? 1 : 0;  // chunk of this row inside the tile
+        // blocks of S' that are zero for every head (after this warp's rows, or
+        // in the other 64-token chunk of the tile) are written once, here
+        const bool zero_blk = J > qd || (Q < kRows && (J >> 1) != (qd >> 1));
+        const bool diag_blk = J == qd;
+        if (zero_blk) {
+            uint32_t z[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) z[q] = 0u;
+            tc::tmem_st16(tP + lq + J * 16, z);
+            tc::tmem_st16(tP + lq + 64 + J * 16, z);
+            tc::tmem_st_wait();
+        }
         uint32_t sph = 0, yoph = 0, nh = 0, ci = 0;
 
         for (int64_t u = blockIdx.x; u < n_items; u += gridDim.x, ++ci) {
@@ -823,77 +841,66 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             yoph ^= 1;
             tc::tc_fence_after();
 
-            // S'(k) into TMEM buffer n & 1, and the rescaled entering-state term
-            // Yo'(k) = exp(cs_i - cs_chunk_start) Yo(sub(i), k) into the columns
-            // of Yo(0, k), where MMA2 accumulates S'(k) X_k onto it
+            // S'(k) block J into TMEM buffer n & 1, and the rescaled entering-state
+            // term Yo'(k) = exp(cs_i - cs_chunk_start) Yo(sub(i), k) into the
+            // columns of Yo(0, k), where MMA2 accumulates S'(k) X_k onto it
             auto prepare = [&](int k, uint32_t n) {
                 const float *cs_ = s_cs + k * 128, *dt_ = s_dt + k * 128, *cf_ = s_colf + k * 128;
                 const float cs_i = cs_[i], Dh = s_D[k], sc = s_sc[k * 128 + i];
                 pwait(&p_empty[n & 1], ((n >> 1) & 1) ^ 1, s_fail);
                 tc::tc_fence_after();
-                const int Jd = qd;
-#pragma unroll 1
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int J = jj == 0 ? Ja : Jb;
+                if (!zero_blk) {
                     float v[32];
-                    if (J < Jd) {
-                        // block before this warp's rows: factorised decay
-                        tc::tmem_ld32(tS + lq + J * 32, v);
-                        tc::tmem_ld_wait();
-                        const bool same = Q >= kRows || (J >> 1) == (Jd >> 1);
-                        const float rf = same ? tc::ex2(cs_i - cs_[J * 32 + 31]) : 0.f;
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * cf_[J * 32 + q];
-                    } else if (J == Jd) {
-                        // block holding this warp's rows: exact decay, causal mask, D on the diagonal
-                        tc::tmem_ld32(tS + lq + J * 32, v);
-                        tc::tmem_ld_wait();
+                    tc::tmem_ld32(tS + lq + J * 32, v);
+                    tc::tmem_ld_wait();
+                    if (diag_blk) {
+                        // exact decay, causal mask, D on the diagonal
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             const int jr = J * 32 + q;
                             const float e = tc::ex2(fminf(cs_i - cs_[jr], 0.f)) * dt_[jr];
-                            float f = jr <= i ? v[q] * e : 0.f;
-                            f += jr == i ? Dh : 0.f;
+                            float f = q <= lane ? v[q] * e : 0.f;
+                            f += q == lane ? Dh : 0.f;
                             v[q] = f;
                         }
                     } else {
+                        // block before this warp's rows: factorised decay
+                        const float rf = tc::ex2(cs_i - cs_[J * 32 + 31]);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) v[q] = 0.f;
+                        for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * cf_[J * 32 + q];
                     }
                     uint32_t pkd[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) pkd[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
                     tc::tmem_st16(tP + lq + (n & 1) * 64 + J * 16, pkd);
                 }
-                {
-                    float ov[32];
-                    tc::tmem_ld32(tAcc + lq + (sub * HB + k) * 64 + 32 * grp, ov);
-                    tc::tmem_ld_wait();
-                    uint32_t r[32];
+                float ov[16];
+                tc::tmem_ld16(tAcc + lq + (sub * HB + k) * 64 + 16 * grp, ov);
+                tc::tmem_ld_wait();
+                uint32_t r[16];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(sc * ov[q]);
-                    tc::tmem_st32(tAcc + lq + k * 64 + 32 * grp, r);
-                }
+                for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(sc * ov[q]);
+                tc::tmem_st16(tAcc + lq + k * 64 + 16 * grp, r);
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 if (k == HB - 1) tc::mbar_arrive(s_empty);  // S fully read for this item
                 tc::mbar_arrive(&p_full[n & 1]);
             };
-            // y(k) = Y(k): this warp's 32 rows x the 32 columns p in [32 grp, 32 grp + 32).
+            // y(k) = Y(k): this warp's 32 rows x the 16 columns p in [16 grp, 16 grp + 16).
             // Head n completes y_full[n & 1]; the MMA of head n + 2 needs
             // prepare(n + 2), which every thread runs after yout(n), so a
             // barrier is never two phases ahead of its waiter.
             auto yout = [&](int k, uint32_t n) {
                 pwait(&y_full[n & 1], (n >> 1) & 1, s_fail);
                 tc::tc_fence_after();
-                float yv[32];
-                tc::tmem_ld32(tAcc + lq + k * 64 + 32 * grp, yv);
+                float yv[16];
+                tc::tmem_ld16(tAcc + lq + k * 64 + 16 * grp, yv);
                 tc::tmem_ld_wait();
                 if (t0 + i < a.L) {
                     __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(a.y) +
-                                          ((b * a.L + t0 + i) * a.H + hg * HB + k) * kP + 32 * grp;
+                                          ((b * a.L + t0 + i) * a.H + hg * HB + k) * kP + 16 * grp;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         const int q = c * 8;
                         const uint4 pk = make_uint4(pack_bf16x2(yv[q], yv[q + 1]), pack_bf16x2(yv[q + 2], yv[q + 3]),
                                                     pack_bf16x2(yv[q + 4], yv[q + 5]),

@@ -143,9 +143,10 @@ ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt,
     }
 
     const int64_t tilesP = (a.P + 63) / 64, tilesN = (a.N + 63) / 64;
-    // the status word reports this call only
-    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked: status reset");
+    // the status word reports this call only: the first kernel of either path
+    // clears it (thread 0 of its first CTA) before any wait of this call can
+    // give up, which takes seconds
+    cudaError_t e;
     if (a.io == ssd::IO_BF16 && !(dims->flags & SSD_FLAG_SIMT) && has_tokens && ssd::chunked_tc_supported(a)) {
         e = ssd::launch_chunked_tc(a, stream);
         if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked (tensor-core path)");

@@ -333,3 +333,20 @@ def test_tensor_core_scan_repeated_no_timeouts(ssd, chunk):
         ssd.ssd_scan_chunked(*args, chunk_size=chunk, y=y, final_state=h, workspace=ws)
         assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK, f"bounded wait expired in repetition {rep}"
     assert torch.equal(y, y0) and torch.equal(h, h0)
+
+
+@pytest.mark.parametrize("case", ["tensor_core", "simt", "no_tokens"])
+def test_scan_clears_a_stale_timeout_status(ssd, case):
+    """The status word reports the latest call only: a TIMEOUT left in the
+    workspace by an earlier call is cleared by the next scan."""
+    L = 0 if case == "no_tokens" else 256
+    io = torch.bfloat16 if case != "simt" else torch.float32
+    d = inputs.ssd_inputs(1, max(L, 1), 4, 64, 128, 1, io_dtype="bf16" if io == torch.bfloat16 else "f32", seed=2)
+    x, dt = dev(d["x"], io)[:, :L].contiguous(), dev(d["dt"], io)[:, :L].contiguous()
+    Bm, Cm = dev(d["B"], io)[:, :L].contiguous(), dev(d["C"], io)[:, :L].contiguous()
+    ws = torch.empty(max(256, ssd.ssd_workspace_size(1, L, 4, 64, 128, 1, io, 128)), dtype=torch.uint8, device="cuda")
+    ssd.ssd_selftest_bounded_wait(ws, 1000)
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_ERR_TIMEOUT
+    ssd.ssd_scan_chunked(x, dt, dev(d["A"]), Bm, Cm, dev(d["D"]), None, chunk_size=128, workspace=ws,
+                         simt=(case == "simt"))
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
