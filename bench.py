@@ -349,40 +349,100 @@ def run_ours(args):
     }
 
     # ---------------- end to end through the C ABI with host buffers
-    hx = {k: v.cpu().pin_memory() for k, v in base.items()}
-    hA, hD = A.cpu().pin_memory(), Dv.cpu().pin_memory()
-    hy = torch.empty(base["x"].shape, dtype=bf).pin_memory()
-    hf = torch.empty((Bz, H, P, N), dtype=torch.float32).pin_memory()
-    s0 = sets[0]
-    dA, dD = torch.empty_like(A), torch.empty_like(Dv)
+    # Every step copies its inputs from pinned host memory and its results
+    # (y and the final state) back, as a serving loop would: the inputs of a
+    # step are one packed host buffer (one copy in), its outputs one packed
+    # device buffer (one copy out), and three streams overlap the copy in of
+    # step i + 1, the scan of step i and the copy out of step i - 1 over two
+    # device buffer sets.
+    in_parts = [("x", base["x"]), ("dt", base["dt"]), ("B", base["B"]), ("C", base["C"]), ("A", A), ("D", Dv)]
 
-    def e2e_step():
-        for k in hx:
-            s0[k].copy_(hx[k], non_blocking=True)
-        dA.copy_(hA, non_blocking=True)
-        dD.copy_(hD, non_blocking=True)
-        binding.ssd_scan_chunked(s0["x"], s0["dt"], dA, s0["B"], s0["C"], dD, None, chunk_size=best_q, y=s0["y"],
-                                 final_state=s0["final"], workspace=s0["ws"])
-        hy.copy_(s0["y"], non_blocking=True)
-        hf.copy_(s0["final"], non_blocking=True)
+    def carve(buf, parts):
+        views, off = {}, 0
+        for name, like in parts:
+            nbytes = like.numel() * like.element_size()
+            views[name] = buf[off:off + nbytes].view(like.dtype).view(like.shape)
+            off += (nbytes + 255) // 256 * 256
+        return views
 
-    Ke = max(1, min(K, 50))
-    for _ in range(max(W, 3)):
-        e2e_step()
+    def packed_bytes(parts):
+        return sum((t.numel() * t.element_size() + 255) // 256 * 256 for _, t in parts)
+
+    y_like = torch.empty(base["x"].shape, dtype=bf, device=dev)
+    f_like = torch.empty((Bz, H, P, N), dtype=torch.float32, device=dev)
+    out_parts = [("y", y_like), ("final", f_like)]
+    hin = torch.empty(packed_bytes(in_parts), dtype=torch.uint8).pin_memory()
+    hout = torch.empty(packed_bytes(out_parts), dtype=torch.uint8).pin_memory()
+    hv = carve(hin, in_parts)
+    for name, t in in_parts:
+        hv[name].copy_(t.cpu())
+    dsets = []
+    for _ in range(2):
+        din = torch.empty(hin.numel(), dtype=torch.uint8, device=dev)
+        dout = torch.empty(hout.numel(), dtype=torch.uint8, device=dev)
+        dsets.append({"din": din, "dout": dout, "in": carve(din, in_parts), "out": carve(dout, out_parts),
+                      "ws": torch.empty(ws_max, dtype=torch.uint8, device=dev)})
+    s_cap, s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(4))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "run", "out")}
+
+    def e2e_step(i):
+        d = dsets[i & 1]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["run"][i & 1])  # the scan two steps back has read these inputs
+            d["din"].copy_(hin, non_blocking=True)
+            ev["in"][i & 1].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev["in"][i & 1])
+            if i >= 2:
+                s_run.wait_event(ev["out"][i & 1])  # the outputs two steps back have been copied out
+            v, o = d["in"], d["out"]
+            binding.ssd_scan_chunked(v["x"], v["dt"], v["A"], v["B"], v["C"], v["D"], None, chunk_size=best_q,
+                                     y=o["y"], final_state=o["final"], workspace=d["ws"], stream=s_run)
+            ev["run"][i & 1].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["run"][i & 1])
+            hout.copy_(d["dout"], non_blocking=True)
+            ev["out"][i & 1].record(s_out)
+
+    def capture_e2e(nsteps):
+        # K steps in one graph: s_cap forks to the three stage streams and joins them
+        g = torch.cuda.CUDAGraph()
+        s_cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(g, stream=s_cap, capture_error_mode="relaxed"):
+            fork = torch.cuda.Event()
+            fork.record(s_cap)
+            for st in (s_in, s_run, s_out):
+                st.wait_event(fork)
+            for i in range(nsteps):
+                e2e_step(i)
+            for st in (s_in, s_run, s_out):
+                s_cap.wait_stream(st)
+        return g
+
+    Ke = max(1, min(K, 200))
+    for i in range(max(W, 3)):  # eager warm-up (tensor maps, lazy loading)
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    ge = capture_e2e(Ke)
+    ge.replay()
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(Ke):
-        e2e_step()
-    e1.record()
+    with torch.cuda.stream(s_cap):
+        e0.record(s_cap)
+        ge.replay()
+        e1.record(s_cap)
     torch.cuda.synchronize(dev)
     ms_e2e = reduce_max(e0.elapsed_time(e1), world, device=dev)
-    h2d = sum(v.numel() * v.element_size() for v in hx.values()) + hA.numel() * 4 + hD.numel() * 4
-    d2h = hy.numel() * hy.element_size() + hf.numel() * 4
+    del ge
+    h2d = sum(t.numel() * t.element_size() for _, t in in_parts)
+    d2h = sum(t.numel() * t.element_size() for _, t in out_parts)
     e2e = {"value": world * tokens * Ke / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "steps": Ke}
-    del sets, hx
+           "d2h_bytes_per_step": d2h, "steps": Ke,
+           "pipeline": "packed pinned buffers; copy in / scan / copy out overlapped on three streams; K steps in "
+                       "one CUDA graph"}
+    del sets, dsets
 
     # ---------------- decode workload
     if not args.skip_extra:
