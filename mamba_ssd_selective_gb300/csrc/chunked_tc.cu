@@ -95,6 +95,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // bytes of the operand space of chunk_state_tc: B^T and x
 __host__ __device__ constexpr int state_region(int Q, int hb) { return Q * 256 + hb * Q * 128; }
+constexpr int kStateHBMax = 8;  // heads per chunk-state CTA (TMEM: 64 columns each)
 //
 // One CTA per (b, chunk c, group of hb heads sharing a B/C group). All heads
 // of the group share the A operand B^T, so their chunk states come out of one
@@ -118,11 +119,11 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
     uint8_t *sB = smem;                    // B^T operand: 2 panels (n 0-63, 64-127) x Q rows x 128 B
     uint8_t *sX = smem + Q * 256;          // x operands of the hb heads: hb panels of Q rows x 128 B
     float *s_w = reinterpret_cast<float *>(smem + state_region(Q, HB));  // [hb][256]
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_w + 4 * 256);
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(s_w + kStateHBMax * 256);
     uint64_t *bar_mma = bar_ld + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
     int *s_fail = reinterpret_cast<int *>(tmem_slot + 1);
-    const uint32_t ncols = HB == 4 ? 256u : HB == 2 ? 128u : 64u;
+    const uint32_t ncols = HB > 4 ? 512u : HB > 2 ? 256u : HB == 2 ? 128u : 64u;  // power of 2 >= 64 hb
 
     // TMEM first: until a CTA has given up its allocation permit, no other
     // CTA is placed on its SM
@@ -217,12 +218,17 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
     } else {
         if (tid == 0) {
             tc::tc_fence_after();
-            const uint32_t idesc = tc::idesc_bf16(128, kP * HB, true, true);
+            // chains of at most 4 heads (N <= 256): heads h0c .. h0c + nh - 1
             const uint32_t b0 = tc::smem_u32(sB), x0 = tc::smem_u32(sX);
-            for (int k = 0; k < Q; k += 16) {
-                const uint64_t da = tc::sdesc_sw128(b0 + k * 128, Q * 128, 1024);
-                const uint64_t db = tc::sdesc_sw128(x0 + k * 128, Q * 128, 1024);
-                tc::mma_bf16(tmem, da, db, idesc, k > 0 ? 1u : 0u);
+            for (int h0c = 0; h0c < HB; h0c += 4) {
+                const int nh = HB - h0c < 4 ? HB - h0c : 4;
+                const uint32_t idesc = tc::idesc_bf16(128, kP * nh, true, true);
+                const uint32_t xc = x0 + (uint32_t)(h0c * Q * 128);
+                for (int k = 0; k < Q; k += 16) {
+                    const uint64_t da = tc::sdesc_sw128(b0 + k * 128, Q * 128, 1024);
+                    const uint64_t db = tc::sdesc_sw128(xc + k * 128, Q * 128, 1024);
+                    tc::mma_bf16(tmem + (uint32_t)(h0c * kP), da, db, idesc, k > 0 ? 1u : 0u);
+                }
             }
             tc::mma_commit(bar_mma);
         }
@@ -1046,7 +1052,7 @@ int device_cc_major() {
     return major;
 }
 
-size_t state_smem(int Q, int hb) { return (size_t)state_region(Q, hb) + 4096 + 64 + 1024; }
+size_t state_smem(int Q, int hb) { return (size_t)state_region(Q, hb) + kStateHBMax * 1024 + 64 + 1024; }
 constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
 size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 2 * (4 * kHBMax * 128 + kHBMax) * 4 + 16 + 512 + 1024; }
@@ -1134,7 +1140,7 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)state_smem(256, 2));
+                                             (int)state_smem(256, 4));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
         if (e != cudaSuccess) return e;
@@ -1172,8 +1178,19 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
     const bool staged = a.stage_ev[0] != nullptr;  // per-stage timing: no programmatic overlap
     cudaError_t e = mark_stage(a, 0, stream);
     if (e != cudaSuccess) return e;
-    // chunk state: groups of hb1 heads (hb1 * Q <= 512 keeps it within shared memory)
-    ps.hb = (a.Q <= 128 && hpg % 4 == 0) ? 4 : hpg % 2 == 0 ? 2 : 1;
+    // chunk state: groups of hb <= 8 heads (64 TMEM columns and Q x 128 bytes of
+    // x each, at most 4 for 256-token chunks). The busiest SM runs
+    // ceil(CTAs / SMs) CTAs of about (2 + hb) heads' work each: take the hb
+    // that minimises that (ties to the larger hb).
+    {
+        int64_t best = INT64_MAX;
+        for (int hb = kStateHBMax; hb >= 1; --hb) {
+            if (hpg % hb || (a.Q > 128 && hb > 4)) continue;
+            const int64_t ctas = a.B * a.nc * (a.H / hb);
+            const int64_t cost = (ctas + num_sms() - 1) / num_sms() * (2 + hb);
+            if (cost < best) { best = cost; ps.hb = hb; }
+        }
+    }
     e = launch_ex(chunk_state_tc, dim3((unsigned)a.nc, (unsigned)(a.H / ps.hb), (unsigned)a.B),
                   state_smem(a.Q, ps.hb), stream, false, ps, 256);
     if (e != cudaSuccess) return e;
