@@ -131,6 +131,9 @@ __global__ void __launch_bounds__(256) chunk_state_tc(const __grid_constant__ Tc
         tc::tmem_alloc(tmem_slot, ncols);
         tc::tmem_relinquish();
     }
+    // Launched as a programmatic dependent of whatever kernel precedes it in the
+    // stream: no global memory is touched before that grid has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // this call's status word starts clear (the first kernel of the call)
     if (tid == 32 && c == 0 && hg == 0 && b == 0) *a.status = SSD_OK;
     // B^T and x by TMA; the cumulative sums and the CTA barrier overlap the loads
@@ -534,9 +537,9 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 // SSD_ERR_TIMEOUT.
 
 constexpr int kHBMax = 4;
-constexpr int kEpiWarp0 = 4;                        // first epilogue warp
+constexpr int kEpiWarp0 = 5;                        // first epilogue warp
 constexpr int kEpiThreads = 512;                    // 16 epilogue warps
-constexpr int kScanPThreads = 32 * kEpiWarp0 + kEpiThreads;  // 20 warps
+constexpr int kScanPThreads = 32 * kEpiWarp0 + kEpiThreads;  // 21 warps
 constexpr int kXStages = 4;
 
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *fail) {
@@ -574,7 +577,8 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     // per-item scalars of every row and head, double-buffered by item:
     // [2][kScal] floats = cs | dt | colf | sc, each [kHBMax][128], then D [kHBMax]
     constexpr int kScal = 4 * kHBMax * 128 + kHBMax;
-    float *s_scal = reinterpret_cast<float *>(sH + 65536);
+    uint8_t *sY = sH + 65536;            // y of one head (128 rows x 128 B, 128-byte swizzle) for the TMA store
+    float *s_scal = reinterpret_cast<float *>(sY + 16384);
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_scal + 2 * kScal + 4);
     uint64_t *tile_full = bars + 0, *tile_empty = bars + 1;
     uint64_t *h_full = bars + 2, *h_empty = bars + 3;
@@ -584,7 +588,8 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     uint64_t *p_full = bars + 10, *p_empty = bars + 12;                 // [2] each
     uint64_t *x_full = bars + 14, *x_empty = bars + 14 + kXStages;      // [kXStages] each
     uint64_t *c_full = bars + 14 + 2 * kXStages, *c_empty = c_full + 2;  // [2] each
-    constexpr int kBars = 18 + 2 * kXStages;
+    uint64_t *ys_full = bars + 18 + 2 * kXStages, *ys_empty = ys_full + 1;
+    constexpr int kBars = 20 + 2 * kXStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -624,6 +629,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         tc::mbar_init(p_full + 1, kEpiThreads);
         tc::mbar_init(c_empty + 0, kEpiThreads);
         tc::mbar_init(c_empty + 1, kEpiThreads);
+        tc::mbar_init(ys_full, kEpiThreads);
         tc::fence_mbar_init();
         *s_fail = 0;
         // the first item's operands (the x ring starts empty and holds every
@@ -642,6 +648,9 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem, tAcc = tmem + 128, tP = tmem + 384;
+    // the next call's chunk state may start its launch now; it waits for this
+    // grid's completion before it touches memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -748,6 +757,26 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&c_full[buf]);
+        }
+    } else if (warp == 4) {
+        // ------------------------------------ TMA store of y, one head at a time:
+        // the epilogue stages y(k) in sY; full 128-byte lines go out instead of
+        // each thread's 16-byte pieces of rows 3 KB apart
+        if (lane == 0) {
+            uint32_t ny = 0;
+            for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
+                int64_t b, tile;
+                int hg;
+                decode(u, b, tile, hg);
+                for (int k = 0; k < HB; ++k, ++ny) {
+                    if (!pwait(ys_full, ny & 1, s_fail)) break;
+                    tc::tma_store_3d(&prm.my, sY, (hg * HB + k) * kP, (int)(tile * kRows), (int)b);
+                    tc::bulk_commit();
+                    tc::bulk_wait_read_all();  // sY may be written again
+                    tc::mbar_arrive(ys_empty);
+                }
+            }
+            tc::bulk_wait_all();  // every store of this CTA is complete
         }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer
@@ -896,24 +925,24 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             // Head n completes y_full[n & 1]; the MMA of head n + 2 needs
             // prepare(n + 2), which every thread runs after yout(n), so a
             // barrier is never two phases ahead of its waiter.
+            // (the store warp writes the staged head to y; rows past L are clipped by the TMA store)
             auto yout = [&](int k, uint32_t n) {
                 pwait(&y_full[n & 1], (n >> 1) & 1, s_fail);
                 tc::tc_fence_after();
                 float yv[16];
                 tc::tmem_ld16(tAcc + lq + k * 64 + 16 * grp, yv);
                 tc::tmem_ld_wait();
-                if (t0 + i < a.L) {
-                    __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(a.y) +
-                                          ((b * a.L + t0 + i) * a.H + hg * HB + k) * kP + 16 * grp;
+                pwait(ys_empty, (n & 1) ^ 1, s_fail);  // the previous head has left sY
+                uint8_t *yrow = sY + i * 128;
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int q = c * 8;
-                        const uint4 pk = make_uint4(pack_bf16x2(yv[q], yv[q + 1]), pack_bf16x2(yv[q + 2], yv[q + 3]),
-                                                    pack_bf16x2(yv[q + 4], yv[q + 5]),
-                                                    pack_bf16x2(yv[q + 6], yv[q + 7]));
-                        *reinterpret_cast<uint4 *>(yrow + q) = pk;
-                    }
+                for (int c = 0; c < 2; ++c) {
+                    const int q = c * 8;
+                    const uint4 pk = make_uint4(pack_bf16x2(yv[q], yv[q + 1]), pack_bf16x2(yv[q + 2], yv[q + 3]),
+                                                pack_bf16x2(yv[q + 4], yv[q + 5]), pack_bf16x2(yv[q + 6], yv[q + 7]));
+                    *reinterpret_cast<uint4 *>(yrow + (((2 * grp + c) ^ (i & 7)) << 4)) = pk;
                 }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(ys_full);
             };
             // prepare(k) runs one head ahead of yout(k - 1); one call site each
 #pragma unroll 1
@@ -1055,7 +1084,7 @@ int device_cc_major() {
 size_t state_smem(int Q, int hb) { return (size_t)state_region(Q, hb) + kStateHBMax * 1024 + 64 + 1024; }
 constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
-size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 2 * (4 * kHBMax * 128 + kHBMax) * 4 + 16 + 512 + 1024; }
+size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 16384 + 2 * (4 * kHBMax * 128 + kHBMax) * 4 + 16 + 512 + 1024; }
 
 int num_sms() {
     static int n = 0;
@@ -1192,7 +1221,7 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
         }
     }
     e = launch_ex(chunk_state_tc, dim3((unsigned)a.nc, (unsigned)(a.H / ps.hb), (unsigned)a.B),
-                  state_smem(a.Q, ps.hb), stream, false, ps, 256);
+                  state_smem(a.Q, ps.hb), stream, !staged, ps, 256);
     if (e != cudaSuccess) return e;
     if ((e = mark_stage(a, 1, stream)) != cudaSuccess) return e;
     e = launch_state_pass(a, false, true, stream, !staged, /*bf16_in=*/true);
