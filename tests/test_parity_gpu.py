@@ -63,6 +63,19 @@ def test_prefill_ragged_groups_init(ssd, io, chunk, shape):
     check(io, h, hr, "final_state")
 
 
+@pytest.mark.parametrize("shape", [(1, 8192, 28, 64, 128, 1), (1, 16384, 16, 64, 128, 1), (2, 2048, 12, 64, 128, 3)])
+def test_prefill_tensor_core_head_groups(ssd, shape):
+    """Tensor-core path at shapes whose per-SM cost model picks chunk-state head
+    groups of 7 and 8 heads (MMA chains of 4 + 3 and 4 + 4 heads) and several B/C
+    groups; every element against the oracle, with an initial state."""
+    Bz, L, H, P, N, G = shape
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=11, init_state=True)
+    yr, hr = ref_scan(d)
+    y, h = run_scan(ssd, d, "bf16", 128)
+    check("bf16", y, yr, "y")
+    check("bf16", h, hr, "final_state")
+
+
 @pytest.mark.parametrize("simt", [False, True])
 @pytest.mark.parametrize("chunk", [64, 128, 256])
 def test_prefill_m2_130m_workload_full(ssd, chunk, simt):
