@@ -537,9 +537,9 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 // SSD_ERR_TIMEOUT.
 
 constexpr int kHBMax = 4;
-constexpr int kEpiWarp0 = 5;                        // first epilogue warp
+constexpr int kEpiWarp0 = 4;                        // first epilogue warp
 constexpr int kEpiThreads = 512;                    // 16 epilogue warps
-constexpr int kScanPThreads = 32 * kEpiWarp0 + kEpiThreads;  // 21 warps
+constexpr int kScanPThreads = 32 * kEpiWarp0 + kEpiThreads;  // 20 warps (5 per SMSP: 96 registers each)
 constexpr int kXStages = 4;
 
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *fail) {
@@ -670,10 +670,26 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             }
         }
     } else if (warp == 2) {
-        // ------------------------------ TMA producer of entering states
+        // ---------- TMA producer of entering states, and TMA store of y: one
+        // head at a time the epilogue stages y(k) in sY, this warp writes it with
+        // one tensor store (full 128-byte lines, instead of each thread's 16-byte
+        // pieces of rows 3 KB apart). Item u's entering states are loaded as soon
+        // as item u - 1's entering-state MMA has read the previous ones, then
+        // item u - 1's heads are stored as the epilogue produces them.
         if (lane == 0) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            uint32_t hcnt = 0;
+            uint32_t hcnt = 0, ny = 0;
+            int64_t pb = -1, ptile = 0;
+            int phg = 0;
+            auto store_item = [&](int64_t sb_, int64_t stile, int shg) {
+                for (int k = 0; k < HB; ++k, ++ny) {
+                    if (!pwait(ys_full, ny & 1, s_fail)) return;
+                    tc::tma_store_3d(&prm.my, sY, (shg * HB + k) * kP, (int)(stile * kRows), (int)sb_);
+                    tc::bulk_commit();
+                    tc::bulk_wait_read_all();  // sY may be written again
+                    tc::mbar_arrive(ys_empty);
+                }
+            };
             for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
                 int64_t b, tile;
                 int hg;
@@ -691,7 +707,13 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                         tc::tma_load_2d(dst + HB * 8192, &prm.mh, h_full, 64, row0);
                     }
                 }
+                if (pb >= 0) store_item(pb, ptile, phg);
+                pb = b;
+                ptile = tile;
+                phg = hg;
             }
+            if (pb >= 0 && !*s_fail) store_item(pb, ptile, phg);
+            tc::bulk_wait_all();  // every store of this CTA is complete
         }
     } else if (warp == 3) {
         // ------------------ per-item scalars, one item ahead of the epilogue
@@ -758,26 +780,6 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&c_full[buf]);
         }
-    } else if (warp == 4) {
-        // ------------------------------------ TMA store of y, one head at a time:
-        // the epilogue stages y(k) in sY; full 128-byte lines go out instead of
-        // each thread's 16-byte pieces of rows 3 KB apart
-        if (lane == 0) {
-            uint32_t ny = 0;
-            for (int64_t u = blockIdx.x; u < n_items && !*s_fail; u += gridDim.x) {
-                int64_t b, tile;
-                int hg;
-                decode(u, b, tile, hg);
-                for (int k = 0; k < HB; ++k, ++ny) {
-                    if (!pwait(ys_full, ny & 1, s_fail)) break;
-                    tc::tma_store_3d(&prm.my, sY, (hg * HB + k) * kP, (int)(tile * kRows), (int)b);
-                    tc::bulk_commit();
-                    tc::bulk_wait_read_all();  // sY may be written again
-                    tc::mbar_arrive(ys_empty);
-                }
-            }
-            tc::bulk_wait_all();  // every store of this CTA is complete
-        }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -838,8 +840,10 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         // ---------------------------------------------------- epilogue
         // 16 warps: TMEM lane quarter qd = warp % 4 (rows 32 qd .. 32 qd + 31)
         // and column group grp. Per head, warp (qd, grp) owns block J = grp
-        // (32 columns j) of S' for its rows and the 16 columns p in
-        // [16 grp, 16 grp + 16) of the entering-state term and of y.
+        // (32 columns j) of S' for its rows when that block lies before the
+        // diagonal, columns [8 grp, 8 grp + 8) of the diagonal block J = qd
+        // (the costly one, shared by the four warps of the quarter), and the
+        // 16 columns p in [16 grp, 16 grp + 16) of the entering-state term and of y.
         const int grp = (warp - kEpiWarp0) >> 2;
         const int qd = warp & 3;
         const int i = qd * 32 + lane;       // tile row
@@ -849,7 +853,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
         // blocks of S' that are zero for every head (after this warp's rows, or
         // in the other 64-token chunk of the tile) are written once, here
         const bool zero_blk = J > qd || (Q < kRows && (J >> 1) != (qd >> 1));
-        const bool diag_blk = J == qd;
+        const bool fact_blk = J < qd && !zero_blk;  // before the diagonal, same chunk
         if (zero_blk) {
             uint32_t z[16];
 #pragma unroll
@@ -884,26 +888,35 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
                 const float cs_i = cs_[i], Dh = s_D[k], sc = s_sc[k * 128 + i];
                 pwait(&p_empty[n & 1], ((n >> 1) & 1) ^ 1, s_fail);
                 tc::tc_fence_after();
-                if (!zero_blk) {
+                {
+                    float vd[8];
+                    tc::tmem_ld8(tS + lq + qd * 32 + 8 * grp, vd);
+                    tc::tmem_ld_wait();
+                    // this warp's 8 columns of the diagonal block: exact decay,
+                    // causal mask, D on the diagonal
+                    uint32_t pk4[4];
+#pragma unroll
+                    for (int q = 0; q < 8; q += 2) {
+                        float f[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int cc = 8 * grp + q + u, jr = qd * 32 + cc;
+                            const float e = tc::ex2(fminf(cs_i - cs_[jr], 0.f)) * dt_[jr];
+                            f[u] = cc <= lane ? vd[q + u] * e : 0.f;
+                            f[u] += cc == lane ? Dh : 0.f;
+                        }
+                        pk4[q / 2] = pack_bf16x2(f[0], f[1]);
+                    }
+                    tc::tmem_st4(tP + lq + (n & 1) * 64 + qd * 16 + 4 * grp, pk4);
+                }
+                if (fact_blk) {
+                    // block before this warp's rows: factorised decay
                     float v[32];
                     tc::tmem_ld32(tS + lq + J * 32, v);
                     tc::tmem_ld_wait();
-                    if (diag_blk) {
-                        // exact decay, causal mask, D on the diagonal
+                    const float rf = tc::ex2(cs_i - cs_[J * 32 + 31]);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const int jr = J * 32 + q;
-                            const float e = tc::ex2(fminf(cs_i - cs_[jr], 0.f)) * dt_[jr];
-                            float f = q <= lane ? v[q] * e : 0.f;
-                            f += q == lane ? Dh : 0.f;
-                            v[q] = f;
-                        }
-                    } else {
-                        // block before this warp's rows: factorised decay
-                        const float rf = tc::ex2(cs_i - cs_[J * 32 + 31]);
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * cf_[J * 32 + q];
-                    }
+                    for (int q = 0; q < 32; ++q) v[q] = v[q] * rf * cf_[J * 32 + q];
                     uint32_t pkd[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) pkd[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
@@ -925,7 +938,7 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             // Head n completes y_full[n & 1]; the MMA of head n + 2 needs
             // prepare(n + 2), which every thread runs after yout(n), so a
             // barrier is never two phases ahead of its waiter.
-            // (the store warp writes the staged head to y; rows past L are clipped by the TMA store)
+            // (warp 2 writes the staged head to y; rows past L are clipped by the TMA store)
             auto yout = [&](int k, uint32_t n) {
                 pwait(&y_full[n & 1], (n >> 1) & 1, s_fail);
                 tc::tc_fence_after();
