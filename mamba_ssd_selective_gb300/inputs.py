@@ -115,14 +115,19 @@ def decode_step_inputs(step: int, batch: int, nheads: int, headdim: int, dstate:
 
 
 def diag_inputs(batch: int, seqlen: int, dim: int, dstate: int, io_dtype: str = "bf16",
-                seed: int = 0, init_state: bool = False) -> dict:
-    """Inputs of one Mamba-1 diagonal scan: x/dt[B,L,D], A[D,N] = -(n+1),
+                seed: int = 0, init_state: bool = False, random_A: bool = False) -> dict:
+    """Inputs of one Mamba-1 diagonal scan: x/dt[B,L,D], A[D,N] = -(n+1)
+    (or, with random_A, -exp(U(ln 1, ln 16)) drawn per (channel, state)),
     B/C[B,L,N], D[D], init_state[B,D,N] (or None)."""
     Bsz, L, Dm, N = batch, seqlen, dim, dstate
+    if random_A:
+        A = -np.exp(_rng(seed, _S_A).uniform(0.0, np.log(16.0), size=(Dm, N)))
+    else:
+        A = -np.broadcast_to(np.arange(1, N + 1, dtype=np.float64), (Dm, N)).copy()
     out = {
         "x": round_to(_rng(seed, _S_X).standard_normal((Bsz, L, Dm)), io_dtype),
         "dt": _dt(seed, (Bsz, L, Dm), Dm, _S_DT_NOISE, io_dtype),
-        "A": round_to(-np.broadcast_to(np.arange(1, N + 1, dtype=np.float64), (Dm, N)).copy(), "f32"),
+        "A": round_to(A, "f32"),
         "B": round_to(_rng(seed, _S_B).standard_normal((Bsz, L, N)), io_dtype),
         "C": round_to(_rng(seed, _S_C).standard_normal((Bsz, L, N)), io_dtype),
         "D": round_to(_rng(seed, _S_D).uniform(0.5, 1.5, size=Dm), "f32"),

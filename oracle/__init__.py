@@ -53,7 +53,8 @@ def _load():
         lib.oracle_ssd_seq.argtypes = [i64] * 6 + [dp] * 9 + [ci]
         lib.oracle_ssd_decode.argtypes = [i64] * 5 + [dp] * 8 + [ci]
         lib.oracle_diag_seq.argtypes = [i64] * 4 + [dp] * 9 + [ci]
-        for f in (lib.oracle_ssd_seq, lib.oracle_ssd_decode, lib.oracle_diag_seq):
+        lib.oracle_diag_seq_ex.argtypes = [i64] * 4 + [dp] * 8 + [ci] + [dp] * 3 + [ci]
+        for f in (lib.oracle_ssd_seq, lib.oracle_ssd_decode, lib.oracle_diag_seq, lib.oracle_diag_seq_ex):
             f.restype = ci
         _lib = lib
     return _lib
@@ -123,11 +124,14 @@ def ssd_decode(state, x, dt, A, B, C, D=None, threads=None):
     return y, st
 
 
-def diag_seq(x, dt, A, B, C, D=None, init_state=None, threads=None):
+def diag_seq(x, dt, A, B, C, D=None, init_state=None, threads=None, z=None, delta_bias=None,
+             delta_softplus=False):
     """Mamba-1 diagonal recurrence in float64.
 
     x/dt[B,L,Dm], A[Dm,N], B/C[B,L,N], D[Dm] or None, init_state[B,Dm,N] or
-    None. Returns (y[B,L,Dm], final_state[B,Dm,N]).
+    None. Options of selective_scan_fn: delta_bias[Dm] is added to dt, then
+    with delta_softplus the step is softplus of the sum; z[B,L,Dm] gates the
+    output by silu(z). Returns (y[B,L,Dm], final_state[B,Dm,N]).
     """
     x = _f64(x)
     Bsz, L, Dm = x.shape
@@ -137,11 +141,14 @@ def diag_seq(x, dt, A, B, C, D=None, init_state=None, threads=None):
     Bm = _f64(B, (Bsz, L, N), "B")
     Cm = _f64(C, (Bsz, L, N), "C")
     D = _f64(D, (Dm,), "D")
+    z = _f64(z, (Bsz, L, Dm), "z")
+    db = _f64(delta_bias, (Dm,), "delta_bias")
     h0 = _f64(init_state, (Bsz, Dm, N), "init_state")
     y = np.empty((Bsz, L, Dm))
     hT = np.empty((Bsz, Dm, N))
-    rc = _load().oracle_diag_seq(Bsz, L, Dm, N, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
-                                 _ptr(D), _ptr(h0), _ptr(y), _ptr(hT), threads or default_threads())
+    rc = _load().oracle_diag_seq_ex(Bsz, L, Dm, N, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                                    _ptr(z), _ptr(db), int(bool(delta_softplus)), _ptr(h0), _ptr(y), _ptr(hT),
+                                    threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_diag_seq: invalid sizes")
     return y, hT

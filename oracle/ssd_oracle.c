@@ -27,6 +27,12 @@
  *     h_t[n] = exp(dt_t * A[d,n]) * h_{t-1}[n] + dt_t * x_t * B_t[n]
  *     y_t    = sum_n C_t[n] * h_t[n] + D_d * x_t
  *   (the selective_scan_fn workload of the COREY page, section 5.1).
+ *   Its options (the same page's kernel-level timing, section 7, which runs
+ *   selective_scan_fn with delta_softplus set): a per-channel delta_bias is
+ *   added to dt, then with delta_softplus the step is softplus of that sum,
+ *       dt_t = softplus(dt_raw_t + delta_bias_d),  softplus(v) = log(1 + e^v),
+ *   and an optional gate z[B,L,Dm] multiplies the output by silu(z):
+ *       out_t = y_t * z_t / (1 + exp(-z_t)).
  *
  * Layouts (row-major, innermost last):
  *   SSD:    x[B,L,H,P]  dt[B,L,H]  A[H]  Bm,Cm[B,L,G,N]  D[H]  state[B,H,P,N]
@@ -138,9 +144,14 @@ typedef struct {
     int64_t B, L, Dm, N;
     const double *x, *dt, *A, *Bm, *Cm, *D, *init;
     double *y, *final_state;
+    const double *delta_bias, *z;
+    int delta_softplus;
     int64_t next_unit, n_units;
     pthread_mutex_t lock;
 } diag_job;
+
+/* softplus(v) = log(1 + e^v), written so that e^v cannot overflow. */
+static double softplus(double v) { return v > 0.0 ? v + log1p(exp(-v)) : log1p(exp(v)); }
 
 /* One (b,d) unit of the Mamba-1 diagonal recurrence. */
 static void diag_unit(const diag_job *j, int64_t b, int64_t d, double *st) {
@@ -151,8 +162,10 @@ static void diag_unit(const diag_job *j, int64_t b, int64_t d, double *st) {
         memcpy(st, j->init + (b * Dm + d) * N, sizeof(double) * N);
     else
         memset(st, 0, sizeof(double) * N);
+    const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
     for (int64_t t = 0; t < L; ++t) {
-        const double dt = j->dt[(b * L + t) * Dm + d];
+        double dt = j->dt[(b * L + t) * Dm + d] + bias;
+        if (j->delta_softplus) dt = softplus(dt);
         const double xt = j->x[(b * L + t) * Dm + d];
         const double *Bt = j->Bm + (b * L + t) * N;
         const double *Ct = j->Cm + (b * L + t) * N;
@@ -161,7 +174,12 @@ static void diag_unit(const diag_job *j, int64_t b, int64_t d, double *st) {
             st[n] = exp(dt * Ad[n]) * st[n] + dt * xt * Bt[n];
             acc += Ct[n] * st[n];
         }
-        j->y[(b * L + t) * Dm + d] = acc + Dd * xt;
+        double out = acc + Dd * xt;
+        if (j->z) {
+            const double zt = j->z[(b * L + t) * Dm + d];
+            out *= zt / (1.0 + exp(-zt));
+        }
+        j->y[(b * L + t) * Dm + d] = out;
     }
     if (j->final_state) memcpy(j->final_state + (b * Dm + d) * N, st, sizeof(double) * N);
 }
@@ -178,14 +196,23 @@ static void *diag_worker(void *arg) {
     return NULL;
 }
 
-int oracle_diag_seq(int64_t B, int64_t L, int64_t Dm, int64_t N, const double *x,
-                    const double *dt, const double *A, const double *Bm, const double *Cm,
-                    const double *D, const double *init_state, double *y, double *final_state,
-                    int nthreads) {
+int oracle_diag_seq_ex(int64_t B, int64_t L, int64_t Dm, int64_t N, const double *x,
+                       const double *dt, const double *A, const double *Bm, const double *Cm,
+                       const double *D, const double *z, const double *delta_bias, int delta_softplus,
+                       const double *init_state, double *y, double *final_state, int nthreads) {
     if (B < 0 || L < 0 || Dm < 1 || N < 1) return -1;
-    diag_job j = {B, L, Dm, N, x, dt, A, Bm, Cm, D, init_state, y, final_state, 0, B * Dm};
+    diag_job j = {B, L, Dm, N, x, dt, A, Bm, Cm, D, init_state, y, final_state,
+                  delta_bias, z, delta_softplus != 0, 0, B * Dm};
     pthread_mutex_init(&j.lock, NULL);
     run_threads(diag_worker, &j, nthreads, B * Dm);
     pthread_mutex_destroy(&j.lock);
     return 0;
+}
+
+int oracle_diag_seq(int64_t B, int64_t L, int64_t Dm, int64_t N, const double *x,
+                    const double *dt, const double *A, const double *Bm, const double *Cm,
+                    const double *D, const double *init_state, double *y, double *final_state,
+                    int nthreads) {
+    return oracle_diag_seq_ex(B, L, Dm, N, x, dt, A, Bm, Cm, D, NULL, NULL, 0, init_state, y,
+                              final_state, nthreads);
 }

@@ -24,6 +24,11 @@ MUTANTS = {
     "dt_missing_on_input": ("const double u = dt * xt[p];", "const double u = xt[p];"),
     "wrong_group_index": ("const int64_t g = h / (H / G);", "const int64_t g = h % G;"),
     "diag_decay_index": ("st[n] = exp(dt * Ad[n]) * st[n]", "st[n] = exp(dt * Ad[0]) * st[n]"),
+    "softplus_before_bias": ("double dt = j->dt[(b * L + t) * Dm + d] + bias;\n        if (j->delta_softplus) dt = softplus(dt);",
+                             "double dt = j->dt[(b * L + t) * Dm + d];\n        if (j->delta_softplus) dt = softplus(dt);\n        dt += bias;"),
+    "softplus_wrong_branch": ("v + log1p(exp(-v))", "v + log1p(exp(v))"),
+    "gate_before_D": ("out *= zt / (1.0 + exp(-zt));", "out = acc * (zt / (1.0 + exp(-zt))) + Dd * xt;"),
+    "gate_sigmoid_only": ("out *= zt / (1.0 + exp(-zt));", "out *= 1.0 / (1.0 + exp(-zt));"),
 }
 
 PINS = [
@@ -31,6 +36,8 @@ PINS = [
     pins.test_dt_zero_keeps_state, pins.test_lfilter_constant_dt, pins.test_brute_force_tiny,
     pins.test_hand_worked_example, pins.test_quadratic_form_matches_recurrence,
     pins.test_mamba2_equals_mamba1_with_tied_decay, pins.test_diag_lfilter_constant_dt,
+    pins.test_diag_delta_bias_and_softplus_reduce_to_transformed_dt, pins.test_diag_softplus_of_large_steps,
+    pins.test_diag_z_gate_is_silu_of_z, pins.test_diag_options_single_token_closed_form,
 ]
 
 
@@ -46,7 +53,7 @@ def test_pins_reject_mutant(name, tmp_path, monkeypatch):
                    check=True)
     oracle._load()  # make sure the real library's argtypes are set up first
     lib = ctypes.CDLL(str(so))
-    for fname in ("oracle_ssd_seq", "oracle_ssd_decode", "oracle_diag_seq"):
+    for fname in ("oracle_ssd_seq", "oracle_ssd_decode", "oracle_diag_seq", "oracle_diag_seq_ex"):
         getattr(lib, fname).argtypes = getattr(oracle._lib, fname).argtypes
         getattr(lib, fname).restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)

@@ -292,6 +292,73 @@ def test_diag_single_token_and_dt_zero():
     np.testing.assert_allclose(y2, ref2, rtol=1e-12, atol=1e-13)
 
 
+def _diag_opt_inputs(seed, L=30, Dm=5, N=4):
+    d = inputs.diag_inputs(2, L, Dm, N, io_dtype="f32", seed=seed, init_state=True)
+    rng = np.random.default_rng(seed + 100)
+    raw = rng.normal(-2.0, 1.5, size=d["dt"].shape)      # pre-activation steps, mostly negative
+    bias = rng.uniform(-3.0, 1.0, size=Dm)
+    z = rng.normal(0.0, 2.0, size=d["x"].shape)
+    return d, raw, bias, z
+
+
+def test_diag_delta_bias_and_softplus_reduce_to_transformed_dt():
+    """delta_bias then softplus equals the plain scan fed softplus(dt + bias),
+    with softplus taken from numpy (logaddexp(0, v) = log(1 + e^v))."""
+    d, raw, bias, _ = _diag_opt_inputs(21)
+    base = (d["A"], d["B"], d["C"], d["D"])
+    for sp in (False, True):
+        for b in (None, bias):
+            v = raw + (0.0 if b is None else b[None, None, :])
+            want = np.logaddexp(0.0, v) if sp else v
+            y1, h1 = oracle.diag_seq(d["x"], raw, *base, d["init_state"], delta_bias=b, delta_softplus=sp)
+            y2, h2 = oracle.diag_seq(d["x"], want, *base, d["init_state"])
+            np.testing.assert_allclose(y1, y2, rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(h1, h2, rtol=1e-13, atol=1e-14)
+
+
+def test_diag_softplus_of_large_steps():
+    """softplus(v) -> v for large v and -> e^v for very negative v: the scan
+    with softplus matches the plain scan fed v (or e^v) there."""
+    d = inputs.diag_inputs(1, 12, 3, 4, io_dtype="f32", seed=5, init_state=True)
+    big = np.full(d["dt"].shape, 40.0)
+    y1, h1 = oracle.diag_seq(d["x"], big, d["A"] * 1e-3, d["B"], d["C"], d["D"], d["init_state"], delta_softplus=True)
+    y2, h2 = oracle.diag_seq(d["x"], big, d["A"] * 1e-3, d["B"], d["C"], d["D"], d["init_state"])
+    np.testing.assert_allclose(y1, y2, rtol=1e-13, atol=1e-14)
+    tiny = np.full(d["dt"].shape, -30.0)
+    y3, h3 = oracle.diag_seq(d["x"], tiny, d["A"], d["B"], d["C"], d["D"], d["init_state"], delta_softplus=True)
+    y4, h4 = oracle.diag_seq(d["x"], np.exp(tiny), d["A"], d["B"], d["C"], d["D"], d["init_state"])
+    np.testing.assert_allclose(y3, y4, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(h3, h4, rtol=1e-12, atol=1e-14)
+
+
+def test_diag_z_gate_is_silu_of_z():
+    """The gate multiplies the finished output (D term included) by
+    z * sigmoid(z), sigmoid from scipy; the state is not gated."""
+    special = pytest.importorskip("scipy.special")
+    d, raw, bias, z = _diag_opt_inputs(33)
+    args = (d["x"], raw, d["A"], d["B"], d["C"], d["D"], d["init_state"])
+    yg, hg = oracle.diag_seq(*args, z=z, delta_bias=bias, delta_softplus=True)
+    y0, h0 = oracle.diag_seq(*args, delta_bias=bias, delta_softplus=True)
+    np.testing.assert_allclose(yg, y0 * z * special.expit(z), rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(hg, h0)
+
+
+def test_diag_options_single_token_closed_form():
+    """L = 1, zero state: out = (s x (C.B) + D x) * z * sigmoid(z) with
+    s = softplus(dt + bias), written out by hand."""
+    d, raw, bias, z = _diag_opt_inputs(8, L=1, Dm=4, N=3)
+    y, h = oracle.diag_seq(d["x"], raw, d["A"], d["B"], d["C"], d["D"], z=z, delta_bias=bias, delta_softplus=True)
+    for b in range(2):
+        cb = sum(d["C"][b, 0, n] * d["B"][b, 0, n] for n in range(3))
+        for ch in range(4):
+            s_ = math.log1p(math.exp(raw[b, 0, ch] + bias[ch]))
+            xv, zv = d["x"][b, 0, ch], z[b, 0, ch]
+            ref = (s_ * xv * cb + d["D"][ch] * xv) * zv / (1.0 + math.exp(-zv))
+            assert abs(y[b, 0, ch] - ref) <= 1e-13 * max(1.0, abs(ref))
+            for n in range(3):
+                assert abs(h[b, ch, n] - s_ * xv * d["B"][b, 0, n]) <= 1e-14 * max(1.0, abs(h[b, ch, n]))
+
+
 def test_diag_split_resume():
     d = inputs.diag_inputs(2, 50, 6, 4, io_dtype="f32", seed=12, init_state=True)
     yf, hf = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"])

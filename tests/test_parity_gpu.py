@@ -270,18 +270,20 @@ def run_diag(ssd, d, io, chunk, init=True):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("shape", [(2, 300, 256, 16), (1, 77, 130, 5), (2, 64, 100, 40)])
+@pytest.mark.parametrize("shape", [(2, 300, 256, 16), (1, 65, 200, 16), (2, 100, 136, 8), (1, 50, 72, 24),
+                                   (1, 77, 130, 5), (2, 64, 100, 40)])
 def test_diag_every_element(ssd, io, shape):
     Bz, L, Dm, N = shape
-    d = inputs.diag_inputs(Bz, L, Dm, N, io_dtype=io, seed=4, init_state=True)
+    d = inputs.diag_inputs(Bz, L, Dm, N, io_dtype=io, seed=4, init_state=True, random_A=True)
     yr, hr = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"])
     y, h = run_diag(ssd, d, io, 64)
     check(io, y, yr, "y")
     check(io, h, hr, "final_state")
 
 
-def test_diag_chunk_size_bitwise_independent(ssd):
-    d = inputs.diag_inputs(2, 1000, 300, 16, io_dtype="bf16", seed=6, init_state=True)
+@pytest.mark.parametrize("dim", [300, 320])
+def test_diag_chunk_size_bitwise_independent(ssd, dim):
+    d = inputs.diag_inputs(2, 1000, dim, 16, io_dtype="bf16", seed=6, init_state=True)
     y0, h0 = run_diag(ssd, d, "bf16", 32)
     for c in (96, 256, 512, 1024, 2048):
         y, h = run_diag(ssd, d, "bf16", c)
