@@ -185,6 +185,56 @@ ssd_status selective_scan_diag(int64_t batch, int64_t seqlen, int64_t dim, int64
                                float *final_state, cudaStream_t stream);
 
 /*
+ * The same scan with selective_scan_fn's options (the kernel-level timing of
+ * "COREY ...", section 7, runs selective_scan_fn with delta_softplus set):
+ *
+ *     dt'_t[d] = dt_t[d] + delta_bias[d]           (delta_bias may be NULL: 0)
+ *     dt''_t[d] = softplus(dt'_t[d]) = log(1 + exp(dt'_t[d]))  if delta_softplus
+ *                 dt'_t[d]                                      otherwise
+ *     the recurrence above with dt'' in place of dt
+ *     out_t[d] = y_t[d] * z_t[d] / (1 + exp(-z_t[d]))   (z may be NULL: no gate)
+ *
+ *   z          [batch, seqlen, dim]  io_dtype, may be NULL
+ *   delta_bias [dim]                 float32, may be NULL
+ *   delta_softplus 0 or 1 (else SSD_ERR_INVALID_ARG)
+ * The gate multiplies the finished output, D term included; the carried
+ * state is not gated. The kernel evaluates softplus(v) as v for v > 20, where
+ * the two agree in float32.
+ *
+ *   workspace  device scratch of selective_scan_diag_workspace_size() bytes,
+ *              256-byte aligned, owned by the caller, or NULL. When the batch
+ *              and dim leave most of the GPU idle (one pass per sequence gives
+ *              fewer than ~39k threads) and a workspace is given, the sequence
+ *              is cut into time segments of a multiple of 32 tokens, scanned in
+ *              parallel from a zero state, chained by one segment pass
+ *              (decay over a segment = exp(A * sum of its steps)), then
+ *              rescanned from their entering states to form y. The result
+ *              equals the one-pass scan up to float32 rounding. The split
+ *              depends on the shape only, so the output stays bitwise
+ *              independent of chunk_size. A workspace smaller than the size
+ *              query (or not 256-byte aligned) is SSD_ERR_INVALID_ARG; NULL
+ *              runs one pass per sequence.
+ * Other arguments, limits, ownership and errors as for selective_scan_diag,
+ * which is this call with z = delta_bias = workspace = NULL and
+ * delta_softplus = 0.
+ */
+ssd_status selective_scan_diag_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                                  int32_t io_dtype, const void *x, const void *dt, const float *A,
+                                  const void *B, const void *C, const float *D, const void *z,
+                                  const float *delta_bias, int32_t delta_softplus,
+                                  const float *init_state, int chunk_size, void *y,
+                                  float *final_state, void *workspace, size_t ws_bytes,
+                                  cudaStream_t stream);
+
+/*
+ * Workspace bytes selective_scan_diag_ex needs for its time-segmented scan of
+ * this shape; 0 when the shape runs one pass per sequence (or the arguments
+ * are invalid). Host-only, no CUDA call.
+ */
+size_t selective_scan_diag_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                                          int32_t io_dtype);
+
+/*
  * Status word of a workspace: waits for `stream`, then reports SSD_OK or the
  * first error a kernel recorded there during the last ssd_scan_chunked call
  * that used it (SSD_ERR_TIMEOUT when a bounded wait gave up). Every bounded

@@ -64,13 +64,18 @@ def load() -> ctypes.CDLL:
             lib.ssd_scan_chunked_noalloc.restype = ctypes.c_int
             lib.ssd_decode_step.argtypes = [dp] + [vp] * 9
             lib.selective_scan_diag.argtypes = [i64, i64, i64, i64, i32] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
+            lib.selective_scan_diag_ex.argtypes = ([i64, i64, i64, i64, i32] + [vp] * 8 + [i32, vp, ctypes.c_int]
+                                                   + [vp] * 3 + [sz, vp])
+            lib.selective_scan_diag_workspace_size.argtypes = [i64, i64, i64, i64, i32]
+            lib.selective_scan_diag_workspace_size.restype = sz
             lib.ssd_workspace_status.argtypes = [vp, vp]
             lib.ssd_selftest_bounded_wait.argtypes = [vp, ctypes.c_int, vp]
             lib.ssd_record_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
             lib.ssd_record_stage_events.restype = ctypes.c_int
             lib.ssd_last_error.argtypes = []
             lib.ssd_last_error.restype = ctypes.c_char_p
-            for f in (lib.ssd_scan_chunked, lib.ssd_decode_step, lib.selective_scan_diag, lib.ssd_workspace_status,
+            for f in (lib.ssd_scan_chunked, lib.ssd_decode_step, lib.selective_scan_diag, lib.selective_scan_diag_ex,
+                      lib.ssd_workspace_status,
                       lib.ssd_selftest_bounded_wait):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -213,10 +218,22 @@ def ssd_decode_step(state, x, dt, A, B, C, D=None, y=None, stream=None):
     return y
 
 
+def selective_scan_diag_workspace_size(batch, seqlen, dim, dstate, io_dtype) -> int:
+    """Bytes of scratch selective_scan_diag needs for its time-segmented scan
+    of this shape (0: one pass per sequence)."""
+    return int(load().selective_scan_diag_workspace_size(batch, seqlen, dim, dstate, _io_code(io_dtype)))
+
+
 def selective_scan_diag(x, dt, A, B, C, D=None, init_state=None, chunk_size=2048, y=None, final_state=None,
-                        stream=None, want_final_state=True):
+                        stream=None, want_final_state=True, z=None, delta_bias=None, delta_softplus=False,
+                        workspace=None, segmented=True):
     """Mamba-1 diagonal scan. x/dt[B,L,D], A[D,N], B/C[B,L,N], D[D],
-    init_state[B,D,N]. Returns (y, final_state)."""
+    init_state[B,D,N]; options of selective_scan_fn: z[B,L,D] (output gate
+    silu(z)), delta_bias[D] and delta_softplus (dt <- softplus(dt + bias)).
+    With segmented (default) the scratch of the time-segmented scan is taken
+    from `workspace` (uint8, at least selective_scan_diag_workspace_size
+    bytes) or allocated here; segmented=False runs one pass per sequence.
+    Returns (y, final_state)."""
     Bsz, L, Dm = x.shape
     N = A.shape[1]
     dev, io = x.device, x.dtype
@@ -226,6 +243,8 @@ def selective_scan_diag(x, dt, A, B, C, D=None, init_state=None, chunk_size=2048
     _need(B, "B", (Bsz, L, N), io, dev)
     _need(C, "C", (Bsz, L, N), io, dev)
     _need(D, "D", (Dm,), torch.float32, dev)
+    _need(z, "z", (Bsz, L, Dm), io, dev)
+    _need(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
     _need(init_state, "init_state", (Bsz, Dm, N), torch.float32, dev)
     if y is None:
         y = torch.empty_like(x)
@@ -233,9 +252,20 @@ def selective_scan_diag(x, dt, A, B, C, D=None, init_state=None, chunk_size=2048
     if final_state is None and want_final_state:
         final_state = torch.empty((Bsz, Dm, N), dtype=torch.float32, device=dev)
     _need(final_state, "final_state", (Bsz, Dm, N), torch.float32, dev)
-    _check(load().selective_scan_diag(Bsz, L, Dm, N, _io_code(io), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                                      _ptr(D), _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state),
-                                      _stream(stream, dev)))
+    ws_bytes = 0
+    if segmented:
+        need = selective_scan_diag_workspace_size(Bsz, L, Dm, N, io) if Bsz > 0 and L > 0 else 0
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None:
+            _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
+            ws_bytes = workspace.numel()
+    else:
+        workspace = None
+    _check(load().selective_scan_diag_ex(Bsz, L, Dm, N, _io_code(io), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                         _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+                                         _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state),
+                                         _ptr(workspace), ws_bytes, _stream(stream, dev)))
     return y, final_state
 
 

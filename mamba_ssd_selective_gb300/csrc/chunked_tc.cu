@@ -868,7 +868,6 @@ __global__ void __launch_bounds__(kScanPThreads, 1) chunk_scan_tc_persistent(con
             int64_t b, tile;
             int hg;
             decode(u, b, tile, hg);
-            const int64_t t0 = tile * kRows;
             // the item's cumulative sums and decays, from the scalar warp
             const uint32_t buf = ci & 1;
             pwait(&c_full[buf], (ci >> 1) & 1, s_fail);

@@ -58,10 +58,27 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream);
 cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool write_bf16,
                               cudaStream_t stream, bool programmatic, bool bf16_in = false);
 
-cudaError_t launch_diag(int io, int64_t B, int64_t L, int64_t Dm, int64_t N, const void *x, const void *dt,
-                        const float *A, const void *Bm, const void *Cm, const float *D,
-                        const float *init_state, int chunk, void *y, float *final_state,
-                        cudaStream_t stream);
+// Arguments of one Mamba-1 diagonal scan (layouts as in selective_scan_diag_ex);
+// z, delta_bias, D, init and final_state may be null. With nseg > 1 the
+// sequence is split into nseg time segments of seg_len tokens (a multiple of
+// 32) scanned in parallel; ws_h [nseg][B][Dm][N] and ws_s [nseg][B][Dm] (float32)
+// hold the per-segment states and step sums.
+struct DiagArgs {
+    int64_t B, L, Dm;
+    int N, chunk, softplus;
+    const void *x, *dt, *z, *Bm, *Cm;
+    const float *A, *D, *delta_bias, *init;
+    void *y;
+    float *final_state;
+    int nseg;
+    int64_t seg_len;
+    float *ws_h, *ws_s;
+};
+// Time segments the scan of this shape is split into (1: one pass per
+// sequence); the workspace the split needs is diag_workspace_bytes.
+int diag_segments(int64_t B, int64_t L, int64_t Dm, int64_t N, int io);
+size_t diag_workspace_bytes(int64_t B, int64_t L, int64_t Dm, int64_t N, int io);
+cudaError_t launch_diag(int io, const DiagArgs &a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 

@@ -177,10 +177,11 @@ ssd_status ssd_decode_step(const ssd_dims *dims, float *state, const void *x, co
     return ok();
 }
 
-ssd_status selective_scan_diag(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int32_t io_dtype,
-                               const void *x, const void *dt, const float *A, const void *B, const void *C,
-                               const float *D, const float *init_state, int chunk_size, void *y,
-                               float *final_state, cudaStream_t stream) {
+ssd_status selective_scan_diag_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int32_t io_dtype,
+                                  const void *x, const void *dt, const float *A, const void *B, const void *C,
+                                  const float *D, const void *z, const float *delta_bias, int32_t delta_softplus,
+                                  const float *init_state, int chunk_size, void *y, float *final_state,
+                                  void *workspace, size_t ws_bytes, cudaStream_t stream) {
     if (batch < 0 || seqlen < 0) return fail(SSD_ERR_INVALID_ARG, "batch and seqlen must be >= 0");
     if (dim < 1) return fail(SSD_ERR_INVALID_ARG, "dim must be >= 1");
     if (dstate < 1) return fail(SSD_ERR_INVALID_ARG, "dstate must be >= 1");
@@ -189,20 +190,68 @@ ssd_status selective_scan_diag(int64_t batch, int64_t seqlen, int64_t dim, int64
         return fail(SSD_ERR_INVALID_ARG, "io_dtype must be SSD_F32 or SSD_BF16 (got %d)", io_dtype);
     if (chunk_size < 32 || chunk_size % 32 != 0)
         return fail(SSD_ERR_INVALID_ARG, "chunk_size must be a positive multiple of 32 (got %d)", chunk_size);
+    if (delta_softplus != 0 && delta_softplus != 1)
+        return fail(SSD_ERR_INVALID_ARG, "delta_softplus must be 0 or 1 (got %d)", delta_softplus);
     if (batch > 65535) return fail(SSD_ERR_UNSUPPORTED, "batch must be <= 65535");
     const bool has_tokens = batch > 0 && seqlen > 0;
     if (has_tokens && (!x || !dt || !A || !B || !C || !y))
         return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C and y must be non-NULL");
     if (batch > 0 && !A) return fail(SSD_ERR_INVALID_ARG, "A must be non-NULL");
-    const void *ptrs[] = {x, dt, A, B, C, D, init_state, y, final_state};
-    const char *names[] = {"x", "dt", "A", "B", "C", "D", "init_state", "y", "final_state"};
-    for (int i = 0; i < 9; ++i)
+    const void *ptrs[] = {x, dt, A, B, C, D, z, delta_bias, init_state, y, final_state};
+    const char *names[] = {"x", "dt", "A", "B", "C", "D", "z", "delta_bias", "init_state", "y", "final_state"};
+    for (int i = 0; i < 11; ++i)
         if (ptrs[i] && !aligned(ptrs[i], 16)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
     if (batch == 0) return ok();
-    cudaError_t e = ssd::launch_diag(io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32, batch, seqlen, dim, dstate,
-                                     x, dt, A, B, C, D, init_state, chunk_size, y, final_state, stream);
+    const int io = io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32;
+    ssd::DiagArgs a{};
+    a.nseg = 1;
+    if (workspace) {
+        if (!aligned(workspace, 256)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+        const size_t need = ssd::diag_workspace_bytes(batch, seqlen, dim, dstate, io);
+        if (ws_bytes < need)
+            return fail(SSD_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", ws_bytes, need);
+        a.nseg = ssd::diag_segments(batch, seqlen, dim, dstate, io);
+        if (a.nseg > 1) {
+            a.ws_h = static_cast<float *>(workspace);
+            const size_t h = (size_t)a.nseg * batch * dim * dstate * sizeof(float);
+            a.ws_s = reinterpret_cast<float *>(static_cast<char *>(workspace) + (h + 255) / 256 * 256);
+        }
+    }
+    a.B = batch;
+    a.L = seqlen;
+    a.Dm = dim;
+    a.N = (int)dstate;
+    a.chunk = chunk_size;
+    a.softplus = delta_softplus;
+    a.x = x;
+    a.dt = dt;
+    a.z = z;
+    a.Bm = B;
+    a.Cm = C;
+    a.A = A;
+    a.D = D;
+    a.delta_bias = delta_bias;
+    a.init = init_state;
+    a.y = y;
+    a.final_state = final_state;
+    cudaError_t e = ssd::launch_diag(io, a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "selective_scan_diag");
     return ok();
+}
+
+ssd_status selective_scan_diag(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int32_t io_dtype,
+                               const void *x, const void *dt, const float *A, const void *B, const void *C,
+                               const float *D, const float *init_state, int chunk_size, void *y,
+                               float *final_state, cudaStream_t stream) {
+    return selective_scan_diag_ex(batch, seqlen, dim, dstate, io_dtype, x, dt, A, B, C, D, nullptr, nullptr, 0,
+                                  init_state, chunk_size, y, final_state, nullptr, 0, stream);
+}
+
+size_t selective_scan_diag_workspace_size(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                                          int32_t io_dtype) {
+    if (batch < 1 || seqlen < 1 || dim < 1 || dstate < 1 || dstate > 64) return 0;
+    if (io_dtype != SSD_F32 && io_dtype != SSD_BF16) return 0;
+    return ssd::diag_workspace_bytes(batch, seqlen, dim, dstate, io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32);
 }
 
 ssd_status ssd_record_stage_events(cudaEvent_t *events, int count) {

@@ -30,6 +30,7 @@ import numpy as np
 
 # stream ids, fixed forever: changing one changes every seeded workload
 _S_X, _S_DT_NOISE, _S_DT0, _S_A, _S_B, _S_C, _S_D, _S_STATE = 1, 2, 3, 4, 5, 6, 7, 8
+_S_Z = 9
 _S_DECODE_BASE = 1000  # decode step s uses streams _S_DECODE_BASE + 8*s + k
 
 
@@ -138,6 +139,29 @@ def diag_inputs(batch: int, seqlen: int, dim: int, dstate: int, io_dtype: str = 
     return out
 
 
+def diag_option_inputs(batch: int, seqlen: int, dim: int, dstate: int, io_dtype: str = "bf16",
+                       seed: int = 0, init_state: bool = False, bias: bool = True, z: bool = True,
+                       random_A: bool = False) -> dict:
+    """Inputs of a Mamba-1 scan run with delta_softplus: "dt" holds the raw
+    pre-activation step. With bias, dt = eps and delta_bias[D] (float32) is
+    the per-channel softplus^{-1} of a log-uniform target step in [1e-3, 1e-1];
+    without, dt = eps + bias rounded to the I/O dtype. eps ~ N(0, 0.5), so
+    softplus(dt + delta_bias) has the distribution of the other workloads'
+    steps. With z, a gate z[B,L,D] ~ N(0, 1)."""
+    out = diag_inputs(batch, seqlen, dim, dstate, io_dtype=io_dtype, seed=seed, init_state=init_state,
+                      random_A=random_A)
+    b = _dt_bias(_rng(seed, _S_DT0), dim)
+    eps = _rng(seed, _S_DT_NOISE).normal(0.0, 0.5, size=(batch, seqlen, dim))
+    if bias:
+        out["dt"] = round_to(eps, io_dtype)
+        out["delta_bias"] = round_to(b, "f32")
+    else:
+        out["dt"] = round_to(eps + b, io_dtype)
+        out["delta_bias"] = None
+    out["z"] = round_to(_rng(seed, _S_Z).standard_normal((batch, seqlen, dim)), io_dtype) if z else None
+    return out
+
+
 # The benchmark workloads, named by what they are.
 WORKLOADS = {
     "ssd_tiny_f32": dict(kind="ssd", batch=1, seqlen=256, nheads=4, headdim=64, dstate=16,
@@ -156,4 +180,8 @@ WORKLOADS = {
                            ngroups=1, io_dtype="bf16", steps=1000),
     "mamba1_B8_L2048_D5120": dict(kind="diag", batch=8, seqlen=2048, dim=5120, dstate=16,
                                   io_dtype="bf16", chunk=2048),
+    # selective_scan_fn as timed with delta_softplus set: batch 1, dim 1024,
+    # length 4096, d_state 16 (the pages ran fp16; bf16 here, same bytes)
+    "mamba1_B1_L4096_D1024_softplus": dict(kind="diag", batch=1, seqlen=4096, dim=1024, dstate=16,
+                                           io_dtype="bf16", chunk=2048, delta_softplus=True),
 }

@@ -127,6 +127,32 @@ def test_decode_and_diag_validation(lib):
     assert lib.ssd_selftest_bounded_wait(vp(0x1000), 0, None) == E
 
 
+def test_diag_ex_validation_and_workspace_size(lib):
+    from mamba_ssd_selective_gb300 import binding
+    vp = ctypes.c_void_p
+    E = binding.SSD_ERR_INVALID_ARG
+    # time segments only where one pass per sequence leaves the GPU idle
+    ws = lib.selective_scan_diag_workspace_size(1, 4096, 1024, 16, 1)
+    assert ws > 0 and ws >= 1024 * 16 * 4 * 2
+    assert lib.selective_scan_diag_workspace_size(8, 2048, 5120, 16, 1) == 0    # enough channels already
+    assert lib.selective_scan_diag_workspace_size(1, 4096, 1024, 16, 0) == 0    # float32 path: one pass
+    assert lib.selective_scan_diag_workspace_size(1, 100, 1024, 16, 1) == 0     # too short to split
+    assert lib.selective_scan_diag_workspace_size(1, 4096, 1024, 65, 1) == 0    # invalid dstate
+    assert lib.selective_scan_diag_workspace_size(0, 4096, 1024, 16, 1) == 0
+
+    def ex(softplus=0, z=None, bias=None, ws_ptr=None, ws_bytes=0, y=0x1000):
+        return lib.selective_scan_diag_ex(1, 4096, 1024, 16, 1, *[vp(0x1000)] * 5, None, z, bias, softplus, None,
+                                          64, vp(y) if y else None, None, ws_ptr, ws_bytes, None)
+    assert ex(softplus=2) == E
+    assert b"delta_softplus" in lib.ssd_last_error()
+    assert ex(z=vp(0x1008)) == E                                    # misaligned z
+    assert ex(bias=vp(0x1004)) == E                                 # misaligned delta_bias
+    assert ex(ws_ptr=vp(0x100010), ws_bytes=1 << 30) == E           # workspace not 256-aligned
+    assert ex(ws_ptr=vp(0x100000), ws_bytes=16) == E                # workspace too small
+    assert b"too small" in lib.ssd_last_error()
+    assert ex(y=0) == E                                             # NULL y
+
+
 def test_binding_checks_shapes_on_cpu_tensors():
     import torch
     from mamba_ssd_selective_gb300 import binding

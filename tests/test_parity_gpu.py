@@ -307,6 +307,106 @@ def test_diag_mamba1_workload_sampled(ssd):
             check_bf16(hh[:, i], hr[:, i], f"channel {c} state")
 
 
+def run_diag_opts(ssd, d, io, chunk, softplus=True, init=True):
+    t = IO_TORCH[io]
+    y, h = ssd.selective_scan_diag(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                   dev(d["D"]), dev(d["init_state"]) if init else None, chunk_size=chunk,
+                                   z=dev(d["z"], t) if d["z"] is not None else None,
+                                   delta_bias=dev(d["delta_bias"]) if d["delta_bias"] is not None else None,
+                                   delta_softplus=softplus)
+    torch.cuda.synchronize()
+    return y, h
+
+
+DIAG_OPTS = {"softplus_bias_z": (True, True, True), "softplus_bias": (True, True, False),
+             "z_only": (False, False, True), "bias_only": (False, True, False)}
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", sorted(DIAG_OPTS))
+@pytest.mark.parametrize("shape", [(2, 300, 256, 16), (2, 100, 136, 8), (1, 50, 72, 24), (1, 77, 130, 5)])
+def test_diag_options_every_element(ssd, io, opts, shape):
+    softplus, bias, z = DIAG_OPTS[opts]
+    Bz, L, Dm, N = shape
+    d = inputs.diag_option_inputs(Bz, L, Dm, N, io_dtype=io, seed=14, init_state=True, bias=bias, z=z,
+                                  random_A=True)
+    if not softplus:   # feed steps that are valid without the softplus
+        d["dt"] = inputs.round_to(np.abs(d["dt"]) * 0.05, io)
+        if d["delta_bias"] is not None:
+            d["delta_bias"] = np.abs(d["delta_bias"]) * 0.01
+    yr, hr = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], z=d["z"],
+                             delta_bias=d["delta_bias"], delta_softplus=softplus)
+    y, h = run_diag_opts(ssd, d, io, 64, softplus=softplus)
+    check(io, y, yr, "y")
+    check(io, h, hr, "final_state")
+
+
+@pytest.mark.parametrize("dim", [300, 320])
+def test_diag_options_chunk_size_bitwise_independent(ssd, dim):
+    d = inputs.diag_option_inputs(2, 1000, dim, 16, io_dtype="bf16", seed=16, init_state=True)
+    y0, h0 = run_diag_opts(ssd, d, "bf16", 32)
+    for c in (96, 256, 1024, 2048):
+        y, h = run_diag_opts(ssd, d, "bf16", c)
+        assert torch.equal(y, y0) and torch.equal(h, h0), f"chunk {c}"
+
+
+@pytest.mark.slow
+def test_diag_softplus_workload_sampled(ssd):
+    """B1 L4096 D1024 N16 with delta_softplus (the raw step carries its bias):
+    full size on the GPU, sampled channels through the oracle."""
+    w = inputs.WORKLOADS["mamba1_B1_L4096_D1024_softplus"]
+    d = inputs.diag_option_inputs(w["batch"], w["seqlen"], w["dim"], w["dstate"], io_dtype="bf16", seed=0,
+                                  bias=False, z=False)
+    chans = np.array([0, 5, 127, 128, 513, 1023])
+    yr, hr = oracle.diag_seq(d["x"][:, :, chans], d["dt"][:, :, chans], d["A"][chans], d["B"], d["C"],
+                             d["D"][chans], delta_softplus=True)
+    for chunk in (256, 2048):
+        y, h = run_diag_opts(ssd, d, "bf16", chunk, init=False)
+        yh, hh = host(y)[:, :, chans], host(h)[:, chans]
+        for i, c in enumerate(chans):
+            check_bf16(yh[:, :, i], yr[:, :, i], f"channel {c} y")
+            check_bf16(hh[:, i], hr[:, i], f"channel {c} state")
+
+
+@pytest.mark.parametrize("opts", ["none", "softplus_bias_z"])
+@pytest.mark.parametrize("shape", [(1, 1000, 64, 16), (2, 777, 136, 8), (1, 513, 72, 24), (1, 4096, 1024, 16)])
+def test_diag_time_segmented_scan(ssd, opts, shape):
+    """Small batch x dim, long sequence: the scan is cut into time segments
+    (ragged last segment); every element against the oracle, and within bf16
+    rounding of the one-pass scan of the same inputs."""
+    Bz, L, Dm, N = shape
+    assert ssd.selective_scan_diag_workspace_size(Bz, L, Dm, N, torch.bfloat16) > 0
+    if opts == "none":
+        d = inputs.diag_inputs(Bz, L, Dm, N, io_dtype="bf16", seed=17, init_state=True, random_A=True)
+        d.update(z=None, delta_bias=None)
+        softplus = False
+    else:
+        d = inputs.diag_option_inputs(Bz, L, Dm, N, io_dtype="bf16", seed=17, init_state=True, random_A=True)
+        softplus = True
+    yr, hr = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], z=d["z"],
+                             delta_bias=d["delta_bias"], delta_softplus=softplus)
+    y, h = run_diag_opts(ssd, d, "bf16", 64, softplus=softplus)
+    check_bf16(y, yr, "y")
+    check_bf16(h, hr, "final_state")
+    t = torch.bfloat16
+    y1, h1 = ssd.selective_scan_diag(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                     dev(d["D"]), dev(d["init_state"]), chunk_size=64,
+                                     z=dev(d["z"], t) if d["z"] is not None else None,
+                                     delta_bias=dev(d["delta_bias"]) if d["delta_bias"] is not None else None,
+                                     delta_softplus=softplus, segmented=False)
+    check_bf16(y, host(y1), "segmented vs one-pass y")
+    np.testing.assert_allclose(host(h), host(h1), rtol=1e-4, atol=1e-5)
+
+
+def test_diag_segmented_chunk_size_bitwise_independent(ssd):
+    d = inputs.diag_option_inputs(1, 3000, 128, 16, io_dtype="bf16", seed=18, init_state=True)
+    assert ssd.selective_scan_diag_workspace_size(1, 3000, 128, 16, torch.bfloat16) > 0
+    y0, h0 = run_diag_opts(ssd, d, "bf16", 32)
+    for c in (96, 256, 1024, 2048):
+        y, h = run_diag_opts(ssd, d, "bf16", c)
+        assert torch.equal(y, y0) and torch.equal(h, h0), f"chunk {c}"
+
+
 # ------------------------------------------------------- failure detection
 
 def test_bounded_wait_times_out_and_context_survives(ssd):
