@@ -347,6 +347,7 @@ def run_ours(args):
         "tflops": round(ssd_flops(w, best_q) / (ms_step / 1e3) / 1e12, 2),
         "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
         "chunk_sweep_ms_per_step": {str(k): round(v, 5) for k, v in sweep.items()},
+        "chunk_policy": binding.ssd_best_chunk(Bz, L, H, P, N, G, torch.bfloat16),
     }
 
     # ---------------- end to end through the C ABI with host buffers

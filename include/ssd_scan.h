@@ -81,6 +81,16 @@ typedef struct {
 size_t ssd_workspace_size(const ssd_dims *dims, int chunk_size);
 
 /*
+ * The chunk size (64, 128 or 256) a static policy picks for these sizes: the
+ * fastest measured on GB300 for the nearest shape of a sweep over batch 1-8,
+ * length 512-8192 and 24-80 heads (bf16, P = 64, N = 128), after the pages'
+ * static-oracle / table policies ("COREY ...", section 5.2). Shapes outside
+ * the tensor-core path get 128. Host-only, no CUDA call; 0 if the dims are
+ * invalid.
+ */
+int ssd_best_chunk(const ssd_dims *dims);
+
+/*
  * Chunked SSD prefill over a whole sequence (the SSD scan run "chunk by chunk,
  * each chunk continuing from the previous chunk's state", "Recurrence Scan",
  * first section; fixed-size chunking, "Compiler-First State Space Duality

@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
             dp = ctypes.POINTER(ssd_dims)
             lib.ssd_workspace_size.argtypes = [dp, ctypes.c_int]
             lib.ssd_workspace_size.restype = sz
+            lib.ssd_best_chunk.argtypes = [dp]
+            lib.ssd_best_chunk.restype = ctypes.c_int
             lib.ssd_scan_chunked.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp, sz, vp]
             lib.ssd_scan_chunked_noalloc.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
             lib.ssd_scan_chunked_noalloc.restype = ctypes.c_int
@@ -128,10 +130,17 @@ def ssd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, io_dtype
     return int(load().ssd_workspace_size(ctypes.byref(d), int(chunk_size)))
 
 
-def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=256, y=None, final_state=None,
+def ssd_best_chunk(batch, seqlen, nheads, headdim, dstate, ngroups, io_dtype) -> int:
+    """Chunk size of the library's static policy for these sizes (0: invalid)."""
+    d = _dims(batch, seqlen, nheads, headdim, dstate, ngroups, _io_code(io_dtype))
+    return int(load().ssd_best_chunk(ctypes.byref(d)))
+
+
+def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=None, y=None, final_state=None,
                      workspace=None, stream=None, simt=False, want_final_state=True):
     """Chunked SSD prefill. x[B,L,H,P], dt[B,L,H], B/C[B,L,G,N] (float32 or
-    bfloat16), A[H], D[H], init_state[B,H,P,N] (float32). Returns (y, final_state)."""
+    bfloat16), A[H], D[H], init_state[B,H,P,N] (float32). chunk_size None takes
+    the library's static policy (ssd_best_chunk). Returns (y, final_state)."""
     if x.dim() != 4 or B.dim() != 4:
         raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
     Bsz, L, H, P = x.shape
@@ -152,6 +161,8 @@ def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=256, y=
     _need(final_state, "final_state", (Bsz, H, P, N), torch.float32, dev)
     d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else 0)
     lib = load()
+    if chunk_size is None:
+        chunk_size = int(lib.ssd_best_chunk(ctypes.byref(d))) or 128
     ws_bytes = int(lib.ssd_workspace_size(ctypes.byref(d), int(chunk_size)))
     if ws_bytes == 0:
         _check(lib.ssd_scan_chunked(ctypes.byref(d), None, None, None, None, None, None, None, int(chunk_size),

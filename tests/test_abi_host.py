@@ -127,6 +127,24 @@ def test_decode_and_diag_validation(lib):
     assert lib.ssd_selftest_bounded_wait(vp(0x1000), 0, None) == E
 
 
+def test_best_chunk_policy(lib):
+    from mamba_ssd_selective_gb300 import binding
+    pick = lambda **kw: lib.ssd_best_chunk(ctypes.byref(_dims(binding, **kw)))
+    bf = dict(headdim=64, dstate=128, io_dtype=1)
+    assert pick(batch=1, seqlen=4096, nheads=24, **bf) == 128     # 130M-shaped layer
+    for L in (1024, 4096, 8192):
+        assert pick(batch=1, seqlen=L, nheads=80, **bf) == 128    # 2.7B-shaped layers
+    assert pick(batch=8, seqlen=2048, nheads=80, **bf) == 128
+    assert pick(batch=1, seqlen=512, nheads=24, **bf) == 64       # the one grid point where 64 won
+    for b, L, h in ((3, 700, 30), (16, 65536, 128), (1, 1, 1), (5, 3000, 64)):   # off the grid
+        assert pick(batch=b, seqlen=L, nheads=h, **bf) in (64, 128, 256)
+    assert pick(batch=1, seqlen=4096, nheads=4, headdim=64, dstate=16, io_dtype=0) == 128   # CUDA-core shapes
+    assert lib.ssd_best_chunk(None) == 0
+    assert pick(batch=1, seqlen=4096, nheads=6, ngroups=4) == 0  # H % G != 0
+    assert pick(batch=0) == 0
+    assert binding.ssd_best_chunk(1, 4096, 24, 64, 128, 1, __import__("torch").bfloat16) == 128
+
+
 def test_diag_ex_validation_and_workspace_size(lib):
     from mamba_ssd_selective_gb300 import binding
     vp = ctypes.c_void_p

@@ -76,6 +76,19 @@ def test_prefill_tensor_core_head_groups(ssd, shape):
     check("bf16", h, hr, "final_state")
 
 
+@pytest.mark.parametrize("shape", [(1, 512, 24, 64, 128, 1), (2, 777, 8, 64, 128, 2)])
+def test_prefill_policy_chunk(ssd, shape):
+    """chunk_size=None takes the static policy's chunk; every element against
+    the oracle."""
+    Bz, L, H, P, N, G = shape
+    assert ssd.ssd_best_chunk(Bz, L, H, P, N, G, torch.bfloat16) in (64, 128, 256)
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=19, init_state=True)
+    yr, hr = ref_scan(d)
+    y, h = run_scan(ssd, d, "bf16", None)
+    check("bf16", y, yr, "y")
+    check("bf16", h, hr, "final_state")
+
+
 @pytest.mark.parametrize("simt", [False, True])
 @pytest.mark.parametrize("chunk", [64, 128, 256])
 def test_prefill_m2_130m_workload_full(ssd, chunk, simt):
