@@ -54,7 +54,10 @@ def _load():
         lib.oracle_ssd_decode.argtypes = [i64] * 5 + [dp] * 8 + [ci]
         lib.oracle_diag_seq.argtypes = [i64] * 4 + [dp] * 9 + [ci]
         lib.oracle_diag_seq_ex.argtypes = [i64] * 4 + [dp] * 8 + [ci] + [dp] * 3 + [ci]
-        for f in (lib.oracle_ssd_seq, lib.oracle_ssd_decode, lib.oracle_diag_seq, lib.oracle_diag_seq_ex):
+        lib.oracle_conv1d_step.argtypes = [i64] * 3 + [dp] * 4 + [ci, dp]
+        lib.oracle_gated_rmsnorm.argtypes = [i64] * 3 + [dp] * 3 + [ctypes.c_double, dp]
+        for f in (lib.oracle_ssd_seq, lib.oracle_ssd_decode, lib.oracle_diag_seq, lib.oracle_diag_seq_ex,
+                  lib.oracle_conv1d_step, lib.oracle_gated_rmsnorm):
             f.restype = ci
         _lib = lib
     return _lib
@@ -152,3 +155,54 @@ def diag_seq(x, dt, A, B, C, D=None, init_state=None, threads=None, z=None, delt
     if rc != 0:
         raise ValueError("oracle_diag_seq: invalid sizes")
     return y, hT
+
+
+def conv1d_step(state, x, w, bias=None, silu=True):
+    """One causal depthwise convolution step in float64.
+
+    state[B,C,W] (the last W inputs, oldest first) is updated in place (it
+    must be a float64 C-contiguous array); x[B,C], w[C,W], bias[C] or None.
+    Returns out[B,C] = act(sum_k w[c,k] * window[k] + bias[c]).
+    """
+    if not (isinstance(state, np.ndarray) and state.dtype == np.float64 and state.flags.c_contiguous):
+        raise TypeError("state must be a C-contiguous float64 array (updated in place)")
+    Bsz, C, W = state.shape
+    x = _f64(x, (Bsz, C), "x")
+    w = _f64(w, (C, W), "w")
+    bias = _f64(bias, (C,), "bias")
+    out = np.empty((Bsz, C))
+    if _load().oracle_conv1d_step(Bsz, C, W, _ptr(state), _ptr(x), _ptr(w), _ptr(bias), int(bool(silu)),
+                                  _ptr(out)) != 0:
+        raise ValueError("oracle_conv1d_step: invalid sizes")
+    return out
+
+
+def gated_rmsnorm(y, z, w, group=None, eps=1e-5):
+    """Gated RMS norm in float64: g = y * silu(z) (z None: g = y), then per
+    group of `group` channels (default: all) g / sqrt(mean(g^2) + eps) * w."""
+    y = _f64(y)
+    Bsz, D = y.shape
+    z = _f64(z, (Bsz, D), "z")
+    w = _f64(w, (D,), "w")
+    group = D if group is None else int(group)
+    out = np.empty((Bsz, D))
+    if _load().oracle_gated_rmsnorm(Bsz, D, group, _ptr(y), _ptr(z), _ptr(w), float(eps), _ptr(out)) != 0:
+        raise ValueError("oracle_gated_rmsnorm: invalid sizes")
+    return out
+
+
+def decode_layer_step(conv_state, ssm_state, xBC, conv_w, conv_b, dt, A, D, z, norm_w, nheads, headdim, dstate,
+                      ngroups, group=None, eps=1e-5):
+    """One token of the Mamba-2 decode layer body in float64, states updated
+    in place: xBC <- silu(causal conv step of xBC); x, B, C = split(xBC)
+    (H*P, G*N, G*N channels); y = SSD decode step; out = gated RMS norm of y
+    with gate z. conv_state[B,Cc,W], ssm_state[B,H,P,N] float64 arrays."""
+    Bsz = xBC.shape[0]
+    H, P, N, G = nheads, headdim, dstate, ngroups
+    xc = conv1d_step(conv_state, xBC, conv_w, conv_b, silu=True)
+    x = xc[:, :H * P].reshape(Bsz, H, P)
+    Bm = xc[:, H * P:H * P + G * N].reshape(Bsz, G, N)
+    Cm = xc[:, H * P + G * N:].reshape(Bsz, G, N)
+    y, st = ssd_decode(ssm_state, x, dt, A, Bm, Cm, D)
+    ssm_state[...] = st
+    return gated_rmsnorm(y.reshape(Bsz, H * P), z, norm_w, group, eps)

@@ -34,12 +34,23 @@
  *   and an optional gate z[B,L,Dm] multiplies the output by silu(z):
  *       out_t = y_t * z_t / (1 + exp(-z_t)).
  *
+ *   Decode-layer neighbours (the fused Mamba-2 decode layer sketched on
+ *   "Mamba-2 SSD fused layer via VGpuWarp — design sketch", section "What has
+ *   to become a device op", items 1 and 2):
+ *     causal conv step, per (b, c), with a rolling window of the last W
+ *     inputs, oldest first:  window <- (window[1..W-1], x_t);
+ *       out = act(sum_k w[c,k] * window[k] + bias[c]), act = identity or silu;
+ *     gated RMS norm, per (b, group of channels):  g = y * silu(z);
+ *       out = g / sqrt(mean over the group of g^2 + eps) * w.
+ *
  * Layouts (row-major, innermost last):
  *   SSD:    x[B,L,H,P]  dt[B,L,H]  A[H]  Bm,Cm[B,L,G,N]  D[H]  state[B,H,P,N]
  *           y[B,L,H,P]
  *   decode: x[B,H,P]    dt[B,H]    A[H]  Bm,Cm[B,G,N]    D[H]  state[B,H,P,N]
  *           y[B,H,P]
  *   diag:   x,dt[B,L,Dm]  A[Dm,N]  Bm,Cm[B,L,N]  D[Dm]  state[B,Dm,N]  y[B,L,Dm]
+ *   conv:   x[B,C]  window state[B,C,W]  w[C,W]  bias[C]  out[B,C]
+ *   norm:   y,z[B,D]  w[D]  out[B,D]
  * D and the initial state may be NULL (read as zero); a NULL final state is
  * not written. Independent (b,h) or (b,d) units run on nthreads POSIX threads.
  */
@@ -215,4 +226,42 @@ int oracle_diag_seq(int64_t B, int64_t L, int64_t Dm, int64_t N, const double *x
                     int nthreads) {
     return oracle_diag_seq_ex(B, L, Dm, N, x, dt, A, Bm, Cm, D, NULL, NULL, 0, init_state, y,
                               final_state, nthreads);
+}
+
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* One causal depthwise convolution step, the window updated in place. */
+int oracle_conv1d_step(int64_t B, int64_t C, int64_t W, double *state, const double *x, const double *w,
+                       const double *bias, int act, double *out) {
+    if (B < 0 || C < 1 || W < 1) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t c = 0; c < C; ++c) {
+            double *win = state + (b * C + c) * W;
+            for (int64_t k = 0; k + 1 < W; ++k) win[k] = win[k + 1];
+            win[W - 1] = x[b * C + c];
+            double acc = bias ? bias[c] : 0.0;
+            for (int64_t k = 0; k < W; ++k) acc += w[c * W + k] * win[k];
+            out[b * C + c] = act ? silu(acc) : acc;
+        }
+    return 0;
+}
+
+/* Gated RMS norm over groups of `group` consecutive channels (D % group == 0). */
+int oracle_gated_rmsnorm(int64_t B, int64_t D, int64_t group, const double *y, const double *z, const double *w,
+                         double eps, double *out) {
+    if (B < 0 || D < 1 || group < 1 || D % group != 0) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g0 = 0; g0 < D; g0 += group) {
+            double ss = 0.0;
+            for (int64_t i = g0; i < g0 + group; ++i) {
+                const double g = y[b * D + i] * (z ? silu(z[b * D + i]) : 1.0);
+                ss += g * g;
+            }
+            const double r = 1.0 / sqrt(ss / (double)group + eps);
+            for (int64_t i = g0; i < g0 + group; ++i) {
+                const double g = y[b * D + i] * (z ? silu(z[b * D + i]) : 1.0);
+                out[b * D + i] = g * r * w[i];
+            }
+        }
+    return 0;
 }

@@ -29,6 +29,15 @@ MUTANTS = {
     "softplus_wrong_branch": ("v + log1p(exp(-v))", "v + log1p(exp(v))"),
     "gate_before_D": ("out *= zt / (1.0 + exp(-zt));", "out = acc * (zt / (1.0 + exp(-zt))) + Dd * xt;"),
     "gate_sigmoid_only": ("out *= zt / (1.0 + exp(-zt));", "out *= 1.0 / (1.0 + exp(-zt));"),
+    "conv_window_newest_first": ("for (int64_t k = 0; k + 1 < W; ++k) win[k] = win[k + 1];\n            win[W - 1] = x[b * C + c];",
+                                 "for (int64_t k = W - 1; k > 0; --k) win[k] = win[k - 1];\n            win[0] = x[b * C + c];"),
+    "conv_bias_dropped": ("double acc = bias ? bias[c] : 0.0;", "double acc = 0.0;"),
+    "conv_no_activation": ("out[b * C + c] = act ? silu(acc) : acc;", "out[b * C + c] = acc;"),
+    "norm_sum_not_mean": ("const double r = 1.0 / sqrt(ss / (double)group + eps);", "const double r = 1.0 / sqrt(ss + eps);"),
+    "norm_gate_after": ("const double g = y[b * D + i] * (z ? silu(z[b * D + i]) : 1.0);\n                ss += g * g;",
+                        "const double g = y[b * D + i];\n                ss += g * g;"),
+    "norm_sigmoid_gate": ("static double silu(double v) { return v / (1.0 + exp(-v)); }",
+                          "static double silu(double v) { return 1.0 / (1.0 + exp(-v)); }"),
 }
 
 PINS = [
@@ -38,6 +47,9 @@ PINS = [
     pins.test_mamba2_equals_mamba1_with_tied_decay, pins.test_diag_lfilter_constant_dt,
     pins.test_diag_delta_bias_and_softplus_reduce_to_transformed_dt, pins.test_diag_softplus_of_large_steps,
     pins.test_diag_z_gate_is_silu_of_z, pins.test_diag_options_single_token_closed_form,
+    pins.test_conv_step_sequence_is_numpy_convolve, pins.test_conv_step_continues_from_its_window,
+    pins.test_gated_rmsnorm_invariants, pins.test_gated_rmsnorm_gate_ratio_and_eps,
+    pins.test_decode_layer_matches_conv_then_prefill_then_norm,
 ]
 
 
@@ -53,7 +65,8 @@ def test_pins_reject_mutant(name, tmp_path, monkeypatch):
                    check=True)
     oracle._load()  # make sure the real library's argtypes are set up first
     lib = ctypes.CDLL(str(so))
-    for fname in ("oracle_ssd_seq", "oracle_ssd_decode", "oracle_diag_seq", "oracle_diag_seq_ex"):
+    for fname in ("oracle_ssd_seq", "oracle_ssd_decode", "oracle_diag_seq", "oracle_diag_seq_ex",
+                  "oracle_conv1d_step", "oracle_gated_rmsnorm"):
         getattr(lib, fname).argtypes = getattr(oracle._lib, fname).argtypes
         getattr(lib, fname).restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)

@@ -359,6 +359,114 @@ def test_diag_options_single_token_closed_form():
                 assert abs(h[b, ch, n] - s_ * xv * d["B"][b, 0, n]) <= 1e-14 * max(1.0, abs(h[b, ch, n]))
 
 
+def test_conv_step_sequence_is_numpy_convolve():
+    """T causal conv steps from a zero window equal the causal convolution of
+    the input sequence with the reversed taps (numpy.convolve), plus bias;
+    silu on top equals v * sigmoid(v) with scipy's sigmoid."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(40)
+    Bz, C, W, T = 2, 5, 4, 23
+    xs = rng.standard_normal((T, Bz, C))
+    w = rng.standard_normal((C, W))
+    bias = rng.standard_normal(C)
+    for silu in (False, True):
+        st = np.zeros((Bz, C, W))
+        outs = np.stack([oracle.conv1d_step(st, xs[t], w, bias, silu=silu) for t in range(T)])
+        for b in range(Bz):
+            for c in range(C):
+                ref = np.convolve(xs[:, b, c], w[c, ::-1])[:T] + bias[c]
+                if silu:
+                    ref = ref * special.expit(ref)
+                np.testing.assert_allclose(outs[:, b, c], ref, rtol=1e-13, atol=1e-14)
+        # the window keeps the last W inputs, oldest first
+        np.testing.assert_array_equal(st, np.moveaxis(xs[T - W:], 0, -1))
+
+
+def test_conv_step_continues_from_its_window():
+    """A window filled by earlier steps makes the next outputs those of the
+    unsplit sequence (numpy.convolve over the concatenation)."""
+    rng = np.random.default_rng(41)
+    C, W, T0, T1 = 3, 3, 7, 9
+    xs = rng.standard_normal((T0 + T1, 1, C))
+    w = rng.standard_normal((C, W))
+    st = np.zeros((1, C, W))
+    for t in range(T0):
+        oracle.conv1d_step(st, xs[t], w, None, silu=False)
+    outs = np.stack([oracle.conv1d_step(st, xs[T0 + t], w, None, silu=False) for t in range(T1)])
+    for c in range(C):
+        ref = np.convolve(xs[:, 0, c], w[c, ::-1])[T0:T0 + T1]
+        np.testing.assert_allclose(outs[:, 0, c], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_gated_rmsnorm_invariants():
+    """With unit weights and eps = 0 every group of the output has RMS 1; the
+    output is invariant to scaling y; groups are independent; a gate of +40
+    (silu(40) = 40 to 1e-17) is no gate at all; a zero gate gives zero."""
+    rng = np.random.default_rng(42)
+    Bz, D, grp = 3, 24, 8
+    y = rng.standard_normal((Bz, D))
+    z = rng.standard_normal((Bz, D))
+    one = np.ones(D)
+    out = oracle.gated_rmsnorm(y, z, one, grp, eps=0.0)
+    rms = np.sqrt((out.reshape(Bz, D // grp, grp) ** 2).mean(-1))
+    np.testing.assert_allclose(rms, 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(7.5 * y, z, one, grp, eps=0.0), out, rtol=1e-13, atol=1e-14)
+    part = oracle.gated_rmsnorm(y[:, 8:16], z[:, 8:16], one[8:16], grp, eps=0.0)
+    np.testing.assert_allclose(part, out[:, 8:16], rtol=1e-13, atol=1e-14)
+    w = rng.standard_normal(D)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(y, np.full((Bz, D), 40.0), w, grp, eps=1e-5),
+                               oracle.gated_rmsnorm(40.0 * y, None, w, grp, eps=1e-5), rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(oracle.gated_rmsnorm(y, np.zeros((Bz, D)), w, grp, eps=1e-5), 0.0)
+
+
+def test_gated_rmsnorm_gate_ratio_and_eps():
+    """y = 1 everywhere: outputs are proportional to silu(z) = z * sigmoid(z)
+    (scipy's sigmoid); and eps enters as sqrt(mean(g^2) + eps)."""
+    special = pytest.importorskip("scipy.special")
+    z = np.array([[0.7, -1.3, 2.2, 0.1]])
+    out = oracle.gated_rmsnorm(np.ones((1, 4)), z, np.ones(4), eps=0.0)
+    s_ = z * special.expit(z)
+    np.testing.assert_allclose(out / out[0, 0], s_ / s_[0, 0], rtol=1e-13)
+    # one channel: out = y / sqrt(y^2 + eps)
+    for yv, eps in ((0.3, 0.5), (2.0, 1e-5)):
+        o = oracle.gated_rmsnorm(np.array([[yv]]), None, np.ones(1), eps=eps)
+        assert abs(o[0, 0] - yv / math.sqrt(yv * yv + eps)) <= 1e-15
+
+
+def test_decode_layer_matches_conv_then_prefill_then_norm():
+    """T decode-layer steps from zero states equal the whole-sequence
+    pipeline built from other pinned pieces: numpy's causal convolution of
+    xBC with silu, the SSD prefill oracle on the split x | B | C, and the
+    gated norm of each token."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(43)
+    Bz, H, P, N, G, W, T = 2, 4, 3, 5, 2, 4, 11
+    Cc = H * P + 2 * G * N
+    xBC = rng.standard_normal((T, Bz, Cc))
+    cw, cb = rng.standard_normal((Cc, W)) * 0.5, rng.standard_normal(Cc) * 0.1
+    dt = np.exp(rng.uniform(np.log(1e-2), np.log(0.3), size=(T, Bz, H)))
+    A = -np.exp(rng.uniform(0, np.log(8), size=H))
+    Dv = rng.uniform(0.5, 1.5, size=H)
+    z = rng.standard_normal((T, Bz, H * P))
+    nw = rng.uniform(0.5, 1.5, size=H * P)
+    cst, sst = np.zeros((Bz, Cc, W)), np.zeros((Bz, H, P, N))
+    outs = np.stack([oracle.decode_layer_step(cst, sst, xBC[t], cw, cb, dt[t], A, Dv, z[t], nw, H, P, N, G,
+                                              group=P * 2, eps=1e-5) for t in range(T)])
+    conv = np.empty_like(xBC)
+    for b in range(Bz):
+        for c in range(Cc):
+            v = np.convolve(xBC[:, b, c], cw[c, ::-1])[:T] + cb[c]
+            conv[:, b, c] = v * special.expit(v)
+    x = np.moveaxis(conv[:, :, :H * P], 0, 1).reshape(Bz, T, H, P)
+    Bm = np.moveaxis(conv[:, :, H * P:H * P + G * N], 0, 1).reshape(Bz, T, G, N)
+    Cm = np.moveaxis(conv[:, :, H * P + G * N:], 0, 1).reshape(Bz, T, G, N)
+    y, hT = oracle.ssd_seq(x, np.moveaxis(dt, 0, 1), A, Bm, Cm, Dv)
+    for t in range(T):
+        ref = oracle.gated_rmsnorm(y[:, t].reshape(Bz, H * P), z[t], nw, P * 2, eps=1e-5)
+        np.testing.assert_allclose(outs[t], ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sst, hT, rtol=1e-11, atol=1e-13)
+
+
 def test_diag_split_resume():
     d = inputs.diag_inputs(2, 50, 6, 4, io_dtype="f32", seed=12, init_state=True)
     yf, hf = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"])
