@@ -449,6 +449,8 @@ def run_ours(args):
     # ---------------- decode workload
     if not args.skip_extra:
         out["decode"] = bench_decode(torch, binding, inputs, dev, hbm_peak, peaks["source"], W)
+        out["decode_layer"] = [bench_decode_layer(torch, binding, inputs, dev, hbm_peak, name, W)
+                               for name in ("decode_layer_B64_H80", "decode_layer_B1_H128_G8")]
         out["mamba1"] = bench_mamba1(torch, binding, inputs, dev, hbm_peak, peaks["source"], K, W)
         out["mamba1_softplus"] = bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W)
 
@@ -475,6 +477,57 @@ def run_ours(args):
     if clocks is not None:
         line["clocks"] = clocks
     print(json.dumps(line), flush=True)
+
+
+def bench_decode_layer(torch, binding, inputs, dev, hbm_peak, name, W):
+    """The decode layer body (conv step, SSD decode step, gated norm) over
+    `steps` tokens as one CUDA graph the library captures; per-step inputs are
+    separate slices (16 generated steps repeated, > L2 in total)."""
+    w = inputs.WORKLOADS[name]
+    Bz, H, P, N, G, Wc, steps = (w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["width"],
+                                 w["steps"])
+    bf = torch.bfloat16
+    Cc = H * P + 2 * G * N
+
+    def t_(a, dtype=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+    prm = inputs.decode_layer_params(Bz, H, P, N, G, Wc, seed=0)
+    pool = [inputs.decode_layer_step_inputs(k, Bz, H, P, N, G, io_dtype="bf16", seed=0) for k in range(16)]
+    xBC = torch.empty((steps, Bz, Cc), dtype=bf, device=dev)
+    dts = torch.empty((steps, Bz, H), dtype=bf, device=dev)
+    zs = torch.empty((steps, Bz, H * P), dtype=bf, device=dev)
+    for k, src in enumerate(pool):
+        xBC[k].copy_(t_(src["xBC"], bf))
+        dts[k].copy_(t_(src["dt"], bf))
+        zs[k].copy_(t_(src["z"], bf))
+    for k in range(len(pool), steps):
+        for buf in (xBC, dts, zs):
+            buf[k].copy_(buf[k % len(pool)])
+    cst, sst = t_(prm["conv_state"]), t_(prm["ssm_state"])
+    cw, cb, A, Dv, nw = t_(prm["conv_w"]), t_(prm["conv_b"]), t_(prm["A"]), t_(prm["D"]), t_(prm["norm_w"])
+    graph = binding.DecodeGraph(xBC, cst, cw, cb, dts, A, Dv, sst, zs, nw, norm_group=w["norm_group"])
+    try:
+        for _ in range(max(W, 3)):
+            graph.launch()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        e0.record()
+        for _ in range(reps):
+            graph.launch()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+    finally:
+        graph.close()
+    nbytes = (2 * Bz * H * P * N * 4 + 2 * Bz * Cc * Wc * 4 + Bz * Cc * 2 + Cc * Wc * 4 + Cc * 4
+              + Bz * H * 2 + 2 * Bz * H * P * 2 + H * P * 4 + 2 * H * 4)
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"workload": name, "us_per_step": round(us, 3), "steps_per_s": round(1e6 / us, 1),
+            "kernels_per_step": 3, "gpu_launches": 3 * steps * reps, "algorithmic_bytes_per_step": nbytes,
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+            "graph": f"{steps} steps captured by ssd_decode_graph_create, one launch"}
 
 
 def bench_decode(torch, binding, inputs, dev, hbm_peak, peak_src, W):

@@ -275,6 +275,85 @@ ssd_status ssd_selftest_bounded_wait(void *workspace, int spin_limit, cudaStream
  */
 ssd_status ssd_record_stage_events(cudaEvent_t *events, int count);
 
+/* ---------------------------------------------------------------------------
+ * Decode-layer neighbours of ssd_decode_step: the pieces of a Mamba-2 decode
+ * layer body that must run on the device so that a token's layer stays
+ * resident and can be replayed as one CUDA graph ("Mamba-2 SSD fused layer via
+ * VGpuWarp — design sketch", section "What has to become a device op",
+ * items 1 and 2, and section "The concrete mechanism").
+ * ------------------------------------------------------------------------- */
+
+typedef enum { SSD_ACT_NONE = 0, SSD_ACT_SILU = 1 } ssd_activation;
+
+/*
+ * One step of a causal depthwise convolution with a rolling window, per
+ * (b, c): the window holds the last `width` inputs, oldest first; x shifts in
+ * (the oldest value drops out), then
+ *     out[b,c] = act(sum_k weight[c,k] * window[b,c,k] + bias[c]).
+ *   x          [batch, channels]          io_dtype
+ *   conv_state [batch, channels, width]   float32, updated in place
+ *   weight     [channels, width]          float32
+ *   bias       [channels]                 float32, may be NULL (0)
+ *   activation SSD_ACT_NONE or SSD_ACT_SILU (v * sigmoid(v))
+ *   out        [batch, channels]          io_dtype, written (may not alias x)
+ * Limits: 1 <= width <= 8. Pointers 16-byte aligned. Errors as for the scans.
+ */
+ssd_status ssd_conv1d_step(int64_t batch, int64_t channels, int64_t width, int32_t io_dtype, const void *x,
+                           float *conv_state, const float *weight, const float *bias, int32_t activation,
+                           void *out, cudaStream_t stream);
+
+/*
+ * Gated RMS norm over groups of `group` consecutive channels:
+ *     g = y * silu(z)                 (z NULL: g = y)
+ *     out = g / sqrt(mean over the group of g^2 + eps) * weight
+ *   y, z, out  [batch, dim]  io_dtype (out may alias y)
+ *   weight     [dim]         float32
+ * Limits: dim % group == 0, eps >= 0. One CTA per (b, group).
+ */
+ssd_status ssd_gated_rmsnorm(int64_t batch, int64_t dim, int64_t group, int32_t io_dtype, const void *y,
+                             const void *z, const float *weight, float eps, void *out, cudaStream_t stream);
+
+/*
+ * One token of the decode layer body, in three kernels on `stream`:
+ *     xBC' = silu(causal conv step of xBC)          (conv_state updated)
+ *     x, B, C = the H*P, G*N and G*N channels of xBC'
+ *     y = ssd_decode_step(x, dt, B, C)              (ssm_state updated)
+ *     out = gated RMS norm of y with gate z over groups of norm_group
+ *   dims       batch, nheads H, headdim P, dstate N, ngroups G, io_dtype
+ *              (seqlen and flags ignored); conv channels Cc = H*P + 2*G*N
+ *   xBC        [batch, Cc] io_dtype        conv_state [batch, Cc, conv_width] f32
+ *   conv_weight [Cc, conv_width] f32       conv_bias [Cc] f32, may be NULL
+ *   dt         [batch, H] io_dtype (used as given)   A [H] f32   D [H] f32, may be NULL
+ *   ssm_state  [batch, H, P, N] f32        z [batch, H*P] io_dtype, may be NULL
+ *   norm_weight [H*P] f32                  out [batch, H*P] io_dtype
+ *   workspace  ssd_decode_layer_workspace_size(dims) bytes, 256-byte aligned:
+ *              holds x, B, C and y of the step in io_dtype.
+ */
+size_t ssd_decode_layer_workspace_size(const ssd_dims *dims);
+ssd_status ssd_decode_layer_step(const ssd_dims *dims, int64_t conv_width, const void *xBC, float *conv_state,
+                                 const float *conv_weight, const float *conv_bias, const void *dt, const float *A,
+                                 const float *D, float *ssm_state, const void *z, const float *norm_weight,
+                                 int64_t norm_group, float eps, void *out, void *workspace, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/*
+ * A decode loop of `steps` layer steps captured once as a CUDA graph and
+ * replayed with one launch. Step s reads xBC + s*batch*Cc, dt + s*batch*H and
+ * z + s*batch*H*P (elements of io_dtype) and writes out + s*batch*H*P; the
+ * states carry from step to step. Arguments as for ssd_decode_layer_step; all
+ * buffers must stay valid while the graph exists. Creation allocates the
+ * graph (host and driver resources) and captures on a private stream; launch
+ * allocates nothing; destroy releases the graph.
+ */
+typedef struct ssd_decode_graph ssd_decode_graph;
+ssd_status ssd_decode_graph_create(const ssd_dims *dims, int64_t conv_width, int32_t steps, const void *xBC,
+                                   float *conv_state, const float *conv_weight, const float *conv_bias,
+                                   const void *dt, const float *A, const float *D, float *ssm_state, const void *z,
+                                   const float *norm_weight, int64_t norm_group, float eps, void *out,
+                                   void *workspace, size_t ws_bytes, ssd_decode_graph **graph);
+ssd_status ssd_decode_graph_launch(ssd_decode_graph *graph, cudaStream_t stream);
+ssd_status ssd_decode_graph_destroy(ssd_decode_graph *graph);
+
 /* Thread-local description of the last error returned on this thread. */
 const char *ssd_last_error(void);
 

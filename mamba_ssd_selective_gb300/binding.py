@@ -61,6 +61,19 @@ def load() -> ctypes.CDLL:
             lib.ssd_workspace_size.restype = sz
             lib.ssd_best_chunk.argtypes = [dp]
             lib.ssd_best_chunk.restype = ctypes.c_int
+            f32 = ctypes.c_float
+            lib.ssd_conv1d_step.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp]
+            lib.ssd_gated_rmsnorm.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, vp, vp]
+            lib.ssd_decode_layer_workspace_size.argtypes = [dp]
+            lib.ssd_decode_layer_workspace_size.restype = sz
+            lib.ssd_decode_layer_step.argtypes = [dp, i64] + [vp] * 10 + [i64, f32, vp, vp, sz, vp]
+            lib.ssd_decode_graph_create.argtypes = [dp, i64, i32] + [vp] * 10 + [i64, f32, vp, vp, sz,
+                                                                                 ctypes.POINTER(vp)]
+            lib.ssd_decode_graph_launch.argtypes = [vp, vp]
+            lib.ssd_decode_graph_destroy.argtypes = [vp]
+            for f in (lib.ssd_conv1d_step, lib.ssd_gated_rmsnorm, lib.ssd_decode_layer_step,
+                      lib.ssd_decode_graph_create, lib.ssd_decode_graph_launch, lib.ssd_decode_graph_destroy):
+                f.restype = ctypes.c_int
             lib.ssd_scan_chunked.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp, sz, vp]
             lib.ssd_scan_chunked_noalloc.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
             lib.ssd_scan_chunked_noalloc.restype = ctypes.c_int
@@ -298,3 +311,119 @@ def ssd_record_stage_events(events) -> None:
 
 def ssd_selftest_bounded_wait(workspace, spin_limit, stream=None) -> None:
     _check(load().ssd_selftest_bounded_wait(_ptr(workspace), int(spin_limit), _stream(stream, workspace.device)))
+
+
+# ------------------------------------------------------- decode-layer pieces
+
+def conv1d_step(x, conv_state, weight, bias=None, silu=True, out=None, stream=None):
+    """Causal depthwise convolution step: x[B,C] shifts into the window
+    conv_state[B,C,W] (float32, in place); returns act(weight . window + bias)."""
+    Bsz, C = x.shape
+    W = conv_state.shape[2]
+    dev, io = x.device, x.dtype
+    _need(conv_state, "conv_state", (Bsz, C, W), torch.float32, dev)
+    _need(weight, "weight", (C, W), torch.float32, dev)
+    _need(bias, "bias", (C,), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", (Bsz, C), io, dev)
+    _check(load().ssd_conv1d_step(Bsz, C, W, _io_code(io), _ptr(x), _ptr(conv_state), _ptr(weight), _ptr(bias),
+                                  1 if silu else 0, _ptr(out), _stream(stream, dev)))
+    return out
+
+
+def gated_rmsnorm(y, z, weight, group=None, eps=1e-5, out=None, stream=None):
+    """out = g / sqrt(mean over each group of g^2 + eps) * weight, g = y * silu(z)."""
+    Bsz, D = y.shape
+    dev, io = y.device, y.dtype
+    _need(z, "z", (Bsz, D), io, dev)
+    _need(weight, "weight", (D,), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(y)
+    _need(out, "out", (Bsz, D), io, dev)
+    _check(load().ssd_gated_rmsnorm(Bsz, D, D if group is None else int(group), _io_code(io), _ptr(y), _ptr(z),
+                                    _ptr(weight), float(eps), _ptr(out), _stream(stream, dev)))
+    return out
+
+
+def _layer_args(xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z, norm_weight, norm_group, out,
+                workspace, steps=None):
+    lead = () if steps is None else (steps,)
+    Bsz, H, P, N = ssm_state.shape
+    Cc = xBC.shape[-1]
+    W = conv_state.shape[2]
+    G = (Cc - H * P) // (2 * N)
+    if G < 1 or H * P + 2 * G * N != Cc:
+        raise ValueError(f"xBC has {Cc} channels; expected H*P + 2*G*N for some G")
+    dev, io = xBC.device, xBC.dtype
+    _need(xBC, "xBC", lead + (Bsz, Cc), io, dev)
+    _need(conv_state, "conv_state", (Bsz, Cc, W), torch.float32, dev)
+    _need(conv_weight, "conv_weight", (Cc, W), torch.float32, dev)
+    _need(conv_bias, "conv_bias", (Cc,), torch.float32, dev)
+    _need(dt, "dt", lead + (Bsz, H), io, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(D, "D", (H,), torch.float32, dev)
+    _need(ssm_state, "ssm_state", (Bsz, H, P, N), torch.float32, dev)
+    _need(z, "z", lead + (Bsz, H * P), io, dev)
+    _need(norm_weight, "norm_weight", (H * P,), torch.float32, dev)
+    if out is None:
+        out = torch.empty(lead + (Bsz, H * P), dtype=io, device=dev)
+    _need(out, "out", lead + (Bsz, H * P), io, dev)
+    d = _dims(Bsz, 1, H, P, N, G, _io_code(io))
+    need = int(load().ssd_decode_layer_workspace_size(ctypes.byref(d)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
+    group = H * P if norm_group is None else int(norm_group)
+    return d, W, group, out, workspace
+
+
+def decode_layer_step(xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z, norm_weight,
+                      norm_group=None, eps=1e-5, out=None, workspace=None, stream=None):
+    """One token of the decode layer body (conv step + silu, SSD decode step,
+    gated RMS norm), states updated in place. xBC[B, H*P + 2*G*N], conv_state
+    [B, Cc, W], ssm_state[B,H,P,N] float32, dt[B,H], z[B, H*P]. Returns out[B, H*P]."""
+    d, W, group, out, workspace = _layer_args(xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z,
+                                              norm_weight, norm_group, out, workspace)
+    _check(load().ssd_decode_layer_step(ctypes.byref(d), W, _ptr(xBC), _ptr(conv_state), _ptr(conv_weight),
+                                        _ptr(conv_bias), _ptr(dt), _ptr(A), _ptr(D), _ptr(ssm_state), _ptr(z),
+                                        _ptr(norm_weight), group, float(eps), _ptr(out), _ptr(workspace),
+                                        workspace.numel(), _stream(stream, xBC.device)))
+    return out
+
+
+class DecodeGraph:
+    """`steps` decode-layer steps captured once as a CUDA graph by the library
+    (ssd_decode_graph_create) and replayed with one launch. xBC[steps,B,Cc],
+    dt[steps,B,H], z[steps,B,H*P] and out[steps,B,H*P] hold the per-step
+    inputs and outputs; every tensor must outlive the graph."""
+
+    def __init__(self, xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z, norm_weight,
+                 norm_group=None, eps=1e-5, out=None, workspace=None):
+        steps = xBC.shape[0]
+        d, W, group, out, workspace = _layer_args(xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z,
+                                                  norm_weight, norm_group, out, workspace, steps=steps)
+        self.out, self._keep = out, (xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z,
+                                     norm_weight, workspace)
+        h = ctypes.c_void_p()
+        _check(load().ssd_decode_graph_create(ctypes.byref(d), W, steps, _ptr(xBC), _ptr(conv_state),
+                                              _ptr(conv_weight), _ptr(conv_bias), _ptr(dt), _ptr(A), _ptr(D),
+                                              _ptr(ssm_state), _ptr(z), _ptr(norm_weight), group, float(eps),
+                                              _ptr(out), _ptr(workspace), workspace.numel(), ctypes.byref(h)))
+        self._h = h
+        self.device = xBC.device
+
+    def launch(self, stream=None):
+        _check(load().ssd_decode_graph_launch(self._h, _stream(stream, self.device)))
+        return self.out
+
+    def close(self):
+        if self._h:
+            _check(load().ssd_decode_graph_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

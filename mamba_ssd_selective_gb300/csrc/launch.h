@@ -80,6 +80,30 @@ int diag_segments(int64_t B, int64_t L, int64_t Dm, int64_t N, int io);
 size_t diag_workspace_bytes(int64_t B, int64_t L, int64_t Dm, int64_t N, int io);
 cudaError_t launch_diag(int io, const DiagArgs &a, cudaStream_t stream);
 
+// Causal depthwise convolution step (layouts as in ssd_conv1d_step). The
+// output of channel c goes to out[s] for the first segment s with
+// c < seg_end[s]; seg_end[2] == C. One segment: seg_end = {C, C, C}.
+struct ConvArgs {
+    int64_t B, C;
+    int W, act;
+    const void *x;
+    float *state;
+    const float *w, *bias;
+    void *out[3];
+    int64_t seg_end[3];
+};
+cudaError_t launch_conv1d_step(int io, const ConvArgs &a, cudaStream_t stream);
+
+// Gated RMS norm over groups of `group` channels (layouts as in ssd_gated_rmsnorm).
+struct NormArgs {
+    int64_t B, D, group;
+    float eps;
+    const void *y, *z;
+    const float *w;
+    void *out;
+};
+cudaError_t launch_gated_rmsnorm(int io, const NormArgs &a, cudaStream_t stream);
+
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 
 // Sets the thread-local text returned by ssd_last_error() and returns `status`.

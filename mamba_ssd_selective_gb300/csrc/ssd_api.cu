@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <new>
 
 #include "launch.h"
 #include "ssd_scan.h"
@@ -252,6 +253,261 @@ size_t selective_scan_diag_workspace_size(int64_t batch, int64_t seqlen, int64_t
     if (batch < 1 || seqlen < 1 || dim < 1 || dstate < 1 || dstate > 64) return 0;
     if (io_dtype != SSD_F32 && io_dtype != SSD_BF16) return 0;
     return ssd::diag_workspace_bytes(batch, seqlen, dim, dstate, io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32);
+}
+
+// ------------------------------------------------------ decode-layer pieces
+
+namespace {
+
+size_t io_size(int32_t io) { return io == SSD_BF16 ? 2 : 4; }
+
+struct LayerWs {
+    size_t x, b, c, y, total;
+};
+LayerWs layer_ws(const ssd_dims *d) {
+    const size_t e = io_size(d->io_dtype), hp = (size_t)(d->batch * d->nheads * d->headdim);
+    const size_t gn = (size_t)(d->batch * d->ngroups * d->dstate);
+    LayerWs w{};
+    w.x = 0;
+    w.b = round256(hp * e);
+    w.c = w.b + round256(gn * e);
+    w.y = w.c + round256(gn * e);
+    w.total = w.y + round256(hp * e);
+    return w;
+}
+
+// Validation shared by the layer step and the graph capture.
+ssd_status check_layer(const ssd_dims *dims, int64_t conv_width, const void *xBC, const float *conv_state,
+                       const float *conv_weight, const float *conv_bias, const void *dt, const float *A,
+                       const float *D, const float *ssm_state, const void *z, const float *norm_weight,
+                       int64_t norm_group, float eps, const void *out, const void *workspace, size_t ws_bytes) {
+    ssd_status s = check_dims(dims, false);
+    if (s != SSD_OK) return s;
+    if (conv_width < 1 || conv_width > 8)
+        return fail(SSD_ERR_INVALID_ARG, "conv_width must be 1..8 (got %lld)", (long long)conv_width);
+    const int64_t hp = dims->nheads * dims->headdim;
+    if (norm_group < 1 || hp % norm_group != 0)
+        return fail(SSD_ERR_INVALID_ARG, "norm_group must divide nheads*headdim (got %lld)", (long long)norm_group);
+    if (!(eps >= 0.f)) return fail(SSD_ERR_INVALID_ARG, "eps must be >= 0");
+    if (dims->batch == 0) return SSD_OK;
+    if (!xBC || !conv_state || !conv_weight || !dt || !A || !ssm_state || !norm_weight || !out || !workspace)
+        return fail(SSD_ERR_INVALID_ARG,
+                    "xBC, conv_state, conv_weight, dt, A, ssm_state, norm_weight, out and workspace must be non-NULL");
+    const void *ptrs[] = {xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z, norm_weight, out};
+    const char *names[] = {"xBC", "conv_state", "conv_weight", "conv_bias", "dt", "A", "D", "ssm_state", "z",
+                           "norm_weight", "out"};
+    for (int i = 0; i < 11; ++i)
+        if (ptrs[i] && !aligned(ptrs[i], 16)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    if (!aligned(workspace, 256)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    const size_t need = layer_ws(dims).total;
+    if (ws_bytes < need) return fail(SSD_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", ws_bytes, need);
+    return SSD_OK;
+}
+
+cudaError_t layer_launch(const ssd_dims *d, int64_t conv_width, const void *xBC, float *conv_state,
+                         const float *conv_weight, const float *conv_bias, const void *dt, const float *A,
+                         const float *D, float *ssm_state, const void *z, const float *norm_weight,
+                         int64_t norm_group, float eps, void *out, void *workspace, cudaStream_t stream) {
+    const int io = d->io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32;
+    const LayerWs w = layer_ws(d);
+    char *ws = static_cast<char *>(workspace);
+    const int64_t hp = d->nheads * d->headdim, gn = d->ngroups * d->dstate;
+    ssd::ConvArgs c{};
+    c.B = d->batch;
+    c.C = hp + 2 * gn;
+    c.W = (int)conv_width;
+    c.act = 1;
+    c.x = xBC;
+    c.state = conv_state;
+    c.w = conv_weight;
+    c.bias = conv_bias;
+    c.out[0] = ws + w.x;
+    c.out[1] = ws + w.b;
+    c.out[2] = ws + w.c;
+    c.seg_end[0] = hp;
+    c.seg_end[1] = hp + gn;
+    c.seg_end[2] = hp + 2 * gn;
+    cudaError_t e = ssd::launch_conv1d_step(io, c, stream);
+    if (e != cudaSuccess) return e;
+    e = ssd::launch_decode(io, d->batch, d->nheads, d->headdim, d->dstate, d->ngroups, ssm_state, ws + w.x, dt, A,
+                           ws + w.b, ws + w.c, D, ws + w.y, stream);
+    if (e != cudaSuccess) return e;
+    ssd::NormArgs n{};
+    n.B = d->batch;
+    n.D = hp;
+    n.group = norm_group;
+    n.eps = eps;
+    n.y = ws + w.y;
+    n.z = z;
+    n.w = norm_weight;
+    n.out = out;
+    return ssd::launch_gated_rmsnorm(io, n, stream);
+}
+
+}  // namespace
+
+ssd_status ssd_conv1d_step(int64_t batch, int64_t channels, int64_t width, int32_t io_dtype, const void *x,
+                           float *conv_state, const float *weight, const float *bias, int32_t activation,
+                           void *out, cudaStream_t stream) {
+    if (batch < 0) return fail(SSD_ERR_INVALID_ARG, "batch must be >= 0");
+    if (channels < 1) return fail(SSD_ERR_INVALID_ARG, "channels must be >= 1");
+    if (width < 1 || width > 8) return fail(SSD_ERR_INVALID_ARG, "width must be 1..8 (got %lld)", (long long)width);
+    if (io_dtype != SSD_F32 && io_dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "io_dtype must be SSD_F32 or SSD_BF16 (got %d)", io_dtype);
+    if (activation != SSD_ACT_NONE && activation != SSD_ACT_SILU)
+        return fail(SSD_ERR_INVALID_ARG, "activation must be SSD_ACT_NONE or SSD_ACT_SILU (got %d)", activation);
+    if (batch * channels > ((int64_t)1 << 38)) return fail(SSD_ERR_UNSUPPORTED, "batch * channels too large");
+    if (batch == 0) return ok();
+    if (!x || !conv_state || !weight || !out)
+        return fail(SSD_ERR_INVALID_ARG, "x, conv_state, weight and out must be non-NULL");
+    const void *ptrs[] = {x, conv_state, weight, bias, out};
+    const char *names[] = {"x", "conv_state", "weight", "bias", "out"};
+    for (int i = 0; i < 5; ++i)
+        if (ptrs[i] && !aligned(ptrs[i], 16)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    if (x == out) return fail(SSD_ERR_INVALID_ARG, "out may not alias x");
+    ssd::ConvArgs c{};
+    c.B = batch;
+    c.C = channels;
+    c.W = (int)width;
+    c.act = activation;
+    c.x = x;
+    c.state = conv_state;
+    c.w = weight;
+    c.bias = bias;
+    c.out[0] = c.out[1] = c.out[2] = out;
+    c.seg_end[0] = c.seg_end[1] = c.seg_end[2] = channels;
+    cudaError_t e = ssd::launch_conv1d_step(io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32, c, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_conv1d_step");
+    return ok();
+}
+
+ssd_status ssd_gated_rmsnorm(int64_t batch, int64_t dim, int64_t group, int32_t io_dtype, const void *y,
+                             const void *z, const float *weight, float eps, void *out, cudaStream_t stream) {
+    if (batch < 0) return fail(SSD_ERR_INVALID_ARG, "batch must be >= 0");
+    if (dim < 1 || group < 1 || dim % group != 0)
+        return fail(SSD_ERR_INVALID_ARG, "dim must be a positive multiple of group (dim %lld, group %lld)",
+                    (long long)dim, (long long)group);
+    if (io_dtype != SSD_F32 && io_dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "io_dtype must be SSD_F32 or SSD_BF16 (got %d)", io_dtype);
+    if (!(eps >= 0.f)) return fail(SSD_ERR_INVALID_ARG, "eps must be >= 0");
+    if (batch * (dim / group) > 0x7fffffffLL) return fail(SSD_ERR_UNSUPPORTED, "batch * dim / group too large");
+    if (batch == 0) return ok();
+    if (!y || !weight || !out) return fail(SSD_ERR_INVALID_ARG, "y, weight and out must be non-NULL");
+    const void *ptrs[] = {y, z, weight, out};
+    const char *names[] = {"y", "z", "weight", "out"};
+    for (int i = 0; i < 4; ++i)
+        if (ptrs[i] && !aligned(ptrs[i], 16)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    ssd::NormArgs n{};
+    n.B = batch;
+    n.D = dim;
+    n.group = group;
+    n.eps = eps;
+    n.y = y;
+    n.z = z;
+    n.w = weight;
+    n.out = out;
+    cudaError_t e = ssd::launch_gated_rmsnorm(io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32, n, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_gated_rmsnorm");
+    return ok();
+}
+
+size_t ssd_decode_layer_workspace_size(const ssd_dims *dims) {
+    if (!dims || dims->batch < 1 || dims->nheads < 1 || dims->headdim < 1 || dims->dstate < 1 ||
+        dims->ngroups < 1 || dims->nheads % dims->ngroups != 0 ||
+        (dims->io_dtype != SSD_F32 && dims->io_dtype != SSD_BF16))
+        return 0;
+    return layer_ws(dims).total;
+}
+
+ssd_status ssd_decode_layer_step(const ssd_dims *dims, int64_t conv_width, const void *xBC, float *conv_state,
+                                 const float *conv_weight, const float *conv_bias, const void *dt, const float *A,
+                                 const float *D, float *ssm_state, const void *z, const float *norm_weight,
+                                 int64_t norm_group, float eps, void *out, void *workspace, size_t ws_bytes,
+                                 cudaStream_t stream) {
+    ssd_status s = check_layer(dims, conv_width, xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z,
+                               norm_weight, norm_group, eps, out, workspace, ws_bytes);
+    if (s != SSD_OK) return s;
+    if (dims->batch == 0) return ok();
+    cudaError_t e = layer_launch(dims, conv_width, xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z,
+                                 norm_weight, norm_group, eps, out, workspace, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_decode_layer_step");
+    return ok();
+}
+
+struct ssd_decode_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+ssd_status ssd_decode_graph_create(const ssd_dims *dims, int64_t conv_width, int32_t steps, const void *xBC,
+                                   float *conv_state, const float *conv_weight, const float *conv_bias,
+                                   const void *dt, const float *A, const float *D, float *ssm_state, const void *z,
+                                   const float *norm_weight, int64_t norm_group, float eps, void *out,
+                                   void *workspace, size_t ws_bytes, ssd_decode_graph **graph) {
+    if (!graph) return fail(SSD_ERR_INVALID_ARG, "graph is NULL");
+    *graph = nullptr;
+    if (steps < 1) return fail(SSD_ERR_INVALID_ARG, "steps must be >= 1 (got %d)", steps);
+    ssd_status s = check_layer(dims, conv_width, xBC, conv_state, conv_weight, conv_bias, dt, A, D, ssm_state, z,
+                               norm_weight, norm_group, eps, out, workspace, ws_bytes);
+    if (s != SSD_OK) return s;
+    if (dims->batch == 0) return fail(SSD_ERR_INVALID_ARG, "batch must be >= 1 for a decode graph");
+    const size_t e = io_size(dims->io_dtype);
+    const int64_t hp = dims->nheads * dims->headdim, cc = hp + 2 * dims->ngroups * dims->dstate;
+    const size_t step_xbc = (size_t)(dims->batch * cc) * e, step_dt = (size_t)(dims->batch * dims->nheads) * e;
+    const size_t step_hp = (size_t)(dims->batch * hp) * e;
+    if (step_xbc % 16 || step_dt % 16 || step_hp % 16)
+        return fail(SSD_ERR_INVALID_ARG, "per-step slices of xBC, dt, z and out must be multiples of 16 bytes");
+    cudaStream_t st = nullptr;
+    cudaError_t ce = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (ce != cudaSuccess) return cuda_fail(ce, "ssd_decode_graph_create: stream");
+    cudaGraph_t g = nullptr;
+    ce = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+    if (ce == cudaSuccess) {
+        cudaError_t le = cudaSuccess;
+        for (int32_t k = 0; k < steps && le == cudaSuccess; ++k)
+            le = layer_launch(dims, conv_width, static_cast<const char *>(xBC) + k * step_xbc, conv_state,
+                              conv_weight, conv_bias, static_cast<const char *>(dt) + k * step_dt, A, D, ssm_state,
+                              z ? static_cast<const char *>(z) + k * step_hp : nullptr, norm_weight, norm_group,
+                              eps, static_cast<char *>(out) + k * step_hp, workspace, st);
+        ce = cudaStreamEndCapture(st, &g);
+        if (le != cudaSuccess) ce = le;
+    }
+    cudaStreamDestroy(st);
+    if (ce != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return cuda_fail(ce, "ssd_decode_graph_create: capture");
+    }
+    cudaGraphExec_t ex = nullptr;
+    ce = cudaGraphInstantiate(&ex, g, 0);
+    if (ce != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return cuda_fail(ce, "ssd_decode_graph_create: instantiate");
+    }
+    auto *h = new (std::nothrow) ssd_decode_graph{g, ex};
+    if (!h) {
+        cudaGraphExecDestroy(ex);
+        cudaGraphDestroy(g);
+        return fail(SSD_ERR_CUDA, "ssd_decode_graph_create: out of host memory");
+    }
+    *graph = h;
+    return ok();
+}
+
+ssd_status ssd_decode_graph_launch(ssd_decode_graph *graph, cudaStream_t stream) {
+    if (!graph) return fail(SSD_ERR_INVALID_ARG, "graph is NULL");
+    cudaError_t e = cudaGraphLaunch(graph->exec, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_decode_graph_launch");
+    return ok();
+}
+
+ssd_status ssd_decode_graph_destroy(ssd_decode_graph *graph) {
+    if (!graph) return ok();
+    cudaError_t e1 = cudaGraphExecDestroy(graph->exec);
+    cudaError_t e2 = cudaGraphDestroy(graph->graph);
+    delete graph;
+    if (e1 != cudaSuccess) return cuda_fail(e1, "ssd_decode_graph_destroy");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "ssd_decode_graph_destroy");
+    return ok();
 }
 
 ssd_status ssd_record_stage_events(cudaEvent_t *events, int count) {

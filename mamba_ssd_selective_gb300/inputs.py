@@ -31,6 +31,8 @@ import numpy as np
 # stream ids, fixed forever: changing one changes every seeded workload
 _S_X, _S_DT_NOISE, _S_DT0, _S_A, _S_B, _S_C, _S_D, _S_STATE = 1, 2, 3, 4, 5, 6, 7, 8
 _S_Z = 9
+_S_CONV_W, _S_CONV_B, _S_NORM_W, _S_CONV_STATE = 10, 11, 12, 13
+_S_LAYER_BASE = 100000  # decode-layer step s uses streams _S_LAYER_BASE + 4*s + k
 _S_DECODE_BASE = 1000  # decode step s uses streams _S_DECODE_BASE + 8*s + k
 
 
@@ -162,6 +164,39 @@ def diag_option_inputs(batch: int, seqlen: int, dim: int, dstate: int, io_dtype:
     return out
 
 
+def decode_layer_params(batch: int, nheads: int, headdim: int, dstate: int, ngroups: int, width: int = 4,
+                        seed: int = 0, conv_state: bool = True) -> dict:
+    """Constants and initial states of a decode layer body: conv_w[Cc,W] ~
+    U(-1/sqrt(W), 1/sqrt(W)), conv_b[Cc] ~ U(-0.1, 0.1), norm_w[H*P] ~
+    U(0.5, 1.5), A/D as the decode workload, conv window[B,Cc,W] ~ N(0, 1)
+    (or zeros), SSM state[B,H,P,N] ~ N(0, 0.1); Cc = H*P + 2*G*N."""
+    Cc = nheads * headdim + 2 * ngroups * dstate
+    r = 1.0 / np.sqrt(width)
+    out = dict(decode_params(nheads, seed))
+    out.update(
+        conv_w=round_to(_rng(seed, _S_CONV_W).uniform(-r, r, size=(Cc, width)), "f32"),
+        conv_b=round_to(_rng(seed, _S_CONV_B).uniform(-0.1, 0.1, size=Cc), "f32"),
+        norm_w=round_to(_rng(seed, _S_NORM_W).uniform(0.5, 1.5, size=nheads * headdim), "f32"),
+        conv_state=(round_to(_rng(seed, _S_CONV_STATE).standard_normal((batch, Cc, width)), "f32") if conv_state
+                    else np.zeros((batch, Cc, width))),
+        ssm_state=decode_state(batch, nheads, headdim, dstate, seed),
+    )
+    return out
+
+
+def decode_layer_step_inputs(step: int, batch: int, nheads: int, headdim: int, dstate: int, ngroups: int,
+                             io_dtype: str = "bf16", seed: int = 0) -> dict:
+    """Per-token inputs of decode-layer step ``step``: xBC[B, H*P + 2*G*N] ~
+    N(0, 1), dt[B,H] as the decode workload, gate z[B, H*P] ~ N(0, 1)."""
+    base = _S_LAYER_BASE + 4 * int(step)
+    Cc = nheads * headdim + 2 * ngroups * dstate
+    return {
+        "xBC": round_to(_rng(seed, base + 0).standard_normal((batch, Cc)), io_dtype),
+        "dt": _dt(seed, (batch, nheads), nheads, base + 1, io_dtype),
+        "z": round_to(_rng(seed, base + 2).standard_normal((batch, nheads * headdim)), io_dtype),
+    }
+
+
 # The benchmark workloads, named by what they are.
 WORKLOADS = {
     "ssd_tiny_f32": dict(kind="ssd", batch=1, seqlen=256, nheads=4, headdim=64, dstate=16,
@@ -180,6 +215,14 @@ WORKLOADS = {
                            ngroups=1, io_dtype="bf16", steps=1000),
     "mamba1_B8_L2048_D5120": dict(kind="diag", batch=8, seqlen=2048, dim=5120, dstate=16,
                                   io_dtype="bf16", chunk=2048),
+    # decode layer body (conv step + silu, SSD decode step, gated RMS norm) as
+    # one captured graph of 1000 steps: the decode workload's shape with a
+    # width-4 conv, and the layer of the fused-decode sketch (d_inner 8192,
+    # 128 heads, 8 groups, conv_dim 10240, norm over all of d_inner)
+    "decode_layer_B64_H80": dict(kind="decode_layer", batch=64, nheads=80, headdim=64, dstate=128, ngroups=1,
+                                 width=4, norm_group=5120, io_dtype="bf16", steps=1000),
+    "decode_layer_B1_H128_G8": dict(kind="decode_layer", batch=1, nheads=128, headdim=64, dstate=128, ngroups=8,
+                                    width=4, norm_group=8192, io_dtype="bf16", steps=1000),
     # selective_scan_fn as timed with delta_softplus set: batch 1, dim 1024,
     # length 4096, d_state 16 (the pages ran fp16; bf16 here, same bytes)
     "mamba1_B1_L4096_D1024_softplus": dict(kind="diag", batch=1, seqlen=4096, dim=1024, dstate=16,

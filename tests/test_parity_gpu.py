@@ -420,6 +420,102 @@ def test_diag_segmented_chunk_size_bitwise_independent(ssd):
         assert torch.equal(y, y0) and torch.equal(h, h0), f"chunk {c}"
 
 
+# ------------------------------------------------- decode-layer neighbours
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("width", [2, 3, 4, 5])
+@pytest.mark.parametrize("shape", [(3, 77), (2, 5376)])
+def test_conv1d_step_every_element(ssd, io, width, shape):
+    """Six steps on one window: every output element against the oracle, and
+    the window (copies of inputs, no arithmetic) bit-exact."""
+    Bz, C = shape
+    rng = np.random.default_rng(50 + width)
+    t = IO_TORCH[io]
+    w = inputs.round_to(rng.uniform(-0.5, 0.5, size=(C, width)), "f32")
+    bias = inputs.round_to(rng.uniform(-0.1, 0.1, size=C), "f32") if width != 3 else None
+    st0 = inputs.round_to(rng.standard_normal((Bz, C, width)), "f32")
+    ref_st = st0.copy()
+    g_st = dev(st0)
+    for step in range(6):
+        x = inputs.round_to(rng.standard_normal((Bz, C)), io)
+        silu = step % 2 == 0
+        ref = oracle.conv1d_step(ref_st, x, w, bias, silu=silu)
+        out = ssd.conv1d_step(dev(x, t), g_st, dev(w), dev(bias), silu=silu)
+        torch.cuda.synchronize()
+        check(io, out, ref, f"step {step} out")
+        np.testing.assert_array_equal(host(g_st), ref_st)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("gate", [True, False])
+@pytest.mark.parametrize("shape", [(3, 512, 512), (3, 512, 128), (64, 5120, 5120), (2, 8192, 1024), (1, 96, 32)])
+def test_gated_rmsnorm_every_element(ssd, io, gate, shape):
+    Bz, D, grp = shape
+    rng = np.random.default_rng(60)
+    t = IO_TORCH[io]
+    y = inputs.round_to(rng.standard_normal((Bz, D)), io)
+    z = inputs.round_to(rng.standard_normal((Bz, D)), io) if gate else None
+    w = inputs.round_to(rng.uniform(0.5, 1.5, size=D), "f32")
+    ref = oracle.gated_rmsnorm(y, z, w, grp, eps=1e-5)
+    out = ssd.gated_rmsnorm(dev(y, t), dev(z, t), dev(w), grp, eps=1e-5)
+    torch.cuda.synchronize()
+    check(io, out, ref, "out")
+
+
+def _layer_case(Bz, H, P, N, G, W, io, steps, seed=7):
+    prm = inputs.decode_layer_params(Bz, H, P, N, G, W, seed=seed)
+    st = [inputs.decode_layer_step_inputs(k, Bz, H, P, N, G, io_dtype=io, seed=seed) for k in range(steps)]
+    return prm, st
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 4, 64, 128, 2, 4, 128), (3, 6, 32, 16, 3, 3, 96), (1, 128, 64, 128, 8, 4, 8192)])
+def test_decode_layer_steps_match_oracle(ssd, io, shape):
+    """Eight layer steps (conv + silu, SSD decode step, gated norm): every
+    output element each step and both states at the end, against the oracle."""
+    Bz, H, P, N, G, W, grp = shape
+    t = IO_TORCH[io]
+    prm, steps = _layer_case(Bz, H, P, N, G, W, io, 8)
+    cst, sst = prm["conv_state"].copy(), prm["ssm_state"].copy()
+    g_cst, g_sst = dev(prm["conv_state"]), dev(prm["ssm_state"])
+    for k, s_ in enumerate(steps):
+        ref = oracle.decode_layer_step(cst, sst, s_["xBC"], prm["conv_w"], prm["conv_b"], s_["dt"], prm["A"],
+                                       prm["D"], s_["z"], prm["norm_w"], H, P, N, G, group=grp, eps=1e-5)
+        out = ssd.decode_layer_step(dev(s_["xBC"], t), g_cst, dev(prm["conv_w"]), dev(prm["conv_b"]),
+                                    dev(s_["dt"], t), dev(prm["A"]), dev(prm["D"]), g_sst, dev(s_["z"], t),
+                                    dev(prm["norm_w"]), norm_group=grp, eps=1e-5)
+        torch.cuda.synchronize()
+        check(io, out, ref, f"step {k} out")
+    np.testing.assert_array_equal(host(g_cst), cst)
+    check(io, g_sst, sst, "ssm_state after 8 steps")
+
+
+def test_decode_graph_equals_eager_steps(ssd):
+    """A 16-step loop captured by the library as one CUDA graph gives the
+    same bits as 16 eager layer steps; a second launch continues the states."""
+    Bz, H, P, N, G, W, K = 4, 8, 64, 128, 1, 4, 16
+    t = torch.bfloat16
+    prm, steps = _layer_case(Bz, H, P, N, G, W, "bf16", K, seed=9)
+    xBC = dev(np.stack([s_["xBC"] for s_ in steps]), t)
+    dt = dev(np.stack([s_["dt"] for s_ in steps]), t)
+    z = dev(np.stack([s_["z"] for s_ in steps]), t)
+    consts = [dev(prm["conv_w"]), dev(prm["conv_b"])]
+    A, Dv, nw = dev(prm["A"]), dev(prm["D"]), dev(prm["norm_w"])
+    e_cst, e_sst = dev(prm["conv_state"]), dev(prm["ssm_state"])
+    g_cst, g_sst = dev(prm["conv_state"]), dev(prm["ssm_state"])
+    graph = ssd.DecodeGraph(xBC, g_cst, *consts, dt, A, Dv, g_sst, z, nw, norm_group=P)
+    try:
+        for rep in range(2):
+            eager = torch.stack([ssd.decode_layer_step(xBC[k], e_cst, *consts, dt[k], A, Dv, e_sst, z[k], nw,
+                                                       norm_group=P) for k in range(K)])
+            out = graph.launch()
+            torch.cuda.synchronize()
+            assert torch.equal(out, eager), f"launch {rep}: outputs differ"
+            assert torch.equal(g_cst, e_cst) and torch.equal(g_sst, e_sst), f"launch {rep}: states differ"
+    finally:
+        graph.close()
+
+
 # ------------------------------------------------------- failure detection
 
 def test_bounded_wait_times_out_and_context_survives(ssd):
