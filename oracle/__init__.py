@@ -55,9 +55,10 @@ def _load():
         lib.oracle_diag_seq.argtypes = [i64] * 4 + [dp] * 9 + [ci]
         lib.oracle_diag_seq_ex.argtypes = [i64] * 4 + [dp] * 8 + [ci] + [dp] * 3 + [ci]
         lib.oracle_conv1d_step.argtypes = [i64] * 3 + [dp] * 4 + [ci, dp]
+        lib.oracle_ssd_seq_bwd.argtypes = [i64] * 6 + [dp] * 16 + [ci]
         lib.oracle_gated_rmsnorm.argtypes = [i64] * 3 + [dp] * 3 + [ctypes.c_double, dp]
         for f in (lib.oracle_ssd_seq, lib.oracle_ssd_decode, lib.oracle_diag_seq, lib.oracle_diag_seq_ex,
-                  lib.oracle_conv1d_step, lib.oracle_gated_rmsnorm):
+                  lib.oracle_conv1d_step, lib.oracle_gated_rmsnorm, lib.oracle_ssd_seq_bwd):
             f.restype = ci
         _lib = lib
     return _lib
@@ -206,3 +207,30 @@ def decode_layer_step(conv_state, ssm_state, xBC, conv_w, conv_b, dt, A, D, z, n
     y, st = ssd_decode(ssm_state, x, dt, A, Bm, Cm, D)
     ssm_state[...] = st
     return gated_rmsnorm(y.reshape(Bsz, H * P), z, norm_w, group, eps)
+
+
+def ssd_seq_bwd(x, dt, A, B, C, dy, D=None, init_state=None, dfinal=None, threads=None):
+    """Gradients of the SSD scan in float64 by reverse-mode differentiation of
+    the token loop, for output cotangent dy[B,L,H,P] and final-state cotangent
+    dfinal[B,H,P,N] (None: 0). Returns dict dx, ddt, dA, dB, dC, dD, dinit."""
+    x = _f64(x)
+    Bsz, L, H, P = x.shape
+    G, N = np.shape(B)[2], np.shape(B)[3]
+    dt = _f64(dt, (Bsz, L, H), "dt")
+    A = _f64(A, (H,), "A")
+    Bm = _f64(B, (Bsz, L, G, N), "B")
+    Cm = _f64(C, (Bsz, L, G, N), "C")
+    D = _f64(D, (H,), "D")
+    h0 = _f64(init_state, (Bsz, H, P, N), "init_state")
+    dy = _f64(dy, (Bsz, L, H, P), "dy")
+    dfinal = _f64(dfinal, (Bsz, H, P, N), "dfinal")
+    out = dict(dx=np.empty((Bsz, L, H, P)), ddt=np.empty((Bsz, L, H)), dA=np.empty(H),
+               dB=np.empty((Bsz, L, G, N)), dC=np.empty((Bsz, L, G, N)), dD=np.empty(H),
+               dinit=np.empty((Bsz, H, P, N)))
+    rc = _load().oracle_ssd_seq_bwd(Bsz, L, H, P, N, G, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                                    _ptr(h0), _ptr(dy), _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddt"]),
+                                    _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                                    _ptr(out["dinit"]), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_ssd_seq_bwd: invalid sizes")
+    return out

@@ -34,6 +34,21 @@
  *   and an optional gate z[B,L,Dm] multiplies the output by silu(z):
  *       out_t = y_t * z_t / (1 + exp(-z_t)).
  *
+ *   SSD backward (the training step of "Compiler-First State Space Duality
+ *   ...", appendix Table 13, forward + backward): reverse-mode differentiation
+ *   of the same token loop. With gbar the adjoint of h_t, walking t downwards
+ *   from gbar = dL/dh_{L-1} (the final-state cotangent, or 0):
+ *     gbar += dy_t C_t^T                      (y_t reads h_t)
+ *     dC_t += dy_t^T h_t;  dD += dy_t . x_t
+ *     dx_t  = D dy_t + dt_t gbar B_t
+ *     dB_t += dt_t gbar^T x_t
+ *     dalpha = <gbar, h_{t-1}>;  alpha = exp(dt_t A)
+ *     ddt_t = dalpha alpha A + x_t . (gbar B_t);  dA += dalpha alpha dt_t
+ *     gbar  = alpha gbar                      (adjoint of h_{t-1})
+ *   and the initial-state cotangent is the last gbar. States h_t are
+ *   recomputed forward from checkpoints every 64 tokens (the same arithmetic
+ *   as the forward loop, so the same values).
+ *
  *   Decode-layer neighbours (the fused Mamba-2 decode layer sketched on
  *   "Mamba-2 SSD fused layer via VGpuWarp — design sketch", section "What has
  *   to become a device op", items 1 and 2):
@@ -226,6 +241,143 @@ int oracle_diag_seq(int64_t B, int64_t L, int64_t Dm, int64_t N, const double *x
                     int nthreads) {
     return oracle_diag_seq_ex(B, L, Dm, N, x, dt, A, Bm, Cm, D, NULL, NULL, 0, init_state, y,
                               final_state, nthreads);
+}
+
+typedef struct {
+    int64_t B, L, H, P, N, G;
+    const double *x, *dt, *A, *Bm, *Cm, *D, *init, *dy, *dfinal;
+    double *dx, *ddt, *dA_part, *dB, *dC, *dD_part, *dinit;
+    int64_t next_unit, n_units;
+    pthread_mutex_t lock;
+} bwd_job;
+
+enum { kCkpt = 64 };
+
+/* Backward of one (b, g) unit: the heads of group g in order, so that the
+   shared dB, dC of the group are accumulated by this unit alone. */
+static void bwd_unit(const bwd_job *j, int64_t b, int64_t g) {
+    const int64_t L = j->L, H = j->H, P = j->P, N = j->N, G = j->G, PN = j->P * j->N;
+    const int64_t hpg = H / G, nck = (L + kCkpt - 1) / kCkpt;
+    double *ck = (double *)malloc(sizeof(double) * (size_t)(nck > 0 ? nck : 1) * PN);
+    double *seg = (double *)malloc(sizeof(double) * (size_t)(kCkpt + 1) * PN);
+    double *gbar = (double *)malloc(sizeof(double) * PN);
+    for (int64_t t = 0; t < L; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            j->dB[((b * L + t) * G + g) * N + n] = 0.0;
+            j->dC[((b * L + t) * G + g) * N + n] = 0.0;
+        }
+    for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
+        const double Ah = j->A[h], Dh = j->D ? j->D[h] : 0.0;
+        double dA = 0.0, dD = 0.0;
+        /* forward: the state entering every kCkpt-token segment */
+        double *st = seg;
+        if (j->init)
+            memcpy(st, j->init + (b * H + h) * PN, sizeof(double) * PN);
+        else
+            memset(st, 0, sizeof(double) * PN);
+        for (int64_t t = 0; t < L; ++t) {
+            if (t % kCkpt == 0) memcpy(ck + (t / kCkpt) * PN, st, sizeof(double) * PN);
+            const double dt = j->dt[(b * L + t) * H + h], alpha = exp(dt * Ah);
+            const double *xt = j->x + ((b * L + t) * H + h) * P, *Bt = j->Bm + ((b * L + t) * G + g) * N;
+            for (int64_t p = 0; p < P; ++p)
+                for (int64_t n = 0; n < N; ++n) st[p * N + n] = alpha * st[p * N + n] + dt * xt[p] * Bt[n];
+        }
+        if (j->dfinal)
+            memcpy(gbar, j->dfinal + (b * H + h) * PN, sizeof(double) * PN);
+        else
+            memset(gbar, 0, sizeof(double) * PN);
+        for (int64_t c = nck - 1; c >= 0; --c) {
+            const int64_t t0 = c * kCkpt, t1 = t0 + kCkpt < L ? t0 + kCkpt : L;
+            /* seg[k] = h_{t0 + k - 1}: the entering state, then each token's state */
+            memcpy(seg, ck + c * PN, sizeof(double) * PN);
+            for (int64_t t = t0; t < t1; ++t) {
+                const double dt = j->dt[(b * L + t) * H + h], alpha = exp(dt * Ah);
+                const double *xt = j->x + ((b * L + t) * H + h) * P, *Bt = j->Bm + ((b * L + t) * G + g) * N;
+                const double *prev = seg + (t - t0) * PN;
+                double *cur = seg + (t - t0 + 1) * PN;
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t n = 0; n < N; ++n) cur[p * N + n] = alpha * prev[p * N + n] + dt * xt[p] * Bt[n];
+            }
+            for (int64_t t = t1 - 1; t >= t0; --t) {
+                const double dt = j->dt[(b * L + t) * H + h], alpha = exp(dt * Ah);
+                const double *xt = j->x + ((b * L + t) * H + h) * P, *dyt = j->dy + ((b * L + t) * H + h) * P;
+                const double *Bt = j->Bm + ((b * L + t) * G + g) * N, *Ct = j->Cm + ((b * L + t) * G + g) * N;
+                const double *ht = seg + (t - t0 + 1) * PN, *hprev = seg + (t - t0) * PN;
+                double *dxt = j->dx + ((b * L + t) * H + h) * P;
+                double *dBt = j->dB + ((b * L + t) * G + g) * N, *dCt = j->dC + ((b * L + t) * G + g) * N;
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t n = 0; n < N; ++n) gbar[p * N + n] += dyt[p] * Ct[n];
+                for (int64_t n = 0; n < N; ++n) {
+                    double c_ = 0.0, b_ = 0.0;
+                    for (int64_t p = 0; p < P; ++p) {
+                        c_ += dyt[p] * ht[p * N + n];
+                        b_ += gbar[p * N + n] * xt[p];
+                    }
+                    dCt[n] += c_;
+                    dBt[n] += dt * b_;
+                }
+                double dalpha = 0.0, xgb = 0.0;
+                for (int64_t p = 0; p < P; ++p) {
+                    double gb = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        gb += gbar[p * N + n] * Bt[n];
+                        dalpha += gbar[p * N + n] * hprev[p * N + n];
+                    }
+                    dxt[p] = Dh * dyt[p] + dt * gb;
+                    xgb += xt[p] * gb;
+                    dD += dyt[p] * xt[p];
+                }
+                j->ddt[(b * L + t) * H + h] = dalpha * alpha * Ah + xgb;
+                dA += dalpha * alpha * dt;
+                for (int64_t k = 0; k < PN; ++k) gbar[k] *= alpha;
+            }
+        }
+        if (j->dinit) memcpy(j->dinit + (b * H + h) * PN, gbar, sizeof(double) * PN);
+        j->dA_part[b * H + h] = dA;
+        j->dD_part[b * H + h] = dD;
+    }
+    free(ck);
+    free(seg);
+    free(gbar);
+}
+
+static void *bwd_worker(void *arg) {
+    bwd_job *j = (bwd_job *)arg;
+    for (;;) {
+        int64_t u = take_unit(&j->next_unit, j->n_units, &j->lock);
+        if (u < 0) break;
+        bwd_unit(j, u / j->G, u % j->G);
+    }
+    return NULL;
+}
+
+/* Gradients of the SSD scan: dx[B,L,H,P], ddt[B,L,H], dA[H], dB/dC[B,L,G,N],
+   dD[H], dinit[B,H,P,N] (may be NULL) for cotangents dy[B,L,H,P] and dfinal
+   [B,H,P,N] (may be NULL: 0). dA and dD sum the per-(b, h) parts in b order. */
+int oracle_ssd_seq_bwd(int64_t B, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G, const double *x,
+                       const double *dt, const double *A, const double *Bm, const double *Cm, const double *D,
+                       const double *init_state, const double *dy, const double *dfinal, double *dx,
+                       double *ddt, double *dA, double *dB, double *dC, double *dD, double *dinit, int nthreads) {
+    if (B < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G != 0) return -1;
+    double *dA_part = (double *)calloc((size_t)(B * H > 0 ? B * H : 1), sizeof(double));
+    double *dD_part = (double *)calloc((size_t)(B * H > 0 ? B * H : 1), sizeof(double));
+    bwd_job j = {B, L, H, P, N, G, x, dt, A, Bm, Cm, D, init_state, dy, dfinal,
+                 dx, ddt, dA_part, dB, dC, dD_part, dinit, 0, B * G};
+    pthread_mutex_init(&j.lock, NULL);
+    run_threads(bwd_worker, &j, nthreads, B * G);
+    pthread_mutex_destroy(&j.lock);
+    for (int64_t h = 0; h < H; ++h) {
+        double a = 0.0, d = 0.0;
+        for (int64_t b = 0; b < B; ++b) {
+            a += dA_part[b * H + h];
+            d += dD_part[b * H + h];
+        }
+        dA[h] = a;
+        if (dD) dD[h] = d;
+    }
+    free(dA_part);
+    free(dD_part);
+    return 0;
 }
 
 static double silu(double v) { return v / (1.0 + exp(-v)); }

@@ -36,6 +36,13 @@ MUTANTS = {
     "norm_sum_not_mean": ("const double r = 1.0 / sqrt(ss / (double)group + eps);", "const double r = 1.0 / sqrt(ss + eps);"),
     "norm_gate_after": ("const double g = y[b * D + i] * (z ? silu(z[b * D + i]) : 1.0);\n                ss += g * g;",
                         "const double g = y[b * D + i];\n                ss += g * g;"),
+    "bwd_adjoint_not_decayed": ("for (int64_t k = 0; k < PN; ++k) gbar[k] *= alpha;", ""),
+    "bwd_dx_without_D": ("dxt[p] = Dh * dyt[p] + dt * gb;", "dxt[p] = dt * gb;"),
+    "bwd_ddt_without_decay_term": ("j->ddt[(b * L + t) * H + h] = dalpha * alpha * Ah + xgb;",
+                                   "j->ddt[(b * L + t) * H + h] = xgb;"),
+    "bwd_dC_from_previous_state": ("c_ += dyt[p] * ht[p * N + n];", "c_ += dyt[p] * hprev[p * N + n];"),
+    "bwd_dalpha_from_current_state": ("dalpha += gbar[p * N + n] * hprev[p * N + n];",
+                                      "dalpha += gbar[p * N + n] * ht[p * N + n];"),
     "norm_sigmoid_gate": ("static double silu(double v) { return v / (1.0 + exp(-v)); }",
                           "static double silu(double v) { return 1.0 / (1.0 + exp(-v)); }"),
 }
@@ -50,6 +57,8 @@ PINS = [
     pins.test_conv_step_sequence_is_numpy_convolve, pins.test_conv_step_continues_from_its_window,
     pins.test_gated_rmsnorm_invariants, pins.test_gated_rmsnorm_gate_ratio_and_eps,
     pins.test_decode_layer_matches_conv_then_prefill_then_norm,
+    lambda: pins.test_backward_matches_central_differences(9, None),
+    lambda: pins.test_backward_matches_central_differences(70, 40),
 ]
 
 
@@ -66,7 +75,7 @@ def test_pins_reject_mutant(name, tmp_path, monkeypatch):
     oracle._load()  # make sure the real library's argtypes are set up first
     lib = ctypes.CDLL(str(so))
     for fname in ("oracle_ssd_seq", "oracle_ssd_decode", "oracle_diag_seq", "oracle_diag_seq_ex",
-                  "oracle_conv1d_step", "oracle_gated_rmsnorm"):
+                  "oracle_conv1d_step", "oracle_gated_rmsnorm", "oracle_ssd_seq_bwd"):
         getattr(lib, fname).argtypes = getattr(oracle._lib, fname).argtypes
         getattr(lib, fname).restype = ctypes.c_int
     monkeypatch.setattr(oracle, "_lib", lib)
@@ -75,5 +84,5 @@ def test_pins_reject_mutant(name, tmp_path, monkeypatch):
         try:
             pin()
         except (AssertionError, ValueError):
-            failed.append(pin.__name__)
+            failed.append(getattr(pin, "__name__", "pin"))
     assert failed, f"no pin rejects the mutant {name}"

@@ -467,6 +467,58 @@ def test_decode_layer_matches_conv_then_prefill_then_norm():
     np.testing.assert_allclose(sst, hT, rtol=1e-11, atol=1e-13)
 
 
+def _fd_case(L, seed):
+    d = inputs.ssd_inputs(2, L, 4, 3, 5, 2, io_dtype="f32", seed=seed, init_state=True)
+    rng = np.random.default_rng(seed + 7)
+    dy = rng.standard_normal(d["x"].shape)
+    dfin = rng.standard_normal(d["init_state"].shape)
+    return d, dy, dfin
+
+
+def _objective(d, dy, dfin, **over):
+    a = {k: over.get(k, d[k]) for k in ("x", "dt", "A", "B", "C", "D", "init_state")}
+    y, hT = oracle.ssd_seq(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["init_state"])
+    return float(np.sum(dy * y) + np.sum(dfin * hT))
+
+
+@pytest.mark.parametrize("L,sample", [(9, None), (70, 40)])
+def test_backward_matches_central_differences(L, sample):
+    """Every gradient of L = <dy, y> + <dfinal, h_T> against central finite
+    differences of the forward oracle (step 1e-6 in float64: truncation
+    ~1e-12, rounding ~1e-10), at a length that stays inside one 64-token
+    checkpoint and one that crosses it; two B/C groups of two heads."""
+    d, dy, dfin = _fd_case(L, 30 + L)
+    g = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"], d["init_state"], dfin)
+    names = {"x": "dx", "dt": "ddt", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "init_state": "dinit"}
+    rng = np.random.default_rng(L)
+    eps = 1e-6
+    for k, gk in names.items():
+        base = np.array(d[k], dtype=np.float64)
+        flat = np.arange(base.size) if sample is None else rng.choice(base.size, min(sample, base.size), False)
+        for i in flat:
+            plus, minus = base.copy(), base.copy()
+            plus.flat[i] += eps
+            minus.flat[i] -= eps
+            fd = (_objective(d, dy, dfin, **{k: plus}) - _objective(d, dy, dfin, **{k: minus})) / (2 * eps)
+            got = g[gk].flat[i]
+            assert abs(got - fd) <= 1e-6 * max(1.0, abs(fd)), f"{gk}[{i}]: {got} vs finite difference {fd}"
+
+
+def test_backward_linearity_in_cotangents():
+    """Gradients are linear in (dy, dfinal): the sum of the gradients for two
+    cotangents is the gradient for their sum; a zero cotangent gives zeros."""
+    d, dy, dfin = _fd_case(20, 5)
+    args = (d["x"], d["dt"], d["A"], d["B"], d["C"])
+    g1 = oracle.ssd_seq_bwd(*args, dy, d["D"], d["init_state"], None)
+    g2 = oracle.ssd_seq_bwd(*args, np.zeros_like(dy), d["D"], d["init_state"], dfin)
+    g12 = oracle.ssd_seq_bwd(*args, dy, d["D"], d["init_state"], dfin)
+    for k in g12:
+        np.testing.assert_allclose(g1[k] + g2[k], g12[k], rtol=1e-12, atol=1e-12)
+    g0 = oracle.ssd_seq_bwd(*args, np.zeros_like(dy), d["D"], d["init_state"], None)
+    for k in g0:
+        assert not np.any(g0[k]), k
+
+
 def test_diag_split_resume():
     d = inputs.diag_inputs(2, 50, 6, 4, io_dtype="f32", seed=12, init_state=True)
     yf, hf = oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"])
