@@ -453,6 +453,7 @@ def run_ours(args):
                                for name in ("decode_layer_B64_H80", "decode_layer_B1_H128_G8")]
         out["mamba1"] = bench_mamba1(torch, binding, inputs, dev, hbm_peak, peaks["source"], K, W)
         out["mamba1_softplus"] = bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W)
+        out["backward"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W)
 
     clocks = sampler.stop() if sampler else None
 
@@ -665,6 +666,50 @@ def bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W):
             "time_segments": ws_bytes > 0,
             "l2": f"inputs rotate over {n_sets} copies", "hbm_frac": round(gbs / hbm_peak, 4),
             "pages_time_ms": {"value": 0.3204, "hardware": "RTX 3070, fp16, selective_scan_fn, delta_softplus"}}
+
+
+def bench_backward(torch, binding, inputs, dev, hbm_peak, W):
+    """SSD backward (recompute, adjoint states, per-chunk gradients) on the
+    130M-shaped layer at L 2048, bf16 inputs, float32 gradients; input copies
+    rotate past L2."""
+    Bz, L, H, P, N, G = 1, 2048, 24, 64, 128, 1
+    bf = torch.bfloat16
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=0)
+    rng = np.random.default_rng(1)
+    dy = inputs.round_to(rng.standard_normal(d["x"].shape), "bf16")
+
+    def t_(a, dtype=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+    n_sets = 8
+    sets = [dict(x=t_(d["x"], bf), dt=t_(d["dt"], bf), B=t_(d["B"], bf), C=t_(d["C"], bf), dy=t_(dy, bf))
+            for _ in range(n_sets)]
+    A, Dv = t_(d["A"]), t_(d["D"])
+    dims = binding._dims(Bz, L, H, P, N, G, binding.SSD_BF16)
+    ws = torch.empty(int(binding.load().ssd_scan_chunked_bwd_workspace_size(binding.ctypes.byref(dims))),
+                     dtype=torch.uint8, device=dev)
+
+    def run(i):
+        s_ = sets[i % n_sets]
+        return binding.ssd_scan_chunked_bwd(s_["x"], s_["dt"], A, s_["B"], s_["C"], s_["dy"], Dv, workspace=ws)
+
+    for i in range(max(W, 3)):
+        run(i)
+    torch.cuda.synchronize(dev)
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        run(i)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / reps
+    # compulsory bytes: x, dt, B, C, dy read (bf16); dx, ddt, dB, dC written (float32)
+    nbytes = Bz * L * (2 * H * P + H + 2 * G * N) * 2 + Bz * L * (H * P + H + 2 * G * N) * 4
+    return {"workload": "ssd_bwd_m2_130m_L2048", "ms": round(ms, 4), "tokens_per_s": round(Bz * L / (ms / 1e3), 1),
+            "kernels_per_call": 6, "gpu_launches": 6 * reps, "hbm_frac": round(nbytes / (ms / 1e3) / 1e9 / hbm_peak, 4),
+            "arith": "float32 CUDA cores, chunks of 64", "l2": f"inputs rotate over {n_sets} copies",
+            "pages_context": "Table 13 (L40S): whole-model forward + backward, not comparable"}
 
 
 # ------------------------------------------------------------ CPU oracle

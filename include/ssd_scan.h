@@ -275,6 +275,32 @@ ssd_status ssd_selftest_bounded_wait(void *workspace, int spin_limit, cudaStream
  */
 ssd_status ssd_record_stage_events(cudaEvent_t *events, int count);
 
+/*
+ * Backward of ssd_scan_chunked (the training step's backward; "Compiler-First
+ * State Space Duality ...", appendix Table 13): the gradients of
+ *     L = <dy, y> + <dfinal_state, final_state>
+ * with respect to every input, for the recurrence of ssd_scan_chunked. It
+ * recomputes the forward entering states in chunks of 64 tokens, runs the
+ * adjoint chunk states and a reverse state pass, then one kernel per
+ * (b, chunk, head) forms every gradient from 64 x 64 products; float32
+ * arithmetic on the CUDA cores. Deterministic (fixed-order sums, no atomics).
+ *   dims      as for ssd_scan_chunked (seqlen L, io_dtype of x, dt, B, C, dy;
+ *             flags ignored). Limits: headdim <= 64, dstate <= 128 (else
+ *             SSD_ERR_UNSUPPORTED).
+ *   x, dt, A, B, C, D, init_state   the forward's inputs (D, init_state may be NULL)
+ *   dy          [B, L, H, P]  io_dtype: cotangent of y
+ *   dfinal_state[B, H, P, N]  float32, may be NULL (0)
+ *   dx [B,L,H,P], ddt [B,L,H], dA [H], dB, dC [B,L,G,N]   float32, written
+ *   dD [H], dinit_state [B,H,P,N]                         float32, may be NULL
+ *   workspace   ssd_scan_chunked_bwd_workspace_size(dims) bytes, 256-byte aligned
+ */
+size_t ssd_scan_chunked_bwd_workspace_size(const ssd_dims *dims);
+ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void *dt, const float *A, const void *B,
+                                const void *C, const float *D, const float *init_state, const void *dy,
+                                const float *dfinal_state, float *dx, float *ddt, float *dA, float *dB, float *dC,
+                                float *dD, float *dinit_state, void *workspace, size_t ws_bytes,
+                                cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Decode-layer neighbours of ssd_decode_step: the pieces of a Mamba-2 decode
  * layer body that must run on the device so that a token's layer stays

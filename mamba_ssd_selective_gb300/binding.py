@@ -61,6 +61,10 @@ def load() -> ctypes.CDLL:
             lib.ssd_workspace_size.restype = sz
             lib.ssd_best_chunk.argtypes = [dp]
             lib.ssd_best_chunk.restype = ctypes.c_int
+            lib.ssd_scan_chunked_bwd_workspace_size.argtypes = [dp]
+            lib.ssd_scan_chunked_bwd_workspace_size.restype = sz
+            lib.ssd_scan_chunked_bwd.argtypes = [dp] + [vp] * 17 + [sz, vp]
+            lib.ssd_scan_chunked_bwd.restype = ctypes.c_int
             f32 = ctypes.c_float
             lib.ssd_conv1d_step.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp]
             lib.ssd_gated_rmsnorm.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, vp, vp]
@@ -188,6 +192,45 @@ def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=None, y
                                 _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream, dev)))
     return y, final_state
+
+
+def ssd_scan_chunked_bwd(x, dt, A, B, C, dy, D=None, init_state=None, dfinal_state=None, workspace=None,
+                         stream=None, want_dinit=True):
+    """Gradients of <dy, y> + <dfinal_state, final_state> for ssd_scan_chunked's
+    inputs. Returns a dict of float32 tensors dx, ddt, dA, dB, dC, dD (None when
+    D is None) and dinit (None unless want_dinit)."""
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev, io = x.device, x.dtype
+    _need(x, "x", (Bsz, L, H, P), io, dev)
+    _need(dt, "dt", (Bsz, L, H), io, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(B, "B", (Bsz, L, G, N), io, dev)
+    _need(C, "C", (Bsz, L, G, N), io, dev)
+    _need(D, "D", (H,), torch.float32, dev)
+    _need(init_state, "init_state", (Bsz, H, P, N), torch.float32, dev)
+    _need(dy, "dy", (Bsz, L, H, P), io, dev)
+    _need(dfinal_state, "dfinal_state", (Bsz, H, P, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty((Bsz, L, H, P), **f32), ddt=torch.empty((Bsz, L, H), **f32), dA=torch.empty(H, **f32),
+             dB=torch.empty((Bsz, L, G, N), **f32), dC=torch.empty((Bsz, L, G, N), **f32),
+             dD=torch.empty(H, **f32) if D is not None else None,
+             dinit=torch.empty((Bsz, H, P, N), **f32) if want_dinit else None)
+    d = _dims(Bsz, L, H, P, N, G, _io_code(io))
+    lib = load()
+    need = int(lib.ssd_scan_chunked_bwd_workspace_size(ctypes.byref(d)))
+    if need == 0:
+        _check(lib.ssd_scan_chunked_bwd(ctypes.byref(d), *[None] * 17, 0, None))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
+    _check(lib.ssd_scan_chunked_bwd(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                    _ptr(init_state), _ptr(dy), _ptr(dfinal_state), _ptr(g["dx"]), _ptr(g["ddt"]),
+                                    _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dinit"]),
+                                    _ptr(workspace), workspace.numel(), _stream(stream, dev)))
+    return g
 
 
 def ssd_scan_chunked_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size=256, y=None, final_state=None,

@@ -1,0 +1,423 @@
+// Backward of the chunked SSD scan on the CUDA cores, float32 arithmetic.
+//
+// The forward states are recomputed in chunks of 64 tokens (chunk state and
+// state pass of the forward), then, with a_t = dt_t A, cs the inclusive
+// cumulative sum of a inside a chunk, e_t = exp(cs_t), and for one (b, h):
+//
+//   adjoint chunk state   Sbar_c       = sum_t e_t dy_t C_t^T              (P x N)
+//   reverse state pass    G_c          = Sbar_c + exp(cs_end(c)) G_{c+1},   G_nc = dfinal
+//                         (G_c: cotangent of the state entering chunk c; dinit = G_0)
+//
+// and per chunk, with Gn = G_{c+1} the cotangent of the state leaving it,
+// hin the state entering it, Ld[t,s] = exp(cs_t - cs_s) for s <= t (else 0),
+// u_s = dt_s x_s and eend_s = exp(cs_end - cs_s):
+//
+//   M1 = Ld o (C B^T),  M2 = Ld o (dY X^T) o dt_s
+//   du  = M1^T dY + eend o (B Gn^T)         dx = dt o du + D dY
+//   dB  = M2^T C  + (dt eend) o (X Gn)      dC = M2 B + e o (dY hin)
+//   d cs_t (from the decays): sum_{s<t} W[t,s] - sum_{t'>t} W[t',t]
+//          + e_t dY_t . (hin C_t) - r_t,    W = M1 o (dY X^T) o dt_s,
+//          r_s = eend_s dt_s x_s . (Gn B_s); the chunk's last token also takes
+//          sum_s r_s + exp(cs_end) <Gn, hin>
+//   da_k = sum_{t >= k} d cs_t,  ddt = da A + x . du,  dA = sum da dt,  dD = sum dY . x
+//
+// These are the reverse-mode derivatives of the token recurrence
+// h_t = exp(dt_t A) h_{t-1} + dt_t x_t B_t^T, y_t = C_t h_t + D x_t, grouped
+// by chunk the way the forward re-associates it ("Recurrence Scan", first
+// section; the training step of "Compiler-First State Space Duality ...",
+// Table 13). Every sum runs in a fixed order: no atomics, run-to-run
+// bit-identical. dB and dC of a B/C group sum the heads' parts in head order.
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "ssd_scan.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kT = 256;
+constexpr int kQ = BwdArgs::kChunk;  // 64 tokens per backward chunk
+
+// Adjoint chunk state of one (b, c, h) and one 64x64 tile of (p, n).
+template <typename T>
+__global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_constant__ BwdArgs a, int tilesP,
+                                                             int tilesN) {
+    const int c = blockIdx.x;
+    const int tiles = tilesP * tilesN;
+    const int h = blockIdx.y / tiles, pt = (blockIdx.y % tiles) / tilesN, nt = blockIdx.y % tilesN;
+    const int64_t b = blockIdx.z;
+    const int64_t L = a.L, H = a.H, P = a.P, N = a.N, G = a.G;
+    const int g = (int)(h / (H / G));
+    const int64_t t0 = (int64_t)c * kQ;
+    const int Qv = (int)imin<int64_t>(kQ, L - t0);
+    const T *dy = static_cast<const T *>(a.dy), *Cm = static_cast<const T *>(a.Cm);
+    const T *dt = static_cast<const T *>(a.dt);
+    __shared__ float s_cs[256], s_e[kQ], scratch[8];
+    __shared__ float Ys[kQ][65], Cs[kQ][65];
+    const int tid = threadIdx.x;
+    const float d = (tid < Qv) ? to_f32(dt[(b * L + t0 + tid) * H + h]) : 0.f;
+    block_inclusive_scan_256(d * a.A[h], kQ, s_cs, scratch);
+    if (tid < kQ) s_e[tid] = expf(s_cs[tid]);
+    for (int e = tid; e < kQ * 64; e += kT) {
+        const int j = e / 64, q = e % 64;
+        const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j;
+        Ys[j][q] = (j < Qv && p < P) ? to_f32(dy[(tok * H + h) * P + p]) : 0.f;
+        Cs[j][q] = (j < Qv && n < N) ? to_f32(Cm[(tok * G + g) * N + n]) : 0.f;
+    }
+    __syncthreads();
+    const int ty = tid / 16, tx = tid % 16;
+    float acc[4][4] = {};
+    for (int j = 0; j < Qv; ++j) {
+        const float w = s_e[j];
+        float ya[4], cb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ya[i] = w * Ys[j][ty * 4 + i];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cb[k] = Cs[j][tx * 4 + k];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(ya[i], cb[k], acc[i][k]);
+    }
+    float *S = a.adj + (((b * a.nc + c) * H + h) * P) * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t p = (int64_t)pt * 64 + ty * 4 + i;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t n = (int64_t)nt * 64 + tx * 4 + k;
+            if (p < P && n < N) S[p * N + n] = acc[i][k];
+        }
+    }
+}
+
+// Reverse pass over the chunks of one (b, h), one state element per thread:
+// replaces Sbar_c by the cotangent of the state leaving chunk c and writes
+// dinit. Decays exp(cs_end(c)) come from the forward recompute.
+__global__ void __launch_bounds__(kT) adj_state_pass_kernel(const __grid_constant__ BwdArgs a) {
+    const int64_t PN = a.P * a.N;
+    const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+    const int h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    if (e >= PN) return;
+    const int64_t H = a.H, nc = a.nc;
+    float carry = a.dfinal ? a.dfinal[(b * H + h) * PN + e] : 0.f;
+    const float *dec = a.chunk_sum + (b * H + h) * nc;
+    for (int64_t c = nc - 1; c >= 0; --c) {
+        float *slot = a.adj + ((b * nc + c) * H + h) * PN + e;
+        const float s = *slot;
+        *slot = carry;
+        carry = fmaf(dec[c], carry, s);
+    }
+    if (a.dinit) a.dinit[(b * H + h) * PN + e] = carry;
+}
+
+// 64 x 64 output block, 4 x 4 per thread: acc[i][j] += sum_k fa(row_i, k) * fb(k, col_j)
+// for rows ty*4+i and columns c0 + tx*4 + j.
+template <typename FA, typename FB>
+__device__ __forceinline__ void mm_block(float (&acc)[4][4], int K, int c0, FA fa, FB fb) {
+    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+    for (int k = 0; k < K; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = fa(ty * 4 + i, k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = fb(k, c0 + tx * 4 + j);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+// Shared memory of the per-chunk gradient kernel, in floats.
+struct ChunkSmem {
+    int P, N;
+    __host__ __device__ int x() const { return 0; }                    // X   [64][P]
+    __host__ __device__ int y() const { return x() + kQ * P; }         // dY  [64][P]
+    __host__ __device__ int bm() const { return y() + kQ * P; }        // B   [64][N]
+    __host__ __device__ int cm() const { return bm() + kQ * N; }       // C   [64][N]
+    __host__ __device__ int hin() const { return cm() + kQ * N; }      // hin [P][N]
+    __host__ __device__ int gn() const { return hin() + P * N; }       // Gn  [P][N]
+    __host__ __device__ int m1() const { return gn() + P * N; }        // 64 x 64
+    __host__ __device__ int m2() const { return m1() + kQ * kQ; }      // 64 x 64
+    __host__ __device__ int w() const { return m2() + kQ * kQ; }       // 64 x 64
+    __host__ __device__ int vec() const { return w() + kQ * kQ; }      // 10 vectors of 64 + 256 + 8
+    __host__ __device__ int total() const { return vec() + 10 * kQ + kT + 8; }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ BwdArgs a) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int64_t L = a.L, H = a.H, G = a.G, nc = a.nc;
+    const int P = (int)a.P, N = (int)a.N;
+    const int g = (int)(h / (H / G));
+    const int64_t t0 = (int64_t)c * kQ;
+    const int Qv = (int)imin<int64_t>(kQ, L - t0);
+    const int tid = threadIdx.x;
+    const ChunkSmem lay{P, N};
+    float *X = sm + lay.x(), *Y = sm + lay.y(), *Bs = sm + lay.bm(), *Cs = sm + lay.cm();
+    float *Hin = sm + lay.hin(), *Gn = sm + lay.gn(), *M1 = sm + lay.m1(), *M2 = sm + lay.m2(), *Wb = sm + lay.w();
+    float *v_dt = sm + lay.vec(), *v_cs = v_dt + kQ, *v_e = v_cs + kQ, *v_eend = v_e + kQ, *v_dcs = v_eend + kQ;
+    float *v_ddt = v_dcs + kQ, *v_r = v_ddt + kQ, *v_v = v_r + kQ, *v_dd = v_v + kQ, *v_da = v_dd + kQ;
+    float *red = v_da + kQ, *scratch = red + kT;
+    const T *x = static_cast<const T *>(a.x), *dy = static_cast<const T *>(a.dy);
+    const T *Bm = static_cast<const T *>(a.Bm), *Cm = static_cast<const T *>(a.Cm);
+    const T *dtp = static_cast<const T *>(a.dt);
+    const float Ah = a.A[h], Dh = a.D ? a.D[h] : 0.f;
+
+    // ---- loads: dt and its cumulative sum, x, dy, B, C, entering state, leaving cotangent
+    const float dv = (tid < Qv) ? to_f32(dtp[(b * L + t0 + tid) * H + h]) : 0.f;
+    if (tid < kQ) v_dt[tid] = dv;
+    block_inclusive_scan_256(dv * Ah, kQ, v_cs, scratch);
+    const float cs_end = v_cs[kQ - 1];  // padded tokens carry a = 0
+    if (tid < kQ) {
+        v_e[tid] = expf(v_cs[tid]);
+        v_eend[tid] = expf(cs_end - v_cs[tid]);
+    }
+    for (int e = tid; e < kQ * P; e += kT) {
+        const int j = e / P, p = e % P;
+        const int64_t o = ((b * L + t0 + j) * H + h) * P + p;
+        X[e] = j < Qv ? to_f32(x[o]) : 0.f;
+        Y[e] = j < Qv ? to_f32(dy[o]) : 0.f;
+    }
+    for (int e = tid; e < kQ * N; e += kT) {
+        const int j = e / N, n = e % N;
+        const int64_t o = ((b * L + t0 + j) * G + g) * N + n;
+        Bs[e] = j < Qv ? to_f32(Bm[o]) : 0.f;
+        Cs[e] = j < Qv ? to_f32(Cm[o]) : 0.f;
+    }
+    const int64_t so = ((b * nc + c) * H + h) * (int64_t)P * N;
+    for (int e = tid; e < P * N; e += kT) {
+        Hin[e] = a.hin[so + e];
+        Gn[e] = a.adj[so + e];
+    }
+    __syncthreads();
+
+    const int ty = tid / 16, tx = tid % 16;
+    // ---- CB = C B^T and YX = dY X^T, then the masked, decayed forms
+    {
+        float cb[4][4] = {}, yx[4][4] = {};
+        mm_block(cb, N, 0, [&](int i, int k) { return Cs[i * N + k]; }, [&](int k, int j) { return Bs[j * N + k]; });
+        mm_block(yx, P, 0, [&](int i, int k) { return Y[i * P + k]; }, [&](int k, int j) { return X[j * P + k]; });
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = ty * 4 + i, s = tx * 4 + j;
+                const float ld = s <= t ? expf(v_cs[t] - v_cs[s]) : 0.f;
+                const float m1 = ld * cb[i][j], m2 = ld * v_dt[s] * yx[i][j];
+                M1[t * kQ + s] = m1;
+                M2[t * kQ + s] = m2;
+                Wb[t * kQ + s] = s < t ? m1 * v_dt[s] * yx[i][j] : 0.f;
+            }
+    }
+    __syncthreads();
+    // d cs from the in-chunk decays: row sum minus column sum of W
+    if (tid < kQ) {
+        float rs = 0.f, cl = 0.f;
+        for (int s = 0; s < kQ; ++s) rs += Wb[tid * kQ + s];
+        for (int t = 0; t < kQ; ++t) cl += Wb[t * kQ + tid];
+        v_dcs[tid] = rs - cl;
+    }
+    __syncthreads();
+    // ---- GB[s][p] = sum_n B[s][n] Gn[p][n] into Wb (P <= 64 columns)
+    {
+        float gb[4][4] = {};
+        mm_block(gb, N, 0, [&](int i, int k) { return Bs[i * N + k]; },
+                 [&](int k, int j) { return j < P ? Gn[j * N + k] : 0.f; });
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx * 4 + j] = gb[i][j];
+    }
+    __syncthreads();
+    // r_s = eend_s dt_s x_s . GB_s
+    if (tid < kQ) {
+        float r = 0.f;
+        for (int p = 0; p < P; ++p) r = fmaf(X[tid * P + p], Wb[tid * kQ + p], r);
+        v_r[tid] = v_eend[tid] * v_dt[tid] * r;
+    }
+    // ---- du = M1^T dY + eend o GB; dx = dt du + D dY; ddt (input part) = x . du
+    {
+        float du[4][4] = {};
+        mm_block(du, kQ, 0, [&](int i, int k) { return M1[k * kQ + i]; },
+                 [&](int k, int j) { return j < P ? Y[k * P + j] : 0.f; });
+        __syncthreads();  // every thread has read M1 and Wb (GB) rows it needs below
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int s = ty * 4 + i;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int p = tx * 4 + j;
+                if (p < P) {
+                    const float u = du[i][j] + v_eend[s] * Wb[s * kQ + p];
+                    M1[s * kQ + p] = u;  // du, for the row dot products below
+                    if (s < Qv)
+                        a.dx[((b * L + t0 + s) * H + h) * (int64_t)P + p] = fmaf(v_dt[s], u, Dh * Y[s * P + p]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < kQ) {
+        float dd = 0.f, xd = 0.f;
+        for (int p = 0; p < P; ++p) {
+            dd = fmaf(X[tid * P + p], M1[tid * kQ + p], dd);
+            xd = fmaf(Y[tid * P + p], X[tid * P + p], xd);
+        }
+        v_ddt[tid] = dd;
+        v_dd[tid] = xd;
+    }
+    // ---- dB = M2^T C + (dt eend) o (X Gn); dC = M2 B + e o (dY hin), 64 columns of n per pass
+    for (int n0 = 0; n0 < N; n0 += 64) {
+        float db[4][4] = {}, dc[4][4] = {};
+        mm_block(db, kQ, n0, [&](int i, int k) { return M2[k * kQ + i]; },
+                 [&](int k, int j) { return j < N ? Cs[k * N + j] : 0.f; });
+        {
+            float xg[4][4] = {};
+            mm_block(xg, P, n0, [&](int i, int k) { return X[i * P + k]; },
+                     [&](int k, int j) { return j < N ? Gn[k * N + j] : 0.f; });
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) db[i][j] = fmaf(v_dt[ty * 4 + i] * v_eend[ty * 4 + i], xg[i][j], db[i][j]);
+        }
+        mm_block(dc, kQ, n0, [&](int i, int k) { return M2[i * kQ + k]; },
+                 [&](int k, int j) { return j < N ? Bs[k * N + j] : 0.f; });
+        {
+            float yh[4][4] = {};
+            mm_block(yh, P, n0, [&](int i, int k) { return Y[i * P + k]; },
+                     [&](int k, int j) { return j < N ? Hin[k * N + j] : 0.f; });
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dc[i][j] = fmaf(v_e[ty * 4 + i], yh[i][j], dc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = ty * 4 + i;
+            if (t >= Qv) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = n0 + tx * 4 + j;
+                if (n < N) {
+                    const int64_t o = ((b * L + t0 + t) * H + h) * (int64_t)N + n;
+                    a.dB_part[o] = db[i][j];
+                    a.dC_part[o] = dc[i][j];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // ---- HC[t][p] = sum_n C[t][n] hin[p][n] into Wb; v_t = e_t dY_t . HC_t
+    {
+        float hc[4][4] = {};
+        mm_block(hc, N, 0, [&](int i, int k) { return Cs[i * N + k]; },
+                 [&](int k, int j) { return j < P ? Hin[j * N + k] : 0.f; });
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx * 4 + j] = hc[i][j];
+    }
+    // <Gn, hin>: fixed per-thread ranges, then a fixed-order sum
+    {
+        float q = 0.f;
+        for (int e = tid; e < P * N; e += kT) q = fmaf(Gn[e], Hin[e], q);
+        red[tid] = q;
+    }
+    __syncthreads();
+    if (tid < kQ) {
+        float vv = 0.f;
+        for (int p = 0; p < P; ++p) vv = fmaf(Y[tid * P + p], Wb[tid * kQ + p], vv);
+        v_v[tid] = v_e[tid] * vv;
+    }
+    __syncthreads();
+    // ---- d cs, da (reverse cumulative sum), ddt, dA and dD parts
+    if (tid == 0) {
+        float q = 0.f;
+        for (int k = 0; k < kT; ++k) q += red[k];
+        float rsum = 0.f;
+        for (int s = 0; s < Qv; ++s) rsum += v_r[s];
+        float run = 0.f, dA = 0.f, dD = 0.f;
+        for (int k = Qv - 1; k >= 0; --k) {
+            float dcs = v_dcs[k] + v_v[k] - v_r[k];
+            if (k == Qv - 1) dcs += rsum + expf(cs_end) * q;
+            run += dcs;
+            v_da[k] = run;
+            dA = fmaf(run, v_dt[k], dA);
+        }
+        for (int k = 0; k < Qv; ++k) dD += v_dd[k];
+        a.dA_part[(b * nc + c) * H + h] = dA;
+        a.dD_part[(b * nc + c) * H + h] = dD;
+    }
+    __syncthreads();
+    if (tid < Qv) a.ddt[(b * L + t0 + tid) * H + h] = fmaf(v_da[tid], Ah, v_ddt[tid]);
+}
+
+// dB, dC: sum of the heads' parts of each B/C group, in head order; dA, dD:
+// sum over (b, chunk) in order.
+__global__ void __launch_bounds__(kT) bwd_reduce_kernel(const __grid_constant__ BwdArgs a) {
+    const int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x;  // (b, t, g, n)
+    const int64_t N = a.N, G = a.G, H = a.H, hpg = a.H / a.G;
+    const int64_t total = a.B * a.L * G * N;
+    if (i < total) {
+        const int64_t n = i % N, g = (i / N) % G, bt = i / (N * G);
+        float sb = 0.f, sc = 0.f;
+        for (int64_t k = 0; k < hpg; ++k) {
+            const int64_t o = (bt * H + g * hpg + k) * N + n;
+            sb += a.dB_part[o];
+            sc += a.dC_part[o];
+        }
+        a.dB[i] = sb;
+        a.dC[i] = sc;
+    }
+    if (i < H) {
+        float sa = 0.f, sd = 0.f;
+        for (int64_t bc = 0; bc < a.B * a.nc; ++bc) {
+            sa += a.dA_part[bc * H + i];
+            sd += a.dD_part[bc * H + i];
+        }
+        a.dA[i] = sa;
+        if (a.dD) a.dD[i] = sd;
+    }
+}
+
+template <typename T>
+cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
+    const int tilesP = (int)((a.P + 63) / 64), tilesN = (int)((a.N + 63) / 64);
+    adj_chunk_state_kernel<T><<<dim3((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B), kT, 0,
+                                stream>>>(a, tilesP, tilesN);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    adj_state_pass_kernel<<<dim3((unsigned)((a.P * a.N + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
+                            stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t smem = (size_t)ChunkSmem{(int)a.P, (int)a.N}.total() * sizeof(float);
+    static size_t configured = 0;  // the attribute only grows; set it once per process
+    if (smem > configured) {
+        const size_t most = (size_t)ChunkSmem{BwdArgs::kMaxP, BwdArgs::kMaxN}.total() * sizeof(float);
+        e = cudaFuncSetAttribute(chunk_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+        if (e != cudaSuccess) return e;
+        configured = most;
+    }
+    chunk_bwd_kernel<T><<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kT, smem, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t n = imax<int64_t>(a.B * a.L * a.G * a.N, a.H);
+    bwd_reduce_kernel<<<(unsigned)((n + kT - 1) / kT), kT, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_chunk_smem_bytes(int64_t P, int64_t N) { return (size_t)ChunkSmem{(int)P, (int)N}.total() * sizeof(float); }
+
+cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream) {
+    if (a.B == 0 || a.nc == 0) return cudaSuccess;
+    return a.io == IO_BF16 ? launch_bwd_t<__nv_bfloat16>(a, stream) : launch_bwd_t<float>(a, stream);
+}
+
+}  // namespace ssd

@@ -460,6 +460,20 @@ cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+cudaError_t launch_forward_states(const ChunkedArgs &a, cudaStream_t stream) {
+    if (a.nc > 0 && a.B > 0) {
+        const int tilesP = (int)((a.P + kTile - 1) / kTile), tilesN = (int)((a.N + kTile - 1) / kTile);
+        const dim3 grid((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B);
+        if (a.io == IO_BF16)
+            chunk_state_simt<__nv_bfloat16><<<grid, kT, 0, stream>>>(a, tilesP, tilesN);
+        else
+            chunk_state_simt<float><<<grid, kT, 0, stream>>>(a, tilesP, tilesN);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return launch_state_pass(a, true, false, stream, false);
+}
+
 cudaError_t launch_chunked_simt(const ChunkedArgs &a, cudaStream_t stream) {
     if (a.io == IO_BF16) return launch_simt_t<__nv_bfloat16>(a, stream);
     return launch_simt_t<float>(a, stream);

@@ -104,6 +104,28 @@ struct NormArgs {
 };
 cudaError_t launch_gated_rmsnorm(int io, const NormArgs &a, cudaStream_t stream);
 
+// Forward chunk states and entering states only (CUDA-core chunk state, then
+// the float32 state pass in place): a.states holds h_in(c), a.chunk_sum the
+// chunk decays. Used by the backward to recompute the forward.
+cudaError_t launch_forward_states(const ChunkedArgs &a, cudaStream_t stream);
+
+// Backward of the chunked scan (layouts as in ssd_scan_chunked_bwd).
+struct BwdArgs {
+    static constexpr int kChunk = 64, kMaxP = 64, kMaxN = 128;
+    int64_t B, L, H, P, N, G, nc;
+    int io;
+    const void *x, *dt, *Bm, *Cm, *dy;
+    const float *A, *D, *dfinal;
+    const float *hin;         // [B, nc, H, P, N] state entering each chunk (forward recompute)
+    float *adj;               // [B, nc, H, P, N] adjoint chunk states, then leaving cotangents
+    const float *chunk_sum;   // [B, H, nc] exp(sum of dt*A over the chunk)
+    float *dB_part, *dC_part; // [B, L, H, N] per-head parts
+    float *dA_part, *dD_part; // [B, nc, H]
+    float *dx, *ddt, *dB, *dC, *dA, *dD, *dinit;
+};
+size_t bwd_chunk_smem_bytes(int64_t P, int64_t N);
+cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream);
+
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 
 // Sets the thread-local text returned by ssd_last_error() and returns `status`.

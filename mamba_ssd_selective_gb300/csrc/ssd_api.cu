@@ -255,6 +255,137 @@ size_t selective_scan_diag_workspace_size(int64_t batch, int64_t seqlen, int64_t
     return ssd::diag_workspace_bytes(batch, seqlen, dim, dstate, io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32);
 }
 
+// ------------------------------------------------------------- backward
+
+namespace {
+
+struct BwdWs {
+    size_t status, hin, adj, chunk_sum, dB_part, dC_part, dA_part, dD_part, total;
+};
+BwdWs bwd_ws(const ssd_dims *d) {
+    const int64_t Q = ssd::BwdArgs::kChunk, nc = (d->seqlen + Q - 1) / Q;
+    const size_t st = (size_t)(d->batch * nc * d->nheads * d->headdim * d->dstate) * sizeof(float);
+    const size_t part = (size_t)(d->batch * d->seqlen * d->nheads * d->dstate) * sizeof(float);
+    const size_t small = (size_t)(d->batch * nc * d->nheads) * sizeof(float);
+    BwdWs w{};
+    w.status = 0;
+    w.hin = 256;
+    w.adj = w.hin + round256(st);
+    w.chunk_sum = w.adj + round256(st);
+    w.dB_part = w.chunk_sum + round256(small);
+    w.dC_part = w.dB_part + round256(part);
+    w.dA_part = w.dC_part + round256(part);
+    w.dD_part = w.dA_part + round256(small);
+    w.total = w.dD_part + round256(small);
+    return w;
+}
+
+}  // namespace
+
+size_t ssd_scan_chunked_bwd_workspace_size(const ssd_dims *dims) {
+    if (!dims || dims->batch < 0 || dims->seqlen < 0 || dims->nheads < 1 || dims->headdim < 1 ||
+        dims->dstate < 1 || dims->ngroups < 1 || dims->nheads % dims->ngroups != 0 ||
+        (dims->io_dtype != SSD_F32 && dims->io_dtype != SSD_BF16) || dims->headdim > ssd::BwdArgs::kMaxP ||
+        dims->dstate > ssd::BwdArgs::kMaxN)
+        return 0;
+    return bwd_ws(dims).total;
+}
+
+ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void *dt, const float *A, const void *B,
+                                const void *C, const float *D, const float *init_state, const void *dy,
+                                const float *dfinal_state, float *dx, float *ddt, float *dA, float *dB, float *dC,
+                                float *dD, float *dinit_state, void *workspace, size_t ws_bytes,
+                                cudaStream_t stream) {
+    ssd_status s = check_dims(dims, true);
+    if (s != SSD_OK) return s;
+    if (dims->headdim > ssd::BwdArgs::kMaxP || dims->dstate > ssd::BwdArgs::kMaxN)
+        return fail(SSD_ERR_UNSUPPORTED, "backward supports headdim <= %d and dstate <= %d", ssd::BwdArgs::kMaxP,
+                    ssd::BwdArgs::kMaxN);
+    if (!A || !dA) return fail(SSD_ERR_INVALID_ARG, "A and dA must be non-NULL");
+    const bool has_tokens = dims->batch > 0 && dims->seqlen > 0;
+    if (has_tokens && (!x || !dt || !B || !C || !dy || !dx || !ddt || !dB || !dC))
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, B, C, dy, dx, ddt, dB and dC must be non-NULL");
+    const void *ptrs[] = {x, dt, A, B, C, D, init_state, dy, dfinal_state, dx, ddt, dA, dB, dC, dD, dinit_state};
+    const char *names[] = {"x", "dt", "A", "B", "C", "D", "init_state", "dy", "dfinal_state", "dx", "ddt", "dA",
+                           "dB", "dC", "dD", "dinit_state"};
+    for (int i = 0; i < 16; ++i)
+        if (ptrs[i] && !aligned(ptrs[i], 16)) return fail(SSD_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    const BwdWs w = bwd_ws(dims);
+    if (!workspace) return fail(SSD_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    if (ws_bytes < w.total) return fail(SSD_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", ws_bytes, w.total);
+    const int io = dims->io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32;
+    char *ws = static_cast<char *>(workspace);
+    cudaError_t e = cudaSuccess;
+    if (!has_tokens) {
+        // no tokens: dinit = dfinal, every other gradient zero
+        const size_t hpn = (size_t)(dims->batch * dims->nheads * dims->headdim * dims->dstate) * sizeof(float);
+        if (dinit_state && hpn)
+            e = dfinal_state ? cudaMemcpyAsync(dinit_state, dfinal_state, hpn, cudaMemcpyDeviceToDevice, stream)
+                             : cudaMemsetAsync(dinit_state, 0, hpn, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dA, 0, (size_t)dims->nheads * sizeof(float), stream);
+        if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, (size_t)dims->nheads * sizeof(float), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked_bwd");
+        return ok();
+    }
+    ssd::ChunkedArgs f{};
+    f.B = dims->batch;
+    f.L = dims->seqlen;
+    f.H = dims->nheads;
+    f.P = dims->headdim;
+    f.N = dims->dstate;
+    f.G = dims->ngroups;
+    f.Q = ssd::BwdArgs::kChunk;
+    f.nc = (f.L + f.Q - 1) / f.Q;
+    f.io = io;
+    f.x = x;
+    f.dt = dt;
+    f.Bm = B;
+    f.Cm = C;
+    f.A = A;
+    f.D = D;
+    f.init_state = init_state;
+    f.status = reinterpret_cast<int *>(ws + w.status);
+    f.states = reinterpret_cast<float *>(ws + w.hin);
+    f.chunk_sum = reinterpret_cast<float *>(ws + w.chunk_sum);
+    e = ssd::launch_forward_states(f, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked_bwd: forward states");
+    ssd::BwdArgs a{};
+    a.B = f.B;
+    a.L = f.L;
+    a.H = f.H;
+    a.P = f.P;
+    a.N = f.N;
+    a.G = f.G;
+    a.nc = f.nc;
+    a.io = io;
+    a.x = x;
+    a.dt = dt;
+    a.Bm = B;
+    a.Cm = C;
+    a.dy = dy;
+    a.A = A;
+    a.D = D;
+    a.dfinal = dfinal_state;
+    a.hin = f.states;
+    a.adj = reinterpret_cast<float *>(ws + w.adj);
+    a.chunk_sum = f.chunk_sum;
+    a.dB_part = reinterpret_cast<float *>(ws + w.dB_part);
+    a.dC_part = reinterpret_cast<float *>(ws + w.dC_part);
+    a.dA_part = reinterpret_cast<float *>(ws + w.dA_part);
+    a.dD_part = reinterpret_cast<float *>(ws + w.dD_part);
+    a.dx = dx;
+    a.ddt = ddt;
+    a.dB = dB;
+    a.dC = dC;
+    a.dA = dA;
+    a.dD = dD;
+    a.dinit = dinit_state;
+    e = ssd::launch_ssd_bwd(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked_bwd");
+    return ok();
+}
+
 // ------------------------------------------------------ decode-layer pieces
 
 namespace {

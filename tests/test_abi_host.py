@@ -127,6 +127,33 @@ def test_decode_and_diag_validation(lib):
     assert lib.ssd_selftest_bounded_wait(vp(0x1000), 0, None) == E
 
 
+def test_backward_validation_and_workspace_size(lib):
+    from mamba_ssd_selective_gb300 import binding
+    vp = ctypes.c_void_p
+    d = _dims(binding, batch=2, seqlen=200, nheads=4, headdim=64, dstate=128, io_dtype=1)
+    ws = lib.ssd_scan_chunked_bwd_workspace_size(ctypes.byref(d))
+    nc = (200 + 63) // 64
+    assert ws >= 2 * (2 * nc * 4 * 64 * 128 * 4) + 2 * (2 * 200 * 4 * 128 * 4) and ws % 256 == 0
+    assert lib.ssd_scan_chunked_bwd_workspace_size(ctypes.byref(_dims(binding, headdim=128))) == 0   # P > 64
+    assert lib.ssd_scan_chunked_bwd_workspace_size(ctypes.byref(_dims(binding, dstate=256))) == 0    # N > 128
+    assert lib.ssd_scan_chunked_bwd_workspace_size(None) == 0
+    ptr = [vp(0x1000)] * 16
+
+    def bwd(dims, ptrs=ptr, ws_ptr=vp(0x100000), ws_bytes=1 << 40):
+        return lib.ssd_scan_chunked_bwd(ctypes.byref(dims) if dims is not None else None, *ptrs, ws_ptr, ws_bytes, None)
+    assert bwd(None) == binding.SSD_ERR_INVALID_ARG
+    assert bwd(_dims(binding, headdim=128)) == binding.SSD_ERR_UNSUPPORTED
+    assert bwd(d, ws_bytes=16) == binding.SSD_ERR_INVALID_ARG
+    assert b"too small" in lib.ssd_last_error()
+    assert bwd(d, ws_ptr=vp(0x100010)) == binding.SSD_ERR_INVALID_ARG                          # not 256-aligned
+    bad = list(ptr)
+    bad[7] = vp(0x1008)                                                                        # dy misaligned
+    assert bwd(d, bad) == binding.SSD_ERR_INVALID_ARG
+    bad = list(ptr)
+    bad[9] = None                                                                              # dx missing
+    assert bwd(d, bad) == binding.SSD_ERR_INVALID_ARG
+
+
 def test_best_chunk_policy(lib):
     from mamba_ssd_selective_gb300 import binding
     pick = lambda **kw: lib.ssd_best_chunk(ctypes.byref(_dims(binding, **kw)))

@@ -420,6 +420,59 @@ def test_diag_segmented_chunk_size_bitwise_independent(ssd):
         assert torch.equal(y, y0) and torch.equal(h, h0), f"chunk {c}"
 
 
+# ---------------------------------------------------------------- backward
+
+def _bwd_case(shape, io, seed):
+    Bz, L, H, P, N, G = shape
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype=io, seed=seed, init_state=True)
+    rng = np.random.default_rng(seed + 1000)
+    dy = inputs.round_to(rng.standard_normal(d["x"].shape), io)
+    dfin = inputs.round_to(rng.normal(0.0, 0.1, size=d["init_state"].shape), "f32")
+    return d, dy, dfin
+
+
+def _check_grads(g, ref, tol, what=""):
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
+        if k not in g or k not in ref:
+            continue
+        got, want = host(g[k]), ref[k]
+        scale = float(np.max(np.abs(want))) if want.size else 0.0
+        err = float(np.max(np.abs(got - want))) if want.size else 0.0
+        assert err <= tol * scale + 1e-30, f"{what} {k}: max|err| = {err:.3e} > {tol} * max|ref| = {tol * scale:.3e}"
+
+
+@pytest.mark.parametrize("io,tol", [("f32", 1e-4), ("bf16", 2e-2)])
+@pytest.mark.parametrize("shape", [(1, 256, 4, 64, 16, 1), (2, 200, 4, 32, 64, 2), (1, 130, 3, 64, 128, 1),
+                                   (2, 77, 6, 16, 32, 3)])
+def test_backward_every_element(ssd, io, tol, shape):
+    """Every gradient (dx, ddt, dA, dB, dC, dD, dinit) against the float64
+    reverse-mode oracle; ragged last chunks, several B/C groups."""
+    d, dy, dfin = _bwd_case(shape, io, 21)
+    ref = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"], d["init_state"], dfin)
+    t = IO_TORCH[io]
+    g = ssd.ssd_scan_chunked_bwd(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                 dev(dy, t), dev(d["D"]), dev(d["init_state"]), dev(dfin))
+    torch.cuda.synchronize()
+    _check_grads(g, ref, tol, f"{io} {shape}")
+
+
+def test_backward_deterministic_and_without_optionals(ssd):
+    """Two runs give the same bits; with no D, no initial state and no final
+    cotangent the gradients still match the oracle."""
+    d, dy, _ = _bwd_case((1, 300, 4, 64, 128, 1), "bf16", 23)
+    t = torch.bfloat16
+    args = (dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t), dev(dy, t))
+    g1 = ssd.ssd_scan_chunked_bwd(*args)
+    g2 = ssd.ssd_scan_chunked_bwd(*args)
+    torch.cuda.synchronize()
+    for k in g1:
+        if g1[k] is not None:
+            assert torch.equal(g1[k], g2[k]), k
+    ref = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy)
+    ref["dD"] = None
+    _check_grads({k: v for k, v in g1.items() if k != "dD"}, {k: v for k, v in ref.items() if k != "dD"}, 2e-2)
+
+
 # ------------------------------------------------- decode-layer neighbours
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
