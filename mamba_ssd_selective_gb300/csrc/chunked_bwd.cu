@@ -92,25 +92,59 @@ __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_consta
     }
 }
 
-// Reverse pass over the chunks of one (b, h), one state element per thread:
+// Reverse pass over the chunks of one (b, h), VW state elements per thread:
 // replaces Sbar_c by the cotangent of the state leaving chunk c and writes
-// dinit. Decays exp(cs_end(c)) come from the forward recompute.
+// dinit. Decays exp(cs_end(c)) come from the forward recompute. The values of
+// kPFA chunks are loaded before the chain consumes them, so that each thread
+// keeps kPFA independent loads in flight.
+constexpr int kPFA = 8;
+
+template <int VW>
 __global__ void __launch_bounds__(kT) adj_state_pass_kernel(const __grid_constant__ BwdArgs a) {
     const int64_t PN = a.P * a.N;
-    const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+    const int64_t e = ((int64_t)blockIdx.x * kT + threadIdx.x) * VW;
     const int h = blockIdx.y;
     const int64_t b = blockIdx.z;
     if (e >= PN) return;
     const int64_t H = a.H, nc = a.nc;
-    float carry = a.dfinal ? a.dfinal[(b * H + h) * PN + e] : 0.f;
+    float carry[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k) carry[k] = a.dfinal ? a.dfinal[(b * H + h) * PN + e + k] : 0.f;
     const float *dec = a.chunk_sum + (b * H + h) * nc;
-    for (int64_t c = nc - 1; c >= 0; --c) {
-        float *slot = a.adj + ((b * nc + c) * H + h) * PN + e;
-        const float s = *slot;
-        *slot = carry;
-        carry = fmaf(dec[c], carry, s);
+    for (int64_t c1 = nc; c1 > 0; c1 -= kPFA) {
+        float v[kPFA][VW], dc[kPFA];
+#pragma unroll
+        for (int u = 0; u < kPFA; ++u) {
+            const int64_t c = c1 - 1 - u;
+            if (c >= 0) {
+                const float *p = a.adj + ((b * nc + c) * H + h) * PN + e;
+                if constexpr (VW == 4) {
+                    const float4 q = *reinterpret_cast<const float4 *>(p);
+                    v[u][0] = q.x; v[u][1] = q.y; v[u][2] = q.z; v[u][3] = q.w;
+                } else {
+                    v[u][0] = *p;
+                }
+                dc[u] = dec[c];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPFA; ++u) {
+            const int64_t c = c1 - 1 - u;
+            if (c >= 0) {
+                float *p = a.adj + ((b * nc + c) * H + h) * PN + e;
+                if constexpr (VW == 4)
+                    *reinterpret_cast<float4 *>(p) = make_float4(carry[0], carry[1], carry[2], carry[3]);
+                else
+                    *p = carry[0];
+#pragma unroll
+                for (int k = 0; k < VW; ++k) carry[k] = fmaf(dc[u], carry[k], v[u][k]);
+            }
+        }
     }
-    if (a.dinit) a.dinit[(b * H + h) * PN + e] = carry;
+    if (a.dinit) {
+#pragma unroll
+        for (int k = 0; k < VW; ++k) a.dinit[(b * H + h) * PN + e + k] = carry[k];
+    }
 }
 
 // 64 x 64 output block, 4 x 4 per thread: acc[i][j] += sum_k fa(row_i, k) * fb(k, col_j)
@@ -131,16 +165,20 @@ __device__ __forceinline__ void mm_block(float (&acc)[4][4], int K, int c0, FA f
     }
 }
 
-// Shared memory of the per-chunk gradient kernel, in floats.
+// Shared memory of the per-chunk gradient kernel, in floats. Rows are padded
+// to an odd stride (P + 1, N + 1) so that the products that read them across a
+// warp row-wise (C B^T, dY X^T, B Gn^T, C hin^T) hit 32 different banks.
 struct ChunkSmem {
     int P, N;
-    __host__ __device__ int x() const { return 0; }                    // X   [64][P]
-    __host__ __device__ int y() const { return x() + kQ * P; }         // dY  [64][P]
-    __host__ __device__ int bm() const { return y() + kQ * P; }        // B   [64][N]
-    __host__ __device__ int cm() const { return bm() + kQ * N; }       // C   [64][N]
-    __host__ __device__ int hin() const { return cm() + kQ * N; }      // hin [P][N]
-    __host__ __device__ int gn() const { return hin() + P * N; }       // Gn  [P][N]
-    __host__ __device__ int m1() const { return gn() + P * N; }        // 64 x 64
+    __host__ __device__ int sp() const { return P + 1; }
+    __host__ __device__ int sn() const { return N + 1; }
+    __host__ __device__ int x() const { return 0; }                    // X   [64][sp]
+    __host__ __device__ int y() const { return x() + kQ * sp(); }      // dY  [64][sp]
+    __host__ __device__ int bm() const { return y() + kQ * sp(); }     // B   [64][sn]
+    __host__ __device__ int cm() const { return bm() + kQ * sn(); }    // C   [64][sn]
+    __host__ __device__ int hin() const { return cm() + kQ * sn(); }   // hin [P][sn]
+    __host__ __device__ int gn() const { return hin() + P * sn(); }    // Gn  [P][sn]
+    __host__ __device__ int m1() const { return gn() + P * sn(); }     // 64 x 64
     __host__ __device__ int m2() const { return m1() + kQ * kQ; }      // 64 x 64
     __host__ __device__ int w() const { return m2() + kQ * kQ; }       // 64 x 64
     __host__ __device__ int vec() const { return w() + kQ * kQ; }      // 10 vectors of 64 + 256 + 8
@@ -159,6 +197,7 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     const int Qv = (int)imin<int64_t>(kQ, L - t0);
     const int tid = threadIdx.x;
     const ChunkSmem lay{P, N};
+    const int SP = lay.sp(), SN = lay.sn();
     float *X = sm + lay.x(), *Y = sm + lay.y(), *Bs = sm + lay.bm(), *Cs = sm + lay.cm();
     float *Hin = sm + lay.hin(), *Gn = sm + lay.gn(), *M1 = sm + lay.m1(), *M2 = sm + lay.m2(), *Wb = sm + lay.w();
     float *v_dt = sm + lay.vec(), *v_cs = v_dt + kQ, *v_e = v_cs + kQ, *v_eend = v_e + kQ, *v_dcs = v_eend + kQ;
@@ -181,19 +220,20 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     for (int e = tid; e < kQ * P; e += kT) {
         const int j = e / P, p = e % P;
         const int64_t o = ((b * L + t0 + j) * H + h) * P + p;
-        X[e] = j < Qv ? to_f32(x[o]) : 0.f;
-        Y[e] = j < Qv ? to_f32(dy[o]) : 0.f;
+        X[j * SP + p] = j < Qv ? to_f32(x[o]) : 0.f;
+        Y[j * SP + p] = j < Qv ? to_f32(dy[o]) : 0.f;
     }
     for (int e = tid; e < kQ * N; e += kT) {
         const int j = e / N, n = e % N;
         const int64_t o = ((b * L + t0 + j) * G + g) * N + n;
-        Bs[e] = j < Qv ? to_f32(Bm[o]) : 0.f;
-        Cs[e] = j < Qv ? to_f32(Cm[o]) : 0.f;
+        Bs[j * SN + n] = j < Qv ? to_f32(Bm[o]) : 0.f;
+        Cs[j * SN + n] = j < Qv ? to_f32(Cm[o]) : 0.f;
     }
     const int64_t so = ((b * nc + c) * H + h) * (int64_t)P * N;
     for (int e = tid; e < P * N; e += kT) {
-        Hin[e] = a.hin[so + e];
-        Gn[e] = a.adj[so + e];
+        const int p = e / N, n = e % N;
+        Hin[p * SN + n] = a.hin[so + e];
+        Gn[p * SN + n] = a.adj[so + e];
     }
     __syncthreads();
 
@@ -201,8 +241,8 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // ---- CB = C B^T and YX = dY X^T, then the masked, decayed forms
     {
         float cb[4][4] = {}, yx[4][4] = {};
-        mm_block(cb, N, 0, [&](int i, int k) { return Cs[i * N + k]; }, [&](int k, int j) { return Bs[j * N + k]; });
-        mm_block(yx, P, 0, [&](int i, int k) { return Y[i * P + k]; }, [&](int k, int j) { return X[j * P + k]; });
+        mm_block(cb, N, 0, [&](int i, int k) { return Cs[i * SN + k]; }, [&](int k, int j) { return Bs[j * SN + k]; });
+        mm_block(yx, P, 0, [&](int i, int k) { return Y[i * SP + k]; }, [&](int k, int j) { return X[j * SP + k]; });
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -227,8 +267,8 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // ---- GB[s][p] = sum_n B[s][n] Gn[p][n] into Wb (P <= 64 columns)
     {
         float gb[4][4] = {};
-        mm_block(gb, N, 0, [&](int i, int k) { return Bs[i * N + k]; },
-                 [&](int k, int j) { return j < P ? Gn[j * N + k] : 0.f; });
+        mm_block(gb, N, 0, [&](int i, int k) { return Bs[i * SN + k]; },
+                 [&](int k, int j) { return j < P ? Gn[j * SN + k] : 0.f; });
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -238,14 +278,14 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // r_s = eend_s dt_s x_s . GB_s
     if (tid < kQ) {
         float r = 0.f;
-        for (int p = 0; p < P; ++p) r = fmaf(X[tid * P + p], Wb[tid * kQ + p], r);
+        for (int p = 0; p < P; ++p) r = fmaf(X[tid * SP + p], Wb[tid * kQ + p], r);
         v_r[tid] = v_eend[tid] * v_dt[tid] * r;
     }
     // ---- du = M1^T dY + eend o GB; dx = dt du + D dY; ddt (input part) = x . du
     {
         float du[4][4] = {};
         mm_block(du, kQ, 0, [&](int i, int k) { return M1[k * kQ + i]; },
-                 [&](int k, int j) { return j < P ? Y[k * P + j] : 0.f; });
+                 [&](int k, int j) { return j < P ? Y[k * SP + j] : 0.f; });
         __syncthreads();  // every thread has read M1 and Wb (GB) rows it needs below
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -257,7 +297,7 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
                     const float u = du[i][j] + v_eend[s] * Wb[s * kQ + p];
                     M1[s * kQ + p] = u;  // du, for the row dot products below
                     if (s < Qv)
-                        a.dx[((b * L + t0 + s) * H + h) * (int64_t)P + p] = fmaf(v_dt[s], u, Dh * Y[s * P + p]);
+                        a.dx[((b * L + t0 + s) * H + h) * (int64_t)P + p] = fmaf(v_dt[s], u, Dh * Y[s * SP + p]);
                 }
             }
         }
@@ -266,8 +306,8 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     if (tid < kQ) {
         float dd = 0.f, xd = 0.f;
         for (int p = 0; p < P; ++p) {
-            dd = fmaf(X[tid * P + p], M1[tid * kQ + p], dd);
-            xd = fmaf(Y[tid * P + p], X[tid * P + p], xd);
+            dd = fmaf(X[tid * SP + p], M1[tid * kQ + p], dd);
+            xd = fmaf(Y[tid * SP + p], X[tid * SP + p], xd);
         }
         v_ddt[tid] = dd;
         v_dd[tid] = xd;
@@ -276,22 +316,22 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     for (int n0 = 0; n0 < N; n0 += 64) {
         float db[4][4] = {}, dc[4][4] = {};
         mm_block(db, kQ, n0, [&](int i, int k) { return M2[k * kQ + i]; },
-                 [&](int k, int j) { return j < N ? Cs[k * N + j] : 0.f; });
+                 [&](int k, int j) { return j < N ? Cs[k * SN + j] : 0.f; });
         {
             float xg[4][4] = {};
-            mm_block(xg, P, n0, [&](int i, int k) { return X[i * P + k]; },
-                     [&](int k, int j) { return j < N ? Gn[k * N + j] : 0.f; });
+            mm_block(xg, P, n0, [&](int i, int k) { return X[i * SP + k]; },
+                     [&](int k, int j) { return j < N ? Gn[k * SN + j] : 0.f; });
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) db[i][j] = fmaf(v_dt[ty * 4 + i] * v_eend[ty * 4 + i], xg[i][j], db[i][j]);
         }
         mm_block(dc, kQ, n0, [&](int i, int k) { return M2[i * kQ + k]; },
-                 [&](int k, int j) { return j < N ? Bs[k * N + j] : 0.f; });
+                 [&](int k, int j) { return j < N ? Bs[k * SN + j] : 0.f; });
         {
             float yh[4][4] = {};
-            mm_block(yh, P, n0, [&](int i, int k) { return Y[i * P + k]; },
-                     [&](int k, int j) { return j < N ? Hin[k * N + j] : 0.f; });
+            mm_block(yh, P, n0, [&](int i, int k) { return Y[i * SP + k]; },
+                     [&](int k, int j) { return j < N ? Hin[k * SN + j] : 0.f; });
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -316,8 +356,8 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // ---- HC[t][p] = sum_n C[t][n] hin[p][n] into Wb; v_t = e_t dY_t . HC_t
     {
         float hc[4][4] = {};
-        mm_block(hc, N, 0, [&](int i, int k) { return Cs[i * N + k]; },
-                 [&](int k, int j) { return j < P ? Hin[j * N + k] : 0.f; });
+        mm_block(hc, N, 0, [&](int i, int k) { return Cs[i * SN + k]; },
+                 [&](int k, int j) { return j < P ? Hin[j * SN + k] : 0.f; });
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -326,13 +366,13 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // <Gn, hin>: fixed per-thread ranges, then a fixed-order sum
     {
         float q = 0.f;
-        for (int e = tid; e < P * N; e += kT) q = fmaf(Gn[e], Hin[e], q);
+        for (int e = tid; e < P * N; e += kT) q = fmaf(Gn[(e / N) * SN + e % N], Hin[(e / N) * SN + e % N], q);
         red[tid] = q;
     }
     __syncthreads();
     if (tid < kQ) {
         float vv = 0.f;
-        for (int p = 0; p < P; ++p) vv = fmaf(Y[tid * P + p], Wb[tid * kQ + p], vv);
+        for (int p = 0; p < P; ++p) vv = fmaf(Y[tid * SP + p], Wb[tid * kQ + p], vv);
         v_v[tid] = v_e[tid] * vv;
     }
     __syncthreads();
@@ -393,8 +433,17 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
                                 stream>>>(a, tilesP, tilesN);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    adj_state_pass_kernel<<<dim3((unsigned)((a.P * a.N + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
-                            stream>>>(a);
+    // float4 elements when every (b, c, h) block of P*N states and the optional
+    // cotangent arrays start 16-byte aligned
+    const int64_t PN = a.P * a.N;
+    const bool vec = PN % 4 == 0 && reinterpret_cast<uintptr_t>(a.dfinal) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(a.dinit) % 16 == 0;
+    if (vec)
+        adj_state_pass_kernel<4><<<dim3((unsigned)((PN / 4 + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
+                                   stream>>>(a);
+    else
+        adj_state_pass_kernel<1><<<dim3((unsigned)((PN + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
+                                   stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem = (size_t)ChunkSmem{(int)a.P, (int)a.N}.total() * sizeof(float);
     static size_t configured = 0;  // the attribute only grows; set it once per process
