@@ -60,32 +60,75 @@ __global__ void __launch_bounds__(256) conv1d_step_kernel(const __grid_constant_
 
 // One CTA per (b, group of `group` channels): g = y * silu(z) (z may be
 // null), sum of g^2 by a block reduction, then out = g * rsqrt(mean + eps) * w.
-// The second pass recomputes g from y and z, which the first pass left in L1/L2.
+// Fast path (REG): the group is read once in 16-byte vectors and each
+// thread's g values stay in registers between the reduction and the output;
+// otherwise a second pass recomputes g from y and z.
 constexpr int kNormThreads = 512;
+constexpr int kNormRegVecs = 4;  // 16-byte vectors per thread held in registers (REG)
 
 template <typename T>
-__global__ void __launch_bounds__(kNormThreads) gated_rmsnorm_kernel(const __grid_constant__ NormArgs a) {
-    const int64_t ngrp = a.D / a.group;
-    const int64_t b = blockIdx.x / ngrp, g0 = (blockIdx.x % ngrp) * a.group;
-    const T *y = static_cast<const T *>(a.y) + b * a.D + g0;
-    const T *z = a.z ? static_cast<const T *>(a.z) + b * a.D + g0 : nullptr;
-    T *out = static_cast<T *>(a.out) + b * a.D + g0;
-    float ss = 0.f;
-    for (int64_t i = threadIdx.x; i < a.group; i += kNormThreads) {
-        const float g = to_f32(y[i]) * (z ? silu_f(to_f32(z[i])) : 1.f);
-        ss = fmaf(g, g, ss);
-    }
-    __shared__ float part[kNormThreads / 32];
+__device__ __forceinline__ float norm_reduce(float ss, float *part) {
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
     for (int k = 0; k < kNormThreads / 32; ++k) tot += part[k];
-    const float r = rsqrtf(tot / (float)a.group + a.eps);
-    for (int64_t i = threadIdx.x; i < a.group; i += kNormThreads) {
-        const float g = to_f32(y[i]) * (z ? silu_f(to_f32(z[i])) : 1.f);
-        out[i] = from_f32<T>(g * r * a.w[g0 + i]);
+    return tot;
+}
+
+template <typename T, bool REG>
+__global__ void __launch_bounds__(kNormThreads) gated_rmsnorm_kernel(const __grid_constant__ NormArgs a) {
+    constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
+    const int64_t ngrp = a.D / a.group;
+    const int64_t b = blockIdx.x / ngrp, g0 = (blockIdx.x % ngrp) * a.group;
+    const T *y = static_cast<const T *>(a.y) + b * a.D + g0;
+    const T *z = a.z ? static_cast<const T *>(a.z) + b * a.D + g0 : nullptr;
+    T *out = static_cast<T *>(a.out) + b * a.D + g0;
+    __shared__ float part[kNormThreads / 32];
+    if constexpr (REG) {
+        float g[kNormRegVecs][V];
+        float ss = 0.f;
+        const int64_t nv = a.group / V;
+#pragma unroll
+        for (int r = 0; r < kNormRegVecs; ++r) {
+            const int64_t v = threadIdx.x + (int64_t)r * kNormThreads;
+            if (v < nv) {
+                const uint4 yv = *reinterpret_cast<const uint4 *>(y + v * V);
+                const T *ye = reinterpret_cast<const T *>(&yv);
+                uint4 zv = make_uint4(0, 0, 0, 0);
+                if (z) zv = *reinterpret_cast<const uint4 *>(z + v * V);
+                const T *ze = reinterpret_cast<const T *>(&zv);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    g[r][k] = to_f32(ye[k]) * (z ? silu_f(to_f32(ze[k])) : 1.f);
+                    ss = fmaf(g[r][k], g[r][k], ss);
+                }
+            }
+        }
+        const float rr = rsqrtf(norm_reduce<T>(ss, part) / (float)a.group + a.eps);
+#pragma unroll
+        for (int r = 0; r < kNormRegVecs; ++r) {
+            const int64_t v = threadIdx.x + (int64_t)r * kNormThreads;
+            if (v < nv) {
+                uint4 ov;
+                T *oe = reinterpret_cast<T *>(&ov);
+#pragma unroll
+                for (int k = 0; k < V; ++k) oe[k] = from_f32<T>(g[r][k] * rr * a.w[g0 + v * V + k]);
+                *reinterpret_cast<uint4 *>(out + v * V) = ov;
+            }
+        }
+    } else {
+        float ss = 0.f;
+        for (int64_t i = threadIdx.x; i < a.group; i += kNormThreads) {
+            const float g = to_f32(y[i]) * (z ? silu_f(to_f32(z[i])) : 1.f);
+            ss = fmaf(g, g, ss);
+        }
+        const float rr = rsqrtf(norm_reduce<T>(ss, part) / (float)a.group + a.eps);
+        for (int64_t i = threadIdx.x; i < a.group; i += kNormThreads) {
+            const float g = to_f32(y[i]) * (z ? silu_f(to_f32(z[i])) : 1.f);
+            out[i] = from_f32<T>(g * rr * a.w[g0 + i]);
+        }
     }
 }
 
@@ -110,10 +153,22 @@ cudaError_t launch_conv1d_step(int io, const ConvArgs &a, cudaStream_t stream) {
 cudaError_t launch_gated_rmsnorm(int io, const NormArgs &a, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(a.B * (a.D / a.group));
-    if (io == IO_BF16)
-        gated_rmsnorm_kernel<__nv_bfloat16><<<grid, kNormThreads, 0, stream>>>(a);
-    else
-        gated_rmsnorm_kernel<float><<<grid, kNormThreads, 0, stream>>>(a);
+    // register path: whole 16-byte vectors, aligned rows, a group that fits
+    const int64_t V = io == IO_BF16 ? 8 : 4;
+    const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    const bool reg = a.group % V == 0 && a.D % V == 0 && a.group <= V * kNormThreads * kNormRegVecs && al(a.y) &&
+                     al(a.out) && al(a.w) && (!a.z || al(a.z));
+    if (io == IO_BF16) {
+        if (reg)
+            gated_rmsnorm_kernel<__nv_bfloat16, true><<<grid, kNormThreads, 0, stream>>>(a);
+        else
+            gated_rmsnorm_kernel<__nv_bfloat16, false><<<grid, kNormThreads, 0, stream>>>(a);
+    } else {
+        if (reg)
+            gated_rmsnorm_kernel<float, true><<<grid, kNormThreads, 0, stream>>>(a);
+        else
+            gated_rmsnorm_kernel<float, false><<<grid, kNormThreads, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 

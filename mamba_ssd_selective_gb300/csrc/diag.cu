@@ -267,18 +267,29 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
 // of its steps. The state entering each segment replaces that segment's local
 // end state in ws_h; the state after the last is the final state.
 __global__ void __launch_bounds__(256) diag_segment_pass_kernel(const __grid_constant__ DiagArgs a) {
+    constexpr int kPF = 8;  // segments whose values are loaded before the chain consumes them
     const int64_t Dm = a.Dm, N = a.N, B = a.B;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (b, d, n)
     if (i >= B * Dm * N) return;
     const int64_t n = i % N, d = (i / N) % Dm, b = i / (N * Dm);
     const float a2 = a.A[d * N + n] * kLog2e;
     float h = a.init ? a.init[i] : 0.f;
-    for (int s = 0; s < a.nseg; ++s) {
-        float *slot = a.ws_h + (int64_t)s * B * Dm * N + i;
-        const float loc = *slot;
-        const float sum = a.ws_s[((int64_t)s * B + b) * Dm + d];
-        *slot = h;
-        h = fmaf(ex2f(a2 * sum), h, loc);
+    for (int s0 = 0; s0 < a.nseg; s0 += kPF) {
+        float loc[kPF], sum[kPF];
+#pragma unroll
+        for (int u = 0; u < kPF; ++u) {
+            if (s0 + u < a.nseg) {
+                loc[u] = a.ws_h[(int64_t)(s0 + u) * B * Dm * N + i];
+                sum[u] = a.ws_s[((int64_t)(s0 + u) * B + b) * Dm + d];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPF; ++u) {
+            if (s0 + u < a.nseg) {
+                a.ws_h[(int64_t)(s0 + u) * B * Dm * N + i] = h;
+                h = fmaf(ex2f(a2 * sum[u]), h, loc[u]);
+            }
+        }
     }
     if (a.final_state) a.final_state[i] = h;
 }
