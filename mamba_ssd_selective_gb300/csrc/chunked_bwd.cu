@@ -147,17 +147,23 @@ __global__ void __launch_bounds__(kT) adj_state_pass_kernel(const __grid_constan
     }
 }
 
-// 64 x 64 output block, 4 x 4 per thread: acc[i][j] += sum_k fa(row_i, k) * fb(k, col_j)
-// for rows ty*4+i and columns c0 + tx*4 + j.
-template <typename FA, typename FB>
-__device__ __forceinline__ void mm_block(float (&acc)[4][4], int K, int c0, FA fa, FB fb) {
+// 64 x 64 output blocks, 4 x 4 per thread (ty = tid / 16 picks rows ty*4 + i):
+//   mm_nt  acc[i][j] += sum_k A[row][k] * Bt[col][k],  col = c0 + tx + 16 j
+//   mm_nn  acc[i][j] += sum_k A[row][k] * B[k][col],    col = c0 + tx*4 + j
+//   mm_tn  acc[i][j] += sum_k At[k][row] * B[k][col],   col = c0 + tx*4 + j
+// Row strides of 68 and 132 floats (4 mod 32): mm_nt's column reads across a
+// warp meet at most two to a bank; mm_nn / mm_tn read 16-byte vectors.
+__device__ __forceinline__ void mm_nt(float (&acc)[4][4], int K, int c0, const float *A, int sa, const float *Bt,
+                                      int sb) {
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+    const float *ar = A + ty * 4 * sa, *br = Bt + (c0 + tx) * sb;
+#pragma unroll 4
     for (int k = 0; k < K; ++k) {
         float av[4], bv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = fa(ty * 4 + i, k);
+        for (int i = 0; i < 4; ++i) av[i] = ar[i * sa + k];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) bv[j] = fb(k, c0 + tx * 4 + j);
+        for (int j = 0; j < 4; ++j) bv[j] = br[j * 16 * sb + k];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -165,29 +171,55 @@ __device__ __forceinline__ void mm_block(float (&acc)[4][4], int K, int c0, FA f
     }
 }
 
-// Shared memory of the per-chunk gradient kernel, in floats. Rows are padded
-// to an odd stride (P + 1, N + 1) so that the products that read them across a
-// warp row-wise (C B^T, dY X^T, B Gn^T, C hin^T) hit 32 different banks.
+__device__ __forceinline__ void mm_nn(float (&acc)[4][4], int K, int c0, const float *A, int sa, const float *B,
+                                      int sb) {
+    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+    const float *ar = A + ty * 4 * sa, *bc = B + c0 + tx * 4;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float av[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = ar[i * sa + k];
+        const float4 b4 = *reinterpret_cast<const float4 *>(bc + k * sb);
+        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+__device__ __forceinline__ void mm_tn(float (&acc)[4][4], int K, int c0, const float *At, int sa, const float *B,
+                                      int sb) {
+    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+    const float *ac = At + ty * 4, *bc = B + c0 + tx * 4;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(ac + k * sa);
+        const float4 b4 = *reinterpret_cast<const float4 *>(bc + k * sb);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+// Shared memory of the per-chunk gradient kernel (floats), laid out for the
+// largest supported head (P 64, N 128) whatever the call's sizes: rows and
+// columns past P, N and the chunk's tokens hold zeros, so every 16-byte
+// vector read stays inside its array and contributes nothing.
+constexpr int kSX = 68;   // row stride of X, dY  [64 tokens][64 p]
+constexpr int kSN = 132;  // row stride of B, C [64 tokens][128 n] and hin, Gn [64 p][128 n]
 struct ChunkSmem {
-    int P, N;
-    __host__ __device__ int sp() const { return P + 1; }
-    __host__ __device__ int sn() const { return N + 1; }
-    __host__ __device__ int x() const { return 0; }                    // X   [64][sp]
-    __host__ __device__ int y() const { return x() + kQ * sp(); }      // dY  [64][sp]
-    __host__ __device__ int bm() const { return y() + kQ * sp(); }     // B   [64][sn]
-    __host__ __device__ int cm() const { return bm() + kQ * sn(); }    // C   [64][sn]
-    __host__ __device__ int hin() const { return cm() + kQ * sn(); }   // hin [P][sn]
-    __host__ __device__ int gn() const { return hin() + P * sn(); }    // Gn  [P][sn]
-    __host__ __device__ int m1() const { return gn() + P * sn(); }     // 64 x 64
-    __host__ __device__ int m2() const { return m1() + kQ * kQ; }      // 64 x 64
-    __host__ __device__ int w() const { return m2() + kQ * kQ; }       // 64 x 64
-    __host__ __device__ int vec() const { return w() + kQ * kQ; }      // 10 vectors of 64 + 256 + 8
-    __host__ __device__ int total() const { return vec() + 10 * kQ + kT + 8; }
+    static constexpr int x = 0, y = x + kQ * kSX, bm = y + kQ * kSX, cm = bm + kQ * kSN, hin = cm + kQ * kSN,
+                         gn = hin + 64 * kSN, m1 = gn + 64 * kSN, m2 = m1 + kQ * kQ, w = m2 + kQ * kQ,
+                         vec = w + kQ * kQ, total = vec + 10 * kQ + kT + 8;
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ BwdArgs a) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int c = blockIdx.x, h = blockIdx.y;
     const int64_t b = blockIdx.z;
     const int64_t L = a.L, H = a.H, G = a.G, nc = a.nc;
@@ -196,11 +228,10 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     const int64_t t0 = (int64_t)c * kQ;
     const int Qv = (int)imin<int64_t>(kQ, L - t0);
     const int tid = threadIdx.x;
-    const ChunkSmem lay{P, N};
-    const int SP = lay.sp(), SN = lay.sn();
-    float *X = sm + lay.x(), *Y = sm + lay.y(), *Bs = sm + lay.bm(), *Cs = sm + lay.cm();
-    float *Hin = sm + lay.hin(), *Gn = sm + lay.gn(), *M1 = sm + lay.m1(), *M2 = sm + lay.m2(), *Wb = sm + lay.w();
-    float *v_dt = sm + lay.vec(), *v_cs = v_dt + kQ, *v_e = v_cs + kQ, *v_eend = v_e + kQ, *v_dcs = v_eend + kQ;
+    float *X = sm + ChunkSmem::x, *Y = sm + ChunkSmem::y, *Bs = sm + ChunkSmem::bm, *Cs = sm + ChunkSmem::cm;
+    float *Hin = sm + ChunkSmem::hin, *Gn = sm + ChunkSmem::gn, *M1 = sm + ChunkSmem::m1, *M2 = sm + ChunkSmem::m2;
+    float *Wb = sm + ChunkSmem::w;
+    float *v_dt = sm + ChunkSmem::vec, *v_cs = v_dt + kQ, *v_e = v_cs + kQ, *v_eend = v_e + kQ, *v_dcs = v_eend + kQ;
     float *v_ddt = v_dcs + kQ, *v_r = v_ddt + kQ, *v_v = v_r + kQ, *v_dd = v_v + kQ, *v_da = v_dd + kQ;
     float *red = v_da + kQ, *scratch = red + kT;
     const T *x = static_cast<const T *>(a.x), *dy = static_cast<const T *>(a.dy);
@@ -217,37 +248,41 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
         v_e[tid] = expf(v_cs[tid]);
         v_eend[tid] = expf(cs_end - v_cs[tid]);
     }
-    for (int e = tid; e < kQ * P; e += kT) {
-        const int j = e / P, p = e % P;
+    for (int e = tid; e < kQ * 64; e += kT) {
+        const int j = e / 64, p = e % 64;
+        const bool in = j < Qv && p < P;
         const int64_t o = ((b * L + t0 + j) * H + h) * P + p;
-        X[j * SP + p] = j < Qv ? to_f32(x[o]) : 0.f;
-        Y[j * SP + p] = j < Qv ? to_f32(dy[o]) : 0.f;
+        X[j * kSX + p] = in ? to_f32(x[o]) : 0.f;
+        Y[j * kSX + p] = in ? to_f32(dy[o]) : 0.f;
     }
-    for (int e = tid; e < kQ * N; e += kT) {
-        const int j = e / N, n = e % N;
+    for (int e = tid; e < kQ * 128; e += kT) {
+        const int j = e / 128, n = e % 128;
+        const bool in = j < Qv && n < N;
         const int64_t o = ((b * L + t0 + j) * G + g) * N + n;
-        Bs[j * SN + n] = j < Qv ? to_f32(Bm[o]) : 0.f;
-        Cs[j * SN + n] = j < Qv ? to_f32(Cm[o]) : 0.f;
+        Bs[j * kSN + n] = in ? to_f32(Bm[o]) : 0.f;
+        Cs[j * kSN + n] = in ? to_f32(Cm[o]) : 0.f;
     }
     const int64_t so = ((b * nc + c) * H + h) * (int64_t)P * N;
-    for (int e = tid; e < P * N; e += kT) {
-        const int p = e / N, n = e % N;
-        Hin[p * SN + n] = a.hin[so + e];
-        Gn[p * SN + n] = a.adj[so + e];
+    for (int e = tid; e < 64 * 128; e += kT) {
+        const int p = e / 128, n = e % 128;
+        const bool in = p < P && n < N;
+        Hin[p * kSN + n] = in ? a.hin[so + p * N + n] : 0.f;
+        Gn[p * kSN + n] = in ? a.adj[so + p * N + n] : 0.f;
     }
     __syncthreads();
 
     const int ty = tid / 16, tx = tid % 16;
-    // ---- CB = C B^T and YX = dY X^T, then the masked, decayed forms
+    // ---- CB = C B^T and YX = dY X^T (rows t, columns s = tx + 16 j), then the
+    //      masked, decayed forms
     {
         float cb[4][4] = {}, yx[4][4] = {};
-        mm_block(cb, N, 0, [&](int i, int k) { return Cs[i * SN + k]; }, [&](int k, int j) { return Bs[j * SN + k]; });
-        mm_block(yx, P, 0, [&](int i, int k) { return Y[i * SP + k]; }, [&](int k, int j) { return X[j * SP + k]; });
+        mm_nt(cb, N, 0, Cs, kSN, Bs, kSN);
+        mm_nt(yx, P, 0, Y, kSX, X, kSX);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int t = ty * 4 + i, s = tx * 4 + j;
+                const int t = ty * 4 + i, s = tx + 16 * j;
                 const float ld = s <= t ? expf(v_cs[t] - v_cs[s]) : 0.f;
                 const float m1 = ld * cb[i][j], m2 = ld * v_dt[s] * yx[i][j];
                 M1[t * kQ + s] = m1;
@@ -264,41 +299,37 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
         v_dcs[tid] = rs - cl;
     }
     __syncthreads();
-    // ---- GB[s][p] = sum_n B[s][n] Gn[p][n] into Wb (P <= 64 columns)
+    // ---- GB[s][p] = sum_n B[s][n] Gn[p][n] into Wb (p = tx + 16 j; zero for p >= P)
     {
         float gb[4][4] = {};
-        mm_block(gb, N, 0, [&](int i, int k) { return Bs[i * SN + k]; },
-                 [&](int k, int j) { return j < P ? Gn[j * SN + k] : 0.f; });
+        mm_nt(gb, N, 0, Bs, kSN, Gn, kSN);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx * 4 + j] = gb[i][j];
+            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx + 16 * j] = gb[i][j];
     }
     __syncthreads();
     // r_s = eend_s dt_s x_s . GB_s
     if (tid < kQ) {
         float r = 0.f;
-        for (int p = 0; p < P; ++p) r = fmaf(X[tid * SP + p], Wb[tid * kQ + p], r);
+        for (int p = 0; p < P; ++p) r = fmaf(X[tid * kSX + p], Wb[tid * kQ + p], r);
         v_r[tid] = v_eend[tid] * v_dt[tid] * r;
     }
     // ---- du = M1^T dY + eend o GB; dx = dt du + D dY; ddt (input part) = x . du
     {
         float du[4][4] = {};
-        mm_block(du, kQ, 0, [&](int i, int k) { return M1[k * kQ + i]; },
-                 [&](int k, int j) { return j < P ? Y[k * SP + j] : 0.f; });
-        __syncthreads();  // every thread has read M1 and Wb (GB) rows it needs below
+        mm_tn(du, kQ, 0, M1, kQ, Y, kSX);
+        __syncthreads();  // every thread has read M1 before du replaces it
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int s = ty * 4 + i;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int p = tx * 4 + j;
-                if (p < P) {
-                    const float u = du[i][j] + v_eend[s] * Wb[s * kQ + p];
-                    M1[s * kQ + p] = u;  // du, for the row dot products below
-                    if (s < Qv)
-                        a.dx[((b * L + t0 + s) * H + h) * (int64_t)P + p] = fmaf(v_dt[s], u, Dh * Y[s * SP + p]);
-                }
+                const float u = du[i][j] + v_eend[s] * Wb[s * kQ + p];
+                M1[s * kQ + p] = u;  // du, for the row dot products below
+                if (s < Qv && p < P)
+                    a.dx[((b * L + t0 + s) * H + h) * (int64_t)P + p] = fmaf(v_dt[s], u, Dh * Y[s * kSX + p]);
             }
         }
     }
@@ -306,8 +337,8 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     if (tid < kQ) {
         float dd = 0.f, xd = 0.f;
         for (int p = 0; p < P; ++p) {
-            dd = fmaf(X[tid * SP + p], M1[tid * kQ + p], dd);
-            xd = fmaf(Y[tid * SP + p], X[tid * SP + p], xd);
+            dd = fmaf(X[tid * kSX + p], M1[tid * kQ + p], dd);
+            xd = fmaf(Y[tid * kSX + p], X[tid * kSX + p], xd);
         }
         v_ddt[tid] = dd;
         v_dd[tid] = xd;
@@ -315,23 +346,19 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // ---- dB = M2^T C + (dt eend) o (X Gn); dC = M2 B + e o (dY hin), 64 columns of n per pass
     for (int n0 = 0; n0 < N; n0 += 64) {
         float db[4][4] = {}, dc[4][4] = {};
-        mm_block(db, kQ, n0, [&](int i, int k) { return M2[k * kQ + i]; },
-                 [&](int k, int j) { return j < N ? Cs[k * SN + j] : 0.f; });
+        mm_tn(db, kQ, n0, M2, kQ, Cs, kSN);
         {
             float xg[4][4] = {};
-            mm_block(xg, P, n0, [&](int i, int k) { return X[i * SP + k]; },
-                     [&](int k, int j) { return j < N ? Gn[k * SN + j] : 0.f; });
+            mm_nn(xg, P, n0, X, kSX, Gn, kSN);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) db[i][j] = fmaf(v_dt[ty * 4 + i] * v_eend[ty * 4 + i], xg[i][j], db[i][j]);
         }
-        mm_block(dc, kQ, n0, [&](int i, int k) { return M2[i * kQ + k]; },
-                 [&](int k, int j) { return j < N ? Bs[k * SN + j] : 0.f; });
+        mm_nn(dc, kQ, n0, M2, kQ, Bs, kSN);
         {
             float yh[4][4] = {};
-            mm_block(yh, P, n0, [&](int i, int k) { return Y[i * SP + k]; },
-                     [&](int k, int j) { return j < N ? Hin[k * SN + j] : 0.f; });
+            mm_nn(yh, P, n0, Y, kSX, Hin, kSN);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -356,23 +383,22 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     // ---- HC[t][p] = sum_n C[t][n] hin[p][n] into Wb; v_t = e_t dY_t . HC_t
     {
         float hc[4][4] = {};
-        mm_block(hc, N, 0, [&](int i, int k) { return Cs[i * SN + k]; },
-                 [&](int k, int j) { return j < P ? Hin[j * SN + k] : 0.f; });
+        mm_nt(hc, N, 0, Cs, kSN, Hin, kSN);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx * 4 + j] = hc[i][j];
+            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx + 16 * j] = hc[i][j];
     }
-    // <Gn, hin>: fixed per-thread ranges, then a fixed-order sum
+    // <Gn, hin>: fixed per-thread ranges (zeros past P, N), then a fixed-order sum
     {
         float q = 0.f;
-        for (int e = tid; e < P * N; e += kT) q = fmaf(Gn[(e / N) * SN + e % N], Hin[(e / N) * SN + e % N], q);
+        for (int e = tid; e < 64 * 128; e += kT) q = fmaf(Gn[(e / 128) * kSN + e % 128], Hin[(e / 128) * kSN + e % 128], q);
         red[tid] = q;
     }
     __syncthreads();
     if (tid < kQ) {
         float vv = 0.f;
-        for (int p = 0; p < P; ++p) vv = fmaf(Y[tid * SP + p], Wb[tid * kQ + p], vv);
+        for (int p = 0; p < P; ++p) vv = fmaf(Y[tid * kSX + p], Wb[tid * kQ + p], vv);
         v_v[tid] = v_e[tid] * vv;
     }
     __syncthreads();
@@ -445,13 +471,12 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
         adj_state_pass_kernel<1><<<dim3((unsigned)((PN + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
                                    stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smem = (size_t)ChunkSmem{(int)a.P, (int)a.N}.total() * sizeof(float);
-    static size_t configured = 0;  // the attribute only grows; set it once per process
-    if (smem > configured) {
-        const size_t most = (size_t)ChunkSmem{BwdArgs::kMaxP, BwdArgs::kMaxN}.total() * sizeof(float);
-        e = cudaFuncSetAttribute(chunk_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    const size_t smem = (size_t)ChunkSmem::total * sizeof(float);
+    static bool configured = false;  // set the attribute once per process
+    if (!configured) {
+        e = cudaFuncSetAttribute(chunk_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured = most;
+        configured = true;
     }
     chunk_bwd_kernel<T><<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kT, smem, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -462,7 +487,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t bwd_chunk_smem_bytes(int64_t P, int64_t N) { return (size_t)ChunkSmem{(int)P, (int)N}.total() * sizeof(float); }
+size_t bwd_chunk_smem_bytes(int64_t, int64_t) { return (size_t)ChunkSmem::total * sizeof(float); }
 
 cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream) {
     if (a.B == 0 || a.nc == 0) return cudaSuccess;
