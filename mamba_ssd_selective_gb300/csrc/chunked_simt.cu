@@ -367,13 +367,14 @@ cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
 }  // namespace
 
 // Tensor-core path: bfloat16 chunk states in states_bf16, replaced in place by
-// the bfloat16 entering states; 2 elements per thread. Up to kPFB chunks are
+// the bfloat16 entering states; 2 elements per thread. Up to PF chunks are
 // loaded before the chain runs (one register per chunk), so that one round
-// trip to L2 brings in the whole chain of sequences up to kPFB chunks long.
-constexpr int kPFB = 32;
-
-__global__ void __launch_bounds__(kT, 3) state_pass_bf16_kernel(ChunkedArgs a) {
-    __shared__ float s_dA[kPFB];
+// trip to L2 brings in the whole chain of sequences up to PF chunks long.
+// Short chains (nc <= 16) take PF = 16 at six CTAs per SM, which keeps more
+// loads in flight per SM than PF = 32 at three.
+template <int PF, int MINB>
+__global__ void __launch_bounds__(kT, MINB) state_pass_bf16_kernel(ChunkedArgs a) {
+    __shared__ float s_dA[PF];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t PN = a.P * a.N;
@@ -391,18 +392,18 @@ __global__ void __launch_bounds__(kT, 3) state_pass_bf16_kernel(ChunkedArgs a) {
     const int64_t stride = H * PN;
     __nv_bfloat16 *base = reinterpret_cast<__nv_bfloat16 *>(a.states_bf16) + ((b * nc) * H + h) * PN + e;
     const bool act = e < PN;
-    for (int64_t c0 = 0; c0 < nc; c0 += kPFB) {
+    for (int64_t c0 = 0; c0 < nc; c0 += PF) {
         // the chunk decays of this (b, h), shared by the CTA
         __syncthreads();
-        if (threadIdx.x < kPFB && c0 + threadIdx.x < nc) s_dA[threadIdx.x] = cs[c0 + threadIdx.x];
+        if (threadIdx.x < PF && c0 + threadIdx.x < nc) s_dA[threadIdx.x] = cs[c0 + threadIdx.x];
         __syncthreads();
         if (!act) continue;
-        uint32_t raw[kPFB];
+        uint32_t raw[PF];
 #pragma unroll
-        for (int u = 0; u < kPFB; ++u)
+        for (int u = 0; u < PF; ++u)
             if (c0 + u < nc) raw[u] = *reinterpret_cast<const uint32_t *>(base + (c0 + u) * stride);
 #pragma unroll
-        for (int u = 0; u < kPFB; ++u) {
+        for (int u = 0; u < PF; ++u) {
             if (c0 + u < nc) {
                 const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
                 *reinterpret_cast<__nv_bfloat162 *>(base + (c0 + u) * stride) = hv;
@@ -437,7 +438,7 @@ cudaError_t launch_state_pass(const ChunkedArgs &a, bool write_f32_inplace, bool
     dim3 grid((unsigned)((PN / VW + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B);
     void (*kern)(ChunkedArgs);
     if (bf16_in && vec && write_bf16 && !write_f32_inplace) {
-        kern = state_pass_bf16_kernel;
+        kern = a.nc <= 16 ? state_pass_bf16_kernel<16, 6> : state_pass_bf16_kernel<32, 3>;
         grid.x = (unsigned)((PN / 2 + kT - 1) / kT);
     }
     else if (bf16_in)

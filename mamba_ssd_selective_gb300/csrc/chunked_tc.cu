@@ -1093,6 +1093,7 @@ int device_cc_major() {
     return major;
 }
 
+constexpr size_t kSmemPerSM = 233472;  // shared memory of one SM with the maximum carveout (228 KB)
 size_t state_smem(int Q, int hb) { return (size_t)state_region(Q, hb) + kStateHBMax * 1024 + 64 + 1024; }
 constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
@@ -1220,15 +1221,23 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
     cudaError_t e = mark_stage(a, 0, stream);
     if (e != cudaSuccess) return e;
     // chunk state: groups of hb <= 8 heads (64 TMEM columns and Q x 128 bytes of
-    // x each, at most 4 for 256-token chunks). The busiest SM runs
-    // ceil(CTAs / SMs) CTAs of about (2 + hb) heads' work each: take the hb
-    // that minimises that (ties to the larger hb).
+    // x each, at most 4 for 256-token chunks). The busiest SM does
+    // ceil(CTAs / SMs) * hb heads' work plus about two heads' worth of load
+    // latency per round of co-resident CTAs; `res` CTAs fit on an SM at once
+    // (shared memory and TMEM columns), and co-resident CTAs overlap one's
+    // loads with another's MMA and stores. Take the hb that minimises that
+    // (ties to the larger hb).
     {
         int64_t best = INT64_MAX;
         for (int hb = kStateHBMax; hb >= 1; --hb) {
             if (hpg % hb || (a.Q > 128 && hb > 4)) continue;
             const int64_t ctas = a.B * a.nc * (a.H / hb);
-            const int64_t cost = (ctas + num_sms() - 1) / num_sms() * (2 + hb);
+            const int ncol = hb > 4 ? 512 : hb > 2 ? 256 : hb == 2 ? 128 : 64;
+            int res = (int)(kSmemPerSM / state_smem(a.Q, hb));
+            res = res < 512 / ncol ? res : 512 / ncol;
+            res = res < 1 ? 1 : res;
+            const int64_t cost = (ctas + num_sms() - 1) / num_sms() * hb +
+                                 (ctas + num_sms() * res - 1) / (num_sms() * res) * 2;
             if (cost < best) { best = cost; ps.hb = hb; }
         }
     }

@@ -63,11 +63,13 @@ def test_prefill_ragged_groups_init(ssd, io, chunk, shape):
     check(io, h, hr, "final_state")
 
 
-@pytest.mark.parametrize("shape", [(1, 8192, 28, 64, 128, 1), (1, 16384, 16, 64, 128, 1), (2, 2048, 12, 64, 128, 3)])
+@pytest.mark.parametrize("shape", [(1, 4096, 21, 64, 128, 3), (2, 8192, 8, 64, 128, 1), (1, 4096, 15, 64, 128, 1),
+                                   (1, 2048, 42, 64, 128, 1), (1, 1024, 39, 64, 128, 1), (2, 2048, 12, 64, 128, 3)])
 def test_prefill_tensor_core_head_groups(ssd, shape):
-    """Tensor-core path at shapes whose per-SM cost model picks chunk-state head
-    groups of 7 and 8 heads (MMA chains of 4 + 3 and 4 + 4 heads) and several B/C
-    groups; every element against the oracle, with an initial state."""
+    """Tensor-core path at shapes whose chunk-state cost model picks head groups
+    of 7, 8, 5, 6 and 3 heads (MMA chains of 4 + 3, 4 + 4, 4 + 1, 4 + 2 and 3)
+    and several B/C groups; every element against the oracle, with an initial
+    state."""
     Bz, L, H, P, N, G = shape
     d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=11, init_state=True)
     yr, hr = ref_scan(d)
