@@ -13,11 +13,13 @@
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;  // 8 warps per (b, h)
 constexpr int kRB = 4;         // rows in flight per warp
 
-template <typename T, int VW>
-__global__ void __launch_bounds__(kThreads, 4)
+// THREADS per (b, h): 128 (four warps, eight CTAs per SM) when the batch of
+// heads fills the GPU many times over, 256 (eight warps) for small batches,
+// where each (b, h) needs the extra warps; both measured on GB300.
+template <typename T, int VW, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == 128 ? 8 : 4)
 decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *__restrict__ dt,
                    const float *__restrict__ A, const T *__restrict__ Bm, const T *__restrict__ Cm,
                    const float *__restrict__ D, T *__restrict__ y, int H, int P, int N, int G) {
@@ -32,7 +34,7 @@ decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *
     const T *Cp = Cm + (b * G + g) * N;
     float *st = state + bh * (int64_t)P * N;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int nwarps = kThreads / 32;
+    constexpr int nwarps = THREADS / 32;
 
     for (int p0 = warp; p0 < P; p0 += nwarps * kRB) {
         float acc[kRB], xp[kRB];
@@ -98,14 +100,18 @@ cudaError_t launch_t(int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, floa
     const int64_t grid = B * H;
     if (grid == 0) return cudaSuccess;
     const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(state) & 15) == 0);
-    if (vec)
-        decode_step_kernel<T, 4><<<(unsigned)grid, kThreads, 0, stream>>>(
-            state, (const T *)x, (const T *)dt, A, (const T *)Bm, (const T *)Cm, D, (T *)y, (int)H, (int)P,
-            (int)N, (int)G);
-    else
-        decode_step_kernel<T, 1><<<(unsigned)grid, kThreads, 0, stream>>>(
-            state, (const T *)x, (const T *)dt, A, (const T *)Bm, (const T *)Cm, D, (T *)y, (int)H, (int)P,
-            (int)N, (int)G);
+    const bool wide = grid >= 8 * 152;  // many (b, h) per SM: four warps each
+    auto go = [&](auto kern, int threads) {
+        kern<<<(unsigned)grid, threads, 0, stream>>>(state, (const T *)x, (const T *)dt, A, (const T *)Bm,
+                                                     (const T *)Cm, D, (T *)y, (int)H, (int)P, (int)N, (int)G);
+    };
+    if (vec) {
+        if (wide) go(decode_step_kernel<T, 4, 128>, 128);
+        else go(decode_step_kernel<T, 4, 256>, 256);
+    } else {
+        if (wide) go(decode_step_kernel<T, 1, 128>, 128);
+        else go(decode_step_kernel<T, 1, 256>, 256);
+    }
     return cudaGetLastError();
 }
 
