@@ -87,13 +87,22 @@ __global__ void __launch_bounds__(kNormThreads) gated_rmsnorm_kernel(const __gri
     T *out = static_cast<T *>(a.out) + b * a.D + g0;
     __shared__ float part[kNormThreads / 32];
     if constexpr (REG) {
-        float g[kNormRegVecs][V];
+        float g[kNormRegVecs][V], wv[kNormRegVecs][V];
         float ss = 0.f;
         const int64_t nv = a.group / V;
 #pragma unroll
         for (int r = 0; r < kNormRegVecs; ++r) {
             const int64_t v = threadIdx.x + (int64_t)r * kNormThreads;
             if (v < nv) {
+                // the weights too, before the reduction: no load after it
+#pragma unroll
+                for (int k = 0; k < V; k += 4) {
+                    const float4 w4 = *reinterpret_cast<const float4 *>(a.w + g0 + v * V + k);
+                    wv[r][k] = w4.x;
+                    wv[r][k + 1] = w4.y;
+                    wv[r][k + 2] = w4.z;
+                    wv[r][k + 3] = w4.w;
+                }
                 const uint4 yv = *reinterpret_cast<const uint4 *>(y + v * V);
                 const T *ye = reinterpret_cast<const T *>(&yv);
                 uint4 zv = make_uint4(0, 0, 0, 0);
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(kNormThreads) gated_rmsnorm_kernel(const __gri
                 uint4 ov;
                 T *oe = reinterpret_cast<T *>(&ov);
 #pragma unroll
-                for (int k = 0; k < V; ++k) oe[k] = from_f32<T>(g[r][k] * rr * a.w[g0 + v * V + k]);
+                for (int k = 0; k < V; ++k) oe[k] = from_f32<T>(g[r][k] * rr * wv[r][k]);
                 *reinterpret_cast<uint4 *>(out + v * V) = ov;
             }
         }
