@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
 // of its steps. The state entering each segment replaces that segment's local
 // end state in ws_h; the state after the last is the final state.
 __global__ void __launch_bounds__(256) diag_segment_pass_kernel(const __grid_constant__ DiagArgs a) {
-    constexpr int kPF = 32;  // segments whose values are loaded before the chain consumes them
+    constexpr int kPF = 16;  // segments whose values are loaded before the chain consumes them
     const int64_t Dm = a.Dm, N = a.N, B = a.B;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (b, d, n)
     if (i >= B * Dm * N) return;
