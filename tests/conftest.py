@@ -24,3 +24,11 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="session")
+def ssd():
+    """The Python binding with libssdscan.so loaded (GPU tests)."""
+    from mamba_ssd_selective_gb300 import binding
+    binding.load()
+    return binding

@@ -15,13 +15,6 @@ from tests.helpers import IO_TORCH, check, check_bf16, dev, head_slice, host
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def ssd():
-    from mamba_ssd_selective_gb300 import binding
-    binding.load()
-    return binding
-
-
 def run_scan(ssd, d, io, chunk, simt=False, init=True, D=True, want_final=True):
     t = IO_TORCH[io]
     y, hT = ssd.ssd_scan_chunked(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
