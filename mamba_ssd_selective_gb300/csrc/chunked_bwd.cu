@@ -402,25 +402,50 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
         v_v[tid] = v_e[tid] * vv;
     }
     __syncthreads();
-    // ---- d cs, da (reverse cumulative sum), ddt, dA and dD parts
-    if (tid == 0) {
-        float q = 0.f;
-        for (int k = 0; k < kT; ++k) q += red[k];
-        float rsum = 0.f;
-        for (int s = 0; s < Qv; ++s) rsum += v_r[s];
-        float run = 0.f, dA = 0.f, dD = 0.f;
-        for (int k = Qv - 1; k >= 0; --k) {
-            float dcs = v_dcs[k] + v_v[k] - v_r[k];
-            if (k == Qv - 1) dcs += rsum + expf(cs_end) * q;
-            run += dcs;
-            v_da[k] = run;
-            dA = fmaf(run, v_dt[k], dA);
+    // ---- d cs, da (reverse cumulative sum), ddt, dA and dD parts: the first two
+    //      warps, one token per lane, fixed-order shuffle trees
+    const int lane = tid & 31, w2 = tid >> 5;
+    float suf = 0.f;  // in-warp suffix sum of d cs
+    if (tid < kQ) {
+        float q = (red[4 * tid] + red[4 * tid + 1]) + (red[4 * tid + 2] + red[4 * tid + 3]);  // kT = 4 kQ
+        float rv = tid < Qv ? v_r[tid] : 0.f;
+        q = warp_sum(q);
+        rv = warp_sum(rv);
+        if (lane == 0) {
+            scratch[w2] = q;
+            scratch[2 + w2] = rv;
         }
-        for (int k = 0; k < Qv; ++k) dD += v_dd[k];
-        a.dA_part[(b * nc + c) * H + h] = dA;
-        a.dD_part[(b * nc + c) * H + h] = dD;
     }
     __syncthreads();
+    if (tid < kQ) {
+        const float q = scratch[0] + scratch[1], rsum = scratch[2] + scratch[3];
+        float dcs = tid < Qv ? v_dcs[tid] + v_v[tid] - v_r[tid] : 0.f;
+        if (tid == Qv - 1) dcs += rsum + expf(cs_end) * q;
+        suf = dcs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_down_sync(0xffffffffu, suf, o);
+            if (lane + o < 32) suf += u;
+        }
+        if (lane == 0) scratch[4 + w2] = suf;  // each warp's total
+    }
+    __syncthreads();
+    if (tid < kQ) {
+        const float da = suf + (w2 == 0 ? scratch[5] : 0.f);
+        if (tid < Qv) v_da[tid] = da;
+        float pa = tid < Qv ? da * v_dt[tid] : 0.f, pd = tid < Qv ? v_dd[tid] : 0.f;
+        pa = warp_sum(pa);
+        pd = warp_sum(pd);
+        if (lane == 0) {
+            scratch[6 + w2] = pa;
+            red[w2] = pd;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        a.dA_part[(b * nc + c) * H + h] = scratch[6] + scratch[7];
+        a.dD_part[(b * nc + c) * H + h] = red[0] + red[1];
+    }
     if (tid < Qv) a.ddt[(b * L + t0 + tid) * H + h] = fmaf(v_da[tid], Ah, v_ddt[tid]);
 }
 
