@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_consta
     const T *dy = static_cast<const T *>(a.dy), *Cm = static_cast<const T *>(a.Cm);
     const T *dt = static_cast<const T *>(a.dt);
     __shared__ float s_cs[256], s_e[kQ], scratch[8];
-    __shared__ float Ys[kQ][65], Cs[kQ][65];
+    __shared__ __align__(16) float Ys[kQ][68], Cs[kQ][68];  // 16-byte aligned rows
     const int tid = threadIdx.x;
     const float d = (tid < Qv) ? to_f32(dt[(b * L + t0 + tid) * H + h]) : 0.f;
     block_inclusive_scan_256(d * a.A[h], kQ, s_cs, scratch);
@@ -70,11 +70,9 @@ __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_consta
     float acc[4][4] = {};
     for (int j = 0; j < Qv; ++j) {
         const float w = s_e[j];
-        float ya[4], cb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ya[i] = w * Ys[j][ty * 4 + i];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) cb[k] = Cs[j][tx * 4 + k];
+        const float4 y4 = *reinterpret_cast<const float4 *>(&Ys[j][ty * 4]);
+        const float4 c4 = *reinterpret_cast<const float4 *>(&Cs[j][tx * 4]);
+        const float ya[4] = {w * y4.x, w * y4.y, w * y4.z, w * y4.w}, cb[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll

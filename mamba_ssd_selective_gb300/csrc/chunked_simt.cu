@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
     const T *x = (const T *)a.x, *Bm = (const T *)a.Bm;
 
     __shared__ float s_dt[256], s_cs[256], s_w[256], scratch[8];
-    __shared__ float Xs[32][kTile + 4], Bs[32][kTile + 4];
+    __shared__ __align__(16) float Xs[32][kTile + 4], Bs[32][kTile + 4];  // 16-byte aligned rows
 
     chunk_cumsum<T>((const T *)a.dt, b, L, H, h, t0, Q, a.A[h], s_dt, s_cs, scratch);
     const float cs_end = s_cs[Q - 1];  // padded tokens carry a = 0
@@ -80,11 +80,9 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
         __syncthreads();
 #pragma unroll 8
         for (int jj = 0; jj < 32; ++jj) {
-            float xa[4], bb[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) xa[i] = Xs[jj][ty * 4 + i];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) bb[k] = Bs[jj][tx * 4 + k];
+            const float4 x4 = *reinterpret_cast<const float4 *>(&Xs[jj][ty * 4]);
+            const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[jj][tx * 4]);
+            const float xa[4] = {x4.x, x4.y, x4.z, x4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
