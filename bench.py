@@ -472,6 +472,8 @@ def run_ours(args):
         "gpu_launches": 3 * K,
         "e2e": e2e,
     }
+    if not args.skip_cpu and not args.skip_extra:
+        oracle_beside(out)
     line.update(out)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -748,6 +750,78 @@ def cpu_baseline(w: dict, seconds: float = 10.0) -> dict:
     return {"value": round(w["batch"] * Ls * reps / el, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"first {Ls} of {w['seqlen']} tokens, all {w['nheads']} heads, float64 token-by-token "
                       f"recurrence, {reps} repetition(s) in {el:.2f} s"}
+
+
+def _timed(fn, seconds):
+    """Seconds per call of fn, repeated for about `seconds` (at least once)."""
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            return el / reps, reps
+
+
+def oracle_beside(out: dict, seconds: float = 2.0) -> None:
+    """The float64 oracle, as it stands, timed on the host cores beside each
+    extra leg on a bounded sample of its workload, in the leg's own unit."""
+    import oracle
+    from mamba_ssd_selective_gb300 import inputs
+    thr = oracle.default_threads()
+
+    def rec(value, unit, sample):
+        return {"value": round(value, 2), "unit": unit, "cores": thr, "kind": "oracle", "sample": sample}
+
+    if "decode" in out:
+        w = inputs.WORKLOADS[DECODE]
+        Bz, H, P, N, G = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+        st = inputs.decode_state(Bz, H, P, N, seed=0)
+        prm = inputs.decode_params(H, seed=0)
+        di = inputs.decode_step_inputs(0, Bz, H, P, N, G, io_dtype="bf16", seed=0)
+        per, reps = _timed(lambda: oracle.ssd_decode(st, di["x"], di["dt"], prm["A"], di["B"], di["C"], prm["D"],
+                                                     threads=thr), seconds)
+        out["decode"]["oracle"] = rec(1.0 / per, "steps/s", f"one full step, {reps} repetition(s)")
+    for leg in out.get("decode_layer", []):
+        w = inputs.WORKLOADS[leg["workload"]]
+        Bz, H, P, N, G, Wc = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["width"]
+        prm = inputs.decode_layer_params(Bz, H, P, N, G, Wc, seed=0)
+        li = inputs.decode_layer_step_inputs(0, Bz, H, P, N, G, io_dtype="bf16", seed=0)
+        cst, sst = prm["conv_state"].copy(), prm["ssm_state"].copy()
+        per, reps = _timed(lambda: oracle.decode_layer_step(cst, sst, li["xBC"], prm["conv_w"], prm["conv_b"],
+                                                            li["dt"], prm["A"], prm["D"], li["z"], prm["norm_w"],
+                                                            H, P, N, G, group=w["norm_group"]), seconds)
+        leg["oracle"] = rec(1.0 / per, "steps/s", f"one full layer step, {reps} repetition(s)")
+    if "mamba1" in out:
+        w = inputs.WORKLOADS[MAMBA1]
+        Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
+        ch = 64  # a 64-channel sample of the workload, same distributions
+        d = inputs.diag_inputs(Bz, L, ch, N, io_dtype="bf16", seed=0)
+        per, reps = _timed(lambda: oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=thr),
+                           seconds)
+        out["mamba1"]["oracle"] = rec(Bz * L / (per * Dm / ch), "tokens/s",
+                                      f"{ch} of {Dm} channels, all {Bz}x{L} tokens, {reps} repetition(s), "
+                                      f"scaled to all channels")
+    if "mamba1_softplus" in out:
+        w = inputs.WORKLOADS[MAMBA1_SP]
+        Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
+        ch = 128  # a 128-channel sample of the workload, same distributions
+        d = inputs.diag_option_inputs(Bz, L, ch, N, io_dtype="bf16", seed=0, bias=False, z=False)
+        per, reps = _timed(lambda: oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=thr,
+                                                   delta_softplus=True), seconds)
+        out["mamba1_softplus"]["oracle"] = rec(Bz * L / (per * Dm / ch), "tokens/s",
+                                               f"{ch} of {Dm} channels, all tokens, {reps} repetition(s), "
+                                               f"scaled to all channels")
+    if "backward" in out:
+        Bz, L, H, P, N, G = 1, 2048, 24, 64, 128, 1
+        hs = 2
+        d = inputs.ssd_inputs(Bz, L, hs, P, N, G, io_dtype="bf16", seed=0)
+        dy = inputs.round_to(np.random.default_rng(1).standard_normal(d["x"].shape), "bf16")
+        per, reps = _timed(lambda: oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"],
+                                                      threads=thr), seconds)
+        out["backward"]["oracle"] = rec(Bz * L / (per * H / hs), "tokens/s",
+                                        f"{hs} of {H} heads (one B/C group, so one host thread), all {L} tokens, "
+                                        f"{reps} repetition(s), scaled to all heads")
 
 
 def run_reference(args):
