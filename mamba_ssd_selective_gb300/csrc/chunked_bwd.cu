@@ -495,11 +495,14 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
                                    stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem = (size_t)ChunkSmem::total * sizeof(float);
-    static bool configured = false;  // set the attribute once per process
-    if (!configured) {
+    static DeviceOnce configured;  // set the attribute once per device
+    int dev = 0;
+    if (configured.pending(&dev, &e)) {
         e = cudaFuncSetAttribute(chunk_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.done(dev);
+    } else if (e != cudaSuccess) {
+        return e;
     }
     chunk_bwd_kernel<T><<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kT, smem, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

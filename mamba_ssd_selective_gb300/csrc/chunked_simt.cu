@@ -347,12 +347,15 @@ cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (a.nc > 0 && a.B > 0) {
         const size_t smem = scan_smem_bytes(a.Q);
-        static int configured = 0;  // the attribute only grows; set it once per process
-        if ((int)smem > configured) {
+        static DeviceOnce configured;  // the largest chunk's size, set once per device
+        int dev = 0;
+        if (configured.pending(&dev, &e)) {
             e = cudaFuncSetAttribute(chunk_scan_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)scan_smem_bytes(256));
             if (e != cudaSuccess) return e;
-            configured = (int)scan_smem_bytes(256);
+            configured.done(dev);
+        } else if (e != cudaSuccess) {
+            return e;
         }
         chunk_scan_simt<T><<<dim3((unsigned)(a.nc * (a.Q / kTile)), (unsigned)(a.H * tilesP), (unsigned)a.B), kT,
                              smem, stream>>>(a, tilesP);

@@ -28,6 +28,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -1086,11 +1087,21 @@ bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, in
     return make_map(out, k);
 }
 
+// An integer attribute of the current device, kept per device ordinal (below
+// 64; others are queried on every call). Returns `fallback` when the query fails.
+int device_attr(cudaDeviceAttr attr, std::atomic<int> (&cache)[64], int fallback) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fallback;
+    const bool keep = dev >= 0 && dev < 64;
+    if (keep && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
+    if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v <= 0) return fallback;
+    if (keep) cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
 int device_cc_major() {
-    int dev = 0, major = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
-    return major;
+    static std::atomic<int> cache[64];
+    return device_attr(cudaDevAttrComputeCapabilityMajor, cache, -1);
 }
 
 constexpr size_t kSmemPerSM = 233472;  // shared memory of one SM with the maximum carveout (228 KB)
@@ -1100,16 +1111,8 @@ constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 16384 + 2 * (4 * kHBMax * 128 + kHBMax) * 4 + 16 + 512 + 1024; }
 
 int num_sms() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            n = v;
-        else
-            n = 1;
-    }
-    return n;
+    static std::atomic<int> cache[64];
+    return device_attr(cudaDevAttrMultiProcessorCount, cache, 1);
 }
 
 cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream_t stream, bool pdl,
@@ -1144,8 +1147,7 @@ bool chunked_tc_supported(const ChunkedArgs &a) {
     if (a.L <= 0 || a.L > 0x7fffffffLL || a.B > 0x7fffffffLL) return false;
     if (a.B * a.nc * a.H * a.P > 0x7fffffffLL) return false;
     if (((a.H * a.P * 2) % 16) != 0 || ((a.G * a.N * 2) % 16) != 0) return false;
-    static int major = device_cc_major();
-    return major == 10;
+    return device_cc_major() == 10;
 }
 
 cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
@@ -1179,8 +1181,10 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
         if (!ok) return cudaErrorInvalidValue;
     }
 
-    static bool configured = false;
-    if (!configured) {
+    static DeviceOnce configured;
+    int dev = 0;
+    cudaError_t de = cudaSuccess;
+    if (configured.pending(&dev, &de)) {
         cudaError_t e = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)state_smem(256, 4));
         if (e != cudaSuccess) return e;
@@ -1197,7 +1201,9 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
                                      (int)cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess) return e;
         }
-        configured = true;
+        configured.done(dev);
+    } else if (de != cudaSuccess) {
+        return de;
     }
     // persistent chunk scan for Q <= 128: head groups of hb heads sharing a B/C
     // group, at most 4 / (chunks per tile) so that their accumulators fit TMEM.

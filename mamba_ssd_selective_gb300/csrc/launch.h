@@ -5,7 +5,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace ssd {
+
+// Kernel attributes (maximum dynamic shared memory, carveout) are kept per
+// device, so a launcher that sets them once remembers it per device ordinal:
+// one bit per device, for ordinals below 64 (others are set on every call).
+class DeviceOnce {
+  public:
+    // true when the current device still needs the attribute calls; *dev gets
+    // the ordinal to pass to done()
+    bool pending(int *dev, cudaError_t *err) {
+        *err = cudaGetDevice(dev);
+        if (*err != cudaSuccess) return false;
+        return *dev < 0 || *dev >= 64 || !((bits_.load(std::memory_order_acquire) >> *dev) & 1ull);
+    }
+    void done(int dev) {
+        if (dev >= 0 && dev < 64) bits_.fetch_or(1ull << dev, std::memory_order_release);
+    }
+
+  private:
+    std::atomic<unsigned long long> bits_{0};
+};
 
 enum IoType { IO_F32 = 0, IO_BF16 = 1 };
 
