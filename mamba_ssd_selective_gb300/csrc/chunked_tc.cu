@@ -525,14 +525,14 @@ __global__ void __launch_bounds__(128) chunk_scan_tc(const __grid_constant__ TcP
 //             read from TMEM: S' never touches shared memory)
 // so y(k) = Y(k) leaves TMEM in one read. Warp roles:
 //   warp 0       TMA producer: C, B (per item), x (per head, 4-deep ring)
-//   warp 10      TMA producer of the entering states (waits for the state pass)
 //   warp 1       MMA issuer (one lane)
-//   warps 2..9   epilogue, two groups of four warps (one warp per TMEM lane
-//                quarter per group): cumulative sums of all heads of the item
-//                (the item's only cross-warp barriers); per head S' -- group 0
-//                the 32-column blocks {0, 3} of S, group 1 {1, 2}, balanced
-//                over the causal triangle --, the entering-state rescale and
-//                the y store of its 32 columns of p.
+//   warp 2       TMA producer of the entering states (waits for the state
+//                pass) and TMA store of each head's y tile staged in shared memory
+//   warp 3       per-item scalars one item ahead: cumulative sums of dt A,
+//                decays and rescale factors of every head
+//   warps 4..19  epilogue, one warp per (TMEM lane quarter, 32-column group):
+//                per head S', the entering-state rescale and the staging of
+//                its 16 columns of y
 // All waits are bounded: a timeout raises a CTA-wide flag, every role then
 // runs to the end of its loop without waiting and the status word records
 // SSD_ERR_TIMEOUT.
