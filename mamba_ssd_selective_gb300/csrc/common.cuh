@@ -19,6 +19,40 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
+// Programmatic dependent launch. A kernel launched by launch_programmatic()
+// may be placed on the GPU while the work before it in the stream drains; its
+// first statement is pdl_wait() (or pdl_enter()), in every thread and before
+// any early return: wait until that work has completed (its writes visible).
+// Because every such kernel waits before it can finish, "the previous kernel
+// has completed" also covers the ones before it. pdl_trigger() lets the next
+// launch be placed once every CTA has triggered or exited: early for
+// memory-bound kernels, at the end of the CTA's work for issue-bound ones,
+// whose throughput drops when the next grid's CTAs sit resident beside them
+// (measured on the Mamba-1 scan). Without the launch attribute these
+// instructions do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename I> __host__ __device__ __forceinline__ I imin(I a, I b) { return a < b ? a : b; }
 template <typename I> __host__ __device__ __forceinline__ I imax(I a, I b) { return a > b ? a : b; }
 

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == 128 ? 8 : 4)
 decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *__restrict__ dt,
                    const float *__restrict__ A, const T *__restrict__ Bm, const T *__restrict__ Cm,
                    const float *__restrict__ D, T *__restrict__ y, int H, int P, int N, int G) {
+    pdl_enter();  // the previous step's state update is complete
     const int64_t bh = blockIdx.x;  // b * H + h
     const int h = (int)(bh % H);
     const int64_t b = bh / H;
@@ -102,17 +103,12 @@ cudaError_t launch_t(int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, floa
     const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(state) & 15) == 0);
     const bool wide = grid >= 8 * 152;  // many (b, h) per SM: four warps each
     auto go = [&](auto kern, int threads) {
-        kern<<<(unsigned)grid, threads, 0, stream>>>(state, (const T *)x, (const T *)dt, A, (const T *)Bm,
-                                                     (const T *)Cm, D, (T *)y, (int)H, (int)P, (int)N, (int)G);
+        return launch_programmatic(kern, dim3((unsigned)grid), dim3(threads), 0, stream, state, (const T *)x,
+                                   (const T *)dt, A, (const T *)Bm, (const T *)Cm, D, (T *)y, (int)H, (int)P,
+                                   (int)N, (int)G);
     };
-    if (vec) {
-        if (wide) go(decode_step_kernel<T, 4, 128>, 128);
-        else go(decode_step_kernel<T, 4, 256>, 256);
-    } else {
-        if (wide) go(decode_step_kernel<T, 1, 128>, 128);
-        else go(decode_step_kernel<T, 1, 256>, 256);
-    }
-    return cudaGetLastError();
+    if (vec) return wide ? go(decode_step_kernel<T, 4, 128>, 128) : go(decode_step_kernel<T, 4, 256>, 256);
+    return wide ? go(decode_step_kernel<T, 1, 128>, 128) : go(decode_step_kernel<T, 1, 256>, 256);
 }
 
 }  // namespace

@@ -23,6 +23,7 @@ __device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); 
 // parts of a conv output into the separate arrays the decode step reads.
 template <typename T, int W>
 __global__ void __launch_bounds__(256) conv1d_step_kernel(const __grid_constant__ ConvArgs a) {
+    pdl_enter();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.B * a.C) return;
     const int64_t b = i / a.C, c = i % a.C;
@@ -79,6 +80,7 @@ __device__ __forceinline__ float norm_reduce(float ss, float *part) {
 
 template <typename T, bool REG>
 __global__ void __launch_bounds__(kNormThreads) gated_rmsnorm_kernel(const __grid_constant__ NormArgs a) {
+    pdl_enter();
     constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
     const int64_t ngrp = a.D / a.group;
     const int64_t b = blockIdx.x / ngrp, g0 = (blockIdx.x % ngrp) * a.group;
@@ -145,11 +147,8 @@ template <typename T>
 cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t stream) {
     const int64_t n = a.B * a.C;
     const unsigned grid = (unsigned)((n + 255) / 256);
-    if (a.W == 4)
-        conv1d_step_kernel<T, 4><<<grid, 256, 0, stream>>>(a);
-    else
-        conv1d_step_kernel<T, 0><<<grid, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_programmatic(a.W == 4 ? conv1d_step_kernel<T, 4> : conv1d_step_kernel<T, 0>, dim3(grid),
+                               dim3(256), 0, stream, a);
 }
 
 }  // namespace
@@ -167,18 +166,12 @@ cudaError_t launch_gated_rmsnorm(int io, const NormArgs &a, cudaStream_t stream)
     const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
     const bool reg = a.group % V == 0 && a.D % V == 0 && a.group <= V * kNormThreads * kNormRegVecs && al(a.y) &&
                      al(a.out) && al(a.w) && (!a.z || al(a.z));
-    if (io == IO_BF16) {
-        if (reg)
-            gated_rmsnorm_kernel<__nv_bfloat16, true><<<grid, kNormThreads, 0, stream>>>(a);
-        else
-            gated_rmsnorm_kernel<__nv_bfloat16, false><<<grid, kNormThreads, 0, stream>>>(a);
-    } else {
-        if (reg)
-            gated_rmsnorm_kernel<float, true><<<grid, kNormThreads, 0, stream>>>(a);
-        else
-            gated_rmsnorm_kernel<float, false><<<grid, kNormThreads, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    void (*kern)(NormArgs);
+    if (io == IO_BF16)
+        kern = reg ? gated_rmsnorm_kernel<__nv_bfloat16, true> : gated_rmsnorm_kernel<__nv_bfloat16, false>;
+    else
+        kern = reg ? gated_rmsnorm_kernel<float, true> : gated_rmsnorm_kernel<float, false>;
+    return launch_programmatic(kern, dim3(grid), dim3(kNormThreads), 0, stream, a);
 }
 
 }  // namespace ssd

@@ -99,6 +99,7 @@ template <int NH, int TPC, int CH, int UNR, bool OPT, int MODE>
 __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_constant__ DiagArgs a) {
     static_assert(TPC == 1 || TPC == 2, "one or two threads per channel");
     static_assert(NH % 4 == 0 && CH % 8 == 0, "four-state groups, 16-byte channel rows");
+    pdl_wait();  // the next launch is let in at the end (issue-bound kernel)
     constexpr int kThr = TPC * CH;
     constexpr int NMAX = TPC * NH;
     const int64_t L = a.L, Dm = a.Dm;
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
             buf ^= 1;
         }
     }
+    pdl_trigger();
     float *h_out = MODE == kWhole ? a.final_state : MODE == kLocal ? a.ws_h + seg * a.B * Dm * N : nullptr;
     if (h_out && valid) {
 #pragma unroll
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
 // end state in ws_h; the state after the last is the final state.
 __global__ void __launch_bounds__(256) diag_segment_pass_kernel(const __grid_constant__ DiagArgs a) {
     constexpr int kPF = 16;  // segments whose values are loaded before the chain consumes them
+    pdl_enter();
     const int64_t Dm = a.Dm, N = a.N, B = a.B;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (b, d, n)
     if (i >= B * Dm * N) return;
@@ -297,6 +300,7 @@ __global__ void __launch_bounds__(256) diag_segment_pass_kernel(const __grid_con
 // General path (float32 I/O, or shapes the vectorised path does not take).
 template <typename T, int NMAX, bool OPT>
 __global__ void __launch_bounds__(128) diag_scan_kernel(const __grid_constant__ DiagArgs a) {
+    pdl_wait();  // the next launch is let in at the end (issue-bound kernel)
     constexpr int kC = 128;
     const int64_t L = a.L, Dm = a.Dm;
     const int N = a.N;
@@ -364,6 +368,7 @@ __global__ void __launch_bounds__(128) diag_scan_kernel(const __grid_constant__ 
             }
         }
     }
+    pdl_trigger();
     if (a.final_state && valid) {
 #pragma unroll
         for (int n = 0; n < NMAX; ++n)
@@ -374,13 +379,10 @@ __global__ void __launch_bounds__(128) diag_scan_kernel(const __grid_constant__ 
 template <typename T, bool OPT>
 cudaError_t launch_general(const DiagArgs &a, int64_t B, cudaStream_t stream) {
     dim3 grid((unsigned)((a.Dm + 127) / 128), (unsigned)B);
-    if (a.N <= 16)
-        diag_scan_kernel<T, 16, OPT><<<grid, 128, 0, stream>>>(a);
-    else if (a.N <= 32)
-        diag_scan_kernel<T, 32, OPT><<<grid, 128, 0, stream>>>(a);
-    else
-        diag_scan_kernel<T, 64, OPT><<<grid, 128, 0, stream>>>(a);
-    return cudaGetLastError();
+    void (*kern)(DiagArgs) = a.N <= 16   ? diag_scan_kernel<T, 16, OPT>
+                             : a.N <= 32 ? diag_scan_kernel<T, 32, OPT>
+                                         : diag_scan_kernel<T, 64, OPT>;
+    return launch_programmatic(kern, grid, dim3(128), 0, stream, a);
 }
 
 template <bool OPT, int MODE>
@@ -389,12 +391,13 @@ cudaError_t launch_bf16_vec(const DiagArgs &a, cudaStream_t stream) {
     const dim3 grid1((unsigned)((a.Dm + kCh1 - 1) / kCh1), (unsigned)a.B, nz);
     const dim3 grid2((unsigned)((a.Dm + kCh - 1) / kCh), (unsigned)a.B, nz);
     if (a.N <= 8)
-        diag_scan_bf16_kernel<8, 1, kCh1, kUnr1, OPT, MODE><<<grid1, kCh1, 0, stream>>>(a);
-    else if (a.N <= 16)
-        diag_scan_bf16_kernel<8, 2, kCh, kUnr2, OPT, MODE><<<grid2, 2 * kCh, 0, stream>>>(a);
-    else
-        diag_scan_bf16_kernel<16, 2, kCh, kUnr2, OPT, MODE><<<grid2, 2 * kCh, 0, stream>>>(a);
-    return cudaGetLastError();
+        return launch_programmatic(diag_scan_bf16_kernel<8, 1, kCh1, kUnr1, OPT, MODE>, grid1, dim3(kCh1), 0,
+                                   stream, a);
+    if (a.N <= 16)
+        return launch_programmatic(diag_scan_bf16_kernel<8, 2, kCh, kUnr2, OPT, MODE>, grid2, dim3(2 * kCh), 0,
+                                   stream, a);
+    return launch_programmatic(diag_scan_bf16_kernel<16, 2, kCh, kUnr2, OPT, MODE>, grid2, dim3(2 * kCh), 0,
+                               stream, a);
 }
 
 template <bool OPT>
@@ -403,8 +406,8 @@ cudaError_t launch_bf16(const DiagArgs &a, cudaStream_t stream) {
     cudaError_t e = launch_bf16_vec<OPT, kLocal>(a, stream);
     if (e != cudaSuccess) return e;
     const int64_t n = a.B * a.Dm * a.N;
-    diag_segment_pass_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_programmatic(diag_segment_pass_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
     return launch_bf16_vec<OPT, kOutput>(a, stream);
 }
 
