@@ -39,6 +39,7 @@ namespace {
 constexpr int kT = 256;
 constexpr int kQ = BwdArgs::kChunk;  // 64 tokens per backward chunk
 
+
 // Adjoint chunk state of one (b, c, h) and one 64x64 tile of (p, n).
 template <typename T>
 __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_constant__ BwdArgs a, int tilesP,
@@ -56,14 +57,38 @@ __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_consta
     __shared__ float s_cs[256], s_e[kQ], scratch[8];
     __shared__ __align__(16) float Ys[kQ][68], Cs[kQ][68];  // 16-byte aligned rows
     const int tid = threadIdx.x;
+    // the dy and C tiles: with P and N multiples of 4, four 16-byte vectors of
+    // each per thread, all in flight across the dt scan; else element by element
+    const bool vec = P % 4 == 0 && N % 4 == 0;
+    constexpr int kU = kQ * 16 / kT;
+    float4 yv[kU], cv[kU];
+    if (vec) {
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int e = tid + u * kT, j = e / 16, q = (e % 16) * 4;
+            const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j;
+            yv[u] = (j < Qv && p < P) ? ld4(dy + (tok * H + h) * P + p) : z4;
+            cv[u] = (j < Qv && n < N) ? ld4(Cm + (tok * G + g) * N + n) : z4;
+        }
+    }
     const float d = (tid < Qv) ? to_f32(dt[(b * L + t0 + tid) * H + h]) : 0.f;
     block_inclusive_scan_256(d * a.A[h], kQ, s_cs, scratch);
     if (tid < kQ) s_e[tid] = expf(s_cs[tid]);
-    for (int e = tid; e < kQ * 64; e += kT) {
-        const int j = e / 64, q = e % 64;
-        const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j;
-        Ys[j][q] = (j < Qv && p < P) ? to_f32(dy[(tok * H + h) * P + p]) : 0.f;
-        Cs[j][q] = (j < Qv && n < N) ? to_f32(Cm[(tok * G + g) * N + n]) : 0.f;
+    if (vec) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int e = tid + u * kT, j = e / 16, q = (e % 16) * 4;
+            *reinterpret_cast<float4 *>(&Ys[j][q]) = yv[u];
+            *reinterpret_cast<float4 *>(&Cs[j][q]) = cv[u];
+        }
+    } else {
+        for (int e = tid; e < kQ * 64; e += kT) {
+            const int j = e / 64, q = e % 64;
+            const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j;
+            Ys[j][q] = (j < Qv && p < P) ? to_f32(dy[(tok * H + h) * P + p]) : 0.f;
+            Cs[j][q] = (j < Qv && n < N) ? to_f32(Cm[(tok * G + g) * N + n]) : 0.f;
+        }
     }
     __syncthreads();
     const int ty = tid / 16, tx = tid % 16;
@@ -149,23 +174,34 @@ __global__ void __launch_bounds__(kT) adj_state_pass_kernel(const __grid_constan
 //   mm_nt  acc[i][j] += sum_k A[row][k] * Bt[col][k],  col = c0 + tx + 16 j
 //   mm_nn  acc[i][j] += sum_k A[row][k] * B[k][col],    col = c0 + tx*4 + j
 //   mm_tn  acc[i][j] += sum_k At[k][row] * B[k][col],   col = c0 + tx*4 + j
-// Row strides of 68 and 132 floats (4 mod 32): mm_nt's column reads across a
-// warp meet at most two to a bank; mm_nn / mm_tn read 16-byte vectors.
+// Every operand is read as 16-byte vectors (mm_nt and mm_nn fetch four k at a
+// time along rows, then add them one k after another: the same sums in the
+// same order as one k per step). K is rounded up to a multiple of 4: rows hold
+// zeros past the call's sizes. Row strides of 68 and 132 floats (4 mod 32)
+// keep the row reads of a warp (two rows of A, sixteen of Bt) two 128-byte
+// wavefronts at most.
+__device__ __forceinline__ float f4at(const float4 &v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
 __device__ __forceinline__ void mm_nt(float (&acc)[4][4], int K, int c0, const float *A, int sa, const float *Bt,
                                       int sb) {
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const float *ar = A + ty * 4 * sa, *br = Bt + (c0 + tx) * sb;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float av[4], bv[4];
+    const int K4 = (K + 3) & ~3;
+#pragma unroll 2
+    for (int k = 0; k < K4; k += 4) {
+        float4 av[4], bv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = ar[i * sa + k];
+        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa + k);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) bv[j] = br[j * 16 * sb + k];
+        for (int j = 0; j < 4; ++j) bv[j] = *reinterpret_cast<const float4 *>(br + j * 16 * sb + k);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(f4at(av[i], kk), f4at(bv[j], kk), acc[i][j]);
     }
 }
 
@@ -173,17 +209,20 @@ __device__ __forceinline__ void mm_nn(float (&acc)[4][4], int K, int c0, const f
                                       int sb) {
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const float *ar = A + ty * 4 * sa, *bc = B + c0 + tx * 4;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float av[4];
+    const int K4 = (K + 3) & ~3;
+#pragma unroll 2
+    for (int k = 0; k < K4; k += 4) {
+        float4 av[4], bv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = ar[i * sa + k];
-        const float4 b4 = *reinterpret_cast<const float4 *>(bc + k * sb);
-        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa + k);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int kk = 0; kk < 4; ++kk) bv[kk] = *reinterpret_cast<const float4 *>(bc + (k + kk) * sb);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(f4at(av[i], kk), f4at(bv[kk], j), acc[i][j]);
     }
 }
 
@@ -203,16 +242,28 @@ __device__ __forceinline__ void mm_tn(float (&acc)[4][4], int K, int c0, const f
     }
 }
 
+// Per-token dot products over p (or s) by four threads per token: token
+// t = tid / 4, thread q = tid % 4 takes p = q, q + 4, ...; the four partial
+// sums meet in a fixed-order butterfly, identical in all four threads. With row
+// strides of 4 mod 32 the reads of a warp (eight tokens x four q) hit 32
+// distinct banks.
+__device__ __forceinline__ float quad_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
+}
+
 // Shared memory of the per-chunk gradient kernel (floats), laid out for the
 // largest supported head (P 64, N 128) whatever the call's sizes: rows and
 // columns past P, N and the chunk's tokens hold zeros, so every 16-byte
 // vector read stays inside its array and contributes nothing.
 constexpr int kSX = 68;   // row stride of X, dY  [64 tokens][64 p]
 constexpr int kSN = 132;  // row stride of B, C [64 tokens][128 n] and hin, Gn [64 p][128 n]
+constexpr int kSM = 68;   // row stride of M1, M2, W [64 tokens][64]
 struct ChunkSmem {
     static constexpr int x = 0, y = x + kQ * kSX, bm = y + kQ * kSX, cm = bm + kQ * kSN, hin = cm + kQ * kSN,
-                         gn = hin + 64 * kSN, m1 = gn + 64 * kSN, m2 = m1 + kQ * kQ, w = m2 + kQ * kQ,
-                         vec = w + kQ * kQ, total = vec + 10 * kQ + kT + 8;
+                         gn = hin + 64 * kSN, m1 = gn + 64 * kSN, m2 = m1 + kQ * kSM, w = m2 + kQ * kSM,
+                         vec = w + kQ * kSM, total = vec + 10 * kQ + kT + 8;
 };
 
 template <typename T>
@@ -237,7 +288,35 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     const T *dtp = static_cast<const T *>(a.dt);
     const float Ah = a.A[h], Dh = a.D ? a.D[h] : 0.f;
 
-    // ---- loads: dt and its cumulative sum, x, dy, B, C, entering state, leaving cotangent
+    // ---- loads: x, dy, B, C, entering state, leaving cotangent, dt and its
+    //      cumulative sum. Rows of four consecutive elements when P and N are
+    //      multiples of 4 (base pointers are 16-byte aligned), else one element
+    //      at a time. Vector loads go out in two batches held in registers (x,
+    //      dy, B, C before the dt scan; hin, Gn after it), so each batch costs
+    //      one memory round trip.
+    const bool vec = P % 4 == 0 && N % 4 == 0;
+    const int64_t so = ((b * nc + c) * H + h) * (int64_t)P * N;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kXU = kQ * 16 / kT, kBU = kQ * 32 / kT, kHU = 64 * 32 / kT;  // vectors per thread
+    float4 xr[kXU], yr[kXU], br[kBU], cr[kBU];
+    if (vec) {
+#pragma unroll
+        for (int u = 0; u < kXU; ++u) {
+            const int e = tid + u * kT, j = e / 16, p = (e % 16) * 4;
+            const bool in = j < Qv && p < P;
+            const int64_t o = ((b * L + t0 + j) * H + h) * P + p;
+            xr[u] = in ? ld4(x + o) : z4;
+            yr[u] = in ? ld4(dy + o) : z4;
+        }
+#pragma unroll
+        for (int u = 0; u < kBU; ++u) {
+            const int e = tid + u * kT, j = e / 32, n = (e % 32) * 4;
+            const bool in = j < Qv && n < N;
+            const int64_t o = ((b * L + t0 + j) * G + g) * N + n;
+            br[u] = in ? ld4(Bm + o) : z4;
+            cr[u] = in ? ld4(Cm + o) : z4;
+        }
+    }
     const float dv = (tid < Qv) ? to_f32(dtp[(b * L + t0 + tid) * H + h]) : 0.f;
     if (tid < kQ) v_dt[tid] = dv;
     block_inclusive_scan_256(dv * Ah, kQ, v_cs, scratch);
@@ -246,30 +325,59 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
         v_e[tid] = expf(v_cs[tid]);
         v_eend[tid] = expf(cs_end - v_cs[tid]);
     }
-    for (int e = tid; e < kQ * 64; e += kT) {
-        const int j = e / 64, p = e % 64;
-        const bool in = j < Qv && p < P;
-        const int64_t o = ((b * L + t0 + j) * H + h) * P + p;
-        X[j * kSX + p] = in ? to_f32(x[o]) : 0.f;
-        Y[j * kSX + p] = in ? to_f32(dy[o]) : 0.f;
-    }
-    for (int e = tid; e < kQ * 128; e += kT) {
-        const int j = e / 128, n = e % 128;
-        const bool in = j < Qv && n < N;
-        const int64_t o = ((b * L + t0 + j) * G + g) * N + n;
-        Bs[j * kSN + n] = in ? to_f32(Bm[o]) : 0.f;
-        Cs[j * kSN + n] = in ? to_f32(Cm[o]) : 0.f;
-    }
-    const int64_t so = ((b * nc + c) * H + h) * (int64_t)P * N;
-    for (int e = tid; e < 64 * 128; e += kT) {
-        const int p = e / 128, n = e % 128;
-        const bool in = p < P && n < N;
-        Hin[p * kSN + n] = in ? a.hin[so + p * N + n] : 0.f;
-        Gn[p * kSN + n] = in ? a.adj[so + p * N + n] : 0.f;
+    if (vec) {
+        float4 hr[kHU], gr[kHU];
+#pragma unroll
+        for (int u = 0; u < kHU; ++u) {
+            const int e = tid + u * kT, p = e / 32, n = (e % 32) * 4;
+            const bool in = p < P && n < N;
+            hr[u] = in ? ld4(a.hin + so + p * N + n) : z4;
+            gr[u] = in ? ld4(a.adj + so + p * N + n) : z4;
+        }
+#pragma unroll
+        for (int u = 0; u < kXU; ++u) {
+            const int e = tid + u * kT, j = e / 16, p = (e % 16) * 4;
+            *reinterpret_cast<float4 *>(X + j * kSX + p) = xr[u];
+            *reinterpret_cast<float4 *>(Y + j * kSX + p) = yr[u];
+        }
+#pragma unroll
+        for (int u = 0; u < kBU; ++u) {
+            const int e = tid + u * kT, j = e / 32, n = (e % 32) * 4;
+            *reinterpret_cast<float4 *>(Bs + j * kSN + n) = br[u];
+            *reinterpret_cast<float4 *>(Cs + j * kSN + n) = cr[u];
+        }
+#pragma unroll
+        for (int u = 0; u < kHU; ++u) {
+            const int e = tid + u * kT, p = e / 32, n = (e % 32) * 4;
+            *reinterpret_cast<float4 *>(Hin + p * kSN + n) = hr[u];
+            *reinterpret_cast<float4 *>(Gn + p * kSN + n) = gr[u];
+        }
+    } else {
+        for (int e = tid; e < kQ * 64; e += kT) {
+            const int j = e / 64, p = e % 64;
+            const bool in = j < Qv && p < P;
+            const int64_t o = ((b * L + t0 + j) * H + h) * P + p;
+            X[j * kSX + p] = in ? to_f32(x[o]) : 0.f;
+            Y[j * kSX + p] = in ? to_f32(dy[o]) : 0.f;
+        }
+        for (int e = tid; e < kQ * 128; e += kT) {
+            const int j = e / 128, n = e % 128;
+            const bool in = j < Qv && n < N;
+            const int64_t o = ((b * L + t0 + j) * G + g) * N + n;
+            Bs[j * kSN + n] = in ? to_f32(Bm[o]) : 0.f;
+            Cs[j * kSN + n] = in ? to_f32(Cm[o]) : 0.f;
+        }
+        for (int e = tid; e < 64 * 128; e += kT) {
+            const int p = e / 128, n = e % 128;
+            const bool in = p < P && n < N;
+            Hin[p * kSN + n] = in ? a.hin[so + p * N + n] : 0.f;
+            Gn[p * kSN + n] = in ? a.adj[so + p * N + n] : 0.f;
+        }
     }
     __syncthreads();
 
     const int ty = tid / 16, tx = tid % 16;
+    const int tq = tid >> 2, tq4 = tid & 3;  // token and quarter of the four-thread dot products
     // ---- CB = C B^T and YX = dY X^T (rows t, columns s = tx + 16 j), then the
     //      masked, decayed forms
     {
@@ -283,18 +391,22 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
                 const int t = ty * 4 + i, s = tx + 16 * j;
                 const float ld = s <= t ? expf(v_cs[t] - v_cs[s]) : 0.f;
                 const float m1 = ld * cb[i][j], m2 = ld * v_dt[s] * yx[i][j];
-                M1[t * kQ + s] = m1;
-                M2[t * kQ + s] = m2;
-                Wb[t * kQ + s] = s < t ? m1 * v_dt[s] * yx[i][j] : 0.f;
+                M1[t * kSM + s] = m1;
+                M2[t * kSM + s] = m2;
+                Wb[t * kSM + s] = s < t ? m1 * v_dt[s] * yx[i][j] : 0.f;
             }
     }
     __syncthreads();
     // d cs from the in-chunk decays: row sum minus column sum of W
-    if (tid < kQ) {
+    {
         float rs = 0.f, cl = 0.f;
-        for (int s = 0; s < kQ; ++s) rs += Wb[tid * kQ + s];
-        for (int t = 0; t < kQ; ++t) cl += Wb[t * kQ + tid];
-        v_dcs[tid] = rs - cl;
+        for (int s = tq4; s < kQ; s += 4) {
+            rs += Wb[tq * kSM + s];
+            cl += Wb[s * kSM + tq];
+        }
+        rs = quad_sum(rs);
+        cl = quad_sum(cl);
+        if (tq4 == 0) v_dcs[tq] = rs - cl;
     }
     __syncthreads();
     // ---- GB[s][p] = sum_n B[s][n] Gn[p][n] into Wb (p = tx + 16 j; zero for p >= P)
@@ -304,47 +416,62 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx + 16 * j] = gb[i][j];
+            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kSM + tx + 16 * j] = gb[i][j];
     }
     __syncthreads();
     // r_s = eend_s dt_s x_s . GB_s
-    if (tid < kQ) {
+    {
         float r = 0.f;
-        for (int p = 0; p < P; ++p) r = fmaf(X[tid * kSX + p], Wb[tid * kQ + p], r);
-        v_r[tid] = v_eend[tid] * v_dt[tid] * r;
+        for (int p = tq4; p < P; p += 4) r = fmaf(X[tq * kSX + p], Wb[tq * kSM + p], r);
+        r = quad_sum(r);
+        if (tq4 == 0) v_r[tq] = v_eend[tq] * v_dt[tq] * r;
     }
     // ---- du = M1^T dY + eend o GB; dx = dt du + D dY; ddt (input part) = x . du
     {
         float du[4][4] = {};
-        mm_tn(du, kQ, 0, M1, kQ, Y, kSX);
+        mm_tn(du, kQ, 0, M1, kSM, Y, kSX);
         __syncthreads();  // every thread has read M1 before du replaces it
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int s = ty * 4 + i;
+            float dxv[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int p = tx * 4 + j;
-                const float u = du[i][j] + v_eend[s] * Wb[s * kQ + p];
-                M1[s * kQ + p] = u;  // du, for the row dot products below
-                if (s < Qv && p < P)
-                    a.dx[((b * L + t0 + s) * H + h) * (int64_t)P + p] = fmaf(v_dt[s], u, Dh * Y[s * kSX + p]);
+                const float u = du[i][j] + v_eend[s] * Wb[s * kSM + p];
+                M1[s * kSM + p] = u;  // du, for the token dot products below
+                dxv[j] = fmaf(v_dt[s], u, Dh * Y[s * kSX + p]);
+            }
+            float *dxr = a.dx + ((b * L + t0 + s) * H + h) * (int64_t)P;
+            if (s < Qv) {
+                if (vec) {
+                    if (tx * 4 < P) *reinterpret_cast<float4 *>(dxr + tx * 4) = make_float4(dxv[0], dxv[1], dxv[2], dxv[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (tx * 4 + j < P) dxr[tx * 4 + j] = dxv[j];
+                }
             }
         }
     }
     __syncthreads();
-    if (tid < kQ) {
+    {
         float dd = 0.f, xd = 0.f;
-        for (int p = 0; p < P; ++p) {
-            dd = fmaf(X[tid * kSX + p], M1[tid * kQ + p], dd);
-            xd = fmaf(Y[tid * kSX + p], X[tid * kSX + p], xd);
+        for (int p = tq4; p < P; p += 4) {
+            dd = fmaf(X[tq * kSX + p], M1[tq * kSM + p], dd);
+            xd = fmaf(Y[tq * kSX + p], X[tq * kSX + p], xd);
         }
-        v_ddt[tid] = dd;
-        v_dd[tid] = xd;
+        dd = quad_sum(dd);
+        xd = quad_sum(xd);
+        if (tq4 == 0) {
+            v_ddt[tq] = dd;
+            v_dd[tq] = xd;
+        }
     }
     // ---- dB = M2^T C + (dt eend) o (X Gn); dC = M2 B + e o (dY hin), 64 columns of n per pass
     for (int n0 = 0; n0 < N; n0 += 64) {
         float db[4][4] = {}, dc[4][4] = {};
-        mm_tn(db, kQ, n0, M2, kQ, Cs, kSN);
+        mm_tn(db, kQ, n0, M2, kSM, Cs, kSN);
         {
             float xg[4][4] = {};
             mm_nn(xg, P, n0, X, kSX, Gn, kSN);
@@ -353,7 +480,7 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
 #pragma unroll
                 for (int j = 0; j < 4; ++j) db[i][j] = fmaf(v_dt[ty * 4 + i] * v_eend[ty * 4 + i], xg[i][j], db[i][j]);
         }
-        mm_nn(dc, kQ, n0, M2, kQ, Bs, kSN);
+        mm_nn(dc, kQ, n0, M2, kSM, Bs, kSN);
         {
             float yh[4][4] = {};
             mm_nn(yh, P, n0, Y, kSX, Hin, kSN);
@@ -366,14 +493,20 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
         for (int i = 0; i < 4; ++i) {
             const int t = ty * 4 + i;
             if (t >= Qv) continue;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n = n0 + tx * 4 + j;
+            const int n = n0 + tx * 4;
+            const int64_t o = ((b * L + t0 + t) * H + h) * (int64_t)N + n;
+            if (vec) {
                 if (n < N) {
-                    const int64_t o = ((b * L + t0 + t) * H + h) * (int64_t)N + n;
-                    a.dB_part[o] = db[i][j];
-                    a.dC_part[o] = dc[i][j];
+                    *reinterpret_cast<float4 *>(a.dB_part + o) = make_float4(db[i][0], db[i][1], db[i][2], db[i][3]);
+                    *reinterpret_cast<float4 *>(a.dC_part + o) = make_float4(dc[i][0], dc[i][1], dc[i][2], dc[i][3]);
                 }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (n + j < N) {
+                        a.dB_part[o + j] = db[i][j];
+                        a.dC_part[o + j] = dc[i][j];
+                    }
             }
         }
     }
@@ -385,19 +518,20 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kQ + tx + 16 * j] = hc[i][j];
+            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kSM + tx + 16 * j] = hc[i][j];
     }
     // <Gn, hin>: fixed per-thread ranges (zeros past P, N), then a fixed-order sum
     {
-        float q = 0.f;
-        for (int e = tid; e < 64 * 128; e += kT) q = fmaf(Gn[(e / 128) * kSN + e % 128], Hin[(e / 128) * kSN + e % 128], q);
-        red[tid] = q;
+        float qv = 0.f;
+        for (int e = tid; e < 64 * 128; e += kT) qv = fmaf(Gn[(e / 128) * kSN + e % 128], Hin[(e / 128) * kSN + e % 128], qv);
+        red[tid] = qv;
     }
     __syncthreads();
-    if (tid < kQ) {
+    {
         float vv = 0.f;
-        for (int p = 0; p < P; ++p) vv = fmaf(Y[tid * kSX + p], Wb[tid * kQ + p], vv);
-        v_v[tid] = v_e[tid] * vv;
+        for (int p = tq4; p < P; p += 4) vv = fmaf(Y[tq * kSX + p], Wb[tq * kSM + p], vv);
+        vv = quad_sum(vv);
+        if (tq4 == 0) v_v[tq] = v_e[tq] * vv;
     }
     __syncthreads();
     // ---- d cs, da (reverse cumulative sum), ddt, dA and dD parts: the first two

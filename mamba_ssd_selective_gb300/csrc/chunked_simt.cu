@@ -69,13 +69,37 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
 
     const int ty = tid / 16, tx = tid % 16;
     float acc[4][4] = {};
+    // with P and N multiples of 4 (16-byte aligned rows) each thread loads its
+    // 16-byte vectors of a 32-token block together, then stores them
+    const bool vec = P % 4 == 0 && N % 4 == 0;
+    constexpr int kU = 32 * kTile / 4 / kT;
     for (int j0 = 0; j0 < Qv; j0 += 32) {
-        for (int e = tid; e < 32 * kTile; e += kT) {
-            const int jj = e / kTile, q = e % kTile, j = j0 + jj;
-            const int64_t p = (int64_t)pt * kTile + q, n = (int64_t)nt * kTile + q;
-            const int64_t tok = b * L + t0 + j;
-            Xs[jj][q] = (j < Qv && p < P) ? s_w[j] * to_f32(x[(tok * H + h) * P + p]) : 0.f;
-            Bs[jj][q] = (j < Qv && n < N) ? to_f32(Bm[(tok * G + g) * N + n]) : 0.f;
+        if (vec) {
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 xv[kU], bv[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int e = tid + u * kT, jj = e / (kTile / 4), q = (e % (kTile / 4)) * 4, j = j0 + jj;
+                const int64_t p = (int64_t)pt * kTile + q, n = (int64_t)nt * kTile + q;
+                const int64_t tok = b * L + t0 + j;
+                xv[u] = (j < Qv && p < P) ? ld4(x + (tok * H + h) * P + p) : z4;
+                bv[u] = (j < Qv && n < N) ? ld4(Bm + (tok * G + g) * N + n) : z4;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int e = tid + u * kT, jj = e / (kTile / 4), q = (e % (kTile / 4)) * 4;
+                const float w = j0 + jj < Qv ? s_w[j0 + jj] : 0.f;
+                *reinterpret_cast<float4 *>(&Xs[jj][q]) = make_float4(w * xv[u].x, w * xv[u].y, w * xv[u].z, w * xv[u].w);
+                *reinterpret_cast<float4 *>(&Bs[jj][q]) = bv[u];
+            }
+        } else {
+            for (int e = tid; e < 32 * kTile; e += kT) {
+                const int jj = e / kTile, q = e % kTile, j = j0 + jj;
+                const int64_t p = (int64_t)pt * kTile + q, n = (int64_t)nt * kTile + q;
+                const int64_t tok = b * L + t0 + j;
+                Xs[jj][q] = (j < Qv && p < P) ? s_w[j] * to_f32(x[(tok * H + h) * P + p]) : 0.f;
+                Bs[jj][q] = (j < Qv && n < N) ? to_f32(Bm[(tok * G + g) * N + n]) : 0.f;
+            }
         }
         __syncthreads();
 #pragma unroll 8

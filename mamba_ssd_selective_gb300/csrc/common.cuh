@@ -53,6 +53,17 @@ inline cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 b
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Four consecutive elements (4-element aligned) as float32.
+template <typename T> __device__ __forceinline__ float4 ld4(const T *p);
+template <> __device__ __forceinline__ float4 ld4<float>(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+template <> __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+
 template <typename I> __host__ __device__ __forceinline__ I imin(I a, I b) { return a < b ? a : b; }
 template <typename I> __host__ __device__ __forceinline__ I imax(I a, I b) { return a > b ? a : b; }
 

@@ -438,10 +438,11 @@ def _check_grads(g, ref, tol, what=""):
 
 @pytest.mark.parametrize("io,tol", [("f32", 1e-4), ("bf16", 2e-2)])
 @pytest.mark.parametrize("shape", [(1, 256, 4, 64, 16, 1), (2, 200, 4, 32, 64, 2), (1, 130, 3, 64, 128, 1),
-                                   (2, 77, 6, 16, 32, 3)])
+                                   (2, 77, 6, 16, 32, 3), (1, 150, 2, 18, 10, 1), (2, 70, 2, 30, 64, 2)])
 def test_backward_every_element(ssd, io, tol, shape):
     """Every gradient (dx, ddt, dA, dB, dC, dD, dinit) against the float64
-    reverse-mode oracle; ragged last chunks, several B/C groups."""
+    reverse-mode oracle; ragged last chunks, several B/C groups, and head
+    sizes that are not multiples of 4 (element-wise loads and stores)."""
     d, dy, dfin = _bwd_case(shape, io, 21)
     ref = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"], d["init_state"], dfin)
     t = IO_TORCH[io]
