@@ -189,19 +189,31 @@ __device__ __forceinline__ void mm_nt(float (&acc)[4][4], int K, int c0, const f
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const float *ar = A + ty * 4 * sa, *br = Bt + (c0 + tx) * sb;
     const int K4 = (K + 3) & ~3;
+    // operands of the next four k are loaded while the current four are used
+    float4 av[4], bv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) bv[j] = *reinterpret_cast<const float4 *>(br + j * 16 * sb);
 #pragma unroll 2
     for (int k = 0; k < K4; k += 4) {
-        float4 av[4], bv[4];
+        const int kn = k + 4 < K4 ? k + 4 : k;
+        float4 an[4], bn[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa + k);
+        for (int i = 0; i < 4; ++i) an[i] = *reinterpret_cast<const float4 *>(ar + i * sa + kn);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) bv[j] = *reinterpret_cast<const float4 *>(br + j * 16 * sb + k);
+        for (int j = 0; j < 4; ++j) bn[j] = *reinterpret_cast<const float4 *>(br + j * 16 * sb + kn);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(f4at(av[i], kk), f4at(bv[j], kk), acc[i][j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            av[i] = an[i];
+            bv[i] = bn[i];
+        }
     }
 }
 
@@ -210,19 +222,92 @@ __device__ __forceinline__ void mm_nn(float (&acc)[4][4], int K, int c0, const f
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const float *ar = A + ty * 4 * sa, *bc = B + c0 + tx * 4;
     const int K4 = (K + 3) & ~3;
+    float4 av[4], bv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) bv[kk] = *reinterpret_cast<const float4 *>(bc + kk * sb);
 #pragma unroll 2
     for (int k = 0; k < K4; k += 4) {
-        float4 av[4], bv[4];
+        const int kn = k + 4 < K4 ? k + 4 : k;
+        float4 an[4], bn[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa + k);
+        for (int i = 0; i < 4; ++i) an[i] = *reinterpret_cast<const float4 *>(ar + i * sa + kn);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) bv[kk] = *reinterpret_cast<const float4 *>(bc + (k + kk) * sb);
+        for (int kk = 0; kk < 4; ++kk) bn[kk] = *reinterpret_cast<const float4 *>(bc + (kn + kk) * sb);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(f4at(av[i], kk), f4at(bv[kk], j), acc[i][j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            av[i] = an[i];
+            bv[i] = bn[i];
+        }
+    }
+}
+
+// Two products in one k loop, for twice the independent FMA chains per warp
+// (eight warps per SM leave little else to hide shared-memory latency):
+//   mm_nt_2  acc1 += A Bt1^T, acc2 += A Bt2^T   (shared A)
+//   mm_nn_2  acc1 += A1 B1,   acc2 += A2 B2     (same strides and K)
+// Each sum keeps the one-k-after-another order of mm_nt / mm_nn.
+__device__ __forceinline__ void mm_nt_2(float (&acc1)[4][4], float (&acc2)[4][4], int K, const float *A, int sa,
+                                        const float *Bt1, const float *Bt2, int sb) {
+    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+    const float *ar = A + ty * 4 * sa, *b1 = Bt1 + tx * sb, *b2 = Bt2 + tx * sb;
+    const int K4 = (K + 3) & ~3;
+#pragma unroll 1
+    for (int k = 0; k < K4; k += 4) {
+        float4 av[4], bv1[4], bv2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4 *>(ar + i * sa + k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            bv1[j] = *reinterpret_cast<const float4 *>(b1 + j * 16 * sb + k);
+            bv2[j] = *reinterpret_cast<const float4 *>(b2 + j * 16 * sb + k);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc1[i][j] = fmaf(f4at(av[i], kk), f4at(bv1[j], kk), acc1[i][j]);
+                    acc2[i][j] = fmaf(f4at(av[i], kk), f4at(bv2[j], kk), acc2[i][j]);
+                }
+    }
+}
+
+__device__ __forceinline__ void mm_nn_2(float (&acc1)[4][4], float (&acc2)[4][4], int K, int c0, const float *A1,
+                                        const float *A2, int sa, const float *B1, const float *B2, int sb) {
+    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+    const float *a1 = A1 + ty * 4 * sa, *a2 = A2 + ty * 4 * sa, *c1 = B1 + c0 + tx * 4, *c2 = B2 + c0 + tx * 4;
+    const int K4 = (K + 3) & ~3;
+#pragma unroll 1
+    for (int k = 0; k < K4; k += 4) {
+        float4 av1[4], av2[4], bv1[4], bv2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            av1[i] = *reinterpret_cast<const float4 *>(a1 + i * sa + k);
+            av2[i] = *reinterpret_cast<const float4 *>(a2 + i * sa + k);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            bv1[kk] = *reinterpret_cast<const float4 *>(c1 + (k + kk) * sb);
+            bv2[kk] = *reinterpret_cast<const float4 *>(c2 + (k + kk) * sb);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc1[i][j] = fmaf(f4at(av1[i], kk), f4at(bv1[kk], j), acc1[i][j]);
+                    acc2[i][j] = fmaf(f4at(av2[i], kk), f4at(bv2[kk], j), acc2[i][j]);
+                }
     }
 }
 
@@ -230,15 +315,19 @@ __device__ __forceinline__ void mm_tn(float (&acc)[4][4], int K, int c0, const f
                                       int sb) {
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const float *ac = At + ty * 4, *bc = B + c0 + tx * 4;
+    float4 a4 = *reinterpret_cast<const float4 *>(ac), b4 = *reinterpret_cast<const float4 *>(bc);
 #pragma unroll 4
     for (int k = 0; k < K; ++k) {
-        const float4 a4 = *reinterpret_cast<const float4 *>(ac + k * sa);
-        const float4 b4 = *reinterpret_cast<const float4 *>(bc + k * sb);
+        const int kn = k + 1 < K ? k + 1 : k;
+        const float4 an = *reinterpret_cast<const float4 *>(ac + kn * sa);
+        const float4 bn = *reinterpret_cast<const float4 *>(bc + kn * sb);
         const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        a4 = an;
+        b4 = bn;
     }
 }
 
@@ -380,9 +469,12 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     const int tq = tid >> 2, tq4 = tid & 3;  // token and quarter of the four-thread dot products
     // ---- CB = C B^T and YX = dY X^T (rows t, columns s = tx + 16 j), then the
     //      masked, decayed forms
+    // HC[t][p] = sum_n C[t][n] hin[p][n] (p = tx + 16 j) comes out of the same
+    // loop as CB and stays in registers until its use at the end
+    float hc[4][4] = {};
     {
         float cb[4][4] = {}, yx[4][4] = {};
-        mm_nt(cb, N, 0, Cs, kSN, Bs, kSN);
+        mm_nt_2(cb, hc, N, Cs, kSN, Bs, Hin, kSN);
         mm_nt(yx, P, 0, Y, kSX, X, kSX);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -472,22 +564,17 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
     for (int n0 = 0; n0 < N; n0 += 64) {
         float db[4][4] = {}, dc[4][4] = {};
         mm_tn(db, kQ, n0, M2, kSM, Cs, kSN);
-        {
-            float xg[4][4] = {};
-            mm_nn(xg, P, n0, X, kSX, Gn, kSN);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) db[i][j] = fmaf(v_dt[ty * 4 + i] * v_eend[ty * 4 + i], xg[i][j], db[i][j]);
-        }
         mm_nn(dc, kQ, n0, M2, kSM, Bs, kSN);
         {
-            float yh[4][4] = {};
-            mm_nn(yh, P, n0, Y, kSX, Hin, kSN);
+            float xg[4][4] = {}, yh[4][4] = {};
+            mm_nn_2(xg, yh, P, n0, X, Y, kSX, Gn, Hin, kSN);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) dc[i][j] = fmaf(v_e[ty * 4 + i], yh[i][j], dc[i][j]);
+                for (int j = 0; j < 4; ++j) {
+                    db[i][j] = fmaf(v_dt[ty * 4 + i] * v_eend[ty * 4 + i], xg[i][j], db[i][j]);
+                    dc[i][j] = fmaf(v_e[ty * 4 + i], yh[i][j], dc[i][j]);
+                }
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -511,15 +598,11 @@ __global__ void __launch_bounds__(kT) chunk_bwd_kernel(const __grid_constant__ B
         }
     }
     __syncthreads();
-    // ---- HC[t][p] = sum_n C[t][n] hin[p][n] into Wb; v_t = e_t dY_t . HC_t
-    {
-        float hc[4][4] = {};
-        mm_nt(hc, N, 0, Cs, kSN, Hin, kSN);
+    // ---- HC (computed with CB) into Wb; v_t = e_t dY_t . HC_t
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kSM + tx + 16 * j] = hc[i][j];
-    }
+        for (int j = 0; j < 4; ++j) Wb[(ty * 4 + i) * kSM + tx + 16 * j] = hc[i][j];
     // <Gn, hin>: fixed per-thread ranges (zeros past P, N), then a fixed-order sum
     {
         float qv = 0.f;
