@@ -106,11 +106,14 @@ __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_consta
     float *S = a.adj + (((b * a.nc + c) * H + h) * P) * N;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int64_t p = (int64_t)pt * 64 + ty * 4 + i;
+        const int64_t p = (int64_t)pt * 64 + ty * 4 + i, n = (int64_t)nt * 64 + tx * 4;
+        if (p >= P) continue;
+        if (vec) {
+            if (n < N) *reinterpret_cast<float4 *>(S + p * N + n) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t n = (int64_t)nt * 64 + tx * 4 + k;
-            if (p < P && n < N) S[p * N + n] = acc[i][k];
+            for (int k = 0; k < 4; ++k)
+                if (n + k < N) S[p * N + n + k] = acc[i][k];
         }
     }
 }
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_consta
 // dinit. Decays exp(cs_end(c)) come from the forward recompute. The values of
 // kPFA chunks are loaded before the chain consumes them, so that each thread
 // keeps kPFA independent loads in flight.
-constexpr int kPFA = 8;
+constexpr int kPFA = 16;
 
 template <int VW>
 __global__ void __launch_bounds__(kT) adj_state_pass_kernel(const __grid_constant__ BwdArgs a) {
@@ -673,10 +676,21 @@ __global__ void __launch_bounds__(kT) bwd_reduce_kernel(const __grid_constant__ 
     if (i < total) {
         const int64_t n = i % N, g = (i / N) % G, bt = i / (N * G);
         float sb = 0.f, sc = 0.f;
-        for (int64_t k = 0; k < hpg; ++k) {
-            const int64_t o = (bt * H + g * hpg + k) * N + n;
-            sb += a.dB_part[o];
-            sc += a.dC_part[o];
+        // eight heads' parts loaded before they are added (in head order)
+        for (int64_t k0 = 0; k0 < hpg; k0 += 8) {
+            float vb[8], vc[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t o = (bt * H + g * hpg + k0 + u) * N + n;
+                vb[u] = k0 + u < hpg ? a.dB_part[o] : 0.f;
+                vc[u] = k0 + u < hpg ? a.dC_part[o] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (k0 + u < hpg) {
+                    sb += vb[u];
+                    sc += vc[u];
+                }
         }
         a.dB[i] = sb;
         a.dC[i] = sc;

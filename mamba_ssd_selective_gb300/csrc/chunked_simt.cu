@@ -117,11 +117,14 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
     float *S = a.states + (((b * a.nc + c) * H + h) * P) * N;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int64_t p = (int64_t)pt * kTile + ty * 4 + i;
+        const int64_t p = (int64_t)pt * kTile + ty * 4 + i, n = (int64_t)nt * kTile + tx * 4;
+        if (p >= P) continue;
+        if (vec) {
+            if (n < N) *reinterpret_cast<float4 *>(S + p * N + n) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t n = (int64_t)nt * kTile + tx * 4 + k;
-            if (p < P && n < N) S[p * N + n] = acc[i][k];
+            for (int k = 0; k < 4; ++k)
+                if (n + k < N) S[p * N + n + k] = acc[i][k];
         }
     }
 }
@@ -132,8 +135,8 @@ __global__ void __launch_bounds__(kT) chunk_state_simt(ChunkedArgs a, int tilesP
 // (tensor-core path, read from and replaced in states_bf16). VW consecutive
 // state elements per thread; the chunk states of kPF chunks are loaded
 // before the serial update consumes them, so each thread keeps kPF
-// independent loads in flight.
-constexpr int kPF = 8;
+// independent loads in flight: 16 on the float32 in-place path (the CUDA-core
+// prefill and the backward's recompute), 8 where more registers are live.
 
 template <typename TIn, bool F32_INPLACE, bool BF16, int VW>
 __global__ void __launch_bounds__(kT, 2) state_pass_kernel(ChunkedArgs a) {
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(kT, 2) state_pass_kernel(ChunkedArgs a) {
     const float *cs = a.chunk_sum + (b * H + h) * nc;
     const int64_t stride = H * PN;  // next chunk, same (b, h, element)
     const int64_t base = ((b * nc) * H + h) * PN + e;
+    constexpr int kPF = std::is_same<TIn, float>::value && F32_INPLACE && !BF16 ? 16 : 8;
     for (int64_t c0 = 0; c0 < nc; c0 += kPF) {
         float s[kPF][VW], dA[kPF];
 #pragma unroll
