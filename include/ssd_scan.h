@@ -24,6 +24,13 @@
  *  - Calls are asynchronous on `stream` (0 = legacy default stream): they
  *    validate their arguments on the host, enqueue kernels and return. There
  *    is no host synchronisation and no exception crosses the ABI.
+ *  - The tensor-core prefill, decode, decode-layer and Mamba-1 kernels are
+ *    launched as programmatic dependents of the kernel before them in the
+ *    stream (CUDA programmatic dependent launch): they may be placed on the
+ *    GPU while it drains, but each waits for its completion before touching
+ *    memory, so stream order means what it means for ordinary launches (a
+ *    kernel of another library before a call has completed before the call
+ *    reads its inputs).
  *  - Validation happens before any CUDA call: an invalid argument returns
  *    SSD_ERR_INVALID_ARG (or SSD_ERR_UNSUPPORTED for a valid but unbuilt
  *    shape) and enqueues nothing. SSD_ERR_CUDA reports a failed launch.
