@@ -54,7 +54,6 @@ struct TcParams {
     CUtensorMap mc;    // C  as (G*N, L, B), box (64, 128, 1)   (chunk scan)
     CUtensorMap my;    // y  as (H*P, L, B), box (64, 128, 1)   (chunk scan)
     CUtensorMap mh;    // bf16 entering states as (N, B*nc*H*P), box (64, 64)   (chunk scan)
-    CUtensorMap my32;  // y  as (H*P, L, B), box (32, 32, 1), 64-byte swizzle (persistent chunk scan)
     int hb;            // heads per work item of the persistent chunk scan (divides H / G)
     int nhg;           // head groups, H / hb
     int64_t n_items;   // work items of the persistent chunk scan, B * tiles * nhg
@@ -1016,11 +1015,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
     const void *base;
     int rank;
-    int swz64;  // 64-byte swizzle instead of 128-byte
     uint64_t dims[3], strides[2];
     uint32_t box[3];
     bool operator==(const MapKey &o) const {
-        if (base != o.base || rank != o.rank || swz64 != o.swz64) return false;
+        if (base != o.base || rank != o.rank) return false;
         for (int k = 0; k < rank; ++k)
             if (dims[k] != o.dims[k] || box[k] != o.box[k]) return false;
         for (int k = 0; k + 1 < rank; ++k)
@@ -1056,7 +1054,7 @@ bool make_map(CUtensorMap *out, const MapKey &k) {
     CUtensorMap m;
     CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)k.rank, const_cast<void *>(k.base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     k.swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lock(g_map_mu);
@@ -1070,10 +1068,8 @@ bool make_map(CUtensorMap *out, const MapKey &k) {
 
 // (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (box_cols, box_rows, 1);
 // 128-byte swizzle for 64-column boxes, 64-byte swizzle for 32-column boxes
-bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
-                int box_cols = 64) {
+bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows) {
     MapKey k{};
-    k.swz64 = box_cols == 32;
     k.base = base;
     k.rank = 3;
     k.dims[0] = (uint64_t)inner;
@@ -1081,7 +1077,7 @@ bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, in
     k.dims[2] = (uint64_t)B;
     k.strides[0] = (uint64_t)inner * 2;
     k.strides[1] = (uint64_t)inner * L * 2;
-    k.box[0] = (uint32_t)box_cols;
+    k.box[0] = 64;
     k.box[1] = (uint32_t)box_rows;
     k.box[2] = 1;
     return make_map(out, k);
@@ -1161,7 +1157,6 @@ cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream) {
     ok &= map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kRows);
     ok &= map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kRows);
     ok &= map_tokens(&p.my, a.y, a.H * a.P, a.L, a.B, kRows);
-    ok &= map_tokens(&p.my32, a.y, a.H * a.P, a.L, a.B, 32, 32);
     {
         MapKey k{};
         k.base = a.states_bf16;
