@@ -193,8 +193,10 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
                 sCf[tt][n] = __bfloat162float(sC[buf][tt][n]);
             }
             __syncthreads();
-            // one token of the recurrence for this thread's states
-            auto token = [&](int tt) {
+            // one token of the recurrence for this thread's states; returns the
+            // thread's part of sum_n C_n h_n. With `finish` the token's y is
+            // completed here (the partner thread's part by a shuffle).
+            auto token = [&](int tt, bool finish) -> float {
                 float dtv = __bfloat162float(sdt[buf][tt][ch]);
                 if (OPT) dtv = step_of(dtv, bias, softplus);
                 if (MODE == kLocal) dt_sum += dtv;
@@ -217,23 +219,49 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
                         if (MODE != kLocal) acc2[r] = fma2(cc, h2[jp], acc2[r]);
                     }
                 }
-                if (MODE == kLocal) return;
+                if (MODE == kLocal) return 0.f;
                 float a0, a1, a2v, a3;
                 up2(acc2[0], a0, a1);
                 up2(acc2[1], a2v, a3);
                 float acc = (a0 + a1) + (a2v + a3);
+                if (!finish) return acc;
                 if (TPC == 2) acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 float out = acc + Dd * xv;
                 if (has_z) out *= silu(__bfloat162float(sz[buf][tt][ch]));
                 if (half == 0) sy[tt][ch] = __float2bfloat16_rn(out);
+                return 0.f;
+            };
+            // y of eight tokens from both threads' parts: the pair exchanges
+            // halves with four shuffles and each thread completes four tokens
+            // (half 0 the first four). The same sums as `finish`: a + b = b + a.
+            auto finish8 = [&](int tt0, const float (&pt)[8]) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float recv = __shfl_xor_sync(0xffffffffu, half ? pt[j] : pt[j + 4], 1);
+                    const int tt = tt0 + (half ? j + 4 : j);
+                    const float acc = (half ? pt[j + 4] : pt[j]) + recv;
+                    float out = acc + Dd * __bfloat162float(sx[buf][tt][ch]);
+                    if (has_z) out *= silu(__bfloat162float(sz[buf][tt][ch]));
+                    sy[tt][ch] = __float2bfloat16_rn(out);
+                }
             };
             // full tiles unrolled so the decays of the next tokens overlap this
             // token's dependent chain; the same arithmetic either way
             if (tn == kTT) {
+                if constexpr (TPC == 2 && MODE != kLocal) {
+#pragma unroll 1
+                    for (int tt0 = 0; tt0 < kTT; tt0 += 8) {
+                        float pt[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pt[j] = token(tt0 + j, false);
+                        finish8(tt0, pt);
+                    }
+                } else {
 #pragma unroll UNR
-                for (int tt = 0; tt < kTT; ++tt) token(tt);
+                    for (int tt = 0; tt < kTT; ++tt) token(tt, true);
+                }
             } else {
-                for (int tt = 0; tt < tn; ++tt) token(tt);
+                for (int tt = 0; tt < tn; ++tt) token(tt, true);
             }
             __syncthreads();
             // write the tile's y rows back, 16 bytes per copy
