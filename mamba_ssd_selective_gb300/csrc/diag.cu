@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
                 if (MODE == kLocal) dt_sum += dtv;
                 const float xv = __bfloat162float(sx[buf][tt][ch]);
                 const uint64_t d2 = pk2(dtv, dtv), u2 = pk2(dtv * xv, dtv * xv);
-                uint64_t acc2[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
+                uint64_t acc2 = pk2(0.f, 0.f);  // packed partial sums of C_n h_n
 #pragma unroll
                 for (int q = 0; q < NH / 4; ++q) {
                     const float4 bq = *reinterpret_cast<const float4 *>(&sBf[tt][nb + 4 * q]);
@@ -216,14 +216,13 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
                         const uint64_t bb = r ? pk2(bq.z, bq.w) : pk2(bq.x, bq.y);
                         const uint64_t cc = r ? pk2(cq.z, cq.w) : pk2(cq.x, cq.y);
                         h2[jp] = fma2(al, h2[jp], mul2(u2, bb));
-                        if (MODE != kLocal) acc2[r] = fma2(cc, h2[jp], acc2[r]);
+                        if (MODE != kLocal) acc2 = fma2(cc, h2[jp], acc2);
                     }
                 }
                 if (MODE == kLocal) return 0.f;
-                float a0, a1, a2v, a3;
-                up2(acc2[0], a0, a1);
-                up2(acc2[1], a2v, a3);
-                float acc = (a0 + a1) + (a2v + a3);
+                float a0, a1;
+                up2(acc2, a0, a1);
+                float acc = a0 + a1;
                 if (!finish) return acc;
                 if (TPC == 2) acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 float out = acc + Dd * xv;
