@@ -205,3 +205,19 @@ def test_binding_checks_shapes_on_cpu_tensors():
     with pytest.raises((ValueError, TypeError)):
         binding.ssd_scan_chunked(x, torch.zeros(1, 8, 3), torch.zeros(2), torch.zeros(1, 8, 1, 4),
                                  torch.zeros(1, 8, 1, 4), chunk_size=64)
+
+
+def test_tensor_core_probe_compiles(tmp_path):
+    """The tensor-core probe of the GPU tests builds against the library's
+    inline-PTX helpers (nvcc cross-compiles for sm_103a without a GPU), so a
+    helper it needs cannot disappear unnoticed before a GPU run."""
+    import subprocess
+    try:
+        nvcc = nvbuild.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not installed")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc", "tc_probe.cu")
+    cmd = [nvcc] + nvbuild.ARCH + ["-O0", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-I", nvbuild.CSRC,
+                                   "-I", nvbuild.INCLUDE, src, "-o", str(tmp_path / "libtcprobe.so")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
