@@ -223,7 +223,8 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
                 float a0, a1;
                 up2(acc2, a0, a1);
                 float acc = a0 + a1;
-                if (!finish) return acc;
+                // without the options half 0's part carries D x (finish8 then needs no x)
+                if (!finish) return OPT ? acc : fmaf(half ? 0.f : Dd, xv, acc);
                 if (TPC == 2) acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 float out = acc + Dd * xv;
                 if (has_z) out *= silu(__bfloat162float(sz[buf][tt][ch]));
@@ -238,8 +239,8 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
                 for (int j = 0; j < 4; ++j) {
                     const float recv = __shfl_xor_sync(0xffffffffu, half ? pt[j] : pt[j + 4], 1);
                     const int tt = tt0 + (half ? j + 4 : j);
-                    const float acc = (half ? pt[j + 4] : pt[j]) + recv;
-                    float out = acc + Dd * __bfloat162float(sx[buf][tt][ch]);
+                    float out = (half ? pt[j + 4] : pt[j]) + recv;
+                    if (OPT) out += Dd * __bfloat162float(sx[buf][tt][ch]);
                     if (has_z) out *= silu(__bfloat162float(sz[buf][tt][ch]));
                     sy[tt][ch] = __float2bfloat16_rn(out);
                 }
@@ -247,7 +248,17 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
             // full tiles unrolled so the decays of the next tokens overlap this
             // token's dependent chain; the same arithmetic either way
             if (tn == kTT) {
-                if constexpr (TPC == 2 && MODE != kLocal) {
+                if constexpr (TPC == 2 && MODE != kLocal && !OPT) {
+                    // two groups of eight per iteration: measured faster without
+                    // the options, slower with them (z gate, softplus)
+#pragma unroll 2
+                    for (int tt0 = 0; tt0 < kTT; tt0 += 8) {
+                        float pt[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pt[j] = token(tt0 + j, false);
+                        finish8(tt0, pt);
+                    }
+                } else if constexpr (TPC == 2 && MODE != kLocal) {
 #pragma unroll 1
                     for (int tt0 = 0; tt0 < kTT; tt0 += 8) {
                         float pt[8];
