@@ -249,9 +249,9 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
             // token's dependent chain; the same arithmetic either way
             if (tn == kTT) {
                 if constexpr (TPC == 2 && MODE != kLocal && !OPT) {
-                    // two groups of eight per iteration: measured faster without
-                    // the options, slower with them (z gate, softplus)
-#pragma unroll 2
+                    // the whole tile's four groups of eight unrolled: measured
+                    // faster without the options, slower with them (z gate, softplus)
+#pragma unroll 4
                     for (int tt0 = 0; tt0 < kTT; tt0 += 8) {
                         float pt[8];
 #pragma unroll
