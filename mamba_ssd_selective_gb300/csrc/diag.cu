@@ -233,7 +233,10 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
             };
             // y of eight tokens from both threads' parts: the pair exchanges
             // halves with four shuffles and each thread completes four tokens
-            // (half 0 the first four). The same sums as `finish`: a + b = b + a.
+            // (half 0 the first four). With the options these are the sums of
+            // `finish` (a + b = b + a); without, D x is already in half 0's part.
+            // Tiles start at multiples of 32 tokens whatever the chunk size, so
+            // which tokens take this path does not depend on it.
             auto finish8 = [&](int tt0, const float (&pt)[8]) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
