@@ -74,3 +74,22 @@ def test_roofline_byte_counts():
     # 28.2 MB per step: zero initial state, so only the final state is moved
     assert abs(b["total"] / 1e6 - 28.25) < 0.01
     assert bench.stage_algorithmic_bytes(w, "chunk_scan") == b["x"] + b["dt"] + b["B"] + b["C"] + b["y"]
+
+
+def test_traffic_records_are_well_formed():
+    """profiles/traffic.json: one record per dominant kernel the bench reports,
+    naming a kernel that exists in its source file, with a positive per-launch
+    byte count and the capture it came from; a record whose source has changed
+    since is reported as null by the bench, never as a stale number."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        recs = json.load(f)
+    assert set(recs) >= {"chunk_scan", "decode_step", "diag_scan"}
+    for key, rec in recs.items():
+        src = os.path.join(ROOT, "mamba_ssd_selective_gb300", "csrc", rec["source"])
+        assert os.path.exists(src), key
+        with open(src) as f:
+            assert rec["kernel"] in f.read(), key
+        assert int(rec["bytes_per_launch"]) > 0 and rec["capture"], key
+        got = bench._traffic_for(key)
+        assert got is None or got == rec["bytes_per_launch"], key
+    assert bench._traffic_for("no_such_kernel") is None
