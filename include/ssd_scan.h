@@ -132,12 +132,11 @@ ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt,
 
 /*
  * ssd_scan_chunked without a caller-provided workspace, for callers that
- * cannot allocate device memory where they run the scan: code running while
- * the stream is being captured into a CUDA graph (cudaMalloc is refused during
- * capture), plug-ins whose host framework owns all device memory, and
- * latency-critical loops that cannot take the device-wide synchronisation of an
- * allocation. The pages have no counterpart of this call; it exists for such
- * callers only.
+ * cannot allocate device memory where they run the scan: plug-ins whose host
+ * framework owns all device memory and forbids allocating inside its enqueue
+ * call, and latency-critical loops that cannot take the device-wide
+ * synchronisation a cudaMalloc/cudaFree pair brings. The pages have no
+ * counterpart of this call; it exists for such callers only.
  *
  * Same arguments and results as ssd_scan_chunked, minus the workspace: the
  * per-chunk states live in a 64 MiB scratch array compiled into the library
@@ -147,12 +146,26 @@ ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt,
  * up the scratch address with that device current; make it before any stream
  * capture begins. Nothing here allocates. All calls on a device share the
  * scratch: calls whose kernels may overlap on the GPU (e.g. on two unordered
- * streams) race on it and must be serialised by the caller.
+ * streams) race on it and must be serialised by the caller. A bounded in-kernel
+ * wait that gives up records SSD_ERR_TIMEOUT in the scratch's status word,
+ * which ssd_scan_chunked_noalloc_status reads.
  */
 ssd_status ssd_scan_chunked_noalloc(const ssd_dims *dims, const void *x, const void *dt, const float *A,
                                     const void *B, const void *C, const float *D,
                                     const float *init_state, int chunk_size, void *y,
                                     float *final_state, cudaStream_t stream);
+
+/*
+ * Status of the latest ssd_scan_chunked_noalloc call on the current device:
+ * waits for `stream` (host synchronisation, like ssd_workspace_status), then
+ * reads the status word at the start of the built-in scratch. Returns SSD_OK,
+ * or SSD_ERR_TIMEOUT when a bounded wait of that call gave up (its y and
+ * final_state are then not valid). When scratch_addr is not NULL it receives
+ * the scratch's device address on the current device (for example to run
+ * ssd_selftest_bounded_wait on its status word). Allocates nothing; like the
+ * scan, its first use on a device looks the scratch address up.
+ */
+ssd_status ssd_scan_chunked_noalloc_status(cudaStream_t stream, void **scratch_addr);
 
 /*
  * One decode token for a batch of sequences, state updated in place (the

@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
             lib.ssd_scan_chunked.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp, sz, vp]
             lib.ssd_scan_chunked_noalloc.argtypes = [dp] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
             lib.ssd_scan_chunked_noalloc.restype = ctypes.c_int
+            lib.ssd_scan_chunked_noalloc_status.argtypes = [vp, ctypes.POINTER(vp)]
+            lib.ssd_scan_chunked_noalloc_status.restype = ctypes.c_int
             lib.ssd_decode_step.argtypes = [dp] + [vp] * 9
             lib.selective_scan_diag.argtypes = [i64, i64, i64, i64, i32] + [vp] * 7 + [ctypes.c_int, vp, vp, vp]
             lib.selective_scan_diag_ex.argtypes = ([i64, i64, i64, i64, i32] + [vp] * 8 + [i32, vp, ctypes.c_int]
@@ -237,15 +239,19 @@ def ssd_scan_chunked_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size
                              stream=None, simt=False):
     """ssd_scan_chunked without a workspace argument: the per-chunk states go to
     the library's built-in 64 MiB device scratch, so the C call allocates
-    nothing (for callers that cannot allocate where they run the scan, e.g.
-    inside someone else's graph capture). `y` and `final_state` must be given
-    by such callers; they are allocated here only for convenience when None.
-    Returns (y, final_state)."""
+    nothing (for callers that cannot allocate where they run the scan, such as
+    plug-ins whose framework owns all device memory). Such callers pass `y`
+    and `final_state`; this wrapper allocates them only when they are None.
+    The scan runs on x's device, which must be the current CUDA device: the
+    library looks the scratch up on the current device. Returns (y, final_state)."""
     if x.dim() != 4 or B.dim() != 4:
         raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     dev, io = x.device, x.dtype
+    if dev.type != "cuda" or dev.index != torch.cuda.current_device():
+        raise ValueError(f"ssd_scan_chunked_noalloc: x is on {dev}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}; the built-in scratch is per device")
     _need(dt, "dt", (Bsz, L, H), io, dev)
     _need(A, "A", (H,), torch.float32, dev)
     _need(B, "B", (Bsz, L, G, N), io, dev)
@@ -255,6 +261,8 @@ def ssd_scan_chunked_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size
     _need(x, "x", (Bsz, L, H, P), io, dev)
     if y is None:
         y = torch.empty_like(x)
+    if final_state is None:
+        final_state = torch.empty((Bsz, H, P, N), dtype=torch.float32, device=dev)
     _need(y, "y", (Bsz, L, H, P), io, dev)
     _need(final_state, "final_state", (Bsz, H, P, N), torch.float32, dev)
     d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else 0)
@@ -262,6 +270,16 @@ def ssd_scan_chunked_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size
                                            _ptr(init_state), int(chunk_size), _ptr(y), _ptr(final_state),
                                            _stream(stream, dev)))
     return y, final_state
+
+
+def ssd_scan_chunked_noalloc_status(stream=None):
+    """Status code of the latest ssd_scan_chunked_noalloc call on the current
+    device (waits for `stream`): SSD_OK or SSD_ERR_TIMEOUT. Also returns the
+    built-in scratch's device address, as (status, address)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    addr = ctypes.c_void_p()
+    rc = load().ssd_scan_chunked_noalloc_status(_stream(stream, dev), ctypes.byref(addr))
+    return int(rc), addr.value
 
 
 def ssd_decode_step(state, x, dt, A, B, C, D=None, y=None, stream=None):

@@ -1106,10 +1106,7 @@ constexpr size_t kScanSmem = 81920 + 5120 + 1024;
 
 size_t scanp_smem(int) { return 65536 + 4 * 16384 + 65536 + 16384 + 2 * (4 * kHBMax * 128 + kHBMax) * 4 + 16 + 512 + 1024; }
 
-int num_sms() {
-    static std::atomic<int> cache[64];
-    return device_attr(cudaDevAttrMultiProcessorCount, cache, 1);
-}
+int num_sms() { return sm_count(1); }
 
 cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream_t stream, bool pdl,
                       const TcParams &p, int threads = 128) {
@@ -1129,6 +1126,11 @@ cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream
 }
 
 }  // namespace
+
+int sm_count(int fallback) {
+    static std::atomic<int> cache[64];
+    return device_attr(cudaDevAttrMultiProcessorCount, cache, fallback);
+}
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream) {
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), stream);

@@ -101,7 +101,7 @@ cudaError_t launch_t(int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, floa
     const int64_t grid = B * H;
     if (grid == 0) return cudaSuccess;
     const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(state) & 15) == 0);
-    const bool wide = grid >= 8 * 152;  // many (b, h) per SM: four warps each
+    const bool wide = grid >= 8 * sm_count(1);  // many (b, h) per SM: four warps each
     auto go = [&](auto kern, int threads) {
         return launch_programmatic(kern, dim3((unsigned)grid), dim3(threads), 0, stream, state, (const T *)x,
                                    (const T *)dt, A, (const T *)Bm, (const T *)Cm, D, (T *)y, (int)H, (int)P,

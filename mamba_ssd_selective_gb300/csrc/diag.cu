@@ -457,21 +457,23 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 }  // namespace
 
 // Time segments: one pass per sequence keeps ~B * dim / 32 CTAs busy; when
-// that leaves the GPU mostly idle (fewer than kSegEnable threads) the sequence
-// is cut into segments of at least 64 tokens (a multiple of 32), as many as
-// bring the threads of all segments to about kSegTarget: measured on GB300,
-// more and shorter segments kept paying down to 64 tokens (B1 L4096 D1024:
-// 81 -> 75 us from 32 to 64 segments; B2 L8192 D1536: 406 -> 312 us) even
-// though every segment's first tile load is exposed. The split depends on the
-// shape only, never on chunk_size.
-constexpr int64_t kSegEnable = 152 * 256;
-constexpr int64_t kSegTarget = 152 * 4096;
+// that leaves the GPU mostly idle (fewer than kSegEnablePerSM threads per SM)
+// the sequence is cut into segments of at least 64 tokens (a multiple of 32),
+// as many as bring the threads of all segments to about kSegTargetPerSM per
+// SM: measured on GB300, more and shorter segments kept paying down to 64
+// tokens (B1 L4096 D1024: 81 -> 75 us from 32 to 64 segments; B2 L8192
+// D1536: 406 -> 312 us) even though every segment's first tile load is
+// exposed. The split depends on the shape and the device's SM count (152 on
+// GB300, also assumed where no device can be queried), never on chunk_size.
+constexpr int64_t kSegEnablePerSM = 256;
+constexpr int64_t kSegTargetPerSM = 4096;
 
 int diag_segments(int64_t B, int64_t L, int64_t Dm, int64_t N, int io) {
     if (io != IO_BF16 || Dm % 8 != 0 || N % 8 != 0 || N > 32 || B < 1 || L < 128) return 1;
+    const int64_t sms = sm_count(152);
     const int64_t thr = B * ((Dm + kCh - 1) / kCh) * (N <= 8 ? kCh1 : 2 * kCh);
-    if (thr >= kSegEnable) return 1;
-    int64_t want = (kSegTarget + thr - 1) / thr;
+    if (thr >= kSegEnablePerSM * sms) return 1;
+    int64_t want = (kSegTargetPerSM * sms + thr - 1) / thr;
     want = imin<int64_t>(want, L / 64);
     if (want <= 1) return 1;
     const int64_t seg_len = ((L + want - 1) / want + 31) / 32 * 32;

@@ -29,6 +29,11 @@ class DeviceOnce {
     std::atomic<unsigned long long> bits_{0};
 };
 
+// Streaming multiprocessors of the current device, queried once per device
+// ordinal (below 64). Returns `fallback` when no device can be queried (host
+// code on a machine without a GPU, e.g. a workspace-size query).
+int sm_count(int fallback = 1);
+
 enum IoType { IO_F32 = 0, IO_BF16 = 1 };
 
 // Sizes and pointers of one chunked SSD prefill call (layouts as in ssd_scan.h).

@@ -2,11 +2,10 @@
 // allocate device memory.
 //
 // Some callers of this library are not allowed to call cudaMalloc at the
-// point where they run the scan: code executing while another component
-// captures the stream into a CUDA graph (allocation is refused during
-// capture), plug-ins whose host framework owns all device memory and forbids
-// allocation inside its enqueue call, and latency-critical loops that cannot
-// afford the implicit device-wide synchronisation of an allocation. Such
+// point where they run the scan: plug-ins whose host framework owns all
+// device memory and forbids allocation inside its enqueue call, and
+// latency-critical loops that cannot afford the implicit device-wide
+// synchronisation of an allocation and its release. Such
 // callers still own their inputs and outputs; what they cannot provide is the
 // per-chunk state workspace. This entry point takes it from a fixed scratch
 // array compiled into the library instead.
@@ -81,4 +80,14 @@ extern "C" ssd_status ssd_scan_chunked_noalloc(const ssd_dims *dims, const void 
     if (s != SSD_OK) return s;
     return ssd_scan_chunked(dims, x, dt, A, B, C, D, init_state, chunk_size, y, final_state, scratch,
                             kScratchBytes, stream);
+}
+
+// The scratch begins with the status word of the workspace layout, so its
+// status is read exactly as a caller workspace's is.
+extern "C" ssd_status ssd_scan_chunked_noalloc_status(cudaStream_t stream, void **scratch_addr) {
+    void *scratch = nullptr;
+    ssd_status s = scratch_address(&scratch);
+    if (s != SSD_OK) return s;
+    if (scratch_addr) *scratch_addr = scratch;
+    return ssd_workspace_status(scratch, stream);
 }

@@ -217,8 +217,8 @@ def _decode_inputs(step, Bz, H, P, N, G, io):
                                    (16, 80, 64, 128, 2), (20, 64, 48, 128, 4)])
 def test_decode_steps_every_element(ssd, io, shape):
     """Ten in-place steps, every y and state element. The last two shapes have
-    at least eight (b, h) per SM, where the state rows are split evenly over
-    a persistent grid (P = 48: warp ranges start inside a (b, h))."""
+    at least eight (b, h) per SM, where the launch takes four-warp CTAs, one
+    per (b, h), eight resident per SM (P = 48: 12 rows per warp)."""
     Bz, H, P, N, G = shape
     t = IO_TORCH[io]
     st_ref = inputs.decode_state(Bz, H, P, N, seed=0)
