@@ -66,7 +66,10 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
 /* Option bits for ssd_dims.flags. */
-#define SSD_FLAG_SIMT 1 /* bf16 prefill: use the CUDA-core kernels instead of the tensor-core ones */
+#define SSD_FLAG_SIMT 1   /* bf16 prefill: use the CUDA-core kernels instead of the tensor-core ones */
+#define SSD_FLAG_FUSED 2  /* bf16 prefill: the single-pass tensor-core kernel (chunk 128 only; else
+                             SSD_ERR_UNSUPPORTED) whatever the shape */
+#define SSD_FLAG_STAGED 4 /* bf16 prefill: the three-kernel tensor-core path whatever the shape */
 
 typedef struct {
     int64_t batch;    /* B >= 0                                   */

@@ -20,6 +20,9 @@ from . import build as _build
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = 0, 1, 2, 3, 4
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_SIMT = 1
+SSD_FLAG_FUSED = 2
+SSD_FLAG_STAGED = 4
+_PATH_FLAGS = {None: 0, "auto": 0, "simt": SSD_FLAG_SIMT, "fused": SSD_FLAG_FUSED, "staged": SSD_FLAG_STAGED}
 
 _STATUS_NAMES = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
                  4: "SSD_ERR_TIMEOUT"}
@@ -156,10 +159,13 @@ def ssd_best_chunk(batch, seqlen, nheads, headdim, dstate, ngroups, io_dtype) ->
 
 
 def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=None, y=None, final_state=None,
-                     workspace=None, stream=None, simt=False, want_final_state=True):
+                     workspace=None, stream=None, simt=False, want_final_state=True, path=None):
     """Chunked SSD prefill. x[B,L,H,P], dt[B,L,H], B/C[B,L,G,N] (float32 or
     bfloat16), A[H], D[H], init_state[B,H,P,N] (float32). chunk_size None takes
-    the library's static policy (ssd_best_chunk). Returns (y, final_state)."""
+    the library's static policy (ssd_best_chunk). `path` forces a kernel path
+    for bf16 inputs: "fused" (single pass, chunk 128), "staged" (three
+    tensor-core kernels), "simt" (CUDA cores); None lets the library choose.
+    Returns (y, final_state)."""
     if x.dim() != 4 or B.dim() != 4:
         raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
     Bsz, L, H, P = x.shape
@@ -178,7 +184,9 @@ def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=None, y
     if final_state is None and want_final_state:
         final_state = torch.empty((Bsz, H, P, N), dtype=torch.float32, device=dev)
     _need(final_state, "final_state", (Bsz, H, P, N), torch.float32, dev)
-    d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else 0)
+    if path not in _PATH_FLAGS:
+        raise ValueError(f"path must be one of {sorted(k for k in _PATH_FLAGS if k)} or None, got {path!r}")
+    d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else _PATH_FLAGS[path])
     lib = load()
     if chunk_size is None:
         chunk_size = int(lib.ssd_best_chunk(ctypes.byref(d))) or 128

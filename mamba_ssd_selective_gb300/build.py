@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libssdscan.so")
 
-SOURCES = ["ssd_api.cu", "decode.cu", "chunked_simt.cu", "chunked_tc.cu", "diag.cu", "noalloc.cu", "chunk_policy.cu", "decode_layer.cu", "chunked_bwd.cu"]
+SOURCES = ["ssd_api.cu", "decode.cu", "chunked_simt.cu", "chunked_tc.cu", "chunked_fused.cu", "diag.cu", "noalloc.cu", "chunk_policy.cu", "decode_layer.cu", "chunked_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "ssd_scan.h"
+#include "tc_host.h"
 #include "tc_ptx.cuh"
 
 namespace ssd {
@@ -1126,6 +1127,12 @@ cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream
 }
 
 }  // namespace
+
+bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows) {
+    return map_tokens(out, base, inner, L, B, box_rows);
+}
+
+int device_cc_major_cached() { return device_cc_major(); }
 
 int sm_count(int fallback) {
     static std::atomic<int> cache[64];

@@ -78,6 +78,14 @@ cudaError_t launch_chunked_simt(const ChunkedArgs &a, cudaStream_t stream);
 bool chunked_tc_supported(const ChunkedArgs &a);
 cudaError_t launch_chunked_tc(const ChunkedArgs &a, cudaStream_t stream);
 
+// Single-pass tensor-core path (chunk 128, bf16, P = 64, N = 128, an even
+// number of heads per B/C group): one persistent kernel (plus a kernel that
+// clears its chain flags) carrying the state across chunks in float32.
+bool chunked_fused_supported(const ChunkedArgs &a);
+cudaError_t launch_chunked_fused(const ChunkedArgs &a, cudaStream_t stream);
+// Whether the automatic path choice takes the single-pass kernel for this shape.
+bool chunked_fused_preferred(const ChunkedArgs &a);
+
 // State passing across chunks (shared by both paths).
 // bf16_in: the chunk states are bfloat16 in states_bf16 (tensor-core path) and
 // the entering states replace them in place; otherwise they are float32 in

@@ -48,7 +48,10 @@ ssd_status check_dims(const ssd_dims *d, bool need_seqlen) {
                     (long long)d->nheads, (long long)d->ngroups);
     if (d->io_dtype != SSD_F32 && d->io_dtype != SSD_BF16)
         return fail(SSD_ERR_INVALID_ARG, "io_dtype must be SSD_F32 or SSD_BF16 (got %d)", d->io_dtype);
-    if (d->flags & ~SSD_FLAG_SIMT) return fail(SSD_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
+    if (d->flags & ~(SSD_FLAG_SIMT | SSD_FLAG_FUSED | SSD_FLAG_STAGED))
+        return fail(SSD_ERR_INVALID_ARG, "unknown flags 0x%x", d->flags);
+    if ((d->flags & SSD_FLAG_FUSED) && (d->flags & (SSD_FLAG_STAGED | SSD_FLAG_SIMT)))
+        return fail(SSD_ERR_INVALID_ARG, "SSD_FLAG_FUSED excludes SSD_FLAG_STAGED and SSD_FLAG_SIMT");
     if (d->nheads > 65535 || d->batch > 65535)
         return fail(SSD_ERR_UNSUPPORTED, "nheads and batch must be <= 65535");
     return SSD_OK;
@@ -148,6 +151,22 @@ ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt,
     // clears it (thread 0 of its first CTA) before any wait of this call can
     // give up, which takes seconds
     cudaError_t e;
+    if (dims->flags & SSD_FLAG_FUSED) {
+        if (!has_tokens) return ok();  // nothing to compute; validated above
+        if (!ssd::chunked_fused_supported(a))
+            return fail(SSD_ERR_UNSUPPORTED,
+                        "SSD_FLAG_FUSED needs bf16, headdim 64, dstate 128, chunk 128 and an even number of heads "
+                        "per group on an sm_100-family GPU");
+        e = ssd::launch_chunked_fused(a, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked (single-pass path)");
+        return ok();
+    }
+    if (a.io == ssd::IO_BF16 && !(dims->flags & (SSD_FLAG_SIMT | SSD_FLAG_STAGED)) && has_tokens &&
+        ssd::chunked_fused_supported(a) && ssd::chunked_fused_preferred(a)) {
+        e = ssd::launch_chunked_fused(a, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked (single-pass path)");
+        return ok();
+    }
     if (a.io == ssd::IO_BF16 && !(dims->flags & SSD_FLAG_SIMT) && has_tokens && ssd::chunked_tc_supported(a)) {
         e = ssd::launch_chunked_tc(a, stream);
         if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked (tensor-core path)");

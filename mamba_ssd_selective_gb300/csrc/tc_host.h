@@ -1,0 +1,17 @@
+// Host-side helpers shared by the tensor-core translation units: cached TMA
+// tensor maps of token-major bf16 tensors and the device's compute capability.
+// Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+namespace ssd {
+
+// (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (64, box_rows, 1),
+// 128-byte swizzle; encoded once per (pointer, shape) and cached.
+bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows);
+
+// Major compute capability of the current device (cached per device), -1 if unknown.
+int device_cc_major_cached();
+
+}  // namespace ssd

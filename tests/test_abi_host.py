@@ -101,6 +101,9 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert _scan(lib, _dims(binding, nheads=6, ngroups=4)) == E
     assert _scan(lib, _dims(binding, io_dtype=7)) == E
     assert _scan(lib, _dims(binding, flags=8)) == E
+    assert _scan(lib, _dims(binding, flags=binding.SSD_FLAG_FUSED | binding.SSD_FLAG_SIMT)) == E
+    assert _scan(lib, _dims(binding, flags=binding.SSD_FLAG_FUSED | binding.SSD_FLAG_STAGED)) == E
+    assert b"SSD_FLAG_FUSED" in lib.ssd_last_error()
     assert _scan(lib, _dims(binding, headdim=0)) == E
     assert _scan(lib, _dims(binding, seqlen=-1)) == E
     assert _scan(lib, _dims(binding, nheads=70000)) == binding.SSD_ERR_UNSUPPORTED

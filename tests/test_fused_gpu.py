@@ -1,0 +1,127 @@
+"""Parity of the single-pass tensor-core prefill (one persistent kernel
+carrying the state across chunks in float32) with the float64 oracle and
+with the three-kernel path.
+
+Every element of y and the final state is compared where the oracle finishes
+in seconds; the full-size 2.7B-shaped workloads compare sampled heads. The
+bf16 bound is max|gpu - ref| <= 2e-2 max|ref| (tests/helpers.py); the
+measured ratio is printed (pytest -s) so the margin to that bound is on
+record.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mamba_ssd_selective_gb300 import inputs
+from tests.helpers import BF16_REL_MAX, check, dev, head_slice, host
+
+pytestmark = pytest.mark.gpu
+bf = torch.bfloat16
+
+
+def run(ssd, d, path, init=True, D=True, want_final=True, chunk=128, workspace=None):
+    y, h = ssd.ssd_scan_chunked(dev(d["x"], bf), dev(d["dt"], bf), dev(d["A"]), dev(d["B"], bf), dev(d["C"], bf),
+                                dev(d["D"]) if D else None, dev(d["init_state"]) if init and d["init_state"] is not None
+                                else None, chunk_size=chunk, path=path, want_final_state=want_final,
+                                workspace=workspace)
+    torch.cuda.synchronize()
+    return y, h
+
+
+def rel(gpu, ref):
+    g = host(gpu) if isinstance(gpu, torch.Tensor) else gpu
+    return float(np.max(np.abs(g - ref)) / max(float(np.max(np.abs(ref))), 1e-30))
+
+
+@pytest.mark.parametrize("init", [True, False])
+@pytest.mark.parametrize("shape", [(1, 128, 2, 64, 128, 1), (2, 1000, 4, 64, 128, 1), (3, 777, 8, 64, 128, 2),
+                                   (1, 2048, 6, 64, 128, 3), (4, 300, 12, 64, 128, 1), (1, 64, 2, 64, 128, 1)])
+def test_fused_every_element(ssd, shape, init):
+    """Forced single pass on ragged lengths, several B/C groups, one to 16
+    chunks, with and without an initial state: every element of y and the
+    final state."""
+    Bz, L, H, P, N, G = shape
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=21, init_state=init)
+    yr, hr = oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"] if init else None)
+    y, h = run(ssd, d, "fused", init=init)
+    check("bf16", y, yr, f"y {shape}")
+    check("bf16", h, hr, f"final_state {shape}")
+    print(f"fused {shape} init={init}: y {rel(y, yr):.2e}, final_state {rel(h, hr):.2e} (bound {BF16_REL_MAX})")
+
+
+def test_fused_without_D_and_final_state(ssd):
+    """D = NULL adds nothing on the diagonal; with final_state = NULL the carry
+    lives in the workspace and y is unchanged."""
+    d = inputs.ssd_inputs(2, 640, 4, 64, 128, 1, io_dtype="bf16", seed=5, init_state=True)
+    yr, _ = oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], None, d["init_state"])
+    y, h = run(ssd, d, "fused", D=False, want_final=False)
+    assert h is None
+    check("bf16", y, yr, "y without D and final state")
+
+
+def test_fused_matches_three_kernel_path(ssd):
+    """Both tensor-core paths on the same inputs agree within the bf16 bound."""
+    d = inputs.ssd_inputs(2, 1536, 8, 64, 128, 2, io_dtype="bf16", seed=4, init_state=True)
+    yf, hf = run(ssd, d, "fused")
+    ys, hs = run(ssd, d, "staged")
+    check("bf16", host(yf), host(ys), "y fused vs staged")
+    check("bf16", host(hf), host(hs), "final_state fused vs staged")
+
+
+def test_fused_repeated_calls_bitwise_and_no_timeouts(ssd):
+    """Back-to-back single-pass calls with one workspace: the chain flags are
+    cleared by every call, no bounded wait expires, and every call gives the
+    same bits (no atomics, fixed association)."""
+    d = inputs.ssd_inputs(4, 2048, 16, 64, 128, 1, io_dtype="bf16", seed=6)
+    x, dt, Bm, Cm = dev(d["x"], bf), dev(d["dt"], bf), dev(d["B"], bf), dev(d["C"], bf)
+    A, Dv = dev(d["A"]), dev(d["D"])
+    ws = torch.empty(ssd.ssd_workspace_size(4, 2048, 16, 64, 128, 1, bf, 128), dtype=torch.uint8, device="cuda")
+    y0, h0 = ssd.ssd_scan_chunked(x, dt, A, Bm, Cm, Dv, None, chunk_size=128, workspace=ws, path="fused")
+    y0, h0 = y0.clone(), h0.clone()
+    y, h = torch.empty_like(y0), torch.empty_like(h0)
+    for _ in range(100):
+        ssd.ssd_scan_chunked(x, dt, A, Bm, Cm, Dv, None, chunk_size=128, y=y, final_state=h, workspace=ws,
+                             path="fused")
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
+    assert torch.equal(y, y0) and torch.equal(h, h0)
+    yr, hr = oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"])
+    check("bf16", y, yr, "y after 100 calls")
+    check("bf16", h, hr, "final_state after 100 calls")
+
+
+def test_fused_clears_a_stale_timeout_status(ssd):
+    d = inputs.ssd_inputs(1, 256, 4, 64, 128, 1, io_dtype="bf16", seed=2)
+    ws = torch.empty(max(256, ssd.ssd_workspace_size(1, 256, 4, 64, 128, 1, bf, 128)), dtype=torch.uint8,
+                     device="cuda")
+    ssd.ssd_selftest_bounded_wait(ws, 1000)
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_ERR_TIMEOUT
+    run(ssd, d, "fused", workspace=ws)
+    assert ssd.ssd_workspace_status(ws) == ssd.SSD_OK
+
+
+def test_fused_rejects_other_chunk_sizes(ssd):
+    d = inputs.ssd_inputs(1, 256, 4, 64, 128, 1, io_dtype="bf16", seed=2)
+    with pytest.raises(ssd.SsdError) as e:
+        run(ssd, d, "fused", chunk=64)
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["ssd_m2_2p7b_B8_L2048", "ssd_m2_2p7b_L8192", "ssd_m2_130m_L4096"])
+def test_fused_full_size_workloads(ssd, name):
+    """The 2.7B-shaped B8 L2048 layer (where the library picks the single pass
+    by itself), the longest chain (B1 L8192, 64 chunks) and the 130M-shaped
+    layer, forced single pass at chunk 128: sampled heads (all batches and
+    tokens) of y and the final state against the oracle."""
+    w = inputs.WORKLOADS[name]
+    Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=0)
+    y, h = run(ssd, d, "fused", init=False)
+    yh, hh = host(y), host(h)
+    for hd in (0, H // 2 + 1, H - 1):
+        s = head_slice(d, hd)
+        yr, hr = oracle.ssd_seq(s["x"], s["dt"], s["A"], s["B"], s["C"], s["D"])
+        check("bf16", yh[:, :, hd:hd + 1], yr, f"{name} y head {hd}")
+        check("bf16", hh[:, hd:hd + 1], hr, f"{name} final_state head {hd}")
+        print(f"{name} head {hd}: y {rel(yh[:, :, hd:hd + 1], yr):.2e}, final_state {rel(hh[:, hd:hd + 1], hr):.2e}")
