@@ -1,23 +1,28 @@
 #!/usr/bin/env python
 """Throughput benchmark of the SSD selective scan on one GB300 (or N replicas).
 
-One step = one chunked SSD prefill (chunk state -> state passing -> chunk scan,
-with the in-chunk cumulative sums fused into both chunk kernels) of the
-Mamba-2-130M-shaped layer workload: batch 1, L 4096, 24 heads, headdim 64,
-d_state 128, 1 group, bf16 x/dt/B/C/y with float32 state and accumulation,
-seeded synthetic inputs. The timed region replays a CUDA graph of exactly K
-steps; the steps rotate over copies of the inputs whose total size exceeds
-the L2 cache, so every step reads its inputs from HBM.
+One step = one chunked SSD prefill of the Mamba-2-2.7B-shaped layer workload
+(batch 8, L 2048, 80 heads, headdim 64, d_state 128, 1 group, bf16
+x/dt/B/C/y with float32 state and accumulation, seeded synthetic inputs), at
+the best static chunk of a 64/128/256 sweep. The timed region replays a CUDA
+graph of exactly K steps; the steps rotate over copies of the inputs whose
+total size exceeds the L2 cache, so every step reads its inputs from HBM.
 
-The same JSON line also carries, each in its own timed region: the decode
-workload (batch 64, 80 heads, 64 x 128 fp32 state, 1000 in-place steps, one
-CUDA graph), the Mamba-1 diagonal scan (batch 8, L 2048, 5120 channels,
-d_state 16, chunk sweep), the per-stage kernel times, the end-to-end number
-through the C ABI with host buffers, and the float64 CPU oracle timed on the
-host cores.
+Each of the other legs has its own timed region and is reported in the same
+final JSON line: the 130M-shaped layer and the 2.7B-shaped layer at B1
+L1024 / L4096 / L8192 (each with its chunk sweep), the decode step (batch 64,
+80 heads, 1000 in-place steps in one graph), the decode-layer body, the
+Mamba-1 diagonal scan (B8 L2048 D5120 N16, chunk sweep) and its softplus
+timing shape, and the SSD backward. Every leg reports the mean and standard
+deviation over 30 timed repetitions and a single-call latency, beside the
+float64 oracle timed on the host cores on a bounded sample of the same
+workload. A first JSON line ("details") carries the descriptions; the last
+line is the result.
 
-`--impl reference` times the float64 CPU oracle on the same workload (a
+`--impl reference` times the float64 CPU oracle on the headline workload (a
 bounded sample of tokens per step) and prints the same kind of line.
+`--chunk-table` measures the best chunk over a grid of shapes (the table the
+library's static chunk policy is built from) and prints it.
 
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU (weak
 scaling, no collective on the data path); timing is the max over ranks.
@@ -29,6 +34,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -40,13 +46,19 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HEADLINE = "ssd_m2_130m_L4096"
+HEADLINE = "ssd_m2_2p7b_B8_L2048"
+PREFILL_LEGS = ("ssd_m2_130m_L4096", "ssd_m2_2p7b_L1024", "ssd_m2_2p7b_L4096", "ssd_m2_2p7b_L8192")
 DECODE = "decode_B64_H80"
 MAMBA1 = "mamba1_B8_L2048_D5120"
 MAMBA1_SP = "mamba1_B1_L4096_D1024_softplus"
+LEGS = ("headline", "prefill", "decode", "decode_layer", "mamba1", "mamba1_softplus", "backward")
 METRIC = "SSD prefill tokens/s + % roofline; decode steps/s + state HBM GB/s"
-STAGES = ("chunk_state", "state_pass", "chunk_scan")
+# stages between the events of a staged call, per kernel path
+STAGES = {"fused": ("flag_clear", "-", "chunk_fused"), "staged": ("chunk_state", "state_pass", "chunk_scan"),
+          "simt": ("chunk_state", "state_pass", "chunk_scan")}
+KERNELS_PER_STEP = {"fused": 2, "staged": 3, "simt": 3}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+REPS = 30  # timed repetitions behind every mean and standard deviation
 
 
 # ----------------------------------------------------------------- helpers
@@ -101,6 +113,25 @@ def file_hash(*paths) -> str:
     return h.hexdigest()[:16]
 
 
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def ssd_compulsory_bytes(w: dict, io_bytes: int = 2) -> dict:
     """Algorithmic bytes of one prefill: every input read once, y and the final
     state written once (no initial state in these workloads)."""
@@ -121,6 +152,10 @@ def stage_algorithmic_bytes(w: dict, stage: str) -> int:
         return b["x"] + b["dt"] + b["B"]
     if stage == "state_pass":
         return b["final_state"]
+    if stage == "chunk_fused":
+        return b["total"]
+    if stage == "flag_clear":
+        return 0
     return b["x"] + b["dt"] + b["B"] + b["C"] + b["y"]
 
 
@@ -129,6 +164,10 @@ def ssd_flops(w: dict, Q: int) -> float:
     contractions, C.B^T once per group)."""
     Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
     return float(Bz * L * (H * (Q * P + 4 * N * P) + G * Q * N))
+
+
+def mean_std(xs):
+    return float(statistics.mean(xs)), float(statistics.stdev(xs)) if len(xs) > 1 else 0.0
 
 
 class ClockSampler:
@@ -189,24 +228,171 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# -------------------------------------------------------------- our arm
-
-def _traffic_for(kernel: str):
-    """ncu DRAM bytes per launch recorded in profiles/traffic.json, only if the
-    kernel's source is unchanged since the capture; else None."""
+def _traffic_record(key: str):
+    """ncu DRAM bytes (read + write) recorded in profiles/traffic.json under
+    `key`, only if none of its kernels' sources changed since the capture;
+    else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            rec = json.load(f).get(kernel)
+            rec = json.load(f).get(key)
     except (OSError, ValueError):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "mamba_ssd_selective_gb300", "csrc", rec["source"])
-    if not os.path.exists(src) or file_hash(src) != rec.get("source_hash"):
+    srcs = [os.path.join(ROOT, "mamba_ssd_selective_gb300", "csrc", s) for s in rec.get("sources", [])]
+    if not srcs or not all(os.path.exists(s) for s in srcs) or file_hash(*srcs) != rec.get("source_hash"):
         return None
-    return rec.get("bytes_per_launch")
+    return rec
 
+
+# --------------------------------------------------------------- prefill legs
+
+class Prefill:
+    """One prefill workload on the device: inputs rotating over copies whose
+    total exceeds 3x the L2 cache, a workspace per copy."""
+
+    def __init__(self, torch, binding, inputs, dev, name, l2):
+        self.torch, self.binding, self.dev, self.name = torch, binding, dev, name
+        w = self.w = dict(inputs.WORKLOADS[name])
+        Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+        self.shape = (Bz, L, H, P, N, G)
+        bf = torch.bfloat16
+        d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=0)
+
+        def t_(a, dtype=torch.float32):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+        self.base = {"x": t_(d["x"], bf), "dt": t_(d["dt"], bf), "B": t_(d["B"], bf), "C": t_(d["C"], bf)}
+        self.A, self.D = t_(d["A"]), t_(d["D"])
+        del d
+        self.ws_max = max(binding.ssd_workspace_size(Bz, L, H, P, N, G, bf, q) for q in (64, 128, 256))
+        in_bytes = sum(v.numel() * v.element_size() for v in self.base.values())
+        self.per_set = 2 * in_bytes + self.ws_max + Bz * H * P * N * 4
+        self.n_sets = max(2, math.ceil(3 * l2 / self.per_set))
+        self.sets = []
+        for _ in range(self.n_sets):
+            s = {k: v.clone() for k, v in self.base.items()}
+            s["y"] = torch.empty_like(self.base["x"])
+            s["final"] = torch.empty((Bz, H, P, N), dtype=torch.float32, device=dev)
+            s["ws"] = torch.empty(self.ws_max, dtype=torch.uint8, device=dev)
+            self.sets.append(s)
+
+    def step(self, i, q, stream=None):
+        s = self.sets[i % self.n_sets]
+        self.binding.ssd_scan_chunked(s["x"], s["dt"], self.A, s["B"], s["C"], self.D, None, chunk_size=q,
+                                      y=s["y"], final_state=s["final"], workspace=s["ws"], stream=stream)
+
+    def path(self, q):
+        Bz, L, H, P, N, G = self.shape
+        return self.binding.ssd_scan_path(Bz, L, H, P, N, G, self.torch.bfloat16, q)
+
+    def capture(self, nsteps, q, stage_events=None):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream(device=self.dev)
+        stream.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(stream):
+            for i in range(min(nsteps, self.n_sets)):  # eager warm-up on the capture stream
+                self.step(i, q)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for i in range(nsteps):
+                if stage_events is not None:
+                    self.binding.ssd_record_stage_events(stage_events[i])
+                self.step(i, q)
+        return g
+
+    def replay_ms(self, g, reps=1):
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1)
+
+    def sweep(self, W):
+        """ms per step at chunk 64 / 128 / 256, graph of back-to-back steps."""
+        out = {}
+        S = 4 * self.n_sets
+        for q in (64, 128, 256):
+            g = self.capture(S, q)
+            for _ in range(max(W, 3)):
+                g.replay()
+            out[q] = self.replay_ms(g, reps=3) / (3 * S)
+            del g
+        return out
+
+    def rep_stats(self, q, W):
+        """Mean and standard deviation of the per-step time over REPS replays of
+        a graph of back-to-back steps, and the single-call latency (one eager
+        call between events, REPS times)."""
+        torch = self.torch
+        S = 2 * self.n_sets
+        g = self.capture(S, q)
+        for _ in range(max(W, 3)):
+            g.replay()
+        per = [self.replay_ms(g) / S for _ in range(REPS)]
+        del g
+        one = []
+        for r in range(REPS):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(self.dev)
+            e0.record()
+            self.step(r, q)
+            e1.record()
+            torch.cuda.synchronize(self.dev)
+            one.append(e0.elapsed_time(e1))
+        m, sd = mean_std(per)
+        return {"mean_ms": m, "std_ms": sd, "reps": REPS, "single_call_ms": statistics.median(one)}
+
+    def stage_ms(self, q, nsteps):
+        """Per-stage kernel times: events between the stages of every step of a
+        graph of nsteps steps; the stages then run without programmatic overlap,
+        so each kernel is timed alone."""
+        torch = self.torch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nsteps)]
+        for row in evs:
+            for e in row:
+                e.record()
+        torch.cuda.synchronize(self.dev)
+        g = self.capture(nsteps, q, stage_events=evs)
+        g.replay()
+        torch.cuda.synchronize(self.dev)
+        names = STAGES[self.path(q)]
+        out = {nm: statistics.mean(r[i].elapsed_time(r[i + 1]) for r in evs) for i, nm in enumerate(names)
+               if nm != "-"}
+        del g
+        return out
+
+    def close(self):
+        del self.sets, self.base
+        self.torch.cuda.empty_cache()
+
+
+def prefill_leg(torch, binding, inputs, dev, name, W, hbm_peak, l2):
+    """A prefill leg: chunk sweep, best chunk, REPS-repetition statistics and
+    single-call latency at that chunk, fraction of the HBM roofline."""
+    pf = Prefill(torch, binding, inputs, dev, name, l2)
+    try:
+        sweep = pf.sweep(W)
+        q = min(sweep, key=sweep.get)
+        st = pf.rep_stats(q, W)
+        comp = ssd_compulsory_bytes(pf.w)["total"]
+        tokens = pf.w["batch"] * pf.w["seqlen"]
+        return {"w": name.replace("ssd_m2_", ""), "q": q, "path": pf.path(q), "us": round(st["mean_ms"] * 1e3, 1),
+                "std": round(st["std_ms"] * 1e3, 1), "one_us": round(st["single_call_ms"] * 1e3, 1),
+                "Mtok_s": round(tokens / st["mean_ms"] / 1e3, 1),
+                "frac": round(comp / (st["mean_ms"] / 1e3) / 1e9 / hbm_peak, 4),
+                "sweep_us": [round(sweep[k] * 1e3, 1) for k in (64, 128, 256)]}
+    finally:
+        pf.close()
+
+
+# ------------------------------------------------------------------- our arm
 
 def run_ours(args):
     import torch
@@ -221,143 +407,147 @@ def run_ours(args):
     hbm_peak = float(peaks["hbm_gbs"])
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or 129 * 2 ** 20
-    bf = torch.bfloat16
     K, W = args.steps, args.warmup
-    out = {}
+    legs = set(args.legs.split(",")) if args.legs else set(LEGS)
+    if args.skip_extra:
+        legs = {"headline"}
+    details, compact = {}, {}
+    line = None
 
     sampler = ClockSampler(local).start() if rank == 0 else None
 
-    # ---------------- prefill (headline)
-    w = dict(inputs.WORKLOADS[HEADLINE])
-    d = inputs.ssd_inputs(w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
-                          io_dtype="bf16", seed=0)
+    # ---------------- the headline: B8 L2048 H80 prefill
+    if "headline" in legs:
+        pf = Prefill(torch, binding, inputs, dev, HEADLINE, l2)
+        w = pf.w
+        Bz, L, H, P, N, G = pf.shape
+        sweep = pf.sweep(W)
+        best_q = args.chunk or min(sweep, key=sweep.get)
+        path = pf.path(best_q)
 
-    def t_(a, dtype=torch.float32):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
-
-    base = {"x": t_(d["x"], bf), "dt": t_(d["dt"], bf), "B": t_(d["B"], bf), "C": t_(d["C"], bf)}
-    A, Dv = t_(d["A"]), t_(d["D"])
-    Bz, L, H, P, N, G = w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
-    ws_max = max(binding.ssd_workspace_size(Bz, L, H, P, N, G, bf, q) for q in (64, 128, 256))
-    per_set = sum(v.numel() * v.element_size() for v in base.values()) * 2 + ws_max + Bz * H * P * N * 4
-    n_sets = max(2, math.ceil(3 * l2 / per_set))
-    sets = []
-    for _ in range(n_sets):
-        s = {k: v.clone() for k, v in base.items()}
-        s["y"] = torch.empty_like(base["x"])
-        s["final"] = torch.empty((Bz, H, P, N), dtype=torch.float32, device=dev)
-        s["ws"] = torch.empty(ws_max, dtype=torch.uint8, device=dev)
-        sets.append(s)
-
-    def step(s, q):
-        binding.ssd_scan_chunked(s["x"], s["dt"], A, s["B"], s["C"], Dv, None, chunk_size=q, y=s["y"],
-                                 final_state=s["final"], workspace=s["ws"])
-
-    def capture(nsteps, q, stage_events=None):
-        g = torch.cuda.CUDAGraph()
-        stream = torch.cuda.Stream(device=dev)
-        stream.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(stream):
-            for i in range(min(nsteps, n_sets)):  # eager warm-up on the capture stream
-                step(sets[i % n_sets], q)
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            for i in range(nsteps):
-                if stage_events is not None:
-                    binding.ssd_record_stage_events(stage_events[i])
-                step(sets[i % n_sets], q)
-        return g
-
-    def time_graph(g, reps=1):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record()
-        for _ in range(reps):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1)
-
-    # chunk sweep: the best static chunk per workload is the one reported
-    sweep = {}
-    S = 8 * n_sets
-    for q in (64, 128, 256):
-        g = capture(S, q)
-        for _ in range(max(W, 3)):
-            g.replay()
-        ms = time_graph(g, reps=5) / (5 * S)
-        sweep[q] = ms
-        del g
-    best_q = args.chunk or min(sweep, key=sweep.get)
-
-    # the timed region: exactly K steps in one graph
-    g = capture(K, best_q)
-    gw = capture(max(W, 3), best_q)
-    for _ in range(2):
-        gw.replay()
-    # keep the GPU busy ~1 s before the timed region so that the clock samples
-    # describe the clocks under this load
-    if rank == 0:
-        t_end = time.time() + 1.0
-        while time.time() < t_end:
+        # the timed region: exactly K steps in one graph
+        g = pf.capture(K, best_q)
+        gw = pf.capture(max(W, 3), best_q)
+        for _ in range(2):
             gw.replay()
-            torch.cuda.synchronize(dev)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.nvtx.range_push("timed_region")
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    ms_total = reduce_max(e0.elapsed_time(e1), world, device=dev)
-    ms_step = ms_total / K
-    tokens = Bz * L
-    value = world * tokens * K / (ms_total / 1e3)
-    del g, gw
+        # keep the GPU busy ~1 s before the timed region so that the clock
+        # samples describe the clocks under this load
+        if rank == 0:
+            t_end = time.time() + 1.0
+            while time.time() < t_end:
+                gw.replay()
+                torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("timed_region")
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ms_total = reduce_max(e0.elapsed_time(e1), world, device=dev)
+        ms_step = ms_total / K
+        tokens = Bz * L
+        value = world * tokens * K / (ms_total / 1e3)
+        del g, gw
 
-    # per-stage kernel times, CUDA events between the stages of every step of a
-    # second K'-step graph of the same workload
-    Ks = min(K, 256)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Ks)]
-    for row in evs:
-        for e in row:
-            e.record()
-    torch.cuda.synchronize(dev)
-    gs = capture(Ks, best_q, stage_events=evs)
-    gs.replay()
-    torch.cuda.synchronize(dev)
-    stage_ms = {nm: statistics.mean(r[i].elapsed_time(r[i + 1]) for r in evs) for i, nm in enumerate(STAGES)}
-    del gs
-    dom = max(stage_ms, key=stage_ms.get)
-    dom_bytes = stage_algorithmic_bytes(w, dom)
-    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
-    comp = ssd_compulsory_bytes(w)
-    src_of = {"chunk_state": "chunked_tc.cu", "state_pass": "chunked_simt.cu", "chunk_scan": "chunked_tc.cu"}
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                "traffic": _traffic_for(dom), "algorithmic_bytes": dom_bytes,
-                "launch_ms": round(stage_ms[dom], 5), "peak_source": peaks["source"]}
-    step_gbs = comp["total"] / (ms_step / 1e3) / 1e9
-    out["prefill"] = {
-        "step_roofline": {"bound": "hbm", "compulsory_bytes": comp["total"], "achieved": round(step_gbs, 1),
-                          "peak": hbm_peak, "unit": "GB/s", "frac": round(step_gbs / hbm_peak, 4)},
-        "tflops": round(ssd_flops(w, best_q) / (ms_step / 1e3) / 1e12, 2),
-        "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
-        "chunk_sweep_ms_per_step": {str(k): round(v, 5) for k, v in sweep.items()},
-        "chunk_policy": binding.ssd_best_chunk(Bz, L, H, P, N, G, torch.bfloat16),
-    }
+        stats = pf.rep_stats(best_q, W)
+        stage_ms = pf.stage_ms(best_q, min(K, 64))
+        dom = max(stage_ms, key=stage_ms.get)
+        dom_bytes = stage_algorithmic_bytes(w, dom)
+        achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+        comp = ssd_compulsory_bytes(w)
+        traffic = _traffic_record(f"step:{HEADLINE}:{path}:{best_q}")
+        step_gbs = comp["total"] / (ms_step / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4), "launch_ms": round(stage_ms[dom], 5),
+                    "alg_bytes": dom_bytes,
+                    "traffic": traffic["read"] + traffic["write"] if traffic else None,
+                    "tr_ratio": round((traffic["read"] + traffic["write"]) / comp["total"], 3) if traffic
+                    else None,
+                    "step_frac": round(step_gbs / hbm_peak, 4), "peak_src": peaks["source"]}
+        details["headline"] = {
+            "workload": HEADLINE, "path": path, "chunk_sweep_ms_per_step": {str(k): round(v, 5) for k, v in sweep.items()},
+            "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+            "tflops": round(ssd_flops(w, best_q) / (ms_step / 1e3) / 1e12, 2),
+            "chunk_policy": binding.ssd_best_chunk(Bz, L, H, P, N, G, torch.bfloat16),
+            "l2": f"inputs rotate over {pf.n_sets} copies ({pf.n_sets * pf.per_set / 2**20:.0f} MiB > L2 "
+                  f"{l2 / 2**20:.0f} MiB)",
+            "traffic_record": traffic,
+            "roofline_note": "frac: the dominant kernel alone (stages launched without programmatic overlap, CUDA "
+                             "events between them) against its algorithmic bytes; step_frac: the whole step "
+                             "(graph of K steps) against the compulsory bytes; traffic: ncu DRAM read + write "
+                             "bytes of one step's kernels, in steady state (cache control off, the next step "
+                             "evicts the previous one's written lines)",
+        }
+        e2e = e2e_headline(torch, binding, pf, best_q, K, W, world, tokens)
+        pf.close()
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": HEADLINE, "batch": Bz, "seqlen": L, "nheads": H, "headdim": P, "dstate": N,
+                       "ngroups": G, "chunk": best_q, "path": path, "l2": "inputs > L2",
+                       "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
+            "timing": {"mean_ms": round(stats["mean_ms"], 5), "std_ms": round(stats["std_ms"], 5), "reps": REPS,
+                       "single_call_ms": round(stats["single_call_ms"], 5)},
+            "roofline": roofline,
+            "gpu_launches": KERNELS_PER_STEP[path] * K,
+            "e2e": {k: v for k, v in e2e.items() if k not in ("pipeline", "steps")},
+        }
+        details["e2e"] = e2e
 
-    # ---------------- end to end through the C ABI with host buffers
-    # Every step copies its inputs from pinned host memory and its results
-    # (y and the final state) back, as a serving loop would: the inputs of a
-    # step are one packed host buffer (one copy in), its outputs one packed
-    # device buffer (one copy out), and three streams overlap the copy in of
-    # step i + 1, the scan of step i and the copy out of step i - 1 over two
-    # device buffer sets.
-    in_parts = [("x", base["x"]), ("dt", base["dt"]), ("B", base["B"]), ("C", base["C"]), ("A", A), ("D", Dv)]
+    # ---------------- the other legs
+    if "prefill" in legs:
+        compact["prefill"] = [prefill_leg(torch, binding, inputs, dev, nm, W, hbm_peak, l2) for nm in PREFILL_LEGS]
+    if "decode" in legs:
+        compact["decode"] = bench_decode(torch, binding, inputs, dev, hbm_peak, W)
+    if "decode_layer" in legs:
+        compact["decode_layer"] = [bench_decode_layer(torch, binding, inputs, dev, hbm_peak, nm, W)
+                                   for nm in ("decode_layer_B64_H80", "decode_layer_B1_H128_G8")]
+    if "mamba1" in legs:
+        compact["mamba1"] = bench_mamba1(torch, binding, inputs, dev, hbm_peak, K, W)
+    if "mamba1_softplus" in legs:
+        compact["mamba1_softplus"] = bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W)
+    if "backward" in legs:
+        compact["backward"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W)
+
+    clocks = sampler.stop() if sampler else None
+    if rank != 0:
+        return
+    if not args.skip_cpu:
+        oracle_beside(compact, details)
+    if line is None:  # no headline leg: a line of the other legs alone
+        line = {"metric": METRIC, "value": None, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": "legs only"}}
+    line["legs"] = compact
+    if not args.skip_cpu and "headline" in legs:
+        line["cpu_baseline"] = cpu_baseline(inputs_workload(HEADLINE))
+    if clocks is not None:
+        line["clocks"] = clocks
+    print(json.dumps({"details": details}), flush=True)
+    print(json.dumps(line), flush=True)
+
+
+def inputs_workload(name):
+    from mamba_ssd_selective_gb300 import inputs
+    return dict(inputs.WORKLOADS[name])
+
+
+def e2e_headline(torch, binding, pf, q, K, W, world, tokens):
+    """The headline metric end to end through the C ABI with host buffers:
+    every step copies its inputs from pinned host memory and its results (y
+    and the final state) back. The inputs of a step are one packed host
+    buffer (one copy in), its outputs one packed device buffer (one copy
+    out); three streams overlap the copy in of step i + 1, the scan of step i
+    and the copy out of step i - 1 over two device buffer sets."""
+    dev, bf = pf.dev, torch.bfloat16
+    Bz, L, H, P, N, G = pf.shape
+    base = pf.base
+    in_parts = [("x", base["x"]), ("dt", base["dt"]), ("B", base["B"]), ("C", base["C"]), ("A", pf.A), ("D", pf.D)]
 
     def carve(buf, parts):
         views, off = {}, 0
@@ -383,7 +573,7 @@ def run_ours(args):
         din = torch.empty(hin.numel(), dtype=torch.uint8, device=dev)
         dout = torch.empty(hout.numel(), dtype=torch.uint8, device=dev)
         dsets.append({"din": din, "dout": dout, "in": carve(din, in_parts), "out": carve(dout, out_parts),
-                      "ws": torch.empty(ws_max, dtype=torch.uint8, device=dev)})
+                      "ws": torch.empty(pf.ws_max, dtype=torch.uint8, device=dev)})
     s_cap, s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(4))
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "run", "out")}
 
@@ -399,7 +589,7 @@ def run_ours(args):
             if i >= 2:
                 s_run.wait_event(ev["out"][i & 1])  # the outputs two steps back have been copied out
             v, o = d["in"], d["out"]
-            binding.ssd_scan_chunked(v["x"], v["dt"], v["A"], v["B"], v["C"], v["D"], None, chunk_size=best_q,
+            binding.ssd_scan_chunked(v["x"], v["dt"], v["A"], v["B"], v["C"], v["D"], None, chunk_size=q,
                                      y=o["y"], final_state=o["final"], workspace=d["ws"], stream=s_run)
             ev["run"][i & 1].record(s_run)
         with torch.cuda.stream(s_out):
@@ -408,7 +598,6 @@ def run_ours(args):
             ev["out"][i & 1].record(s_out)
 
     def capture_e2e(nsteps):
-        # K steps in one graph: s_cap forks to the three stage streams and joins them
         g = torch.cuda.CUDAGraph()
         s_cap.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.graph(g, stream=s_cap, capture_error_mode="relaxed"):
@@ -437,49 +626,57 @@ def run_ours(args):
         e1.record(s_cap)
     torch.cuda.synchronize(dev)
     ms_e2e = reduce_max(e0.elapsed_time(e1), world, device=dev)
-    del ge
+    del ge, dsets
     h2d = sum(t.numel() * t.element_size() for _, t in in_parts)
     d2h = sum(t.numel() * t.element_size() for _, t in out_parts)
-    e2e = {"value": world * tokens * Ke / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "steps": Ke,
-           "pipeline": "packed pinned buffers; copy in / scan / copy out overlapped on three streams; K steps in "
-                       "one CUDA graph"}
-    del sets, dsets
+    return {"value": round(world * tokens * Ke / (ms_e2e / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": Ke,
+            "pipeline": "packed pinned buffers; copy in / scan / copy out overlapped on three streams; K steps in "
+                        "one CUDA graph"}
 
-    # ---------------- decode workload
-    if not args.skip_extra:
-        out["decode"] = bench_decode(torch, binding, inputs, dev, hbm_peak, peaks["source"], W)
-        out["decode_layer"] = [bench_decode_layer(torch, binding, inputs, dev, hbm_peak, name, W)
-                               for name in ("decode_layer_B64_H80", "decode_layer_B1_H128_G8")]
-        out["mamba1"] = bench_mamba1(torch, binding, inputs, dev, hbm_peak, peaks["source"], K, W)
-        out["mamba1_softplus"] = bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W)
-        out["backward"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W)
 
-    clocks = sampler.stop() if sampler else None
+def graph_rep_stats(torch, g, steps_per_replay, reps=REPS):
+    """Mean and standard deviation (ms per step) over `reps` replays of a graph."""
+    per = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) / steps_per_replay)
+    return mean_std(per)
 
-    if rank != 0:
-        return
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded: x,B,C~N(0,1); dt=softplus(N(0,.5)+b), A=-exp(U(0,ln16)))",
-        "config": {"workload": HEADLINE, "batch": Bz, "seqlen": L, "nheads": H, "headdim": P, "dstate": N,
-                   "ngroups": G, "chunk": best_q, "io": "bf16 x/dt/B/C/y, fp32 state and accumulation",
-                   "l2": f"inputs rotate over {n_sets} copies ({n_sets * per_set / 2**20:.0f} MiB > L2 "
-                         f"{l2 / 2**20:.0f} MiB)", "graph": "K steps in one CUDA graph",
-                   "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
-        "roofline": roofline,
-        "gpu_launches": 3 * K,
-        "e2e": e2e,
-    }
-    if not args.skip_cpu and not args.skip_extra:
-        oracle_beside(out)
-    line.update(out)
-    if not args.skip_cpu:
-        line["cpu_baseline"] = cpu_baseline(w)
-    if clocks is not None:
-        line["clocks"] = clocks
-    print(json.dumps(line), flush=True)
+
+def batch_rep_stats(torch, fn, per_batch=10, reps=REPS):
+    """Mean and standard deviation (ms per call) over `reps` batches of
+    `per_batch` back-to-back calls, each batch between events."""
+    per = []
+    for r in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(per_batch):
+            fn(r * per_batch + i)
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) / per_batch)
+    return mean_std(per)
+
+
+def call_rep_stats(torch, fn, reps=REPS):
+    """Mean and standard deviation (ms) of single calls, each between events."""
+    per = []
+    for i in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1))
+    return mean_std(per)
 
 
 def bench_decode_layer(torch, binding, inputs, dev, hbm_peak, name, W):
@@ -514,26 +711,28 @@ def bench_decode_layer(torch, binding, inputs, dev, hbm_peak, name, W):
         for _ in range(max(W, 3)):
             graph.launch()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 3
-        e0.record()
-        for _ in range(reps):
+        per = []
+        for _ in range(REPS):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record()
             graph.launch()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            per.append(e0.elapsed_time(e1) * 1e3 / steps)
+        us, sd = mean_std(per)
     finally:
         graph.close()
+    one, _ = call_rep_stats(torch, lambda i: binding.decode_layer_step(xBC[i], cst, cw, cb, dts[i], A, Dv, sst, zs[i],
+                                                                       nw, norm_group=w["norm_group"]))
     nbytes = (2 * Bz * H * P * N * 4 + 2 * Bz * Cc * Wc * 4 + Bz * Cc * 2 + Cc * Wc * 4 + Cc * 4
               + Bz * H * 2 + 2 * Bz * H * P * 2 + H * P * 4 + 2 * H * 4)
     gbs = nbytes / (us / 1e6) / 1e9
-    return {"workload": name, "us_per_step": round(us, 3), "steps_per_s": round(1e6 / us, 1),
-            "kernels_per_step": 3, "gpu_launches": 3 * steps * reps, "algorithmic_bytes_per_step": nbytes,
-            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
-            "graph": f"{steps} steps captured by ssd_decode_graph_create, one launch"}
+    return {"w": name.replace("decode_layer_", "layer_"), "us": round(us, 2), "std": round(sd, 2),
+            "one_us": round(one * 1e3, 1), "steps_s": round(1e6 / us, 1), "frac": round(gbs / hbm_peak, 4)}
 
 
-def bench_decode(torch, binding, inputs, dev, hbm_peak, peak_src, W):
+def bench_decode(torch, binding, inputs, dev, hbm_peak, W):
     w = inputs.WORKLOADS[DECODE]
     Bz, H, P, N, G, steps = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["steps"]
     bf = torch.bfloat16
@@ -564,24 +763,21 @@ def bench_decode(torch, binding, inputs, dev, hbm_peak, peak_src, W):
     for _ in range(max(W, 3) // 3 + 1):
         g.replay()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / steps
+    ms, sd = graph_rep_stats(torch, g, steps)
+    del g
+    one, _ = call_rep_stats(torch, lambda i: binding.ssd_decode_step(state, xs[i], dts[i], A, Bs[i], Cs[i], Dv,
+                                                                     y=ys[i]))
     state_bytes = 2 * Bz * H * P * N * 4
     step_bytes = state_bytes + Bz * H * P * 2 * 2 + Bz * H * 2 + 2 * Bz * G * N * 2
     gbs = step_bytes / (ms / 1e3) / 1e9
-    return {"workload": DECODE, "steps": steps, "ms_per_step": round(ms, 6), "steps_per_s": round(1e3 / ms, 1),
-            "state_gbs": round(state_bytes / (ms / 1e3) / 1e9, 1), "gpu_launches": steps,
-            "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": round(gbs, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes": step_bytes,
-                         "traffic": _traffic_for("decode_step"), "frac_of_8tbs": round(gbs / 8000.0, 4),
-                         "peak_source": peak_src}}
+    tr = _traffic_record("kernel:decode_step")
+    return {"w": DECODE, "us": round(ms * 1e3, 2), "std": round(sd * 1e3, 2), "one_us": round(one * 1e3, 1),
+            "steps_s": round(1e3 / ms, 1), "state_gbs": round(state_bytes / (ms / 1e3) / 1e9, 1),
+            "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4), "frac_8tbs": round(gbs / 8000.0, 4),
+            "tr_ratio": round((tr["read"] + tr["write"]) / step_bytes, 3) if tr else None}
 
 
-def bench_mamba1(torch, binding, inputs, dev, hbm_peak, peak_src, K, W):
+def bench_mamba1(torch, binding, inputs, dev, hbm_peak, K, W):
     w = inputs.WORKLOADS[MAMBA1]
     Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
     bf = torch.bfloat16
@@ -592,32 +788,36 @@ def bench_mamba1(torch, binding, inputs, dev, hbm_peak, peak_src, K, W):
 
     x, dt, Bm, Cm = t_(d["x"], bf), t_(d["dt"], bf), t_(d["B"], bf), t_(d["C"], bf)
     A, Dv = t_(d["A"]), t_(d["D"])
+    del d
     y = torch.empty_like(x)
     hT = torch.empty((Bz, Dm, N), dtype=torch.float32, device=dev)
     reps = max(5, min(K, 50))
+
+    def run(i, chunk):
+        binding.selective_scan_diag(x, dt, A, Bm, Cm, Dv, None, chunk_size=chunk, y=y, final_state=hT)
+
     sweep = {}
     for chunk in (256, 512, 1024, 2048):
-        for _ in range(max(W, 3)):
-            binding.selective_scan_diag(x, dt, A, Bm, Cm, Dv, None, chunk_size=chunk, y=y, final_state=hT)
+        for i in range(max(W, 3)):
+            run(i, chunk)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(reps):
-            binding.selective_scan_diag(x, dt, A, Bm, Cm, Dv, None, chunk_size=chunk, y=y, final_state=hT)
+        for i in range(reps):
+            run(i, chunk)
         e1.record()
         torch.cuda.synchronize(dev)
         sweep[chunk] = e0.elapsed_time(e1) / reps
     best = min(sweep, key=sweep.get)
-    ms = sweep[best]
+    ms, sd = batch_rep_stats(torch, lambda i: run(i, best), per_batch=5)
+    one, _ = call_rep_stats(torch, lambda i: run(i, best))
     nbytes = 3 * Bz * L * Dm * 2 + 2 * Bz * L * N * 2 + Dm * N * 4 + Dm * 4 + Bz * Dm * N * 4
     gbs = nbytes / (ms / 1e3) / 1e9
-    n_exp = Bz * L * Dm * N
-    return {"workload": MAMBA1, "chunk": best, "ms": round(ms, 5), "tokens_per_s": round(Bz * L / (ms / 1e3), 1),
-            "chunk_sweep_ms": {str(k): round(v, 5) for k, v in sweep.items()},
-            "exp_per_s": round(n_exp / (ms / 1e3), 1), "gpu_launches": reps,
-            "roofline": {"bound": "hbm", "kernel": "diag_scan", "achieved": round(gbs, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "algorithmic_bytes": nbytes,
-                         "traffic": _traffic_for("diag_scan"), "peak_source": peak_src}}
+    tr = _traffic_record("kernel:diag_scan")
+    return {"w": MAMBA1, "q": best, "us": round(ms * 1e3, 1), "std": round(sd * 1e3, 1), "one_us": round(one * 1e3, 1),
+            "Mtok_s": round(Bz * L / ms / 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+            "tr_ratio": round((tr["read"] + tr["write"]) / nbytes, 3) if tr else None,
+            "sweep_us": [round(sweep[k] * 1e3, 1) for k in (256, 512, 1024, 2048)]}
 
 
 def bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W):
@@ -636,7 +836,6 @@ def bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W):
                  y=torch.empty((Bz, L, Dm), dtype=bf, device=dev)) for _ in range(n_sets)]
     A, Dv = t_(d["A"]), t_(d["D"])
     hT = torch.empty((Bz, Dm, N), dtype=torch.float32, device=dev)
-    reps = max(8, min(K, 200))
     ws_bytes = binding.selective_scan_diag_workspace_size(Bz, L, Dm, N, bf)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     launches = 3 if ws_bytes else 1   # segment-local scan, segment pass, output scan
@@ -646,28 +845,15 @@ def bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W):
         binding.selective_scan_diag(s_["x"], s_["dt"], A, s_["B"], s_["C"], Dv, None, chunk_size=chunk, y=s_["y"],
                                     final_state=hT, delta_softplus=True, workspace=ws)
 
-    sweep = {}
-    for chunk in (256, 2048):
-        for i in range(max(W, 3)):
-            run(i, chunk)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(reps):
-            run(i, chunk)
-        e1.record()
-        torch.cuda.synchronize(dev)
-        sweep[chunk] = e0.elapsed_time(e1) / reps
-    best = min(sweep, key=sweep.get)
-    ms = sweep[best]
+    for i in range(max(W, 3)):
+        run(i, 2048)
+    torch.cuda.synchronize(dev)
+    ms, sd = batch_rep_stats(torch, lambda i: run(i, 2048))
+    one, _ = call_rep_stats(torch, lambda i: run(i, 2048))
     nbytes = 3 * Bz * L * Dm * 2 + 2 * Bz * L * N * 2 + Dm * N * 4 + Dm * 4 + Bz * Dm * N * 4
     gbs = nbytes / (ms / 1e3) / 1e9
-    return {"workload": MAMBA1_SP, "chunk": best, "ms": round(ms, 5),
-            "tokens_per_s": round(Bz * L / (ms / 1e3), 1),
-            "chunk_sweep_ms": {str(k): round(v, 5) for k, v in sweep.items()}, "gpu_launches": reps * launches,
-            "time_segments": ws_bytes > 0,
-            "l2": f"inputs rotate over {n_sets} copies", "hbm_frac": round(gbs / hbm_peak, 4),
-            "pages_time_ms": {"value": 0.3204, "hardware": "RTX 3070, fp16, selective_scan_fn, delta_softplus"}}
+    return {"w": MAMBA1_SP, "q": 2048, "us": round(ms * 1e3, 1), "std": round(sd * 1e3, 1), "one_us": round(one * 1e3, 1),
+            "Mtok_s": round(Bz * L / ms / 1e3, 2), "frac": round(gbs / hbm_peak, 4), "kernels": launches}
 
 
 def bench_backward(torch, binding, inputs, dev, hbm_peak, W):
@@ -698,30 +884,21 @@ def bench_backward(torch, binding, inputs, dev, hbm_peak, W):
     for i in range(max(W, 3)):
         run(i)
     torch.cuda.synchronize(dev)
-    reps = 20
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(reps):
-        run(i)
-    e1.record()
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / reps
+    ms, sd = batch_rep_stats(torch, run, per_batch=5)
     # compulsory bytes: x, dt, B, C, dy read (bf16); dx, ddt, dB, dC written (float32)
     nbytes = Bz * L * (2 * H * P + H + 2 * G * N) * 2 + Bz * L * (H * P + H + 2 * G * N) * 4
-    return {"workload": "ssd_bwd_m2_130m_L2048", "ms": round(ms, 4), "tokens_per_s": round(Bz * L / (ms / 1e3), 1),
-            "kernels_per_call": 6, "gpu_launches": 6 * reps, "hbm_frac": round(nbytes / (ms / 1e3) / 1e9 / hbm_peak, 4),
-            "arith": "float32 CUDA cores, chunks of 64", "l2": f"inputs rotate over {n_sets} copies",
-            "pages_context": "Table 13 (L40S): whole-model forward + backward, not comparable"}
+    return {"w": "bwd_130m_L2048", "us": round(ms * 1e3, 1), "std": round(sd * 1e3, 1),
+            "Mtok_s": round(Bz * L / ms / 1e3, 2), "frac": round(nbytes / (ms / 1e3) / 1e9 / hbm_peak, 4)}
 
 
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample_tokens(w: dict, seconds: float, threads: int) -> int:
-    """Tokens of the workload (from the start of the sequence, all heads) the
-    oracle processes in about `seconds`, measured on a short probe run."""
+    """Tokens of the workload (from the start of the sequence, all batches and
+    heads) the oracle processes in about `seconds`, measured on a short probe."""
     import oracle
     from mamba_ssd_selective_gb300 import inputs
-    probe = min(256, w["seqlen"])
+    probe = min(64, w["seqlen"])
     d = inputs.ssd_inputs(w["batch"], probe, w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
                           io_dtype="bf16", seed=0)
     t0 = time.perf_counter()
@@ -735,7 +912,7 @@ def cpu_baseline(w: dict, seconds: float = 10.0) -> dict:
     import oracle
     from mamba_ssd_selective_gb300 import inputs
     threads = oracle.default_threads()
-    Ls = oracle_sample_tokens(w, seconds, threads)
+    Ls = oracle_sample_tokens(w, seconds / 2, threads)
     d = inputs.ssd_inputs(w["batch"], Ls, w["nheads"], w["headdim"], w["dstate"], w["ngroups"], io_dtype="bf16",
                           seed=0)
     # repeat the sample until about `seconds` of host time have been spent
@@ -748,8 +925,9 @@ def cpu_baseline(w: dict, seconds: float = 10.0) -> dict:
         if el >= seconds or reps >= 10000:
             break
     return {"value": round(w["batch"] * Ls * reps / el, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {Ls} of {w['seqlen']} tokens, all {w['nheads']} heads, float64 token-by-token "
-                      f"recurrence, {reps} repetition(s) in {el:.2f} s"}
+            "cpu": host_cpu(),
+            "sample": f"first {Ls} of {w['seqlen']} tokens of all {w['batch']} sequences and {w['nheads']} heads, "
+                      f"float64 token loop, {reps} rep(s) in {el:.1f} s"}
 
 
 def _timed(fn, seconds):
@@ -763,17 +941,25 @@ def _timed(fn, seconds):
             return el / reps, reps
 
 
-def oracle_beside(out: dict, seconds: float = 2.0) -> None:
+def oracle_beside(compact: dict, details: dict, seconds: float = 2.0) -> None:
     """The float64 oracle, as it stands, timed on the host cores beside each
-    extra leg on a bounded sample of its workload, in the leg's own unit."""
+    leg on a bounded sample of its workload, in the leg's own unit: the value
+    goes into the leg as "cpu", the sample's description into the details."""
     import oracle
     from mamba_ssd_selective_gb300 import inputs
     thr = oracle.default_threads()
+    notes = details.setdefault("oracle_samples", {"cores": thr, "cpu": host_cpu()})
 
-    def rec(value, unit, sample):
-        return {"value": round(value, 2), "unit": unit, "cores": thr, "kind": "oracle", "sample": sample}
-
-    if "decode" in out:
+    for leg in compact.get("prefill", []):
+        w = inputs.WORKLOADS["ssd_m2_" + leg["w"]]
+        Ls = oracle_sample_tokens(w, seconds / 2, thr)
+        d = inputs.ssd_inputs(w["batch"], Ls, w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                              io_dtype="bf16", seed=0)
+        per, reps = _timed(lambda: oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=thr),
+                           seconds)
+        leg["cpu"] = round(w["batch"] * Ls / per, 1)
+        notes[leg["w"]] = f"first {Ls} tokens, all heads, {reps} rep(s)"
+    if "decode" in compact:
         w = inputs.WORKLOADS[DECODE]
         Bz, H, P, N, G = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
         st = inputs.decode_state(Bz, H, P, N, seed=0)
@@ -781,9 +967,10 @@ def oracle_beside(out: dict, seconds: float = 2.0) -> None:
         di = inputs.decode_step_inputs(0, Bz, H, P, N, G, io_dtype="bf16", seed=0)
         per, reps = _timed(lambda: oracle.ssd_decode(st, di["x"], di["dt"], prm["A"], di["B"], di["C"], prm["D"],
                                                      threads=thr), seconds)
-        out["decode"]["oracle"] = rec(1.0 / per, "steps/s", f"one full step, {reps} repetition(s)")
-    for leg in out.get("decode_layer", []):
-        w = inputs.WORKLOADS[leg["workload"]]
+        compact["decode"]["cpu"] = round(1.0 / per, 2)
+        notes[DECODE] = f"one full step, {reps} rep(s)"
+    for leg in compact.get("decode_layer", []):
+        w = inputs.WORKLOADS[leg["w"].replace("layer_", "decode_layer_")]
         Bz, H, P, N, G, Wc = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["width"]
         prm = inputs.decode_layer_params(Bz, H, P, N, G, Wc, seed=0)
         li = inputs.decode_layer_step_inputs(0, Bz, H, P, N, G, io_dtype="bf16", seed=0)
@@ -791,37 +978,35 @@ def oracle_beside(out: dict, seconds: float = 2.0) -> None:
         per, reps = _timed(lambda: oracle.decode_layer_step(cst, sst, li["xBC"], prm["conv_w"], prm["conv_b"],
                                                             li["dt"], prm["A"], prm["D"], li["z"], prm["norm_w"],
                                                             H, P, N, G, group=w["norm_group"]), seconds)
-        leg["oracle"] = rec(1.0 / per, "steps/s", f"one full layer step, {reps} repetition(s)")
-    if "mamba1" in out:
+        leg["cpu"] = round(1.0 / per, 2)
+        notes[leg["w"]] = f"one full layer step, {reps} rep(s)"
+    if "mamba1" in compact:
         w = inputs.WORKLOADS[MAMBA1]
         Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
         ch = 64  # a 64-channel sample of the workload, same distributions
         d = inputs.diag_inputs(Bz, L, ch, N, io_dtype="bf16", seed=0)
         per, reps = _timed(lambda: oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=thr),
                            seconds)
-        out["mamba1"]["oracle"] = rec(Bz * L / (per * Dm / ch), "tokens/s",
-                                      f"{ch} of {Dm} channels, all {Bz}x{L} tokens, {reps} repetition(s), "
-                                      f"scaled to all channels")
-    if "mamba1_softplus" in out:
+        compact["mamba1"]["cpu"] = round(Bz * L / (per * Dm / ch), 1)
+        notes[MAMBA1] = f"{ch} of {Dm} channels, all tokens, {reps} rep(s), scaled to all channels"
+    if "mamba1_softplus" in compact:
         w = inputs.WORKLOADS[MAMBA1_SP]
         Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
-        ch = 128  # a 128-channel sample of the workload, same distributions
+        ch = 128
         d = inputs.diag_option_inputs(Bz, L, ch, N, io_dtype="bf16", seed=0, bias=False, z=False)
         per, reps = _timed(lambda: oracle.diag_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], threads=thr,
                                                    delta_softplus=True), seconds)
-        out["mamba1_softplus"]["oracle"] = rec(Bz * L / (per * Dm / ch), "tokens/s",
-                                               f"{ch} of {Dm} channels, all tokens, {reps} repetition(s), "
-                                               f"scaled to all channels")
-    if "backward" in out:
+        compact["mamba1_softplus"]["cpu"] = round(Bz * L / (per * Dm / ch), 1)
+        notes[MAMBA1_SP] = f"{ch} of {Dm} channels, all tokens, {reps} rep(s), scaled to all channels"
+    if "backward" in compact:
         Bz, L, H, P, N, G = 1, 2048, 24, 64, 128, 1
         hs = 2
         d = inputs.ssd_inputs(Bz, L, hs, P, N, G, io_dtype="bf16", seed=0)
         dy = inputs.round_to(np.random.default_rng(1).standard_normal(d["x"].shape), "bf16")
         per, reps = _timed(lambda: oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"],
                                                       threads=thr), seconds)
-        out["backward"]["oracle"] = rec(Bz * L / (per * H / hs), "tokens/s",
-                                        f"{hs} of {H} heads (one B/C group, so one host thread), all {L} tokens, "
-                                        f"{reps} repetition(s), scaled to all heads")
+        compact["backward"]["cpu"] = round(Bz * L / (per * H / hs), 1)
+        notes["backward"] = f"{hs} of {H} heads (one host thread), all {L} tokens, {reps} rep(s), scaled to all heads"
 
 
 def run_reference(args):
@@ -846,7 +1031,7 @@ def run_reference(args):
     el = time.perf_counter() - t0
     tokens = w["batch"] * Ls
     value = tokens * K / el
-    sample = f"first {Ls} of {w['seqlen']} tokens per step, all {w['nheads']} heads, float64"
+    sample = f"first {Ls} of {w['seqlen']} tokens of all {w['batch']} sequences per step, all {w['nheads']} heads, float64"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True,
@@ -855,27 +1040,187 @@ def run_reference(args):
                    "nheads": w["nheads"], "headdim": w["headdim"], "dstate": w["dstate"], "ngroups": w["ngroups"],
                    "parallelism": "host threads"},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "cpu": host_cpu(), "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ chunk table
+
+CT_CHUNKS = (64, 128, 256)
+CT_BATCHES = (1, 2, 4, 8)
+CT_LENGTHS = (512, 1024, 2048, 4096, 8192)
+CT_HEADS = (24, 48, 80)
+
+
+def run_chunk_table(args):
+    """The fastest chunk size per shape over a grid of batch, length and head
+    count (bf16, headdim 64, d_state 128, one group), each shape in a graph of
+    back-to-back calls whose inputs rotate past L2 (random device tensors:
+    timing only). Prints one JSON line per shape, then the C table of the
+    static chunk policy (ssd_best_chunk) -- the pages' static-oracle /
+    learned-table policy ("COREY ...", section 5.2)."""
+    import torch
+    from mamba_ssd_selective_gb300 import binding
+    binding.load()
+    dev, bf = torch.device("cuda"), torch.bfloat16
+    P, N = 64, 128
+    rows = []
+    for H in CT_HEADS:
+        for Bz in CT_BATCHES:
+            for L in CT_LENGTHS:
+                g = torch.Generator(device=dev).manual_seed(0)
+                per = Bz * L * (2 * H * P + H + 2 * N) * 2
+                nsets = max(2, math.ceil(3 * 129e6 / per))
+                ws_max = max(binding.ssd_workspace_size(Bz, L, H, P, N, 1, bf, q) for q in CT_CHUNKS)
+                A = -torch.exp(torch.rand(H, generator=g, device=dev) * math.log(16.0))
+                Dv = torch.rand(H, generator=g, device=dev) + 0.5
+                sets = []
+                for _ in range(nsets):
+                    sets.append(dict(
+                        x=torch.randn(Bz, L, H, P, generator=g, device=dev).to(bf),
+                        dt=torch.nn.functional.softplus(torch.randn(Bz, L, H, generator=g, device=dev) * 0.5 - 4).to(bf),
+                        B=torch.randn(Bz, L, 1, N, generator=g, device=dev).to(bf),
+                        C=torch.randn(Bz, L, 1, N, generator=g, device=dev).to(bf),
+                        y=torch.empty(Bz, L, H, P, dtype=bf, device=dev), f=torch.empty(Bz, H, P, N, device=dev),
+                        ws=torch.empty(ws_max, dtype=torch.uint8, device=dev)))
+                us = {}
+                for q in CT_CHUNKS:
+                    def step(s):
+                        binding.ssd_scan_chunked(s["x"], s["dt"], A, s["B"], s["C"], Dv, None, chunk_size=q,
+                                                 y=s["y"], final_state=s["f"], workspace=s["ws"])
+                    st = torch.cuda.Stream()
+                    st.wait_stream(torch.cuda.current_stream())
+                    with torch.cuda.stream(st):
+                        for s in sets:
+                            step(s)
+                    st.synchronize()
+                    steps = max(4, 2 * nsets)
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph, stream=st, capture_error_mode="relaxed"):
+                        for i in range(steps):
+                            step(sets[i % nsets])
+                    for _ in range(2):
+                        graph.replay()
+                    ms, _ = graph_rep_stats(torch, graph, steps, reps=3)
+                    us[q] = ms * 1e3
+                    del graph
+                del sets
+                torch.cuda.empty_cache()
+                best = min(us, key=us.get)
+                rows.append({"batch": Bz, "seqlen": L, "nheads": H, "best": best,
+                             "us": {str(q): round(v, 2) for q, v in us.items()}})
+                print(json.dumps(rows[-1]), flush=True)
+    print("// {batch, seqlen, nheads, best chunk}: measured by bench.py --chunk-table")
+    print("const ChunkEntry kChunkTable[] = {")
+    for r in rows:
+        print(f"    {{{r['batch']}, {r['seqlen']}, {r['nheads']}, {r['best']}}},")
+    print("};")
+
+
+def run_profile_calls(args):
+    """N plain calls of each selected leg's workload (prefill legs at chunk 128,
+    the headline at its chunk argument or 128), no timing, for profiler launch
+    lists; inputs as in the timed legs."""
+    import torch
+    from mamba_ssd_selective_gb300 import binding, inputs
+    binding.load()
+    dev = torch.device("cuda")
+    bf = torch.bfloat16
+    legs = set(args.legs.split(",")) if args.legs else set(LEGS)
+    n = args.profile_calls
+
+    def t_(a, dtype=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype)
+
+    names = ([HEADLINE] if "headline" in legs else []) + (list(PREFILL_LEGS) if "prefill" in legs else [])
+    for nm in names:
+        w = inputs.WORKLOADS[nm]
+        d = inputs.ssd_inputs(w["batch"], w["seqlen"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"],
+                              io_dtype="bf16", seed=0)
+        a = (t_(d["x"], bf), t_(d["dt"], bf), t_(d["A"]), t_(d["B"], bf), t_(d["C"], bf), t_(d["D"]))
+        del d
+        q = (args.chunk or 128) if nm == HEADLINE else 128
+        for _ in range(n):
+            binding.ssd_scan_chunked(*a, None, chunk_size=q)
+        torch.cuda.synchronize()
+        del a
+    if "decode" in legs:
+        w = inputs.WORKLOADS[DECODE]
+        Bz, H, P, N, G = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"]
+        st = t_(inputs.decode_state(Bz, H, P, N, seed=0))
+        prm = inputs.decode_params(H, seed=0)
+        for s in range(n):
+            di = inputs.decode_step_inputs(s, Bz, H, P, N, G, io_dtype="bf16", seed=0)
+            binding.ssd_decode_step(st, t_(di["x"], bf), t_(di["dt"], bf), t_(prm["A"]), t_(di["B"], bf),
+                                    t_(di["C"], bf), t_(prm["D"]))
+        torch.cuda.synchronize()
+    if "decode_layer" in legs:
+        w = inputs.WORKLOADS["decode_layer_B64_H80"]
+        Bz, H, P, N, G, Wc = w["batch"], w["nheads"], w["headdim"], w["dstate"], w["ngroups"], w["width"]
+        prm = inputs.decode_layer_params(Bz, H, P, N, G, Wc, seed=0)
+        li = inputs.decode_layer_step_inputs(0, Bz, H, P, N, G, io_dtype="bf16", seed=0)
+        cst, sst = t_(prm["conv_state"]), t_(prm["ssm_state"])
+        for _ in range(n):
+            binding.decode_layer_step(t_(li["xBC"], bf), cst, t_(prm["conv_w"]), t_(prm["conv_b"]), t_(li["dt"], bf),
+                                      t_(prm["A"]), t_(prm["D"]), sst, t_(li["z"], bf), t_(prm["norm_w"]),
+                                      norm_group=w["norm_group"])
+        torch.cuda.synchronize()
+    if "mamba1" in legs:
+        w = inputs.WORKLOADS[MAMBA1]
+        d = inputs.diag_inputs(w["batch"], w["seqlen"], w["dim"], w["dstate"], io_dtype="bf16", seed=0)
+        a = (t_(d["x"], bf), t_(d["dt"], bf), t_(d["A"]), t_(d["B"], bf), t_(d["C"], bf), t_(d["D"]))
+        del d
+        for _ in range(n):
+            binding.selective_scan_diag(*a, None, chunk_size=w["chunk"])
+        torch.cuda.synchronize()
+        del a
+    if "mamba1_softplus" in legs:
+        w = inputs.WORKLOADS[MAMBA1_SP]
+        d = inputs.diag_option_inputs(w["batch"], w["seqlen"], w["dim"], w["dstate"], io_dtype="bf16", seed=0,
+                                      bias=False, z=False)
+        a = (t_(d["x"], bf), t_(d["dt"], bf), t_(d["A"]), t_(d["B"], bf), t_(d["C"], bf), t_(d["D"]))
+        for _ in range(n):
+            binding.selective_scan_diag(*a, None, chunk_size=w["chunk"], delta_softplus=True)
+        torch.cuda.synchronize()
+    if "backward" in legs:
+        d = inputs.ssd_inputs(1, 2048, 24, 64, 128, 1, io_dtype="bf16", seed=0)
+        dy = inputs.round_to(np.random.default_rng(1).standard_normal(d["x"].shape), "bf16")
+        a = (t_(d["x"], bf), t_(d["dt"], bf), t_(d["A"]), t_(d["B"], bf), t_(d["C"], bf), t_(dy, bf), t_(d["D"]))
+        for _ in range(n):
+            binding.ssd_scan_chunked_bwd(*a)
+        torch.cuda.synchronize()
+    print(json.dumps({"profile_calls": n, "legs": sorted(legs)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--chunk", type=int, default=0, help="force a chunk size (default: best of 64/128/256)")
+    ap.add_argument("--chunk", type=int, default=0, help="force the headline's chunk size (default: best of 64/128/256)")
+    ap.add_argument("--legs", default=None, help=f"comma-separated subset of {','.join(LEGS)} (default: all)")
     ap.add_argument("--workload", default=None, help="reference arm: workload name (default: the headline)")
     ap.add_argument("--ref-budget-s", type=float, default=60.0, help="reference arm: total oracle seconds")
-    ap.add_argument("--skip-extra", action="store_true", help="skip the decode and Mamba-1 lines")
-    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--skip-extra", action="store_true", help="the headline leg only")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU oracle baselines")
+    ap.add_argument("--chunk-table", action="store_true", help="measure the chunk-policy table and print it")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="make this many plain calls of each selected leg's workload (for profiler launch lists)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3  # at least three warm-up steps
-    if args.impl == "reference":
+    if args.legs:
+        bad = set(args.legs.split(",")) - set(LEGS)
+        if bad:
+            ap.error(f"unknown legs: {sorted(bad)}")
+    if args.chunk_table:
+        run_chunk_table(args)
+    elif args.profile_calls > 0:
+        run_profile_calls(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -100,6 +100,23 @@ size_t ssd_workspace_size(const ssd_dims *dims, int chunk_size);
  */
 int ssd_best_chunk(const ssd_dims *dims);
 
+/* Kernel paths of ssd_scan_chunked (return values of ssd_scan_path). */
+#define SSD_PATH_SIMT 0   /* CUDA cores, float32: chunk state, state passing, chunk scan */
+#define SSD_PATH_STAGED 1 /* tensor cores: the same three steps as three kernels */
+#define SSD_PATH_FUSED 2  /* tensor cores: one persistent kernel (and a kernel that clears its flags) */
+
+/*
+ * The kernel path ssd_scan_chunked takes for these sizes, chunk size and
+ * dims->flags on the current device (SSD_PATH_*), or -1 if the arguments are
+ * invalid or SSD_FLAG_FUSED is set for sizes the single pass does not take.
+ * Without flags the single pass is taken for bf16, headdim 64, dstate 128,
+ * chunk 128 and an even number of heads per group when batch * nheads / 2 is
+ * at least the SM count: those chains (b, head pair) are then numerous enough
+ * to hide the hand-off of the carried state from one work item to the next.
+ * Host-only: no launch, no synchronisation.
+ */
+int ssd_scan_path(const ssd_dims *dims, int chunk_size);
+
 /*
  * Chunked SSD prefill over a whole sequence (the SSD scan run "chunk by chunk,
  * each chunk continuing from the previous chunk's state", "Recurrence Scan",

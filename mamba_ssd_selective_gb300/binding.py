@@ -22,6 +22,7 @@ SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_SIMT = 1
 SSD_FLAG_FUSED = 2
 SSD_FLAG_STAGED = 4
+PATH_NAMES = {0: "simt", 1: "staged", 2: "fused"}
 _PATH_FLAGS = {None: 0, "auto": 0, "simt": SSD_FLAG_SIMT, "fused": SSD_FLAG_FUSED, "staged": SSD_FLAG_STAGED}
 
 _STATUS_NAMES = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
@@ -64,6 +65,8 @@ def load() -> ctypes.CDLL:
             lib.ssd_workspace_size.restype = sz
             lib.ssd_best_chunk.argtypes = [dp]
             lib.ssd_best_chunk.restype = ctypes.c_int
+            lib.ssd_scan_path.argtypes = [dp, ctypes.c_int]
+            lib.ssd_scan_path.restype = ctypes.c_int
             lib.ssd_scan_chunked_bwd_workspace_size.argtypes = [dp]
             lib.ssd_scan_chunked_bwd_workspace_size.restype = sz
             lib.ssd_scan_chunked_bwd.argtypes = [dp] + [vp] * 17 + [sz, vp]
@@ -156,6 +159,16 @@ def ssd_best_chunk(batch, seqlen, nheads, headdim, dstate, ngroups, io_dtype) ->
     """Chunk size of the library's static policy for these sizes (0: invalid)."""
     d = _dims(batch, seqlen, nheads, headdim, dstate, ngroups, _io_code(io_dtype))
     return int(load().ssd_best_chunk(ctypes.byref(d)))
+
+
+def ssd_scan_path(batch, seqlen, nheads, headdim, dstate, ngroups, io_dtype, chunk_size, path=None) -> str:
+    """Name of the kernel path ("simt", "staged", "fused") ssd_scan_chunked
+    takes for these sizes on the current device."""
+    d = _dims(batch, seqlen, nheads, headdim, dstate, ngroups, _io_code(io_dtype), _PATH_FLAGS[path])
+    code = int(load().ssd_scan_path(ctypes.byref(d), int(chunk_size)))
+    if code < 0:
+        raise SsdError(SSD_ERR_INVALID_ARG, "invalid sizes, chunk size or path for ssd_scan_path")
+    return PATH_NAMES[code]
 
 
 def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=None, y=None, final_state=None,

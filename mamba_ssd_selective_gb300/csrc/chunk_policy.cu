@@ -4,7 +4,7 @@
 // per regime ("COREY ...", section 5.2: the static-oracle and learned-table
 // policies, where a length-keyed table matched the per-regime oracle). This is
 // that table for the bf16 tensor-core path (P = 64, N = 128) on GB300, measured
-// by `python -m mamba_ssd_selective_gb300.chunk_table` over batch 1-8, sequence
+// by `python bench.py --chunk-table` over batch 1-8, sequence
 // length 512-8192 and 24-80 heads; a shape off the grid takes its nearest grid
 // point in (log2 batch, log2 length, heads). Shapes the tensor-core path does
 // not take were not measured and get 128.
@@ -19,7 +19,7 @@ struct ChunkEntry {
     int batch, seqlen, nheads, chunk;
 };
 
-// {batch, seqlen, nheads, best chunk}: measured by mamba_ssd_selective_gb300.chunk_table
+// {batch, seqlen, nheads, best chunk}: measured by bench.py --chunk-table
 const ChunkEntry kChunkTable[] = {
     {1, 512, 24, 64},
     {1, 1024, 24, 128},

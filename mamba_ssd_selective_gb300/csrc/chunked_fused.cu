@@ -37,7 +37,10 @@
 // n contiguous, is one 128-byte line), S'_0 [384,448), S'_1 [448,512).
 //
 // Warp roles (20 warps, one CTA per SM):
-//   warp 0       TMA producer: C, B, x (two items x two heads)
+//   warp 0       TMA producer: x (two chunks x two heads), C (two chunks), B;
+//                each x tile is loaded twice: for the chunk-state MMA, which
+//                reads it after the chain group has scaled it in place by w,
+//                and again (from L2, microseconds later) for S' X
 //   warp 1       MMA issuer (one lane)
 //   warp 2       TMA store of y, one head at a time, staged in shared memory
 //   warp 3       per-item scalars: cumulative sums of dt A (base 2), decays
@@ -85,40 +88,41 @@ struct FusedParams {
 };
 
 // shared memory carve (bytes from the 1024-aligned base)
-constexpr uint32_t kOffC = 0;          // 32 KB: C tile, K-major, 2 panels of n
-constexpr uint32_t kOffB = 32768;      // 32 KB: B tile (K-major for S, MN-major for the chunk state)
-constexpr uint32_t kOffX = 65536;      // 4 x 16 KB: x tiles, slot 2 (item & 1) + k
-constexpr uint32_t kOffWX = 131072;    // 32 KB: w o x of both heads (MN-major B operand, N = (k, p))
+constexpr uint32_t kOffC = 0;          // 2 x 32 KB: C tiles (chunk & 1), K-major, 2 panels of n
+constexpr uint32_t kOffB = 65536;      // 32 KB: B tile (K-major for S, MN-major for the chunk state)
+constexpr uint32_t kOffX = 98304;      // 4 x 16 KB: x tiles, slot 2 (chunk & 1) + k; the two slots of a
+                                       // chunk are the N = (k, p) panels of the chunk-state B operand
 constexpr uint32_t kOffH = 163840;     // 32 KB: h_in bf16, rows (k, p), 2 panels of n
 constexpr uint32_t kOffY = 196608;     // 16 KB: y of one head, 128-byte swizzle
 constexpr uint32_t kOffS = 212992;     // scalars, two item buffers
 constexpr int kScal = 5 * kHB * kQ + 2 * kHB;  // cs | dt | colf | sc | w, then D, alpha
 constexpr uint32_t kOffBar = kOffS + 2 * kScal * 4;
 enum {
-    BAR_CB_FULL = 0,
-    BAR_C_EMPTY = 1,
-    BAR_B_EMPTY = 2,
-    BAR_X_FULL = 3,    // [4]
-    BAR_X_EMPTY = 7,   // [4]
-    BAR_S_FULL = 11,
-    BAR_S_EMPTY = 12,
-    BAR_WX_FULL = 13,
-    BAR_WX_EMPTY = 14,
-    BAR_HIN_FULL = 15,
-    BAR_SC_FULL = 16,
-    BAR_H_EMPTY = 17,
-    BAR_YO_FULL = 18,
-    BAR_P_FULL = 19,   // [2]
-    BAR_P_EMPTY = 21,  // [2]
-    BAR_Y_FULL = 23,   // [2]
-    BAR_ACC_EMPTY = 25,
-    BAR_SCAL_FULL = 26,   // [2]
-    BAR_SCAL_EMPTY = 28,  // [2]
-    BAR_YS_FULL = 30,
-    BAR_YS_EMPTY = 31,
-    BAR_CARRY_DONE = 32,
-    BAR_FLAG_OK = 33,
-    kBars = 34
+    BAR_C_FULL = 0,     // [2]
+    BAR_C_EMPTY = 2,    // [2]
+    BAR_B_FULL = 4,
+    BAR_B_EMPTY = 5,    // S and the chunk-state MMA have read B and the scaled x
+    BAR_X_FULL = 6,     // [4] first load of x (scaled in place for the chunk state)
+    BAR_X2_FULL = 10,   // [4] second load of x (for S' X)
+    BAR_X_EMPTY = 14,   // [4]
+    BAR_S_FULL = 18,
+    BAR_S_EMPTY = 19,
+    BAR_WX_FULL = 20,
+    BAR_HIN_FULL = 21,
+    BAR_SC_FULL = 22,
+    BAR_H_EMPTY = 23,
+    BAR_YO_FULL = 24,
+    BAR_P_FULL = 25,    // [2]
+    BAR_P_EMPTY = 27,   // [2]
+    BAR_Y_FULL = 29,    // [2]
+    BAR_ACC_EMPTY = 31,
+    BAR_SCAL_FULL = 32,   // [2]
+    BAR_SCAL_EMPTY = 34,  // [2]
+    BAR_YS_FULL = 36,
+    BAR_YS_EMPTY = 37,
+    BAR_CARRY_DONE = 38,
+    BAR_FLAG_OK = 39,
+    kBars = 40
 };
 constexpr uint32_t kSmemBytes = kOffBar + kBars * 8 + 16 + 1024;
 
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sC = smem + kOffC, *sB = smem + kOffB, *sX = smem + kOffX, *sWX = smem + kOffWX;
+    uint8_t *sC = smem + kOffC, *sB = smem + kOffB, *sX = smem + kOffX;
     uint8_t *sH = smem + kOffH, *sY = smem + kOffY;
     float *s_scal = reinterpret_cast<float *>(smem + kOffS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -222,13 +226,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // the unscaled x of chunk `rit` back into its slots, for S' X
+            auto reload_x = [&](int rb, int64_t rc, int rhg, uint32_t rit) {
+                for (int k = 0; k < kHB; ++k) {
+                    const int slot = 2 * (int)(rit & 1) + k;
+                    tc::mbar_arrive_expect_tx(&bars[BAR_X2_FULL + slot], 16384u);
+                    tc::tma_load_3d(sX + slot * 16384, &prm.mx, &bars[BAR_X2_FULL + slot], (rhg * kHB + k) * kP,
+                                    (int)(rc * kQ), rb);
+                }
+            };
+            int pb = 0, phg = 0;
+            int64_t pc = 0;
+            uint32_t n_done = 0;
             for_chunks([&](int64_t b, int64_t c, int hg, uint32_t it, bool, bool) -> bool {
                 if (*s_fail) return false;
+                n_done = it + 1;
                 const uint32_t par = it & 1, ph = it & 1, ph2 = (it >> 1) & 1;
                 const int t0 = (int)(c * kQ), bb = (int)b;
                 const int g = (int)((int64_t)hg * kHB / (a.H / a.G));
-                // x first: its two-chunk ring frees long before the single C
-                // tile, which waits for the previous chunk's Yo MMA
                 for (int k = 0; k < kHB; ++k) {
                     const int slot = 2 * par + k;
                     if (!pwait(&bars[BAR_X_EMPTY + slot], ph2 ^ 1, s_fail)) return false;
@@ -236,16 +251,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                     tc::tma_load_3d(sX + slot * 16384, &prm.mx, &bars[BAR_X_FULL + slot], (hg * kHB + k) * kP, t0,
                                     bb);
                 }
-                if (!pwait(&bars[BAR_B_EMPTY], ph ^ 1, s_fail)) return false;
-                if (!pwait(&bars[BAR_C_EMPTY], ph ^ 1, s_fail)) return false;
-                uint64_t *cb = &bars[BAR_CB_FULL];
-                tc::mbar_arrive_expect_tx(cb, 65536u);
-                tc::tma_load_3d(sB, &prm.mb, cb, g * kN, t0, bb);
-                tc::tma_load_3d(sB + 16384, &prm.mb, cb, g * kN + 64, t0, bb);
-                tc::tma_load_3d(sC, &prm.mc, cb, g * kN, t0, bb);
-                tc::tma_load_3d(sC + 16384, &prm.mc, cb, g * kN + 64, t0, bb);
+                if (!pwait(&bars[BAR_C_EMPTY + par], ph2 ^ 1, s_fail)) return false;  // Yo of chunk it - 2 is done
+                tc::mbar_arrive_expect_tx(&bars[BAR_C_FULL + par], 32768u);
+                tc::tma_load_3d(sC + par * 32768, &prm.mc, &bars[BAR_C_FULL + par], g * kN, t0, bb);
+                tc::tma_load_3d(sC + par * 32768 + 16384, &prm.mc, &bars[BAR_C_FULL + par], g * kN + 64, t0, bb);
+                if (!pwait(&bars[BAR_B_EMPTY], ph ^ 1, s_fail)) return false;  // chunk it - 1's MMAs read B, w o x
+                tc::mbar_arrive_expect_tx(&bars[BAR_B_FULL], 32768u);
+                tc::tma_load_3d(sB, &prm.mb, &bars[BAR_B_FULL], g * kN, t0, bb);
+                tc::tma_load_3d(sB + 16384, &prm.mb, &bars[BAR_B_FULL], g * kN + 64, t0, bb);
+                if (it > 0) reload_x(pb, pc, phg, it - 1);  // chunk it - 1's slots are free again
+                pb = bb;
+                pc = c;
+                phg = hg;
                 return true;
             });
+            // the last chunk's reload, once its MMAs have read the scaled x
+            if (n_done > 0 && !*s_fail && pwait(&bars[BAR_B_EMPTY], (n_done - 1) & 1, s_fail))
+                reload_x(pb, pc, phg, n_done - 1);
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
@@ -254,12 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
             const uint32_t idH = tc::idesc_bf16(128, 128, true, true);
             const uint32_t idO = tc::idesc_bf16(128, 128, false, false);
             const uint32_t idY = tc::idesc_bf16(128, kP, false, true);
-            const uint32_t c0 = tc::smem_u32(sC), b0 = tc::smem_u32(sB), w0 = tc::smem_u32(sWX);
+            const uint32_t b0 = tc::smem_u32(sB);
             const uint32_t h0 = tc::smem_u32(sH);
             for_chunks([&](int64_t, int64_t, int, uint32_t it, bool, bool) -> bool {
                 if (*s_fail) return false;
                 const uint32_t par = it & 1, ph = it & 1, ph2 = (it >> 1) & 1;
-                if (!pwait(&bars[BAR_CB_FULL], ph, s_fail)) return false;
+                const uint32_t c0 = tc::smem_u32(sC + par * 32768), w0 = tc::smem_u32(sX + 2 * par * 16384);
+                if (!pwait(&bars[BAR_C_FULL + par], ph2, s_fail)) return false;
+                if (!pwait(&bars[BAR_B_FULL], ph, s_fail)) return false;
                 // S = C B^T (the previous chunk's S has been read)
                 if (!pwait(&bars[BAR_S_EMPTY], ph ^ 1, s_fail)) return false;
                 tc::tc_fence_after();
@@ -279,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                     tc::mma_bf16(tH, da, db, idH, 1u);
                 }
                 tc::mma_commit(&bars[BAR_SC_FULL]);
-                tc::mma_commit(&bars[BAR_WX_EMPTY]);
                 tc::mma_commit(&bars[BAR_B_EMPTY]);
                 // Yo = C h_in^T for both heads into Y (the previous chunk's y has been read)
                 if (!pwait(&bars[BAR_ACC_EMPTY], ph ^ 1, s_fail)) return false;
@@ -291,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 }
                 tc::mma_commit(&bars[BAR_YO_FULL]);
                 tc::mma_commit(&bars[BAR_H_EMPTY]);
-                tc::mma_commit(&bars[BAR_C_EMPTY]);
+                tc::mma_commit(&bars[BAR_C_EMPTY + par]);
                 // Y_k += S'_k X_k onto the rescaled Yo_k
                 for (int kh = 0; kh < kHB; ++kh) {
                     const int slot = 2 * par + kh;
-                    if (!pwait(&bars[BAR_X_FULL + slot], ph2, s_fail)) return false;
+                    if (!pwait(&bars[BAR_X2_FULL + slot], ph2, s_fail)) return false;  // the unscaled x again
                     if (!pwait(&bars[BAR_P_FULL + kh], ph, s_fail)) return false;
                     tc::tc_fence_after();
                     const uint32_t x0 = tc::smem_u32(sX + slot * 16384);
@@ -405,11 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
             const float *base = s_scal + par * kScal;
             const float *s_w = base + 4 * kHB * kQ, *s_alpha = base + 5 * kHB * kQ + kHB;
 
-            // (1) w o x of both heads, row j of head k scaled by w_k,j (the
-            // 128-byte swizzle only permutes 16-byte pieces inside a row)
+            // (1) w o x of both heads in place, row j of head k scaled by w_k,j
+            // (the 128-byte swizzle only permutes 16-byte pieces inside a row)
             pwait(&bars[BAR_X_FULL + 2 * par], ph2, s_fail);
             pwait(&bars[BAR_X_FULL + 2 * par + 1], ph2, s_fail);
-            pwait(&bars[BAR_WX_EMPTY], ph ^ 1, s_fail);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int v = ctid + kGroupThreads * r;  // 16-byte piece of the two 16 KB tiles
@@ -423,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                     const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[m]));
                     o[m] = pack_bf16x2(f.x * w, f.y * w);
                 }
-                *reinterpret_cast<uint4 *>(sWX + k * 16384 + (v & 1023) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(sX + (2 * par + k) * 16384 + (v & 1023) * 16) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
             }
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(&bars[BAR_WX_FULL]);

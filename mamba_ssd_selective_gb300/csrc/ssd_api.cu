@@ -103,6 +103,23 @@ size_t ssd_workspace_size(const ssd_dims *dims, int chunk_size) {
         .total;
 }
 
+int ssd_scan_path(const ssd_dims *dims, int chunk_size) {
+    if (check_dims(dims, true) != SSD_OK || !valid_chunk(chunk_size)) return -1;
+    ssd::ChunkedArgs a{};
+    a.B = dims->batch; a.L = dims->seqlen; a.H = dims->nheads; a.P = dims->headdim; a.N = dims->dstate;
+    a.G = dims->ngroups; a.Q = chunk_size;
+    a.nc = (a.L + chunk_size - 1) / chunk_size;
+    a.io = dims->io_dtype == SSD_BF16 ? ssd::IO_BF16 : ssd::IO_F32;
+    const bool has_tokens = a.B > 0 && a.L > 0;
+    if (dims->flags & SSD_FLAG_FUSED) return ssd::chunked_fused_supported(a) ? SSD_PATH_FUSED : -1;
+    if (a.io == ssd::IO_BF16 && !(dims->flags & (SSD_FLAG_SIMT | SSD_FLAG_STAGED)) && has_tokens &&
+        ssd::chunked_fused_supported(a) && ssd::chunked_fused_preferred(a))
+        return SSD_PATH_FUSED;
+    if (a.io == ssd::IO_BF16 && !(dims->flags & SSD_FLAG_SIMT) && has_tokens && ssd::chunked_tc_supported(a))
+        return SSD_PATH_STAGED;
+    return SSD_PATH_SIMT;
+}
+
 ssd_status ssd_scan_chunked(const ssd_dims *dims, const void *x, const void *dt, const float *A, const void *B,
                             const void *C, const float *D, const float *init_state, int chunk_size, void *y,
                             float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream) {

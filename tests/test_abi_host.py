@@ -157,6 +157,17 @@ def test_backward_validation_and_workspace_size(lib):
     assert bwd(d, bad) == binding.SSD_ERR_INVALID_ARG
 
 
+def test_scan_path_query(lib):
+    from mamba_ssd_selective_gb300 import binding
+    r = ctypes.byref
+    assert lib.ssd_scan_path(None, 128) == -1
+    assert lib.ssd_scan_path(r(_dims(binding)), 100) == -1
+    assert lib.ssd_scan_path(r(_dims(binding, nheads=6, ngroups=4)), 128) == -1
+    # float32 inputs and the SIMT flag always take the CUDA-core path
+    assert lib.ssd_scan_path(r(_dims(binding, io_dtype=binding.SSD_F32)), 128) == 0
+    assert lib.ssd_scan_path(r(_dims(binding, io_dtype=binding.SSD_BF16, flags=binding.SSD_FLAG_SIMT)), 128) == 0
+
+
 def test_best_chunk_policy(lib):
     from mamba_ssd_selective_gb300 import binding
     pick = lambda **kw: lib.ssd_best_chunk(ctypes.byref(_dims(binding, **kw)))

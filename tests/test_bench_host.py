@@ -68,28 +68,39 @@ def test_roofline_byte_counts():
     from mamba_ssd_selective_gb300 import inputs
     w = inputs.WORKLOADS[bench.HEADLINE]
     b = bench.ssd_compulsory_bytes(w)
-    # x and y: 4096 tokens x 24 heads x 64 x 2 bytes each
-    assert b["x"] == 4096 * 24 * 64 * 2 == b["y"]
+    # x and y: 8 x 2048 tokens x 80 heads x 64 x 2 bytes each
+    assert b["x"] == 8 * 2048 * 80 * 64 * 2 == b["y"]
     assert b["total"] == b["x"] + b["y"] + b["dt"] + b["B"] + b["C"] + b["final_state"]
-    # 28.2 MB per step: zero initial state, so only the final state is moved
-    assert abs(b["total"] / 1e6 - 28.25) < 0.01
+    # 367.5 MB per step: zero initial state, so only the final state is moved
+    assert abs(b["total"] / 1e6 - 367.53) < 0.01
     assert bench.stage_algorithmic_bytes(w, "chunk_scan") == b["x"] + b["dt"] + b["B"] + b["C"] + b["y"]
+    # the single-pass kernel moves the whole step's compulsory bytes
+    assert bench.stage_algorithmic_bytes(w, "chunk_fused") == b["total"]
+    w130 = inputs.WORKLOADS["ssd_m2_130m_L4096"]
+    assert abs(bench.ssd_compulsory_bytes(w130)["total"] / 1e6 - 28.25) < 0.01
 
 
 def test_traffic_records_are_well_formed():
-    """profiles/traffic.json: one record per dominant kernel the bench reports,
-    naming a kernel that exists in its source file, with a positive per-launch
-    byte count and the capture it came from; a record whose source has changed
-    since is reported as null by the bench, never as a stale number."""
+    """profiles/traffic.json: per-step records ("step:<workload>:<path>:<chunk>")
+    and per-kernel records ("kernel:<name>") with DRAM read and write bytes,
+    the kernels and the source files they come from (every kernel name found in
+    them), a hash of those sources and the capture's command; a record whose
+    sources have changed since is reported as null by the bench, never as a
+    stale number."""
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         recs = json.load(f)
-    assert set(recs) >= {"chunk_scan", "decode_step", "diag_scan"}
+    assert any(k.startswith("step:" + bench.HEADLINE) for k in recs)
     for key, rec in recs.items():
-        src = os.path.join(ROOT, "mamba_ssd_selective_gb300", "csrc", rec["source"])
-        assert os.path.exists(src), key
-        with open(src) as f:
-            assert rec["kernel"] in f.read(), key
-        assert int(rec["bytes_per_launch"]) > 0 and rec["capture"], key
-        got = bench._traffic_for(key)
-        assert got is None or got == rec["bytes_per_launch"], key
-    assert bench._traffic_for("no_such_kernel") is None
+        assert key.startswith(("step:", "kernel:")), key
+        srcs = [os.path.join(ROOT, "mamba_ssd_selective_gb300", "csrc", s) for s in rec["sources"]]
+        text = ""
+        for src in srcs:
+            assert os.path.exists(src), key
+            with open(src) as f:
+                text += f.read()
+        for k in rec["kernels"]:
+            assert k in text, (key, k)
+        assert int(rec["read"]) > 0 and int(rec["write"]) >= 0 and rec["capture"] and rec["command"], key
+        got = bench._traffic_record(key)
+        assert got is None or got == rec, key
+    assert bench._traffic_record("kernel:no_such_kernel") is None
