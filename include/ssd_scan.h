@@ -60,7 +60,8 @@ typedef enum {
     SSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment, short workspace */
     SSD_ERR_UNSUPPORTED = 2, /* valid arguments, shape outside what the kernels handle */
     SSD_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
-    SSD_ERR_TIMEOUT = 4      /* a bounded in-kernel wait gave up (see ssd_workspace_status) */
+    SSD_ERR_TIMEOUT = 4,     /* a bounded in-kernel wait gave up (see ssd_workspace_status) */
+    SSD_ERR_BOUNDS = 5       /* debug builds: a kernel's bounds check failed (see ssd_debug_bounds_status) */
 } ssd_status;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
@@ -314,6 +315,20 @@ ssd_status ssd_selftest_bounded_wait(void *workspace, int spin_limit, cudaStream
  * programmatic overlap. count must be 4; events = NULL cancels a request.
  */
 ssd_status ssd_record_stage_events(cudaEvent_t *events, int count);
+
+/*
+ * Bounds checks of a debug build. A library compiled with -DSSD_DEBUG_BOUNDS
+ * (python -m mamba_ssd_selective_gb300.build --debug-bounds, which writes
+ * lib/libssdscan_dbg.so) checks the raw global-memory accesses of its decode,
+ * Mamba-1, state-pass and single-pass prefill kernels against the extents of
+ * their buffers: a failing access is skipped (never a trap) and the first
+ * failure is recorded. This call waits for the device, then returns SSD_OK if
+ * no check has failed, or SSD_ERR_BOUNDS with *site (a site number of
+ * csrc/debug_bounds.cuh) and *index (the first element of the failing
+ * access) filled in; clear != 0 resets the record. site and index may be
+ * NULL. A release build returns SSD_ERR_UNSUPPORTED.
+ */
+ssd_status ssd_debug_bounds_status(int *site, int64_t *index, int clear);
 
 /*
  * Backward of ssd_scan_chunked (the training step's backward; "Compiler-First

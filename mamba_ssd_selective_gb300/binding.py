@@ -17,7 +17,7 @@ import torch
 
 from . import build as _build
 
-SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = 0, 1, 2, 3, 4
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_BOUNDS = 0, 1, 2, 3, 4, 5
 SSD_F32, SSD_BF16 = 0, 1
 SSD_FLAG_SIMT = 1
 SSD_FLAG_FUSED = 2
@@ -26,7 +26,7 @@ PATH_NAMES = {0: "simt", 1: "staged", 2: "fused"}
 _PATH_FLAGS = {None: 0, "auto": 0, "simt": SSD_FLAG_SIMT, "fused": SSD_FLAG_FUSED, "staged": SSD_FLAG_STAGED}
 
 _STATUS_NAMES = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
-                 4: "SSD_ERR_TIMEOUT"}
+                 4: "SSD_ERR_TIMEOUT", 5: "SSD_ERR_BOUNDS"}
 
 
 class SsdError(RuntimeError):
@@ -46,7 +46,9 @@ _lock = threading.Lock()
 
 
 def lib_path() -> str:
-    return _build.LIB_PATH
+    """The library this process loads: the bounds-checked debug build when the
+    environment sets SSD_DEBUG_BOUNDS_LIB=1, else the release build."""
+    return _build.DBG_LIB_PATH if os.environ.get("SSD_DEBUG_BOUNDS_LIB") == "1" else _build.LIB_PATH
 
 
 def load() -> ctypes.CDLL:
@@ -97,6 +99,9 @@ def load() -> ctypes.CDLL:
             lib.selective_scan_diag_workspace_size.restype = sz
             lib.ssd_workspace_status.argtypes = [vp, vp]
             lib.ssd_selftest_bounded_wait.argtypes = [vp, ctypes.c_int, vp]
+            lib.ssd_debug_bounds_status.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int64),
+                                                    ctypes.c_int]
+            lib.ssd_debug_bounds_status.restype = ctypes.c_int
             lib.ssd_record_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
             lib.ssd_record_stage_events.restype = ctypes.c_int
             lib.ssd_last_error.argtypes = []
@@ -389,6 +394,14 @@ def ssd_record_stage_events(events) -> None:
         return
     arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(int(e.cuda_event)) for e in events])
     _check(load().ssd_record_stage_events(arr, len(events)))
+
+
+def ssd_debug_bounds_status(clear=True):
+    """(status, site, index) of the bounds checks of a debug build (see
+    ssd_debug_bounds_status in ssd_scan.h); waits for the device."""
+    site, index = ctypes.c_int(0), ctypes.c_int64(-1)
+    rc = int(load().ssd_debug_bounds_status(ctypes.byref(site), ctypes.byref(index), 1 if clear else 0))
+    return rc, site.value, index.value
 
 
 def ssd_selftest_bounded_wait(workspace, spin_limit, stream=None) -> None:

@@ -22,6 +22,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libssdscan.so")
+# debug build: bounds predicates in the kernels (-DSSD_DEBUG_BOUNDS), separate objects and library
+DBG_BUILD_DIR = os.path.join(PKG, "_build_dbg")
+DBG_LIB_PATH = os.path.join(LIB_DIR, "libssdscan_dbg.so")
 
 SOURCES = ["ssd_api.cu", "decode.cu", "chunked_simt.cu", "chunked_tc.cu", "chunked_fused.cu", "diag.cu", "noalloc.cu", "chunk_policy.cu", "decode_layer.cu", "chunked_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,8 +41,10 @@ def nvcc() -> str:
     return p
 
 
-def _flags(verbose: bool):
+def _flags(verbose: bool, debug_bounds: bool = False):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    if debug_bounds:
+        f += ["-DSSD_DEBUG_BOUNDS"]
     if verbose:
         f += ["-Xptxas", "-v"]
     return f
@@ -57,12 +62,13 @@ def _stale(target: str, sources) -> bool:
     return any(os.path.getmtime(s) > t for s in sources)
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+def _compile(src: str, verbose: bool, debug_bounds: bool = False) -> str:
+    obj = os.path.join(DBG_BUILD_DIR if debug_bounds else BUILD_DIR,
+                       os.path.splitext(os.path.basename(src))[0] + ".o")
     if not _stale(obj, [src] + _deps()) and not verbose:
         return obj
     tmp = obj + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + _flags(verbose) + ["-c", src, "-o", tmp]
+    cmd = [nvcc()] + _flags(verbose, debug_bounds) + ["-c", src, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -72,22 +78,24 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    """Compiles and links libssdscan.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose: bool = False, debug_bounds: bool = False) -> str:
+    """Compiles and links libssdscan.so (with debug_bounds, the checked
+    libssdscan_dbg.so); returns its path."""
+    bdir, lib = (DBG_BUILD_DIR, DBG_LIB_PATH) if debug_bounds else (BUILD_DIR, LIB_PATH)
+    os.makedirs(bdir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    if _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug_bounds), srcs))
+    if _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

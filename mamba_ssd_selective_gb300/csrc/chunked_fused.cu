@@ -61,6 +61,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "debug_bounds.cuh"
 #include "launch.h"
 #include "ssd_scan.h"
 #include "tc_host.h"
@@ -366,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int64_t t = t0 + 4 * lane + q;
-                    dv[k][q] = t < a.L ? __bfloat162float(dtp[(b * a.L + t) * a.H + hg * kHB + k]) : 0.f;
+                    const int64_t o = (b * a.L + t) * a.H + hg * kHB + k;
+                    dv[k][q] = (t < a.L && SSD_IN_BOUNDS(o, 1, a.B * a.L * a.H, kSiteFusedDt)) ? __bfloat162float(dtp[o])
+                                                                                               : 0.f;
                 }
             const uint32_t par = it & 1;
             if (!pwait(&bars[BAR_SCAL_EMPTY + par], ((it >> 1) & 1) ^ 1, s_fail)) return false;
@@ -463,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 pwait(&bars[BAR_FLAG_OK], nfirst & 1, s_fail);
                 ++nfirst;
                 src = c > 0 ? prm.carry + st0 : (a.init_state ? a.init_state + st0 : nullptr);
-                if (*s_fail) src = nullptr;
+                if (*s_fail || !SSD_IN_BOUNDS(st0, (kP - 1) * kN + 1, a.B * a.H * kP * kN, kSiteFusedCarry))
+                    src = nullptr;
             } else {
                 tc::tc_fence_after();  // the previous chunk's MMA is complete (SC_FULL was waited for)
             }
@@ -507,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                     float hv2[32];
                     tc::tmem_ld32(tH + lq + hf * kP + 32 * s, hv2);
                     tc::tmem_ld_wait();
-                    if (!*s_fail) {
+                    if (!*s_fail && SSD_IN_BOUNDS(st0 + (int64_t)(32 * s) * kN, 31 * kN + 1, a.B * a.H * kP * kN,
+                                                  kSiteFusedCarry)) {
                         float *dst = prm.carry + st0 + (int64_t)(32 * s) * kN;
 #pragma unroll
                         for (int q = 0; q < 32; ++q) __stcg(dst + q * kN, hv2[q]);
@@ -534,7 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 int64_t b, sc;
                 int hg;
                 decode(U, b, sc, hg);
-                if (sc > 0 && !*s_fail) {
+                const int64_t n_flags = Bsz * nhg * nsc;
+                (void)n_flags;
+                if (sc > 0 && !*s_fail && SSD_IN_BOUNDS((b * nhg + hg) * nsc + (sc - 1), 1, n_flags, kSiteFusedFlags)) {
                     const int *fp = prm.flags + ((b * nhg + hg) * nsc + (sc - 1));
                     if (ld_acquire(fp) == 0) {
                         const uint64_t t0 = tc::global_ns();
@@ -549,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 }
                 tc::mbar_arrive(&bars[BAR_FLAG_OK]);
                 if (!pwait(&bars[BAR_CARRY_DONE], it & 1, s_fail)) break;
-                if (sc + 1 < nsc && !*s_fail) st_release(prm.flags + ((b * nhg + hg) * nsc + sc), 1);
+                if (sc + 1 < nsc && !*s_fail && SSD_IN_BOUNDS((b * nhg + hg) * nsc + sc, 1, n_flags, kSiteFusedFlags))
+                    st_release(prm.flags + ((b * nhg + hg) * nsc + sc), 1);
             }
         }
     } else {
@@ -682,6 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
 }
 
 }  // namespace
+
+SSD_BOUNDS_HOST_READER(bounds_word_fused)
 
 bool chunked_fused_supported(const ChunkedArgs &a) {
     if (a.io != IO_BF16 || a.P != kP || a.N != kN || a.Q != kQ) return false;

@@ -19,6 +19,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "debug_bounds.cuh"
 #include "launch.h"
 #include "ssd_scan.h"
 
@@ -395,6 +396,8 @@ cudaError_t launch_simt_t(const ChunkedArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
+SSD_BOUNDS_HOST_READER(bounds_word_simt)
+
 // Tensor-core path: bfloat16 chunk states in states_bf16, replaced in place by
 // the bfloat16 entering states; 2 elements per thread. Up to PF chunks are
 // loaded before the chain runs (one register per chunk), so that one round
@@ -428,12 +431,15 @@ __global__ void __launch_bounds__(kT, MINB) state_pass_bf16_kernel(ChunkedArgs a
         __syncthreads();
         if (!act) continue;
         uint32_t raw[PF];
+        const int64_t n_states = a.B * nc * H * PN, e0 = ((b * nc) * H + h) * PN + e;
+        (void)n_states; (void)e0;
 #pragma unroll
         for (int u = 0; u < PF; ++u)
-            if (c0 + u < nc) raw[u] = *reinterpret_cast<const uint32_t *>(base + (c0 + u) * stride);
+            if (c0 + u < nc && SSD_IN_BOUNDS(e0 + (c0 + u) * stride, 2, n_states, kSiteStatePass))
+                raw[u] = *reinterpret_cast<const uint32_t *>(base + (c0 + u) * stride);
 #pragma unroll
         for (int u = 0; u < PF; ++u) {
-            if (c0 + u < nc) {
+            if (c0 + u < nc && SSD_IN_BOUNDS(e0 + (c0 + u) * stride, 2, n_states, kSiteStatePass)) {
                 const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
                 *reinterpret_cast<__nv_bfloat162 *>(base + (c0 + u) * stride) = hv;
                 const float2 sv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[u]));

@@ -8,6 +8,7 @@
 // The state is touched once, with streaming cache hints, so it does not evict
 // the small per-token inputs from L2.
 #include "common.cuh"
+#include "debug_bounds.cuh"
 #include "launch.h"
 
 namespace ssd {
@@ -28,6 +29,10 @@ decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *
     const int h = (int)(bh % H);
     const int64_t b = bh / H;
     const int g = h / (H / G);
+    // extents of the buffers (the grid is B * H): state, x / y, B / C
+    const int64_t n_state = (int64_t)gridDim.x * P * N, n_io = (int64_t)gridDim.x * P;
+    const int64_t n_bc = (int64_t)(gridDim.x / H) * G * N;
+    (void)n_state; (void)n_io; (void)n_bc;
     const float dtv = to_f32(dt[bh]);
     const float alpha = expf(dtv * A[h]);
     const float Dh = D ? D[h] : 0.f;
@@ -43,21 +48,23 @@ decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *
         for (int r = 0; r < kRB; ++r) {
             const int p = p0 + r * nwarps;
             acc[r] = 0.f;
-            xp[r] = p < P ? to_f32(x[bh * P + p]) : 0.f;
+            xp[r] = (p < P && SSD_IN_BOUNDS(bh * P + p, 1, n_io, kSiteDecodeIO)) ? to_f32(x[bh * P + p]) : 0.f;
         }
         for (int n0 = lane * VW; n0 < N; n0 += 32 * VW) {
             float bv[VW], cv[VW];
 #pragma unroll
+            const bool bc_ok = SSD_IN_BOUNDS((b * G + g) * N + n0, VW, n_bc, kSiteDecodeIO);
+#pragma unroll
             for (int k = 0; k < VW; ++k) {
-                bv[k] = to_f32(Bp[n0 + k]);
-                cv[k] = to_f32(Cp[n0 + k]);
+                bv[k] = bc_ok ? to_f32(Bp[n0 + k]) : 0.f;
+                cv[k] = bc_ok ? to_f32(Cp[n0 + k]) : 0.f;
             }
             float hv[kRB][VW];
             // issue all loads of the row batch before any arithmetic
 #pragma unroll
             for (int r = 0; r < kRB; ++r) {
                 const int p = p0 + r * nwarps;
-                if (p < P) {
+                if (p < P && SSD_IN_BOUNDS(bh * P * N + (int64_t)p * N + n0, VW, n_state, kSiteDecodeState)) {
                     if constexpr (VW == 4) {
                         float4 v = __ldcs(reinterpret_cast<const float4 *>(st + (int64_t)p * N + n0));
                         hv[r][0] = v.x; hv[r][1] = v.y; hv[r][2] = v.z; hv[r][3] = v.w;
@@ -69,7 +76,7 @@ decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *
 #pragma unroll
             for (int r = 0; r < kRB; ++r) {
                 const int p = p0 + r * nwarps;
-                if (p < P) {
+                if (p < P && SSD_IN_BOUNDS(bh * P * N + (int64_t)p * N + n0, VW, n_state, kSiteDecodeState)) {
                     const float u = dtv * xp[r];
 #pragma unroll
                     for (int k = 0; k < VW; ++k) {
@@ -89,7 +96,8 @@ decode_step_kernel(float *__restrict__ state, const T *__restrict__ x, const T *
         for (int r = 0; r < kRB; ++r) {
             const float s = warp_sum(acc[r]);
             const int p = p0 + r * nwarps;
-            if (lane == 0 && p < P) y[bh * P + p] = from_f32<T>(s + Dh * xp[r]);
+            if (lane == 0 && p < P && SSD_IN_BOUNDS(bh * P + p, 1, n_io, kSiteDecodeIO))
+                y[bh * P + p] = from_f32<T>(s + Dh * xp[r]);
         }
     }
 }
@@ -112,6 +120,8 @@ cudaError_t launch_t(int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, floa
 }
 
 }  // namespace
+
+SSD_BOUNDS_HOST_READER(bounds_word_decode)
 
 cudaError_t launch_decode(int io, int64_t B, int64_t H, int64_t P, int64_t N, int64_t G, float *state,
                           const void *x, const void *dt, const float *A, const void *Bm, const void *Cm,

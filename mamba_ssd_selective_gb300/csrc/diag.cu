@@ -20,6 +20,7 @@
 // double-buffered so the next tile lands while this one is computed; y is
 // staged in shared memory and written back with 16-byte stores.
 #include "common.cuh"
+#include "debug_bounds.cuh"
 #include "launch.h"
 
 namespace ssd {
@@ -139,7 +140,8 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
         for (int u = 0; u < 2; ++u) {
             const int n = nb + 2 * jp + u;
             const bool on = valid && n < N;
-            hv[u] = (on && h_in) ? h_in[(b * Dm + d) * N + n] : 0.f;
+            hv[u] = (on && h_in && SSD_IN_BOUNDS((b * Dm + d) * N + n, 1, a.B * Dm * N, kSiteDiagState))
+                        ? h_in[(b * Dm + d) * N + n] : 0.f;
             av[u] = on ? a.A[d * N + n] * kLog2e : 0.f;
         }
         h2[jp] = pk2(hv[0], hv[1]);
@@ -155,17 +157,19 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
         constexpr int kV = CH / 8;  // 16-byte vectors per row
         for (int e = tid; e < kTT * kV; e += kThr) {
             const int tt = e / kV, v = e % kV;
-            const bool in = tt < tn && d0 + v * 8 < Dm;
-            const int64_t o = (b * L + t0 + (in ? tt : 0)) * Dm + d0 + (in ? v * 8 : 0);
-            cp_async16(&sx[s][tt][v * 8], x + o, in);
-            cp_async16(&sdt[s][tt][v * 8], dt + o, in);
-            if (has_z) cp_async16(&sz[s][tt][v * 8], zg + o, in);
+            const int64_t o = (b * L + t0 + tt) * Dm + d0 + v * 8;
+            const bool in = tt < tn && d0 + v * 8 < Dm && SSD_IN_BOUNDS(o, 8, a.B * L * Dm, kSiteDiagIO);
+            const int64_t oc = in ? o : (b * L + t0) * Dm + d0;  // a valid address when zero-filling
+            cp_async16(&sx[s][tt][v * 8], x + oc, in);
+            cp_async16(&sdt[s][tt][v * 8], dt + oc, in);
+            if (has_z) cp_async16(&sz[s][tt][v * 8], zg + oc, in);
         }
         constexpr int nv = NMAX / 8;
         for (int e = tid; e < kTT * nv; e += kThr) {
             const int tt = e / nv, v = e % nv;
-            const bool in = tt < tn && v * 8 < N;
-            const int64_t o = (b * L + t0 + (tt < tn ? tt : 0)) * N + (in ? v * 8 : 0);
+            const bool in = tt < tn && v * 8 < N &&
+                            SSD_IN_BOUNDS((b * L + t0 + tt) * N + v * 8, 8, a.B * L * N, kSiteDiagBC);
+            const int64_t o = (b * L + t0 + (in ? tt : 0)) * N + (in ? v * 8 : 0);
             cp_async16(&sB[s][tt][v * 8], Bm + o, in);
             cp_async16(&sC[s][tt][v * 8], Cm + o, in);
         }
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
             if (MODE != kLocal)
                 for (int e = tid; e < tn * kV; e += kThr) {
                     const int tt = e / kV, v = e % kV;
-                    if (d0 + v * 8 < Dm)
+                    if (d0 + v * 8 < Dm && SSD_IN_BOUNDS((b * L + t0 + tt) * Dm + d0 + v * 8, 8, a.B * L * Dm, kSiteDiagIO))
                         *reinterpret_cast<uint4 *>(y + (b * L + t0 + tt) * Dm + d0 + v * 8) =
                             *reinterpret_cast<const uint4 *>(&sy[tt][v * 8]);
                 }
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
     }
     pdl_trigger();
     float *h_out = MODE == kWhole ? a.final_state : MODE == kLocal ? a.ws_h + seg * a.B * Dm * N : nullptr;
-    if (h_out && valid) {
+    if (h_out && valid && SSD_IN_BOUNDS((b * Dm + d) * N + nb, imax(0, imin(NH, N - nb)), a.B * Dm * N, kSiteDiagState)) {
 #pragma unroll
         for (int jp = 0; jp < NH / 2; ++jp) {
             float h0, h1;
@@ -455,6 +459,8 @@ cudaError_t launch_bf16(const DiagArgs &a, cudaStream_t stream) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+SSD_BOUNDS_HOST_READER(bounds_word_diag)
 
 // Time segments: one pass per sequence keeps ~B * dim / 32 CTAs busy; when
 // that leaves the GPU mostly idle (fewer than kSegEnablePerSM threads per SM)

@@ -163,6 +163,13 @@ cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 
+// The bounds-check record of each translation unit with checked kernels (0
+// when nothing failed or in a release build); clear resets it.
+cudaError_t bounds_word_decode(unsigned long long *out, bool clear);
+cudaError_t bounds_word_diag(unsigned long long *out, bool clear);
+cudaError_t bounds_word_fused(unsigned long long *out, bool clear);
+cudaError_t bounds_word_simt(unsigned long long *out, bool clear);
+
 // Sets the thread-local text returned by ssd_last_error() and returns `status`.
 int set_error(int status, const char *fmt, ...);
 

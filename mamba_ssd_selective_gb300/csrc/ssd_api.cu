@@ -701,6 +701,36 @@ ssd_status ssd_workspace_status(const void *workspace, cudaStream_t stream) {
     return fail((ssd_status)word, "kernel recorded status %d", word);
 }
 
+ssd_status ssd_debug_bounds_status(int *site, int64_t *index, int clear) {
+#ifndef SSD_DEBUG_BOUNDS
+    (void)site;
+    (void)index;
+    (void)clear;
+    return fail(SSD_ERR_UNSUPPORTED, "this library was built without SSD_DEBUG_BOUNDS: no bounds checks run");
+#else
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_debug_bounds_status: synchronize");
+    cudaError_t (*readers[])(unsigned long long *, bool) = {ssd::bounds_word_decode, ssd::bounds_word_diag,
+                                                            ssd::bounds_word_fused, ssd::bounds_word_simt};
+    unsigned long long first = 0;
+    for (auto rd : readers) {
+        unsigned long long w = 0;
+        if ((e = rd(&w, clear != 0)) != cudaSuccess) return cuda_fail(e, "ssd_debug_bounds_status: read");
+        if (!first) first = w;
+    }
+    if (!first) {
+        if (site) *site = 0;
+        if (index) *index = -1;
+        return ok();
+    }
+    const int st = (int)((first >> 48) & 0xff);
+    const int64_t idx = (int64_t)(first & 0xffffffffffffull);
+    if (site) *site = st;
+    if (index) *index = idx;
+    return fail(SSD_ERR_BOUNDS, "bounds check failed at site %d, element %lld", st, (long long)idx);
+#endif
+}
+
 ssd_status ssd_selftest_bounded_wait(void *workspace, int spin_limit, cudaStream_t stream) {
     if (!workspace) return fail(SSD_ERR_INVALID_ARG, "workspace is NULL");
     if (!aligned(workspace, 16)) return fail(SSD_ERR_INVALID_ARG, "workspace is not 16-byte aligned");

@@ -235,3 +235,22 @@ def test_tensor_core_probe_compiles(tmp_path):
                                    "-I", nvbuild.INCLUDE, src, "-o", str(tmp_path / "libtcprobe.so")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+def test_debug_bounds_status_in_a_release_build(lib):
+    """The release library runs no bounds checks and says so, without a CUDA call."""
+    from mamba_ssd_selective_gb300 import binding
+    site, index = ctypes.c_int(7), ctypes.c_int64(7)
+    assert lib.ssd_debug_bounds_status(ctypes.byref(site), ctypes.byref(index), 0) == binding.SSD_ERR_UNSUPPORTED
+    assert b"SSD_DEBUG_BOUNDS" in lib.ssd_last_error()
+
+
+def test_debug_bounds_translation_units_compile(tmp_path):
+    """Every translation unit with bounds predicates compiles with -DSSD_DEBUG_BOUNDS (nvcc, sm_103a)."""
+    from mamba_ssd_selective_gb300 import build
+    import subprocess
+    for src in ("decode.cu", "diag.cu", "chunked_fused.cu", "chunked_simt.cu", "ssd_api.cu"):
+        cmd = [build.nvcc()] + build._flags(False, True) + ["-c", os.path.join(build.CSRC, src), "-o",
+                                                            str(tmp_path / (src + ".o"))]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr[-2000:]
