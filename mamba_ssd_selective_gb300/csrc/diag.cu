@@ -157,12 +157,13 @@ __global__ void __launch_bounds__(TPC * CH) diag_scan_bf16_kernel(const __grid_c
         constexpr int kV = CH / 8;  // 16-byte vectors per row
         for (int e = tid; e < kTT * kV; e += kThr) {
             const int tt = e / kV, v = e % kV;
-            const int64_t o = (b * L + t0 + tt) * Dm + d0 + v * 8;
-            const bool in = tt < tn && d0 + v * 8 < Dm && SSD_IN_BOUNDS(o, 8, a.B * L * Dm, kSiteDiagIO);
-            const int64_t oc = in ? o : (b * L + t0) * Dm + d0;  // a valid address when zero-filling
-            cp_async16(&sx[s][tt][v * 8], x + oc, in);
-            cp_async16(&sdt[s][tt][v * 8], dt + oc, in);
-            if (has_z) cp_async16(&sz[s][tt][v * 8], zg + oc, in);
+            const bool in = tt < tn && d0 + v * 8 < Dm &&
+                            SSD_IN_BOUNDS((b * L + t0 + tt) * Dm + d0 + v * 8, 8, a.B * L * Dm, kSiteDiagIO);
+            // a valid address when zero-filling
+            const int64_t o = (b * L + t0 + (in ? tt : 0)) * Dm + d0 + (in ? v * 8 : 0);
+            cp_async16(&sx[s][tt][v * 8], x + o, in);
+            cp_async16(&sdt[s][tt][v * 8], dt + o, in);
+            if (has_z) cp_async16(&sz[s][tt][v * 8], zg + o, in);
         }
         constexpr int nv = NMAX / 8;
         for (int e = tid; e < kTT * nv; e += kThr) {
