@@ -42,12 +42,13 @@
 //                reads it after the chain group has scaled it in place by w,
 //                and again (from L2, microseconds later) for S' X
 //   warp 1       MMA issuer (one lane)
-//   warp 2       TMA store of y, one head at a time, staged in shared memory
+//   warp 2       idle
 //   warp 3       per-item scalars: cumulative sums of dt A (base 2), decays
 //   warps 4-11   chain group, one item ahead of the output group: w o x, the
 //                carried state in (alpha h_in into TMEM, h_in as bf16 for Yo),
 //                the next state out
-//   warps 12-19  output group: S', the Yo rescale and y
+//   warps 12-19  output group: S', the Yo rescale and y (each warp stores its
+//                32 x 32 part of a head's y tile with its own TMA store)
 //   warp 20      chain flags: waits for the flag of the item's predecessor
 //                (ahead of the chain group), and sets the item's own flag once
 //                every chain-group store of its last state is done, so that
@@ -79,7 +80,7 @@ constexpr int kThreads = 32 * kOutWarp0 + kGroupThreads + 32;  // 21 warps, 80 r
 
 struct FusedParams {
     ChunkedArgs a;
-    CUtensorMap mx, mb, mc, my;
+    CUtensorMap mx, mb, mc, my;  // my: y in boxes of 32 rows x 32 columns (one output warp's part)
     int nhg;          // head pairs, H / 2
     int gc;           // chunks per work item
     int64_t nsc;      // work items per chain, ceil(nc / gc)
@@ -93,8 +94,8 @@ constexpr uint32_t kOffC = 0;          // 2 x 32 KB: C tiles (chunk & 1), K-majo
 constexpr uint32_t kOffB = 65536;      // 32 KB: B tile (K-major for S, MN-major for the chunk state)
 constexpr uint32_t kOffX = 98304;      // 4 x 16 KB: x tiles, slot 2 (chunk & 1) + k; the two slots of a
                                        // chunk are the N = (k, p) panels of the chunk-state B operand
-constexpr uint32_t kOffH = 163840;     // 32 KB: h_in bf16, rows (k, p), 2 panels of n
-constexpr uint32_t kOffY = 196608;     // 16 KB: y of one head, 128-byte swizzle
+constexpr uint32_t kOffH = 163840;     // 32 KB: h_in bf16, rows n, 2 panels (k) of 64 p
+constexpr uint32_t kOffY = 196608;     // 8 x 2 KB: y staging of each output warp, 64-byte swizzle
 constexpr uint32_t kOffS = 212992;     // scalars, two item buffers
 constexpr int kScal = 5 * kHB * kQ + 2 * kHB;  // cs | dt | colf | sc | w, then D, alpha
 constexpr uint32_t kOffBar = kOffS + 2 * kScal * 4;
@@ -119,11 +120,9 @@ enum {
     BAR_ACC_EMPTY = 31,
     BAR_SCAL_FULL = 32,   // [2]
     BAR_SCAL_EMPTY = 34,  // [2]
-    BAR_YS_FULL = 36,
-    BAR_YS_EMPTY = 37,
-    BAR_CARRY_DONE = 38,
-    BAR_FLAG_OK = 39,
-    kBars = 40
+    BAR_CARRY_DONE = 36,
+    BAR_FLAG_OK = 37,
+    kBars = 38
 };
 constexpr uint32_t kSmemBytes = kOffBar + kBars * 8 + 16 + 1024;
 
@@ -203,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
 
     if (tid == 0) {
         for (int k = 0; k < kBars; ++k) tc::mbar_init(bars + k, 1);
-        const int group_counted[] = {BAR_S_EMPTY,   BAR_WX_FULL, BAR_HIN_FULL,  BAR_P_FULL,
-                                     BAR_P_FULL + 1, BAR_ACC_EMPTY, BAR_YS_FULL, BAR_CARRY_DONE};
+        const int group_counted[] = {BAR_S_EMPTY,    BAR_WX_FULL,   BAR_HIN_FULL,  BAR_P_FULL,
+                                     BAR_P_FULL + 1, BAR_ACC_EMPTY, BAR_CARRY_DONE};
         for (int k : group_counted) tc::mbar_init(bars + k, kGroupThreads);
         tc::mbar_init(bars + BAR_SCAL_EMPTY, 2 * kGroupThreads);
         tc::mbar_init(bars + BAR_SCAL_EMPTY + 1, 2 * kGroupThreads);
@@ -275,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
         if (lane == 0) {
             const uint32_t idS = tc::idesc_bf16(128, 128, false, false);
             const uint32_t idH = tc::idesc_bf16(128, 128, true, true);
-            const uint32_t idO = tc::idesc_bf16(128, 128, false, false);
+            const uint32_t idO = tc::idesc_bf16(128, 128, false, true);
             const uint32_t idY = tc::idesc_bf16(128, kP, false, true);
             const uint32_t b0 = tc::smem_u32(sB);
             const uint32_t h0 = tc::smem_u32(sH);
@@ -310,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 tc::tc_fence_after();
                 for (int k = 0; k < kN; k += 16) {
                     const uint64_t da = tc::sdesc_sw128(c0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
-                    const uint64_t db = tc::sdesc_sw128(h0 + (k >> 6) * 16384 + (k & 63) * 2, 16, 1024);
+                    const uint64_t db = tc::sdesc_sw128(h0 + k * 128, 16384, 1024);
                     tc::mma_bf16(tY, da, db, idO, k > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&bars[BAR_YO_FULL]);
@@ -334,21 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
             });
         }
     } else if (warp == 2) {
-        // ------------------------------------------------- TMA store of y
-        if (lane == 0) {
-            uint32_t ny = 0;
-            for_chunks([&](int64_t b, int64_t c, int hg, uint32_t, bool, bool) -> bool {
-                for (int k = 0; k < kHB; ++k, ++ny) {
-                    if (!pwait(&bars[BAR_YS_FULL], ny & 1, s_fail)) return false;
-                    tc::tma_store_3d(&prm.my, sY, (hg * kHB + k) * kP, (int)(c * kQ), (int)b);
-                    tc::bulk_commit();
-                    tc::bulk_wait_read_all();  // sY may be written again
-                    tc::mbar_arrive(&bars[BAR_YS_EMPTY]);
-                }
-                return true;
-            });
-            tc::bulk_wait_all();
-        }
+        // idle (every other branch below is taken by its own warps only)
     } else if (warp == 3) {
         // ---------------------------------------------------- per-item scalars
         // For both heads k and chunk rows i (base-2 units; lane l owns rows 4l..4l+3):
@@ -487,10 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
 #pragma unroll
                     for (int q = 0; q < 32; ++q) hv[q] = 0.f;
                 }
+                // row n of head hf's panel (p contiguous, 128-byte swizzle): four
+                // 16-byte pieces of eight p each
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    *reinterpret_cast<__nv_bfloat16 *>(sH + tc::sw128_offset(hf * kP + 32 * s2 + q, nn, 128)) =
-                        __float2bfloat16_rn(hv[q]);
+                for (int u = 0; u < 4; ++u) {
+                    const int piece = 4 * s2 + u;
+                    *reinterpret_cast<uint4 *>(sH + hf * 16384 + nn * 128 + ((piece ^ (nn & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(hv[8 * u], hv[8 * u + 1]), pack_bf16x2(hv[8 * u + 2], hv[8 * u + 3]),
+                                   pack_bf16x2(hv[8 * u + 4], hv[8 * u + 5]), pack_bf16x2(hv[8 * u + 6], hv[8 * u + 7]));
+                }
                 uint32_t r[32];
 #pragma unroll
                 for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(al * hv[q]);
@@ -580,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 }
             tc::tmem_st_wait();
         }
-        uint32_t ny = 0;
-        for_chunks([&](int64_t, int64_t, int, uint32_t it, bool, bool) -> bool {
+        uint8_t *ybuf = sY + (warp - kOutWarp0) * 2048;
+        for_chunks([&](int64_t b, int64_t c, int hg, uint32_t it, bool, bool) -> bool {
             const uint32_t par = it & 1, ph = it & 1, ph2 = (it >> 1) & 1;
             pwait(&bars[BAR_SCAL_FULL + par], ph2, s_fail);
             const float *base = s_scal + par * kScal;
@@ -598,6 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 {
                     float vd[16];
                     tc::tmem_ld16(tS + lq + qd * 32 + 16 * ho, vd);
+                    float csv[16], dtv[16];  // columns of the diagonal block, four at a time
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 a4 = reinterpret_cast<const float4 *>(cs_ + qd * 32 + 16 * ho)[u];
+                        const float4 d4 = reinterpret_cast<const float4 *>(dt_ + qd * 32 + 16 * ho)[u];
+                        csv[4 * u] = a4.x, csv[4 * u + 1] = a4.y, csv[4 * u + 2] = a4.z, csv[4 * u + 3] = a4.w;
+                        dtv[4 * u] = d4.x, dtv[4 * u + 1] = d4.y, dtv[4 * u + 2] = d4.z, dtv[4 * u + 3] = d4.w;
+                    }
                     tc::tmem_ld_wait();
                     uint32_t pk[8];
 #pragma unroll
@@ -605,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                         float f[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int cc = 16 * ho + q + e, jr = qd * 32 + cc;
-                            const float d = tc::ex2(fminf(cs_i - cs_[jr], 0.f)) * dt_[jr];
+                            const int cc = 16 * ho + q + e;
+                            const float d = tc::ex2(fminf(cs_i - csv[q + e], 0.f)) * dtv[q + e];
                             f[e] = cc <= lane ? vd[q + e] * d : 0.f;
                             f[e] += cc == lane ? Dh : 0.f;
                         }
@@ -624,13 +622,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                     if (J >= qd) continue;
                     float v[32];
                     tc::tmem_ld32(tS + lq + J * 32, v);
-                    tc::tmem_ld_wait();
                     const float rf = tc::ex2(cs_i - cs_[J * 32 + 31]);
+                    tc::tmem_ld_wait();
                     uint32_t pkd[16];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        pkd[q] = pack_bf16x2(v[2 * q] * rf * cf_[J * 32 + 2 * q],
-                                             v[2 * q + 1] * rf * cf_[J * 32 + 2 * q + 1]);
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 c4 = reinterpret_cast<const float4 *>(cf_ + J * 32)[q];
+                        pkd[2 * q] = pack_bf16x2(v[4 * q] * (rf * c4.x), v[4 * q + 1] * (rf * c4.y));
+                        pkd[2 * q + 1] = pack_bf16x2(v[4 * q + 2] * (rf * c4.z), v[4 * q + 3] * (rf * c4.w));
+                    }
                     tc::tmem_st16(tP + lq + k * 64 + J * 16, pkd);
                 }
                 tc::tmem_st_wait();
@@ -654,25 +654,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 tc::tc_fence_before();
                 tc::mbar_arrive(&bars[BAR_P_FULL + k]);
             }
-            // y_k: 32 rows x 32 columns of this warp, staged for the TMA store
+            // y_k: 32 rows x 32 columns of this warp, staged in the warp's own
+            // 2 KB (64-byte swizzle: 16-byte piece h of row r at h ^ (r / 2 % 4))
+            // and written by the warp's own TMA store
 #pragma unroll 1
-            for (int k = 0; k < kHB; ++k, ++ny) {
+            for (int k = 0; k < kHB; ++k) {
                 pwait(&bars[BAR_Y_FULL + k], ph, s_fail);
                 tc::tc_fence_after();
                 float yv[32];
                 tc::tmem_ld32(tY + lq + k * 64 + 32 * ho, yv);
                 tc::tmem_ld_wait();
-                pwait(&bars[BAR_YS_EMPTY], (ny & 1) ^ 1, s_fail);  // the previous head has left sY
-                uint8_t *yrow = sY + i * 128;
+                if (lane == 0) tc::bulk_wait_read_all();  // the warp's previous store has read ybuf
+                __syncwarp();
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const int q = h * 8;
                     const uint4 pk = make_uint4(pack_bf16x2(yv[q], yv[q + 1]), pack_bf16x2(yv[q + 2], yv[q + 3]),
                                                 pack_bf16x2(yv[q + 4], yv[q + 5]), pack_bf16x2(yv[q + 6], yv[q + 7]));
-                    *reinterpret_cast<uint4 *>(yrow + (((4 * ho + h) ^ (i & 7)) << 4)) = pk;
+                    *reinterpret_cast<uint4 *>(ybuf + lane * 64 + ((h ^ ((lane >> 1) & 3)) << 4)) = pk;
                 }
                 tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&bars[BAR_YS_FULL]);
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_3d(&prm.my, ybuf, (hg * kHB + k) * kP + 32 * ho, (int)(c * kQ) + 32 * qd, (int)b);
+                    tc::bulk_commit();
+                }
             }
             tc::tc_fence_before();
             tc::mbar_arrive(&bars[BAR_ACC_EMPTY]);
@@ -680,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
             return true;
         });
         tc::tc_fence_before();
+        if (lane == 0) tc::bulk_wait_all();  // the warp's last store is complete
     }
     __syncthreads();
     if (tid == 0 && *s_fail) atomicCAS(a.status, SSD_OK, SSD_ERR_TIMEOUT);
@@ -732,7 +739,7 @@ cudaError_t launch_chunked_fused(const ChunkedArgs &a, cudaStream_t stream) {
     ok &= tma_map_tokens(&p.mx, a.x, a.H * a.P, a.L, a.B, kQ);
     ok &= tma_map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kQ);
     ok &= tma_map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kQ);
-    ok &= tma_map_tokens(&p.my, a.y, a.H * a.P, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.my, a.y, a.H * a.P, a.L, a.B, 32, 32);
     if (!ok) return cudaErrorInvalidValue;
     p.nhg = (int)(a.H / kHB);
     p.gc = fused_chunks_per_item(a);

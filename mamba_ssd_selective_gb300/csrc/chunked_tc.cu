@@ -1011,8 +1011,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor map with the 128-byte swizzle; dims/strides innermost first,
-// strides in bytes for dims 1..rank-1.
+// bf16 tensor map, 128-byte swizzle for 64-column boxes and 64-byte swizzle
+// for 32-column boxes; dims/strides innermost first, strides in bytes for
+// dims 1..rank-1.
 struct MapKey {
     const void *base;
     int rank;
@@ -1055,7 +1056,7 @@ bool make_map(CUtensorMap *out, const MapKey &k) {
     CUtensorMap m;
     CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)k.rank, const_cast<void *>(k.base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B,
+                     k.box[0] >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lock(g_map_mu);
@@ -1069,7 +1070,8 @@ bool make_map(CUtensorMap *out, const MapKey &k) {
 
 // (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (box_cols, box_rows, 1);
 // 128-byte swizzle for 64-column boxes, 64-byte swizzle for 32-column boxes
-bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows) {
+bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
+                int box_cols = 64) {
     MapKey k{};
     k.base = base;
     k.rank = 3;
@@ -1078,7 +1080,7 @@ bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, in
     k.dims[2] = (uint64_t)B;
     k.strides[0] = (uint64_t)inner * 2;
     k.strides[1] = (uint64_t)inner * L * 2;
-    k.box[0] = 64;
+    k.box[0] = (uint32_t)box_cols;
     k.box[1] = (uint32_t)box_rows;
     k.box[2] = 1;
     return make_map(out, k);
@@ -1128,8 +1130,9 @@ cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream
 
 }  // namespace
 
-bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows) {
-    return map_tokens(out, base, inner, L, B, box_rows);
+bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
+                    int box_cols) {
+    return map_tokens(out, base, inner, L, B, box_rows, box_cols);
 }
 
 int device_cc_major_cached() { return device_cc_major(); }

@@ -7,9 +7,11 @@
 
 namespace ssd {
 
-// (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (64, box_rows, 1),
-// 128-byte swizzle; encoded once per (pointer, shape) and cached.
-bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows);
+// (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (box_cols, box_rows, 1):
+// 64 columns with the 128-byte swizzle or 32 columns with the 64-byte swizzle;
+// encoded once per (pointer, shape, box) and cached.
+bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
+                    int box_cols = 64);
 
 // Major compute capability of the current device (cached per device), -1 if unknown.
 int device_cc_major_cached();
