@@ -457,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                 tc::tc_fence_after();  // the previous chunk's MMA is complete (SC_FULL was waited for)
             }
             // in two halves of 32 p: h_in as bf16 into the B operand of Yo
-            // (row (k, p), column n) and alpha h_in into TMEM, where the
-            // chunk-state MMA accumulates
+            // (row n, columns (k, p), 16-byte stores) and alpha h_in into
+            // TMEM, where the chunk-state MMA accumulates
 #pragma unroll 1
             for (int s2 = 0; s2 < 2; ++s2) {
                 float hv[32];
