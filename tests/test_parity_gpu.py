@@ -522,7 +522,8 @@ def _layer_case(Bz, H, P, N, G, W, io, steps, seed=7):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("shape", [(2, 4, 64, 128, 2, 4, 128), (3, 6, 32, 16, 3, 3, 96), (1, 128, 64, 128, 8, 4, 8192)])
+@pytest.mark.parametrize("shape", [(2, 4, 64, 128, 2, 4, 128), (3, 6, 32, 16, 3, 3, 96), (1, 128, 64, 128, 8, 4, 8192),
+                                   (2, 8, 64, 128, 1, 4, 64), (16, 80, 64, 128, 1, 4, 5120)])
 def test_decode_layer_steps_match_oracle(ssd, io, shape):
     """Eight layer steps (conv + silu, SSD decode step, gated norm): every
     output element each step and both states at the end, against the oracle."""
