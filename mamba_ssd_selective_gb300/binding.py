@@ -223,10 +223,11 @@ def ssd_scan_chunked(x, dt, A, B, C, D=None, init_state=None, chunk_size=None, y
 
 
 def ssd_scan_chunked_bwd(x, dt, A, B, C, dy, D=None, init_state=None, dfinal_state=None, workspace=None,
-                         stream=None, want_dinit=True):
+                         stream=None, want_dinit=True, simt=False):
     """Gradients of <dy, y> + <dfinal_state, final_state> for ssd_scan_chunked's
     inputs. Returns a dict of float32 tensors dx, ddt, dA, dB, dC, dD (None when
-    D is None) and dinit (None unless want_dinit)."""
+    D is None) and dinit (None unless want_dinit). simt=True keeps the
+    per-chunk gradients on the CUDA cores where the tensor cores would take them."""
     if x.dim() != 4 or B.dim() != 4:
         raise ValueError("x must be [B,L,H,P] and B, C [B,L,G,N]")
     Bsz, L, H, P = x.shape
@@ -246,7 +247,7 @@ def ssd_scan_chunked_bwd(x, dt, A, B, C, dy, D=None, init_state=None, dfinal_sta
              dB=torch.empty((Bsz, L, G, N), **f32), dC=torch.empty((Bsz, L, G, N), **f32),
              dD=torch.empty(H, **f32) if D is not None else None,
              dinit=torch.empty((Bsz, H, P, N), **f32) if want_dinit else None)
-    d = _dims(Bsz, L, H, P, N, G, _io_code(io))
+    d = _dims(Bsz, L, H, P, N, G, _io_code(io), SSD_FLAG_SIMT if simt else 0)
     lib = load()
     need = int(lib.ssd_scan_chunked_bwd_workspace_size(ctypes.byref(d)))
     if need == 0:

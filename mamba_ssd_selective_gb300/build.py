@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libssdscan.so")
 DBG_BUILD_DIR = os.path.join(PKG, "_build_dbg")
 DBG_LIB_PATH = os.path.join(LIB_DIR, "libssdscan_dbg.so")
 
-SOURCES = ["ssd_api.cu", "decode.cu", "chunked_simt.cu", "chunked_tc.cu", "chunked_fused.cu", "diag.cu", "noalloc.cu", "chunk_policy.cu", "decode_layer.cu", "chunked_bwd.cu"]
+SOURCES = ["ssd_api.cu", "decode.cu", "chunked_simt.cu", "chunked_tc.cu", "chunked_fused.cu", "diag.cu", "noalloc.cu", "chunk_policy.cu", "decode_layer.cu", "chunked_bwd.cu", "chunked_bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

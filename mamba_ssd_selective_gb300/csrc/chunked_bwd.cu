@@ -40,68 +40,73 @@ constexpr int kT = 256;
 constexpr int kQ = BwdArgs::kChunk;  // 64 tokens per backward chunk
 
 
-// Adjoint chunk state of one (b, c, h) and one 64x64 tile of (p, n).
-template <typename T>
+// Adjoint chunk state of one (b, c, h) and one 64x64 tile of (p, n), for
+// chunks of Q tokens (64 or 128: the dt scan covers the chunk, the sum runs
+// over sub-tiles of 64 tokens staged in shared memory in turn).
+template <typename T, int Q>
 __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_constant__ BwdArgs a, int tilesP,
                                                              int tilesN) {
+    static_assert(Q % 64 == 0 && Q <= 256, "chunks of 64-token sub-tiles");
     const int c = blockIdx.x;
     const int tiles = tilesP * tilesN;
     const int h = blockIdx.y / tiles, pt = (blockIdx.y % tiles) / tilesN, nt = blockIdx.y % tilesN;
     const int64_t b = blockIdx.z;
     const int64_t L = a.L, H = a.H, P = a.P, N = a.N, G = a.G;
     const int g = (int)(h / (H / G));
-    const int64_t t0 = (int64_t)c * kQ;
-    const int Qv = (int)imin<int64_t>(kQ, L - t0);
+    const int64_t t0 = (int64_t)c * Q;
+    const int Qv = (int)imin<int64_t>(Q, L - t0);
     const T *dy = static_cast<const T *>(a.dy), *Cm = static_cast<const T *>(a.Cm);
     const T *dt = static_cast<const T *>(a.dt);
-    __shared__ float s_cs[256], s_e[kQ], scratch[8];
-    __shared__ __align__(16) float Ys[kQ][68], Cs[kQ][68];  // 16-byte aligned rows
+    __shared__ float s_cs[256], s_e[Q], scratch[8];
+    __shared__ __align__(16) float Ys[64][68], Cs[64][68];  // 16-byte aligned rows
     const int tid = threadIdx.x;
-    // the dy and C tiles: with P and N multiples of 4, four 16-byte vectors of
-    // each per thread, all in flight across the dt scan; else element by element
     const bool vec = P % 4 == 0 && N % 4 == 0;
-    constexpr int kU = kQ * 16 / kT;
-    float4 yv[kU], cv[kU];
-    if (vec) {
-        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int e = tid + u * kT, j = e / 16, q = (e % 16) * 4;
-            const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j;
-            yv[u] = (j < Qv && p < P) ? ld4(dy + (tok * H + h) * P + p) : z4;
-            cv[u] = (j < Qv && n < N) ? ld4(Cm + (tok * G + g) * N + n) : z4;
-        }
-    }
     const float d = (tid < Qv) ? to_f32(dt[(b * L + t0 + tid) * H + h]) : 0.f;
-    block_inclusive_scan_256(d * a.A[h], kQ, s_cs, scratch);
-    if (tid < kQ) s_e[tid] = expf(s_cs[tid]);
-    if (vec) {
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int e = tid + u * kT, j = e / 16, q = (e % 16) * 4;
-            *reinterpret_cast<float4 *>(&Ys[j][q]) = yv[u];
-            *reinterpret_cast<float4 *>(&Cs[j][q]) = cv[u];
-        }
-    } else {
-        for (int e = tid; e < kQ * 64; e += kT) {
-            const int j = e / 64, q = e % 64;
-            const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j;
-            Ys[j][q] = (j < Qv && p < P) ? to_f32(dy[(tok * H + h) * P + p]) : 0.f;
-            Cs[j][q] = (j < Qv && n < N) ? to_f32(Cm[(tok * G + g) * N + n]) : 0.f;
-        }
-    }
-    __syncthreads();
+    block_inclusive_scan_256(d * a.A[h], Q, s_cs, scratch);
+    if (tid < Q) s_e[tid] = expf(s_cs[tid]);
     const int ty = tid / 16, tx = tid % 16;
     float acc[4][4] = {};
-    for (int j = 0; j < Qv; ++j) {
-        const float w = s_e[j];
-        const float4 y4 = *reinterpret_cast<const float4 *>(&Ys[j][ty * 4]);
-        const float4 c4 = *reinterpret_cast<const float4 *>(&Cs[j][tx * 4]);
-        const float ya[4] = {w * y4.x, w * y4.y, w * y4.z, w * y4.w}, cb[4] = {c4.x, c4.y, c4.z, c4.w};
+    for (int j0 = 0; j0 < Qv; j0 += 64) {
+        // the dy and C rows of this sub-tile: with P and N multiples of 4, four
+        // 16-byte vectors of each per thread; else element by element
+        if (vec) {
+            constexpr int kU = 64 * 16 / kT;
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 yv[kU], cv[kU];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+            for (int u = 0; u < kU; ++u) {
+                const int e = tid + u * kT, j = e / 16, q = (e % 16) * 4;
+                const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j0 + j;
+                yv[u] = (j0 + j < Qv && p < P) ? ld4(dy + (tok * H + h) * P + p) : z4;
+                cv[u] = (j0 + j < Qv && n < N) ? ld4(Cm + (tok * G + g) * N + n) : z4;
+            }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(ya[i], cb[k], acc[i][k]);
+            for (int u = 0; u < kU; ++u) {
+                const int e = tid + u * kT, j = e / 16, q = (e % 16) * 4;
+                *reinterpret_cast<float4 *>(&Ys[j][q]) = yv[u];
+                *reinterpret_cast<float4 *>(&Cs[j][q]) = cv[u];
+            }
+        } else {
+            for (int e = tid; e < 64 * 64; e += kT) {
+                const int j = e / 64, q = e % 64;
+                const int64_t p = (int64_t)pt * 64 + q, n = (int64_t)nt * 64 + q, tok = b * L + t0 + j0 + j;
+                Ys[j][q] = (j0 + j < Qv && p < P) ? to_f32(dy[(tok * H + h) * P + p]) : 0.f;
+                Cs[j][q] = (j0 + j < Qv && n < N) ? to_f32(Cm[(tok * G + g) * N + n]) : 0.f;
+            }
+        }
+        __syncthreads();
+        const int jn = imin(64, Qv - j0);
+        for (int j = 0; j < jn; ++j) {
+            const float w = s_e[j0 + j];
+            const float4 y4 = *reinterpret_cast<const float4 *>(&Ys[j][ty * 4]);
+            const float4 c4 = *reinterpret_cast<const float4 *>(&Cs[j][tx * 4]);
+            const float ya[4] = {w * y4.x, w * y4.y, w * y4.z, w * y4.w}, cb[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(ya[i], cb[k], acc[i][k]);
+        }
+        __syncthreads();  // the sub-tile is read before the next one replaces it
     }
     float *S = a.adj + (((b * a.nc + c) * H + h) * P) * N;
 #pragma unroll
@@ -709,8 +714,11 @@ __global__ void __launch_bounds__(kT) bwd_reduce_kernel(const __grid_constant__ 
 template <typename T>
 cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     const int tilesP = (int)((a.P + 63) / 64), tilesN = (int)((a.N + 63) / 64);
-    adj_chunk_state_kernel<T><<<dim3((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B), kT, 0,
-                                stream>>>(a, tilesP, tilesN);
+    const dim3 agrid((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B);
+    if (a.Q == 128)
+        adj_chunk_state_kernel<T, 128><<<agrid, kT, 0, stream>>>(a, tilesP, tilesN);
+    else
+        adj_chunk_state_kernel<T, 64><<<agrid, kT, 0, stream>>>(a, tilesP, tilesN);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // float4 elements when every (b, c, h) block of P*N states and the optional
@@ -725,6 +733,13 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
         adj_state_pass_kernel<1><<<dim3((unsigned)((PN + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
                                    stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.Q == 128) {
+        // chunks of 128 tokens: the per-chunk gradients on the tensor cores
+        if ((e = launch_chunk_bwd_tc(a, stream)) != cudaSuccess) return e;
+        const int64_t n = imax<int64_t>(a.B * a.L * a.G * a.N, a.H);
+        bwd_reduce_kernel<<<(unsigned)((n + kT - 1) / kT), kT, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
     const size_t smem = (size_t)ChunkSmem::total * sizeof(float);
     static DeviceOnce configured;  // set the attribute once per device
     int dev = 0;

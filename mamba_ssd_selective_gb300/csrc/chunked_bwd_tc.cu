@@ -1,0 +1,494 @@
+// Per-chunk gradients of the chunked SSD scan on the tensor cores: bf16
+// inputs, headdim P = 64, d_state N = 128, chunks of Q = 128 tokens.
+//
+// The algebra is that of chunk_bwd_kernel (chunked_bwd.cu, where it is
+// written out): for one (b, chunk, head), with cs the inclusive cumulative
+// sum of dt A in the chunk, e = exp(cs), eend = exp(cs_end - cs),
+// Ld[t,s] = exp(cs_t - cs_s) for s <= t (else 0), h_in the state entering the
+// chunk and Gn the cotangent of the state leaving it,
+//
+//   M1 = Ld o (C B^T),  M2 = Ld o (dY X^T) o dt_s,  W = M1 o (dY X^T) o dt_s
+//   du = M1^T dY + eend o (B Gn^T)          dx  = dt o du + D dY
+//   dB = M2^T C + (dt eend) o (X Gn)        dC  = M2 B + e o (dY h_in)
+//   d cs_t = sum_{s<t} W[t,s] - sum_{t'>t} W[t',t] + e_t dY_t . (h_in C_t) - r_t,
+//   r_s = eend_s dt_s x_s . (Gn B_s), the last token also taking
+//   sum_s r_s + exp(cs_end) <Gn, h_in>; da = suffix sums of d cs,
+//   ddt = da A + x . du, dA = sum da dt, dD = sum dY . x.
+//
+// Eleven tcgen05 MMA groups in three phases, float32 accumulators in TMEM
+// (512 columns), operands bf16 in shared memory with the 128-byte swizzle
+// (rows of 64 elements; the same tile serves as a K-major or an MN-major
+// operand depending on the product):
+//   phase 1  CB = C B^T, YX = dY X^T (rows t), HC = C h_in^T, GB = B Gn^T
+//   phase 2  BC = B C^T, XY = X dY^T (rows s: the transposed scores)
+//   phase 3  du = M1^T dY, dB = M2^T C + Xs Gn (Xs = x scaled by dt eend per
+//            row), dC^T = B^T M2^T and (dY h_in)^T (rows n)
+// The epilogues run on the CUDA cores in float32, a thread per TMEM lane
+// (row) and two threads per row (column halves): the row sums of W from the
+// phase-1 rows, M1^T and M2^T (bf16, the phase-3 A operands) and the column
+// sums of W from the phase-2 rows, then the gradients. h_in and Gn enter the
+// products rounded to bf16 (as do M1 and M2); <Gn, h_in> and every
+// elementwise step stay float32. Sums run in a fixed order (no atomics).
+#include <cuda.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+#include "ssd_scan.h"
+#include "tc_host.h"
+#include "tc_ptx.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kQ = 128, kP = 64, kN = 128, kThreads = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct BwdTcParams {
+    BwdArgs a;
+    CUtensorMap mx, mdy, mb, mc;
+};
+
+// shared memory (bytes from the 1024-aligned base)
+constexpr uint32_t kOffC = 0;        // C  [128 t][128 n]: 2 panels of n (16 KB each)
+constexpr uint32_t kOffB = 32768;    // B  [128 s][128 n]
+constexpr uint32_t kOffX = 65536;    // x  [128 t][64 p]
+constexpr uint32_t kOffY = 81920;    // dy [128 t][64 p]
+constexpr uint32_t kOffHin = 98304;  // h_in [64 p][128 n]: 2 panels of n (8 KB each)
+constexpr uint32_t kOffGn = 114688;  // Gn   [64 p][128 n]
+constexpr uint32_t kOffM1 = 131072;  // M1^T [128 s][128 t]: 2 panels of t
+constexpr uint32_t kOffM2 = 163840;  // M2^T [128 s][128 t]
+constexpr uint32_t kOffXs = 196608;  // x scaled by dt_s eend_s [128 s][64 p]
+constexpr uint32_t kOffV = 212992;   // float32 vectors of kQ values
+enum {
+    V_CS = 0, V_E, V_EEND, V_DT,
+    V_ROW, V_COL = V_ROW + 2, V_HC = V_COL + 2, V_R = V_HC + 2, V_XDU = V_R + 2, V_DD = V_XDU + 2,  // [2] halves
+    kNV = V_DD + 2
+};
+constexpr uint32_t kOffRed = kOffV + kNV * kQ * 4;               // kThreads partial sums + 16 scratch
+constexpr uint32_t kOffBar = kOffRed + (kThreads + 16) * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 4 * 8 + 16 + 1024;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+// 16-byte piece `piece` (0..7) of row `row` of a 128-byte-swizzled tile of 128-byte rows
+__device__ __forceinline__ uint32_t swz(int row, int piece) { return (uint32_t)(row * 128 + ((piece ^ (row & 7)) << 4)); }
+
+__device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *fail) {
+    const uint32_t addr = tc::smem_u32(bar);
+    if (tc::mbar_try_wait(addr, parity)) return true;
+    if (*fail) return false;
+    const uint64_t t0 = tc::global_ns();
+    for (;;) {
+        if (tc::mbar_try_wait(addr, parity)) return true;
+        if (*fail) return false;
+        if (tc::global_ns() - t0 > kWaitNs) {
+            *fail = 1;
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_constant__ BwdTcParams prm) {
+    const BwdArgs &a = prm.a;
+    const int c = blockIdx.x, h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int64_t L = a.L, H = a.H, G = a.G, nc = a.nc;
+    const int g = (int)(h / (H / G));
+    const int64_t t0 = (int64_t)c * kQ;
+    const int Qv = (int)imin<int64_t>(kQ, L - t0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
+    const uint32_t lq = (uint32_t)(qd * 32) << 16;
+    const int row = qd * 32 + lane;  // this thread's TMEM lane (t, s or n)
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *V = reinterpret_cast<float *>(sm + kOffV);
+    float *red = reinterpret_cast<float *>(sm + kOffRed), *scratch = red + kThreads;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+    volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *v_cs = V + V_CS * kQ, *v_e = V + V_E * kQ, *v_eend = V + V_EEND * kQ, *v_dt = V + V_DT * kQ;
+
+    if (tid == 0) {
+        for (int k = 0; k < 4; ++k) tc::mbar_init(bars + k, 1);
+        tc::fence_mbar_init();
+        *s_fail = 0;
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t T0 = tmem, T1 = tmem + 128, T2 = tmem + 256, T3 = tmem + 320, T4 = tmem + 384;
+
+    // x, dy, B, C of the chunk by TMA (rows past L read as zero)
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(&bars[0], 2u * 16384u + 4u * 16384u);
+        tc::tma_load_3d(sm + kOffX, &prm.mx, &bars[0], h * kP, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kOffY, &prm.mdy, &bars[0], h * kP, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kOffB, &prm.mb, &bars[0], g * kN, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kOffB + 16384, &prm.mb, &bars[0], g * kN + 64, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kOffC, &prm.mc, &bars[0], g * kN, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kOffC + 16384, &prm.mc, &bars[0], g * kN + 64, (int)t0, (int)b);
+    }
+    // h_in and Gn: float32 [p][n] rows into bf16 tiles (rows p, panels of 64 n),
+    // 8 n per 16-byte piece; <Gn, h_in> in float32 on the way
+    {
+        const int64_t so = ((b * nc + c) * H + h) * (int64_t)kP * kN;
+        float q = 0.f;
+        for (int e = tid; e < kP * kN / 8; e += kThreads) {
+            const int p = e >> 4, n8 = e & 15;
+            const float4 *hp = reinterpret_cast<const float4 *>(a.hin + so + p * kN + n8 * 8);
+            const float4 *gp = reinterpret_cast<const float4 *>(a.adj + so + p * kN + n8 * 8);
+            const float4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
+            q = fmaf(g0.x, h0.x, q); q = fmaf(g0.y, h0.y, q); q = fmaf(g0.z, h0.z, q); q = fmaf(g0.w, h0.w, q);
+            q = fmaf(g1.x, h1.x, q); q = fmaf(g1.y, h1.y, q); q = fmaf(g1.z, h1.z, q); q = fmaf(g1.w, h1.w, q);
+            const uint32_t off = (uint32_t)(n8 >> 3) * 8192u + swz(p, n8 & 7);
+            *reinterpret_cast<uint4 *>(sm + kOffHin + off) = make_uint4(
+                pack_bf16x2(h0.x, h0.y), pack_bf16x2(h0.z, h0.w), pack_bf16x2(h1.x, h1.y), pack_bf16x2(h1.z, h1.w));
+            *reinterpret_cast<uint4 *>(sm + kOffGn + off) = make_uint4(
+                pack_bf16x2(g0.x, g0.y), pack_bf16x2(g0.z, g0.w), pack_bf16x2(g1.x, g1.y), pack_bf16x2(g1.z, g1.w));
+        }
+        red[tid] = q;
+    }
+    // dt and its cumulative sum over the chunk (padded tokens carry dt = 0)
+    const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
+    const float dv = tid < Qv ? __bfloat162float(dtp[(b * L + t0 + tid) * H + h]) : 0.f;
+    block_inclusive_scan_256(dv * a.A[h], kQ, v_cs, scratch);
+    const float cs_end = v_cs[kQ - 1];
+    if (tid < kQ) {
+        v_dt[tid] = dv;
+        v_e[tid] = expf(v_cs[tid]);
+        v_eend[tid] = expf(cs_end - v_cs[tid]);
+    }
+    pwait(&bars[0], 0, s_fail);
+    __syncthreads();
+    // Xs: x scaled by dt_s eend_s (a 16-byte piece per step; the swizzle only
+    // permutes pieces inside a row, so the row of piece e is e / 8)
+    for (int e = tid; e < kQ * 8; e += kThreads) {
+        const int s = e >> 3;
+        const float f = v_dt[s] * v_eend[s];
+        float xv[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + e * 16), xv);
+        *reinterpret_cast<uint4 *>(sm + kOffXs + e * 16) =
+            make_uint4(pack_bf16x2(f * xv[0], f * xv[1]), pack_bf16x2(f * xv[2], f * xv[3]),
+                       pack_bf16x2(f * xv[4], f * xv[5]), pack_bf16x2(f * xv[6], f * xv[7]));
+    }
+    tc::fence_proxy_async_smem();  // h_in, Gn, Xs written here are read by the MMAs
+    tc::tc_fence_before();
+    __syncthreads();
+
+    const uint32_t c0 = tc::smem_u32(sm + kOffC), b0 = tc::smem_u32(sm + kOffB);
+    const uint32_t x0 = tc::smem_u32(sm + kOffX), y0 = tc::smem_u32(sm + kOffY);
+    const uint32_t hn0 = tc::smem_u32(sm + kOffHin), gn0 = tc::smem_u32(sm + kOffGn);
+    const uint32_t m10 = tc::smem_u32(sm + kOffM1), m20 = tc::smem_u32(sm + kOffM2), xs0 = tc::smem_u32(sm + kOffXs);
+    // K-major tile with panels of 64 along K (panel bytes `pb`), K offset k
+    auto kmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + (k >> 6) * pb + (k & 63) * 2, 16, 1024); };
+    // MN-major tile: K offset k in rows of 128 bytes, panels of 64 along M/N `pb` apart
+    auto mnmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + k * 128, pb, 1024); };
+
+    // ---- phase 1: CB, YX (rows t), HC, GB
+    if (tid == 0 && !*s_fail) {
+        tc::tc_fence_after();
+        const uint32_t id128 = tc::idesc_bf16(128, 128, false, false), id64 = tc::idesc_bf16(128, 64, false, false);
+        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(c0, k, 16384), kmaj(b0, k, 16384), id128, k > 0);
+        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(y0, k, 0), kmaj(x0, k, 0), id128, k > 0);
+        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T2, kmaj(c0, k, 16384), kmaj(hn0, k, 8192), id64, k > 0);
+        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T3, kmaj(b0, k, 16384), kmaj(gn0, k, 8192), id64, k > 0);
+        tc::mma_commit(&bars[1]);
+    }
+    pwait(&bars[1], 0, s_fail);
+    tc::tc_fence_after();
+    // epilogue A (lanes t): sum_{s<t} W[t,s] over this half's 64 columns,
+    // and dY_t . HC_t over this half's 32 columns of p
+    {
+        const int t = row;
+        const float cs_t = v_cs[t];
+        float rs = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int s0 = 64 * hf + 32 * j;
+            float cb[32], yx[32];
+            tc::tmem_ld32(T0 + lq + s0, cb);
+            tc::tmem_ld32(T1 + lq + s0, yx);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int s = s0 + u;
+                if (s < t) rs += expf(cs_t - v_cs[s]) * cb[u] * v_dt[s] * yx[u];
+            }
+        }
+        V[(V_ROW + hf) * kQ + t] = rs;
+        float hc[32];
+        tc::tmem_ld32(T2 + lq + 32 * hf, hc);
+        tc::tmem_ld_wait();
+        float acc = 0.f;
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+            float dy[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(t, 4 * hf + pc)), dy);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = fmaf(dy[i], hc[8 * pc + i], acc);
+        }
+        V[(V_HC + hf) * kQ + t] = acc;
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+
+    // ---- phase 2: BC = B C^T, XY = X dY^T (rows s)
+    if (tid == 0 && !*s_fail) {
+        tc::tc_fence_after();
+        const uint32_t id128 = tc::idesc_bf16(128, 128, false, false);
+        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(b0, k, 16384), kmaj(c0, k, 16384), id128, k > 0);
+        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(x0, k, 0), kmaj(y0, k, 0), id128, k > 0);
+        tc::mma_commit(&bars[2]);
+    }
+    pwait(&bars[2], 0, s_fail);
+    tc::tc_fence_after();
+    // epilogue B (lanes s): M1^T and M2^T rows (bf16, this half's 64 t), the
+    // column sums of W (t > s), and x_s . GB_s over this half's 32 p
+    {
+        const int s = row;
+        const float cs_s = v_cs[s], dts = v_dt[s];
+        float cl = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int tb = 64 * hf + 32 * j;
+            float bc[32], xy[32];
+            tc::tmem_ld32(T0 + lq + tb, bc);
+            tc::tmem_ld32(T1 + lq + tb, xy);
+            tc::tmem_ld_wait();
+            uint32_t m1p[16], m2p[16];
+#pragma unroll
+            for (int u = 0; u < 32; u += 2) {
+                float m1v[2], m2v[2];
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int t = tb + u + e2;
+                    const float ld = s <= t ? expf(v_cs[t] - cs_s) : 0.f;
+                    const float m1 = ld * bc[u + e2];
+                    if (t > s) cl += m1 * dts * xy[u + e2];
+                    m1v[e2] = m1;
+                    m2v[e2] = ld * dts * xy[u + e2];
+                }
+                m1p[u / 2] = pack_bf16x2(m1v[0], m1v[1]);
+                m2p[u / 2] = pack_bf16x2(m2v[0], m2v[1]);
+            }
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) {
+                const uint32_t off = (uint32_t)(tb >> 6) * 16384u + swz(s, ((tb & 63) >> 3) + pc);
+                *reinterpret_cast<uint4 *>(sm + kOffM1 + off) =
+                    make_uint4(m1p[4 * pc], m1p[4 * pc + 1], m1p[4 * pc + 2], m1p[4 * pc + 3]);
+                *reinterpret_cast<uint4 *>(sm + kOffM2 + off) =
+                    make_uint4(m2p[4 * pc], m2p[4 * pc + 1], m2p[4 * pc + 2], m2p[4 * pc + 3]);
+            }
+        }
+        V[(V_COL + hf) * kQ + s] = cl;
+        float gb[32];
+        tc::tmem_ld32(T3 + lq + 32 * hf, gb);
+        tc::tmem_ld_wait();
+        float rr = 0.f;
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+            float xv[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 4 * hf + pc)), xv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rr = fmaf(xv[i], gb[8 * pc + i], rr);
+        }
+        V[(V_R + hf) * kQ + s] = rr;
+    }
+    tc::fence_proxy_async_smem();  // M1^T, M2^T are read by the phase-3 MMAs
+    tc::tc_fence_before();
+    __syncthreads();
+
+    // ---- phase 3: du, dB, dC^T, (dY h_in)^T
+    if (tid == 0 && !*s_fail) {
+        tc::tc_fence_after();
+        // du = M1^T dY: A rows s (K = t), B = dy as MN-major (N = p, K = t)
+        const uint32_t idu = tc::idesc_bf16(128, 64, false, true);
+        for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T2, kmaj(m10, k, 16384), mnmaj(y0, k, 16384), idu, k > 0);
+        // dB = M2^T C + Xs Gn: B operands MN-major (N = n)
+        const uint32_t idb = tc::idesc_bf16(128, 128, false, true);
+        for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T0, kmaj(m20, k, 16384), mnmaj(c0, k, 16384), idb, k > 0);
+        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T0, kmaj(xs0, k, 0), mnmaj(gn0, k, 8192), idb, 1u);
+        // dC1^T = B^T M2^T: rows n (A = B as MN-major, M = n), N = t (M2^T as MN-major)
+        const uint32_t idc = tc::idesc_bf16(128, 128, true, true);
+        for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T4, mnmaj(b0, k, 16384), mnmaj(m20, k, 16384), idc, k > 0);
+        // (dY h_in)^T = h_in^T dY^T: rows n (A = h_in as MN-major), N = t (dy K-major, K = p)
+        const uint32_t idy = tc::idesc_bf16(128, 128, true, false);
+        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, mnmaj(hn0, k, 8192), kmaj(y0, k, 0), idy, k > 0);
+        tc::mma_commit(&bars[3]);
+    }
+    pwait(&bars[3], 0, s_fail);
+    tc::tc_fence_after();
+    const float Dh = a.D ? a.D[h] : 0.f;
+    // epilogue C: du, dx and x . du (lanes s, this half's 32 p); dB (lanes s,
+    // this half's 64 n); dC (lanes n, this half's 64 t); dY . x
+    {
+        const int s = row;
+        float du[32], gb[32];
+        tc::tmem_ld32(T2 + lq + 32 * hf, du);
+        tc::tmem_ld32(T3 + lq + 32 * hf, gb);
+        tc::tmem_ld_wait();
+        const float ee = v_eend[s], dts = v_dt[s];
+        float xd = 0.f, yxd = 0.f, dxv[32];
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+            float xv[8], yv[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 4 * hf + pc)), xv);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(s, 4 * hf + pc)), yv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float u = fmaf(ee, gb[8 * pc + i], du[8 * pc + i]);
+                xd = fmaf(xv[i], u, xd);
+                yxd = fmaf(yv[i], xv[i], yxd);
+                dxv[8 * pc + i] = fmaf(dts, u, Dh * yv[i]);
+            }
+        }
+        V[(V_XDU + hf) * kQ + s] = xd;
+        V[(V_DD + hf) * kQ + s] = yxd;
+        if (s < Qv) {
+            float4 *dxr = reinterpret_cast<float4 *>(a.dx + ((b * L + t0 + s) * H + h) * (int64_t)kP + 32 * hf);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                dxr[q4] = make_float4(dxv[4 * q4], dxv[4 * q4 + 1], dxv[4 * q4 + 2], dxv[4 * q4 + 3]);
+        }
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            float v[32];
+            tc::tmem_ld32(T0 + lq + 64 * hf + 32 * j, v);
+            tc::tmem_ld_wait();
+            if (s < Qv) {
+                float4 *dbr = reinterpret_cast<float4 *>(a.dB_part + ((b * L + t0 + s) * H + h) * (int64_t)kN +
+                                                         64 * hf + 32 * j);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) dbr[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            }
+        }
+        const int n = row;
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int tb = 64 * hf + 32 * j;
+            float d1[32], yh[32];
+            tc::tmem_ld32(T4 + lq + tb, d1);
+            tc::tmem_ld32(T1 + lq + tb, yh);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int t = tb + u;
+                if (t < Qv) a.dC_part[((b * L + t0 + t) * H + h) * (int64_t)kN + n] = fmaf(v_e[t], yh[u], d1[u]);
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+
+    // ---- d cs, da (suffix sums), ddt, dA and dD parts: tokens on warps 0-3
+    float suf = 0.f;
+    if (tid < kQ) {
+        const int t = tid;
+        const float q = red[2 * t] + red[2 * t + 1];
+        const float rv = t < Qv ? v_eend[t] * v_dt[t] * (V[V_R * kQ + t] + V[(V_R + 1) * kQ + t]) : 0.f;
+        const float qs = warp_sum(q), rs = warp_sum(rv);
+        if (lane == 0) {
+            scratch[warp] = qs;
+            scratch[4 + warp] = rs;
+        }
+        V[V_R * kQ + t] = rv;  // r_t replaces this thread's own partial, read just above
+    }
+    __syncthreads();
+    if (tid < kQ) {
+        const int t = tid;
+        const float q = (scratch[0] + scratch[1]) + (scratch[2] + scratch[3]);
+        const float rsum = (scratch[4] + scratch[5]) + (scratch[6] + scratch[7]);
+        float dcs = 0.f;
+        if (t < Qv)
+            dcs = (V[V_ROW * kQ + t] + V[(V_ROW + 1) * kQ + t]) - (V[V_COL * kQ + t] + V[(V_COL + 1) * kQ + t]) +
+                  v_e[t] * (V[V_HC * kQ + t] + V[(V_HC + 1) * kQ + t]) - V[V_R * kQ + t];
+        if (t == Qv - 1) dcs += rsum + expf(cs_end) * q;
+        suf = dcs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_down_sync(0xffffffffu, suf, o);
+            if (lane + o < 32) suf += u;
+        }
+        if (lane == 0) scratch[8 + warp] = suf;  // each warp's total
+    }
+    __syncthreads();
+    if (tid < kQ) {
+        const int t = tid;
+        float later = 0.f;
+        for (int w = warp + 1; w < 4; ++w) later += scratch[8 + w];
+        const float da = suf + later;
+        const float xdu = V[V_XDU * kQ + t] + V[(V_XDU + 1) * kQ + t];
+        if (t < Qv) a.ddt[(b * L + t0 + t) * H + h] = fmaf(da, a.A[h], xdu);
+        float pa = t < Qv ? da * v_dt[t] : 0.f, pd = t < Qv ? V[V_DD * kQ + t] + V[(V_DD + 1) * kQ + t] : 0.f;
+        pa = warp_sum(pa);
+        pd = warp_sum(pd);
+        if (lane == 0) {
+            red[kThreads - 8 + warp] = pa;
+            red[kThreads - 4 + warp] = pd;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        a.dA_part[(b * nc + c) * H + h] =
+            (red[kThreads - 8] + red[kThreads - 7]) + (red[kThreads - 6] + red[kThreads - 5]);
+        a.dD_part[(b * nc + c) * H + h] =
+            (red[kThreads - 4] + red[kThreads - 3]) + (red[kThreads - 2] + red[kThreads - 1]);
+        if (*s_fail && a.status) atomicCAS(a.status, SSD_OK, SSD_ERR_TIMEOUT);
+    }
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool chunk_bwd_tc_supported(int io, int64_t P, int64_t N) {
+    return io == IO_BF16 && P == kP && N == kN && device_cc_major_cached() == 10;
+}
+
+cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
+    if (a.Q != kQ || a.P != kP || a.N != kN || a.io != IO_BF16) return cudaErrorInvalidValue;
+    BwdTcParams p;
+    memset(&p, 0, sizeof(p));
+    p.a = a;
+    bool ok = true;
+    ok &= tma_map_tokens(&p.mx, a.x, a.H * a.P, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.mdy, a.dy, a.H * a.P, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kQ);
+    if (!ok) return cudaErrorInvalidValue;
+    static DeviceOnce configured;
+    int dev = 0;
+    cudaError_t e = cudaSuccess;
+    if (configured.pending(&dev, &e)) {
+        e = cudaFuncSetAttribute(chunk_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.done(dev);
+    } else if (e != cudaSuccess) {
+        return e;
+    }
+    chunk_bwd_tc_kernel<<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

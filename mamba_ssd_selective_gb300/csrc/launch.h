@@ -149,6 +149,8 @@ struct BwdArgs {
     static constexpr int kChunk = 64, kMaxP = 64, kMaxN = 128;
     int64_t B, L, H, P, N, G, nc;
     int io;
+    int Q;                    // tokens per chunk: 64 (CUDA cores) or 128 (tensor-core gradients)
+    int *status;              // SSD_OK, or SSD_ERR_TIMEOUT when a bounded wait gave up
     const void *x, *dt, *Bm, *Cm, *dy;
     const float *A, *D, *dfinal;
     const float *hin;         // [B, nc, H, P, N] state entering each chunk (forward recompute)
@@ -160,6 +162,10 @@ struct BwdArgs {
 };
 size_t bwd_chunk_smem_bytes(int64_t P, int64_t N);
 cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream);
+// The per-chunk gradients on the tensor cores (chunks of 128 tokens, bf16
+// inputs, P = 64, N = 128, a GB300-class device); the other steps as above.
+bool chunk_bwd_tc_supported(int io, int64_t P, int64_t N);
+cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 

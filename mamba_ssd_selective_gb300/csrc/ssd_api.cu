@@ -364,6 +364,10 @@ ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void 
         if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked_bwd");
         return ok();
     }
+    // chunks of 128 tokens with the per-chunk gradients on the tensor cores
+    // (bf16, P 64, N 128, unless SSD_FLAG_SIMT), else 64 on the CUDA cores;
+    // the workspace is sized for 64
+    const bool tc = !(dims->flags & SSD_FLAG_SIMT) && ssd::chunk_bwd_tc_supported(io, dims->headdim, dims->dstate);
     ssd::ChunkedArgs f{};
     f.B = dims->batch;
     f.L = dims->seqlen;
@@ -371,7 +375,7 @@ ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void 
     f.P = dims->headdim;
     f.N = dims->dstate;
     f.G = dims->ngroups;
-    f.Q = ssd::BwdArgs::kChunk;
+    f.Q = tc ? 128 : ssd::BwdArgs::kChunk;
     f.nc = (f.L + f.Q - 1) / f.Q;
     f.io = io;
     f.x = x;
@@ -395,6 +399,8 @@ ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void 
     a.G = f.G;
     a.nc = f.nc;
     a.io = io;
+    a.Q = f.Q;
+    a.status = f.status;
     a.x = x;
     a.dt = dt;
     a.Bm = B;

@@ -456,6 +456,29 @@ def test_backward_every_element(ssd, io, tol, shape):
     _check_grads(g, ref, tol, f"{io} {shape}")
 
 
+@pytest.mark.parametrize("simt", [False, True])
+@pytest.mark.parametrize("shape", [(1, 128, 2, 64, 128, 1), (2, 300, 4, 64, 128, 2), (1, 1000, 6, 64, 128, 3),
+                                   (3, 129, 2, 64, 128, 1)])
+def test_backward_tensor_core_shapes(ssd, shape, simt):
+    """bf16, P 64, N 128: the per-chunk gradients on the tensor cores (chunks
+    of 128 tokens) and, forced, on the CUDA cores (chunks of 64): every
+    gradient against the float64 oracle within the bf16 bound; one full chunk,
+    ragged last chunks (300 = 2 x 128 + 44, 129 = 128 + 1), several B/C groups,
+    eight chunks."""
+    d, dy, dfin = _bwd_case(shape, "bf16", 31)
+    ref = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"], d["init_state"], dfin)
+    t = torch.bfloat16
+    g = ssd.ssd_scan_chunked_bwd(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                 dev(dy, t), dev(d["D"]), dev(d["init_state"]), dev(dfin), simt=simt)
+    torch.cuda.synchronize()
+    _check_grads(g, ref, 2e-2, f"bf16 {shape} simt={simt}")
+    worst = {}
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
+        want = ref[k]
+        worst[k] = float(np.max(np.abs(host(g[k]) - want)) / max(float(np.max(np.abs(want))), 1e-30))
+    print(f"backward {shape} simt={simt}: " + ", ".join(f"{k} {v:.1e}" for k, v in worst.items()))
+
+
 def test_backward_deterministic_and_without_optionals(ssd):
     """Two runs give the same bits; with no D, no initial state and no final
     cotangent the gradients still match the oracle."""
