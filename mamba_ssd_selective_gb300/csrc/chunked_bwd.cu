@@ -714,12 +714,14 @@ __global__ void __launch_bounds__(kT) bwd_reduce_kernel(const __grid_constant__ 
 template <typename T>
 cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     const int tilesP = (int)((a.P + 63) / 64), tilesN = (int)((a.N + 63) / 64);
-    const dim3 agrid((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B);
-    if (a.Q == 128)
-        adj_chunk_state_kernel<T, 128><<<agrid, kT, 0, stream>>>(a, tilesP, tilesN);
-    else
-        adj_chunk_state_kernel<T, 64><<<agrid, kT, 0, stream>>>(a, tilesP, tilesN);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (a.Q == 128) {
+        e = launch_adj_chunk_state_tc(a, stream);
+    } else {
+        adj_chunk_state_kernel<T, 64><<<dim3((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B), kT, 0,
+                                        stream>>>(a, tilesP, tilesN);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     // float4 elements when every (b, c, h) block of P*N states and the optional
     // cotangent arrays start 16-byte aligned

@@ -460,6 +460,128 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     }
 }
 
+// ---------------------------------------------------------------------------
+// Float32 chunk states on the tensor cores, for the backward's chunks of 128
+// tokens (bf16, P 64, N 128), one CTA per (b, chunk, head):
+//   forward  S_c[p,n]    = sum_t exp(cs_end - cs_t) dt_t x[t,p] B[t,n]
+//            (and the chunk decay exp(cs_end); the first kernel of the call
+//            also clears the status word)
+//   adjoint  Sbar_c[p,n] = sum_t exp(cs_t) dy[t,p] C[t,n]
+// as one MMA chain: rows n (B or C as the MN-major A operand), columns p (x
+// or dy, its rows scaled in place by the weights, the MN-major B operand),
+// K = t; the weights and the scaled operand are rounded to bf16 for the MMA.
+struct StateTcParams {
+    CUtensorMap ma, mx;  // A: B or C as (G*N, L, B); X: x or dy as (H*P, L, B); boxes 64 x 128
+    const __nv_bfloat16 *dt;
+    const float *A;
+    float *out;        // [B, nc, H, P, N]
+    float *chunk_sum;  // forward: [B, H, nc]
+    int *status;
+    int64_t B, L, H, G, nc;
+};
+constexpr uint32_t kStOffA = 0, kStOffX = 32768, kStOffV = 49152;
+constexpr uint32_t kStOffBar = kStOffV + (2 * kQ + 16) * 4;
+constexpr uint32_t kStSmem = kStOffBar + 2 * 8 + 16 + 1024;
+
+template <bool ADJ>
+__global__ void __launch_bounds__(kThreads) chunk_state_f32_tc(const __grid_constant__ StateTcParams p) {
+    const int c = blockIdx.x, h = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int64_t L = p.L, H = p.H;
+    const int g = (int)(h / (H / p.G));
+    const int64_t t0 = (int64_t)c * kQ;
+    const int Qv = (int)imin<int64_t>(kQ, L - t0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *v_cs = reinterpret_cast<float *>(sm + kStOffV), *v_w = v_cs + kQ, *scratch = v_w + kQ;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kStOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    if (!ADJ && tid == 0 && c == 0 && h == 0 && b == 0 && p.status) *p.status = SSD_OK;  // first kernel of the call
+    if (tid == 0) {
+        tc::mbar_init(bars, 1);
+        tc::mbar_init(bars + 1, 1);
+        tc::fence_mbar_init();
+        *s_fail = 0;
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, 64);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(&bars[0], 3u * 16384u);
+        tc::tma_load_3d(sm + kStOffA, &p.ma, &bars[0], g * kN, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kStOffA + 16384, &p.ma, &bars[0], g * kN + 64, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kStOffX, &p.mx, &bars[0], h * kP, (int)t0, (int)b);
+    }
+    const float dv = tid < Qv ? __bfloat162float(p.dt[(b * L + t0 + tid) * H + h]) : 0.f;
+    block_inclusive_scan_256(dv * p.A[h], kQ, v_cs, scratch);
+    const float cs_end = v_cs[kQ - 1];
+    if (tid < kQ) v_w[tid] = ADJ ? expf(v_cs[tid]) : expf(cs_end - v_cs[tid]) * dv;
+    if (!ADJ && tid == 0) p.chunk_sum[(b * H + h) * p.nc + c] = expf(cs_end);
+    pwait(&bars[0], 0, s_fail);
+    __syncthreads();
+    for (int e = tid; e < kQ * 8; e += kThreads) {  // rows of x / dy scaled by the weights
+        const float f = v_w[e >> 3];
+        float xv[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + kStOffX + e * 16), xv);
+        *reinterpret_cast<uint4 *>(sm + kStOffX + e * 16) =
+            make_uint4(pack_bf16x2(f * xv[0], f * xv[1]), pack_bf16x2(f * xv[2], f * xv[3]),
+                       pack_bf16x2(f * xv[4], f * xv[5]), pack_bf16x2(f * xv[6], f * xv[7]));
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && !*s_fail) {
+        tc::tc_fence_after();
+        const uint32_t a0 = tc::smem_u32(sm + kStOffA), x0 = tc::smem_u32(sm + kStOffX);
+        const uint32_t id = tc::idesc_bf16(128, 64, true, true);
+        for (int k = 0; k < kQ; k += 16)
+            tc::mma_bf16(tmem, tc::sdesc_sw128(a0 + k * 128, 16384, 1024), tc::sdesc_sw128(x0 + k * 128, 16384, 1024),
+                         id, k > 0);
+        tc::mma_commit(&bars[1]);
+    }
+    pwait(&bars[1], 0, s_fail);
+    tc::tc_fence_after();
+    {
+        // lanes n, columns p: for each p the warp's 32 lanes store 32 consecutive n
+        const int qd = warp & 3, hf = warp >> 2, n = qd * 32 + lane;
+        float v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + 32 * hf, v);
+        tc::tmem_ld_wait();
+        float *o = p.out + ((b * p.nc + c) * H + h) * (int64_t)kP * kN + n;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) o[(int64_t)(32 * hf + q) * kN] = v[q];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && *s_fail && p.status) atomicCAS(p.status, SSD_OK, SSD_ERR_TIMEOUT);
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 64);
+    }
+}
+
+template <bool ADJ>
+cudaError_t launch_state_tc(const StateTcParams &p, cudaStream_t stream) {
+    static DeviceOnce configured;
+    int dev = 0;
+    cudaError_t e = cudaSuccess;
+    if (configured.pending(&dev, &e)) {
+        e = cudaFuncSetAttribute(chunk_state_f32_tc<ADJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStSmem);
+        if (e != cudaSuccess) return e;
+        configured.done(dev);
+    } else if (e != cudaSuccess) {
+        return e;
+    }
+    chunk_state_f32_tc<ADJ><<<dim3((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B), kThreads, kStSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool chunk_bwd_tc_supported(int io, int64_t P, int64_t N) {
@@ -489,6 +611,50 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
     }
     chunk_bwd_tc_kernel<<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace ssd
+
+namespace ssd {
+
+cudaError_t launch_forward_states_tc(const ChunkedArgs &f, cudaStream_t stream) {
+    if (f.Q != kQ || f.P != kP || f.N != kN || f.io != IO_BF16) return cudaErrorInvalidValue;
+    if (f.nc > 0 && f.B > 0) {
+        StateTcParams p;
+        memset(&p, 0, sizeof(p));
+        if (!tma_map_tokens(&p.ma, f.Bm, f.G * f.N, f.L, f.B, kQ) || !tma_map_tokens(&p.mx, f.x, f.H * f.P, f.L, f.B, kQ))
+            return cudaErrorInvalidValue;
+        p.dt = static_cast<const __nv_bfloat16 *>(f.dt);
+        p.A = f.A;
+        p.out = f.states;
+        p.chunk_sum = f.chunk_sum;
+        p.status = f.status;
+        p.B = f.B;
+        p.L = f.L;
+        p.H = f.H;
+        p.G = f.G;
+        p.nc = f.nc;
+        cudaError_t e = launch_state_tc<false>(p, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_state_pass(f, true, false, stream, false);
+}
+
+cudaError_t launch_adj_chunk_state_tc(const BwdArgs &a, cudaStream_t stream) {
+    StateTcParams p;
+    memset(&p, 0, sizeof(p));
+    if (!tma_map_tokens(&p.ma, a.Cm, a.G * a.N, a.L, a.B, kQ) || !tma_map_tokens(&p.mx, a.dy, a.H * a.P, a.L, a.B, kQ))
+        return cudaErrorInvalidValue;
+    p.dt = static_cast<const __nv_bfloat16 *>(a.dt);
+    p.A = a.A;
+    p.out = a.adj;
+    p.status = a.status;
+    p.B = a.B;
+    p.L = a.L;
+    p.H = a.H;
+    p.G = a.G;
+    p.nc = a.nc;
+    return launch_state_tc<true>(p, stream);
 }
 
 }  // namespace ssd

@@ -166,6 +166,11 @@ cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream);
 // inputs, P = 64, N = 128, a GB300-class device); the other steps as above.
 bool chunk_bwd_tc_supported(int io, int64_t P, int64_t N);
 cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream);
+// The backward's forward recompute and adjoint chunk states for those chunks
+// on the tensor cores (float32 states; the forward one followed by the
+// float32 state pass in place).
+cudaError_t launch_forward_states_tc(const ChunkedArgs &f, cudaStream_t stream);
+cudaError_t launch_adj_chunk_state_tc(const BwdArgs &a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 

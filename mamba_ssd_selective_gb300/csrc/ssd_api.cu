@@ -388,7 +388,7 @@ ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void 
     f.status = reinterpret_cast<int *>(ws + w.status);
     f.states = reinterpret_cast<float *>(ws + w.hin);
     f.chunk_sum = reinterpret_cast<float *>(ws + w.chunk_sum);
-    e = ssd::launch_forward_states(f, stream);
+    e = tc ? ssd::launch_forward_states_tc(f, stream) : ssd::launch_forward_states(f, stream);
     if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked_bwd: forward states");
     ssd::BwdArgs a{};
     a.B = f.B;
