@@ -48,7 +48,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct BwdTcParams {
     BwdArgs a;
-    CUtensorMap mx, mdy, mb, mc;
+    CUtensorMap mx, mdy, mb, mc;  // bf16 inputs, boxes 64 x 128
+    CUtensorMap mdx, mdb, mdc;    // float32 dx, dB and dC parts, boxes 32 x 32
 };
 
 // shared memory (bytes from the 1024-aligned base)
@@ -137,35 +138,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     const uint32_t tmem = *tmem_slot;
     const uint32_t T0 = tmem, T1 = tmem + 128, T2 = tmem + 256, T3 = tmem + 320, T4 = tmem + 384;
 
-    // x, dy, B, C of the chunk by TMA (rows past L read as zero)
+    // x, dy, B, C of the chunk by TMA (rows past L read as zero); h_in and Gn
+    // (float32 [p][n], contiguous per (b, chunk, head)) by bulk copies into
+    // the M1^T / M2^T regions, which epilogue B fills later
+    const int64_t so = ((b * nc + c) * H + h) * (int64_t)kP * kN;
     if (tid == 0) {
-        tc::mbar_arrive_expect_tx(&bars[0], 2u * 16384u + 4u * 16384u);
+        tc::mbar_arrive_expect_tx(&bars[0], 6u * 16384u + 2u * 32768u);
         tc::tma_load_3d(sm + kOffX, &prm.mx, &bars[0], h * kP, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffY, &prm.mdy, &bars[0], h * kP, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffB, &prm.mb, &bars[0], g * kN, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffB + 16384, &prm.mb, &bars[0], g * kN + 64, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffC, &prm.mc, &bars[0], g * kN, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffC + 16384, &prm.mc, &bars[0], g * kN + 64, (int)t0, (int)b);
-    }
-    // h_in and Gn: float32 [p][n] rows into bf16 tiles (rows p, panels of 64 n),
-    // 8 n per 16-byte piece; <Gn, h_in> in float32 on the way
-    {
-        const int64_t so = ((b * nc + c) * H + h) * (int64_t)kP * kN;
-        float q = 0.f;
-        for (int e = tid; e < kP * kN / 8; e += kThreads) {
-            const int p = e >> 4, n8 = e & 15;
-            const float4 *hp = reinterpret_cast<const float4 *>(a.hin + so + p * kN + n8 * 8);
-            const float4 *gp = reinterpret_cast<const float4 *>(a.adj + so + p * kN + n8 * 8);
-            const float4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
-            q = fmaf(g0.x, h0.x, q); q = fmaf(g0.y, h0.y, q); q = fmaf(g0.z, h0.z, q); q = fmaf(g0.w, h0.w, q);
-            q = fmaf(g1.x, h1.x, q); q = fmaf(g1.y, h1.y, q); q = fmaf(g1.z, h1.z, q); q = fmaf(g1.w, h1.w, q);
-            const uint32_t off = (uint32_t)(n8 >> 3) * 8192u + swz(p, n8 & 7);
-            *reinterpret_cast<uint4 *>(sm + kOffHin + off) = make_uint4(
-                pack_bf16x2(h0.x, h0.y), pack_bf16x2(h0.z, h0.w), pack_bf16x2(h1.x, h1.y), pack_bf16x2(h1.z, h1.w));
-            *reinterpret_cast<uint4 *>(sm + kOffGn + off) = make_uint4(
-                pack_bf16x2(g0.x, g0.y), pack_bf16x2(g0.z, g0.w), pack_bf16x2(g1.x, g1.y), pack_bf16x2(g1.z, g1.w));
-        }
-        red[tid] = q;
+        tc::bulk_load(sm + kOffM1, a.hin + so, (uint32_t)(kP * kN * 4), &bars[0]);
+        tc::bulk_load(sm + kOffM2, a.adj + so, (uint32_t)(kP * kN * 4), &bars[0]);
     }
     // dt and its cumulative sum over the chunk (padded tokens carry dt = 0)
     const __nv_bfloat16 *dtp = static_cast<const __nv_bfloat16 *>(a.dt);
@@ -179,6 +165,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     }
     pwait(&bars[0], 0, s_fail);
     __syncthreads();
+    // h_in and Gn into bf16 tiles (rows p, panels of 64 n), 8 n per 16-byte
+    // piece; <Gn, h_in> in float32 on the way
+    {
+        float q = 0.f;
+        for (int e = tid; e < kP * kN / 8; e += kThreads) {
+            const int p = e >> 4, n8 = e & 15;
+            const float4 *hp = reinterpret_cast<const float4 *>(sm + kOffM1 + e * 32);
+            const float4 *gp = reinterpret_cast<const float4 *>(sm + kOffM2 + e * 32);
+            const float4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
+            q = fmaf(g0.x, h0.x, q); q = fmaf(g0.y, h0.y, q); q = fmaf(g0.z, h0.z, q); q = fmaf(g0.w, h0.w, q);
+            q = fmaf(g1.x, h1.x, q); q = fmaf(g1.y, h1.y, q); q = fmaf(g1.z, h1.z, q); q = fmaf(g1.w, h1.w, q);
+            const uint32_t off = (uint32_t)(n8 >> 3) * 8192u + swz(p, n8 & 7);
+            *reinterpret_cast<uint4 *>(sm + kOffHin + off) = make_uint4(
+                pack_bf16x2(h0.x, h0.y), pack_bf16x2(h0.z, h0.w), pack_bf16x2(h1.x, h1.y), pack_bf16x2(h1.z, h1.w));
+            *reinterpret_cast<uint4 *>(sm + kOffGn + off) = make_uint4(
+                pack_bf16x2(g0.x, g0.y), pack_bf16x2(g0.z, g0.w), pack_bf16x2(g1.x, g1.y), pack_bf16x2(g1.z, g1.w));
+        }
+        red[tid] = q;
+    }
     // Xs: x scaled by dt_s eend_s (a 16-byte piece per step; the swizzle only
     // permutes pieces inside a row, so the row of piece e is e / 8)
     for (int e = tid; e < kQ * 8; e += kThreads) {
@@ -339,7 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     tc::tc_fence_after();
     const float Dh = a.D ? a.D[h] : 0.f;
     // epilogue C: du, dx and x . du (lanes s, this half's 32 p); dB (lanes s,
-    // this half's 64 n); dC (lanes n, this half's 64 t); dY . x
+    // this half's 64 n); dC (lanes n, this half's 64 t); dY . x. Each warp
+    // stages its five 32 x 32 float32 boxes (dx, two of dB, two of dC; 4 KB
+    // each, 128-byte swizzle) in shared memory that the phase-3 MMAs no longer
+    // read, and stores them by TMA; rows past L are clipped by the tensor maps.
+    uint8_t *stg = sm + (warp < 3 ? warp * 20480 : kOffHin + (warp - 3) * 20480);
     {
         const int s = row;
         float du[32], gb[32];
@@ -363,25 +372,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
         }
         V[(V_XDU + hf) * kQ + s] = xd;
         V[(V_DD + hf) * kQ + s] = yxd;
-        if (s < Qv) {
-            float4 *dxr = reinterpret_cast<float4 *>(a.dx + ((b * L + t0 + s) * H + h) * (int64_t)kP + 32 * hf);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                dxr[q4] = make_float4(dxv[4 * q4], dxv[4 * q4 + 1], dxv[4 * q4 + 2], dxv[4 * q4 + 3]);
-        }
+        for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<float4 *>(stg + swz(lane, q4)) =
+                make_float4(dxv[4 * q4], dxv[4 * q4 + 1], dxv[4 * q4 + 2], dxv[4 * q4 + 3]);
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
             float v[32];
             tc::tmem_ld32(T0 + lq + 64 * hf + 32 * j, v);
             tc::tmem_ld_wait();
-            if (s < Qv) {
-                float4 *dbr = reinterpret_cast<float4 *>(a.dB_part + ((b * L + t0 + s) * H + h) * (int64_t)kN +
-                                                         64 * hf + 32 * j);
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) dbr[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-            }
+            for (int q4 = 0; q4 < 8; ++q4)
+                *reinterpret_cast<float4 *>(stg + 4096 * (1 + j) + swz(lane, q4)) =
+                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
         }
-        const int n = row;
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && qd * 32 < Qv) {
+            const int rs = (int)t0 + qd * 32;
+            tc::tma_store_3d(&prm.mdx, stg, h * kP + 32 * hf, rs, (int)b);
+            tc::tma_store_3d(&prm.mdb, stg + 4096, h * kN + 64 * hf, rs, (int)b);
+            tc::tma_store_3d(&prm.mdb, stg + 8192, h * kN + 64 * hf + 32, rs, (int)b);
+            tc::bulk_commit();
+        }
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
             const int tb = 64 * hf + 32 * j;
@@ -389,11 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
             tc::tmem_ld32(T4 + lq + tb, d1);
             tc::tmem_ld32(T1 + lq + tb, yh);
             tc::tmem_ld_wait();
+            uint8_t *box = stg + 4096 * (3 + j) + (lane & 3) * 4;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int t = tb + u;
-                if (t < Qv) a.dC_part[((b * L + t0 + t) * H + h) * (int64_t)kN + n] = fmaf(v_e[t], yh[u], d1[u]);
-            }
+            for (int u = 0; u < 32; ++u)
+                *reinterpret_cast<float *>(box + u * 128 + (((lane >> 2) ^ (u & 7)) << 4)) = fmaf(v_e[tb + u], yh[u], d1[u]);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j)
+                if (64 * hf + 32 * j < Qv)
+                    tc::tma_store_3d(&prm.mdc, stg + 4096 * (3 + j), h * kN + 32 * qd, (int)t0 + 64 * hf + 32 * j, (int)b);
+            tc::bulk_commit();
         }
     }
     tc::tc_fence_before();
@@ -454,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
             (red[kThreads - 4] + red[kThreads - 3]) + (red[kThreads - 2] + red[kThreads - 1]);
         if (*s_fail && a.status) atomicCAS(a.status, SSD_OK, SSD_ERR_TIMEOUT);
     }
+    if (lane == 0) tc::bulk_wait_read_all();  // this warp's staged boxes have been read
     if (warp == 0) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
@@ -598,6 +620,9 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
     ok &= tma_map_tokens(&p.mdy, a.dy, a.H * a.P, a.L, a.B, kQ);
     ok &= tma_map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kQ);
     ok &= tma_map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kQ);
+    ok &= tma_map_tokens_f32(&p.mdx, a.dx, a.H * a.P, a.L, a.B, 32);
+    ok &= tma_map_tokens_f32(&p.mdb, a.dB_part, a.H * a.N, a.L, a.B, 32);
+    ok &= tma_map_tokens_f32(&p.mdc, a.dC_part, a.H * a.N, a.L, a.B, 32);
     if (!ok) return cudaErrorInvalidValue;
     static DeviceOnce configured;
     int dev = 0;

@@ -1017,10 +1017,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
     const void *base;
     int rank;
+    int f32;  // float32 elements (else bf16)
     uint64_t dims[3], strides[2];
     uint32_t box[3];
     bool operator==(const MapKey &o) const {
-        if (base != o.base || rank != o.rank) return false;
+        if (base != o.base || rank != o.rank || f32 != o.f32) return false;
         for (int k = 0; k < rank; ++k)
             if (dims[k] != o.dims[k] || box[k] != o.box[k]) return false;
         for (int k = 0; k + 1 < rank; ++k)
@@ -1054,9 +1055,10 @@ bool make_map(CUtensorMap *out, const MapKey &k) {
     }
     for (int e = 0; e + 1 < k.rank; ++e) strides[e] = k.strides[e];
     CUtensorMap m;
-    CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)k.rank, const_cast<void *>(k.base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     k.box[0] >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+    const uint32_t row_bytes = k.box[0] * (k.f32 ? 4u : 2u);
+    CUresult r = enc(&m, k.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)k.rank,
+                     const_cast<void *>(k.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lock(g_map_mu);
@@ -1068,18 +1070,21 @@ bool make_map(CUtensorMap *out, const MapKey &k) {
     return true;
 }
 
-// (inner, rows, batch) view of a [B, L, inner] bf16 tensor, box (box_cols, box_rows, 1);
-// 128-byte swizzle for 64-column boxes, 64-byte swizzle for 32-column boxes
+// (inner, rows, batch) view of a [B, L, inner] bf16 (or float32) tensor, box
+// (box_cols, box_rows, 1); the 128-byte swizzle for boxes of 128-byte rows,
+// else the 64-byte swizzle
 bool map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
-                int box_cols = 64) {
+                int box_cols = 64, bool f32 = false) {
     MapKey k{};
     k.base = base;
     k.rank = 3;
+    k.f32 = f32 ? 1 : 0;
+    const uint64_t es = f32 ? 4 : 2;
     k.dims[0] = (uint64_t)inner;
     k.dims[1] = (uint64_t)L;
     k.dims[2] = (uint64_t)B;
-    k.strides[0] = (uint64_t)inner * 2;
-    k.strides[1] = (uint64_t)inner * L * 2;
+    k.strides[0] = (uint64_t)inner * es;
+    k.strides[1] = (uint64_t)inner * L * es;
     k.box[0] = (uint32_t)box_cols;
     k.box[1] = (uint32_t)box_rows;
     k.box[2] = 1;
@@ -1133,6 +1138,10 @@ cudaError_t launch_ex(void (*kern)(TcParams), dim3 grid, size_t smem, cudaStream
 bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
                     int box_cols) {
     return map_tokens(out, base, inner, L, B, box_rows, box_cols);
+}
+
+bool tma_map_tokens_f32(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows) {
+    return map_tokens(out, base, inner, L, B, box_rows, 32, true);
 }
 
 int device_cc_major_cached() { return device_cc_major(); }
