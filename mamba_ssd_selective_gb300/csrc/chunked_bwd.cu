@@ -41,8 +41,8 @@ constexpr int kQ = BwdArgs::kChunk;  // 64 tokens per backward chunk
 
 
 // Adjoint chunk state of one (b, c, h) and one 64x64 tile of (p, n), for
-// chunks of Q tokens (64 or 128: the dt scan covers the chunk, the sum runs
-// over sub-tiles of 64 tokens staged in shared memory in turn).
+// chunks of Q tokens (the dt scan covers the chunk, the sum runs over
+// sub-tiles of 64 tokens staged in shared memory in turn).
 template <typename T, int Q>
 __global__ void __launch_bounds__(kT) adj_chunk_state_kernel(const __grid_constant__ BwdArgs a, int tilesP,
                                                              int tilesN) {
@@ -753,16 +753,20 @@ __global__ void __launch_bounds__(kT) bwd_reduce4_kernel(const __grid_constant__
 
 template <typename T>
 cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
-    const int tilesP = (int)((a.P + 63) / 64), tilesN = (int)((a.N + 63) / 64);
     cudaError_t e;
     if (a.Q == 128) {
-        e = launch_adj_chunk_state_tc(a, stream);
-    } else {
-        adj_chunk_state_kernel<T, 64><<<dim3((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B), kT, 0,
-                                        stream>>>(a, tilesP, tilesN);
-        e = cudaGetLastError();
+        // chunks of 128 tokens: chunk states, the passes over the chunks and
+        // the per-chunk gradients on the tensor cores
+        if ((e = launch_bwd_states_tc(a, stream)) != cudaSuccess) return e;
+        if ((e = launch_chunk_bwd_tc(a, stream)) != cudaSuccess) return e;
+        const int64_t n = imax<int64_t>(a.B * a.L * a.G * a.N / 4, a.H);  // N is 128 here
+        bwd_reduce4_kernel<<<(unsigned)((n + kT - 1) / kT), kT, 0, stream>>>(a);
+        return cudaGetLastError();
     }
-    if (e != cudaSuccess) return e;
+    const int tilesP = (int)((a.P + 63) / 64), tilesN = (int)((a.N + 63) / 64);
+    adj_chunk_state_kernel<T, 64><<<dim3((unsigned)a.nc, (unsigned)(a.H * tilesP * tilesN), (unsigned)a.B), kT, 0,
+                                    stream>>>(a, tilesP, tilesN);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // float4 elements when every (b, c, h) block of P*N states and the optional
     // cotangent arrays start 16-byte aligned
     const int64_t PN = a.P * a.N;
@@ -775,13 +779,6 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
         adj_state_pass_kernel<1><<<dim3((unsigned)((PN + kT - 1) / kT), (unsigned)a.H, (unsigned)a.B), kT, 0,
                                    stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (a.Q == 128) {
-        // chunks of 128 tokens: the per-chunk gradients on the tensor cores
-        if ((e = launch_chunk_bwd_tc(a, stream)) != cudaSuccess) return e;
-        const int64_t n = imax<int64_t>(a.B * a.L * a.G * a.N / 4, a.H);  // N is 128 here
-        bwd_reduce4_kernel<<<(unsigned)((n + kT - 1) / kT), kT, 0, stream>>>(a);
-        return cudaGetLastError();
-    }
     const size_t smem = (size_t)ChunkSmem::total * sizeof(float);
     static DeviceOnce configured;  // set the attribute once per device
     int dev = 0;

@@ -484,20 +484,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
 
 // ---------------------------------------------------------------------------
 // Float32 chunk states on the tensor cores, for the backward's chunks of 128
-// tokens (bf16, P 64, N 128), one CTA per (b, chunk, head):
+// tokens (bf16, P 64, N 128), one CTA per (b, chunk, head) and direction
+// (blockIdx.z < B: forward, else adjoint for batch z - B):
 //   forward  S_c[p,n]    = sum_t exp(cs_end - cs_t) dt_t x[t,p] B[t,n]
-//            (and the chunk decay exp(cs_end); the first kernel of the call
-//            also clears the status word)
+//            (and the chunk decay exp(cs_end); block (0, 0, 0) also clears
+//            the status word, this being the call's first kernel)
 //   adjoint  Sbar_c[p,n] = sum_t exp(cs_t) dy[t,p] C[t,n]
 // as one MMA chain: rows n (B or C as the MN-major A operand), columns p (x
 // or dy, its rows scaled in place by the weights, the MN-major B operand),
 // K = t; the weights and the scaled operand are rounded to bf16 for the MMA.
 struct StateTcParams {
-    CUtensorMap ma, mx;  // A: B or C as (G*N, L, B); X: x or dy as (H*P, L, B); boxes 64 x 128
+    CUtensorMap mb, mx;   // forward: B as (G*N, L, B), x as (H*P, L, B); boxes 64 x 128
+    CUtensorMap mc, mdy;  // adjoint: C, dy
     const __nv_bfloat16 *dt;
     const float *A;
-    float *out;        // [B, nc, H, P, N]
-    float *chunk_sum;  // forward: [B, H, nc]
+    float *states, *adj;  // [B, nc, H, P, N]
+    float *chunk_sum;     // [B, H, nc]
     int *status;
     int64_t B, L, H, G, nc;
 };
@@ -505,10 +507,10 @@ constexpr uint32_t kStOffA = 0, kStOffX = 32768, kStOffV = 49152;
 constexpr uint32_t kStOffBar = kStOffV + (2 * kQ + 16) * 4;
 constexpr uint32_t kStSmem = kStOffBar + 2 * 8 + 16 + 1024;
 
-template <bool ADJ>
-__global__ void __launch_bounds__(kThreads) chunk_state_f32_tc(const __grid_constant__ StateTcParams p) {
+__global__ void __launch_bounds__(kThreads) chunk_states_tc(const __grid_constant__ StateTcParams p) {
+    const bool adj = blockIdx.z >= p.B;
     const int c = blockIdx.x, h = blockIdx.y;
-    const int64_t b = blockIdx.z;
+    const int64_t b = adj ? blockIdx.z - p.B : blockIdx.z;
     const int64_t L = p.L, H = p.H;
     const int g = (int)(h / (H / p.G));
     const int64_t t0 = (int64_t)c * kQ;
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_f32_tc(const __grid_cons
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kStOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    if (!ADJ && tid == 0 && c == 0 && h == 0 && b == 0 && p.status) *p.status = SSD_OK;  // first kernel of the call
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && p.status) *p.status = SSD_OK;
     if (tid == 0) {
         tc::mbar_init(bars, 1);
         tc::mbar_init(bars + 1, 1);
@@ -535,16 +537,17 @@ __global__ void __launch_bounds__(kThreads) chunk_state_f32_tc(const __grid_cons
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (tid == 0) {
+        const CUtensorMap *ma = adj ? &p.mc : &p.mb, *mx = adj ? &p.mdy : &p.mx;
         tc::mbar_arrive_expect_tx(&bars[0], 3u * 16384u);
-        tc::tma_load_3d(sm + kStOffA, &p.ma, &bars[0], g * kN, (int)t0, (int)b);
-        tc::tma_load_3d(sm + kStOffA + 16384, &p.ma, &bars[0], g * kN + 64, (int)t0, (int)b);
-        tc::tma_load_3d(sm + kStOffX, &p.mx, &bars[0], h * kP, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kStOffA, ma, &bars[0], g * kN, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kStOffA + 16384, ma, &bars[0], g * kN + 64, (int)t0, (int)b);
+        tc::tma_load_3d(sm + kStOffX, mx, &bars[0], h * kP, (int)t0, (int)b);
     }
     const float dv = tid < Qv ? __bfloat162float(p.dt[(b * L + t0 + tid) * H + h]) : 0.f;
     block_inclusive_scan_256(dv * p.A[h], kQ, v_cs, scratch);
     const float cs_end = v_cs[kQ - 1];
-    if (tid < kQ) v_w[tid] = ADJ ? expf(v_cs[tid]) : expf(cs_end - v_cs[tid]) * dv;
-    if (!ADJ && tid == 0) p.chunk_sum[(b * H + h) * p.nc + c] = expf(cs_end);
+    if (tid < kQ) v_w[tid] = adj ? expf(v_cs[tid]) : expf(cs_end - v_cs[tid]) * dv;
+    if (!adj && tid == 0) p.chunk_sum[(b * H + h) * p.nc + c] = expf(cs_end);
     pwait(&bars[0], 0, s_fail);
     __syncthreads();
     for (int e = tid; e < kQ * 8; e += kThreads) {  // rows of x / dy scaled by the weights
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_f32_tc(const __grid_cons
         float v[32];
         tc::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + 32 * hf, v);
         tc::tmem_ld_wait();
-        float *o = p.out + ((b * p.nc + c) * H + h) * (int64_t)kP * kN + n;
+        float *o = (adj ? p.adj : p.states) + ((b * p.nc + c) * H + h) * (int64_t)kP * kN + n;
 #pragma unroll
         for (int q = 0; q < 32; ++q) o[(int64_t)(32 * hf + q) * kN] = v[q];
     }
@@ -588,20 +591,53 @@ __global__ void __launch_bounds__(kThreads) chunk_state_f32_tc(const __grid_cons
     }
 }
 
-template <bool ADJ>
-cudaError_t launch_state_tc(const StateTcParams &p, cudaStream_t stream) {
-    static DeviceOnce configured;
-    int dev = 0;
-    cudaError_t e = cudaSuccess;
-    if (configured.pending(&dev, &e)) {
-        e = cudaFuncSetAttribute(chunk_state_f32_tc<ADJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStSmem);
-        if (e != cudaSuccess) return e;
-        configured.done(dev);
-    } else if (e != cudaSuccess) {
-        return e;
+// Both passes over the chunks of one (b, h), four state elements per thread
+// (blockIdx.z < B: forward, else adjoint for batch z - B):
+//   forward  states[c] <- h entering chunk c (init, or zero, before chunk 0),
+//            h <- exp(cs_end(c)) h + S_c
+//   adjoint  adj[c] <- cotangent of the state leaving chunk c (dfinal, or
+//            zero, after the last), g <- exp(cs_end(c)) g + Sbar_c; dinit = g
+// The values of kPF chunks are loaded before the chain consumes them.
+struct PassParams {
+    float *states, *adj, *dinit;
+    const float *init, *dfinal, *chunk_sum;
+    int64_t B, H, PN, nc;
+};
+constexpr int kPF = 16;
+
+__global__ void __launch_bounds__(kThreads) bwd_state_passes(const __grid_constant__ PassParams p) {
+    const bool adj = blockIdx.z >= p.B;
+    const int64_t b = adj ? blockIdx.z - p.B : blockIdx.z;
+    const int64_t PN = p.PN, H = p.H, nc = p.nc;
+    const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 4;
+    const int h = blockIdx.y;
+    if (e >= PN) return;
+    const float *src0 = adj ? p.dfinal : p.init;
+    float4 carry = src0 ? *reinterpret_cast<const float4 *>(src0 + (b * H + h) * PN + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float *buf = adj ? p.adj : p.states;
+    const float *dec = p.chunk_sum + (b * H + h) * nc;
+    for (int64_t k0 = 0; k0 < nc; k0 += kPF) {
+        float4 v[kPF];
+        float dc[kPF];
+#pragma unroll
+        for (int u = 0; u < kPF; ++u)
+            if (k0 + u < nc) {
+                const int64_t c = adj ? nc - 1 - (k0 + u) : k0 + u;
+                v[u] = *reinterpret_cast<const float4 *>(buf + ((b * nc + c) * H + h) * PN + e);
+                dc[u] = dec[c];
+            }
+#pragma unroll
+        for (int u = 0; u < kPF; ++u)
+            if (k0 + u < nc) {
+                const int64_t c = adj ? nc - 1 - (k0 + u) : k0 + u;
+                *reinterpret_cast<float4 *>(buf + ((b * nc + c) * H + h) * PN + e) = carry;
+                carry.x = fmaf(dc[u], carry.x, v[u].x);
+                carry.y = fmaf(dc[u], carry.y, v[u].y);
+                carry.z = fmaf(dc[u], carry.z, v[u].z);
+                carry.w = fmaf(dc[u], carry.w, v[u].w);
+            }
     }
-    chunk_state_f32_tc<ADJ><<<dim3((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B), kThreads, kStSmem, stream>>>(p);
-    return cudaGetLastError();
+    if (adj && p.dinit) *reinterpret_cast<float4 *>(p.dinit + (b * H + h) * PN + e) = carry;
 }
 
 }  // namespace
@@ -642,44 +678,52 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
 
 namespace ssd {
 
-cudaError_t launch_forward_states_tc(const ChunkedArgs &f, cudaStream_t stream) {
-    if (f.Q != kQ || f.P != kP || f.N != kN || f.io != IO_BF16) return cudaErrorInvalidValue;
-    if (f.nc > 0 && f.B > 0) {
-        StateTcParams p;
-        memset(&p, 0, sizeof(p));
-        if (!tma_map_tokens(&p.ma, f.Bm, f.G * f.N, f.L, f.B, kQ) || !tma_map_tokens(&p.mx, f.x, f.H * f.P, f.L, f.B, kQ))
-            return cudaErrorInvalidValue;
-        p.dt = static_cast<const __nv_bfloat16 *>(f.dt);
-        p.A = f.A;
-        p.out = f.states;
-        p.chunk_sum = f.chunk_sum;
-        p.status = f.status;
-        p.B = f.B;
-        p.L = f.L;
-        p.H = f.H;
-        p.G = f.G;
-        p.nc = f.nc;
-        cudaError_t e = launch_state_tc<false>(p, stream);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_state_pass(f, true, false, stream, false);
-}
-
-cudaError_t launch_adj_chunk_state_tc(const BwdArgs &a, cudaStream_t stream) {
+cudaError_t launch_bwd_states_tc(const BwdArgs &a, cudaStream_t stream) {
+    if (a.Q != kQ || a.P != kP || a.N != kN || a.io != IO_BF16) return cudaErrorInvalidValue;
     StateTcParams p;
     memset(&p, 0, sizeof(p));
-    if (!tma_map_tokens(&p.ma, a.Cm, a.G * a.N, a.L, a.B, kQ) || !tma_map_tokens(&p.mx, a.dy, a.H * a.P, a.L, a.B, kQ))
-        return cudaErrorInvalidValue;
+    bool ok = true;
+    ok &= tma_map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.mx, a.x, a.H * a.P, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kQ);
+    ok &= tma_map_tokens(&p.mdy, a.dy, a.H * a.P, a.L, a.B, kQ);
+    if (!ok) return cudaErrorInvalidValue;
     p.dt = static_cast<const __nv_bfloat16 *>(a.dt);
     p.A = a.A;
-    p.out = a.adj;
+    p.states = a.hin;
+    p.adj = a.adj;
+    p.chunk_sum = const_cast<float *>(a.chunk_sum);
     p.status = a.status;
     p.B = a.B;
     p.L = a.L;
     p.H = a.H;
     p.G = a.G;
     p.nc = a.nc;
-    return launch_state_tc<true>(p, stream);
+    static DeviceOnce configured;
+    int dev = 0;
+    cudaError_t e = cudaSuccess;
+    if (configured.pending(&dev, &e)) {
+        e = cudaFuncSetAttribute(chunk_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStSmem);
+        if (e != cudaSuccess) return e;
+        configured.done(dev);
+    } else if (e != cudaSuccess) {
+        return e;
+    }
+    chunk_states_tc<<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)(2 * a.B)), kThreads, kStSmem, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    PassParams q;
+    q.states = a.hin;
+    q.adj = a.adj;
+    q.dinit = a.dinit;
+    q.init = a.init;
+    q.dfinal = a.dfinal;
+    q.chunk_sum = a.chunk_sum;
+    q.B = a.B;
+    q.H = a.H;
+    q.PN = (int64_t)kP * kN;
+    q.nc = a.nc;
+    bwd_state_passes<<<dim3((unsigned)(q.PN / 4 / kThreads), (unsigned)a.H, (unsigned)(2 * a.B)), kThreads, 0, stream>>>(q);
+    return cudaGetLastError();
 }
 
 }  // namespace ssd

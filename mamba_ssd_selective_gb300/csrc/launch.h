@@ -153,7 +153,8 @@ struct BwdArgs {
     int *status;              // SSD_OK, or SSD_ERR_TIMEOUT when a bounded wait gave up
     const void *x, *dt, *Bm, *Cm, *dy;
     const float *A, *D, *dfinal;
-    const float *hin;         // [B, nc, H, P, N] state entering each chunk (forward recompute)
+    float *hin;               // [B, nc, H, P, N] state entering each chunk (forward recompute)
+    const float *init;        // [B, H, P, N] or null: state before the first chunk (tensor-core path)
     float *adj;               // [B, nc, H, P, N] adjoint chunk states, then leaving cotangents
     const float *chunk_sum;   // [B, H, nc] exp(sum of dt*A over the chunk)
     float *dB_part, *dC_part; // [B, L, H, N] per-head parts
@@ -166,11 +167,10 @@ cudaError_t launch_ssd_bwd(const BwdArgs &a, cudaStream_t stream);
 // inputs, P = 64, N = 128, a GB300-class device); the other steps as above.
 bool chunk_bwd_tc_supported(int io, int64_t P, int64_t N);
 cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream);
-// The backward's forward recompute and adjoint chunk states for those chunks
-// on the tensor cores (float32 states; the forward one followed by the
-// float32 state pass in place).
-cudaError_t launch_forward_states_tc(const ChunkedArgs &f, cudaStream_t stream);
-cudaError_t launch_adj_chunk_state_tc(const BwdArgs &a, cudaStream_t stream);
+// The backward's float32 chunk states for those chunks on the tensor cores
+// (forward recompute into hin with chunk_sum, adjoint into adj; one launch),
+// then both passes over the chunks in place (one launch; writes dinit).
+cudaError_t launch_bwd_states_tc(const BwdArgs &a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int *status, int spin_limit, cudaStream_t stream);
 

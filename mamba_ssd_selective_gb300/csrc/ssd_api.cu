@@ -388,8 +388,9 @@ ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void 
     f.status = reinterpret_cast<int *>(ws + w.status);
     f.states = reinterpret_cast<float *>(ws + w.hin);
     f.chunk_sum = reinterpret_cast<float *>(ws + w.chunk_sum);
-    e = tc ? ssd::launch_forward_states_tc(f, stream) : ssd::launch_forward_states(f, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_chunked_bwd: forward states");
+    // the tensor-core path recomputes the forward states inside launch_ssd_bwd
+    if (!tc && (e = ssd::launch_forward_states(f, stream)) != cudaSuccess)
+        return cuda_fail(e, "ssd_scan_chunked_bwd: forward states");
     ssd::BwdArgs a{};
     a.B = f.B;
     a.L = f.L;
@@ -410,6 +411,7 @@ ssd_status ssd_scan_chunked_bwd(const ssd_dims *dims, const void *x, const void 
     a.D = D;
     a.dfinal = dfinal_state;
     a.hin = f.states;
+    a.init = init_state;
     a.adj = reinterpret_cast<float *>(ws + w.adj);
     a.chunk_sum = f.chunk_sum;
     a.dB_part = reinterpret_cast<float *>(ws + w.dB_part);
