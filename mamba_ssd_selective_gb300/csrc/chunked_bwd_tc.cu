@@ -44,12 +44,16 @@ namespace ssd {
 namespace {
 
 constexpr int kQ = 128, kP = 64, kN = 128, kThreads = 256;
+// the per-chunk gradient kernel: 16 warps, warp w on TMEM lane quarter w % 4
+// and column quarter w / 4 of every product it reads back
+constexpr int kBT = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct BwdTcParams {
     BwdArgs a;
     CUtensorMap mx, mdy, mb, mc;  // bf16 inputs, boxes 64 x 128
-    CUtensorMap mdx, mdb, mdc;    // float32 dx, dB and dC parts, boxes 32 x 32
+    CUtensorMap mdx;              // float32 dx, boxes 16 x 32 (64-byte swizzle)
+    CUtensorMap mdb, mdc;         // float32 dB and dC parts, boxes 32 x 32 (128-byte swizzle)
 };
 
 // shared memory (bytes from the 1024-aligned base)
@@ -65,12 +69,13 @@ constexpr uint32_t kOffXs = 196608;  // x scaled by dt_s eend_s [128 s][64 p]
 constexpr uint32_t kOffV = 212992;   // float32 vectors of kQ values
 enum {
     V_CS = 0, V_E, V_EEND, V_DT,
-    V_ROW, V_COL = V_ROW + 2, V_HC = V_COL + 2, V_R = V_HC + 2, V_XDU = V_R + 2, V_DD = V_XDU + 2,  // [2] halves
-    kNV = V_DD + 2
+    V_ROW, V_COL = V_ROW + 4, V_HC = V_COL + 4, V_R = V_HC + 4, V_XDU = V_R + 4, V_DD = V_XDU + 4,  // [4] quarters
+    kNV = V_DD + 4
 };
-constexpr uint32_t kOffRed = kOffV + kNV * kQ * 4;               // kThreads partial sums + 16 scratch
-constexpr uint32_t kOffBar = kOffRed + (kThreads + 16) * 4;
+constexpr uint32_t kOffRed = kOffV + kNV * kQ * 4;               // kBT partial sums + 16 scratch
+constexpr uint32_t kOffBar = kOffRed + (kBT + 16) * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 4 * 8 + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "one CTA per SM with the maximum opt-in shared memory");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -102,7 +107,7 @@ __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile i
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_constant__ BwdTcParams prm) {
+__global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_constant__ BwdTcParams prm) {
     const BwdArgs &a = prm.a;
     const int c = blockIdx.x, h = blockIdx.y;
     const int64_t b = blockIdx.z;
@@ -111,18 +116,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     const int64_t t0 = (int64_t)c * kQ;
     const int Qv = (int)imin<int64_t>(kQ, L - t0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qd = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
+    const int qd = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
     const uint32_t lq = (uint32_t)(qd * 32) << 16;
     const int row = qd * 32 + lane;  // this thread's TMEM lane (t, s or n)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *V = reinterpret_cast<float *>(sm + kOffV);
-    float *red = reinterpret_cast<float *>(sm + kOffRed), *scratch = red + kThreads;
+    float *red = reinterpret_cast<float *>(sm + kOffRed), *scratch = red + kBT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *v_cs = V + V_CS * kQ, *v_e = V + V_E * kQ, *v_eend = V + V_EEND * kQ, *v_dt = V + V_DT * kQ;
+    // sum of the four column quarters' partials of vector k at index i, in a fixed order
+    auto q4sum = [&](int k, int i) { return (V[k * kQ + i] + V[(k + 1) * kQ + i]) + (V[(k + 2) * kQ + i] + V[(k + 3) * kQ + i]); };
 
     if (tid == 0) {
         for (int k = 0; k < 4; ++k) tc::mbar_init(bars + k, 1);
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     // piece; <Gn, h_in> in float32 on the way
     {
         float q = 0.f;
-        for (int e = tid; e < kP * kN / 8; e += kThreads) {
+        for (int e = tid; e < kP * kN / 8; e += kBT) {
             const int p = e >> 4, n8 = e & 15;
             const float4 *hp = reinterpret_cast<const float4 *>(sm + kOffM1 + e * 32);
             const float4 *gp = reinterpret_cast<const float4 *>(sm + kOffM2 + e * 32);
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     }
     // Xs: x scaled by dt_s eend_s (a 16-byte piece per step; the swizzle only
     // permutes pieces inside a row, so the row of piece e is e / 8)
-    for (int e = tid; e < kQ * 8; e += kThreads) {
+    for (int e = tid; e < kQ * 8; e += kBT) {
         const int s = e >> 3;
         const float f = v_dt[s] * v_eend[s];
         float xv[8];
@@ -220,38 +227,32 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     }
     pwait(&bars[1], 0, s_fail);
     tc::tc_fence_after();
-    // epilogue A (lanes t): sum_{s<t} W[t,s] over this half's 64 columns,
-    // and dY_t . HC_t over this half's 32 columns of p
+    // epilogue A (lanes t): sum_{s<t} W[t,s] over this quarter's 32 columns,
+    // and dY_t . HC_t over this quarter's 16 columns of p
     {
-        const int t = row;
+        const int t = row, s0 = 32 * cq;
         const float cs_t = v_cs[t];
-        float rs = 0.f;
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int s0 = 64 * hf + 32 * j;
-            float cb[32], yx[32];
-            tc::tmem_ld32(T0 + lq + s0, cb);
-            tc::tmem_ld32(T1 + lq + s0, yx);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int s = s0 + u;
-                if (s < t) rs += expf(cs_t - v_cs[s]) * cb[u] * v_dt[s] * yx[u];
-            }
-        }
-        V[(V_ROW + hf) * kQ + t] = rs;
-        float hc[32];
-        tc::tmem_ld32(T2 + lq + 32 * hf, hc);
+        float cb[32], yx[32], hc[16];
+        tc::tmem_ld32(T0 + lq + s0, cb);
+        tc::tmem_ld32(T1 + lq + s0, yx);
+        tc::tmem_ld16(T2 + lq + 16 * cq, hc);
         tc::tmem_ld_wait();
+        float rs = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int s = s0 + u;
+            if (s < t) rs += expf(cs_t - v_cs[s]) * cb[u] * v_dt[s] * yx[u];
+        }
+        V[(V_ROW + cq) * kQ + t] = rs;
         float acc = 0.f;
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
+        for (int pc = 0; pc < 2; ++pc) {
             float dy[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(t, 4 * hf + pc)), dy);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(t, 2 * cq + pc)), dy);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc = fmaf(dy[i], hc[8 * pc + i], acc);
         }
-        V[(V_HC + hf) * kQ + t] = acc;
+        V[(V_HC + cq) * kQ + t] = acc;
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -266,57 +267,51 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     }
     pwait(&bars[2], 0, s_fail);
     tc::tc_fence_after();
-    // epilogue B (lanes s): M1^T and M2^T rows (bf16, this half's 64 t), the
-    // column sums of W (t > s), and x_s . GB_s over this half's 32 p
+    // epilogue B (lanes s): M1^T and M2^T rows (bf16, this quarter's 32 t), the
+    // column sums of W (t > s), and x_s . GB_s over this quarter's 16 p
     {
-        const int s = row;
+        const int s = row, tb = 32 * cq;
         const float cs_s = v_cs[s], dts = v_dt[s];
+        float bc[32], xy[32];
+        tc::tmem_ld32(T0 + lq + tb, bc);
+        tc::tmem_ld32(T1 + lq + tb, xy);
+        tc::tmem_ld_wait();
         float cl = 0.f;
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int tb = 64 * hf + 32 * j;
-            float bc[32], xy[32];
-            tc::tmem_ld32(T0 + lq + tb, bc);
-            tc::tmem_ld32(T1 + lq + tb, xy);
-            tc::tmem_ld_wait();
-            uint32_t m1p[16], m2p[16];
 #pragma unroll
-            for (int u = 0; u < 32; u += 2) {
+        for (int pc = 0; pc < 4; ++pc) {
+            uint32_t m1p[4], m2p[4];
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) {
                 float m1v[2], m2v[2];
 #pragma unroll
                 for (int e2 = 0; e2 < 2; ++e2) {
-                    const int t = tb + u + e2;
+                    const int j = 8 * pc + u + e2, t = tb + j;
                     const float ld = s <= t ? expf(v_cs[t] - cs_s) : 0.f;
-                    const float m1 = ld * bc[u + e2];
-                    if (t > s) cl += m1 * dts * xy[u + e2];
+                    const float m1 = ld * bc[j];
+                    if (t > s) cl += m1 * dts * xy[j];
                     m1v[e2] = m1;
-                    m2v[e2] = ld * dts * xy[u + e2];
+                    m2v[e2] = ld * dts * xy[j];
                 }
                 m1p[u / 2] = pack_bf16x2(m1v[0], m1v[1]);
                 m2p[u / 2] = pack_bf16x2(m2v[0], m2v[1]);
             }
-#pragma unroll
-            for (int pc = 0; pc < 4; ++pc) {
-                const uint32_t off = (uint32_t)(tb >> 6) * 16384u + swz(s, ((tb & 63) >> 3) + pc);
-                *reinterpret_cast<uint4 *>(sm + kOffM1 + off) =
-                    make_uint4(m1p[4 * pc], m1p[4 * pc + 1], m1p[4 * pc + 2], m1p[4 * pc + 3]);
-                *reinterpret_cast<uint4 *>(sm + kOffM2 + off) =
-                    make_uint4(m2p[4 * pc], m2p[4 * pc + 1], m2p[4 * pc + 2], m2p[4 * pc + 3]);
-            }
+            const uint32_t off = (uint32_t)(tb >> 6) * 16384u + swz(s, ((tb & 63) >> 3) + pc);
+            *reinterpret_cast<uint4 *>(sm + kOffM1 + off) = make_uint4(m1p[0], m1p[1], m1p[2], m1p[3]);
+            *reinterpret_cast<uint4 *>(sm + kOffM2 + off) = make_uint4(m2p[0], m2p[1], m2p[2], m2p[3]);
         }
-        V[(V_COL + hf) * kQ + s] = cl;
-        float gb[32];
-        tc::tmem_ld32(T3 + lq + 32 * hf, gb);
+        V[(V_COL + cq) * kQ + s] = cl;
+        float gb[16];
+        tc::tmem_ld16(T3 + lq + 16 * cq, gb);
         tc::tmem_ld_wait();
         float rr = 0.f;
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
+        for (int pc = 0; pc < 2; ++pc) {
             float xv[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 4 * hf + pc)), xv);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 2 * cq + pc)), xv);
 #pragma unroll
             for (int i = 0; i < 8; ++i) rr = fmaf(xv[i], gb[8 * pc + i], rr);
         }
-        V[(V_R + hf) * kQ + s] = rr;
+        V[(V_R + cq) * kQ + s] = rr;
     }
     tc::fence_proxy_async_smem();  // M1^T, M2^T are read by the phase-3 MMAs
     tc::tc_fence_before();
@@ -343,25 +338,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     pwait(&bars[3], 0, s_fail);
     tc::tc_fence_after();
     const float Dh = a.D ? a.D[h] : 0.f;
-    // epilogue C: du, dx and x . du (lanes s, this half's 32 p); dB (lanes s,
-    // this half's 64 n); dC (lanes n, this half's 64 t); dY . x. Each warp
-    // stages its five 32 x 32 float32 boxes (dx, two of dB, two of dC; 4 KB
-    // each, 128-byte swizzle) in shared memory that the phase-3 MMAs no longer
-    // read, and stores them by TMA; rows past L are clipped by the tensor maps.
-    uint8_t *stg = sm + (warp < 3 ? warp * 20480 : kOffHin + (warp - 3) * 20480);
+    // epilogue C: du, dx and x . du (lanes s, this quarter's 16 p); dB (lanes
+    // s, this quarter's 32 n); dC (lanes n, this quarter's 32 t); dY . x. Each
+    // warp stages its three float32 boxes (dx 32 x 16 with the 64-byte swizzle,
+    // dB and dC 32 x 32 with the 128-byte swizzle; 10 KB) in shared memory
+    // that the phase-3 MMAs no longer read, and stores them by TMA; rows past
+    // L are clipped by the tensor maps.
+    uint8_t *stg = sm + (warp < 6 ? warp * 10240 : kOffHin + (warp - 6) * 10240);
     {
         const int s = row;
-        float du[32], gb[32];
-        tc::tmem_ld32(T2 + lq + 32 * hf, du);
-        tc::tmem_ld32(T3 + lq + 32 * hf, gb);
+        float du[16], gb[16];
+        tc::tmem_ld16(T2 + lq + 16 * cq, du);
+        tc::tmem_ld16(T3 + lq + 16 * cq, gb);
         tc::tmem_ld_wait();
         const float ee = v_eend[s], dts = v_dt[s];
-        float xd = 0.f, yxd = 0.f, dxv[32];
+        float xd = 0.f, yxd = 0.f, dxv[16];
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
+        for (int pc = 0; pc < 2; ++pc) {
             float xv[8], yv[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 4 * hf + pc)), xv);
-            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(s, 4 * hf + pc)), yv);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 2 * cq + pc)), xv);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(s, 2 * cq + pc)), yv);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float u = fmaf(ee, gb[8 * pc + i], du[8 * pc + i]);
@@ -370,39 +366,37 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
                 dxv[8 * pc + i] = fmaf(dts, u, Dh * yv[i]);
             }
         }
-        V[(V_XDU + hf) * kQ + s] = xd;
-        V[(V_DD + hf) * kQ + s] = yxd;
+        V[(V_XDU + cq) * kQ + s] = xd;
+        V[(V_DD + cq) * kQ + s] = yxd;
+        // dx box: rows of 64 bytes, 16-byte piece k of row r at k ^ ((r >> 1) & 3)
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<float4 *>(stg + swz(lane, q4)) =
-                make_float4(dxv[4 * q4], dxv[4 * q4 + 1], dxv[4 * q4 + 2], dxv[4 * q4 + 3]);
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4 *>(stg + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                make_float4(dxv[4 * k], dxv[4 * k + 1], dxv[4 * k + 2], dxv[4 * k + 3]);
+        {
             float v[32];
-            tc::tmem_ld32(T0 + lq + 64 * hf + 32 * j, v);
+            tc::tmem_ld32(T0 + lq + 32 * cq, v);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                *reinterpret_cast<float4 *>(stg + 4096 * (1 + j) + swz(lane, q4)) =
-                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float4 *>(stg + 2048 + swz(lane, k)) =
+                    make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qd * 32 < Qv) {
             const int rs = (int)t0 + qd * 32;
-            tc::tma_store_3d(&prm.mdx, stg, h * kP + 32 * hf, rs, (int)b);
-            tc::tma_store_3d(&prm.mdb, stg + 4096, h * kN + 64 * hf, rs, (int)b);
-            tc::tma_store_3d(&prm.mdb, stg + 8192, h * kN + 64 * hf + 32, rs, (int)b);
+            tc::tma_store_3d(&prm.mdx, stg, h * kP + 16 * cq, rs, (int)b);
+            tc::tma_store_3d(&prm.mdb, stg + 2048, h * kN + 32 * cq, rs, (int)b);
             tc::bulk_commit();
         }
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int tb = 64 * hf + 32 * j;
+        {
+            const int tb = 32 * cq;
             float d1[32], yh[32];
             tc::tmem_ld32(T4 + lq + tb, d1);
             tc::tmem_ld32(T1 + lq + tb, yh);
             tc::tmem_ld_wait();
-            uint8_t *box = stg + 4096 * (3 + j) + (lane & 3) * 4;
+            uint8_t *box = stg + 6144 + (lane & 3) * 4;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
                 *reinterpret_cast<float *>(box + u * 128 + (((lane >> 2) ^ (u & 7)) << 4)) = fmaf(v_e[tb + u], yh[u], d1[u]);
@@ -410,10 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-#pragma unroll 1
-            for (int j = 0; j < 2; ++j)
-                if (64 * hf + 32 * j < Qv)
-                    tc::tma_store_3d(&prm.mdc, stg + 4096 * (3 + j), h * kN + 32 * qd, (int)t0 + 64 * hf + 32 * j, (int)b);
+            if (32 * cq < Qv) tc::tma_store_3d(&prm.mdc, stg + 6144, h * kN + 32 * qd, (int)t0 + 32 * cq, (int)b);
             tc::bulk_commit();
         }
     }
@@ -424,14 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
     float suf = 0.f;
     if (tid < kQ) {
         const int t = tid;
-        const float q = red[2 * t] + red[2 * t + 1];
-        const float rv = t < Qv ? v_eend[t] * v_dt[t] * (V[V_R * kQ + t] + V[(V_R + 1) * kQ + t]) : 0.f;
+        const float q = (red[4 * t] + red[4 * t + 1]) + (red[4 * t + 2] + red[4 * t + 3]);
+        const float rv = t < Qv ? v_eend[t] * v_dt[t] * q4sum(V_R, t) : 0.f;
         const float qs = warp_sum(q), rs = warp_sum(rv);
         if (lane == 0) {
             scratch[warp] = qs;
             scratch[4 + warp] = rs;
         }
-        V[V_R * kQ + t] = rv;  // r_t replaces this thread's own partial, read just above
+        V[V_R * kQ + t] = rv;  // r_t replaces this thread's own partials, read just above
     }
     __syncthreads();
     if (tid < kQ) {
@@ -439,9 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
         const float q = (scratch[0] + scratch[1]) + (scratch[2] + scratch[3]);
         const float rsum = (scratch[4] + scratch[5]) + (scratch[6] + scratch[7]);
         float dcs = 0.f;
-        if (t < Qv)
-            dcs = (V[V_ROW * kQ + t] + V[(V_ROW + 1) * kQ + t]) - (V[V_COL * kQ + t] + V[(V_COL + 1) * kQ + t]) +
-                  v_e[t] * (V[V_HC * kQ + t] + V[(V_HC + 1) * kQ + t]) - V[V_R * kQ + t];
+        if (t < Qv) dcs = q4sum(V_ROW, t) - q4sum(V_COL, t) + v_e[t] * q4sum(V_HC, t) - V[V_R * kQ + t];
         if (t == Qv - 1) dcs += rsum + expf(cs_end) * q;
         suf = dcs;
 #pragma unroll
@@ -457,22 +446,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_tc_kernel(const __grid_
         float later = 0.f;
         for (int w = warp + 1; w < 4; ++w) later += scratch[8 + w];
         const float da = suf + later;
-        const float xdu = V[V_XDU * kQ + t] + V[(V_XDU + 1) * kQ + t];
+        const float xdu = q4sum(V_XDU, t);
         if (t < Qv) a.ddt[(b * L + t0 + t) * H + h] = fmaf(da, a.A[h], xdu);
-        float pa = t < Qv ? da * v_dt[t] : 0.f, pd = t < Qv ? V[V_DD * kQ + t] + V[(V_DD + 1) * kQ + t] : 0.f;
+        float pa = t < Qv ? da * v_dt[t] : 0.f, pd = t < Qv ? q4sum(V_DD, t) : 0.f;
         pa = warp_sum(pa);
         pd = warp_sum(pd);
         if (lane == 0) {
-            red[kThreads - 8 + warp] = pa;
-            red[kThreads - 4 + warp] = pd;
+            red[kBT - 8 + warp] = pa;
+            red[kBT - 4 + warp] = pd;
         }
     }
     __syncthreads();
     if (tid == 0) {
-        a.dA_part[(b * nc + c) * H + h] =
-            (red[kThreads - 8] + red[kThreads - 7]) + (red[kThreads - 6] + red[kThreads - 5]);
-        a.dD_part[(b * nc + c) * H + h] =
-            (red[kThreads - 4] + red[kThreads - 3]) + (red[kThreads - 2] + red[kThreads - 1]);
+        a.dA_part[(b * nc + c) * H + h] = (red[kBT - 8] + red[kBT - 7]) + (red[kBT - 6] + red[kBT - 5]);
+        a.dD_part[(b * nc + c) * H + h] = (red[kBT - 4] + red[kBT - 3]) + (red[kBT - 2] + red[kBT - 1]);
         if (*s_fail && a.status) atomicCAS(a.status, SSD_OK, SSD_ERR_TIMEOUT);
     }
     if (lane == 0) tc::bulk_wait_read_all();  // this warp's staged boxes have been read
@@ -656,7 +643,7 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
     ok &= tma_map_tokens(&p.mdy, a.dy, a.H * a.P, a.L, a.B, kQ);
     ok &= tma_map_tokens(&p.mb, a.Bm, a.G * a.N, a.L, a.B, kQ);
     ok &= tma_map_tokens(&p.mc, a.Cm, a.G * a.N, a.L, a.B, kQ);
-    ok &= tma_map_tokens_f32(&p.mdx, a.dx, a.H * a.P, a.L, a.B, 32);
+    ok &= tma_map_tokens_f32(&p.mdx, a.dx, a.H * a.P, a.L, a.B, 32, 16);
     ok &= tma_map_tokens_f32(&p.mdb, a.dB_part, a.H * a.N, a.L, a.B, 32);
     ok &= tma_map_tokens_f32(&p.mdc, a.dC_part, a.H * a.N, a.L, a.B, 32);
     if (!ok) return cudaErrorInvalidValue;
@@ -670,7 +657,7 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
     } else if (e != cudaSuccess) {
         return e;
     }
-    chunk_bwd_tc_kernel<<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kThreads, kSmemBytes, stream>>>(p);
+    chunk_bwd_tc_kernel<<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)a.B), kBT, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

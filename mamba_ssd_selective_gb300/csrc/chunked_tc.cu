@@ -1140,8 +1140,9 @@ bool tma_map_tokens(CUtensorMap *out, const void *base, int64_t inner, int64_t L
     return map_tokens(out, base, inner, L, B, box_rows, box_cols);
 }
 
-bool tma_map_tokens_f32(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows) {
-    return map_tokens(out, base, inner, L, B, box_rows, 32, true);
+bool tma_map_tokens_f32(CUtensorMap *out, const void *base, int64_t inner, int64_t L, int64_t B, int box_rows,
+                        int box_cols) {
+    return map_tokens(out, base, inner, L, B, box_rows, box_cols, true);
 }
 
 int device_cc_major_cached() { return device_cc_major(); }

@@ -74,10 +74,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Inclusive prefix sum over a[0..n) held one value per thread (threads >= n
-// hold 0), for blockDim.x == 256 and n <= 256. Result written to out[0..n).
-// Fixed association (warp shuffle scan, then a scan of the 8 warp totals), so
-// it is bitwise reproducible. `scratch` holds at least 8 floats. Ends with a
-// __syncthreads().
+// hold 0), for blockDim.x a multiple of 32 of at least 256 and n <= 256.
+// Result written to out[0..n). Fixed association (warp shuffle scan, then a
+// scan of the first 8 warp totals), so it is bitwise reproducible and the same
+// for any such block size. `scratch` holds at least 8 floats. Every thread of
+// the block calls it; ends with a __syncthreads().
 __device__ __forceinline__ void block_inclusive_scan_256(float a, int n, float *out, float *scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float v = a;
@@ -86,7 +87,7 @@ __device__ __forceinline__ void block_inclusive_scan_256(float a, int n, float *
         float u = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += u;
     }
-    if (lane == 31) scratch[warp] = v;
+    if (lane == 31 && warp < 8) scratch[warp] = v;
     __syncthreads();
     if (warp == 0) {
         float t = lane < 8 ? scratch[lane] : 0.f;
@@ -98,7 +99,7 @@ __device__ __forceinline__ void block_inclusive_scan_256(float a, int n, float *
         if (lane < 8) scratch[lane] = t;  // inclusive totals
     }
     __syncthreads();
-    if (warp > 0) v += scratch[warp - 1];
+    if (warp > 0 && warp < 8) v += scratch[warp - 1];
     if ((int)threadIdx.x < n) out[threadIdx.x] = v;
     __syncthreads();
 }
