@@ -458,13 +458,15 @@ def test_backward_every_element(ssd, io, tol, shape):
 
 @pytest.mark.parametrize("simt", [False, True])
 @pytest.mark.parametrize("shape", [(1, 128, 2, 64, 128, 1), (2, 300, 4, 64, 128, 2), (1, 1000, 6, 64, 128, 3),
-                                   (3, 129, 2, 64, 128, 1)])
+                                   (3, 129, 2, 64, 128, 1), (1, 300, 3, 64, 128, 1), (2, 257, 6, 64, 128, 6)])
 def test_backward_tensor_core_shapes(ssd, shape, simt):
     """bf16, P 64, N 128: the per-chunk gradients on the tensor cores (chunks
     of 128 tokens) and, forced, on the CUDA cores (chunks of 64): every
     gradient against the float64 oracle within the bf16 bound; one full chunk,
-    ragged last chunks (300 = 2 x 128 + 44, 129 = 128 + 1), several B/C groups,
-    eight chunks."""
+    ragged last chunks (300 = 2 x 128 + 44, 129 = 128 + 1, 257 = 2 x 128 + 1),
+    several B/C groups, eight chunks; an even number of heads per group (the
+    gradient kernel sums pairs of heads) and an odd one (3, and 1 with six
+    groups: one part per head)."""
     d, dy, dfin = _bwd_case(shape, "bf16", 31)
     ref = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"], d["init_state"], dfin)
     t = torch.bfloat16
