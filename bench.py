@@ -512,7 +512,7 @@ def run_ours(args):
     if "mamba1_softplus" in legs:
         compact["mamba1_softplus"] = bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W)
     if "backward" in legs:
-        compact["backward"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W)
+        compact["backward"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W, bwd_shape(args))
 
     clocks = sampler.stop() if sampler else None
     if rank != 0:
@@ -856,11 +856,18 @@ def bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W):
             "Mtok_s": round(Bz * L / ms / 1e3, 2), "frac": round(gbs / hbm_peak, 4), "kernels": launches}
 
 
-def bench_backward(torch, binding, inputs, dev, hbm_peak, W):
+def bwd_shape(args):
+    """(B, L, H) of the backward leg: the 130M-shaped layer at L 2048 unless
+    --bwd-shape names another."""
+    return tuple(int(v) for v in (getattr(args, "bwd_shape", None) or "1,2048,24").split(","))
+
+
+def bench_backward(torch, binding, inputs, dev, hbm_peak, W, shape=(1, 2048, 24)):
     """SSD backward (recompute, adjoint states, per-chunk gradients) on the
-    130M-shaped layer at L 2048, bf16 inputs, float32 gradients; input copies
-    rotate past L2."""
-    Bz, L, H, P, N, G = 1, 2048, 24, 64, 128, 1
+    130M-shaped layer at L 2048 (or another (B, L, H) with P 64, N 128, one
+    group), bf16 inputs, float32 gradients; input copies rotate past L2."""
+    Bz, L, H = shape
+    P, N, G = 64, 128, 1
     bf = torch.bfloat16
     d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=0)
     rng = np.random.default_rng(1)
@@ -887,7 +894,8 @@ def bench_backward(torch, binding, inputs, dev, hbm_peak, W):
     ms, sd = batch_rep_stats(torch, run, per_batch=5)
     # compulsory bytes: x, dt, B, C, dy read (bf16); dx, ddt, dB, dC written (float32)
     nbytes = Bz * L * (2 * H * P + H + 2 * G * N) * 2 + Bz * L * (H * P + H + 2 * G * N) * 4
-    return {"w": "bwd_130m_L2048", "us": round(ms * 1e3, 1), "std": round(sd * 1e3, 1),
+    name = "bwd_130m_L2048" if shape == (1, 2048, 24) else f"bwd_B{Bz}_L{L}_H{H}"
+    return {"w": name, "shape": [Bz, L, H], "us": round(ms * 1e3, 1), "std": round(sd * 1e3, 1),
             "Mtok_s": round(Bz * L / ms / 1e3, 2), "frac": round(nbytes / (ms / 1e3) / 1e9 / hbm_peak, 4)}
 
 
@@ -999,7 +1007,7 @@ def oracle_beside(compact: dict, details: dict, seconds: float = 2.0) -> None:
         compact["mamba1_softplus"]["cpu"] = round(Bz * L / (per * Dm / ch), 1)
         notes[MAMBA1_SP] = f"{ch} of {Dm} channels, all tokens, {reps} rep(s), scaled to all channels"
     if "backward" in compact:
-        Bz, L, H, P, N, G = 1, 2048, 24, 64, 128, 1
+        (Bz, L, H), (P, N, G) = compact["backward"].get("shape", (1, 2048, 24)), (64, 128, 1)
         hs = 2
         d = inputs.ssd_inputs(Bz, L, hs, P, N, G, io_dtype="bf16", seed=0)
         dy = inputs.round_to(np.random.default_rng(1).standard_normal(d["x"].shape), "bf16")
@@ -1185,7 +1193,8 @@ def run_profile_calls(args):
             binding.selective_scan_diag(*a, None, chunk_size=w["chunk"], delta_softplus=True)
         torch.cuda.synchronize()
     if "backward" in legs:
-        d = inputs.ssd_inputs(1, 2048, 24, 64, 128, 1, io_dtype="bf16", seed=0)
+        Bz, L, H = bwd_shape(args)
+        d = inputs.ssd_inputs(Bz, L, H, 64, 128, 1, io_dtype="bf16", seed=0)
         dy = inputs.round_to(np.random.default_rng(1).standard_normal(d["x"].shape), "bf16")
         a = (t_(d["x"], bf), t_(d["dt"], bf), t_(d["A"]), t_(d["B"], bf), t_(d["C"], bf), t_(dy, bf), t_(d["D"]))
         for _ in range(n):
@@ -1202,6 +1211,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk", type=int, default=0, help="force the headline's chunk size (default: best of 64/128/256)")
     ap.add_argument("--legs", default=None, help=f"comma-separated subset of {','.join(LEGS)} (default: all)")
+    ap.add_argument("--bwd-shape", default=None, help="B,L,H of the backward leg (default 1,2048,24; P 64, N 128)")
     ap.add_argument("--workload", default=None, help="reference arm: workload name (default: the headline)")
     ap.add_argument("--ref-budget-s", type=float, default=60.0, help="reference arm: total oracle seconds")
     ap.add_argument("--skip-extra", action="store_true", help="the headline leg only")
