@@ -335,13 +335,17 @@ ssd_status ssd_debug_bounds_status(int *site, int64_t *index, int clear);
  * State Space Duality ...", appendix Table 13): the gradients of
  *     L = <dy, y> + <dfinal_state, final_state>
  * with respect to every input, for the recurrence of ssd_scan_chunked. It
- * recomputes the forward entering states in chunks of 64 tokens, runs the
- * adjoint chunk states and a reverse state pass, then one kernel per
- * (b, chunk, head) forms every gradient from 64 x 64 products; float32
- * arithmetic on the CUDA cores. Deterministic (fixed-order sums, no atomics).
+ * recomputes the forward entering states chunk by chunk, runs the adjoint
+ * chunk states and a reverse state pass, then one CTA per (b, chunk, head)
+ * forms every gradient of that chunk. bf16 inputs with headdim 64 and dstate
+ * 128 on a GB300-class device take chunks of 128 tokens with every product
+ * on the tensor cores (bf16 operands, float32 accumulation and elementwise
+ * steps); everything else, or flags containing SSD_FLAG_SIMT, takes chunks of
+ * 64 tokens in float32 on the CUDA cores. Deterministic (fixed-order sums,
+ * no atomics).
  *   dims      as for ssd_scan_chunked (seqlen L, io_dtype of x, dt, B, C, dy;
- *             flags ignored). Limits: headdim <= 64, dstate <= 128 (else
- *             SSD_ERR_UNSUPPORTED).
+ *             of the flags only SSD_FLAG_SIMT is read). Limits: headdim <= 64,
+ *             dstate <= 128 (else SSD_ERR_UNSUPPORTED).
  *   x, dt, A, B, C, D, init_state   the forward's inputs (D, init_state may be NULL)
  *   dy          [B, L, H, P]  io_dtype: cotangent of y
  *   dfinal_state[B, H, P, N]  float32, may be NULL (0)
