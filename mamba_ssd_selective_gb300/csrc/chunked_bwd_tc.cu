@@ -15,20 +15,21 @@
 //   sum_s r_s + exp(cs_end) <Gn, h_in>; da = suffix sums of d cs,
 //   ddt = da A + x . du, dA = sum da dt, dD = sum dY . x.
 //
-// Eleven tcgen05 MMA groups in three phases, float32 accumulators in TMEM
-// (512 columns), operands bf16 in shared memory with the 128-byte swizzle
-// (rows of 64 elements; the same tile serves as a K-major or an MN-major
-// operand depending on the product):
-//   phase 1  CB = C B^T, YX = dY X^T (rows t), HC = C h_in^T, GB = B Gn^T
-//   phase 2  BC = B C^T, XY = X dY^T (rows s: the transposed scores)
-//   phase 3  du = M1^T dY, dB = M2^T C + Xs Gn (Xs = x scaled by dt eend per
+// Nine tcgen05 MMA groups in two phases, float32 accumulators in TMEM (512
+// columns), operands bf16 in shared memory with the 128-byte swizzle (rows of
+// 64 elements; the same tile serves as a K-major or an MN-major operand
+// depending on the product):
+//   phase 1  BC = B C^T, XY = X dY^T (rows s: the transposed scores),
+//            HC = C h_in^T (rows t), GB = B Gn^T (rows s)
+//   phase 2  du = M1^T dY, dB = M2^T C + Xs Gn (Xs = x scaled by dt eend per
 //            row), dC^T = B^T M2^T and (dY h_in)^T (rows n)
-// The epilogues run on the CUDA cores in float32, a thread per TMEM lane
-// (row) and two threads per row (column halves): the row sums of W from the
-// phase-1 rows, M1^T and M2^T (bf16, the phase-3 A operands) and the column
-// sums of W from the phase-2 rows, then the gradients. h_in and Gn enter the
-// products rounded to bf16 (as do M1 and M2); <Gn, h_in> and every
-// elementwise step stay float32. Sums run in a fixed order (no atomics).
+// The epilogues run on the CUDA cores in float32, a thread per TMEM lane and
+// column quarter: after phase 1, M1^T and M2^T (bf16, the phase-2 A operands),
+// the sums of W along each row of the transposed scores (W's column sums) and
+// across the lanes of each warp (its row sums), the per-token dot products;
+// after phase 2, the gradients. h_in and Gn enter the products rounded to bf16
+// (as do M1 and M2); <Gn, h_in> and every elementwise step stay float32. Sums
+// run in a fixed order (no atomics).
 #include <cuda.h>
 
 #include <cstdint>
@@ -220,60 +221,23 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     // MN-major tile: K offset k in rows of 128 bytes, panels of 64 along M/N `pb` apart
     auto mnmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + k * 128, pb, 1024); };
 
-    // ---- phase 1: CB, YX (rows t), HC, GB
+    // ---- phase 1: BC = B C^T, XY = X dY^T (rows s: the transposed scores), HC, GB
     if (tid == 0 && !*s_fail) {
         tc::tc_fence_after();
         const uint32_t id128 = tc::idesc_bf16(128, 128, false, false), id64 = tc::idesc_bf16(128, 64, false, false);
-        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(c0, k, 16384), kmaj(b0, k, 16384), id128, k > 0);
-        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(y0, k, 0), kmaj(x0, k, 0), id128, k > 0);
+        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(b0, k, 16384), kmaj(c0, k, 16384), id128, k > 0);
+        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(x0, k, 0), kmaj(y0, k, 0), id128, k > 0);
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T2, kmaj(c0, k, 16384), kmaj(hn0, k, 8192), id64, k > 0);
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T3, kmaj(b0, k, 16384), kmaj(gn0, k, 8192), id64, k > 0);
         tc::mma_commit(&bars[1]);
     }
     pwait(&bars[1], 0, s_fail);
     tc::tc_fence_after();
-    // epilogue A (lanes t): sum_{s<t} W[t,s] over this quarter's 32 columns,
-    // and dY_t . HC_t over this quarter's 16 columns of p
-    {
-        const int t = row, s0 = 32 * cq;
-        const float cs_t = v_cs[t];
-        float cb[32], yx[32], hc[16];
-        tc::tmem_ld32(T0 + lq + s0, cb);
-        tc::tmem_ld32(T1 + lq + s0, yx);
-        tc::tmem_ld16(T2 + lq + 16 * cq, hc);
-        tc::tmem_ld_wait();
-        float rs = 0.f;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int s = s0 + u;
-            if (s < t) rs += expf(cs_t - v_cs[s]) * cb[u] * v_dt[s] * yx[u];
-        }
-        V[(V_ROW + cq) * kQ + t] = rs;
-        float acc = 0.f;
-#pragma unroll
-        for (int pc = 0; pc < 2; ++pc) {
-            float dy[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(t, 2 * cq + pc)), dy);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc = fmaf(dy[i], hc[8 * pc + i], acc);
-        }
-        V[(V_HC + cq) * kQ + t] = acc;
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-
-    // ---- phase 2: BC = B C^T, XY = X dY^T (rows s)
-    if (tid == 0 && !*s_fail) {
-        tc::tc_fence_after();
-        const uint32_t id128 = tc::idesc_bf16(128, 128, false, false);
-        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(b0, k, 16384), kmaj(c0, k, 16384), id128, k > 0);
-        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(x0, k, 0), kmaj(y0, k, 0), id128, k > 0);
-        tc::mma_commit(&bars[2]);
-    }
-    pwait(&bars[2], 0, s_fail);
-    tc::tc_fence_after();
-    // epilogue B (lanes s): M1^T and M2^T rows (bf16, this quarter's 32 t), the
-    // column sums of W (t > s), and x_s . GB_s over this quarter's 16 p
+    // epilogue B (lanes s, this quarter's 32 t): M1^T and M2^T rows (bf16), W
+    // (t > s) summed along the row (its column sums) and across the warp's 32
+    // lanes (its row sums, a partial per lane quarter), x_s . GB_s over this
+    // quarter's 16 p; and, for the token t of this thread's TMEM lane, dY_t . HC_t
+    // over the same 16 p
     {
         const int s = row, tb = 32 * cq;
         const float cs_s = v_cs[s], dts = v_dt[s];
@@ -293,9 +257,11 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
                     const int j = 8 * pc + u + e2, t = tb + j;
                     const float ld = s <= t ? expf(v_cs[t] - cs_s) : 0.f;
                     const float m1 = ld * bc[j];
-                    if (t > s) cl += m1 * dts * xy[j];
+                    const float w = t > s ? m1 * dts * xy[j] : 0.f;
+                    cl += w;
                     m1v[e2] = m1;
                     m2v[e2] = ld * dts * xy[j];
+                    bc[j] = w;  // W[t, s], summed across the lanes below
                 }
                 m1p[u / 2] = pack_bf16x2(m1v[0], m1v[1]);
                 m2p[u / 2] = pack_bf16x2(m2v[0], m2v[1]);
@@ -305,24 +271,44 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
             *reinterpret_cast<uint4 *>(sm + kOffM2 + off) = make_uint4(m2p[0], m2p[1], m2p[2], m2p[3]);
         }
         V[(V_COL + cq) * kQ + s] = cl;
-        float gb[16];
+        // reduce-scatter over the 32 lanes: halve the live columns each step,
+        // keeping the half this lane's bit selects; lane j ends with the sum
+        // of column j over the warp's lanes
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) {
+            const bool up = (lane & k) != 0;
+#pragma unroll
+            for (int i = 0; i < k; ++i) {
+                const float send = up ? bc[i] : bc[i + k];
+                const float keep = up ? bc[i + k] : bc[i];
+                bc[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+            }
+        }
+        V[(V_ROW + qd) * kQ + tb + lane] = bc[0];
+        float gb[16], hc[16];
         tc::tmem_ld16(T3 + lq + 16 * cq, gb);
+        tc::tmem_ld16(T2 + lq + 16 * cq, hc);
         tc::tmem_ld_wait();
-        float rr = 0.f;
+        float rr = 0.f, acc = 0.f;
 #pragma unroll
         for (int pc = 0; pc < 2; ++pc) {
-            float xv[8];
+            float xv[8], dy[8];
             unpack8(*reinterpret_cast<const uint4 *>(sm + kOffX + swz(s, 2 * cq + pc)), xv);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffY + swz(s, 2 * cq + pc)), dy);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) rr = fmaf(xv[i], gb[8 * pc + i], rr);
+            for (int i = 0; i < 8; ++i) {
+                rr = fmaf(xv[i], gb[8 * pc + i], rr);
+                acc = fmaf(dy[i], hc[8 * pc + i], acc);
+            }
         }
         V[(V_R + cq) * kQ + s] = rr;
+        V[(V_HC + cq) * kQ + s] = acc;
     }
-    tc::fence_proxy_async_smem();  // M1^T, M2^T are read by the phase-3 MMAs
+    tc::fence_proxy_async_smem();  // M1^T, M2^T are read by the phase-2 MMAs
     tc::tc_fence_before();
     __syncthreads();
 
-    // ---- phase 3: du, dB, dC^T, (dY h_in)^T
+    // ---- phase 2: du, dB, dC^T, (dY h_in)^T
     if (tid == 0 && !*s_fail) {
         tc::tc_fence_after();
         // du = M1^T dY: A rows s (K = t), B = dy as MN-major (N = p, K = t)
@@ -338,16 +324,16 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         // (dY h_in)^T = h_in^T dY^T: rows n (A = h_in as MN-major), N = t (dy K-major, K = p)
         const uint32_t idy = tc::idesc_bf16(128, 128, true, false);
         for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, mnmaj(hn0, k, 8192), kmaj(y0, k, 0), idy, k > 0);
-        tc::mma_commit(&bars[3]);
+        tc::mma_commit(&bars[2]);
     }
-    pwait(&bars[3], 0, s_fail);
+    pwait(&bars[2], 0, s_fail);
     tc::tc_fence_after();
     const float Dh = a.D ? a.D[h] : 0.f;
-    // epilogue C: du, dx and x . du (lanes s, this quarter's 16 p); dB (lanes
+    // epilogue after phase 2: du, dx and x . du (lanes s, this quarter's 16 p); dB (lanes
     // s, this quarter's 32 n); dC (lanes n, this quarter's 32 t); dY . x. Each
     // warp stages its three float32 boxes (dx 32 x 16 with the 64-byte swizzle,
     // dB and dC 32 x 32 with the 128-byte swizzle; 10 KB) in shared memory
-    // that the phase-3 MMAs no longer read, and stores them by TMA; rows past
+    // that the phase-2 MMAs no longer read, and stores them by TMA; rows past
     // L are clipped by the tensor maps.
     uint8_t *stg = sm + (warp < 6 ? warp * 10240 : kOffHin + (warp - 6) * 10240);
     {
