@@ -481,6 +481,34 @@ def test_backward_tensor_core_shapes(ssd, shape, simt):
     print(f"backward {shape} simt={simt}: " + ", ".join(f"{k} {v:.1e}" for k, v in worst.items()))
 
 
+@pytest.mark.parametrize("shape,optionals", [((1, 2048, 24, 64, 128, 1), False), ((4, 2048, 80, 64, 128, 1), True)])
+def test_backward_full_size_every_element(ssd, shape, optionals):
+    """The sizes the bench times, on the tensor-core path: the 130M-shaped
+    layer at L 2048 with the bench's own inputs (no initial state, no final
+    cotangent), and the 2.7B-shaped layer at B4 L2048 with both; every element
+    of every gradient against the float64 oracle within the bf16 bound (the
+    oracle runs on the host's threads: a few seconds)."""
+    Bz, L, H, P, N, G = shape
+    if optionals:
+        d, dy, dfin = _bwd_case(shape, "bf16", 41)
+    else:
+        d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=0)
+        dy = inputs.round_to(np.random.default_rng(1).standard_normal(d["x"].shape), "bf16")
+        d["init_state"], dfin = None, None
+    ref = oracle.ssd_seq_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dy, d["D"], d["init_state"], dfin)
+    t = torch.bfloat16
+    g = ssd.ssd_scan_chunked_bwd(dev(d["x"], t), dev(d["dt"], t), dev(d["A"]), dev(d["B"], t), dev(d["C"], t),
+                                 dev(dy, t), dev(d["D"]), None if d["init_state"] is None else dev(d["init_state"]),
+                                 None if dfin is None else dev(dfin))
+    torch.cuda.synchronize()
+    if not optionals:
+        ref = {k: v for k, v in ref.items() if k != "dinit"}
+    _check_grads(g, ref, 2e-2, f"bf16 {shape}")
+    worst = {k: float(np.max(np.abs(host(g[k]) - ref[k])) / max(float(np.max(np.abs(ref[k]))), 1e-30))
+             for k in ("dx", "ddt", "dA", "dB", "dC", "dD")}
+    print(f"backward {shape}: " + ", ".join(f"{k} {v:.1e}" for k, v in worst.items()))
+
+
 def test_backward_deterministic_and_without_optionals(ssd):
     """Two runs give the same bits; with no D, no initial state and no final
     cotangent the gradients still match the oracle."""
