@@ -462,8 +462,8 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
 
 // ---------------------------------------------------------------------------
 // Float32 chunk states on the tensor cores, for the backward's chunks of 128
-// tokens (bf16, P 64, N 128), one CTA per (b, chunk, head) and direction
-// (blockIdx.z < B: forward, else adjoint for batch z - B):
+// tokens (bf16, P 64, N 128), one CTA per (b, chunk, one or two heads) and
+// direction (blockIdx.z < B: forward, else adjoint for batch z - B):
 //   forward  S_c[p,n]    = sum_t exp(cs_end - cs_t) dt_t x[t,p] B[t,n]
 //            (and the chunk decay exp(cs_end); block (0, 0, 0) also clears
 //            the status word, this being the call's first kernel)
@@ -481,23 +481,31 @@ struct StateTcParams {
     int *status;
     int64_t B, L, H, G, nc;
 };
-constexpr uint32_t kStOffA = 0, kStOffX = 32768, kStOffV = 49152;
-constexpr uint32_t kStOffBar = kStOffV + (2 * kQ + 16) * 4;
-constexpr uint32_t kStSmem = kStOffBar + 2 * 8 + 16 + 1024;
+// Shared memory of the chunk-state kernel for HB heads per CTA: the B or C
+// tile, HB x / dy tiles, per head the cumulative sums and the weights.
+template <int HB> struct StSmem {
+    static constexpr uint32_t A = 0, X = 32768, V = X + HB * 16384;
+    static constexpr uint32_t Bar = V + (HB * 2 * kQ + 16) * 4;
+    static constexpr uint32_t total = Bar + 2 * 8 + 16 + 1024;
+};
 
+// HB heads per CTA (2 when a group's heads pair up): they share the B or C
+// tile, and one MMA chain of N = 64 HB covers both.
+template <int HB>
 __global__ void __launch_bounds__(kThreads) chunk_states_tc(const __grid_constant__ StateTcParams p) {
+    using SM = StSmem<HB>;
     const bool adj = blockIdx.z >= p.B;
-    const int c = blockIdx.x, h = blockIdx.y;
+    const int c = blockIdx.x, h0 = blockIdx.y * HB;
     const int64_t b = adj ? blockIdx.z - p.B : blockIdx.z;
     const int64_t L = p.L, H = p.H;
-    const int g = (int)(h / (H / p.G));
+    const int g = (int)(h0 / (H / p.G));
     const int64_t t0 = (int64_t)c * kQ;
     const int Qv = (int)imin<int64_t>(kQ, L - t0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *v_cs = reinterpret_cast<float *>(sm + kStOffV), *v_w = v_cs + kQ, *scratch = v_w + kQ;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kStOffBar);
+    float *vec = reinterpret_cast<float *>(sm + SM::V), *scratch = vec + HB * 2 * kQ;  // head k: cs, then w
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::Bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
     if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && p.status) *p.status = SSD_OK;
@@ -508,7 +516,7 @@ __global__ void __launch_bounds__(kThreads) chunk_states_tc(const __grid_constan
         *s_fail = 0;
     }
     if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, 64);
+        tc::tmem_alloc(tmem_slot, 64 * HB);
         tc::tmem_relinquish();
     }
     __syncthreads();
@@ -516,23 +524,30 @@ __global__ void __launch_bounds__(kThreads) chunk_states_tc(const __grid_constan
     const uint32_t tmem = *tmem_slot;
     if (tid == 0) {
         const CUtensorMap *ma = adj ? &p.mc : &p.mb, *mx = adj ? &p.mdy : &p.mx;
-        tc::mbar_arrive_expect_tx(&bars[0], 3u * 16384u);
-        tc::tma_load_3d(sm + kStOffA, ma, &bars[0], g * kN, (int)t0, (int)b);
-        tc::tma_load_3d(sm + kStOffA + 16384, ma, &bars[0], g * kN + 64, (int)t0, (int)b);
-        tc::tma_load_3d(sm + kStOffX, mx, &bars[0], h * kP, (int)t0, (int)b);
+        tc::mbar_arrive_expect_tx(&bars[0], (2u + HB) * 16384u);
+        tc::tma_load_3d(sm + SM::A, ma, &bars[0], g * kN, (int)t0, (int)b);
+        tc::tma_load_3d(sm + SM::A + 16384, ma, &bars[0], g * kN + 64, (int)t0, (int)b);
+#pragma unroll
+        for (int k = 0; k < HB; ++k)
+            tc::tma_load_3d(sm + SM::X + k * 16384, mx, &bars[0], (h0 + k) * kP, (int)t0, (int)b);
     }
-    const float dv = tid < Qv ? __bfloat162float(p.dt[(b * L + t0 + tid) * H + h]) : 0.f;
-    block_inclusive_scan_256(dv * p.A[h], kQ, v_cs, scratch);
-    const float cs_end = v_cs[kQ - 1];
-    if (tid < kQ) v_w[tid] = adj ? expf(v_cs[tid]) : expf(cs_end - v_cs[tid]) * dv;
-    if (!adj && tid == 0) p.chunk_sum[(b * H + h) * p.nc + c] = expf(cs_end);
+#pragma unroll
+    for (int k = 0; k < HB; ++k) {
+        float *v_cs = vec + k * 2 * kQ, *v_w = v_cs + kQ;
+        const float dv = tid < Qv ? __bfloat162float(p.dt[(b * L + t0 + tid) * H + h0 + k]) : 0.f;
+        block_inclusive_scan_256(dv * p.A[h0 + k], kQ, v_cs, scratch);
+        const float cs_end = v_cs[kQ - 1];
+        if (tid < kQ) v_w[tid] = adj ? expf(v_cs[tid]) : expf(cs_end - v_cs[tid]) * dv;
+        if (!adj && tid == 0) p.chunk_sum[(b * H + h0 + k) * p.nc + c] = expf(cs_end);
+    }
     pwait(&bars[0], 0, s_fail);
     __syncthreads();
-    for (int e = tid; e < kQ * 8; e += kThreads) {  // rows of x / dy scaled by the weights
-        const float f = v_w[e >> 3];
+    for (int e = tid; e < HB * kQ * 8; e += kThreads) {  // rows of x / dy scaled by their head's weights
+        const int k = e / (kQ * 8);
+        const float f = vec[k * 2 * kQ + kQ + ((e % (kQ * 8)) >> 3)];
         float xv[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sm + kStOffX + e * 16), xv);
-        *reinterpret_cast<uint4 *>(sm + kStOffX + e * 16) =
+        unpack8(*reinterpret_cast<const uint4 *>(sm + SM::X + e * 16), xv);
+        *reinterpret_cast<uint4 *>(sm + SM::X + e * 16) =
             make_uint4(pack_bf16x2(f * xv[0], f * xv[1]), pack_bf16x2(f * xv[2], f * xv[3]),
                        pack_bf16x2(f * xv[4], f * xv[5]), pack_bf16x2(f * xv[6], f * xv[7]));
     }
@@ -541,8 +556,8 @@ __global__ void __launch_bounds__(kThreads) chunk_states_tc(const __grid_constan
     __syncthreads();
     if (tid == 0 && !*s_fail) {
         tc::tc_fence_after();
-        const uint32_t a0 = tc::smem_u32(sm + kStOffA), x0 = tc::smem_u32(sm + kStOffX);
-        const uint32_t id = tc::idesc_bf16(128, 64, true, true);
+        const uint32_t a0 = tc::smem_u32(sm + SM::A), x0 = tc::smem_u32(sm + SM::X);
+        const uint32_t id = tc::idesc_bf16(128, 64 * HB, true, true);
         for (int k = 0; k < kQ; k += 16)
             tc::mma_bf16(tmem, tc::sdesc_sw128(a0 + k * 128, 16384, 1024), tc::sdesc_sw128(x0 + k * 128, 16384, 1024),
                          id, k > 0);
@@ -551,21 +566,25 @@ __global__ void __launch_bounds__(kThreads) chunk_states_tc(const __grid_constan
     pwait(&bars[1], 0, s_fail);
     tc::tc_fence_after();
     {
-        // lanes n, columns p: for each p the warp's 32 lanes store 32 consecutive n
+        // lanes n, columns (head, p): for each column the warp's 32 lanes store 32 consecutive n
         const int qd = warp & 3, hf = warp >> 2, n = qd * 32 + lane;
-        float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + 32 * hf, v);
-        tc::tmem_ld_wait();
-        float *o = (adj ? p.adj : p.states) + ((b * p.nc + c) * H + h) * (int64_t)kP * kN + n;
+#pragma unroll 1
+        for (int j = 0; j < HB; ++j) {
+            const int col0 = 32 * HB * hf + 32 * j, k = col0 / kP, p0 = col0 % kP;
+            float v[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + col0, v);
+            tc::tmem_ld_wait();
+            float *o = (adj ? p.adj : p.states) + ((b * p.nc + c) * H + h0 + k) * (int64_t)kP * kN + n;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) o[(int64_t)(32 * hf + q) * kN] = v[q];
+            for (int q = 0; q < 32; ++q) o[(int64_t)(p0 + q) * kN] = v[q];
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0 && *s_fail && p.status) atomicCAS(p.status, SSD_OK, SSD_ERR_TIMEOUT);
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 64);
+        tc::tmem_dealloc(tmem, 64 * HB);
     }
 }
 
@@ -692,17 +711,21 @@ cudaError_t launch_bwd_states_tc(const BwdArgs &a, cudaStream_t stream) {
     p.H = a.H;
     p.G = a.G;
     p.nc = a.nc;
-    static DeviceOnce configured;
+    // two heads per CTA when the heads of a group pair up
+    const int hb = (a.H / a.G) % 2 == 0 ? 2 : 1;
+    static DeviceOnce configured[2];
     int dev = 0;
     cudaError_t e = cudaSuccess;
-    if (configured.pending(&dev, &e)) {
-        e = cudaFuncSetAttribute(chunk_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStSmem);
+    auto kern = hb == 2 ? chunk_states_tc<2> : chunk_states_tc<1>;
+    const uint32_t smem = hb == 2 ? StSmem<2>::total : StSmem<1>::total;
+    if (configured[hb - 1].pending(&dev, &e)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured.done(dev);
+        configured[hb - 1].done(dev);
     } else if (e != cudaSuccess) {
         return e;
     }
-    chunk_states_tc<<<dim3((unsigned)a.nc, (unsigned)a.H, (unsigned)(2 * a.B)), kThreads, kStSmem, stream>>>(p);
+    kern<<<dim3((unsigned)a.nc, (unsigned)(a.H / hb), (unsigned)(2 * a.B)), kThreads, smem, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     PassParams q;
     q.states = a.hin;
