@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *v_cs = V + V_CS * kQ, *v_e = V + V_E * kQ, *v_eend = V + V_EEND * kQ, *v_dt = V + V_DT * kQ;
     // sum of the four column quarters' partials of vector k at index i, in a fixed order
-    auto q4sum = [&](int k, int i) { return (V[k * kQ + i] + V[(k + 1) * kQ + i]) + (V[(k + 2) * kQ + i] + V[(k + 3) * kQ + i]); };
+    auto q4sum = [&](int k, int i) {
+        return (V[k * kQ + i] + V[(k + 1) * kQ + i]) + (V[(k + 2) * kQ + i] + V[(k + 3) * kQ + i]);
+    };
 
     if (tid == 0) {
         for (int k = 0; k < 4; ++k) tc::mbar_init(bars + k, 1);
@@ -217,7 +219,9 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     const uint32_t hn0 = tc::smem_u32(sm + kOffHin), gn0 = tc::smem_u32(sm + kOffGn);
     const uint32_t m10 = tc::smem_u32(sm + kOffM1), m20 = tc::smem_u32(sm + kOffM2), xs0 = tc::smem_u32(sm + kOffXs);
     // K-major tile with panels of 64 along K (panel bytes `pb`), K offset k
-    auto kmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + (k >> 6) * pb + (k & 63) * 2, 16, 1024); };
+    auto kmaj = [](uint32_t base, int k, uint32_t pb) {
+        return tc::sdesc_sw128(base + (k >> 6) * pb + (k & 63) * 2, 16, 1024);
+    };
     // MN-major tile: K offset k in rows of 128 bytes, panels of 64 along M/N `pb` apart
     auto mnmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + k * 128, pb, 1024); };
 
@@ -390,7 +394,8 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
             uint8_t *box = stg + 6144 + (lane & 3) * 4;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
-                *reinterpret_cast<float *>(box + u * 128 + (((lane >> 2) ^ (u & 7)) << 4)) = fmaf(v_e[tb + u], yh[u], d1[u]);
+                *reinterpret_cast<float *>(box + u * 128 + (((lane >> 2) ^ (u & 7)) << 4)) =
+                    fmaf(v_e[tb + u], yh[u], d1[u]);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
