@@ -777,6 +777,9 @@ def bench_decode(torch, binding, inputs, dev, hbm_peak, W):
             "tr_ratio": round((tr["read"] + tr["write"]) / step_bytes, 3) if tr else None}
 
 
+MAMBA1_PROBE_MHZ = 2070.0  # the SM clock the pipe-rate probe's rates are per (the GB300's maximum)
+
+
 def bench_mamba1(torch, binding, inputs, dev, hbm_peak, K, W):
     w = inputs.WORKLOADS[MAMBA1]
     Bz, L, Dm, N = w["batch"], w["seqlen"], w["dim"], w["dstate"]
@@ -814,8 +817,17 @@ def bench_mamba1(torch, binding, inputs, dev, hbm_peak, K, W):
     nbytes = 3 * Bz * L * Dm * 2 + 2 * Bz * L * N * 2 + Dm * N * 4 + Dm * 4 + Bz * Dm * N * 4
     gbs = nbytes / (ms / 1e3) / 1e9
     tr = _traffic_record("kernel:diag_scan")
+    # The scan's pipe floor beside its HBM fraction: one ex2 and two packed
+    # float32 FMA-pipe instructions per state update, at the rates the probe
+    # tests/probes/xu_fma_rates.cu measured on GB300 (29.4 ex2 and 59.4
+    # fma.rn.f32x2 per SM per clock), at the device's SM count and maximum clock
+    props = torch.cuda.get_device_properties(dev)
+    sm_hz = MAMBA1_PROBE_MHZ * 1e6
+    per_update = max(1.0 / 29.4, 2.0 / 59.4)  # SM clocks per state update on the busier pipe
+    pipe_floor_s = Bz * L * Dm * N * per_update / (props.multi_processor_count * sm_hz)
     return {"w": MAMBA1, "q": best, "us": round(ms * 1e3, 1), "std": round(sd * 1e3, 1), "one_us": round(one * 1e3, 1),
             "Mtok_s": round(Bz * L / ms / 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+            "pipe_floor_us": round(pipe_floor_s * 1e6, 1), "pipe_frac": round(pipe_floor_s / (ms / 1e3), 4),
             "tr_ratio": round((tr["read"] + tr["write"]) / nbytes, 3) if tr else None,
             "sweep_us": [round(sweep[k] * 1e3, 1) for k in (256, 512, 1024, 2048)]}
 
