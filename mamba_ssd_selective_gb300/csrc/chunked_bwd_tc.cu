@@ -75,7 +75,7 @@ enum {
 };
 constexpr uint32_t kOffRed = kOffV + kNV * kQ * 4;               // kBT partial sums + 16 scratch
 constexpr uint32_t kOffBar = kOffRed + (kBT + 16) * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 4 * 8 + 16 + 1024;
+constexpr uint32_t kSmemBytes = kOffBar + 8 * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "one CTA per SM with the maximum opt-in shared memory");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     float *V = reinterpret_cast<float *>(sm + kOffV);
     float *red = reinterpret_cast<float *>(sm + kOffRed), *scratch = red + kBT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *v_cs = V + V_CS * kQ, *v_e = V + V_E * kQ, *v_eend = V + V_EEND * kQ, *v_dt = V + V_DT * kQ;
     // sum of the four column quarters' partials of vector k at index i, in a fixed order
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     };
 
     if (tid == 0) {
-        for (int k = 0; k < 4; ++k) tc::mbar_init(bars + k, 1);
+        for (int k = 0; k < 5; ++k) tc::mbar_init(bars + k, 1);
         tc::fence_mbar_init();
         *s_fail = 0;
     }
@@ -231,9 +231,10 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         const uint32_t id128 = tc::idesc_bf16(128, 128, false, false), id64 = tc::idesc_bf16(128, 64, false, false);
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(b0, k, 16384), kmaj(c0, k, 16384), id128, k > 0);
         for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(x0, k, 0), kmaj(y0, k, 0), id128, k > 0);
+        tc::mma_commit(&bars[1]);  // the scores: the epilogue starts on them
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T2, kmaj(c0, k, 16384), kmaj(hn0, k, 8192), id64, k > 0);
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T3, kmaj(b0, k, 16384), kmaj(gn0, k, 8192), id64, k > 0);
-        tc::mma_commit(&bars[1]);
+        tc::mma_commit(&bars[3]);
     }
     pwait(&bars[1], 0, s_fail);
     tc::tc_fence_after();
@@ -289,6 +290,8 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
             }
         }
         V[(V_ROW + qd) * kQ + tb + lane] = bc[0];
+        pwait(&bars[3], 0, s_fail);
+        tc::tc_fence_after();
         float gb[16], hc[16];
         tc::tmem_ld16(T3 + lq + 16 * cq, gb);
         tc::tmem_ld16(T2 + lq + 16 * cq, hc);
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         // du = M1^T dY: A rows s (K = t), B = dy as MN-major (N = p, K = t)
         const uint32_t idu = tc::idesc_bf16(128, 64, false, true);
         for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T2, kmaj(m10, k, 16384), mnmaj(y0, k, 16384), idu, k > 0);
+        tc::mma_commit(&bars[4]);  // du: dx is formed while the rest run
         // dB = M2^T C + Xs Gn: B operands MN-major (N = n)
         const uint32_t idb = tc::idesc_bf16(128, 128, false, true);
         for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T0, kmaj(m20, k, 16384), mnmaj(c0, k, 16384), idb, k > 0);
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, mnmaj(hn0, k, 8192), kmaj(y0, k, 0), idy, k > 0);
         tc::mma_commit(&bars[2]);
     }
-    pwait(&bars[2], 0, s_fail);
+    pwait(&bars[4], 0, s_fail);
     tc::tc_fence_after();
     const float Dh = a.D ? a.D[h] : 0.f;
     // epilogue after phase 2: du, dx and x . du (lanes s, this quarter's 16 p); dB (lanes
@@ -363,6 +367,9 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         }
         V[(V_XDU + cq) * kQ + s] = xd;
         V[(V_DD + cq) * kQ + s] = yxd;
+        // the staging regions are operands of the remaining phase-2 MMAs
+        pwait(&bars[2], 0, s_fail);
+        tc::tc_fence_after();
         // dx box: rows of 64 bytes, 16-byte piece k of row r at k ^ ((r >> 1) & 3)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
