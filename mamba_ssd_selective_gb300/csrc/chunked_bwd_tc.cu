@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     };
 
     if (tid == 0) {
-        for (int k = 0; k < 5; ++k) tc::mbar_init(bars + k, 1);
+        for (int k = 0; k < 6; ++k) tc::mbar_init(bars + k, 1);
         tc::fence_mbar_init();
         *s_fail = 0;
     }
@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         const uint32_t idb = tc::idesc_bf16(128, 128, false, true);
         for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T0, kmaj(m20, k, 16384), mnmaj(c0, k, 16384), idb, k > 0);
         for (int k = 0; k < kP; k += 16) tc::mma_bf16(T0, kmaj(xs0, k, 0), mnmaj(gn0, k, 8192), idb, 1u);
+        tc::mma_commit(&bars[5]);  // dB: C, Gn, Xs and M1 are free from here
         // dC1^T = B^T M2^T: rows n (A = B as MN-major, M = n), N = t (M2^T as MN-major)
         const uint32_t idc = tc::idesc_bf16(128, 128, true, true);
         for (int k = 0; k < kQ; k += 16) tc::mma_bf16(T4, mnmaj(b0, k, 16384), mnmaj(m20, k, 16384), idc, k > 0);
@@ -340,10 +341,13 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     // epilogue after phase 2: du, dx and x . du (lanes s, this quarter's 16 p); dB (lanes
     // s, this quarter's 32 n); dC (lanes n, this quarter's 32 t); dY . x. Each
     // warp stages its three float32 boxes (dx 32 x 16 with the 64-byte swizzle,
-    // dB and dC 32 x 32 with the 128-byte swizzle; 10 KB) in shared memory
-    // that the phase-2 MMAs no longer read, and stores them by TMA; rows past
-    // L are clipped by the tensor maps.
-    uint8_t *stg = sm + (warp < 6 ? warp * 10240 : kOffHin + (warp - 6) * 10240);
+    // dB and dC 32 x 32 with the 128-byte swizzle) in shared memory that the
+    // phase-2 MMAs still running no longer read -- dx in Gn / Xs and dB in C / M1
+    // once du and dB are done, dC in B / M2 once every product is -- and
+    // stores them by TMA; rows past L are clipped by the tensor maps.
+    uint8_t *stg_dx = sm + (warp < 8 ? kOffGn + warp * 2048 : kOffXs + (warp - 8) * 2048);
+    uint8_t *stg_db = sm + (warp < 8 ? kOffC + warp * 4096 : kOffM1 + (warp - 8) * 4096);
+    uint8_t *stg_dc = sm + (warp < 8 ? kOffB + warp * 4096 : kOffM2 + (warp - 8) * 4096);
     {
         const int s = row;
         float du[16], gb[16];
@@ -367,13 +371,12 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         }
         V[(V_XDU + cq) * kQ + s] = xd;
         V[(V_DD + cq) * kQ + s] = yxd;
-        // the staging regions are operands of the remaining phase-2 MMAs
-        pwait(&bars[2], 0, s_fail);
+        pwait(&bars[5], 0, s_fail);
         tc::tc_fence_after();
         // dx box: rows of 64 bytes, 16-byte piece k of row r at k ^ ((r >> 1) & 3)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<float4 *>(stg + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+            *reinterpret_cast<float4 *>(stg_dx + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
                 make_float4(dxv[4 * k], dxv[4 * k + 1], dxv[4 * k + 2], dxv[4 * k + 3]);
         {
             float v[32];
@@ -381,24 +384,26 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
             tc::tmem_ld_wait();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                *reinterpret_cast<float4 *>(stg + 2048 + swz(lane, k)) =
+                *reinterpret_cast<float4 *>(stg_db + swz(lane, k)) =
                     make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qd * 32 < Qv) {
             const int rs = (int)t0 + qd * 32;
-            tc::tma_store_3d(&prm.mdx, stg, h * kP + 16 * cq, rs, (int)b);
-            tc::tma_store_3d(&prm.mdb, stg + 2048, h * kN + 32 * cq, rs, (int)b);
+            tc::tma_store_3d(&prm.mdx, stg_dx, h * kP + 16 * cq, rs, (int)b);
+            tc::tma_store_3d(&prm.mdb, stg_db, h * kN + 32 * cq, rs, (int)b);
             tc::bulk_commit();
         }
+        pwait(&bars[2], 0, s_fail);
+        tc::tc_fence_after();
         {
             const int tb = 32 * cq;
             float d1[32], yh[32];
             tc::tmem_ld32(T4 + lq + tb, d1);
             tc::tmem_ld32(T1 + lq + tb, yh);
             tc::tmem_ld_wait();
-            uint8_t *box = stg + 6144 + (lane & 3) * 4;
+            uint8_t *box = stg_dc + (lane & 3) * 4;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
                 *reinterpret_cast<float *>(box + u * 128 + (((lane >> 2) ^ (u & 7)) << 4)) =
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (32 * cq < Qv) tc::tma_store_3d(&prm.mdc, stg + 6144, h * kN + 32 * qd, (int)t0 + 32 * cq, (int)b);
+            if (32 * cq < Qv) tc::tma_store_3d(&prm.mdc, stg_dc, h * kN + 32 * qd, (int)t0 + 32 * cq, (int)b);
             tc::bulk_commit();
         }
     }
