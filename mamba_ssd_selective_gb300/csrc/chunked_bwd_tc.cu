@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     };
 
     if (tid == 0) {
-        for (int k = 0; k < 6; ++k) tc::mbar_init(bars + k, 1);
+        for (int k = 0; k < 7; ++k) tc::mbar_init(bars + k, 1);
         tc::fence_mbar_init();
         *s_fail = 0;
     }
@@ -148,15 +148,15 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
     const uint32_t T0 = tmem, T1 = tmem + 128, T2 = tmem + 256, T3 = tmem + 320, T4 = tmem + 384;
 
-    // x, dy, B, C of the chunk by TMA (rows past L read as zero); h_in and Gn
-    // (float32 [p][n], contiguous per (b, chunk, head)) by bulk copies into
-    // the M1^T / M2^T regions, which epilogue B fills later
-    // The call's inputs are read before the wait for the state passes (this
-    // kernel is their programmatic dependent), the states after it; only the
-    // thread that issues the copies waits.
+    // x, dy, B, C of the chunk by TMA (rows past L read as zero) on one
+    // barrier; h_in and Gn (float32 [p][n], contiguous per (b, chunk, head)) by
+    // bulk copies into the M1^T / M2^T regions, which epilogue 1 fills later, on
+    // another. The call's inputs are read before the wait for the state passes
+    // (this kernel is their programmatic dependent), the states after it; only
+    // the thread that issues the copies waits.
     const int64_t so = ((b * nc + c) * H + h) * (int64_t)kP * kN;
     if (tid == 0) {
-        tc::mbar_arrive_expect_tx(&bars[0], 6u * 16384u + 2u * 32768u);
+        tc::mbar_arrive_expect_tx(&bars[0], 6u * 16384u);
         tc::tma_load_3d(sm + kOffX, &prm.mx, &bars[0], h * kP, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffY, &prm.mdy, &bars[0], h * kP, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffB, &prm.mb, &bars[0], g * kN, (int)t0, (int)b);
@@ -164,8 +164,9 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         tc::tma_load_3d(sm + kOffC, &prm.mc, &bars[0], g * kN, (int)t0, (int)b);
         tc::tma_load_3d(sm + kOffC + 16384, &prm.mc, &bars[0], g * kN + 64, (int)t0, (int)b);
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        tc::bulk_load(sm + kOffM1, a.hin + so, (uint32_t)(kP * kN * 4), &bars[0]);
-        tc::bulk_load(sm + kOffM2, a.adj + so, (uint32_t)(kP * kN * 4), &bars[0]);
+        tc::mbar_arrive_expect_tx(&bars[6], 2u * 32768u);
+        tc::bulk_load(sm + kOffM1, a.hin + so, (uint32_t)(kP * kN * 4), &bars[6]);
+        tc::bulk_load(sm + kOffM2, a.adj + so, (uint32_t)(kP * kN * 4), &bars[6]);
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // dt and its cumulative sum over the chunk (padded tokens carry dt = 0)
@@ -178,7 +179,29 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         v_e[tid] = expf(v_cs[tid]);
         v_eend[tid] = expf(cs_end - v_cs[tid]);
     }
+
+    const uint32_t c0 = tc::smem_u32(sm + kOffC), b0 = tc::smem_u32(sm + kOffB);
+    const uint32_t x0 = tc::smem_u32(sm + kOffX), y0 = tc::smem_u32(sm + kOffY);
+    const uint32_t hn0 = tc::smem_u32(sm + kOffHin), gn0 = tc::smem_u32(sm + kOffGn);
+    const uint32_t m10 = tc::smem_u32(sm + kOffM1), m20 = tc::smem_u32(sm + kOffM2), xs0 = tc::smem_u32(sm + kOffXs);
+    // K-major tile with panels of 64 along K (panel bytes `pb`), K offset k
+    auto kmaj = [](uint32_t base, int k, uint32_t pb) {
+        return tc::sdesc_sw128(base + (k >> 6) * pb + (k & 63) * 2, 16, 1024);
+    };
+    // MN-major tile: K offset k in rows of 128 bytes, panels of 64 along M/N `pb` apart
+    auto mnmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + k * 128, pb, 1024); };
+    const uint32_t id128 = tc::idesc_bf16(128, 128, false, false), id64 = tc::idesc_bf16(128, 64, false, false);
+
+    // ---- phase 1a: BC = B C^T, XY = X dY^T (rows s: the transposed scores), as
+    // soon as the tiles are in, while the states are rounded below
     pwait(&bars[0], 0, s_fail);
+    if (tid == 0 && !*s_fail) {
+        tc::tc_fence_after();
+        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(b0, k, 16384), kmaj(c0, k, 16384), id128, k > 0);
+        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(x0, k, 0), kmaj(y0, k, 0), id128, k > 0);
+        tc::mma_commit(&bars[1]);
+    }
+    pwait(&bars[6], 0, s_fail);
     __syncthreads();
     // h_in and Gn into bf16 tiles (rows p, panels of 64 n), 8 n per 16-byte
     // piece; <Gn, h_in> in float32 on the way
@@ -214,24 +237,9 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
     tc::tc_fence_before();
     __syncthreads();
 
-    const uint32_t c0 = tc::smem_u32(sm + kOffC), b0 = tc::smem_u32(sm + kOffB);
-    const uint32_t x0 = tc::smem_u32(sm + kOffX), y0 = tc::smem_u32(sm + kOffY);
-    const uint32_t hn0 = tc::smem_u32(sm + kOffHin), gn0 = tc::smem_u32(sm + kOffGn);
-    const uint32_t m10 = tc::smem_u32(sm + kOffM1), m20 = tc::smem_u32(sm + kOffM2), xs0 = tc::smem_u32(sm + kOffXs);
-    // K-major tile with panels of 64 along K (panel bytes `pb`), K offset k
-    auto kmaj = [](uint32_t base, int k, uint32_t pb) {
-        return tc::sdesc_sw128(base + (k >> 6) * pb + (k & 63) * 2, 16, 1024);
-    };
-    // MN-major tile: K offset k in rows of 128 bytes, panels of 64 along M/N `pb` apart
-    auto mnmaj = [](uint32_t base, int k, uint32_t pb) { return tc::sdesc_sw128(base + k * 128, pb, 1024); };
-
-    // ---- phase 1: BC = B C^T, XY = X dY^T (rows s: the transposed scores), HC, GB
+    // ---- phase 1b: HC = C h_in^T (rows t), GB = B Gn^T (rows s)
     if (tid == 0 && !*s_fail) {
         tc::tc_fence_after();
-        const uint32_t id128 = tc::idesc_bf16(128, 128, false, false), id64 = tc::idesc_bf16(128, 64, false, false);
-        for (int k = 0; k < kN; k += 16) tc::mma_bf16(T0, kmaj(b0, k, 16384), kmaj(c0, k, 16384), id128, k > 0);
-        for (int k = 0; k < kP; k += 16) tc::mma_bf16(T1, kmaj(x0, k, 0), kmaj(y0, k, 0), id128, k > 0);
-        tc::mma_commit(&bars[1]);  // the scores: the epilogue starts on them
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T2, kmaj(c0, k, 16384), kmaj(hn0, k, 8192), id64, k > 0);
         for (int k = 0; k < kN; k += 16) tc::mma_bf16(T3, kmaj(b0, k, 16384), kmaj(gn0, k, 8192), id64, k > 0);
         tc::mma_commit(&bars[3]);
