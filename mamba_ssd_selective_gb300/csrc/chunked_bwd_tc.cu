@@ -55,6 +55,7 @@ struct BwdTcParams {
     CUtensorMap mx, mdy, mb, mc;  // bf16 inputs, boxes 64 x 128
     CUtensorMap mdx;              // float32 dx, boxes 16 x 32 (64-byte swizzle)
     CUtensorMap mdb, mdc;         // float32 dB and dC parts, boxes 32 x 32 (128-byte swizzle)
+    int64_t prefetch_ahead;       // items between a CTA and the one whose tiles it prefetches (0: none)
 };
 
 // shared memory (bytes from the 1024-aligned base)
@@ -167,6 +168,18 @@ __global__ void __launch_bounds__(kBT, 1) chunk_bwd_tc_kernel(const __grid_const
         tc::mbar_arrive_expect_tx(&bars[6], 2u * 32768u);
         tc::bulk_load(sm + kOffM1, a.hin + so, (uint32_t)(kP * kN * 4), &bars[6]);
         tc::bulk_load(sm + kOffM2, a.adj + so, (uint32_t)(kP * kN * 4), &bars[6]);
+        // into L2 ahead of time: the per-head tiles of the item one CTA per SM
+        // later in launch order, which starts about when this one ends
+        const int64_t nxt = ((b * H + h) * nc + c) + prm.prefetch_ahead;
+        if (prm.prefetch_ahead > 0 && nxt < nc * H * a.B) {
+            const int c_ = (int)(nxt % nc), h_ = (int)((nxt / nc) % H);
+            const int64_t b_ = nxt / (nc * H);
+            const int64_t so_ = ((b_ * nc + c_) * H + h_) * (int64_t)kP * kN;
+            tc::prefetch_l2_3d(&prm.mx, h_ * kP, c_ * kQ, (int)b_);
+            tc::prefetch_l2_3d(&prm.mdy, h_ * kP, c_ * kQ, (int)b_);
+            tc::prefetch_l2(a.hin + so_, (uint32_t)(kP * kN * 4));
+            tc::prefetch_l2(a.adj + so_, (uint32_t)(kP * kN * 4));
+        }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // dt and its cumulative sum over the chunk (padded tokens carry dt = 0)
@@ -685,6 +698,11 @@ cudaError_t launch_chunk_bwd_tc(const BwdArgs &a, cudaStream_t stream) {
     ok &= tma_map_tokens_f32(&p.mdb, a.dB_part, a.H * a.N, a.L, a.B, 32);
     ok &= tma_map_tokens_f32(&p.mdc, a.dC_part, a.H * a.N, a.L, a.B, 32);
     if (!ok) return cudaErrorInvalidValue;
+    // one CTA per SM: prefetch one SM count ahead, on grids of four waves or
+    // more (measured: B4 L2048 H80 734 -> 725 us; at 2.5 waves, B1 L2048 H24,
+    // it cost ~1 us)
+    const int64_t sms = sm_count(152);
+    p.prefetch_ahead = a.nc * a.H * a.B >= 4 * sms ? sms : 0;
     static DeviceOnce configured;
     int dev = 0;
     cudaError_t e = cudaSuccess;
