@@ -20,16 +20,21 @@
 // chunk continuing from the previous chunk's state", "Recurrence Scan", first
 // section). The carry of the last chunk is the final state.
 //
-// A work item is a run of gc consecutive chunks of one chain (b, head pair):
-// inside it the state stays in TMEM from chunk to chunk; between items it is
-// carried in float32 through global memory (L2). Items are ordered
-// chunk-major (U = ((s B + b) nhg + hg), s the item's place in its chain),
-// and each CTA takes U = blockIdx.x, blockIdx.x + gridDim.x, ... in order:
-// item s of a chain waits (bounded) on a flag that item s - 1 sets once its
-// carry is written, and that item was taken earlier in the same order by a
-// CTA that is resident (the grid is at most one CTA per SM), so every wait
-// ends; with B * H / 2 chains between a chain's consecutive items, the wait
-// is normally already satisfied when it is reached.
+// Work is balanced by chunks: the chains (b, head pair), each of nc chunks,
+// are laid end to end (chain j = b nhg + hg, then its chunks in order) and
+// CTA i takes the i-th of gridDim.x equal segments of that sequence (to one
+// chunk). A segment splits into work items at chain boundaries: the tail of
+// the chain it begins in (a continuation, when the segment starts inside a
+// chain), whole chains, and the head of the chain it ends in (a prefix, when
+// it ends inside one). Inside an item the state stays in TMEM from chunk to
+// chunk; between items it is carried in float32 through global memory (L2).
+// A CTA runs its prefix first, then its whole chains, then its continuation,
+// which waits (bounded) on a flag that the previous CTA's prefix of the same
+// chain sets once its carry is written. With the grid at most one CTA per
+// SM and at most one per chain, a segment is at least one chain long, so a
+// chain spans at most two CTAs, every prefix starts at chunk 0 and waits on
+// nothing, and every wait ends; the previous CTA runs that prefix first, so
+// the wait is normally already satisfied when it is reached.
 //
 // TMEM (512 columns): S [0,128), Y [128,256) (64 per head), the carried state
 // [256,384) (lanes = n, columns = (k, p): a warp's 32 lanes are 32
@@ -82,10 +87,7 @@ struct FusedParams {
     ChunkedArgs a;
     CUtensorMap mx, mb, mc, my;  // my: y in boxes of 32 rows x 32 columns (one output warp's part)
     int nhg;          // head pairs, H / 2
-    int gc;           // chunks per work item
-    int64_t nsc;      // work items per chain, ceil(nc / gc)
-    int64_t n_items;  // B * nsc * nhg
-    int *flags;       // [B][nhg][nsc]: 1 once the state leaving item s is in `carry`
+    int *flags;       // [B][nhg][nc]: 1 once the state leaving chunk c is in `carry`
     float *carry;     // [B][H][P][N] float32 carried state (the final state at the end)
 };
 
@@ -166,8 +168,8 @@ __global__ void fused_init(int *status, int *flags, int64_t nflags) {
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_constant__ FusedParams prm) {
     const ChunkedArgs &a = prm.a;
-    const int nhg = prm.nhg, gc = prm.gc;
-    const int64_t n_items = prm.n_items, nc = a.nc, nsc = prm.nsc, Bsz = a.B;
+    const int nhg = prm.nhg;
+    const int64_t nc = a.nc, Bsz = a.B;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     extern __shared__ uint8_t smem_raw[];
@@ -179,28 +181,62 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
     volatile int *s_fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    // work item U -> (b, place s in its chain, head pair hg)
-    auto decode = [&](int64_t U, int64_t &b, int64_t &sc, int &hg) {
-        hg = (int)(U % nhg);
-        const int64_t t = U / nhg;
-        b = t % Bsz;
-        sc = t / Bsz;
+    // This CTA's work items, set up once by thread 0 (below) in static shared
+    // memory: s_seg = {prefix chain, prefix end, first whole chain,
+    // continuation chain, continuation start, continuation end} and s_nseg =
+    // {prefixes (0 or 1), whole chains, continuations (0 or 1)}.
+    __shared__ int s_seg[6];
+    __shared__ int s_nseg[3];
+    // item k of this CTA, in the order it runs them: the prefix, the whole
+    // chains, the continuation
+    auto item_at = [&](int k, int &j, int &c0, int &c1) {
+        if (k < s_nseg[0]) {
+            j = s_seg[0], c0 = 0, c1 = s_seg[1];
+        } else if (k < s_nseg[0] + s_nseg[1]) {
+            j = s_seg[2] + (k - s_nseg[0]), c0 = 0, c1 = (int)nc;
+        } else {
+            j = s_seg[3], c0 = s_seg[4], c1 = s_seg[5];
+        }
+    };
+    // item(j, c0, c1) for each work item of this CTA; stops when item returns false
+    auto for_items = [&](auto &&item) {
+        const int n = s_nseg[0] + s_nseg[1] + s_nseg[2];
+        for (int k = 0; k < n; ++k) {
+            int j, c0, c1;
+            item_at(k, j, c0, c1);
+            if (!item(j, c0, c1)) return;
+        }
     };
     // body(b, c, hg, it, first, last) for each chunk of this CTA's items, in
     // order (it counts them); stops when body returns false
     auto for_chunks = [&](auto &&body) {
         uint32_t it = 0;
-        for (int64_t U = blockIdx.x; U < n_items; U += gridDim.x) {
-            int64_t b, sc;
-            int hg;
-            decode(U, b, sc, hg);
-            const int64_t c0 = sc * gc, c1 = imin<int64_t>(nc, c0 + gc);
-            for (int64_t c = c0; c < c1; ++c, ++it)
-                if (!body(b, c, hg, it, c == c0, c + 1 == c1)) return;
-        }
+        for_items([&](int j, int c0, int c1) -> bool {
+            const int bi = j / nhg, hg = j - bi * nhg;
+            for (int c = c0; c < c1; ++c, ++it)
+                if (!body((int64_t)bi, (int64_t)c, hg, it, c == c0, c + 1 == c1)) return false;
+            return true;
+        });
     };
 
     if (tid == 0) {
+        // the chunks [start, end) of the chains laid end to end, split at chain boundaries
+        const int64_t total = Bsz * nhg * nc, G = gridDim.x;
+        const int64_t start = (int64_t)blockIdx.x * total / G, end = ((int64_t)blockIdx.x + 1) * total / G;
+        s_nseg[0] = s_nseg[1] = s_nseg[2] = 0;
+        if (start < end) {
+            const int64_t j0 = start / nc, j1 = (end - 1) / nc, cs = start % nc, ce = (end - 1) % nc + 1;
+            if (j0 == j1 && (cs > 0 || ce < nc)) {
+                s_seg[3] = (int)j0, s_seg[4] = (int)cs, s_seg[5] = (int)ce;  // a part of one chain
+                s_nseg[2] = 1;
+            } else {
+                if (ce < nc) s_seg[0] = (int)j1, s_seg[1] = (int)ce, s_nseg[0] = 1;
+                const int64_t jf0 = cs > 0 ? j0 + 1 : j0, jf1 = ce < nc ? j1 - 1 : j1;
+                s_seg[2] = (int)jf0;
+                s_nseg[1] = jf1 >= jf0 ? (int)(jf1 - jf0 + 1) : 0;
+                if (cs > 0) s_seg[3] = (int)j0, s_seg[4] = (int)cs, s_seg[5] = (int)nc, s_nseg[2] = 1;
+            }
+        }
         for (int k = 0; k < kBars; ++k) tc::mbar_init(bars + k, 1);
         const int group_counted[] = {BAR_S_EMPTY,    BAR_WX_FULL,   BAR_HIN_FULL,  BAR_P_FULL,
                                      BAR_P_FULL + 1, BAR_ACC_EMPTY, BAR_CARRY_DONE};
@@ -525,14 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
         // earlier item finds its flag set by an earlier iteration of this loop.
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t U = blockIdx.x; U < n_items; U += gridDim.x, ++it) {
-                int64_t b, sc;
-                int hg;
-                decode(U, b, sc, hg);
-                const int64_t n_flags = Bsz * nhg * nsc;
-                (void)n_flags;
-                if (sc > 0 && !*s_fail && SSD_IN_BOUNDS((b * nhg + hg) * nsc + (sc - 1), 1, n_flags, kSiteFusedFlags)) {
-                    const int *fp = prm.flags + ((b * nhg + hg) * nsc + (sc - 1));
+            const int64_t n_flags = Bsz * nhg * nc;
+            (void)n_flags;
+            for_items([&](int j, int c0, int c1) -> bool {
+                if (c0 > 0 && !*s_fail && SSD_IN_BOUNDS(j * nc + (c0 - 1), 1, n_flags, kSiteFusedFlags)) {
+                    const int *fp = prm.flags + (j * nc + (c0 - 1));
                     if (ld_acquire(fp) == 0) {
                         const uint64_t t0 = tc::global_ns();
                         while (ld_acquire(fp) == 0) {
@@ -545,10 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
                     }
                 }
                 tc::mbar_arrive(&bars[BAR_FLAG_OK]);
-                if (!pwait(&bars[BAR_CARRY_DONE], it & 1, s_fail)) break;
-                if (sc + 1 < nsc && !*s_fail && SSD_IN_BOUNDS((b * nhg + hg) * nsc + sc, 1, n_flags, kSiteFusedFlags))
-                    st_release(prm.flags + ((b * nhg + hg) * nsc + sc), 1);
-            }
+                if (!pwait(&bars[BAR_CARRY_DONE], it & 1, s_fail)) return false;
+                ++it;
+                if (c1 < nc && !*s_fail && SSD_IN_BOUNDS(j * nc + (c1 - 1), 1, n_flags, kSiteFusedFlags))
+                    st_release(prm.flags + (j * nc + (c1 - 1)), 1);
+                return true;
+            });
         }
     } else {
         // ---------------------------------------------------- output group
@@ -708,25 +743,10 @@ bool chunked_fused_supported(const ChunkedArgs &a) {
     return device_cc_major_cached() == 10;
 }
 
-// Chunks per work item: the largest of 1, 2, 4 and 8 that still leaves at
-// least four work items per SM, so that the busiest SM runs few more chunks
-// than the average (runs of chunks keep the state on chip: fewer round trips
-// through L2 and fewer waits between items). Measured on GB300 (chunks per
-// item 2 / 4 / 8 / 16): B8 L2048 H80 207 / 202 / 200 / 225 us, B4 L2048 H80
-// 113 / 108 / 120 / 153 us.
-int fused_chunks_per_item(const ChunkedArgs &a) {
-    const int64_t chains = a.B * (a.H / kHB), want = 4 * (int64_t)sm_count(152);
-    int gc = 1;
-    for (int g = 2; g <= 8; g *= 2)
-        if (chains * ((a.nc + g - 1) / g) >= want) gc = g;
-    return gc;
-}
-
-// The single pass wins when the chains (b, head pair) are many: the item that
-// continues a chain is then taken B * H / 2 items after its predecessor, time
-// enough for the carried state to arrive; with few chains the items wait on
-// one another and the three-kernel path, whose state pass runs every state
-// element in parallel, is faster. Measured on GB300 (graph of back-to-back
+// The single pass wins when the chains (b, head pair) are many: every SM then
+// runs at least one whole chain's worth of chunks; with few chains a chain's
+// chunks run one after another on few SMs and the three-kernel path, whose
+// state pass runs every state element in parallel, is faster. Measured on GB300 (graph of back-to-back
 // calls, inputs past L2): 160 and 320 chains (B4 / B8, L2048, H80) 115 / 205
 // us against 136 / 251 us; 96 chains (B8 L2048 H24) 110 against 83 us.
 bool chunked_fused_preferred(const ChunkedArgs &a) { return a.B * (a.H / kHB) >= (int64_t)sm_count(152); }
@@ -742,10 +762,7 @@ cudaError_t launch_chunked_fused(const ChunkedArgs &a, cudaStream_t stream) {
     ok &= tma_map_tokens(&p.my, a.y, a.H * a.P, a.L, a.B, 32, 32);
     if (!ok) return cudaErrorInvalidValue;
     p.nhg = (int)(a.H / kHB);
-    p.gc = fused_chunks_per_item(a);
-    p.nsc = (a.nc + p.gc - 1) / p.gc;
-    p.n_items = a.B * p.nsc * p.nhg;
-    // the chain flags reuse the per-chunk decay area ([B, H, nc] floats >= [B, H/2, nsc] ints);
+    // the chain flags reuse the per-chunk decay area ([B, H, nc] floats >= [B, H/2, nc] ints);
     // the carry is the caller's final state, else the per-chunk state area
     p.flags = reinterpret_cast<int *>(a.chunk_sum);
     p.carry = a.final_state ? a.final_state : a.states;
@@ -767,7 +784,7 @@ cudaError_t launch_chunked_fused(const ChunkedArgs &a, cudaStream_t stream) {
     const bool staged = a.stage_ev[0] != nullptr;
     cudaError_t e = mark_stage(a, 0, stream);
     if (e != cudaSuccess) return e;
-    const int64_t nflags = a.B * p.nhg * p.nsc;
+    const int64_t nflags = a.B * p.nhg * a.nc;
     const unsigned init_blocks = (unsigned)imin<int64_t>((nflags + 255) / 256, 64);
     if (staged) {
         fused_init<<<init_blocks, 256, 0, stream>>>(a.status, p.flags, nflags);
@@ -778,7 +795,9 @@ cudaError_t launch_chunked_fused(const ChunkedArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if ((e = mark_stage(a, 1, stream)) != cudaSuccess) return e;
     if ((e = mark_stage(a, 2, stream)) != cudaSuccess) return e;
-    const int64_t grid = imin<int64_t>(p.n_items, sm_count(1));
+    // one CTA per SM, and no more CTAs than chains, so that a segment holds at
+    // least one chain's worth of chunks
+    const int64_t grid = imin<int64_t>(a.B * p.nhg, sm_count(1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
