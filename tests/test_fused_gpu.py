@@ -50,6 +50,21 @@ def test_fused_every_element(ssd, shape, init):
     print(f"fused {shape} init={init}: y {rel(y, yr):.2e}, final_state {rel(h, hr):.2e} (bound {BF16_REL_MAX})")
 
 
+@pytest.mark.parametrize("shape", [(2, 1000, 160, 64, 128, 1), (3, 520, 112, 64, 128, 4)])
+def test_fused_chains_split_between_ctas(ssd, shape):
+    """More chains (b, head pair) than SMs: each CTA takes an equal segment of
+    the chains laid end to end, so chains are split between two CTAs (a
+    prefix handing its state to the next CTA's continuation); ragged last
+    chunks, one and four B/C groups: every element of y and the final state."""
+    Bz, L, H, P, N, G = shape
+    d = inputs.ssd_inputs(Bz, L, H, P, N, G, io_dtype="bf16", seed=25, init_state=True)
+    yr, hr = oracle.ssd_seq(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"])
+    y, h = run(ssd, d, "fused")
+    check("bf16", y, yr, f"y {shape}")
+    check("bf16", h, hr, f"final_state {shape}")
+    print(f"fused split chains {shape}: y {rel(y, yr):.2e}, final_state {rel(h, hr):.2e} (bound {BF16_REL_MAX})")
+
+
 def test_fused_without_D_and_final_state(ssd):
     """D = NULL adds nothing on the diagonal; with final_state = NULL the carry
     lives in the workspace and y is unchanged."""
