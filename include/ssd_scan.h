@@ -112,9 +112,9 @@ int ssd_best_chunk(const ssd_dims *dims);
  * invalid or SSD_FLAG_FUSED is set for sizes the single pass does not take.
  * Without flags the single pass is taken for bf16, headdim 64, dstate 128,
  * chunk 128 and an even number of heads per group when batch * nheads / 2 is
- * at least the SM count: every SM then runs at least one whole chain (b, head
- * pair) of chunks, and a chain split between two SMs hands its carried state
- * over once.
+ * at least 0.6 times the SM count: it runs at least one whole chain (b, head
+ * pair) of chunks per SM, and a chain split between two SMs hands its
+ * carried state over once.
  * Host-only: no launch, no synchronisation.
  */
 int ssd_scan_path(const ssd_dims *dims, int chunk_size);

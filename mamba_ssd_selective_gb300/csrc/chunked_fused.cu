@@ -743,13 +743,18 @@ bool chunked_fused_supported(const ChunkedArgs &a) {
     return device_cc_major_cached() == 10;
 }
 
-// The single pass wins when the chains (b, head pair) are many: every SM then
-// runs at least one whole chain's worth of chunks; with few chains a chain's
-// chunks run one after another on few SMs and the three-kernel path, whose
-// state pass runs every state element in parallel, is faster. Measured on GB300 (graph of back-to-back
-// calls, inputs past L2): 160 and 320 chains (B4 / B8, L2048, H80) 115 / 205
-// us against 136 / 251 us; 96 chains (B8 L2048 H24) 110 against 83 us.
-bool chunked_fused_preferred(const ChunkedArgs &a) { return a.B * (a.H / kHB) >= (int64_t)sm_count(152); }
+// The single pass runs one chain (b, head pair) per CTA at least: with C
+// chains and nc chunks each it takes about max(nc, C nc / SMs) chunk times,
+// while the three-kernel path spreads all C nc chunk-pairs over every SM. So
+// the single pass wins from ~0.6 SM count chains up. Measured on GB300 (graph
+// of back-to-back calls, inputs past L2; single pass against three kernels):
+// 96 chains (B8 L2048 H24, B4 L2048 H48) 80.3 / 80.7 against 83.0 / 84.4 us;
+// 80 chains (B2 L2048 H80, B2 L4096 H80) 79.1 / 150.6 against 73.2 / 131.1 us;
+// 192 chains (B16 L1024 H24) 63.7 against 92.5 us; 320 chains (B8 L2048 H80)
+// 174 against 251 us.
+bool chunked_fused_preferred(const ChunkedArgs &a) {
+    return 5 * a.B * (a.H / kHB) >= 3 * (int64_t)sm_count(152);
+}
 
 cudaError_t launch_chunked_fused(const ChunkedArgs &a, cudaStream_t stream) {
     FusedParams p;
