@@ -2,12 +2,13 @@
 // d_state N = 128, chunks of Q = 128 tokens.
 //
 // The three-step decomposition (chunk state, state passing, chunk scan; see
-// chunked_simt.cu for the algebra) runs as ONE persistent kernel. Its work
-// items are (b, chunk c, pair of heads k = 0, 1 sharing a B/C group); per item:
+// chunked_simt.cu for the algebra) runs as ONE persistent kernel. Its unit of
+// work is (b, chunk c, pair of heads k = 0, 1 sharing a B/C group); per unit:
 //
 //   S      = C B^T                      (M = 128 rows i, N = 128 cols j, K = N)
-//   h_in   = the state entering chunk c, carried in float32 from the item of
-//            chunk c - 1 of the same (b, heads) through global memory (L2);
+//   h_in   = the state entering chunk c: h_next of chunk c - 1 of the same
+//            (b, heads), kept in TMEM, or carried in float32 through global
+//            memory (L2) where the chain passes from one CTA to the next;
 //            h_in(0) = init_state (or 0)
 //   h_next = alpha h_in + B^T (w o x)   (M = n, N = (k, p) of both heads, K = j):
 //            the chunk-state MMA accumulates onto alpha h_in, alpha =
@@ -553,12 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_fused_tc(const __grid_const
         tc::tc_fence_before();
     } else if (warp == kFlagWarp) {
         // ------------------------------------------------------ chain flags
-        // Per work item: wait (acquire, bounded) for the flag of its
-        // predecessor and tell the chain group (mbarrier); then, once every
-        // chain-group thread has stored its part of the item's last state
-        // (the mbarrier orders their stores before this thread), one release
-        // store publishes it. An item whose predecessor was this CTA's own
-        // earlier item finds its flag set by an earlier iteration of this loop.
+        // Per work item: a continuation waits (acquire, bounded) for the flag
+        // of the chunk before it, which the previous CTA's prefix sets, and
+        // tells the chain group (mbarrier); then, once every chain-group thread
+        // has stored its part of the item's last state (the mbarrier orders
+        // their stores before this thread), a prefix publishes it with one
+        // release store.
         if (lane == 0) {
             uint32_t it = 0;
             const int64_t n_flags = Bsz * nhg * nc;
