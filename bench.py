@@ -513,6 +513,9 @@ def run_ours(args):
         compact["mamba1_softplus"] = bench_mamba1_softplus(torch, binding, inputs, dev, hbm_peak, K, W)
     if "backward" in legs:
         compact["backward"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W, bwd_shape(args))
+        if getattr(args, "bwd_shape", None) is None:
+            # and the 2.7B-shaped layer at B4 L2048, where the chunk states and parts cross HBM
+            compact["backward_2p7b"] = bench_backward(torch, binding, inputs, dev, hbm_peak, W, (4, 2048, 80))
 
     clocks = sampler.stop() if sampler else None
     if rank != 0:
