@@ -65,6 +65,21 @@ def test_fused_chains_split_between_ctas(ssd, shape):
     print(f"fused split chains {shape}: y {rel(y, yr):.2e}, final_state {rel(h, hr):.2e} (bound {BF16_REL_MAX})")
 
 
+def test_path_rule_on_this_device(ssd):
+    """bf16, P 64, N 128, chunk 128 without flags: the single pass from 0.6 x
+    the SM count of chains (b, head pair) up, the three-kernel path below;
+    chunk 64 and float32 never take the single pass."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    need = -(-3 * sms // 5)  # chains for the single pass: ceil(0.6 sms)
+    bf16 = torch.bfloat16
+    assert ssd.ssd_scan_path(1, 2048, 2 * need, 64, 128, 1, bf16, 128) == "fused"
+    assert ssd.ssd_scan_path(1, 2048, 2 * (need - 1), 64, 128, 1, bf16, 128) == "staged"
+    assert ssd.ssd_scan_path(8, 2048, 80, 64, 128, 1, bf16, 128) == "fused"     # the 2.7B-shaped B8 layer
+    assert ssd.ssd_scan_path(1, 4096, 24, 64, 128, 1, bf16, 128) == "staged"    # the 130M-shaped layer
+    assert ssd.ssd_scan_path(8, 2048, 80, 64, 128, 1, bf16, 64) == "staged"
+    assert ssd.ssd_scan_path(8, 2048, 80, 64, 128, 1, torch.float32, 128) == "simt"
+
+
 def test_fused_without_D_and_final_state(ssd):
     """D = NULL adds nothing on the diagonal; with final_state = NULL the carry
     lives in the workspace and y is unchanged."""

@@ -481,13 +481,15 @@ def test_backward_tensor_core_shapes(ssd, shape, simt):
     print(f"backward {shape} simt={simt}: " + ", ".join(f"{k} {v:.1e}" for k, v in worst.items()))
 
 
-@pytest.mark.parametrize("shape,optionals", [((1, 2048, 24, 64, 128, 1), False), ((4, 2048, 80, 64, 128, 1), True)])
+@pytest.mark.parametrize("shape,optionals", [((1, 2048, 24, 64, 128, 1), False), ((4, 2048, 80, 64, 128, 1), True),
+                                             ((2, 4096, 48, 64, 128, 8), True)])
 def test_backward_full_size_every_element(ssd, shape, optionals):
     """The sizes the bench times, on the tensor-core path: the 130M-shaped
     layer at L 2048 with the bench's own inputs (no initial state, no final
-    cotangent), and the 2.7B-shaped layer at B4 L2048 with both; every element
-    of every gradient against the float64 oracle within the bf16 bound (the
-    oracle runs on the host's threads: a few seconds)."""
+    cotangent), and the 2.7B-shaped layer at B4 L2048 with both; and eight
+    B/C groups of six heads at B2 L4096; every element of every gradient
+    against the float64 oracle within the bf16 bound (the oracle runs on the
+    host's threads: a few seconds)."""
     Bz, L, H, P, N, G = shape
     if optionals:
         d, dy, dfin = _bwd_case(shape, "bf16", 41)
