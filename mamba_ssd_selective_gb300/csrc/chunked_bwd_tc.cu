@@ -640,14 +640,16 @@ struct PassParams {
 };
 constexpr int kPF = 16;
 
-__global__ void __launch_bounds__(kThreads) bwd_state_passes(const __grid_constant__ PassParams p) {
+constexpr int kPassThreads = 128;  // smaller blocks: the passes' grid fills the GPU in one wave at small sizes
+
+__global__ void __launch_bounds__(kPassThreads) bwd_state_passes(const __grid_constant__ PassParams p) {
     // the gradient kernel (a programmatic dependent of this one) may be
     // scheduled now; it waits for this grid before it reads the states
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const bool adj = blockIdx.z >= p.B;
     const int64_t b = adj ? blockIdx.z - p.B : blockIdx.z;
     const int64_t PN = p.PN, H = p.H, nc = p.nc;
-    const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 4;
+    const int64_t e = ((int64_t)blockIdx.x * kPassThreads + threadIdx.x) * 4;
     const int h = blockIdx.y;
     if (e >= PN) return;
     const float *src0 = adj ? p.dfinal : p.init;
@@ -781,7 +783,8 @@ cudaError_t launch_bwd_states_tc(const BwdArgs &a, cudaStream_t stream) {
     q.H = a.H;
     q.PN = (int64_t)kP * kN;
     q.nc = a.nc;
-    bwd_state_passes<<<dim3((unsigned)(q.PN / 4 / kThreads), (unsigned)a.H, (unsigned)(2 * a.B)), kThreads, 0, stream>>>(q);
+    bwd_state_passes<<<dim3((unsigned)(q.PN / 4 / kPassThreads), (unsigned)a.H, (unsigned)(2 * a.B)), kPassThreads, 0,
+                       stream>>>(q);
     return cudaGetLastError();
 }
 
